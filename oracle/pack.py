@@ -1,0 +1,58 @@
+"""Bit packing of the stored record (oracle side).
+
+[video] (fused-operator remarks): several small codes are packed into one
+32-bit word so that the GPU reads whole words and decodes them in registers.
+The pages fix no bit order.  The reading taken here packs bit-planes:
+
+* index block, w·d/32 words per vector, plane-major: word p·(d/32) + k holds
+  bit p (p = 0 is the least significant bit) of idx[32k + i] at bit i,
+  i = 0..31.
+* sign block, m/32 words per vector: word k holds σ[32k + i] at bit i, with
+  bit value 1 <-> σ = +1.
+
+So every stored word carries 32 consecutive coordinates of one bit-plane.
+Parity: pinned by hand-computed words for fixed patterns and by round trips.
+"""
+
+import numpy as np
+
+_SHIFTS = np.arange(32, dtype=np.uint64)
+
+
+def _bits_to_words(bits: np.ndarray) -> np.ndarray:
+    """bits [..., n] in {0, 1} with n % 32 == 0 -> uint32 words [..., n/32]."""
+    n = bits.shape[-1]
+    if n % 32:
+        raise ValueError("bit count must be a multiple of 32")
+    b = bits.astype(np.uint64).reshape(bits.shape[:-1] + (n // 32, 32))
+    return np.sum(b << _SHIFTS, axis=-1).astype(np.uint32)
+
+
+def _words_to_bits(words: np.ndarray) -> np.ndarray:
+    w = words.astype(np.uint64)[..., None]
+    b = (w >> _SHIFTS) & np.uint64(1)
+    return b.reshape(words.shape[:-1] + (words.shape[-1] * 32,)).astype(np.int64)
+
+
+def pack_indices(idx: np.ndarray, w: int) -> np.ndarray:
+    """idx [N, d] ints in [0, 2^w) -> uint32 [N, w*d/32] (plane-major)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    planes = [_bits_to_words((idx >> p) & 1) for p in range(w)]
+    return np.concatenate(planes, axis=-1)
+
+
+def unpack_indices(words: np.ndarray, w: int, d: int) -> np.ndarray:
+    nw = d // 32
+    idx = np.zeros(words.shape[:-1] + (d,), dtype=np.int64)
+    for p in range(w):
+        idx |= _words_to_bits(words[..., p * nw:(p + 1) * nw]) << p
+    return idx
+
+
+def pack_signs(sgn: np.ndarray) -> np.ndarray:
+    """sgn [N, m] bool (True <-> +1) -> uint32 [N, m/32]."""
+    return _bits_to_words(np.asarray(sgn).astype(np.int64))
+
+
+def unpack_signs(words: np.ndarray) -> np.ndarray:
+    return _words_to_bits(words).astype(bool)

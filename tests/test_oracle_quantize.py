@@ -1,0 +1,176 @@
+"""Pins for the oracle's quantizer, QJL estimator and packing (no GPU)."""
+
+import math
+
+import numpy as np
+import pytest
+from scipy import special
+
+from oracle import codebook, pack, prng, qjl, quantize, rotation
+
+
+def _setup(d, w, m=None, rs=11, qs=22):
+    m = d if m is None else m
+    Pi = rotation.make_rotation(d, rs)
+    S = qjl.make_qjl(m, d, qs)
+    c, b, mse, _ = codebook.lloyd_max(d, w)
+    return Pi, S, c, b, mse
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_bucketize_is_brute_force_nearest_codeword(w):
+    d = 8
+    Pi, S, c, b, _ = _setup(d, w)
+    X = prng.normals(3, 4000 * d).reshape(4000, d)
+    q = quantize.quantize(X, Pi, S, c, b)
+    dist = np.abs(q.u[..., None] - c[None, None, :])
+    nearest = np.argmin(dist, axis=-1)
+    sorted_d = np.sort(dist, axis=-1)
+    clear = (sorted_d[..., 1] - sorted_d[..., 0]) > 1e-12
+    assert clear.mean() > 0.999
+    assert np.array_equal(q.idx[clear], nearest[clear])
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_vectors_on_a_codeword_ray(w):
+    """x = t·Πᵀc[idx]: u = c[idx]/‖c[idx]‖ keeps idx, x̃ = ‖x‖Πᵀc[idx], so
+    ‖r‖ = t·‖c[idx]‖·|1 - ‖c[idx]‖| and r is parallel to x."""
+    d = 32
+    Pi, S, c, b, _ = _setup(d, w)
+    rng = np.random.default_rng(0)
+    idx = rng.integers(0, 1 << w, size=(50, d))
+    cn = np.linalg.norm(c[idx], axis=1)
+    # keep rows where c[idx]/‖c[idx]‖ stays strictly inside every cell
+    lo = np.concatenate([[-np.inf], b])[idx]
+    hi = np.concatenate([b, [np.inf]])[idx]
+    v = c[idx] / cn[:, None]
+    keep = np.all((v > lo + 1e-9) & (v < hi - 1e-9), axis=1)
+    idx, cn = idx[keep], cn[keep]
+    assert len(idx) > 5
+    t = 2.0 ** rng.integers(-3, 4, size=len(idx))
+    X = t[:, None] * (c[idx] @ Pi)
+    q = quantize.quantize(X, Pi, S, c, b)
+    assert np.array_equal(q.idx, idx)
+    assert np.allclose(q.norm, t * cn, rtol=1e-7, atol=0)
+    assert np.allclose(q.rnorm64, t * cn * np.abs(1.0 - cn), rtol=1e-9, atol=1e-14)
+
+
+def test_zero_vector_rule():
+    d, w = 32, 2
+    Pi, S, c, b, _ = _setup(d, w)
+    q = quantize.quantize(np.zeros((1, d)), Pi, S, c, b)
+    # u = 0 lies on the middle boundary 0: #{β < 0} = 1 (tie -> lower cell)
+    assert np.all(q.idx == 1)
+    assert q.norm[0] == 0 and q.rnorm[0] == 0 and q.sgn.all()
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_stage1_distortion_matches_codebook_and_printed_bounds(w):
+    d, N = 128, 20000
+    Pi, S, c, b, mse = _setup(d, w)
+    X = prng.normals(77, N * d).reshape(N, d)
+    X /= np.linalg.norm(X, axis=1, keepdims=True)
+    _, _, _, xt = quantize.stage1(X, Pi, c, b)
+    err = np.sum((X - xt) ** 2, axis=1)
+    se = err.std() / math.sqrt(N)
+    assert abs(err.mean() - d * mse) < 4 * se
+    assert 4.0 ** -w <= err.mean() <= math.sqrt(3) * math.pi / 2 * 4.0 ** -w
+
+
+def test_one_bit_mse_quantizer_shrinks_inner_products_toward_2_over_pi():
+    """E⟨x, x̃⟩ / ‖x‖² = d·c² (exact), which tends to 2/π ≈ 0.637 as d grows."""
+    gaps = []
+    for d in (128, 1024):
+        Pi, S, c, b, _ = _setup(d, 1)
+        N = 4000
+        X = prng.normals(d, N * d).reshape(N, d)
+        X /= np.linalg.norm(X, axis=1, keepdims=True)
+        _, _, _, xt = quantize.stage1(X, Pi, c, b)
+        ratio = np.sum(X * xt, axis=1)
+        exact = d * c[1] ** 2
+        assert abs(ratio.mean() - exact) < 4 * ratio.std() / math.sqrt(N) + 1e-12
+        gaps.append(abs(exact - 2 / math.pi))
+    assert gaps[1] < gaps[0] and gaps[1] < 5e-4
+
+
+def test_qjl_estimator_unbiased_with_closed_form_variance():
+    d = m = 32
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal(d)
+    r = rng.standard_normal(d)
+    est = []
+    for s in range(10000):
+        S = qjl.make_qjl(m, d, 500000 + s)
+        est.append(qjl.estimate(S, q, np.linalg.norm(r), qjl.signs(S, r)))
+    est = np.array(est)
+    truth = q @ r
+    se = est.std() / math.sqrt(len(est))
+    assert abs(est.mean() - truth) < 3 * se
+    var = ((math.pi / 2) * (q @ q) * (r @ r) - truth ** 2) / m
+    assert abs(est.var() / var - 1.0) < 0.05
+
+
+def test_two_stage_score_is_unbiased_over_S():
+    """Stage 1 + QJL on the residual: E_S[⟨q, x̂⟩] = ⟨q, x⟩."""
+    d = m = 32
+    w = 1
+    Pi = rotation.make_rotation(d, 3)
+    c, b, _, _ = codebook.lloyd_max(d, w)
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((1, d))
+    q = rng.standard_normal(d)
+    vals = []
+    for s in range(10000):
+        S = qjl.make_qjl(m, d, 900000 + s)
+        z = quantize.quantize(x, Pi, S, c, b)
+        xh = quantize.reconstruct(z.idx, z.sgn, z.norm, z.rnorm, Pi, S, c)
+        vals.append(float(xh[0] @ q))
+    vals = np.array(vals)
+    # fp32 storage of the norms biases by at most ~1e-7 relative
+    assert abs(vals.mean() - float(x[0] @ q)) < 3 * vals.std() / math.sqrt(len(vals)) + 1e-6
+
+
+def test_reconstruct_inner_product_is_the_estimator():
+    d, w = 64, 2
+    Pi, S, c, b, _ = _setup(d, w)
+    rng = np.random.default_rng(1)
+    X = rng.standard_normal((5, d))
+    qv = rng.standard_normal(d)
+    z = quantize.quantize(X, Pi, S, c, b)
+    xh = quantize.reconstruct(z.idx, z.sgn, z.norm, z.rnorm, Pi, S, c)
+    for i in range(5):
+        mse_part = float(z.norm[i]) * float(c[z.idx[i]] @ (Pi @ qv))
+        sig = np.where(z.sgn[i], 1.0, -1.0)
+        est = mse_part + qjl.estimate(S, qv, float(z.rnorm[i]), sig)
+        assert abs(xh[i] @ qv - est) < 1e-12 * (1 + abs(est))
+
+
+# ---- packing ---------------------------------------------------------------
+
+def test_pack_hand_patterns():
+    d = 64
+    j = np.arange(d)
+    # w = 2, idx = j mod 4: plane 0 = odd j, plane 1 = j mod 4 in {2, 3}
+    words = pack.pack_indices((j % 4)[None, :], 2)[0]
+    assert [int(x) for x in words] == [0xAAAAAAAA, 0xAAAAAAAA, 0xCCCCCCCC, 0xCCCCCCCC]
+    # w = 3, idx = j mod 8
+    words = pack.pack_indices((j % 8)[None, :], 3)[0]
+    assert [int(x) for x in words] == [0xAAAAAAAA] * 2 + [0xCCCCCCCC] * 2 + [0xF0F0F0F0] * 2
+    # all zero / all ones
+    assert not pack.pack_indices(np.zeros((1, d), int), 3).any()
+    assert np.all(pack.pack_indices(np.full((1, d), 7), 3) == 0xFFFFFFFF)
+    # idx = 1 only at coordinate 33 -> plane 0, word 1, bit 1
+    idx = np.zeros((1, d), int)
+    idx[0, 33] = 1
+    assert [int(x) for x in pack.pack_indices(idx, 2)[0]] == [0, 2, 0, 0]
+    # signs: +1 at even j -> 0x55555555
+    assert [int(x) for x in pack.pack_signs((j % 2 == 0)[None, :])[0]] == [0x55555555, 0x55555555]
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_pack_round_trip(w):
+    rng = np.random.default_rng(w)
+    idx = rng.integers(0, 1 << w, size=(7, 96))
+    sg = rng.integers(0, 2, size=(7, 128)).astype(bool)
+    assert np.array_equal(pack.unpack_indices(pack.pack_indices(idx, w), w, 96), idx)
+    assert np.array_equal(pack.unpack_signs(pack.pack_signs(sg)), sg)
