@@ -1,0 +1,361 @@
+#!/usr/bin/env python
+"""Benchmark of the TurboQuant hot path on one B300 (or N replicas).
+
+One step = the whole hot path over one batch: quantize the layer's K and V
+caches (rotation, Lloyd-Max bucketing, QJL signs, packing) and run one GQA
+decode step of attention over the compressed cache (query rotation, scores,
+online softmax, rotated-domain V accumulation, split merge and unrotation).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama8b] [--bits 3]
+    python bench.py --impl reference ...   # the float64 CPU oracle on host cores
+
+Prints one JSON line.  N > 1 runs as torchrun ranks, each an independent
+replica of the workload (weak scaling; the path has no exchange step).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV-tokens/s & % of 8 TB/s HBM roofline; quantize Mvectors/s"
+UNIT = "KV-tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--bits", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def rec_bytes(d, m, w):
+    return (w * d + m) // 8 + 8
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "online_kv_cache_04_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = sources_sha()
+    for line in open(path):
+        v = line.split()
+        if len(v) == 4 and not line.startswith("#") and v[0] == kernel and v[1] == sha and v[3] == workload:
+            return float(v[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            v = [x.strip() for x in line.split(",")]
+            if len(v) < 9:
+                continue
+            try:
+                sm.append(float(v[1]))
+                smax.append(float(v[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, v[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- oracle arm
+
+def oracle_step(wl, w, heads):
+    """The float64 oracle on `heads` kv heads of batch row 0: quantize K, V, then decode."""
+    import numpy as np
+
+    from online_kv_cache_04_b300.workloads import QJL_SEED, ROTATION_SEED, make_kv, make_queries
+    from oracle import codebook, decode, qjl, quantize, rotation
+
+    d = wl.d
+    Pi = rotation.make_rotation(d, ROTATION_SEED)
+    S = qjl.make_qjl(wl.m, d, QJL_SEED)
+    c, b, _, _ = codebook.lloyd_max(d, w)
+    K = make_kv(wl, B=1, which=0)[:, :heads].float().numpy()
+    V = make_kv(wl, B=1, which=1)[:, :heads].float().numpy()
+    G = wl.Hq // wl.Hkv
+    q = make_queries(wl, B=1)[:, :heads * G].float().numpy()
+    T = K.shape[2]
+
+    def run():
+        recs = []
+        for X in (K, V):
+            z = quantize.quantize(X.reshape(-1, d), Pi, S, c, b)
+            recs.append({"idx": z.idx.reshape(1, heads, T, d), "sgn": z.sgn.reshape(1, heads, T, wl.m),
+                         "norm": z.norm.reshape(1, heads, T), "rnorm": z.rnorm.reshape(1, heads, T)})
+        decode.decode_attention(q, recs[0], recs[1], np.array([T]), Pi, S, c)
+
+    return run, T * heads / wl.Hkv  # KV tokens of the full layer that one run stands for
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+
+        blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except Exception:
+        blas = 1
+    return blas, os.cpu_count()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from online_kv_cache_04_b300.workloads import WORKLOADS
+
+    wl = WORKLOADS[args.workload]
+    w = args.bits - 1
+    heads = 2  # bounded sample: 2 of the kv heads, full context
+    run, tokens = oracle_step(wl, w, heads)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = tokens / dt
+    threads, cores = cpu_cores()
+    sample = f"{heads} of {wl.Hkv} kv heads, batch row 0, full context {wl.ctx}, per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, args.bits),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "host_cpus": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl, bits):
+    return {"workload": (f"{wl.name}: B={wl.B}, Hq={wl.Hq}, Hkv={wl.Hkv}, d={wl.d}, m={wl.m}, ctx={wl.ctx}, "
+                         f"b={bits}, K/V {str(wl.dtype).replace('torch.', '')}"),
+            "step": "quantize K and V caches + one GQA decode step over the compressed cache",
+            "l2": "flushed between timed steps (256 MiB write)"}
+
+
+# --------------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    from online_kv_cache_04_b300 import _lib
+    from online_kv_cache_04_b300.workloads import QJL_SEED, ROTATION_SEED, WORKLOADS, make_kv, make_queries
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    wl = WORKLOADS[args.workload]
+    w = args.bits - 1
+    d, m = wl.d, wl.m
+    B, Hq, Hkv, T = wl.B, wl.Hq, wl.Hkv, wl.ctx
+    nvec = B * Hkv * T
+    plan = _lib.Plan(d, m, w, ROTATION_SEED, QJL_SEED)
+    K = make_kv(wl, which=0, device="cuda").reshape(nvec, d)
+    V = make_kv(wl, which=1, device="cuda").reshape(nvec, d)
+    q = make_queries(wl, device="cuda")
+    Kr, Vr = _lib.Records(nvec, d, m, w), _lib.Records(nvec, d, m, w)
+    ws = torch.empty(_lib.tq_decode_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+    ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, Hq, d, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev):
+        ev[0].record(stream)
+        _lib.tq_quantize(plan, K, Kr)
+        ev[1].record(stream)
+        _lib.tq_quantize(plan, V, Vr)
+        ev[2].record(stream)
+        _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws)
+        ev[3].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(max(args.warmup, 3)):
+        step(mk())
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    events = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        ev = mk()
+        step(ev)
+        events.append(ev)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    t_step = sum(e[0].elapsed_time(e[3]) for e in events) / args.steps / 1e3
+    t_quant = sum(e[0].elapsed_time(e[1]) + e[1].elapsed_time(e[2]) for e in events) / (2 * args.steps) / 1e3
+    t_dec = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps / 1e3
+    if world > 1:
+        tt = torch.tensor([t_step], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+
+    # ---- end to end: pinned host inputs in, attention output out, every step
+    Kh = K.cpu().pin_memory()
+    Vh = V.cpu().pin_memory()
+    qh = q.cpu().pin_memory()
+    outh = torch.empty_like(out, device="cpu").pin_memory()
+    Kd, Vd, qd = torch.empty_like(K), torch.empty_like(V), torch.empty_like(q)
+
+    def e2e_step():
+        Kd.copy_(Kh, non_blocking=True)
+        Vd.copy_(Vh, non_blocking=True)
+        qd.copy_(qh, non_blocking=True)
+        _lib.tq_quantize(plan, Kd, Kr)
+        _lib.tq_quantize(plan, Vd, Vr)
+        _lib.tq_decode_attention(plan, qd, Kr, Vr, ctx, T, Hkv, out, ws)
+        outh.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, args.steps // 2)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) / n_e2e / 1e3
+    h2d = (Kh.numel() + Vh.numel()) * Kh.element_size() + qh.numel() * qh.element_size()
+    d2h = outh.numel() * outh.element_size()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    rb = rec_bytes(d, m, w)
+    in_bytes = nvec * d * K.element_size()
+    q_bytes = rb * nvec + in_bytes  # one quantize launch: read x, write records
+    dec_bytes = 2 * nvec * rb + q.numel() * q.element_size() + out.numel() * 4
+    kernels = {
+        "quantize": {"launches_per_step": 2, "ms_per_launch": t_quant * 1e3, "bytes_per_launch": q_bytes,
+                     "gbs": q_bytes / t_quant / 1e9, "mvec_per_s": nvec / t_quant / 1e6},
+        "decode_attention": {"launches_per_step": 3, "ms_per_call": t_dec * 1e3, "bytes_per_call": dec_bytes,
+                             "gbs": dec_bytes / t_dec / 1e9, "kv_tokens_per_s": B * T / t_dec,
+                             "frac_of_8tbs": dec_bytes / t_dec / 1e9 / NOMINAL_HBM_GBS},
+    }
+    dom = "quantize" if 2 * t_quant >= t_dec else "decode_attention"
+    if dom == "quantize":
+        ach, kname, traffic_key = q_bytes / t_quant / 1e9, "quantize", "quantize_simt_kernel"
+    else:
+        ach, kname, traffic_key = dec_bytes / t_dec / 1e9, "decode_attention", "split_kernel"
+    traffic = dram_traffic(traffic_key, wl.name)
+    line = {
+        "metric": METRIC, "value": B * T * world / t_step, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(wl, args.bits),
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
+                     "frac": ach / peak, "peak_kind": peak_kind, "traffic": traffic},
+        "kernels": kernels,
+        "decode_kv_tokens_per_s": B * T / t_dec,
+        "decode_frac_of_8tbs": dec_bytes / t_dec / 1e9 / NOMINAL_HBM_GBS,
+        "quantize_mvec_per_s": nvec / t_quant / 1e6,
+        "e2e": {"value": B * T * world / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        run, tokens = oracle_step(wl, w, 1)
+        run()
+        n, t0 = 0, time.perf_counter()
+        while n < 3 or time.perf_counter() - t0 < 10.0:
+            run()
+            n += 1
+        dt = (time.perf_counter() - t0) / n
+        threads, cores = cpu_cores()
+        line["cpu_baseline"] = {"value": tokens / dt, "unit": UNIT, "cores": threads, "host_cpus": cores,
+                                "kind": "oracle",
+                                "sample": f"1 of {Hkv} kv heads, batch row 0, full context {T}; {n} runs"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

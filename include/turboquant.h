@@ -1,0 +1,195 @@
+/*
+ * libturboquant -- TurboQuant's online KV-vector quantizer and decode
+ * attention over the compressed cache, for NVIDIA B300 (sm_103a).
+ *
+ * Plain C ABI: pointers and sizes only.  Sources of each operation are cited
+ * by page title and section:
+ *   [memory-wall]  "谷歌TurboQuant如何绕过内存墙？重新审视它的技术突破"
+ *                  (youleyou), §2 "TurboQuant到底做了什么？", stage 1 and
+ *                  stage 2.
+ *   [efficiency]   "TurboQuant 与 AI 效率革命：当旧数学遇到新智能"
+ *                  (mini-blog), §三 (JL transform, asymmetric estimator, bit
+ *                  accounting) and §四 (three-step pipeline, H100 timings).
+ *   [video]        "TurboQuant压缩效果" (douyin transcripts): fused operators
+ *                  that read packed 32-bit words and decode in registers.
+ *   [yeyu]         yeyulingfeng article: codebook computed once, no
+ *                  calibration data.
+ *
+ * Conventions shared by every call
+ *   - Ownership: the caller owns every buffer.  The library never allocates
+ *     or frees memory, keeps no global state and may be called concurrently
+ *     on different streams with disjoint outputs.
+ *   - Device calls are asynchronous on the given stream (NULL = legacy
+ *     default stream).  Argument errors are detected on the host and
+ *     returned before anything is launched; a failed launch returns
+ *     TQ_ERR_CUDA.  Device pointers must be 16-byte aligned.
+ *   - Shapes: d (head dim) and m (QJL rows) are multiples of 32 in
+ *     [32, 1024]; w = b - 1 index bits per coordinate, w in {1, 2, 3}
+ *     (b = 2, 3, 4 total bits).
+ *   - Stored record of one vector (SoA, see tq_records): w*d/32 index words
+ *     (bit-planes: word p*(d/32)+k holds bit p of idx[32k+i] at bit i),
+ *     m/32 sign words (bit i of word k = 1 <-> sign(S r)[32k+i] = +1), the
+ *     fp32 norm ||x|| and the fp32 residual norm ||r||.
+ */
+#ifndef TURBOQUANT_H
+#define TURBOQUANT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_ARG = -1,          /* invalid argument (size, pointer, alignment)   */
+  TQ_ERR_UNSUPPORTED = -2,  /* valid but not supported by this build         */
+  TQ_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed          */
+  TQ_ERR_WORKSPACE = -4,    /* workspace smaller than the size query says    */
+  TQ_ERR_NUMERIC = -5       /* setup iteration failed to converge            */
+} tq_status;
+
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
+
+/* Same object as cudaStream_t, without including the CUDA headers. */
+typedef struct CUstream_st* tq_stream;
+
+/* ------------------------------------------------------------------ setup
+ * Host-only, float64, deterministic, not timed.  Run once per shape; the
+ * outputs are reused for any model ([yeyu]: computed once, no calibration).
+ */
+
+/* Random rotation Π, [memory-wall] §2 stage 1 / [efficiency] §四 Step 1.
+ * G = d x d iid N(0,1) from SplitMix64(seed) + Box-Muller, row-major fill;
+ * G = QR (Householder); Π = Q diag(sign diag R) (Haar).  Convention u = Π x.
+ * pi: host, d*d doubles, row-major, written.  Errors: TQ_ERR_ARG if d is not
+ * in [2, 4096] or pi is NULL. */
+tq_status tq_make_rotation(int d, uint64_t seed, double* pi);
+
+/* Lloyd-Max codebook with 2^w levels for the post-rotation coordinate law
+ * f_d(x) ∝ (1-x²)^((d-3)/2) on [-1, 1], [memory-wall] §2 stage 1.
+ * centroids: host, 2^w doubles ascending; bounds: host, 2^w-1 doubles
+ * ascending (midpoints); mse_per_coord: host, 1 double, may be NULL.
+ * Errors: TQ_ERR_ARG (d < 3, w not in [1, 4], NULL outputs),
+ * TQ_ERR_NUMERIC (no convergence). */
+tq_status tq_make_codebook(int d, int w, double* centroids, double* bounds, double* mse_per_coord);
+
+/* QJL matrix, [efficiency] §三 "JL 变换" and §四 Step 3: S = m x d iid
+ * N(0,1) from SplitMix64(seed), row-major.  If pi and s_rot are both
+ * non-NULL, also writes s_rot = S Πᵀ (m x d), so that S r = s_rot (Π r).
+ * S: host m*d doubles, written.  Errors: TQ_ERR_ARG. */
+tq_status tq_make_qjl(int m, int d, uint64_t seed, const double* pi, double* S, double* s_rot);
+
+/* ------------------------------------------------------------------ plan
+ * Device copies of the setup tables, laid out for the kernels.  All
+ * pointers live inside one caller-owned device buffer of tq_plan_bytes().
+ */
+typedef struct tq_plan {
+  int d, m, w;
+  float qjl_alpha;          /* √(π/2)/m                                     */
+  const float* pi;          /* [d][d]  Π, row-major (u = Π x)               */
+  const float* pi_t;        /* [d][d]  Πᵀ                                   */
+  const float* s_rot;       /* [m][d]  S Πᵀ                                 */
+  const float* s_rot_t;     /* [d][m]  (S Πᵀ)ᵀ                               */
+  const float* centroids;   /* [2^w]                                        */
+  const float* bounds;      /* [2^w - 1]                                    */
+  const float* walsh;       /* [2^w] Walsh coefficients of the codebook    */
+  const uint16_t* pi_bf16;  /* [2][d][d] bf16 hi/lo split of Π              */
+  const uint16_t* s_bf16;   /* [2][m][d] bf16 hi/lo split of S Πᵀ           */
+} tq_plan;
+
+/* Device bytes needed by tq_plan_init for (d, m, w); 0 if unsupported. */
+size_t tq_plan_bytes(int d, int m, int w);
+
+/* Fill `plan` and the device buffer `dev` (bytes >= tq_plan_bytes) from the
+ * host float64 tables of tq_make_rotation / tq_make_qjl / tq_make_codebook.
+ * Copies are issued on `stream`; the host tables may be released once the
+ * stream has passed this call.  walsh[mask] holds the coefficients of the
+ * expansion c[idx] = Σ_mask walsh[mask] · Π_{p in mask} (2·bit_p(idx) - 1)
+ * (exact; only odd-size masks are non-zero for a symmetric codebook), which
+ * lets the decode kernels score ±1 bit-planes directly.
+ * Errors: TQ_ERR_ARG (shape, NULL, bytes too small), TQ_ERR_CUDA. */
+tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const double* pi, const double* s_rot,
+                       const double* centroids, const double* bounds, void* dev, size_t bytes,
+                       tq_stream stream);
+
+/* ------------------------------------------------------------------ records
+ * Compressed vectors, structure of arrays in device memory.  Row i of a
+ * cache of `capacity` rows: idx[i*(w*d/32) ...], sgn[i*(m/32) ...],
+ * norm[i], rnorm[i].  KV caches use row (b*Hkv + h)*ctx_stride + t.
+ */
+typedef struct tq_records {
+  uint32_t* idx;
+  uint32_t* sgn;
+  float* norm;
+  float* rnorm;
+  int64_t capacity;
+} tq_records;
+
+/* ------------------------------------------------------------------ quantize
+ * Online quantization of n vectors, [memory-wall] §2 (stages 1 and 2) and
+ * [efficiency] §四 (three-step pipeline): n = ||x||, u = Π x / n,
+ * idx_j = #{k: bounds_k < u_j}, ρ = u - c[idx] (= Π r / n), ||r|| = n ||ρ||,
+ * σ = sign(S r) = sign(s_rot ρ) with sign(0) = +1; packed as described
+ * above.  A zero vector gives u = 0, ||r|| = 0 and all σ = +1.
+ * x: device, n rows of d elements of `dtype`, row stride ld_x elements
+ * (>= d, multiple of 8).  Writes rows [out_offset, out_offset + n) of
+ * `out` (online append into a preallocated cache).  n = 0 is a no-op.
+ * Errors: TQ_ERR_ARG (n < 0, rows beyond capacity, NULL, misaligned),
+ * TQ_ERR_CUDA. */
+tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
+                      const tq_records* out, int64_t out_offset, tq_stream stream);
+
+/* ------------------------------------------------------------------ decode
+ * One decode step of GQA softmax attention over compressed K/V caches.
+ * Per query head g (kv head h = g / (Hq/Hkv)) and token t < ctx_len[b]:
+ *   s_{g,t} = scale * ( ||k_t|| <Π q_g, c[idx_t]>
+ *                       + √(π/2)/m ||r_t|| <S q_g, σ_t> )
+ * ([efficiency] §三 asymmetric estimator on the residual, [memory-wall] §2
+ * stage 2); p = softmax_t(s); the value side is accumulated in the rotated
+ * domain, acc = Σ_t p_t (||v_t|| c[idx_t] + √(π/2)/m ||r_t|| s_rotᵀ σ_t),
+ * and o_g = Πᵀ acc -- a single unrotation, with no dequantized copy
+ * written anywhere ([video]: decode in registers while reading).
+ * q: device [B][Hq][d] of q_dtype.  ctx_len: device int32 [B], each in
+ * [0, ctx_stride] (a row with ctx_len 0 outputs zeros).  scale <= 0 means
+ * 1/√d.  out: device fp32 [B][Hq][d].  workspace: device, at least
+ * tq_decode_workspace_size() bytes for the same (B, Hq, Hkv, ctx_stride).
+ * Errors: TQ_ERR_ARG (Hq % Hkv, sizes, capacity < B*Hkv*ctx_stride, NULL),
+ * TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_decode_workspace_size(const tq_plan* plan, int B, int Hq, int Hkv, int64_t ctx_stride,
+                                   size_t* bytes);
+tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
+                              const tq_records* K, const tq_records* V, const int32_t* ctx_len,
+                              int64_t ctx_stride, float scale, float* out, void* workspace,
+                              size_t ws_bytes, tq_stream stream);
+
+/* Attention logits alone (the quantity the H100 timings of [efficiency] §四
+ * and [memory-wall] §2 measure): scores[b][g][t] = s_{g,t} as above for
+ * t < ctx_len[b]; entries t >= ctx_len[b] are left untouched.
+ * scores: device fp32 [B][Hq][ctx_stride].  workspace as for
+ * tq_decode_attention.  Errors as above. */
+tq_status tq_decode_scores(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
+                           const tq_records* K, const int32_t* ctx_len, int64_t ctx_stride, float scale,
+                           float* scores, void* workspace, size_t ws_bytes, tq_stream stream);
+
+/* ------------------------------------------------------------------ search
+ * Inner-product top-k over n compressed vectors ([video] / [memory-wall]:
+ * vector search engines): score_i = ||x_i|| <Π q, c[idx_i]> + √(π/2)/m
+ * ||r_i|| <S q, σ_i>, k largest in descending order, equal scores -> lower
+ * index.  q: device [nq][d] of q_dtype; idx_out: device int32 [nq][k];
+ * score_out: device fp32 [nq][k]; 1 <= k <= 64.
+ * Errors: TQ_ERR_ARG, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_search_workspace_size(const tq_plan* plan, int nq, int64_t n, int k, size_t* bytes);
+tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype q_dtype, int nq, const tq_records* recs,
+                         int64_t n, int k, int32_t* idx_out, float* score_out, void* workspace,
+                         size_t ws_bytes, tq_stream stream);
+
+/* Human-readable name of a status code (static string). */
+const char* tq_status_str(tq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TURBOQUANT_H */

@@ -1,0 +1,11 @@
+"""TurboQuant online KV-vector quantization and compressed-cache decode attention
+for NVIDIA B300 (sm_103a).
+
+The compute lives in ``libturboquant.so`` (CUDA kernels behind a C ABI,
+declared in ``include/turboquant.h``).  ``_lib`` is a thin ctypes binding with
+the same names; ``workloads`` draws the seeded synthetic inputs.
+"""
+
+from ._lib import (Plan, Records, TQError, load, tq_decode_attention, tq_decode_scores,  # noqa: F401
+                   tq_decode_workspace_size, tq_make_codebook, tq_make_qjl, tq_make_rotation, tq_quantize,
+                   tq_search_topk, tq_search_workspace_size)

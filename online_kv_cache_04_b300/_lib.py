@@ -1,0 +1,232 @@
+"""ctypes binding of libturboquant (argument marshalling only).
+
+Every function here has the name of the C entry point it wraps and does no
+arithmetic of its own: torch tensors supply device memory and streams, and
+every step of the quantizer and the attention runs in the library's CUDA
+kernels.  If the library is missing, ``load()`` raises: there is no fallback.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libturboquant.so")
+
+TQ_OK, TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_WORKSPACE, TQ_ERR_NUMERIC = 0, -1, -2, -3, -4, -5
+TQ_F32, TQ_BF16 = 0, 1
+
+_c_double_p = ctypes.POINTER(ctypes.c_double)
+_vp = ctypes.c_void_p
+
+
+class tq_plan(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("m", ctypes.c_int), ("w", ctypes.c_int), ("qjl_alpha", ctypes.c_float),
+                ("pi", _vp), ("pi_t", _vp), ("s_rot", _vp), ("s_rot_t", _vp), ("centroids", _vp),
+                ("bounds", _vp), ("walsh", _vp), ("pi_bf16", _vp), ("s_bf16", _vp)]
+
+
+class tq_records(ctypes.Structure):
+    _fields_ = [("idx", _vp), ("sgn", _vp), ("norm", _vp), ("rnorm", _vp), ("capacity", ctypes.c_int64)]
+
+
+# name -> (restype, argtypes)
+_SIGNATURES = {
+    "tq_make_rotation": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64, _c_double_p]),
+    "tq_make_codebook": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _c_double_p, _c_double_p, _c_double_p]),
+    "tq_make_qjl": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_uint64, _c_double_p, _c_double_p,
+                                   _c_double_p]),
+    "tq_plan_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "tq_plan_init": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_double_p,
+                                    _c_double_p, _c_double_p, _c_double_p, _vp, ctypes.c_size_t, _vp]),
+    "tq_quantize": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.POINTER(tq_records), ctypes.c_int64, _vp]),
+    "tq_decode_workspace_size": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]),
+    "tq_decode_attention": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), _vp,
+                                           ctypes.c_int64, ctypes.c_float, _vp, _vp, ctypes.c_size_t, _vp]),
+    "tq_decode_scores": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.POINTER(tq_records), _vp, ctypes.c_int64, ctypes.c_float,
+                                        _vp, _vp, ctypes.c_size_t, _vp]),
+    "tq_search_workspace_size": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_size_t)]),
+    "tq_search_topk": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(tq_records), ctypes.c_int64, ctypes.c_int, _vp, _vp, _vp,
+                                      ctypes.c_size_t, _vp]),
+    "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+def load():
+    """Load libturboquant.so (built in-tree); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libturboquant.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+class TQError(RuntimeError):
+    def __init__(self, name, code):
+        msg = load().tq_status_str(code).decode()
+        super().__init__(f"{name} failed: {msg} ({code})")
+        self.code = code
+
+
+def _check(name, code):
+    if code != TQ_OK:
+        raise TQError(name, code)
+
+
+def _dptr(a):
+    return a.ctypes.data_as(_c_double_p) if a is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.float32:
+        return TQ_F32
+    if t.dtype == torch.bfloat16:
+        return TQ_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+# ----------------------------------------------------------------- host setup
+
+def tq_make_rotation(d, seed):
+    pi = np.empty((d, d), dtype=np.float64)
+    _check("tq_make_rotation", load().tq_make_rotation(d, seed, _dptr(pi)))
+    return pi
+
+
+def tq_make_codebook(d, w):
+    c = np.empty(1 << w, dtype=np.float64)
+    b = np.empty((1 << w) - 1, dtype=np.float64)
+    mse = np.empty(1, dtype=np.float64)
+    _check("tq_make_codebook", load().tq_make_codebook(d, w, _dptr(c), _dptr(b), _dptr(mse)))
+    return c, b, float(mse[0])
+
+
+def tq_make_qjl(m, d, seed, pi=None):
+    S = np.empty((m, d), dtype=np.float64)
+    s_rot = np.empty((m, d), dtype=np.float64) if pi is not None else None
+    pi_c = np.ascontiguousarray(pi, dtype=np.float64) if pi is not None else None
+    _check("tq_make_qjl", load().tq_make_qjl(m, d, seed, _dptr(pi_c), _dptr(S), _dptr(s_rot)))
+    return S, s_rot
+
+
+# ----------------------------------------------------------------- device objects
+
+class Plan:
+    """Device tables of one (d, m, w) shape: a tq_plan over a torch buffer."""
+
+    def __init__(self, d, m, w, rotation_seed, qjl_seed, device="cuda", stream=None):
+        import torch
+
+        self.d, self.m, self.w = d, m, w
+        self.pi = tq_make_rotation(d, rotation_seed)
+        self.S, self.s_rot = tq_make_qjl(m, d, qjl_seed, self.pi)
+        self.centroids, self.bounds, self.mse = tq_make_codebook(d, w)
+        nbytes = load().tq_plan_bytes(d, m, w)
+        if nbytes == 0:
+            raise TQError("tq_plan_bytes", TQ_ERR_ARG)
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.c = tq_plan()
+        _check("tq_plan_init", load().tq_plan_init(
+            ctypes.byref(self.c), d, m, w, _dptr(self.pi), _dptr(self.s_rot), _dptr(self.centroids),
+            _dptr(self.bounds), self.buffer.data_ptr(), nbytes, _stream(stream)))
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+class Records:
+    """Compressed vectors (SoA) in torch device tensors."""
+
+    def __init__(self, capacity, d, m, w, device="cuda"):
+        import torch
+
+        self.capacity, self.d, self.m, self.w = capacity, d, m, w
+        self.idx = torch.empty(capacity, w * d // 32, dtype=torch.int32, device=device)
+        self.sgn = torch.empty(capacity, m // 32, dtype=torch.int32, device=device)
+        self.norm = torch.empty(capacity, dtype=torch.float32, device=device)
+        self.rnorm = torch.empty(capacity, dtype=torch.float32, device=device)
+        self.c = tq_records(self.idx.data_ptr(), self.sgn.data_ptr(), self.norm.data_ptr(), self.rnorm.data_ptr(),
+                            capacity)
+
+    @classmethod
+    def wrap(cls, idx, sgn, norm, rnorm, d, m, w):
+        """Records over existing tensors (e.g. the oracle's packed words)."""
+        self = cls.__new__(cls)
+        self.capacity, self.d, self.m, self.w = norm.shape[0], d, m, w
+        self.idx, self.sgn, self.norm, self.rnorm = idx, sgn, norm, rnorm
+        self.c = tq_records(idx.data_ptr(), sgn.data_ptr(), norm.data_ptr(), rnorm.data_ptr(), self.capacity)
+        return self
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+# ----------------------------------------------------------------- device calls
+
+def tq_quantize(plan, x, out, out_offset=0, stream=None):
+    """Quantize the rows of x [n, ld>=d] (fp32 or bf16, device) into out[out_offset:]."""
+    n = x.shape[0]
+    ld = x.stride(0) if x.dim() == 2 and n > 0 else plan.d
+    _check("tq_quantize", load().tq_quantize(plan.ref, x.data_ptr(), _dtype_code(x), n, ld, out.ref, out_offset,
+                                             _stream(stream)))
+
+
+def tq_decode_workspace_size(plan, B, Hq, Hkv, ctx_stride):
+    n = ctypes.c_size_t(0)
+    _check("tq_decode_workspace_size", load().tq_decode_workspace_size(plan.ref, B, Hq, Hkv, ctx_stride,
+                                                                       ctypes.byref(n)))
+    return n.value
+
+
+def tq_decode_attention(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, workspace, scale=0.0, stream=None):
+    B, Hq, _ = q.shape
+    _check("tq_decode_attention", load().tq_decode_attention(
+        plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride,
+        float(scale), out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def tq_decode_scores(plan, q, K, ctx_len, ctx_stride, Hkv, scores, workspace, scale=0.0, stream=None):
+    B, Hq, _ = q.shape
+    _check("tq_decode_scores", load().tq_decode_scores(
+        plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, ctx_len.data_ptr(), ctx_stride, float(scale),
+        scores.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_search_workspace_size(plan, nq, n, k):
+    b = ctypes.c_size_t(0)
+    _check("tq_search_workspace_size", load().tq_search_workspace_size(plan.ref, nq, n, k, ctypes.byref(b)))
+    return b.value
+
+
+def tq_search_topk(plan, q, recs, n, k, idx_out, score_out, workspace, stream=None):
+    _check("tq_search_topk", load().tq_search_topk(
+        plan.ref, q.data_ptr(), _dtype_code(q), q.shape[0], recs.ref, n, k, idx_out.data_ptr(),
+        score_out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)))

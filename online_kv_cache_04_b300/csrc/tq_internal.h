@@ -1,0 +1,42 @@
+// Internal helpers shared by the libturboquant translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/turboquant.h"
+
+namespace tq {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline bool valid_shape(int d, int m, int w) {
+  return d >= 32 && d <= 1024 && d % 32 == 0 && m >= 32 && m <= 1024 && m % 32 == 0 && w >= 1 && w <= 3;
+}
+
+inline bool valid_plan(const tq_plan* p) {
+  return p != nullptr && valid_shape(p->d, p->m, p->w) && p->pi && p->pi_t && p->s_rot && p->s_rot_t &&
+         p->centroids && p->bounds && p->walsh && p->pi_bf16 && p->s_bf16;
+}
+
+inline bool valid_records(const tq_records* r) {
+  return r != nullptr && r->idx && r->sgn && r->norm && r->rnorm && r->capacity >= 0 && aligned16(r->idx) &&
+         aligned16(r->sgn) && aligned16(r->norm) && aligned16(r->rnorm);
+}
+
+// Status of the most recent launch on this thread.
+inline tq_status launch_status() { return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+// q̃ = Π q and s̃ = (S Πᵀ) q̃ for nheads query vectors of length d (tq_decode.cu).
+tq_status launch_query_prep(const tq_plan* plan, const void* q, tq_dtype qd, int nheads, float* qt, float* st,
+                            cudaStream_t stream);
+
+}  // namespace tq

@@ -1,0 +1,118 @@
+// Device plan: fp32 / bf16 copies of the setup tables in one caller-owned
+// buffer.  Host-side conversion, then plain cudaMemcpyAsync uploads.
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "tq_internal.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t pi, pi_t, s_rot, s_rot_t, cent, bnd, walsh, pi_bf, s_bf, total;
+};
+
+Layout layout(int d, int m, int w) {
+  Layout l{};
+  size_t o = 0;
+  const size_t L = size_t(1) << w;
+  l.pi = o;      o += up(sizeof(float) * d * d);
+  l.pi_t = o;    o += up(sizeof(float) * d * d);
+  l.s_rot = o;   o += up(sizeof(float) * size_t(m) * d);
+  l.s_rot_t = o; o += up(sizeof(float) * size_t(m) * d);
+  l.cent = o;    o += up(sizeof(float) * L);
+  l.bnd = o;     o += up(sizeof(float) * L);
+  l.walsh = o;   o += up(sizeof(float) * L);
+  l.pi_bf = o;   o += up(sizeof(uint16_t) * 2 * d * d);
+  l.s_bf = o;    o += up(sizeof(uint16_t) * 2 * size_t(m) * d);
+  l.total = o;
+  return l;
+}
+
+// round-to-nearest-even float -> bf16 bits (inputs are finite)
+uint16_t bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+double bf16_value(uint16_t h) {
+  uint32_t u = uint32_t(h) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+}  // namespace
+
+extern "C" size_t tq_plan_bytes(int d, int m, int w) {
+  if (!tq::valid_shape(d, m, w)) return 0;
+  return layout(d, m, w).total;
+}
+
+extern "C" tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const double* pi, const double* s_rot,
+                                  const double* centroids, const double* bounds, void* dev, size_t bytes,
+                                  tq_stream stream) {
+  if (!plan || !pi || !s_rot || !centroids || !bounds || !dev || !tq::valid_shape(d, m, w)) return TQ_ERR_ARG;
+  const Layout l = layout(d, m, w);
+  if (bytes < l.total || (reinterpret_cast<uintptr_t>(dev) % kAlign) != 0) return TQ_ERR_ARG;
+  const int L = 1 << w;
+  std::vector<unsigned char> host(l.total, 0);
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(host.data() + off); };
+  auto H = [&](size_t off) { return reinterpret_cast<uint16_t*>(host.data() + off); };
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < d; ++j) {
+      double v = pi[size_t(i) * d + j];
+      F(l.pi)[size_t(i) * d + j] = static_cast<float>(v);
+      F(l.pi_t)[size_t(j) * d + i] = static_cast<float>(v);
+      uint16_t hi = bf16_rne(static_cast<float>(v));
+      uint16_t lo = bf16_rne(static_cast<float>(v - bf16_value(hi)));
+      H(l.pi_bf)[size_t(i) * d + j] = hi;
+      H(l.pi_bf)[size_t(d) * d + size_t(i) * d + j] = lo;
+    }
+  for (int i = 0; i < m; ++i)
+    for (int j = 0; j < d; ++j) {
+      double v = s_rot[size_t(i) * d + j];
+      F(l.s_rot)[size_t(i) * d + j] = static_cast<float>(v);
+      F(l.s_rot_t)[size_t(j) * m + i] = static_cast<float>(v);
+      uint16_t hi = bf16_rne(static_cast<float>(v));
+      uint16_t lo = bf16_rne(static_cast<float>(v - bf16_value(hi)));
+      H(l.s_bf)[size_t(i) * d + j] = hi;
+      H(l.s_bf)[size_t(m) * d + size_t(i) * d + j] = lo;
+    }
+  for (int k = 0; k < L; ++k) F(l.cent)[k] = static_cast<float>(centroids[k]);
+  for (int k = 0; k < L - 1; ++k) F(l.bnd)[k] = static_cast<float>(bounds[k]);
+  // Walsh coefficients: walsh[mask] = 2^-w Σ_idx c[idx] Π_{p in mask} (2 bit_p(idx) - 1)
+  for (int mask = 0; mask < L; ++mask) {
+    double s = 0.0;
+    for (int idx = 0; idx < L; ++idx) {
+      double sign = 1.0;
+      for (int p = 0; p < w; ++p)
+        if (mask >> p & 1) sign *= ((idx >> p) & 1) ? 1.0 : -1.0;
+      s += centroids[idx] * sign;
+    }
+    F(l.walsh)[mask] = static_cast<float>(s / L);
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dev, host.data(), l.total, cudaMemcpyHostToDevice, st) != cudaSuccess) return TQ_ERR_CUDA;
+  // pageable source: the copy has been staged when the call returns, so `host` may go
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TQ_ERR_CUDA;
+  unsigned char* base = static_cast<unsigned char*>(dev);
+  plan->d = d;
+  plan->m = m;
+  plan->w = w;
+  plan->qjl_alpha = static_cast<float>(std::sqrt(M_PI / 2.0) / m);
+  plan->pi = reinterpret_cast<const float*>(base + l.pi);
+  plan->pi_t = reinterpret_cast<const float*>(base + l.pi_t);
+  plan->s_rot = reinterpret_cast<const float*>(base + l.s_rot);
+  plan->s_rot_t = reinterpret_cast<const float*>(base + l.s_rot_t);
+  plan->centroids = reinterpret_cast<const float*>(base + l.cent);
+  plan->bounds = reinterpret_cast<const float*>(base + l.bnd);
+  plan->walsh = reinterpret_cast<const float*>(base + l.walsh);
+  plan->pi_bf16 = reinterpret_cast<const uint16_t*>(base + l.pi_bf);
+  plan->s_bf16 = reinterpret_cast<const uint16_t*>(base + l.s_bf);
+  return TQ_OK;
+}

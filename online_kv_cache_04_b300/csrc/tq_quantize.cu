@@ -1,0 +1,178 @@
+// tq_quantize: online two-stage quantization of KV vectors.
+//
+// Steps per vector ("谷歌TurboQuant如何绕过内存墙？" §2, stages 1 and 2;
+// "TurboQuant 与 AI 效率革命" §四, three-step pipeline):
+//   n = ||x||;  u = Π x / n;  idx_j = #{k : β_k < u_j};  ρ = u - c[idx]
+//   (= Π r / n);  ||r|| = n ||ρ||;  σ = sign(S r) = sign(S Πᵀ ρ), sign(0) = +1.
+// Indices are stored as w bit-planes of 32-coordinate words and the signs as
+// m/32 words ("TurboQuant压缩效果": several codes per 32-bit word).
+//
+// This file holds the portable SIMT path (fp32 FMA, any d, m multiple of 32
+// up to 1024).  A tile of TV vectors is staged in shared memory; each thread
+// owns coordinates j ≡ tid (mod 128), so every warp holds 32 consecutive
+// coordinates and one warp ballot forms one packed word.
+#include <cuda_bf16.h>
+
+#include "tq_internal.h"
+
+namespace {
+
+struct QuantArgs {
+  const void* x;
+  int64_t n, ld;
+  int d, m, w;
+  const float* pi_t;     // [d][d]  Πᵀ  (pi_t[i*d + j] = Π[j][i])
+  const float* s_rot_t;  // [d][m]  (S Πᵀ)ᵀ
+  const float* centroids;
+  const float* bounds;
+  uint32_t* idx;         // rows already offset
+  uint32_t* sgn;
+  float* norm;
+  float* rnorm;
+};
+
+template <typename T>
+__device__ __forceinline__ float load_elem(const T* p);
+template <>
+__device__ __forceinline__ float load_elem<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float load_elem<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+constexpr int kThreads = 128;
+
+template <int TV, typename T>
+__global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
+  extern __shared__ float sm[];
+  const int d = a.d, m = a.m, w = a.w, L = 1 << w;
+  float* xs = sm;              // [TV][d] input tile, fp32
+  float* rs = xs + TV * d;     // [TV][d] residual ρ (unit-norm domain)
+  float* nrm = rs + TV * d;    // [TV]
+  float* rsq = nrm + TV;       // [TV]   ||ρ||²
+  float* cent = rsq + TV;      // [L]
+  float* bnd = cent + 8;       // [L-1]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < L) cent[tid] = a.centroids[tid];
+  if (tid < L - 1) bnd[tid] = a.bounds[tid];
+  const int64_t ntiles = (a.n + TV - 1) / TV;
+  const int words_idx = w * d / 32, words_sgn = m / 32;
+  const T* x = static_cast<const T*>(a.x);
+
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t v0 = tile * TV;
+    for (int e = tid; e < TV * d; e += kThreads) {
+      const int v = e / d, i = e - v * d;
+      const int64_t row = v0 + v;
+      xs[e] = row < a.n ? load_elem<T>(x + row * a.ld + i) : 0.0f;
+    }
+    if (tid < TV) rsq[tid] = 0.0f;
+    __syncthreads();
+    for (int v = warp; v < TV; v += kThreads / 32) {
+      float s = 0.0f;
+      for (int i = lane; i < d; i += 32) s = fmaf(xs[v * d + i], xs[v * d + i], s);
+      s = warp_sum(s);
+      if (lane == 0) nrm[v] = sqrtf(s);
+    }
+    __syncthreads();
+
+    // stage 1: u = Π x / n, bucketize, residual, index bit-planes
+    for (int j = tid; j < d; j += kThreads) {
+      float acc[TV];
+#pragma unroll
+      for (int v = 0; v < TV; ++v) acc[v] = 0.0f;
+      for (int i = 0; i < d; ++i) {
+        const float pij = __ldg(a.pi_t + (size_t)i * d + j);
+#pragma unroll
+        for (int v = 0; v < TV; ++v) acc[v] = fmaf(pij, xs[v * d + i], acc[v]);
+      }
+#pragma unroll
+      for (int v = 0; v < TV; ++v) {
+        const float n = nrm[v];
+        const float u = n > 0.0f ? acc[v] / n : 0.0f;
+        int idx = 0;
+        for (int k = 0; k < L - 1; ++k) idx += (bnd[k] < u) ? 1 : 0;
+        const float rho = n > 0.0f ? u - cent[idx] : 0.0f;
+        rs[v * d + j] = rho;
+        const int64_t row = v0 + v;
+        for (int p = 0; p < w; ++p) {
+          const uint32_t word = __ballot_sync(0xffffffffu, (idx >> p) & 1);
+          if (lane == 0 && row < a.n) a.idx[row * words_idx + p * (d / 32) + j / 32] = word;
+        }
+        const float r2 = warp_sum(rho * rho);
+        if (lane == 0) atomicAdd(&rsq[v], r2);
+      }
+    }
+    __syncthreads();
+
+    // stage 2: σ = sign(S Πᵀ ρ)
+    for (int jj = tid; jj < m; jj += kThreads) {
+      float acc[TV];
+#pragma unroll
+      for (int v = 0; v < TV; ++v) acc[v] = 0.0f;
+      for (int i = 0; i < d; ++i) {
+        const float sij = __ldg(a.s_rot_t + (size_t)i * m + jj);
+#pragma unroll
+        for (int v = 0; v < TV; ++v) acc[v] = fmaf(sij, rs[v * d + i], acc[v]);
+      }
+#pragma unroll
+      for (int v = 0; v < TV; ++v) {
+        const uint32_t word = __ballot_sync(0xffffffffu, acc[v] >= 0.0f);
+        const int64_t row = v0 + v;
+        if (lane == 0 && row < a.n) a.sgn[row * words_sgn + jj / 32] = word;
+      }
+    }
+    if (tid < TV && v0 + tid < a.n) {
+      a.norm[v0 + tid] = nrm[tid];
+      a.rnorm[v0 + tid] = nrm[tid] * sqrtf(rsq[tid]);
+    }
+    __syncthreads();
+  }
+}
+
+template <int TV, typename T>
+tq_status launch_simt(const QuantArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(float) * (2 * TV * a.d + 2 * TV + 16);
+  auto kern = quantize_simt_kernel<TV, T>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  const int64_t ntiles = (a.n + TV - 1) / TV;
+  const int64_t grid = std::min<int64_t>(ntiles, int64_t(tq::sm_count()) * 8);
+  kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
+  return tq::launch_status();
+}
+
+}  // namespace
+
+extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
+                                 const tq_records* out, int64_t out_offset, tq_stream stream) {
+  if (!tq::valid_plan(plan) || !tq::valid_records(out) || n < 0 || out_offset < 0) return TQ_ERR_ARG;
+  if (dtype != TQ_F32 && dtype != TQ_BF16) return TQ_ERR_ARG;
+  if (n == 0) return TQ_OK;
+  if (x == nullptr || !tq::aligned16(x) || ld_x < plan->d || ld_x % 8 != 0) return TQ_ERR_ARG;
+  if (out_offset > out->capacity || n > out->capacity - out_offset) return TQ_ERR_ARG;
+  QuantArgs a;
+  a.x = x;
+  a.n = n;
+  a.ld = ld_x;
+  a.d = plan->d;
+  a.m = plan->m;
+  a.w = plan->w;
+  a.pi_t = plan->pi_t;
+  a.s_rot_t = plan->s_rot_t;
+  a.centroids = plan->centroids;
+  a.bounds = plan->bounds;
+  a.idx = out->idx + out_offset * (plan->w * plan->d / 32);
+  a.sgn = out->sgn + out_offset * (plan->m / 32);
+  a.norm = out->norm + out_offset;
+  a.rnorm = out->rnorm + out_offset;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (plan->d <= 256)
+    return dtype == TQ_F32 ? launch_simt<16, float>(a, st) : launch_simt<16, __nv_bfloat16>(a, st);
+  return dtype == TQ_F32 ? launch_simt<8, float>(a, st) : launch_simt<8, __nv_bfloat16>(a, st);
+}

@@ -27,9 +27,23 @@ import numpy as np
 from scipy import special
 
 
+def gamma_half_ratio(d: int) -> float:
+    """Γ(d/2) / Γ((d-1)/2), from Γ(3/2)/Γ(1) = √π/2, Γ(2)/Γ(3/2) = 2/√π and the
+    recurrence ratio(d + 2) = ratio(d) · d / (d - 1) (Γ(x + 1) = x Γ(x)); for
+    d > 4096 the classical expansion Γ(x+½)/Γ(x) = √x (1 - 1/(8x) + 1/(128x²)
+    + 5/(1024x³) - 21/(32768x⁴) + ...) with x = (d-1)/2."""
+    if d > 4096:
+        x = (d - 1) / 2.0
+        return math.sqrt(x) * (1 - 1 / (8 * x) + 1 / (128 * x ** 2) + 5 / (1024 * x ** 3) - 21 / (32768 * x ** 4))
+    r = math.sqrt(math.pi) / 2.0 if d % 2 == 1 else 2.0 / math.sqrt(math.pi)
+    for k in range(3 if d % 2 == 1 else 4, d, 2):
+        r *= k / (k - 1.0)
+    return r
+
+
 def density_const(d: int) -> float:
-    """Normalising constant Γ(d/2) / (√π Γ((d-1)/2)) = 1 / B(1/2, (d-1)/2) of f_d."""
-    return 1.0 / special.beta(0.5, (d - 1) / 2.0)
+    """Normalising constant Γ(d/2) / (√π Γ((d-1)/2)) of f_d."""
+    return gamma_half_ratio(d) / math.sqrt(math.pi)
 
 
 def density(x, d: int):

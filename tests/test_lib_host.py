@@ -1,0 +1,121 @@
+"""libturboquant on the host (no GPU): exports, setup tables vs the oracle, argument checks."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from online_kv_cache_04_b300 import _lib
+from oracle import codebook as ocb
+from oracle import prng as oprng
+from oracle import rotation as orot
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "turboquant.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:tq_status|size_t|const char\*)\s+(tq_\w+)\s*\(", src, re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.load()
+    names = _declared()
+    assert len(names) >= 12
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(_lib._SIGNATURES)
+
+
+@pytest.mark.parametrize("d", [8, 128, 1024])
+def test_rotation_matches_oracle(d):
+    seed = 0x71550001
+    got = _lib.tq_make_rotation(d, seed)
+    want = orot.make_rotation(d, seed)
+    tol = 1e-12 if d <= 128 else 2e-11  # Householder vs LAPACK: rounding grows with d·cond(G)
+    assert np.abs(got - want).max() < tol
+
+
+@pytest.mark.parametrize("d", [8, 32, 128, 1024])
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_codebook_matches_oracle(d, w):
+    c, b, mse = _lib.tq_make_codebook(d, w)
+    oc, ob, omse, _ = ocb.lloyd_max(d, w)
+    # relative to the outermost centroid: the oracle's incomplete-beta masses
+    # carry ~1e-15 noise at d = 1024, which the fixed point amplifies to ~1e-13
+    scale = np.abs(oc).max()
+    assert np.abs(c - oc).max() < 1e-12 * scale
+    assert np.abs(b - ob).max() < 1e-12 * scale
+    assert abs(mse - omse) < 1e-12 / d
+
+
+def test_qjl_matrix_matches_oracle_generator():
+    m, d, seed = 64, 128, 0x71550002
+    pi = orot.make_rotation(d, 0x71550001)
+    S, s_rot = _lib.tq_make_qjl(m, d, seed, pi)
+    So = oprng.gaussian_matrix(seed, m, d)
+    assert np.abs(S - So).max() < 1e-13
+    assert np.abs(s_rot - So @ pi.T).max() < 1e-12
+
+
+def test_status_strings():
+    lib = _lib.load()
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.tq_status_str(code)
+
+
+def _fake_plan(d=128, m=128, w=2):
+    """A plan whose device pointers are never dereferenced: only host checks run."""
+    p = _lib.tq_plan()
+    p.d, p.m, p.w = d, m, w
+    for f in ("pi", "pi_t", "s_rot", "s_rot_t", "centroids", "bounds", "walsh", "pi_bf16", "s_bf16"):
+        setattr(p, f, 4096)
+    return p
+
+
+def _fake_records(cap):
+    return _lib.tq_records(4096, 8192, 12288, 16384, cap)
+
+
+def test_argument_errors_return_codes_without_launching():
+    lib = _lib.load()
+    p = _fake_plan()
+    r = _fake_records(100)
+    ref = ctypes.byref
+    # n < 0, beyond capacity, misaligned input, bad ld, bad dtype
+    assert lib.tq_quantize(ref(p), 4096, 1, -1, 128, ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize(ref(p), 4096, 1, 90, 128, ref(r), 20, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize(ref(p), 4100, 1, 10, 128, ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize(ref(p), 4096, 1, 10, 100, ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize(ref(p), 4096, 7, 10, 128, ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize(ref(p), 4096, 1, 0, 128, ref(r), 0, None) == _lib.TQ_OK  # n = 0: no-op
+    # invalid plan shapes
+    for d, m, w in ((100, 128, 2), (128, 128, 4), (2048, 128, 2), (128, 16, 2)):
+        bad = _fake_plan(d, m, w)
+        assert lib.tq_quantize(ref(bad), 4096, 1, 1, 128, ref(r), 0, None) == _lib.TQ_ERR_ARG
+        assert lib.tq_plan_bytes(d, m, w) == 0
+    # decode: Hq % Hkv, capacity, workspace
+    n = ctypes.c_size_t(0)
+    assert lib.tq_decode_workspace_size(ref(p), 1, 6, 4, 64, ref(n)) == _lib.TQ_ERR_ARG
+    assert lib.tq_decode_workspace_size(ref(p), 1, 8, 2, 64, ref(n)) == _lib.TQ_OK and n.value > 0
+    kv = _fake_records(2 * 64)
+    args = (ref(p), 4096, 1, 1, 8, 2, ref(kv), ref(kv), 4096, 64, 0.0, 4096, 4096)
+    assert lib.tq_decode_attention(*args, n.value - 4, None) == _lib.TQ_ERR_WORKSPACE
+    small = _fake_records(2 * 64 - 1)
+    assert lib.tq_decode_attention(ref(p), 4096, 1, 1, 8, 2, ref(small), ref(kv), 4096, 64, 0.0, 4096, 4096,
+                                   n.value, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_decode_attention(ref(p), 4096, 1, 1, 6, 4, ref(kv), ref(kv), 4096, 64, 0.0, 4096, 4096,
+                                   n.value, None) == _lib.TQ_ERR_ARG
+    # decode limits: more than 8 query heads per kv head is unsupported
+    big = _fake_records(64)
+    assert lib.tq_decode_workspace_size(ref(p), 1, 16, 1, 64, ref(n)) == _lib.TQ_OK
+    assert lib.tq_decode_attention(ref(p), 4096, 1, 1, 16, 1, ref(big), ref(big), 4096, 64, 0.0, 4096, 4096,
+                                   n.value, None) == _lib.TQ_ERR_UNSUPPORTED
+    # search: k range
+    assert lib.tq_search_workspace_size(ref(p), 4, 100, 0, ref(n)) == _lib.TQ_ERR_ARG
+    assert lib.tq_search_workspace_size(ref(p), 4, 100, 65, ref(n)) == _lib.TQ_ERR_ARG
+    # setup
+    assert lib.tq_make_rotation(1, 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_make_codebook(2, 1, None, None, None) == _lib.TQ_ERR_ARG

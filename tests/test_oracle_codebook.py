@@ -26,9 +26,12 @@ def _max_table():
 @pytest.mark.parametrize("d", [8, 128, 1024])
 def test_one_bit_closed_form(d):
     c, b, mse, _ = codebook.lloyd_max(d, 1)
-    # E|X| = Γ(d/2) / (√π Γ((d+1)/2)) = B(d/2, 1/2) / π
-    want = special.beta(d / 2.0, 0.5) / math.pi
-    assert np.allclose(c, [-want, want], rtol=1e-13, atol=0)
+    # E|X| = Γ(d/2) / (√π Γ((d+1)/2)), evaluated in 30-digit arithmetic
+    import mpmath as mp
+
+    mp.mp.dps = 30
+    want = float(mp.gamma(mp.mpf(d) / 2) / (mp.sqrt(mp.pi) * mp.gamma(mp.mpf(d + 1) / 2)))
+    assert np.allclose(c, [-want, want], rtol=2e-15, atol=0)
     assert b.tolist() == [0.0]
     assert abs(mse - (1.0 / d - want * want)) < 1e-15
 
@@ -103,3 +106,21 @@ def test_lloyd_max_is_a_local_minimum():
             cc.sort()
             bb = 0.5 * (cc[:-1] + cc[1:])
             assert codebook.codebook_mse_numeric(cc, bb, d) > base
+
+
+@pytest.mark.parametrize("d,w", [(128, 2), (128, 3), (1024, 3)])
+def test_lloyd_conditions_hold_in_30_digit_arithmetic(d, w):
+    """Centroid = conditional mean of its midpoint cell, checked by mpmath quadrature."""
+    import mpmath as mp
+
+    mp.mp.dps = 30
+    c, _, _, _ = codebook.lloyd_max(d, w)
+    half = len(c) // 2
+    pos = [mp.mpf(float(v)) for v in c[half:]]
+    edges = [mp.mpf(0)] + [(pos[k] + pos[k + 1]) / 2 for k in range(half - 1)] + [mp.mpf(1)]
+    a = mp.mpf(d - 3) / 2
+    for k in range(half):
+        lo, hi = edges[k], edges[k + 1]
+        m0 = mp.quad(lambda x: (1 - x * x) ** a, [lo, hi])
+        m1 = mp.quad(lambda x: x * (1 - x * x) ** a, [lo, hi])
+        assert abs(float(m1 / m0 - pos[k])) < 1e-12 * float(pos[-1])
