@@ -17,8 +17,9 @@
  *
  * Conventions shared by every call
  *   - Ownership: the caller owns every buffer.  The library never allocates
- *     or frees memory, keeps no global state and may be called concurrently
- *     on different streams with disjoint outputs.
+ *     or frees memory and may be called concurrently on different streams
+ *     with disjoint outputs.  Its only state is one device word of fault
+ *     bits (see tq_fault_flags).
  *   - Device calls are asynchronous on the given stream (NULL = legacy
  *     default stream).  Argument errors are detected on the host and
  *     returned before anything is launched; a failed launch returns
@@ -184,6 +185,13 @@ tq_status tq_search_workspace_size(const tq_plan* plan, int nq, int64_t n, int k
 tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype q_dtype, int nq, const tq_records* recs,
                          int64_t n, int k, int32_t* idx_out, float* score_out, void* workspace,
                          size_t ws_bytes, tq_stream stream);
+
+/* Fault bits set on the device by kernels whose pipeline waits are bounded
+ * (bit 0: a tensor-core quantize wait ran out of its bound, a few seconds;
+ * rows of that launch are undefined).  Kernels never spin forever: they set
+ * the bit and finish.  Copies the word to *flags (synchronous) and clears it
+ * when reset != 0.  Errors: TQ_ERR_ARG (NULL), TQ_ERR_CUDA. */
+tq_status tq_fault_flags(uint32_t* flags, int reset);
 
 /* Human-readable name of a status code (static string). */
 const char* tq_status_str(tq_status s);

@@ -55,6 +55,7 @@ _SIGNATURES = {
     "tq_search_topk": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int,
                                       ctypes.POINTER(tq_records), ctypes.c_int64, ctypes.c_int, _vp, _vp, _vp,
                                       ctypes.c_size_t, _vp]),
+    "tq_fault_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -230,3 +231,10 @@ def tq_search_topk(plan, q, recs, n, k, idx_out, score_out, workspace, stream=No
     _check("tq_search_topk", load().tq_search_topk(
         plan.ref, q.data_ptr(), _dtype_code(q), q.shape[0], recs.ref, n, k, idx_out.data_ptr(),
         score_out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_fault_flags(reset=True):
+    """Device fault bits of the bounded-wait kernels (0 = none)."""
+    v = ctypes.c_uint32(0)
+    _check("tq_fault_flags", load().tq_fault_flags(ctypes.byref(v), 1 if reset else 0))
+    return v.value

@@ -39,4 +39,12 @@ inline int sm_count() {
 tq_status launch_query_prep(const tq_plan* plan, const void* q, tq_dtype qd, int nheads, float* qt, float* st,
                             cudaStream_t stream);
 
+// Device word of fault bits set by bounded waits (tq_quantize_tc.cu).
+unsigned* fault_word();
+
+// tcgen05 quantizer (bf16 input, d = m = 128); rows already offset.
+bool quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n);
+tq_status quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, uint32_t* idx, uint32_t* sgn,
+                      float* norm, float* rnorm, cudaStream_t st);
+
 }  // namespace tq

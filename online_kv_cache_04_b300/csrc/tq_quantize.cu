@@ -172,6 +172,8 @@ extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dt
   a.norm = out->norm + out_offset;
   a.rnorm = out->rnorm + out_offset;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (tq::quantize_tc_supported(plan, dtype, n))
+    return tq::quantize_tc(plan, x, n, ld_x, a.idx, a.sgn, a.norm, a.rnorm, st);
   if (plan->d <= 256)
     return dtype == TQ_F32 ? launch_simt<16, float>(a, st) : launch_simt<16, __nv_bfloat16>(a, st);
   return dtype == TQ_F32 ? launch_simt<8, float>(a, st) : launch_simt<8, __nv_bfloat16>(a, st);

@@ -1,0 +1,389 @@
+// tq_quantize on the 5th-generation tensor cores (tcgen05), for bf16 input
+// with d = m = 128: the head-dim-128 KV-cache case.
+//
+// Per tile of 128 vectors (one CTA per SM, persistent over tiles):
+//   TMA        x tile (bf16, 128-byte swizzle) -> shared memory, 2 stages
+//   GEMM1      U = x Πᵀ as x·Π_hiᵀ + x·Π_loᵀ (Π split into two bf16 terms;
+//              bf16 x is exact), fp32 accumulator in TMEM
+//   epilogue 1 n = ||x|| from the staged tile, u = U / n, bucketize against
+//              the Lloyd-Max bounds -> index bit-planes, ρ = u - c[idx],
+//              ||ρ||², ρ split into bf16 hi + lo written back to TMEM
+//   GEMM2      P = ρ (S Πᵀ)ᵀ as ρ_hi·S_hi + ρ_hi·S_lo + ρ_lo·S_hi, with ρ
+//              read from TMEM as the A operand
+//   epilogue 2 σ = [P >= 0] packed into words, ||r|| = n ||ρ||, stores
+// ("谷歌TurboQuant如何绕过内存墙？" §2 stages 1 and 2; "TurboQuant 与 AI 效率革命"
+// §四 three-step pipeline; "TurboQuant压缩效果": codes packed into 32-bit words.)
+//
+// Two TMEM slots and two epilogue warpgroups let the tensor core work on one
+// tile while the epilogue of the other runs.  Warp roles (320 threads):
+// warps 0-3 epilogue of even tiles, 4-7 of odd tiles (warp % 4 = TMEM lane
+// quadrant), warp 8 issues MMAs and owns TMEM, warp 9 issues TMA loads.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "tq_internal.h"
+#include "tq_sm100.cuh"
+
+namespace {
+
+using namespace tq::sm100;
+
+constexpr int kTile = 128;                       // vectors per tile (MMA M)
+constexpr int kBoxBytes = 64 * 128 * 2;          // TMA box: 64 bf16 columns x 128 rows
+constexpr int kMatBytes = 2 * kBoxBytes;         // one 128 x 128 bf16 operand
+constexpr int kOffPiHi = 0, kOffPiLo = kMatBytes, kOffSHi = 2 * kMatBytes, kOffSLo = 3 * kMatBytes;
+constexpr int kOffX = 4 * kMatBytes;             // two x stages
+constexpr int kOffBar = kOffX + 2 * kMatBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024; // barriers + alignment slack
+constexpr int kThreads = 320, kMmaWarp = 8, kTmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;              // slot s: acc [256s, +128), rho_hi [+128, +64), rho_lo [+192, +64)
+
+constexpr unsigned kFaultWait = 1u;              // fault bit: a pipeline wait ran out of its bound
+
+struct Bars {
+  uint64_t b_full;
+  uint64_t x_full[2], x_empty[2], u_full[2], rho_full[2], p_full[2], acc_empty[2];
+  uint32_t tmem_base;
+};
+
+struct TcArgs {
+  int64_t n;
+  uint32_t* idx;
+  uint32_t* sgn;
+  float* norm;
+  float* rnorm;
+  const float* centroids;  // device [2^w]
+  const float* bounds;     // device [2^w - 1]
+  unsigned* fault;
+};
+
+__device__ unsigned g_fault_word;
+
+template <int W>
+__device__ __forceinline__ int bucket(float u, const float (&bnd)[8]) {
+  int idx = 0;
+#pragma unroll
+  for (int k = 0; k < (1 << W) - 1; ++k) idx += (bnd[k] < u) ? 1 : 0;
+  return idx;
+}
+
+template <int W>
+__device__ __forceinline__ float centroid(int idx, const float (&cent)[8]) {
+  float c = cent[0];
+#pragma unroll
+  for (int k = 1; k < (1 << W); ++k) c = (idx == k) ? cent[k] : c;
+  return c;
+}
+
+template <int W>
+__global__ void __launch_bounds__(kThreads, 1)
+    quantize_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi,
+                       const __grid_constant__ CUtensorMap tm_s, const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t base = smem_u32(smem);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t ntiles = (a.n + kTile - 1) / kTile;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->b_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->x_full[s]), 1);
+      mbar_init(smem_u32(&bars->x_empty[s]), 1 + 4);
+      mbar_init(smem_u32(&bars->u_full[s]), 1);
+      mbar_init(smem_u32(&bars->rho_full[s]), 4);
+      mbar_init(smem_u32(&bars->p_full[s]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[s]), 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_pi);
+    tma_prefetch_desc(&tm_s);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      const uint32_t bfull = smem_u32(&bars->b_full);
+      mbar_arrive_expect_tx(bfull, 4 * kMatBytes);
+      for (int mat = 0; mat < 2; ++mat)
+        for (int h = 0; h < 2; ++h) {
+          tma_load_2d(base + kOffPiHi + mat * kMatBytes + h * kBoxBytes, &tm_pi, h * 64, mat * 128, bfull);
+          tma_load_2d(base + kOffSHi + mat * kMatBytes + h * kBoxBytes, &tm_s, h * 64, mat * 128, bfull);
+        }
+      int it = 0, last_k[2] = {-1, -1};
+      for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        const int s = it & 1, k = it >> 1;
+        if (!mbar_wait(smem_u32(&bars->x_empty[s]), (k & 1) ^ 1, a.fault, kFaultWait)) break;
+        const uint32_t xf = smem_u32(&bars->x_full[s]);
+        mbar_arrive_expect_tx(xf, kMatBytes);
+        const uint32_t dst = base + kOffX + s * kMatBytes;
+        tma_load_2d(dst, &tm_x, 0, (int32_t)(tile * kTile), xf);
+        tma_load_2d(dst + kBoxBytes, &tm_x, 64, (int32_t)(tile * kTile), xf);
+        last_k[s] = k;
+      }
+      // no copy of this CTA may still be in flight when it exits
+      mbar_wait(bfull, 0, a.fault, kFaultWait);
+      for (int s = 0; s < 2; ++s)
+        if (last_k[s] >= 0) mbar_wait(smem_u32(&bars->x_full[s]), last_k[s] & 1, a.fault, kFaultWait);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      bool ok = mbar_wait(smem_u32(&bars->b_full), 0, a.fault, kFaultWait);
+      tc_fence_after();
+      auto gemm2 = [&](int j) {
+        const int s = j & 1, k = j >> 1;
+        if (!mbar_wait(smem_u32(&bars->rho_full[s]), k & 1, a.fault, kFaultWait)) return false;
+        tc_fence_after();
+        const uint32_t acc = tmem + 256 * s;
+        // terms (ρ_hi, S_hi), (ρ_hi, S_lo), (ρ_lo, S_hi)
+#pragma unroll 1
+        for (int t = 0; t < 3; ++t) {
+          const uint32_t rho = acc + (t == 2 ? 192 : 128);
+          const uint64_t sd = desc_sw128(base + (t == 1 ? kOffSLo : kOffSHi));
+#pragma unroll 1
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t boff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;  // start address advances in 16 B units
+            mma_ts(acc, rho + kk * 8, sd + (boff >> 4), idesc, (t | kk) != 0);
+          }
+        }
+        mma_commit(smem_u32(&bars->p_full[s]));
+        return true;
+      };
+      int it = 0;
+      for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+        const int s = it & 1, k = it >> 1;
+        if (!mbar_wait(smem_u32(&bars->x_full[s]), k & 1, a.fault, kFaultWait)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars->acc_empty[s]), (k & 1) ^ 1, a.fault, kFaultWait)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t acc = tmem + 256 * s;
+        const uint32_t xa = base + kOffX + s * kMatBytes;
+        const uint64_t xd = desc_sw128(xa);
+#pragma unroll 1
+        for (int term = 0; term < 2; ++term) {
+          const uint64_t pd = desc_sw128(base + (term ? kOffPiLo : kOffPiHi));
+#pragma unroll 1
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss(acc, xd + off, pd + off, idesc, (term | kk) != 0);
+          }
+        }
+        mma_commit(smem_u32(&bars->u_full[s]));
+        mma_commit(smem_u32(&bars->x_empty[s]));
+        if (it >= 1 && !gemm2(it - 1)) { ok = false; break; }
+      }
+      if (ok && it >= 1) gemm2(it - 1);
+    }
+  } else {
+    // epilogue: warpgroup g = warp / 4 handles tiles it ≡ g (mod 2); thread = one vector (TMEM lane)
+    float cent[8], bnd[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      cent[k] = k < (1 << W) ? __ldg(a.centroids + k) : 0.f;
+      bnd[k] = k < (1 << W) - 1 ? __ldg(a.bounds + k) : 0.f;
+    }
+    const int g = warp >> 2, q = warp & 3, r = q * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int s = g;
+    const uint32_t acc = tmem + lane_base + 256 * s;
+    int it = g;
+    for (int64_t tile = blockIdx.x + (int64_t)g * gridDim.x; tile < ntiles; tile += 2 * (int64_t)gridDim.x, it += 2) {
+      const int ph = (it >> 1) & 1;
+      if (!mbar_wait(smem_u32(&bars->x_full[s]), ph, a.fault, kFaultWait)) break;
+      // ||x|| from the staged tile (row r, both 64-column boxes, 128-byte swizzle)
+      float ss[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint8_t* xt = smem + kOffX + s * kMatBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint8_t* row = xt + h * kBoxBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xFFFF0000u);
+            ss[e] = fmaf(lo, lo, ss[e]);
+            ss[e] = fmaf(hi, hi, ss[e]);
+          }
+        }
+      }
+      const float n = sqrtf((ss[0] + ss[1]) + (ss[2] + ss[3]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->x_empty[s]));
+      if (!mbar_wait(smem_u32(&bars->u_full[s]), ph, a.fault, kFaultWait)) break;
+      tc_fence_after();
+      const float inv = n > 0.f ? 1.0f / n : 0.f;
+      uint32_t planes[W][4];
+      float rsq = 0.f;
+#pragma unroll
+      for (int p = 0; p < W; ++p)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) planes[p][c] = 0u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {  // 16 coordinates per step
+        uint32_t v[16];
+        tmem_ld16(acc + 16 * c, v);
+        tmem_ld_wait();
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float rho2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float u = __uint_as_float(v[2 * j + e]) * inv;
+            const int idx = bucket<W>(u, bnd);
+            const float rho = n > 0.f ? u - centroid<W>(idx, cent) : 0.f;
+            rsq = fmaf(rho, rho, rsq);
+            rho2[e] = rho;
+            const int bit = 16 * (c & 1) + 2 * j + e;
+#pragma unroll
+            for (int p = 0; p < W; ++p) planes[p][c >> 1] |= static_cast<uint32_t>((idx >> p) & 1) << bit;
+          }
+          const __nv_bfloat162 h = __floats2bfloat162_rn(rho2[0], rho2[1]);
+          const float2 hf = __bfloat1622float2(h);
+          const __nv_bfloat162 l = __floats2bfloat162_rn(rho2[0] - hf.x, rho2[1] - hf.y);
+          hi[j] = *reinterpret_cast<const uint32_t*>(&h);
+          lo[j] = *reinterpret_cast<const uint32_t*>(&l);
+        }
+        tmem_st8(acc + 128 + 8 * c, hi);
+        tmem_st8(acc + 192 + 8 * c, lo);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->rho_full[s]));
+      const int64_t row = tile * kTile + r;
+      if (row < a.n) {
+        uint4* ip = reinterpret_cast<uint4*>(a.idx + row * (4 * W));
+#pragma unroll
+        for (int p = 0; p < W; ++p) ip[p] = make_uint4(planes[p][0], planes[p][1], planes[p][2], planes[p][3]);
+      }
+      if (!mbar_wait(smem_u32(&bars->p_full[s]), ph, a.fault, kFaultWait)) break;
+      tc_fence_after();
+      uint32_t sg[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[16];
+        tmem_ld16(acc + 16 * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          sg[c >> 1] |= static_cast<uint32_t>(__uint_as_float(v[j]) >= 0.f) << (16 * (c & 1) + j);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[s]));
+      if (row < a.n) {
+        *reinterpret_cast<uint4*>(a.sgn + row * 4) = make_uint4(sg[0], sg[1], sg[2], sg[3]);
+        a.norm[row] = n;
+        a.rnorm[row] = n * sqrtf(rsq);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// rows x cols bf16 matrix with row stride ld elements; 64 x 128 boxes, 128-byte swizzle
+bool map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int W>
+tq_status launch_w(const CUtensorMap& mx, const CUtensorMap& mp, const CUtensorMap& ms, const TcArgs& a,
+                   cudaStream_t st) {
+  auto kern = quantize_tc_kernel<W>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  const int64_t ntiles = (a.n + kTile - 1) / kTile;
+  const int grid = (int)std::min<int64_t>(ntiles, tq::sm_count());
+  kern<<<grid, kThreads, kSmemBytes, st>>>(mx, mp, ms, a);
+  return tq::launch_status();
+}
+
+}  // namespace
+
+unsigned* tq::fault_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
+  return static_cast<unsigned*>(p);
+}
+
+bool tq::quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n) {
+  return plan->d == 128 && plan->m == 128 && dtype == TQ_BF16 && n < (int64_t(1) << 31) && encode_fn() != nullptr;
+}
+
+tq_status tq::quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, uint32_t* idx, uint32_t* sgn,
+                          float* norm, float* rnorm, cudaStream_t st) {
+  CUtensorMap mx, mp, ms;
+  if (!map_bf16(&mx, x, (uint64_t)n, 128, (uint64_t)ld_x) || !map_bf16(&mp, plan->pi_bf16, 256, 128, 128) ||
+      !map_bf16(&ms, plan->s_bf16, 256, 128, 128))
+    return TQ_ERR_CUDA;
+  TcArgs a{};
+  a.n = n;
+  a.idx = idx;
+  a.sgn = sgn;
+  a.norm = norm;
+  a.rnorm = rnorm;
+  a.centroids = plan->centroids;
+  a.bounds = plan->bounds;
+  a.fault = tq::fault_word();
+  if (!a.fault) return TQ_ERR_CUDA;
+  switch (plan->w) {
+    case 1: return launch_w<1>(mx, mp, ms, a, st);
+    case 2: return launch_w<2>(mx, mp, ms, a, st);
+    default: return launch_w<3>(mx, mp, ms, a, st);
+  }
+}
+
+extern "C" tq_status tq_fault_flags(uint32_t* flags, int reset) {
+  if (flags == nullptr) return TQ_ERR_ARG;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fault_word, sizeof(v)) != cudaSuccess) return TQ_ERR_CUDA;
+  *flags = v;
+  if (reset) {
+    const unsigned z = 0;
+    if (cudaMemcpyToSymbol(g_fault_word, &z, sizeof(z)) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  return TQ_OK;
+}

@@ -60,6 +60,20 @@ def test_ragged_counts_and_append_offset(gpu_lib, n):
     assert torch.all(rec.idx[:off] == -1) and torch.all(rec.idx[off + n:] == -1)
 
 
+@pytest.mark.parametrize("w", [1, 2, 3])
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 300, 2000])
+def test_bf16_tensor_core_path_ragged_and_offset(gpu_lib, n, w):
+    """bf16, d = m = 128 runs on the tcgen05 kernel: tails of every tile size, append offset."""
+    wl = WORKLOADS["llama8b"]
+    X = make_kv(wl, B=1, T=n, which=0)[0, n % 8]  # bf16 [n, 128]
+    off = 5
+    rec = _run(X.cuda(), 128, 128, w, offset=off, capacity=n + off + 3)
+    _compare(X.float().numpy(), rec, slice(off, off + n), 128, 128, w)
+    assert torch.all(rec.idx[:off] == -1) and torch.all(rec.idx[off + n:] == -1)
+    assert torch.all(rec.sgn[:off] == -1) and torch.all(rec.sgn[off + n:] == -1)
+    assert _lib.tq_fault_flags() == 0
+
+
 def test_zero_vector_and_bf16_input(gpu_lib):
     wl = WORKLOADS["llama8b"]
     X = make_kv(wl, B=1, T=64, which=1)[0, 3]  # bf16 [64, 128]
