@@ -34,7 +34,7 @@ NOMINAL_HBM_GBS = 8000.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b")
@@ -94,6 +94,15 @@ class ClockSampler:
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def wait_first(self, timeout=5.0):
+        """Block until nvidia-smi has written its first sample (it starts slowly)."""
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < timeout:
+            self.file.flush()
+            if os.path.getsize(self.file.name) > 0:
+                return
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -253,6 +262,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
+    sampler.wait_first()
     events = []
     for _ in range(args.steps):
         flush.fill_(1)
