@@ -165,6 +165,25 @@ tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_dtype q_dty
                               int64_t ctx_stride, float scale, float* out, void* workspace,
                               size_t ws_bytes, tq_stream stream);
 
+/* Decode attention without a caller workspace, for callers that cannot
+ * allocate device memory (graph captures that forbid allocation, embedded
+ * runtimes with memory fixed at start-up, plugins whose host owns the
+ * allocator).  The paper has no counterpart: this is a deployment variant of
+ * tq_decode_attention, with the same arguments minus the workspace and the
+ * same results.
+ * Scratch: one array of TQ_NOALLOC_SCRATCH_BYTES (8 MiB) compiled into the
+ * library, resident on every GPU that loads it until the process exits.  The
+ * first call on a device looks up the array's device address (make that first
+ * call before any stream capture); no call allocates or frees memory.  All
+ * calls share the array: calls whose GPU work overlaps race on it, so order
+ * them on one stream.  Nothing in the array needs clearing between calls.
+ * Errors: as tq_decode_attention; TQ_ERR_WORKSPACE when the shape needs more
+ * scratch than TQ_NOALLOC_SCRATCH_BYTES (tq_decode_workspace_size tells). */
+#define TQ_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+tq_status tq_decode_attention_noalloc(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
+                                      const tq_records* K, const tq_records* V, const int32_t* ctx_len,
+                                      int64_t ctx_stride, float scale, float* out, tq_stream stream);
+
 /* Attention logits alone (the quantity the H100 timings of [efficiency] §四
  * and [memory-wall] §2 measure): scores[b][g][t] = s_{g,t} as above for
  * t < ctx_len[b]; entries t >= ctx_len[b] are left untouched.

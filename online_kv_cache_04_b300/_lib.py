@@ -47,6 +47,10 @@ _SIGNATURES = {
     "tq_decode_attention": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), _vp,
                                            ctypes.c_int64, ctypes.c_float, _vp, _vp, ctypes.c_size_t, _vp]),
+    "tq_decode_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.POINTER(tq_records),
+                                                   ctypes.POINTER(tq_records), _vp, ctypes.c_int64, ctypes.c_float,
+                                                   _vp, _vp]),
     "tq_decode_scores": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.POINTER(tq_records), _vp, ctypes.c_int64, ctypes.c_float,
                                         _vp, _vp, ctypes.c_size_t, _vp]),
@@ -212,6 +216,14 @@ def tq_decode_attention(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, workspace,
         plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride,
         float(scale), out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def tq_decode_attention_noalloc(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, scale=0.0, stream=None):
+    """tq_decode_attention with the library's built-in scratch array (no workspace argument)."""
+    B, Hq, _ = q.shape
+    _check("tq_decode_attention_noalloc", load().tq_decode_attention_noalloc(
+        plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride,
+        float(scale), out.data_ptr(), _stream(stream)))
 
 
 def tq_decode_scores(plan, q, K, ctx_len, ctx_stride, Hkv, scores, workspace, scale=0.0, stream=None):
