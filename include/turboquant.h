@@ -116,16 +116,33 @@ tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const double* pi, con
                        tq_stream stream);
 
 /* ------------------------------------------------------------------ records
- * Compressed vectors, structure of arrays in device memory.  Row i of a
- * cache of `capacity` rows: idx[i*(w*d/32) ...], sgn[i*(m/32) ...],
- * norm[i], rnorm[i].  KV caches use row (b*Hkv + h)*ctx_stride + t.
+ * Compressed vectors, structure of arrays in device memory.  KV caches use
+ * row (b*Hkv + h)*ctx_stride + t.  norm[i] and rnorm[i] belong to row i in
+ * both layouts; the bit words are laid out by `layout`:
+ *
+ * TQ_LAYOUT_ROWS (0, any capacity): row i owns idx[i*(w*d/32) ...] and
+ *   sgn[i*(m/32) ...], with the bit-plane words described at the top.
+ *   Keys, search sets, and any cache read by vector.
+ * TQ_LAYOUT_BLOCK32 (1, capacity a multiple of 32): rows are grouped in
+ *   blocks of 32 (block r/32).  Block k owns idx[k*w*d ...], where word
+ *   p*d + j holds bit p of idx[j] of the block's 32 rows, and sgn[k*m ...],
+ *   where word j holds σ[j] of the 32 rows.  Row t of the block sits at bit
+ *   t/2 + 16*(t%2) (even rows in the low half-word, odd rows in the high
+ *   half).  The same bytes as layout 0, transposed so that one word carries
+ *   one coordinate of 32 consecutive tokens: the layout the value cache
+ *   needs for the tensor-core attention-times-values contraction, which sums
+ *   over tokens.  Writers of one block (tq_quantize appends) merge into it,
+ *   so calls that write the same block must be ordered on one stream.
  */
+typedef enum { TQ_LAYOUT_ROWS = 0, TQ_LAYOUT_BLOCK32 = 1 } tq_layout;
+
 typedef struct tq_records {
   uint32_t* idx;
   uint32_t* sgn;
   float* norm;
   float* rnorm;
   int64_t capacity;
+  int32_t layout;  /* tq_layout */
 } tq_records;
 
 /* ------------------------------------------------------------------ quantize

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libturboquant.so")
 
 TQ_OK, TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_WORKSPACE, TQ_ERR_NUMERIC = 0, -1, -2, -3, -4, -5
 TQ_F32, TQ_BF16 = 0, 1
+TQ_LAYOUT_ROWS, TQ_LAYOUT_BLOCK32 = 0, 1
 
 _c_double_p = ctypes.POINTER(ctypes.c_double)
 _vp = ctypes.c_void_p
@@ -28,7 +29,8 @@ class tq_plan(ctypes.Structure):
 
 
 class tq_records(ctypes.Structure):
-    _fields_ = [("idx", _vp), ("sgn", _vp), ("norm", _vp), ("rnorm", _vp), ("capacity", ctypes.c_int64)]
+    _fields_ = [("idx", _vp), ("sgn", _vp), ("norm", _vp), ("rnorm", _vp), ("capacity", ctypes.c_int64),
+                ("layout", ctypes.c_int32)]
 
 
 # name -> (restype, argtypes)
@@ -166,26 +168,31 @@ class Plan:
 
 
 class Records:
-    """Compressed vectors (SoA) in torch device tensors."""
+    """Compressed vectors (SoA) in torch device tensors.
 
-    def __init__(self, capacity, d, m, w, device="cuda"):
+    layout TQ_LAYOUT_ROWS: one row of bit words per vector; TQ_LAYOUT_BLOCK32:
+    32-row blocks with one coordinate per word (the value-cache layout of the
+    tensor-core decode; capacity a multiple of 32).  Both hold the same bytes.
+    """
+
+    def __init__(self, capacity, d, m, w, device="cuda", layout=TQ_LAYOUT_ROWS):
         import torch
 
-        self.capacity, self.d, self.m, self.w = capacity, d, m, w
+        self.capacity, self.d, self.m, self.w, self.layout = capacity, d, m, w, layout
         self.idx = torch.empty(capacity, w * d // 32, dtype=torch.int32, device=device)
         self.sgn = torch.empty(capacity, m // 32, dtype=torch.int32, device=device)
         self.norm = torch.empty(capacity, dtype=torch.float32, device=device)
         self.rnorm = torch.empty(capacity, dtype=torch.float32, device=device)
         self.c = tq_records(self.idx.data_ptr(), self.sgn.data_ptr(), self.norm.data_ptr(), self.rnorm.data_ptr(),
-                            capacity)
+                            capacity, layout)
 
     @classmethod
-    def wrap(cls, idx, sgn, norm, rnorm, d, m, w):
+    def wrap(cls, idx, sgn, norm, rnorm, d, m, w, layout=TQ_LAYOUT_ROWS):
         """Records over existing tensors (e.g. the oracle's packed words)."""
         self = cls.__new__(cls)
-        self.capacity, self.d, self.m, self.w = norm.shape[0], d, m, w
+        self.capacity, self.d, self.m, self.w, self.layout = norm.shape[0], d, m, w, layout
         self.idx, self.sgn, self.norm, self.rnorm = idx, sgn, norm, rnorm
-        self.c = tq_records(idx.data_ptr(), sgn.data_ptr(), norm.data_ptr(), rnorm.data_ptr(), self.capacity)
+        self.c = tq_records(idx.data_ptr(), sgn.data_ptr(), norm.data_ptr(), rnorm.data_ptr(), self.capacity, layout)
         return self
 
     @property

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const T* __restrict__ q, cons
 
 struct SplitArgs {
   DecodeShape s;
+  int v_layout;                        // tq_layout of the value records
   const uint32_t* kidx; const uint32_t* ksgn; const float* knorm; const float* krnorm;
   const uint32_t* vidx; const uint32_t* vsgn; const float* vnorm; const float* vrnorm;
   const int32_t* ctx_len;
@@ -201,12 +202,25 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
         for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
         if (lane == 0 && g < G) red[warp * kMaxG + g] = v;
       }
-      // stage this chunk's value records
-      if (valid) {
-        const uint32_t* ip = a.vidx + (rowbase + t) * wi;
-        const uint32_t* sp = a.vsgn + (rowbase + t) * ws;
-        for (int k = 0; k < wi; ++k) vw[tid * wr + k] = __ldg(ip + k);
-        for (int k = 0; k < ws; ++k) vw[tid * wr + wi + k] = __ldg(sp + k);
+      // stage this chunk's value records.  Rows layout: token tid's words at
+      // vw[tid*wr ...].  Block layout (c0 is a multiple of 32 and so is the
+      // row base): block kb of the chunk at vw[kb*(w*d+m) ...], plane-major
+      // index words then sign words, one coordinate per word.
+      if (a.v_layout == TQ_LAYOUT_ROWS) {
+        if (valid) {
+          const uint32_t* ip = a.vidx + (rowbase + t) * wi;
+          const uint32_t* sp = a.vsgn + (rowbase + t) * ws;
+          for (int k = 0; k < wi; ++k) vw[tid * wr + k] = __ldg(ip + k);
+          for (int k = 0; k < ws; ++k) vw[tid * wr + wi + k] = __ldg(sp + k);
+        }
+      } else {
+        const int nb = (cnt + 31) >> 5, bw = w * d + m;
+        const int64_t blk = (rowbase + c0) >> 5;
+        for (int e = tid; e < nb * bw; e += kThreads) {
+          const int kb = e / bw, o = e - kb * bw;
+          vw[e] = o < w * d ? __ldg(a.vidx + (blk + kb) * (int64_t)(w * d) + o)
+                            : __ldg(a.vsgn + (blk + kb) * (int64_t)m + (o - w * d));
+        }
       }
       __syncthreads();
       if (tid < G) {
@@ -239,10 +253,16 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
           acc_r[k][g] *= corr[g < G ? g : 0];
           acc_s[k][g] *= corr[g < G ? g : 0];
         }
+        const bool vrows = a.v_layout == TQ_LAYOUT_ROWS;
+        const int bw = w * d + m;
         if (j < d) {
           for (int tt = 0; tt < cnt; ++tt) {
             int idx = 0;
-            for (int p = 0; p < w; ++p) idx |= ((vw[tt * wr + p * (d / 32) + (j >> 5)] >> (j & 31)) & 1) << p;
+            if (vrows)
+              for (int p = 0; p < w; ++p) idx |= ((vw[tt * wr + p * (d / 32) + (j >> 5)] >> (j & 31)) & 1) << p;
+            else
+              for (int p = 0; p < w; ++p)
+                idx |= ((vw[(tt >> 5) * bw + p * d + j] >> tq::block32_bit(tt & 31)) & 1) << p;
             const float c = cent[idx];
 #pragma unroll
             for (int g = 0; g < kMaxG; ++g)
@@ -251,7 +271,9 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
         }
         if (j < m) {
           for (int tt = 0; tt < cnt; ++tt) {
-            const float sg = ((vw[tt * wr + wi + (j >> 5)] >> (j & 31)) & 1) ? 1.0f : -1.0f;
+            const uint32_t sw = vrows ? vw[tt * wr + wi + (j >> 5)] >> (j & 31)
+                                      : vw[(tt >> 5) * bw + w * d + j] >> tq::block32_bit(tt & 31);
+            const float sg = (sw & 1) ? 1.0f : -1.0f;
 #pragma unroll
             for (int g = 0; g < kMaxG; ++g)
               if (g < G) acc_s[k][g] = fmaf(pr[g * kThreads + tt], sg, acc_s[k][g]);
@@ -337,6 +359,7 @@ tq_status check_common(const tq_plan* plan, const void* q, tq_dtype qd, const tq
                        const DecodeShape& s) {
   if (!q || !ctx_len || !tq::aligned16(q) || (qd != TQ_F32 && qd != TQ_BF16)) return TQ_ERR_ARG;
   if (!tq::valid_records(K)) return TQ_ERR_ARG;
+  if (K->layout != TQ_LAYOUT_ROWS) return TQ_ERR_UNSUPPORTED;
   if (K->capacity / s.ctx_stride < int64_t(s.B) * s.Hkv) return TQ_ERR_ARG;
   if (!supported(s)) return TQ_ERR_UNSUPPORTED;
   (void)plan;
@@ -349,7 +372,7 @@ tq_status launch_prep(const tq_plan* plan, const void* q, tq_dtype qd, const Dec
 }
 
 size_t split_smem(const DecodeShape& s) {
-  const int wr = (s.w * s.d + s.m) / 32;
+  const int wr = (s.w * s.d + s.m) / 32;  // words per record: 128 records == 4 blocks of 32
   return sizeof(float) * (s.G * (s.d + s.m) + 8 + 2 * s.G * kThreads + 4 * kMaxG + 2 * kMaxG) +
          sizeof(uint32_t) * kThreads * wr;
 }
@@ -385,6 +408,7 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
   tq_status st = check_common(plan, q, q_dtype, K, ctx_len, s);
   if (st != TQ_OK) return st;
   if (!tq::valid_records(V) || V->capacity / s.ctx_stride < int64_t(B) * Hkv) return TQ_ERR_ARG;
+  if (V->layout == TQ_LAYOUT_BLOCK32 && ctx_stride % 32 != 0) return TQ_ERR_ARG;
   if (!out || !tq::aligned16(out) || !workspace || !tq::aligned16(workspace)) return TQ_ERR_ARG;
   if (ws_bytes < sizeof(float) * ws_floats(s)) return TQ_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -396,6 +420,7 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
   a.s = s;
   a.kidx = K->idx; a.ksgn = K->sgn; a.knorm = K->norm; a.krnorm = K->rnorm;
   a.vidx = V->idx; a.vsgn = V->sgn; a.vnorm = V->norm; a.vrnorm = V->rnorm;
+  a.v_layout = V->layout;
   a.ctx_len = ctx_len;
   a.qt = qt; a.st = stv;
   a.centroids = plan->centroids;

@@ -21,9 +21,14 @@ inline bool valid_plan(const tq_plan* p) {
 }
 
 inline bool valid_records(const tq_records* r) {
-  return r != nullptr && r->idx && r->sgn && r->norm && r->rnorm && r->capacity >= 0 && aligned16(r->idx) &&
-         aligned16(r->sgn) && aligned16(r->norm) && aligned16(r->rnorm);
+  if (r == nullptr || !r->idx || !r->sgn || !r->norm || !r->rnorm || r->capacity < 0) return false;
+  if (!aligned16(r->idx) || !aligned16(r->sgn) || !aligned16(r->norm) || !aligned16(r->rnorm)) return false;
+  if (r->layout == TQ_LAYOUT_ROWS) return true;
+  return r->layout == TQ_LAYOUT_BLOCK32 && r->capacity % 32 == 0;
 }
+
+// Bit of row t (0..31) inside a 32-row block word of TQ_LAYOUT_BLOCK32.
+__host__ __device__ inline int block32_bit(int t) { return (t >> 1) + ((t & 1) << 4); }
 
 // Status of the most recent launch on this thread.
 inline tq_status launch_status() { return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
@@ -44,7 +49,8 @@ unsigned* fault_word();
 
 // tcgen05 quantizer (bf16 input, d = m = 128); rows already offset.
 bool quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n);
-tq_status quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, uint32_t* idx, uint32_t* sgn,
-                      float* norm, float* rnorm, cudaStream_t st);
+// Rows [row0, row0 + n) of `out`; for TQ_LAYOUT_BLOCK32, row0 % 32 == 0.
+tq_status quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, const tq_records* out,
+                      int64_t row0, cudaStream_t st);
 
 }  // namespace tq

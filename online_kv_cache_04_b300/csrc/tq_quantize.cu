@@ -13,6 +13,8 @@
 // coordinates and one warp ballot forms one packed word.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "tq_internal.h"
 
 namespace {
@@ -25,11 +27,28 @@ struct QuantArgs {
   const float* s_rot_t;  // [d][m]  (S Πᵀ)ᵀ
   const float* centroids;
   const float* bounds;
-  uint32_t* idx;         // rows already offset
+  uint32_t* idx;         // layout 0: rows already offset; layout 1: base of the cache
   uint32_t* sgn;
-  float* norm;
+  float* norm;           // rows already offset
   float* rnorm;
+  int64_t row0;          // cache row of x's row 0 (layout 1 addressing)
 };
+
+// Layout 1: merge the bits of the tile's rows into the 32-row block words.
+// Rows [r_lo, r_lo + TV) span at most two blocks; `bits[k]` / `mask[k]` hold
+// the rows of block (r_lo >> 5) + k.  Each bit has one writer per call, so
+// and-then-or on disjoint masks is race-free across CTAs.
+__device__ __forceinline__ void merge_block_word(uint32_t* w0, uint32_t* w1, const uint32_t (&bits)[2],
+                                                 const uint32_t (&mask)[2]) {
+  if (mask[0]) {
+    atomicAnd(w0, ~mask[0]);
+    atomicOr(w0, bits[0] & mask[0]);
+  }
+  if (mask[1]) {
+    atomicAnd(w1, ~mask[1]);
+    atomicOr(w1, bits[1] & mask[1]);
+  }
+}
 
 template <typename T>
 __device__ __forceinline__ float load_elem(const T* p);
@@ -46,8 +65,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 constexpr int kThreads = 128;
 
-template <int TV, typename T>
+template <int TV, typename T, int LAYOUT>
 __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
+  static_assert(TV <= 32 && 32 % TV == 0, "a tile spans at most two 32-row blocks");
   extern __shared__ float sm[];
   const int d = a.d, m = a.m, w = a.w, L = 1 << w;
   float* xs = sm;              // [TV][d] input tile, fp32
@@ -81,7 +101,11 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
     __syncthreads();
 
     // stage 1: u = Π x / n, bucketize, residual, index bit-planes
+    const int64_t blk0 = (a.row0 + v0) & ~int64_t(31);  // first block row of this tile
     for (int j = tid; j < d; j += kThreads) {
+      uint32_t mask[2] = {0u, 0u}, pbits[3][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}};
+      (void)mask;
+      (void)pbits;
       float acc[TV];
 #pragma unroll
       for (int v = 0; v < TV; ++v) acc[v] = 0.0f;
@@ -99,12 +123,28 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
         const float rho = n > 0.0f ? u - cent[idx] : 0.0f;
         rs[v * d + j] = rho;
         const int64_t row = v0 + v;
-        for (int p = 0; p < w; ++p) {
-          const uint32_t word = __ballot_sync(0xffffffffu, (idx >> p) & 1);
-          if (lane == 0 && row < a.n) a.idx[row * words_idx + p * (d / 32) + j / 32] = word;
+        if constexpr (LAYOUT == TQ_LAYOUT_ROWS) {
+          for (int p = 0; p < w; ++p) {
+            const uint32_t word = __ballot_sync(0xffffffffu, (idx >> p) & 1);
+            if (lane == 0 && row < a.n) a.idx[row * words_idx + p * (d / 32) + j / 32] = word;
+          }
+        } else {
+          const int64_t r = a.row0 + row;
+          const int k = (int)((r >> 5) - (blk0 >> 5));
+          const uint32_t bit = row < a.n ? 1u << tq::block32_bit((int)(r & 31)) : 0u;
+          mask[k] |= bit;
+#pragma unroll
+          for (int p = 0; p < 3; ++p)
+            if (p < w && ((idx >> p) & 1)) pbits[p][k] |= bit;
         }
         const float r2 = warp_sum(rho * rho);
         if (lane == 0) atomicAdd(&rsq[v], r2);
+      }
+      if constexpr (LAYOUT == TQ_LAYOUT_BLOCK32) {
+        for (int p = 0; p < w; ++p) {
+          uint32_t* w0 = a.idx + (blk0 >> 5) * (int64_t)(w * d) + p * d + j;
+          merge_block_word(w0, w0 + w * d, pbits[p], mask);
+        }
       }
     }
     __syncthreads();
@@ -119,11 +159,25 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
 #pragma unroll
         for (int v = 0; v < TV; ++v) acc[v] = fmaf(sij, rs[v * d + i], acc[v]);
       }
+      if constexpr (LAYOUT == TQ_LAYOUT_ROWS) {
 #pragma unroll
-      for (int v = 0; v < TV; ++v) {
-        const uint32_t word = __ballot_sync(0xffffffffu, acc[v] >= 0.0f);
-        const int64_t row = v0 + v;
-        if (lane == 0 && row < a.n) a.sgn[row * words_sgn + jj / 32] = word;
+        for (int v = 0; v < TV; ++v) {
+          const uint32_t word = __ballot_sync(0xffffffffu, acc[v] >= 0.0f);
+          const int64_t row = v0 + v;
+          if (lane == 0 && row < a.n) a.sgn[row * words_sgn + jj / 32] = word;
+        }
+      } else {
+        uint32_t mask[2] = {0u, 0u}, sbits[2] = {0u, 0u};
+#pragma unroll
+        for (int v = 0; v < TV; ++v) {
+          const int64_t row = v0 + v, r = a.row0 + row;
+          const int k = (int)((r >> 5) - (blk0 >> 5));
+          const uint32_t bit = row < a.n ? 1u << tq::block32_bit((int)(r & 31)) : 0u;
+          mask[k] |= bit;
+          if (acc[v] >= 0.0f) sbits[k] |= bit;
+        }
+        uint32_t* w0 = a.sgn + (blk0 >> 5) * (int64_t)m + jj;
+        merge_block_word(w0, w0 + m, sbits, mask);
       }
     }
     if (tid < TV && v0 + tid < a.n) {
@@ -134,10 +188,10 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
   }
 }
 
-template <int TV, typename T>
+template <int TV, typename T, int LAYOUT>
 tq_status launch_simt(const QuantArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(float) * (2 * TV * a.d + 2 * TV + 16);
-  auto kern = quantize_simt_kernel<TV, T>;
+  auto kern = quantize_simt_kernel<TV, T, LAYOUT>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return TQ_ERR_CUDA;
@@ -145,6 +199,13 @@ tq_status launch_simt(const QuantArgs& a, cudaStream_t st) {
   const int64_t grid = std::min<int64_t>(ntiles, int64_t(tq::sm_count()) * 8);
   kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
   return tq::launch_status();
+}
+
+template <int LAYOUT>
+tq_status launch_simt_any(const QuantArgs& a, tq_dtype dtype, cudaStream_t st) {
+  if (a.d <= 256)
+    return dtype == TQ_F32 ? launch_simt<16, float, LAYOUT>(a, st) : launch_simt<16, __nv_bfloat16, LAYOUT>(a, st);
+  return dtype == TQ_F32 ? launch_simt<8, float, LAYOUT>(a, st) : launch_simt<8, __nv_bfloat16, LAYOUT>(a, st);
 }
 
 }  // namespace
@@ -156,6 +217,7 @@ extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dt
   if (n == 0) return TQ_OK;
   if (x == nullptr || !tq::aligned16(x) || ld_x < plan->d || ld_x % 8 != 0) return TQ_ERR_ARG;
   if (out_offset > out->capacity || n > out->capacity - out_offset) return TQ_ERR_ARG;
+  const bool rows = out->layout == TQ_LAYOUT_ROWS;
   QuantArgs a;
   a.x = x;
   a.n = n;
@@ -167,14 +229,35 @@ extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dt
   a.s_rot_t = plan->s_rot_t;
   a.centroids = plan->centroids;
   a.bounds = plan->bounds;
-  a.idx = out->idx + out_offset * (plan->w * plan->d / 32);
-  a.sgn = out->sgn + out_offset * (plan->m / 32);
+  a.idx = rows ? out->idx + out_offset * (plan->w * plan->d / 32) : out->idx;
+  a.sgn = rows ? out->sgn + out_offset * (plan->m / 32) : out->sgn;
   a.norm = out->norm + out_offset;
   a.rnorm = out->rnorm + out_offset;
+  a.row0 = out_offset;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (tq::quantize_tc_supported(plan, dtype, n))
-    return tq::quantize_tc(plan, x, n, ld_x, a.idx, a.sgn, a.norm, a.rnorm, st);
-  if (plan->d <= 256)
-    return dtype == TQ_F32 ? launch_simt<16, float>(a, st) : launch_simt<16, __nv_bfloat16>(a, st);
-  return dtype == TQ_F32 ? launch_simt<8, float>(a, st) : launch_simt<8, __nv_bfloat16>(a, st);
+  if (rows) {
+    if (tq::quantize_tc_supported(plan, dtype, n)) return tq::quantize_tc(plan, x, n, ld_x, out, out_offset, st);
+    return launch_simt_any<TQ_LAYOUT_ROWS>(a, dtype, st);
+  }
+  // 32-row blocks: rows up to the first block boundary go through the SIMT
+  // kernel (it merges into a partly written block); the aligned rest may take
+  // the tensor-core kernel, which owns whole blocks.
+  const int64_t head = std::min<int64_t>(n, (32 - out_offset % 32) % 32);
+  if (head > 0) {
+    QuantArgs h = a;
+    h.n = head;
+    tq_status s = launch_simt_any<TQ_LAYOUT_BLOCK32>(h, dtype, st);
+    if (s != TQ_OK || head == n) return s;
+  }
+  const int64_t rest = n - head;
+  const size_t esz = dtype == TQ_F32 ? 4 : 2;
+  const void* xr = static_cast<const char*>(x) + head * ld_x * esz;
+  if (tq::quantize_tc_supported(plan, dtype, rest)) return tq::quantize_tc(plan, xr, rest, ld_x, out, out_offset + head, st);
+  QuantArgs r = a;
+  r.x = xr;
+  r.n = rest;
+  r.norm += head;
+  r.rnorm += head;
+  r.row0 = out_offset + head;
+  return launch_simt_any<TQ_LAYOUT_BLOCK32>(r, dtype, st);
 }

@@ -51,9 +51,9 @@ struct Bars {
 
 struct TcArgs {
   int64_t n;
-  uint32_t* idx;
+  uint32_t* idx;           // TQ_LAYOUT_ROWS: row 0 of this call; TQ_LAYOUT_BLOCK32: block of row 0
   uint32_t* sgn;
-  float* norm;
+  float* norm;             // row 0 of this call
   float* rnorm;
   const float* centroids;  // device [2^w]
   const float* bounds;     // device [2^w - 1]
@@ -70,6 +70,45 @@ __device__ __forceinline__ int bucket(float u, const float (&bnd)[8]) {
   return idx;
 }
 
+// 32 x 32 bit transpose across a warp: lane r holds row r on entry (bit c =
+// element (r, c)); on exit lane c holds column c (bit r = element (r, c)).
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+  const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int sh = 16 >> k;
+    const uint32_t m = masks[k];
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, sh);
+    x = (lane & sh) ? ((x & ~m) | ((y >> sh) & m)) : ((x & m) | ((y & m) << sh));
+  }
+  return x;
+}
+
+// Even bits to the low half-word, odd bits to the high half (bit t -> t/2 + 16(t%2)).
+__device__ __forceinline__ uint32_t unshuffle32(uint32_t x) {
+  uint32_t t;
+  t = (x ^ (x >> 1)) & 0x22222222u; x = x ^ t ^ (t << 1);
+  t = (x ^ (x >> 2)) & 0x0C0C0C0Cu; x = x ^ t ^ (t << 2);
+  t = (x ^ (x >> 4)) & 0x00F000F0u; x = x ^ t ^ (t << 4);
+  t = (x ^ (x >> 8)) & 0x0000FF00u; x = x ^ t ^ (t << 8);
+  return x;
+}
+
+// TQ_LAYOUT_BLOCK32 store of one warp's 32 rows (one block): `words[c]` is
+// this lane's row word for coordinates 32c..32c+31; `valid` has bit L set for
+// valid row L.  Lane L writes the block words of coordinates 32c + L,
+// merging with the stored bits of rows that this call does not write.
+__device__ __forceinline__ void store_block32(uint32_t* blk, const uint32_t (&words)[4], uint32_t valid, int lane) {
+  const uint32_t vm = unshuffle32(valid);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t col = unshuffle32(warp_transpose32(words[c], lane));
+    uint32_t* dst = blk + 32 * c + lane;
+    if (vm == 0xFFFFFFFFu) *dst = col;
+    else if (vm != 0u) *dst = (*dst & ~vm) | (col & vm);
+  }
+}
+
 template <int W>
 __device__ __forceinline__ float centroid(int idx, const float (&cent)[8]) {
   float c = cent[0];
@@ -78,7 +117,7 @@ __device__ __forceinline__ float centroid(int idx, const float (&cent)[8]) {
   return c;
 }
 
-template <int W>
+template <int W, int LAYOUT>
 __global__ void __launch_bounds__(kThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi,
                        const __grid_constant__ CUtensorMap tm_s, const TcArgs a) {
@@ -268,10 +307,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->rho_full[s]));
       const int64_t row = tile * kTile + r;
-      if (row < a.n) {
-        uint4* ip = reinterpret_cast<uint4*>(a.idx + row * (4 * W));
+      const int64_t blk_row = tile * kTile + q * 32;  // this warp's block (layout 1)
+      const uint32_t valid = __ballot_sync(0xffffffffu, row < a.n);
+      if constexpr (LAYOUT == TQ_LAYOUT_ROWS) {
+        if (row < a.n) {
+          uint4* ip = reinterpret_cast<uint4*>(a.idx + row * (4 * W));
 #pragma unroll
-        for (int p = 0; p < W; ++p) ip[p] = make_uint4(planes[p][0], planes[p][1], planes[p][2], planes[p][3]);
+          for (int p = 0; p < W; ++p) ip[p] = make_uint4(planes[p][0], planes[p][1], planes[p][2], planes[p][3]);
+        }
+      } else {
+        if (valid != 0u) {
+#pragma unroll
+          for (int p = 0; p < W; ++p)
+            store_block32(a.idx + (blk_row >> 5) * (W * 128) + p * 128, planes[p], valid, lane);
+        }
       }
       if (!mbar_wait(smem_u32(&bars->p_full[s]), ph, a.fault, kFaultWait)) break;
       tc_fence_after();
@@ -288,8 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[s]));
+      if constexpr (LAYOUT == TQ_LAYOUT_ROWS) {
+        if (row < a.n) *reinterpret_cast<uint4*>(a.sgn + row * 4) = make_uint4(sg[0], sg[1], sg[2], sg[3]);
+      } else {
+        if (valid != 0u) store_block32(a.sgn + (blk_row >> 5) * 128, sg, valid, lane);
+      }
       if (row < a.n) {
-        *reinterpret_cast<uint4*>(a.sgn + row * 4) = make_uint4(sg[0], sg[1], sg[2], sg[3]);
         a.norm[row] = n;
         a.rnorm[row] = n * sqrtf(rsq);
       }
@@ -329,10 +382,10 @@ bool map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int W>
+template <int W, int LAYOUT>
 tq_status launch_w(const CUtensorMap& mx, const CUtensorMap& mp, const CUtensorMap& ms, const TcArgs& a,
                    cudaStream_t st) {
-  auto kern = quantize_tc_kernel<W>;
+  auto kern = quantize_tc_kernel<W, LAYOUT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return TQ_ERR_CUDA;
   const int64_t ntiles = (a.n + kTile - 1) / kTile;
@@ -353,26 +406,36 @@ bool tq::quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n) {
   return plan->d == 128 && plan->m == 128 && dtype == TQ_BF16 && n < (int64_t(1) << 31) && encode_fn() != nullptr;
 }
 
-tq_status tq::quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, uint32_t* idx, uint32_t* sgn,
-                          float* norm, float* rnorm, cudaStream_t st) {
+tq_status tq::quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, const tq_records* out,
+                          int64_t row0, cudaStream_t st) {
+  const bool rows = out->layout == TQ_LAYOUT_ROWS;
+  if (!rows && row0 % 32 != 0) return TQ_ERR_ARG;
   CUtensorMap mx, mp, ms;
   if (!map_bf16(&mx, x, (uint64_t)n, 128, (uint64_t)ld_x) || !map_bf16(&mp, plan->pi_bf16, 256, 128, 128) ||
       !map_bf16(&ms, plan->s_bf16, 256, 128, 128))
     return TQ_ERR_CUDA;
+  const int w = plan->w;
   TcArgs a{};
   a.n = n;
-  a.idx = idx;
-  a.sgn = sgn;
-  a.norm = norm;
-  a.rnorm = rnorm;
+  a.idx = rows ? out->idx + row0 * (w * 4) : out->idx + (row0 / 32) * (w * 128);
+  a.sgn = rows ? out->sgn + row0 * 4 : out->sgn + (row0 / 32) * 128;
+  a.norm = out->norm + row0;
+  a.rnorm = out->rnorm + row0;
   a.centroids = plan->centroids;
   a.bounds = plan->bounds;
   a.fault = tq::fault_word();
   if (!a.fault) return TQ_ERR_CUDA;
-  switch (plan->w) {
-    case 1: return launch_w<1>(mx, mp, ms, a, st);
-    case 2: return launch_w<2>(mx, mp, ms, a, st);
-    default: return launch_w<3>(mx, mp, ms, a, st);
+  if (rows) {
+    switch (w) {
+      case 1: return launch_w<1, TQ_LAYOUT_ROWS>(mx, mp, ms, a, st);
+      case 2: return launch_w<2, TQ_LAYOUT_ROWS>(mx, mp, ms, a, st);
+      default: return launch_w<3, TQ_LAYOUT_ROWS>(mx, mp, ms, a, st);
+    }
+  }
+  switch (w) {
+    case 1: return launch_w<1, TQ_LAYOUT_BLOCK32>(mx, mp, ms, a, st);
+    case 2: return launch_w<2, TQ_LAYOUT_BLOCK32>(mx, mp, ms, a, st);
+    default: return launch_w<3, TQ_LAYOUT_BLOCK32>(mx, mp, ms, a, st);
   }
 }
 

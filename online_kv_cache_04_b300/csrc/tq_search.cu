@@ -186,6 +186,7 @@ extern "C" tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype
       n > recs->capacity || n > INT32_MAX || k < 1 || k > 64 || !idx_out || !score_out || !workspace ||
       !tq::aligned16(workspace) || (q_dtype != TQ_F32 && q_dtype != TQ_BF16))
     return TQ_ERR_ARG;
+  if (recs->layout != TQ_LAYOUT_ROWS) return TQ_ERR_UNSUPPORTED;
   const SearchLayout l = layout(plan->d, plan->m, nq, n, k);
   if (ws_bytes < l.total) return TQ_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -56,20 +56,37 @@ def oracle_quantize(X, d, m, w):
 
 
 def gpu_records_to_numpy(rec, rows, d, m, w):
-    """Unpack rows of a GPU Records object with the oracle's unpacker."""
-    idx_w = rec.idx[rows].cpu().numpy().view(np.uint32)
-    sgn_w = rec.sgn[rows].cpu().numpy().view(np.uint32)
-    return {"idx": opack.unpack_indices(idx_w, w, d), "sgn": opack.unpack_signs(sgn_w),
-            "norm": rec.norm[rows].cpu().numpy(), "rnorm": rec.rnorm[rows].cpu().numpy(),
-            "idx_words": idx_w, "sgn_words": sgn_w}
+    """Unpack rows of a GPU Records object with the oracle's unpacker (either layout)."""
+    if getattr(rec, "layout", _lib.TQ_LAYOUT_ROWS) == _lib.TQ_LAYOUT_ROWS:
+        idx_w = rec.idx[rows].cpu().numpy().view(np.uint32)
+        sgn_w = rec.sgn[rows].cpu().numpy().view(np.uint32)
+        return {"idx": opack.unpack_indices(idx_w, w, d), "sgn": opack.unpack_signs(sgn_w),
+                "norm": rec.norm[rows].cpu().numpy(), "rnorm": rec.rnorm[rows].cpu().numpy(),
+                "idx_words": idx_w, "sgn_words": sgn_w}
+    # block layout: unpack whole blocks, then pick the rows
+    rows = np.arange(rec.capacity)[rows] if isinstance(rows, slice) else np.asarray(rows)
+    b0, b1 = int(rows.min()) // 32, int(rows.max()) // 32 + 1
+    iw = rec.idx.reshape(-1)[b0 * 32 * (w * d // 32):b1 * 32 * (w * d // 32)].cpu().numpy().view(np.uint32)
+    sw = rec.sgn.reshape(-1)[b0 * 32 * (m // 32):b1 * 32 * (m // 32)].cpu().numpy().view(np.uint32)
+    idx = opack.unpack_indices_block32(iw.reshape(b1 - b0, w * d), w, d)[rows - 32 * b0]
+    sgn = opack.unpack_signs_block32(sw.reshape(b1 - b0, m))[rows - 32 * b0]
+    return {"idx": idx, "sgn": sgn, "norm": rec.norm[torch.as_tensor(rows)].cpu().numpy(),
+            "rnorm": rec.rnorm[torch.as_tensor(rows)].cpu().numpy(),
+            "idx_words": opack.pack_indices(idx, w), "sgn_words": opack.pack_signs(sgn)}
 
 
-def oracle_records_to_gpu(q, d, m, w, device="cuda"):
+def oracle_records_to_gpu(q, d, m, w, device="cuda", layout=None):
     """Pack an oracle Quantized result with the oracle's packer and upload it."""
-    idx_w = opack.pack_indices(q.idx, w).view(np.int32)
-    sgn_w = opack.pack_signs(q.sgn).view(np.int32)
+    layout = _lib.TQ_LAYOUT_ROWS if layout is None else layout
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
-    return _lib.Records.wrap(t(idx_w), t(sgn_w), t(q.norm), t(q.rnorm), d, m, w)
+    if layout == _lib.TQ_LAYOUT_ROWS:
+        idx_w = opack.pack_indices(q.idx, w).view(np.int32)
+        sgn_w = opack.pack_signs(q.sgn).view(np.int32)
+    else:
+        n = q.idx.shape[0]
+        idx_w = opack.pack_indices_block32(q.idx, w).reshape(n, w * d // 32).view(np.int32)
+        sgn_w = opack.pack_signs_block32(q.sgn).reshape(n, m // 32).view(np.int32)
+    return _lib.Records.wrap(t(idx_w), t(sgn_w), t(q.norm), t(q.rnorm), d, m, w, layout=layout)
 
 
 def check_indices(got_idx, oq, bounds, min_match=0.9999, tol=1e-5):

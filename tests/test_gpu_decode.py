@@ -166,3 +166,24 @@ def test_longctx_full_size_sampled(gpu_lib, w):
         qs = q[b:b + 1, h * 4:(h + 1) * 4].float().cpu().numpy()
         want, _ = odec.decode_attention(qs, shp(kg), shp(vg), [ctx[b]], Pi, S, c)
         assert rel_l2(out[b, h * 4:(h + 1) * 4], want[0]) <= 1e-3
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_block_layout_values_oracle_records(gpu_lib, w):
+    """V records in 32-row blocks (any shape takes the general kernel): oracle-packed, ragged lengths."""
+    d = m = 128
+    g = torch.Generator().manual_seed(40 + w)
+    B, Hq, Hkv, T = 2, 6, 2, 96
+    K = torch.randn(B, Hkv, T, d, generator=g)
+    V = torch.randn(B, Hkv, T, d, generator=g) * 3
+    q = torch.randn(B, Hq, d, generator=g)
+    kq, krec = _oracle_cache_records(K.numpy(), d, m, w)
+    vq, vrec = _oracle_cache_records(V.numpy(), d, m, w)
+    Pi, S, c, _ = oracle_tables(d, m, w)
+    ctx = [96, 45]
+    want, _ = odec.decode_attention(q.numpy(), krec, vrec, ctx, Pi, S, c)
+    p = plan(d, m, w)
+    Kr = oracle_records_to_gpu(kq, d, m, w)
+    Vr = oracle_records_to_gpu(vq, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    out, _ = _gpu_decode(p, q.cuda(), Kr, Vr, ctx, T, Hkv)
+    assert rel_l2(out, want) <= 1e-3

@@ -118,3 +118,80 @@ def test_generic_d1024_sampled(gpu_lib):
     rec = _run(X, 1024, 1024, 3)
     rows = torch.arange(0, 65536, 64)
     _compare(X[rows.cuda()].cpu().numpy(), rec, rows, 1024, 1024, 3)
+
+
+# ---- 32-row block layout (value caches) -----------------------------------
+
+def _run_block(X, d, m, w, offset, capacity, prefill=None):
+    p = plan(d, m, w)
+    rec = _lib.Records(capacity, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    rec.idx.fill_(-1 if prefill is None else prefill)
+    rec.sgn.fill_(-1 if prefill is None else prefill)
+    _lib.tq_quantize(p, X, rec, out_offset=offset)
+    torch.cuda.synchronize()
+    return rec
+
+
+def _compare_block(X_host, rec, offset, d, m, w):
+    from oracle import pack as opack
+
+    n = X_host.shape[0]
+    rows = np.arange(offset, offset + n)
+    oq = oracle_quantize(X_host, d, m, w)
+    got = gpu_records_to_numpy(rec, rows, d, m, w)
+    _, _, _, bounds = oracle_tables(d, m, w)
+    ok = check_indices(got["idx"], oq, bounds)
+    check_signs(got["sgn"], oq, ok, d)
+    check_norms(got, oq, ok)
+    # whole blocks whose 32 rows all match: block words bit-identical to the oracle's packer
+    iw = rec.idx.reshape(-1, w * d).cpu().numpy().view(np.uint32)
+    sw = rec.sgn.reshape(-1, m).cpu().numpy().view(np.uint32)
+    sg_ok = ok & np.all(got["sgn"] == oq.sgn, axis=1)
+    checked = 0
+    for b in range((offset + 31) // 32, (offset + n) // 32):
+        sel = slice(32 * b - offset, 32 * b - offset + 32)
+        if ok[sel].all():
+            assert np.array_equal(iw[b], opack.pack_indices_block32(oq.idx[sel], w)[0])
+            checked += 1
+        if sg_ok[sel].all():
+            assert np.array_equal(sw[b], opack.pack_signs_block32(oq.sgn[sel])[0])
+    return oq, got, checked
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+@pytest.mark.parametrize("n,off", [(4096, 0), (300, 64), (129, 0), (77, 5), (40, 60), (1, 31)])
+def test_block_layout_bf16_tensor_core(gpu_lib, n, off, w):
+    """bf16 d = m = 128: aligned rows on the tcgen05 kernel, a partial first block on the SIMT kernel."""
+    wl = WORKLOADS["llama8b"]
+    X = make_kv(wl, B=1, T=n, which=1)[0, (n + w) % 8]
+    cap = ((off + n + 31) // 32 + 1) * 32
+    rec = _run_block(X.cuda(), 128, 128, w, off, cap)
+    _, _, checked = _compare_block(X.float().numpy(), rec, off, 128, 128, w)
+    if n >= 64:
+        assert checked > 0
+    assert _lib.tq_fault_flags() == 0
+
+
+def test_block_layout_merges_into_partly_written_blocks(gpu_lib):
+    """Appending rows one call at a time keeps the other rows' bits of a block."""
+    wl = WORKLOADS["llama8b"]
+    d = m = 128
+    w = 2
+    X = make_kv(wl, B=1, T=100, which=0)[0, 2]
+    p = plan(d, m, w)
+    rec = _lib.Records(128, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    rec.idx.fill_(0x5A5A5A5A)
+    rec.sgn.fill_(0x5A5A5A5A)
+    Xd = X.cuda()
+    for a, b in ((0, 3), (3, 4), (4, 37), (37, 70), (70, 100)):
+        _lib.tq_quantize(p, Xd[a:b], rec, out_offset=a)
+    torch.cuda.synchronize()
+    _compare_block(X.float().numpy(), rec, 0, d, m, w)
+
+
+@pytest.mark.parametrize("w", [1, 3])
+def test_block_layout_fp32_simt(gpu_lib, w):
+    wl = WORKLOADS["tiny"]
+    K = make_kv(wl, which=1)[0, 0][:1000]
+    rec = _run_block(K.cuda(), 128, 128, w, 24, 1024 + 32)
+    _compare_block(K.numpy(), rec, 24, 128, 128, w)

@@ -119,3 +119,31 @@ def test_argument_errors_return_codes_without_launching():
     # setup
     assert lib.tq_make_rotation(1, 0, None) == _lib.TQ_ERR_ARG
     assert lib.tq_make_codebook(2, 1, None, None, None) == _lib.TQ_ERR_ARG
+
+
+def test_layout_argument_checks():
+    lib = _lib.load()
+    p = _fake_plan()
+    ref = ctypes.byref
+    # block layout needs a capacity that is a multiple of 32; unknown layouts are rejected
+    odd = _lib.tq_records(4096, 8192, 12288, 16384, 100, _lib.TQ_LAYOUT_BLOCK32)
+    assert lib.tq_quantize(ref(p), 4096, 1, 10, 128, ref(odd), 0, None) == _lib.TQ_ERR_ARG
+    bad = _lib.tq_records(4096, 8192, 12288, 16384, 128, 7)
+    assert lib.tq_quantize(ref(p), 4096, 1, 10, 128, ref(bad), 0, None) == _lib.TQ_ERR_ARG
+    rows = _lib.tq_records(4096, 8192, 12288, 16384, 2 * 64, _lib.TQ_LAYOUT_ROWS)
+    blk = _lib.tq_records(4096, 8192, 12288, 16384, 2 * 64, _lib.TQ_LAYOUT_BLOCK32)
+    n = ctypes.c_size_t(0)
+    assert lib.tq_decode_workspace_size(ref(p), 1, 8, 2, 64, ref(n)) == _lib.TQ_OK
+    # keys are read by vector: the block layout is refused for K
+    assert lib.tq_decode_attention(ref(p), 4096, 1, 1, 8, 2, ref(blk), ref(blk), 4096, 64, 0.0, 4096, 4096,
+                                   n.value, None) == _lib.TQ_ERR_UNSUPPORTED
+    # block-layout values need ctx_stride % 32 == 0
+    blk2 = _lib.tq_records(4096, 8192, 12288, 16384, 2 * 96, _lib.TQ_LAYOUT_BLOCK32)
+    assert lib.tq_decode_workspace_size(ref(p), 1, 8, 2, 90, ref(n)) == _lib.TQ_OK
+    rows2 = _lib.tq_records(4096, 8192, 12288, 16384, 2 * 96, _lib.TQ_LAYOUT_ROWS)
+    assert lib.tq_decode_attention(ref(p), 4096, 1, 1, 8, 2, ref(rows2), ref(blk2), 4096, 90, 0.0, 4096, 4096,
+                                   n.value, None) == _lib.TQ_ERR_ARG
+    # search reads vectors: block layout unsupported
+    assert lib.tq_search_workspace_size(ref(p), 4, 100, 10, ref(n)) == _lib.TQ_OK
+    assert lib.tq_search_topk(ref(p), 4096, 1, 4, ref(blk), 100, 10, 4096, 4096, 4096, n.value,
+                              None) == _lib.TQ_ERR_UNSUPPORTED

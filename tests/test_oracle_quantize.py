@@ -174,3 +174,45 @@ def test_pack_round_trip(w):
     sg = rng.integers(0, 2, size=(7, 128)).astype(bool)
     assert np.array_equal(pack.unpack_indices(pack.pack_indices(idx, w), w, 96), idx)
     assert np.array_equal(pack.unpack_signs(pack.pack_signs(sg)), sg)
+
+
+def test_pack_block32_hand_patterns():
+    d, w = 64, 2
+    idx = np.zeros((64, d), int)
+    idx[1, 5] = 1           # block 0, row 1 -> bit 16 of plane-0 word 5
+    idx[2, 5] = 2           # block 0, row 2 -> bit 1 of plane-1 word 5
+    idx[32 + 31, 63] = 3    # block 1, row 31 -> bit 31 of both planes' word 63
+    words = pack.pack_indices_block32(idx, w)
+    assert words.shape == (2, w * d)
+    expect = np.zeros((2, w * d), np.uint64)
+    expect[0, 5] = 1 << 16
+    expect[0, d + 5] = 1 << 1
+    expect[1, 63] = 1 << 31
+    expect[1, d + 63] = 1 << 31
+    assert np.array_equal(words, expect.astype(np.uint32))
+    # every even row set -> low half-word full; every odd row -> high half
+    sg = np.zeros((32, 32), bool)
+    sg[0::2, 0] = True
+    sg[1::2, 1] = True
+    sw = pack.pack_signs_block32(sg)[0]
+    assert int(sw[0]) == 0x0000FFFF and int(sw[1]) == 0xFFFF0000 and not sw[2:].any()
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_pack_block32_round_trip_and_transpose_of_row_layout(w):
+    rng = np.random.default_rng(10 + w)
+    N, d, m = 96, 64, 96
+    idx = rng.integers(0, 1 << w, size=(N, d))
+    sg = rng.integers(0, 2, size=(N, m)).astype(bool)
+    bw = pack.pack_indices_block32(idx, w)
+    assert np.array_equal(pack.unpack_indices_block32(bw, w, d), idx)
+    assert np.array_equal(pack.unpack_signs_block32(pack.pack_signs_block32(sg)), sg)
+    # same bits as the row layout: bit j % 32 of row word (p, j // 32) of row r
+    # equals bit β(r % 32) of block word (r // 32, p, j)
+    rw = pack.pack_indices(idx, w)
+    for r in (0, 1, 31, 32, 77, 95):
+        for p in range(w):
+            for j in (0, 17, 33, 63):
+                a = (int(rw[r, p * (d // 32) + j // 32]) >> (j % 32)) & 1
+                b = (int(bw[r // 32, p * d + j]) >> int(pack.block32_bit(r % 32))) & 1
+                assert a == b
