@@ -40,6 +40,12 @@ def parse():
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--bits", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the long-context decode sweep")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time tq_decode_attention alone (cold L2) on --workload / --batch; for profilers")
+    ap.add_argument("--quantize-only", action="store_true",
+                    help="time tq_quantize alone (K then V) on --workload / --batch; for profilers")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (0: keep)")
     return ap.parse_args()
 
 
@@ -135,8 +141,8 @@ class ClockSampler:
 
 # --------------------------------------------------------------------- oracle arm
 
-def oracle_step(wl, w, heads):
-    """The float64 oracle on `heads` kv heads of batch row 0: quantize K, V, then decode."""
+def oracle_step(wl, w, heads, T):
+    """The float64 oracle on `heads` kv heads x T tokens of batch row 0: quantize K, V, then decode."""
     import numpy as np
 
     from online_kv_cache_04_b300.workloads import QJL_SEED, ROTATION_SEED, make_kv, make_queries
@@ -146,11 +152,10 @@ def oracle_step(wl, w, heads):
     Pi = rotation.make_rotation(d, ROTATION_SEED)
     S = qjl.make_qjl(wl.m, d, QJL_SEED)
     c, b, _, _ = codebook.lloyd_max(d, w)
-    K = make_kv(wl, B=1, which=0)[:, :heads].float().numpy()
-    V = make_kv(wl, B=1, which=1)[:, :heads].float().numpy()
+    K = make_kv(wl, B=1, T=T, which=0)[:, :heads].float().numpy()
+    V = make_kv(wl, B=1, T=T, which=1)[:, :heads].float().numpy()
     G = wl.Hq // wl.Hkv
     q = make_queries(wl, B=1)[:, :heads * G].float().numpy()
-    T = K.shape[2]
 
     def run():
         recs = []
@@ -173,6 +178,19 @@ def cpu_cores():
     return blas, os.cpu_count()
 
 
+def oracle_sample(wl, w, budget_s):
+    """(run, tokens, T) with T tokens of one kv head chosen so one run takes about budget_s."""
+    probe_T = 1024
+    run, _ = oracle_step(wl, w, 1, probe_T)
+    run()
+    t0 = time.perf_counter()
+    run()
+    per_token = (time.perf_counter() - t0) / probe_T
+    T = int(max(128, min(wl.ctx, budget_s / max(per_token, 1e-9))) // 128 * 128)
+    run, tokens = oracle_step(wl, w, 1, T)
+    return run, tokens, T
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -181,8 +199,9 @@ def run_reference(args):
 
     wl = WORKLOADS[args.workload]
     w = args.bits - 1
-    heads = 2  # bounded sample: 2 of the kv heads, full context
-    run, tokens = oracle_step(wl, w, heads)
+    # the whole --warmup/--steps run stays within about two minutes of host time
+    budget = min(10.0, 120.0 / max(1, args.steps + args.warmup))
+    run, tokens, T = oracle_sample(wl, w, budget)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -191,7 +210,8 @@ def run_reference(args):
     dt = (time.perf_counter() - t0) / args.steps
     value = tokens / dt
     threads, cores = cpu_cores()
-    sample = f"{heads} of {wl.Hkv} kv heads, batch row 0, full context {wl.ctx}, per step"
+    sample = (f"1 of {wl.Hkv} kv heads x first {T} of {wl.ctx} tokens (batch row 0) per step, "
+              f"scaled to the layer's KV tokens")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -211,10 +231,116 @@ def workload_config(wl, bits):
 
 # --------------------------------------------------------------------- GPU arm
 
+def timed(stream, fn, iters, flush=None):
+    """Mean device ms of fn() over iters calls, each preceded (untimed) by an L2 flush."""
+    import torch
+
+    tot = 0.0
+    for _ in range(iters):
+        if flush is not None:
+            flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    return tot / iters
+
+
+def decode_sweep(_lib, plan_cache, stream, flush, bits_list, iters=20):
+    """Decode-only timing on the long-context batch (B=16, ctx 131072, 8 kv heads, GQA 4:1)."""
+    import torch
+
+    from online_kv_cache_04_b300.workloads import QJL_SEED, ROTATION_SEED, WORKLOADS, make_kv, make_queries
+
+    wl = WORKLOADS["longctx"]
+    d, m = wl.d, wl.m
+    B, Hq, Hkv, T = wl.B, wl.Hq, wl.Hkv, wl.ctx
+    res = []
+    for bits in bits_list:
+        w = bits - 1
+        plan = plan_cache.setdefault(w, _lib.Plan(d, m, w, ROTATION_SEED, QJL_SEED))
+        Kr = _lib.Records(B * Hkv * T, d, m, w)
+        Vr = _lib.Records(B * Hkv * T, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+        for which, rec in ((0, Kr), (1, Vr)):
+            for b0 in range(0, B, 4):
+                X = make_kv(wl, B=4, which=which, device="cuda")
+                _lib.tq_quantize(plan, X.reshape(-1, d), rec, out_offset=b0 * Hkv * T)
+                del X
+        q = make_queries(wl, device="cuda")
+        ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        out = torch.empty(B, Hq, d, device="cuda")
+        ws = torch.empty(_lib.tq_decode_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+        fn = lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws)
+        for _ in range(3):
+            fn()
+        ms = timed(stream, fn, iters, flush)
+        rb = rec_bytes(d, m, w)
+        nbytes = 2 * B * Hkv * T * rb + q.numel() * q.element_size() + out.numel() * 4
+        res.append({"bits": bits, "ms_per_call": ms, "bytes_per_call": nbytes, "gbs": nbytes / ms / 1e6,
+                    "frac_of_8tbs": nbytes / ms / 1e6 / NOMINAL_HBM_GBS, "kv_tokens_per_s": B * T / ms * 1e3,
+                    "l2": "flushed before every call"})
+        del Kr, Vr, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_single(args):
+    """One kernel family alone on a (possibly smaller) workload: the command profilers capture."""
+    import dataclasses
+
+    import torch
+
+    from online_kv_cache_04_b300 import _lib
+    from online_kv_cache_04_b300.workloads import QJL_SEED, ROTATION_SEED, WORKLOADS, make_kv, make_queries
+
+    wl = WORKLOADS[args.workload]
+    if args.batch:
+        wl = dataclasses.replace(wl, B=args.batch)
+    w = args.bits - 1
+    d, m = wl.d, wl.m
+    B, Hq, Hkv, T = wl.B, wl.Hq, wl.Hkv, wl.ctx
+    nvec = B * Hkv * T
+    plan = _lib.Plan(d, m, w, ROTATION_SEED, QJL_SEED)
+    Kr = _lib.Records(nvec, d, m, w)
+    Vr = _lib.Records(nvec, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    rb = rec_bytes(d, m, w)
+    if args.quantize_only:
+        K = make_kv(wl, which=0, device="cuda").reshape(nvec, d)
+        V = make_kv(wl, which=1, device="cuda").reshape(nvec, d)
+        fn = lambda: (_lib.tq_quantize(plan, K, Kr), _lib.tq_quantize(plan, V, Vr))
+        nbytes = 2 * nvec * (rb + d * K.element_size())
+        what = "quantize K and V"
+    else:
+        for which, rec in ((0, Kr), (1, Vr)):
+            X = make_kv(wl, which=which, device="cuda").reshape(nvec, d)
+            _lib.tq_quantize(plan, X, rec)
+            del X
+        q = make_queries(wl, device="cuda")
+        ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        out = torch.empty(B, Hq, d, device="cuda")
+        ws = torch.empty(_lib.tq_decode_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+        fn = lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws)
+        nbytes = 2 * nvec * rb
+        what = "decode attention"
+    for _ in range(args.warmup):
+        fn()
+    ms = timed(stream, fn, args.steps, flush)
+    print(json.dumps({"mode": what, "workload": f"{wl.name} B={B}", "bits": args.bits, "ms": ms,
+                      "bytes": nbytes, "gbs": nbytes / ms / 1e6, "fault_flags": _lib.tq_fault_flags()}),
+          flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.decode_only or args.quantize_only:
+        run_single(args)
         return
     import torch
     import torch.distributed as dist
@@ -238,7 +364,9 @@ def main():
     K = make_kv(wl, which=0, device="cuda").reshape(nvec, d)
     V = make_kv(wl, which=1, device="cuda").reshape(nvec, d)
     q = make_queries(wl, device="cuda")
-    Kr, Vr = _lib.Records(nvec, d, m, w), _lib.Records(nvec, d, m, w)
+    # keys by row, values in 32-row blocks (the layout the tensor-core decode reads)
+    Kr = _lib.Records(nvec, d, m, w)
+    Vr = _lib.Records(nvec, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
     ws = torch.empty(_lib.tq_decode_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
     ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
     out = torch.empty(B, Hq, d, device="cuda")
@@ -276,11 +404,16 @@ def main():
     clocks = sampler.stop()
     t_step = sum(e[0].elapsed_time(e[3]) for e in events) / args.steps / 1e3
     t_quant = sum(e[0].elapsed_time(e[1]) + e[1].elapsed_time(e[2]) for e in events) / (2 * args.steps) / 1e3
-    t_dec = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps / 1e3
+    t_dec_step = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps / 1e3
     if world > 1:
         tt = torch.tensor([t_step], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_step = float(tt.item())
+    fault = _lib.tq_fault_flags()
+
+    # decode alone with a cold L2 (inside the step it reads records that quantize just wrote)
+    t_dec = timed(stream, lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws),
+                  max(20, args.steps // 5), flush) / 1e3
 
     # ---- end to end: pinned host inputs in, attention output out, every step
     Kh = K.cpu().pin_memory()
@@ -302,7 +435,7 @@ def main():
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_e2e = max(3, args.steps // 2)
+    n_e2e = max(3, min(args.steps // 2, 50))
     e0.record(stream)
     for _ in range(n_e2e):
         e2e_step()
@@ -325,15 +458,15 @@ def main():
     kernels = {
         "quantize": {"launches_per_step": 2, "ms_per_launch": t_quant * 1e3, "bytes_per_launch": q_bytes,
                      "gbs": q_bytes / t_quant / 1e9, "mvec_per_s": nvec / t_quant / 1e6},
-        "decode_attention": {"launches_per_step": 3, "ms_per_call": t_dec * 1e3, "bytes_per_call": dec_bytes,
-                             "gbs": dec_bytes / t_dec / 1e9, "kv_tokens_per_s": B * T / t_dec,
-                             "frac_of_8tbs": dec_bytes / t_dec / 1e9 / NOMINAL_HBM_GBS},
+        "decode_attention": {"launches_per_call": 3, "ms_per_call_in_step": t_dec_step * 1e3,
+                             "ms_per_call_cold_l2": t_dec * 1e3, "bytes_per_call": dec_bytes,
+                             "gbs_cold_l2": dec_bytes / t_dec / 1e9, "kv_tokens_per_s_cold_l2": B * T / t_dec,
+                             "frac_of_8tbs_cold_l2": dec_bytes / t_dec / 1e9 / NOMINAL_HBM_GBS},
     }
-    dom = "quantize" if 2 * t_quant >= t_dec else "decode_attention"
-    if dom == "quantize":
-        ach, kname, traffic_key = q_bytes / t_quant / 1e9, "quantize", "quantize_simt_kernel"
+    if 2 * t_quant >= t_dec_step:
+        kname, ach, traffic_key = "quantize_tc_kernel", q_bytes / t_quant / 1e9, "quantize_tc_kernel"
     else:
-        ach, kname, traffic_key = dec_bytes / t_dec / 1e9, "decode_attention", "split_kernel"
+        kname, ach, traffic_key = "decode_tc_kernel (prep + main + combine)", dec_bytes / t_dec / 1e9, "decode_tc_kernel"
     traffic = dram_traffic(traffic_key, wl.name)
     line = {
         "metric": METRIC, "value": B * T * world / t_step, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -348,10 +481,13 @@ def main():
         "quantize_mvec_per_s": nvec / t_quant / 1e6,
         "e2e": {"value": B * T * world / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 5 * args.steps,
+        "fault_flags": fault,
         "clocks": clocks,
     }
+    if world == 1 and not args.no_sweep:
+        line["decode_longctx"] = decode_sweep(_lib, {}, stream, flush, (2, 3, 4))
     if world == 1 and not args.no_cpu_baseline:
-        run, tokens = oracle_step(wl, w, 1)
+        run, tokens, Ts = oracle_sample(wl, w, 3.0)
         run()
         n, t0 = 0, time.perf_counter()
         while n < 3 or time.perf_counter() - t0 < 10.0:
@@ -361,7 +497,8 @@ def main():
         threads, cores = cpu_cores()
         line["cpu_baseline"] = {"value": tokens / dt, "unit": UNIT, "cores": threads, "host_cpus": cores,
                                 "kind": "oracle",
-                                "sample": f"1 of {Hkv} kv heads, batch row 0, full context {T}; {n} runs"}
+                                "sample": (f"1 of {Hkv} kv heads x first {Ts} of {T} tokens (batch row 0), "
+                                           f"{n} runs, scaled to the layer's KV tokens")}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -43,9 +43,19 @@ int choose_splits(int B, int Hkv, int64_t ctx_stride) {
   return (int)std::max<int64_t>(1, std::min(want, maxs));
 }
 
+// Partial slots per head of the tensor-core path (0 when it cannot apply).
+int tc_slots(const DecodeShape& s) {
+  if (s.d != 128 || s.m != 128 || s.G > kMaxG || s.ctx_stride % 128 != 0) return 0;
+  const int64_t units = int64_t(s.B) * s.Hkv, tpu = s.ctx_stride / 128;
+  return tq::decode_tc_slots(units, tpu, tq::decode_tc_ctas(units, tpu));
+}
+
+// Workspace: q̃ and s̃ per query head, then the split partials of whichever
+// path runs (sized for the larger of the two).
 size_t ws_floats(const DecodeShape& s) {
   const size_t heads = size_t(s.B) * s.Hq;
-  return heads * (s.d + s.m) + heads * s.nsplit * (2 + s.d + s.m);
+  const size_t parts = std::max<size_t>(s.nsplit, tc_slots(s));
+  return heads * (s.d + s.m) + heads * parts * (2 + s.d + s.m);
 }
 
 bool fill_shape(const tq_plan* plan, int B, int Hq, int Hkv, int64_t ctx_stride, DecodeShape* s) {
@@ -303,6 +313,8 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
 
 struct CombineArgs {
   DecodeShape s;
+  int slots;              // partial slots per head (stride); 0: the general path's nsplit
+  int64_t tpu, ctas;      // tensor-core path: per-unit slot count from its tile partition
   const float* part;
   const float* pi;        // [d][d] Π
   const float* s_rot;     // [m][d] S Πᵀ
@@ -312,13 +324,22 @@ struct CombineArgs {
 
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   extern __shared__ float sm[];
-  const int d = a.s.d, m = a.s.m, ns = a.s.nsplit, stride = 2 + d + m;
+  const int d = a.s.d, m = a.s.m, stride = 2 + d + m;
+  const int head = blockIdx.x;
+  int ns = a.s.nsplit, pitch = a.s.nsplit;
+  if (a.slots > 0) {
+    // CTA c owns flat tiles [c·T/C, (c+1)·T/C): the unit's tiles span CTAs first..last
+    const int b = head / a.s.Hq, hq = head - b * a.s.Hq;
+    const int64_t u = int64_t(b) * a.s.Hkv + hq / a.s.G, T = int64_t(a.s.B) * a.s.Hkv * a.tpu;
+    const int64_t first = ((u * a.tpu + 1) * a.ctas - 1) / T, last = (((u + 1) * a.tpu) * a.ctas - 1) / T;
+    ns = (int)(last - first + 1);
+    pitch = a.slots;
+  }
   float* acc = sm;              // [d + m]
   float* y = acc + d + m;       // [d]
   float* wgt = y + d;           // [ns]
   __shared__ float lsum;
-  const int head = blockIdx.x;
-  const float* pp = a.part + (size_t)head * ns * stride;
+  const float* pp = a.part + (size_t)head * pitch * stride;
   if (threadIdx.x == 0) {
     float mx = -INFINITY;
     for (int k = 0; k < ns; ++k) mx = fmaxf(mx, pp[(size_t)k * stride]);
@@ -416,6 +437,25 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
   float* stv = qt + size_t(B) * Hq * s.d;
   float* part = stv + size_t(B) * Hq * s.m;
   if ((st = launch_prep(plan, q, q_dtype, s, qt, stv, cs)) != TQ_OK) return st;
+  const float sc = scale > 0.0f ? scale : 1.0f / sqrtf((float)s.d);
+  if (tq::decode_tc_supported(plan, s.G, V, ctx_stride)) {
+    const int slots = tc_slots(s);
+    if ((st = tq::launch_decode_tc(plan, K, V, ctx_len, B, Hq, Hkv, ctx_stride, sc, qt, stv, part, slots, cs)) !=
+        TQ_OK)
+      return st;
+    CombineArgs c{};
+    c.s = s;
+    c.slots = slots;
+    c.tpu = ctx_stride / 128;
+    c.ctas = tq::decode_tc_ctas(int64_t(B) * Hkv, c.tpu);
+    c.part = part;
+    c.pi = plan->pi;
+    c.s_rot = plan->s_rot;
+    c.alpha = plan->qjl_alpha;
+    c.out = out;
+    combine_kernel<<<B * Hq, 256, sizeof(float) * (2 * s.d + s.m + slots), cs>>>(c);
+    return tq::launch_status();
+  }
   SplitArgs a{};
   a.s = s;
   a.kidx = K->idx; a.ksgn = K->sgn; a.knorm = K->norm; a.krnorm = K->rnorm;

@@ -53,4 +53,13 @@ bool quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n);
 tq_status quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, const tq_records* out,
                       int64_t row0, cudaStream_t st);
 
+// Tensor-core decode (tq_decode_tc.cu): d = m = 128, G <= 8, values in
+// TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Partials [B*Hq][slots][2 + 256].
+bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride);
+int decode_tc_ctas(int64_t units, int64_t tpu);
+int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas);
+tq_status launch_decode_tc(const tq_plan* plan, const tq_records* K, const tq_records* V, const int32_t* ctx_len,
+                           int B, int Hq, int Hkv, int64_t ctx_stride, float scale, const float* qt, const float* st,
+                           float* part, int smax, cudaStream_t stream);
+
 }  // namespace tq
