@@ -55,17 +55,10 @@ using namespace tq::sm100;
 constexpr int kTile = 128;
 constexpr int kD = 128;
 constexpr int kStages = 4;
-constexpr int kKR = 4, kVR = 2;               // TMEM ring slots: key planes, value planes
-constexpr int kThreads = 320, kMmaWarp = 8, kLoadWarp = 9;
+constexpr int kThreads = 352, kMmaWarp = 8, kLoadWarp = 9, kVMmaWarp = 10;
 constexpr float kTau = 6.0f;                  // lazy-rescale threshold (log2 units)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFaultDecode = 2u;
-
-constexpr uint32_t kColK = 0;                 // kKR x 32 columns (128 e4m3 per lane)
-constexpr uint32_t kColV = 128;               // kVR x 64 columns (128 f16 per lane)
-constexpr uint32_t kColS = 256;               // 2 buffers x (MSE | QJL) x NH columns
-constexpr uint32_t kColVD = 384;              // NP x 16 columns
-constexpr uint32_t kColOne = 480;             // 8 columns: f16 -1 at elements 0..7, then zeros
 constexpr uint32_t kTmemCols = 512;
 
 // e4m3 key operand, layer i = bit i of each byte: value C (bit clear) or C' (bit set)
@@ -79,7 +72,7 @@ __constant__ float c_v_delta[6] = {0.5f, 0.75f, 0.9375f, 0.99609375f, 2.0f, -2.0
 __constant__ float c_v_mean[6] = {0.75f, 0.625f, 0.53125f, 0.501953125f, 1.0f, 0.0f};
 
 // Token pair i (tokens 2i, 2i+1 of a 32-row block sit at bits i, i+16) is
-// shifted left by vshift(i) so that it lands on position vpos(i) in 10..15.
+// shifted left so that it lands on position vpos(i) in 10..15.
 __host__ __device__ constexpr int vpos(int i) { return i >= 10 ? i : (i >= 4 ? i + 6 : i + 12); }
 
 struct TcArgs {
@@ -104,11 +97,24 @@ __host__ __device__ inline int64_t owner(int64_t f, int64_t total, int64_t ctas)
   return ((f + 1) * ctas - 1) / total;
 }
 
-template <int W>
+// Per-instantiation sizes.  TMEM columns: key ring (KR slots of one plane,
+// 32 columns = 128 e4m3), value ring (VR slots of half a plane, 32 columns =
+// 64 tokens of f16), score accumulators (2 buffers x MSE|QJL x NH), value
+// accumulators (NP x 16), one constant -1 operand column group (8).
+template <int W, int GP>
 struct Shape {
   static constexpr int NPM = W == 3 ? 4 : W;  // ±1 planes of the codebook
   static constexpr int NP = NPM + 1;          // plus the QJL sign plane
-  static constexpr int kIdxBytes = kTile * 4 * W * 4;       // keys, rows layout
+  static constexpr int NH = 4 * GP;           // 4 pieces x GP heads
+  static constexpr int kRing = (512 - 4 * NH - 16 * NP - 8) / 32;  // key + value slots that fit
+  static constexpr int KR = (kRing + 1) / 2 < 2 * NP ? (kRing + 1) / 2 : 2 * NP;
+  static constexpr int VR = kRing - KR < 4 * NP ? kRing - KR : 4 * NP;
+  static constexpr uint32_t kColK = 0, kColV = 32 * KR, kColS = kColV + 32 * VR, kColVD = kColS + 4 * NH,
+                            kColOne = kColVD + 16 * NP;
+  static_assert(kColOne + 8 <= kTmemCols, "TMEM plan exceeds 512 columns");
+  static_assert(KR >= NP && VR >= 2, "rings too small for one tile");
+  static_assert(VR <= 4 * NP, "value ring deeper than two tiles breaks the end-of-segment wait");
+  static constexpr int kIdxBytes = kTile * 4 * W * 4;
   static constexpr int kStage = 2 * kIdxBytes + 2 * 2048 + 4 * 512;
   static constexpr int kOffKIdx = 0, kOffKSgn = kIdxBytes, kOffKNorm = kOffKSgn + 2048, kOffKRn = kOffKNorm + 512;
   static constexpr int kOffVIdx = kOffKRn + 512, kOffVSgn = kOffVIdx + kIdxBytes, kOffVNorm = kOffVSgn + 2048,
@@ -120,22 +126,22 @@ constexpr int kOffBV = 5 * 4096;           // 2 buffers x 3 SW128 atoms of 2 KB 
 constexpr int kBVBytes = 3 * 2048;
 constexpr int kOffRing = kOffBV + 2 * kBVBytes;
 constexpr int kMiscBytes = 4096;
+constexpr int kMaxRing = 16;
 
 struct Misc {
   uint64_t ld_full[kStages], ld_empty[kStages];
-  uint64_t ka_full[kKR], ka_empty[kKR], va_full[kVR], va_empty[kVR];
+  uint64_t ka_full[kMaxRing], ka_empty[kMaxRing], va_full[kMaxRing], va_empty[kMaxRing];
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
-  uint64_t vd_done, bk_full, vd_free, kgroup, st_full[2], st_empty[2];
+  uint64_t bk_full, vd_free, kgroup, st_full[2], st_empty[2];
   uint32_t tmem_base;
   int abort;
   float red[2][4][8];       // per-tile warp maxima [parity][warp][head]
   float amax[2][8];         // per-unit weight maxima (as non-negative float bits)
-  float E[2][8], O[2][8];   // piece scale and offset per (part, head)
+  float O[2][8];            // per-unit offset per (part, head)
   float coef[4];
   float stat_m[2][8];       // per segment parity: reference M per head
   float stat_l[2][4][8];    // per segment parity, per key warp: Σ p
 };
-
 static_assert(sizeof(Misc) <= kMiscBytes, "barriers and per-head state must fit their region");
 
 // Segment of this CTA's tile range that falls in one unit.
@@ -180,11 +186,44 @@ __device__ __forceinline__ uint32_t sw128(int n, int e) {
 // two SW128 atoms of 64 tokens (128 bytes per row), 2 KB apart.
 __device__ __forceinline__ uint32_t bv_off(int n, int t) { return (t >> 6) * 2048 + sw128(n, (t & 63) * 2); }
 
+// Sum (or max) of N values over the 32 lanes of a warp, N a power of two <= 32,
+// by halving: afterwards lane L holds the result for index bits (L >> (5 -
+// log2 N)) ... of v (see lane_index), written to v[0].
+template <int N, bool MAX>
+__device__ __forceinline__ float warp_reduce_many(float (&v)[N], int lane) {
+#pragma unroll
+  for (int n = N, sh = 16; n > 1; n >>= 1, sh >>= 1) {
+    const bool upper = lane & sh;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, sh);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  float x = v[0];
+#pragma unroll
+  for (int sh = 32 / N / 2; sh > 0; sh >>= 1) {
+    const float got = __shfl_xor_sync(0xffffffffu, x, sh);
+    x = MAX ? fmaxf(x, got) : x + got;
+  }
+  return x;
+}
+// Index of the value that warp_reduce_many<N> leaves in lane L.
+template <int N>
+__device__ __forceinline__ int lane_index(int lane) {
+  int idx = 0;
+#pragma unroll
+  for (int n = N, sh = 16, bit = N / 2; n > 1; n >>= 1, sh >>= 1, bit >>= 1)
+    if (lane & sh) idx += bit;
+  return idx;
+}
+
 template <int W, int GP>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) {
-  using Sh = Shape<W>;
-  constexpr int NPM = Sh::NPM, NP = Sh::NP;
-  constexpr int NH = 4 * GP;                     // 4 pieces x GP heads
+  using Sh = Shape<W, GP>;
+  constexpr int NPM = Sh::NPM, NP = Sh::NP, NH = Sh::NH, KR = Sh::KR, VR = Sh::VR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -198,11 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       mbar_init(smem_u32(&ms->ld_full[s]), 1);
       mbar_init(smem_u32(&ms->ld_empty[s]), 8);
     }
-    for (int s = 0; s < kKR; ++s) {
+    for (int s = 0; s < KR; ++s) {
       mbar_init(smem_u32(&ms->ka_full[s]), 4);
       mbar_init(smem_u32(&ms->ka_empty[s]), 1);
     }
-    for (int s = 0; s < kVR; ++s) {
+    for (int s = 0; s < VR; ++s) {
       mbar_init(smem_u32(&ms->va_full[s]), 4);
       mbar_init(smem_u32(&ms->va_empty[s]), 1);
     }
@@ -214,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       mbar_init(smem_u32(&ms->st_full[s]), 4);
       mbar_init(smem_u32(&ms->st_empty[s]), 4);
     }
-    mbar_init(smem_u32(&ms->vd_done), 1);
     mbar_init(smem_u32(&ms->bk_full), 4);
     mbar_init(smem_u32(&ms->vd_free), 4);
     mbar_init(smem_u32(&ms->kgroup), 4);
@@ -269,37 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         mbar_wait(smem_u32(&ms->ld_full[g % kStages]), (uint32_t)((g / kStages) & 1), a.fault, kFaultDecode);
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issue
+    // ------------------------------------------------------------ key MMAs (scores)
     if (lane == 0) {
       constexpr uint32_t idk = idesc_e4m3_f32(128, NH);
-      constexpr uint32_t idv = idesc_f16_f32(128, 16);
-      int64_t gi = 0, kc = 0, vc = 0;
+      int64_t gi = 0, kc = 0;
       int nseg = 0;
       bool ok = true;
-      auto vmma = [&](int64_t g, bool first) {
-        const int sb = (int)(g & 1);
-        if (!wait(&ms->p_full[sb], (uint32_t)((g >> 1) & 1))) return false;
-        if (first && nseg >= 1 && !wait(&ms->vd_free, (uint32_t)((nseg - 1) & 1))) return false;
-        tc_fence_after();
-        const uint32_t bv = sbase + kOffBV + sb * kBVBytes;
-#pragma unroll 1
-        for (int P = 0; P < NP; ++P, ++vc) {
-          const int slot = (int)(vc % kVR);
-          if (!wait(&ms->va_full[slot], (uint32_t)((vc / kVR) & 1))) return false;
-          tc_fence_after();
-#pragma unroll 1
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bd = desc_sw128(bv + (kk >> 2) * 2048) + (((kk & 3) * 32) >> 4);
-            mma_ts(tmem + kColVD + 16 * P, tmem + kColV + slot * 64 + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
-          }
-          // minus this tile's operand offsets Σ w·(C + C')/2 (per key warp, f16 hi + lo)
-          mma_ts(tmem + kColVD + 16 * P, tmem + kColOne, desc_sw128(bv + 2 * 2048), idv, 1u);
-          mma_commit(smem_u32(&ms->va_empty[slot]));
-        }
-        mma_commit(smem_u32(&ms->p_empty[sb]));
-        mma_commit(smem_u32(&ms->vd_done));
-        return true;
-      };
       for (int64_t f = f0; ok && f < f1;) {
         int64_t next;
         const Seg sg = segment_at(a, f, f1, &next);
@@ -313,23 +326,66 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           if (g >= 2 && !(ok = wait(&ms->s_empty[sb], (uint32_t)(((g >> 1) - 1) & 1)))) break;
 #pragma unroll 1
           for (int P = 0; P < NP; ++P, ++kc) {
-            const int slot = (int)(kc % kKR);
-            if (!(ok = wait(&ms->ka_full[slot], (uint32_t)((kc / kKR) & 1)))) break;
+            const int slot = (int)(kc % KR);
+            if (!(ok = wait(&ms->ka_full[slot], (uint32_t)((kc / KR) & 1)))) break;
             tc_fence_after();
-            const uint32_t d = tmem + kColS + sb * 2 * NH + (P < NPM ? 0 : NH);
+            const uint32_t d = tmem + Sh::kColS + sb * 2 * NH + (P < NPM ? 0 : NH);
             const uint64_t bd = desc_sw128(sbase + kOffBK + P * 4096);
 #pragma unroll 1
             for (int kk = 0; kk < 4; ++kk) {
               const uint32_t acc = (P < NPM) ? ((P > 0 || kk > 0) ? 1u : 0u) : (kk > 0 ? 1u : 0u);
-              mma_ts_f8(d, tmem + kColK + slot * 32 + kk * 8, bd + ((kk * 32) >> 4), idk, acc);
+              mma_ts_f8(d, tmem + Sh::kColK + slot * 32 + kk * 8, bd + ((kk * 32) >> 4), idk, acc);
             }
             mma_commit(smem_u32(&ms->ka_empty[slot]));
           }
           if (!ok) break;
           mma_commit(smem_u32(&ms->s_full[sb]));
-          if (k >= 1 && !(ok = vmma(g - 1, k == 1))) break;
         }
-        if (ok) ok = vmma(gi + sg.n - 1, sg.n == 1);
+        gi += sg.n;
+        ++nseg;
+      }
+    }
+  } else if (warp == kVMmaWarp) {
+    // ------------------------------------------------------------ value MMAs (weights x values)
+    if (lane == 0) {
+      constexpr uint32_t idv = idesc_f16_f32(128, 16);
+      int64_t gi = 0, vc = 0;
+      int nseg = 0;
+      bool ok = true;
+      for (int64_t f = f0; ok && f < f1;) {
+        int64_t next;
+        const Seg sg = segment_at(a, f, f1, &next);
+        f = next;
+        if (sg.n == 0) continue;
+        for (int k = 0; ok && k < sg.n; ++k) {
+          const int64_t g = gi + k;
+          const int sb = (int)(g & 1);
+          const bool first = k == 0;
+          if (!(ok = wait(&ms->p_full[sb], (uint32_t)((g >> 1) & 1)))) break;
+          if (first && nseg >= 1 && !(ok = wait(&ms->vd_free, (uint32_t)((nseg - 1) & 1)))) break;
+          tc_fence_after();
+          const uint32_t bv = sbase + kOffBV + sb * kBVBytes;
+#pragma unroll 1
+          for (int P = 0; ok && P < NP; ++P) {
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half, ++vc) {
+              const int slot = (int)(vc % VR);
+              if (!(ok = wait(&ms->va_full[slot], (uint32_t)((vc / VR) & 1)))) break;
+              tc_fence_after();
+              const uint32_t d = tmem + Sh::kColVD + 16 * P;
+#pragma unroll 1
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = desc_sw128(bv + half * 2048) + ((kk * 32) >> 4);
+                mma_ts(d, tmem + Sh::kColV + slot * 32 + kk * 8, bd, idv, (first && half == 0 && kk == 0) ? 0u : 1u);
+              }
+              // minus this tile's operand offsets Σ w·(C + C')/2 (per key warp, f16 hi + lo)
+              if (half == 1) mma_ts(d, tmem + Sh::kColOne, desc_sw128(bv + 2 * 2048), idv, 1u);
+              mma_commit(smem_u32(&ms->va_empty[slot]));
+            }
+          }
+          if (!ok) break;
+          mma_commit(smem_u32(&ms->p_empty[sb]));
+        }
         gi += sg.n;
         ++nseg;
       }
@@ -343,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
     int segc = 0;
     bool ok = true;
     float M[GP], lsum[GP], E_m[GP], E_q[GP], O_m[GP], O_q[GP];
-    const int pair = (r & 31) >> 1, vp = vpos(pair) - 10;
-    const float vdelta = c_v_delta[vp], vmean = c_v_mean[vp];
-    // expand tile g (stage g % kStages) into kNP key planes of the TMEM ring
+    const int vp = vpos((r & 31) >> 1) - 10;
+    const float two_over_delta = 2.0f / c_v_delta[vp], vmean = c_v_mean[vp];
+    // expand tile g (stage g % kStages) into the NP key planes of the TMEM ring
     auto expand = [&](int64_t g) {
       const int s = (int)(g % kStages);
       if (!wait(&ms->ld_full[s], (uint32_t)((g / kStages) & 1))) return false;
@@ -363,25 +419,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
       for (int k = 0; k < 4; ++k)  // w = 3: the product plane s0·s1·s2 has bit b0 ^ b1 ^ b2
         tw[k] = W == 3 ? iw[k] ^ iw[(4 + k) % (4 * W)] ^ iw[(8 + k) % (4 * W)] : 0u;
+      // all planes of the tile are stored, then one wait for the stores, then
+      // every slot is released to the MMA warp
 #pragma unroll
       for (int P = 0; P < NP; ++P) {
         uint32_t pw[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) pw[k] = P < W ? iw[(4 * P + k) % (4 * W)] : (P < NPM ? tw[k] : sw[k]);
-        const int slot = (int)(kc % kKR);
-        if (kc >= kKR && !wait(&ms->ka_empty[slot], (uint32_t)((kc / kKR - 1) & 1))) return false;
+        const int64_t c = kc + P;
+        const int slot = (int)(c % KR);
+        if (c >= KR && !wait(&ms->ka_empty[slot], (uint32_t)((c / KR - 1) & 1))) return false;
         uint32_t vals[32];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
           for (int i = 0; i < 8; ++i) vals[8 * k + i] = (pw[k] & (0x01010101u << i)) | c_k_base[i];
-        tmem_st32(tmem + lane_base + kColK + slot * 32, vals);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ms->ka_full[slot]));
-        ++kc;
+        tmem_st32(tmem + lane_base + Sh::kColK + slot * 32, vals);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0)
+        for (int P = 0; P < NP; ++P) mbar_arrive(smem_u32(&ms->ka_full[(kc + P) % KR]));
+      kc += NP;
       return true;
     };
     for (int64_t f = f0; ok && f < f1;) {
@@ -480,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             uint32_t v[32];
 #pragma unroll
             for (int c = 0; c < 2 * NH / 32; ++c) {
-              tmem_ld32(tmem + lane_base + kColS + sb * 2 * NH + 32 * c, v);
+              tmem_ld32(tmem + lane_base + Sh::kColS + sb * 2 * NH + 32 * c, v);
               tmem_ld_wait();
 #pragma unroll
               for (int e = 0; e < 32; ++e) dv[32 * c + e] = __uint_as_float(v[e]);
@@ -510,12 +570,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             av[hh] = s2[hh] + fmaxf(lvn, -32.f);
           }
           // tile maximum of log2(p·‖v‖) per head, across the four key warps
+          {
+            float x[GP];
 #pragma unroll
-          for (int hh = 0; hh < GP; ++hh) {
-            float x = av[hh];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-            if (lane == 0) ms->red[g & 1][warp][hh] = x;
+            for (int hh = 0; hh < GP; ++hh) x[hh] = av[hh];
+            const float mx = warp_reduce_many<GP, true>(x, lane);
+            if ((lane & (32 / GP - 1)) == 0) ms->red[g & 1][warp][lane_index<GP>(lane)] = mx;
           }
           if (!(ok = kgroup_sync(ms, &kgc, a.fault))) break;
           float fac[GP];
@@ -532,13 +592,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             M[hh] = nm;
           }
           if (rescale) {
-            // value accumulators of the tiles so far: wait for their MMAs, scale in place
-            if (!(ok = wait(&ms->vd_done, (uint32_t)((g - 1) & 1)))) break;
+            // value accumulators of the tiles so far: wait for their MMAs (tile g-1's
+            // weight buffer release; its phase is at most one behind, since tile g-3's
+            // release was awaited before tile g-1's weights were written), scale in place
+            if (!(ok = wait(&ms->p_empty[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1)))) break;
             tc_fence_after();
 #pragma unroll
             for (int P = 0; P < NP; ++P) {
               uint32_t v[16];
-              tmem_ld16(tmem + lane_base + kColVD + 16 * P, v);
+              tmem_ld16(tmem + lane_base + Sh::kColVD + 16 * P, v);
               tmem_ld_wait();
 #pragma unroll
               for (int c = 0; c < 16; ++c) {
@@ -548,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
               uint32_t v8a[8], v8b[8];
 #pragma unroll
               for (int c = 0; c < 8; ++c) v8a[c] = v[c], v8b[c] = v[8 + c];
-              tmem_st8(tmem + lane_base + kColVD + 16 * P, v8a);
-              tmem_st8(tmem + lane_base + kColVD + 16 * P + 8, v8b);
+              tmem_st8(tmem + lane_base + Sh::kColVD + 16 * P, v8a);
+              tmem_st8(tmem + lane_base + Sh::kColVD + 16 * P + 8, v8b);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -559,30 +621,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           // attention weights of this tile -> f16 B operand of the value MMA
           if (g >= 2 && !(ok = wait(&ms->p_empty[sb], (uint32_t)(((g >> 1) - 1) & 1)))) break;
           uint8_t* bv = smem + kOffBV + sb * kBVBytes;
+          float off[2 * GP];
 #pragma unroll
           for (int hh = 0; hh < GP; ++hh) {
+            off[hh] = off[GP + hh] = 0.f;
             if (hh >= a.G) continue;
             const bool live = valid && M[hh] != -INFINITY;
             const float p = live ? exp2f(s2[hh] - M[hh]) : 0.f;
             const float wm = live ? exp2f(s2[hh] + lvn - M[hh]) : 0.f;
             const float wq = p * vr;
             lsum[hh] += p;
-            const __half hm = __float2half_rn(2.f * wm / vdelta);
-            const __half hq = __float2half_rn(2.f * wq / vdelta);
+            const __half hm = __float2half_rn(wm * two_over_delta);
+            const __half hq = __float2half_rn(wq * two_over_delta);
             *reinterpret_cast<__half*>(bv + bv_off(hh, r)) = hm;
             *reinterpret_cast<__half*>(bv + bv_off(8 + hh, r)) = hq;
-            // this warp's operand offset for both weight rows, as f16 hi + lo at
-            // elements 2·warp, 2·warp + 1 of the offset row (A there is -1)
-            float om = __half2float(hm) * vmean, oq = __half2float(hq) * vmean;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              om += __shfl_xor_sync(0xffffffffu, om, o);
-              oq += __shfl_xor_sync(0xffffffffu, oq, o);
-            }
-            if (lane < 2) {
-              const float x = lane == 0 ? om : oq;
-              const __half hi = __float2half_rn(x), lo = __float2half_rn(x - __half2float(hi));
-              const int n = lane == 0 ? hh : 8 + hh;
+            off[hh] = __half2float(hm) * vmean;
+            off[GP + hh] = __half2float(hq) * vmean;
+          }
+          // this warp's operand offsets for every weight row, as f16 hi + lo at
+          // elements 2·warp, 2·warp + 1 of the offset row (A there is -1)
+          {
+            const float o = warp_reduce_many<2 * GP, false>(off, lane);
+            const int c = lane_index<2 * GP>(lane);
+            if ((lane & (16 / GP - 1)) == 0 && (c % GP) < a.G) {
+              const __half hi = __float2half_rn(o), lo = __float2half_rn(o - __half2float(hi));
+              const int n = c < GP ? c : 8 + (c - GP);
               *reinterpret_cast<__half2*>(bv + 2 * 2048 + sw128(n, 4 * warp)) = __halves2half2(hi, lo);
             }
           }
@@ -619,12 +682,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
     const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
     {
       const uint32_t one[8] = {0xBC00BC00u, 0xBC00BC00u, 0xBC00BC00u, 0xBC00BC00u, 0u, 0u, 0u, 0u};
-      tmem_st8(tmem + lane_base + kColOne, one);
+      tmem_st8(tmem + lane_base + Sh::kColOne, one);
       tmem_st_wait();
       tc_fence_before();
     }
     int64_t gi = 0, vc = 0;
-    int segc = 0, nseg = 0;
+    int segc = 0;
     bool ok = true;
     for (int64_t f = f0; ok && f < f1;) {
       int64_t next;
@@ -636,8 +699,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         if (!(ok = wait(&ms->ld_full[s], (uint32_t)((g / kStages) & 1)))) break;
         const uint32_t* vi = reinterpret_cast<const uint32_t*>(smem + kOffRing + s * Sh::kStage + Sh::kOffVIdx);
         const uint32_t* vsg = reinterpret_cast<const uint32_t*>(smem + kOffRing + s * Sh::kStage + Sh::kOffVSgn);
+        // half-planes are stored in groups of up to VR, one store wait per group
+        int pending = 0;
+        auto release = [&]() {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0)
+            for (int e = 0; e < pending; ++e) mbar_arrive(smem_u32(&ms->va_full[(vc - pending + e) % VR]));
+          pending = 0;
+        };
 #pragma unroll 1
-        for (int P = 0; P < NP; ++P, ++vc) {
+        for (int P = 0; ok && P < NP; ++P) {
           uint32_t bw[4];
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
@@ -646,10 +719,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
               bw[kb] = vi[(kb * W) * kD + j] ^ vi[(kb * W + 1 % W) * kD + j] ^ vi[(kb * W + 2 % W) * kD + j];
             else bw[kb] = vsg[kb * kD + j];
           }
-          const int slot = (int)(vc % kVR);
-          if (vc >= kVR && !(ok = wait(&ms->va_empty[slot], (uint32_t)((vc / kVR - 1) & 1)))) break;
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
+            const int slot = (int)(vc % VR);
+            if (pending == VR) release();
+            if (vc >= VR && !(ok = wait(&ms->va_empty[slot], (uint32_t)((vc / VR - 1) & 1)))) break;
             uint32_t vals[32];
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
@@ -662,14 +736,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
                 vals[16 * kk + i] = (src & ((1u << p) | (1u << (p + 16)))) | c_v_base[p - 10];
               }
             }
-            tmem_st32(tmem + lane_base + kColV + slot * 64 + 32 * half, vals);
+            tmem_st32(tmem + lane_base + Sh::kColV + slot * 32, vals);
+            ++vc;
+            ++pending;
           }
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ms->va_full[slot]));
         }
         if (!ok) break;
+        if (pending > 0) release();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ms->ld_empty[s]));
       }
@@ -679,12 +752,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       if (!(ok = wait(&ms->st_full[sp], (uint32_t)((segc >> 1) & 1)))) break;
       float d[NP][16];
       if (sg.n > 0) {
-        if (!(ok = wait(&ms->vd_done, (uint32_t)((gi + sg.n - 1) & 1)))) break;
+        // all value MMAs of the segment: the last tile's weight-buffer release.
+        // Its phase is at most one behind: expanding the last tile needed ring
+        // slots freed by the value MMAs of two tiles earlier (the ring holds at
+        // most two tiles), and those MMAs released the same buffer one phase ago.
+        const int64_t last = gi + sg.n - 1;
+        if (!(ok = wait(&ms->p_empty[last & 1], (uint32_t)((last >> 1) & 1)))) break;
         tc_fence_after();
 #pragma unroll
         for (int P = 0; P < NP; ++P) {
           uint32_t v[16];
-          tmem_ld16(tmem + lane_base + kColVD + 16 * P, v);
+          tmem_ld16(tmem + lane_base + Sh::kColVD + 16 * P, v);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 16; ++c) d[P][c] = __uint_as_float(v[c]);
@@ -716,11 +794,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         if (sg.n > 0) mbar_arrive(smem_u32(&ms->vd_free));
         mbar_arrive(smem_u32(&ms->st_empty[sp]));
       }
-      if (sg.n > 0) ++nseg;
       gi += sg.n;
       ++segc;
     }
-    (void)nseg;
   }
   tc_fence_before();
   __syncthreads();
@@ -732,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 
 template <int W>
 constexpr int smem_bytes() {
-  return 1024 + kOffRing + kStages * Shape<W>::kStage + kMiscBytes;
+  return 1024 + kOffRing + kStages * Shape<W, 4>::kStage + kMiscBytes;
 }
 
 }  // namespace

@@ -35,6 +35,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try_wait, but the thread may stay suspended in hardware until the
+// phase completes or about `hint_ns` nanoseconds pass, instead of returning at
+// once: waiting warps then take no issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Bound of every pipeline wait, in SM clock cycles (about two seconds at the
 // boost clock): a phase that has not completed by then means a lost arrival,
 // not a slow producer.
@@ -48,8 +62,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 0 && clock64() - t0 > kWaitBoundCycles) break;
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if ((i & 15) == 0 && clock64() - t0 > kWaitBoundCycles) break;
   }
   atomicOr(fault, code);
   return false;
@@ -89,8 +103,8 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parit
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if ((i & 3) == 0) {
       if (*abort) return false;
       if (clock64() - t0 > kWaitBoundCycles) break;
     }

@@ -84,6 +84,16 @@ def test_lazy_rescale_and_value_norm_range(gpu_lib):
     assert rel_l2(out, want) <= 1e-3
 
 
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_rescale_within_a_cta(gpu_lib, w):
+    """512 tiles of one kv head over at most 148 CTAs (several tiles each); key scale cycles
+    1, 2, 4, 8 per tile so the running reference jumps inside a CTA's range."""
+    ks = lambda T: 2.0 ** ((torch.arange(T) // 128) % 4).float()
+    vs = lambda T: torch.exp(torch.sin(torch.arange(T).float() / 300.0) * 4.0)
+    out, want = _case(1, 4, 1, 65536, [65536], w, seed=17 + w, kscale=ks, vscale=vs)
+    assert rel_l2(out, want) <= 1e-3
+
+
 @pytest.mark.parametrize("w", [2, 3])
 def test_llama8b_full_size_gpu_records(gpu_lib, w):
     """32 / 8 heads, ctx 32768, bf16 K/V: GPU quantize (keys by row, values in blocks), tensor-core decode."""
