@@ -1,5 +1,5 @@
-// Decode attention over the compressed cache on the 5th-generation tensor
-// cores (tcgen05), for d = m = 128 and up to 8 query heads per kv head.
+// Decode attention over the compressed cache on the tensor cores, for
+// d = m = 128 and up to 8 query heads per kv head.
 //
 // What is computed is the same as the general kernel in tq_decode.cu
 // ("TurboQuant 与 AI 效率革命" §三, the asymmetric estimator applied to the
@@ -10,36 +10,41 @@
 // registers; no dequantized key or value is ever written to memory
 // ("TurboQuant压缩效果": decode in registers while reading).
 //
-// Bits as exact tensor-core operands.  A symmetric Lloyd-Max codebook is a
-// sum of ±1 bit-planes, c[idx] = Σ_P coef_P·s_P with s = 2·bit − 1 (Walsh
-// expansion; w = 1: one plane, w = 2: two, w = 3: three plus their product).
-// The QJL signs are one more ±1 plane.  A plane word is expanded with one
-// and-or per output register: bit i of every byte (e4m3 operand) or bit p of
-// every half-word (f16 operand) is placed over a constant, giving one of two
-// exactly representable values C or C' per element.  The affine map back to
-// ±1 (s = 2(F − (C + C')/2)/(C' − C)) is folded into the other operand and a
-// per-column correction.
+// Bits as exact operands.  A symmetric Lloyd-Max codebook is a sum of ±1
+// bit-planes, c[idx] = Σ_P coef_P·s_P with s = 2·bit − 1 (Walsh expansion;
+// w = 1: one plane, w = 2: two, w = 3: three plus their product).  The QJL
+// signs are one more ±1 plane.  One and-or turns a 32-bit plane word into
+// an e4m3 operand register: it keeps bit i of every byte (layer i) over a
+// constant byte C_i, giving per element one of two exact values C_i, C'_i.
+// The affine map back to ±1, s = 2(F − (C + C')/2)/(C' − C), is folded into
+// the other operand (weights 2x/(C' − C)) and an offset Σ w·(C + C')/2.
 //
-//   keys:   A = expanded key planes (e4m3) in TMEM, lane = token;
-//           B = query weights 2·coef·q̃_j/δ split into four e4m3 pieces
-//           (each carries the next 4 bits), kind::f8f6f4.
-//   values: A = expanded value planes (f16) in TMEM, lane = coordinate,
-//           which needs the 32-row block layout (one coordinate of 32 tokens
-//           per word); B = attention weights p·‖v‖ and p·‖r_v‖ (f16),
-//           kind::f16, accumulated over the whole context in TMEM.
-// Softmax is online with a lazy reference: the running reference M moves
-// only when a tile exceeds it by more than 2^8, and then the value
-// accumulators in TMEM are rescaled once.  M tracks log2(p·‖v‖) so that the
-// f16 weights stay in range for any value norm.
+//   scores: mma.sync m16n8k32 e4m3, rows = 16 tokens, K = 32 coordinates
+//           of one plane word, B = the query weights in three e4m3 pieces
+//           (each the next 4 bits; one power-of-two scale per head and
+//           part), held in registers for the whole (batch, kv head) unit.
+//   values: mma.sync m16n8k32 e4m3, rows = 16 coordinates of one plane,
+//           K = 32 tokens (one 32-row block word of TQ_LAYOUT_BLOCK32),
+//           B = attention weights p·‖v‖ / p·‖r_v‖ in three e4m3 pieces;
+//           fp32 accumulators stay in registers over the whole context,
+//           and each tile's operand offset is subtracted after the tile.
+// Warp-level mma.sync is used instead of tcgen05.mma: decode has one query
+// per head, so every MMA here is 8 columns wide, and a tcgen05.mma costs its
+// issuing thread ~110-160 cycles whatever its width, while register-operand
+// mma.sync lets every warp drive the tensor pipe on its own.
+//
+// Softmax is online with a lazy reference: the running reference M (of
+// log2(p·‖v‖), clamped at ‖v‖ ≥ 2^-32) moves only when a tile exceeds it
+// by more than 2^6; the value warps then rescale their accumulators.
 //
 // Work split: a persistent grid of one CTA per SM takes contiguous ranges of
 // 128-token tiles over all (batch, kv head) units; a unit cut between CTAs
 // leaves one partial per CTA, merged by the combine kernel of tq_decode.cu.
-//
-// Warp roles (320 threads): 0-3 keys (thread = token), 4-7 values (thread =
-// coordinate), 8 MMA issue + TMEM owner, 9 bulk-copy loader.  Every wait is
-// bounded; on timeout the kernel sets a fault bit (tq_fault_flags) and
-// unwinds.
+// Warp roles (288 threads, so that 3 warps per scheduler may use 168
+// registers): 0-3 keys (32 tokens each: scores, softmax, weights), 4-7 values
+// (32 coordinates of every plane each, as two 16-row MMA tiles), 8 bulk-copy
+// loader.  Every wait is bounded; on timeout the kernel sets a fault bit
+// (tq_fault_flags) and unwinds.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -55,25 +60,56 @@ using namespace tq::sm100;
 constexpr int kTile = 128;
 constexpr int kD = 128;
 constexpr int kStages = 4;
-constexpr int kThreads = 352, kMmaWarp = 8, kLoadWarp = 9, kVMmaWarp = 10;
-constexpr float kTau = 6.0f;                  // lazy-rescale threshold (log2 units)
+constexpr int kKW = 4, kVW = 4;                        // key warps, value warps (32 coordinates each)
+constexpr int kLoadWarp = kKW + kVW;
+constexpr int kThreads = 32 * (kKW + kVW + 1);
+constexpr float kTau = 6.0f;                           // lazy-rescale threshold (log2 units)
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kVScale = 0.125f;                      // value weights carry 2/δ·2^-3 (below 2^7)
 constexpr unsigned kFaultDecode = 2u;
-constexpr uint32_t kTmemCols = 512;
 
-// e4m3 key operand, layer i = bit i of each byte: value C (bit clear) or C' (bit set)
-__constant__ uint32_t c_k_base[8] = {0x38383838u, 0x38383838u, 0x38383838u, 0x30303030u,
-                                     0x28282828u, 0x18181818u, 0x00000000u, 0x38383838u};
-__constant__ float c_k_delta[8] = {0.125f, 0.25f, 0.5f, 0.5f, 0.75f, 0.9375f, 2.0f, -2.0f};  // C' - C
-__constant__ float c_k_mean[8] = {1.0625f, 1.125f, 1.25f, 0.75f, 0.625f, 0.53125f, 1.0f, 0.0f};  // (C + C')/2
-// f16 value operand, bit position p in 10..15 of each half-word
-__constant__ uint32_t c_v_base[6] = {0x38003800u, 0x34003400u, 0x2C002C00u, 0x1C001C00u, 0x00000000u, 0x3C003C00u};
-__constant__ float c_v_delta[6] = {0.5f, 0.75f, 0.9375f, 0.99609375f, 2.0f, -2.0f};
-__constant__ float c_v_mean[6] = {0.75f, 0.625f, 0.53125f, 0.501953125f, 1.0f, 0.0f};
+// e4m3 operand, layer i = bit i of each byte: value C_i (bit clear) or C'_i (bit set)
+__constant__ uint32_t c_base[8] = {0x38383838u, 0x38383838u, 0x38383838u, 0x30303030u,
+                                   0x28282828u, 0x18181818u, 0x00000000u, 0x38383838u};
+__constant__ float c_delta[8] = {0.125f, 0.25f, 0.5f, 0.5f, 0.75f, 0.9375f, 2.0f, -2.0f};     // C' - C
+__constant__ float c_mean[8] = {1.0625f, 1.125f, 1.25f, 0.75f, 0.625f, 0.53125f, 1.0f, 0.0f};  // (C + C')/2
 
-// Token pair i (tokens 2i, 2i+1 of a 32-row block sit at bits i, i+16) is
-// shifted left so that it lands on position vpos(i) in 10..15.
-__host__ __device__ constexpr int vpos(int i) { return i >= 10 ? i : (i >= 4 ? i + 6 : i + 12); }
+// A-operand register of layer tig (lo) or 4 + tig (hi) of plane word w: one and-or.
+struct Layers {
+  uint32_t mlo, mhi, blo, bhi;
+  __device__ __forceinline__ explicit Layers(int tig)
+      : mlo(0x01010101u << tig), mhi(0x10101010u << tig), blo(c_base[tig]), bhi(c_base[4 + tig]) {}
+  __device__ __forceinline__ uint32_t lo(uint32_t w) const { return (w & mlo) | blo; }
+  __device__ __forceinline__ uint32_t hi(uint32_t w) const { return (w & mhi) | bhi; }
+};
+
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float e4m3_value(uint8_t b) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw(b, __NV_E4M3)));
+}
+
+// Three e4m3 pieces of x (each the next 4 bits): x ≈ v0 + v1/16 + v2/256.
+// Writes the bytes and returns the represented value.
+__device__ __forceinline__ float pieces3(float x, uint8_t (&p)[3]) {
+  float rep = 0.f, sc = 1.f;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const __nv_fp8_storage_t b = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+    const float v = e4m3_value(b);
+    p[k] = b;
+    rep = fmaf(v, sc, rep);
+    x = (x - v) * 16.f;
+    sc *= 0.0625f;
+  }
+  return rep;
+}
 
 struct TcArgs {
   const uint32_t *kidx, *ksgn, *vidx, *vsgn;
@@ -97,52 +133,54 @@ __host__ __device__ inline int64_t owner(int64_t f, int64_t total, int64_t ctas)
   return ((f + 1) * ctas - 1) / total;
 }
 
-// Per-instantiation sizes.  TMEM columns: key ring (KR slots of one plane,
-// 32 columns = 128 e4m3), value ring (VR slots of half a plane, 32 columns =
-// 64 tokens of f16), score accumulators (2 buffers x MSE|QJL x NH), value
-// accumulators (NP x 16), one constant -1 operand column group (8).
 template <int W, int GP>
 struct Shape {
-  static constexpr int NPM = W == 3 ? 4 : W;  // ±1 planes of the codebook
-  static constexpr int NP = NPM + 1;          // plus the QJL sign plane
-  static constexpr int NH = 4 * GP;           // 4 pieces x GP heads
-  static constexpr int kRing = (512 - 4 * NH - 16 * NP - 8) / 32;  // key + value slots that fit
-  static constexpr int KR = (kRing + 1) / 2 < 2 * NP ? (kRing + 1) / 2 : 2 * NP;
-  static constexpr int VR = kRing - KR < 4 * NP ? kRing - KR : 4 * NP;
-  static constexpr uint32_t kColK = 0, kColV = 32 * KR, kColS = kColV + 32 * VR, kColVD = kColS + 4 * NH,
-                            kColOne = kColVD + 16 * NP;
-  static_assert(kColOne + 8 <= kTmemCols, "TMEM plan exceeds 512 columns");
-  static_assert(KR >= NP && VR >= 2, "rings too small for one tile");
-  static_assert(VR <= 4 * NP, "value ring deeper than two tiles breaks the end-of-segment wait");
+  static constexpr int NPM = W == 3 ? 4 : W;   // ±1 planes of the codebook
+  static constexpr int NP = NPM + 1;           // plus the QJL sign plane
+  static constexpr int NKS = 4 * NP;           // score K-steps: 4 words of 32 coordinates per plane
+  static constexpr int NC = 3 * GP;            // columns of one part: 3 pieces x GP heads
+  static constexpr int NCP = NC <= 16 ? 16 : 32;  // NC rounded up to a power of two
+  static constexpr int NT = (NC + 7) / 8;      // n-tiles of 8 columns
+  static constexpr bool kBRegs = NKS * NT * 2 <= 80;  // query-weight fragments held in registers
   static constexpr int kIdxBytes = kTile * 4 * W * 4;
   static constexpr int kStage = 2 * kIdxBytes + 2 * 2048 + 4 * 512;
   static constexpr int kOffKIdx = 0, kOffKSgn = kIdxBytes, kOffKNorm = kOffKSgn + 2048, kOffKRn = kOffKNorm + 512;
   static constexpr int kOffVIdx = kOffKRn + 512, kOffVSgn = kOffVIdx + kIdxBytes, kOffVNorm = kOffVSgn + 2048,
                        kOffVRn = kOffVNorm + 512;
+  // shared memory plan
+  static constexpr int kBKBytes = NKS * NT * 256;           // [ks][nt][n 8][k 32] query weight bytes
+  static constexpr int SP = 2 * NT * 8 + 1;                // score row pitch in floats (odd: no bank conflicts)
+  static constexpr int kSBytes = (kTile * SP * 4 + 15) / 16 * 16;  // raw score pieces [token][part][col]
+  static constexpr int kBVBytes = 2 * 4 * NT * 256;         // [part][block][nt][n][k] weight bytes
+  static constexpr int kScratch = 32 * NT * 8 * 4;          // per value warp, one plane
+  static constexpr int kOffRing = 0;
+  static constexpr int kOffBK = kOffRing + kStages * kStage;
+  static constexpr int kOffS = kOffBK + kBKBytes;
+  static constexpr int kOffBV = kOffS + kSBytes;
+  static constexpr int kOffScr = kOffBV + 2 * kBVBytes;
+  static constexpr int kOffMisc = kOffScr + kVW * kScratch;
 };
-
-constexpr int kOffBK = 0;                  // NP planes x 4 KB (NH <= 32 rows of 128 bytes)
-constexpr int kOffBV = 5 * 4096;           // 2 buffers x 3 SW128 atoms of 2 KB (tokens 0-63, 64-127, offsets)
-constexpr int kBVBytes = 3 * 2048;
-constexpr int kOffRing = kOffBV + 2 * kBVBytes;
-constexpr int kMiscBytes = 4096;
-constexpr int kMaxRing = 16;
 
 struct Misc {
   uint64_t ld_full[kStages], ld_empty[kStages];
-  uint64_t ka_full[kMaxRing], ka_empty[kMaxRing], va_full[kMaxRing], va_empty[kMaxRing];
-  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
-  uint64_t bk_full, vd_free, kgroup, st_full[2], st_empty[2];
-  uint32_t tmem_base;
+  uint64_t p_full[2], p_empty[2], kgroup, st_full[2], st_empty[2];
   int abort;
-  float red[2][4][8];       // per-tile warp maxima [parity][warp][head]
-  float amax[2][8];         // per-unit weight maxima (as non-negative float bits)
-  float O[2][8];            // per-unit offset per (part, head)
+  float red[2][kKW][8];       // per-tile warp maxima [parity][warp][head]
+  float amax[2][8];           // per-unit weight maxima (as non-negative float bits)
+  float O[2][8];              // per-unit score offsets per (part, head)
   float coef[4];
-  float stat_m[2][8];       // per segment parity: reference M per head
-  float stat_l[2][4][8];    // per segment parity, per key warp: Σ p
+  float fac[2][8];            // per weight buffer: accumulator rescale factor per head
+  float off[2][kKW][2][24];   // per weight buffer, per key warp: value operand offsets per (part, col)
+  float stat_m[2][8];         // per segment parity: reference M per head
+  float stat_l[2][kKW][8];    // per segment parity, per key warp: Σ p
 };
+constexpr int kMiscBytes = 4096;
 static_assert(sizeof(Misc) <= kMiscBytes, "barriers and per-head state must fit their region");
+
+template <int W>
+constexpr int smem_bytes() {
+  return 1024 + Shape<W, 8>::kOffMisc + kMiscBytes;
+}
 
 // Segment of this CTA's tile range that falls in one unit.
 struct Seg {
@@ -168,7 +206,7 @@ __device__ __forceinline__ Seg segment_at(const TcArgs& a, int64_t f, int64_t f1
   return s;
 }
 
-__device__ __forceinline__ uint32_t kgroup_sync(Misc* ms, uint32_t* count, unsigned* fault) {
+__device__ __forceinline__ bool kgroup_sync(Misc* ms, uint32_t* count, unsigned* fault) {
   __syncwarp();
   const uint32_t bar = smem_u32(&ms->kgroup);
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
@@ -177,18 +215,8 @@ __device__ __forceinline__ uint32_t kgroup_sync(Misc* ms, uint32_t* count, unsig
   return ok;
 }
 
-// SW128 K-major offset of element (row n, byte e) in a tile of 128-byte rows.
-__device__ __forceinline__ uint32_t sw128(int n, int e) {
-  return (n >> 3) * 1024 + (n & 7) * 128 + ((((e >> 4) ^ (n & 7))) << 4) + (e & 15);
-}
-
-// Offset of f16 element (row n, token t) in a 16 x 128 attention-weight tile:
-// two SW128 atoms of 64 tokens (128 bytes per row), 2 KB apart.
-__device__ __forceinline__ uint32_t bv_off(int n, int t) { return (t >> 6) * 2048 + sw128(n, (t & 63) * 2); }
-
 // Sum (or max) of N values over the 32 lanes of a warp, N a power of two <= 32,
-// by halving: afterwards lane L holds the result for index bits (L >> (5 -
-// log2 N)) ... of v (see lane_index), written to v[0].
+// by halving; lane L ends with the result for index lane_index<N>(L).
 template <int N, bool MAX>
 __device__ __forceinline__ float warp_reduce_many(float (&v)[N], int lane) {
 #pragma unroll
@@ -210,7 +238,6 @@ __device__ __forceinline__ float warp_reduce_many(float (&v)[N], int lane) {
   }
   return x;
 }
-// Index of the value that warp_reduce_many<N> leaves in lane L.
 template <int N>
 __device__ __forceinline__ int lane_index(int lane) {
   int idx = 0;
@@ -223,54 +250,35 @@ __device__ __forceinline__ int lane_index(int lane) {
 template <int W, int GP>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) {
   using Sh = Shape<W, GP>;
-  constexpr int NPM = Sh::NPM, NP = Sh::NP, NH = Sh::NH, KR = Sh::KR, VR = Sh::VR;
+  constexpr int NPM = Sh::NPM, NP = Sh::NP, NKS = Sh::NKS, NC = Sh::NC, NCP = Sh::NCP, NT = Sh::NT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  Misc* ms = reinterpret_cast<Misc*>(smem + kOffRing + kStages * Sh::kStage);
+  Misc* ms = reinterpret_cast<Misc*>(smem + Sh::kOffMisc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tig = lane & 3;  // mma fragment coordinates
+  const Layers ly(tig);
   const int64_t C = gridDim.x;
   const int64_t f0 = (int64_t)blockIdx.x * a.total / C, f1 = ((int64_t)blockIdx.x + 1) * a.total / C;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ms->ld_full[s]), 1);
-      mbar_init(smem_u32(&ms->ld_empty[s]), 8);
-    }
-    for (int s = 0; s < KR; ++s) {
-      mbar_init(smem_u32(&ms->ka_full[s]), 4);
-      mbar_init(smem_u32(&ms->ka_empty[s]), 1);
-    }
-    for (int s = 0; s < VR; ++s) {
-      mbar_init(smem_u32(&ms->va_full[s]), 4);
-      mbar_init(smem_u32(&ms->va_empty[s]), 1);
+      mbar_init(smem_u32(&ms->ld_empty[s]), kKW + kVW);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&ms->s_full[s]), 1);
-      mbar_init(smem_u32(&ms->s_empty[s]), 4);
-      mbar_init(smem_u32(&ms->p_full[s]), 4);
-      mbar_init(smem_u32(&ms->p_empty[s]), 1);
-      mbar_init(smem_u32(&ms->st_full[s]), 4);
-      mbar_init(smem_u32(&ms->st_empty[s]), 4);
+      mbar_init(smem_u32(&ms->p_full[s]), kKW);
+      mbar_init(smem_u32(&ms->p_empty[s]), kVW);
+      mbar_init(smem_u32(&ms->st_full[s]), kKW);
+      mbar_init(smem_u32(&ms->st_empty[s]), kVW);
     }
-    mbar_init(smem_u32(&ms->bk_full), 4);
-    mbar_init(smem_u32(&ms->vd_free), 4);
-    mbar_init(smem_u32(&ms->kgroup), 4);
+    mbar_init(smem_u32(&ms->kgroup), kKW);
     ms->abort = 0;
     fence_mbar_init();
   }
-  // attention-weight operands start at zero (rows of absent heads stay zero)
-  for (int e = threadIdx.x; e < 2 * kBVBytes / 16; e += kThreads)
-    reinterpret_cast<uint4*>(smem + kOffBV)[e] = make_uint4(0u, 0u, 0u, 0u);
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&ms->tmem_base), kTmemCols);
-    tmem_relinquish();
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
+  // weight operands start at zero (columns of absent heads stay zero)
+  for (int e = threadIdx.x; e < 2 * Sh::kBVBytes / 16; e += kThreads)
+    reinterpret_cast<uint4*>(smem + Sh::kOffBV)[e] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ms->tmem_base;
   volatile int* abort_flag = &ms->abort;
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait_abortable(smem_u32(bar), parity, a.fault, kFaultDecode, abort_flag);
@@ -279,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ loader
     if (lane == 0) {
+      const uint32_t sbase = smem_u32(smem);
       int64_t gi = 0;
       bool ok = true;
       for (int64_t f = f0; ok && f < f1;) {
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           if (gi >= kStages && !(ok = wait(&ms->ld_empty[s], (uint32_t)((gi / kStages - 1) & 1)))) break;
           const int64_t row0 = sg.u * a.ctx_stride + (sg.t0 + k) * kTile;
           const uint32_t bar = smem_u32(&ms->ld_full[s]);
-          const uint32_t dst = sbase + kOffRing + s * Sh::kStage;
+          const uint32_t dst = sbase + Sh::kOffRing + s * Sh::kStage;
           mbar_arrive_expect_tx(bar, Sh::kStage);
           bulk_load(dst + Sh::kOffKIdx, a.kidx + row0 * (4 * W), Sh::kIdxBytes, bar);
           bulk_load(dst + Sh::kOffKSgn, a.ksgn + row0 * 4, 2048, bar);
@@ -306,144 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       for (int64_t g = max((int64_t)0, gi - kStages); g < gi; ++g)
         mbar_wait(smem_u32(&ms->ld_full[g % kStages]), (uint32_t)((g / kStages) & 1), a.fault, kFaultDecode);
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ key MMAs (scores)
-    if (lane == 0) {
-      constexpr uint32_t idk = idesc_e4m3_f32(128, NH);
-      int64_t gi = 0, kc = 0;
-      int nseg = 0;
-      bool ok = true;
-      for (int64_t f = f0; ok && f < f1;) {
-        int64_t next;
-        const Seg sg = segment_at(a, f, f1, &next);
-        f = next;
-        if (sg.n == 0) continue;
-        if (!(ok = wait(&ms->bk_full, (uint32_t)(nseg & 1)))) break;
-        tc_fence_after();
-        for (int k = 0; ok && k < sg.n; ++k) {
-          const int64_t g = gi + k;
-          const int sb = (int)(g & 1);
-          if (g >= 2 && !(ok = wait(&ms->s_empty[sb], (uint32_t)(((g >> 1) - 1) & 1)))) break;
-#pragma unroll 1
-          for (int P = 0; P < NP; ++P, ++kc) {
-            const int slot = (int)(kc % KR);
-            if (!(ok = wait(&ms->ka_full[slot], (uint32_t)((kc / KR) & 1)))) break;
-            tc_fence_after();
-            const uint32_t d = tmem + Sh::kColS + sb * 2 * NH + (P < NPM ? 0 : NH);
-            const uint64_t bd = desc_sw128(sbase + kOffBK + P * 4096);
-#pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t acc = (P < NPM) ? ((P > 0 || kk > 0) ? 1u : 0u) : (kk > 0 ? 1u : 0u);
-              mma_ts_f8(d, tmem + Sh::kColK + slot * 32 + kk * 8, bd + ((kk * 32) >> 4), idk, acc);
-            }
-            mma_commit(smem_u32(&ms->ka_empty[slot]));
-          }
-          if (!ok) break;
-          mma_commit(smem_u32(&ms->s_full[sb]));
-        }
-        gi += sg.n;
-        ++nseg;
-      }
-    }
-  } else if (warp == kVMmaWarp) {
-    // ------------------------------------------------------------ value MMAs (weights x values)
-    if (lane == 0) {
-      constexpr uint32_t idv = idesc_f16_f32(128, 16);
-      int64_t gi = 0, vc = 0;
-      int nseg = 0;
-      bool ok = true;
-      for (int64_t f = f0; ok && f < f1;) {
-        int64_t next;
-        const Seg sg = segment_at(a, f, f1, &next);
-        f = next;
-        if (sg.n == 0) continue;
-        for (int k = 0; ok && k < sg.n; ++k) {
-          const int64_t g = gi + k;
-          const int sb = (int)(g & 1);
-          const bool first = k == 0;
-          if (!(ok = wait(&ms->p_full[sb], (uint32_t)((g >> 1) & 1)))) break;
-          if (first && nseg >= 1 && !(ok = wait(&ms->vd_free, (uint32_t)((nseg - 1) & 1)))) break;
-          tc_fence_after();
-          const uint32_t bv = sbase + kOffBV + sb * kBVBytes;
-#pragma unroll 1
-          for (int P = 0; ok && P < NP; ++P) {
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half, ++vc) {
-              const int slot = (int)(vc % VR);
-              if (!(ok = wait(&ms->va_full[slot], (uint32_t)((vc / VR) & 1)))) break;
-              tc_fence_after();
-              const uint32_t d = tmem + Sh::kColVD + 16 * P;
-#pragma unroll 1
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = desc_sw128(bv + half * 2048) + ((kk * 32) >> 4);
-                mma_ts(d, tmem + Sh::kColV + slot * 32 + kk * 8, bd, idv, (first && half == 0 && kk == 0) ? 0u : 1u);
-              }
-              // minus this tile's operand offsets Σ w·(C + C')/2 (per key warp, f16 hi + lo)
-              if (half == 1) mma_ts(d, tmem + Sh::kColOne, desc_sw128(bv + 2 * 2048), idv, 1u);
-              mma_commit(smem_u32(&ms->va_empty[slot]));
-            }
-          }
-          if (!ok) break;
-          mma_commit(smem_u32(&ms->p_empty[sb]));
-        }
-        gi += sg.n;
-        ++nseg;
-      }
-    }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ keys: thread = token
-    const int r = threadIdx.x;  // token of the tile, TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t kgc = 0;           // kgroup phases used
-    int64_t gi = 0, kc = 0;
+  } else if (warp < kKW) {
+    // ------------------------------------------------------------ keys
+    const int r = threadIdx.x;  // token of the tile in the softmax phase; coordinate in the weight set-up
+    uint32_t kgc = 0;
+    int64_t gi = 0;
     int segc = 0;
     bool ok = true;
-    float M[GP], lsum[GP], E_m[GP], E_q[GP], O_m[GP], O_q[GP];
-    const int vp = vpos((r & 31) >> 1) - 10;
-    const float two_over_delta = 2.0f / c_v_delta[vp], vmean = c_v_mean[vp];
-    // expand tile g (stage g % kStages) into the NP key planes of the TMEM ring
-    auto expand = [&](int64_t g) {
-      const int s = (int)(g % kStages);
-      if (!wait(&ms->ld_full[s], (uint32_t)((g / kStages) & 1))) return false;
-      const uint8_t* st = smem + kOffRing + s * Sh::kStage;
-      uint32_t iw[4 * W], sw[4], tw[4];
-#pragma unroll
-      for (int p = 0; p < W; ++p) {
-        const uint4 v = reinterpret_cast<const uint4*>(st + Sh::kOffKIdx + r * 16 * W)[p];
-        iw[4 * p] = v.x; iw[4 * p + 1] = v.y; iw[4 * p + 2] = v.z; iw[4 * p + 3] = v.w;
-      }
-      {
-        const uint4 v = reinterpret_cast<const uint4*>(st + Sh::kOffKSgn)[r];
-        sw[0] = v.x; sw[1] = v.y; sw[2] = v.z; sw[3] = v.w;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)  // w = 3: the product plane s0·s1·s2 has bit b0 ^ b1 ^ b2
-        tw[k] = W == 3 ? iw[k] ^ iw[(4 + k) % (4 * W)] ^ iw[(8 + k) % (4 * W)] : 0u;
-      // all planes of the tile are stored, then one wait for the stores, then
-      // every slot is released to the MMA warp
-#pragma unroll
-      for (int P = 0; P < NP; ++P) {
-        uint32_t pw[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pw[k] = P < W ? iw[(4 * P + k) % (4 * W)] : (P < NPM ? tw[k] : sw[k]);
-        const int64_t c = kc + P;
-        const int slot = (int)(c % KR);
-        if (c >= KR && !wait(&ms->ka_empty[slot], (uint32_t)((c / KR - 1) & 1))) return false;
-        uint32_t vals[32];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) vals[8 * k + i] = (pw[k] & (0x01010101u << i)) | c_k_base[i];
-        tmem_st32(tmem + lane_base + Sh::kColK + slot * 32, vals);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0)
-        for (int P = 0; P < NP; ++P) mbar_arrive(smem_u32(&ms->ka_full[(kc + P) % KR]));
-      kc += NP;
-      return true;
-    };
+    float M[GP], lsum[GP], E[2][GP], O[2][GP];
+    uint32_t bf[Sh::kBRegs ? NKS : 1][NT][2];
+    // bit position of this token in a 32-row block word: its e4m3 layer and K-element
+    const int xb = tq::block32_bit(r & 31), vlay = xb & 7, vk = 4 * (xb & 7) + (xb >> 3);
+    const float vw2 = 2.0f * kVScale / c_delta[vlay], vmean = c_mean[vlay];
+    float* S = reinterpret_cast<float*>(smem + Sh::kOffS);
+    uint8_t* BK = smem + Sh::kOffBK;
     for (int64_t f = f0; ok && f < f1;) {
       int64_t next;
       const Seg sg = segment_at(a, f, f1, &next);
@@ -453,22 +338,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
       for (int g = 0; g < GP; ++g) M[g] = -INFINITY, lsum[g] = 0.f;
       if (sg.n > 0) {
-        // ---- query weights for this unit: B_K planes, piece scales E, offsets O
+        // ---- query weights of this unit: piece scales E, pieces in BK, offsets O
+        for (int e = r; e < Sh::kBKBytes / 16; e += 32 * kKW) reinterpret_cast<uint4*>(BK)[e] = make_uint4(0, 0, 0, 0);
         if (r < 16) {
           ms->amax[r >> 3][r & 7] = 0.f;
           ms->O[r >> 3][r & 7] = 0.f;
         }
         if (r < NPM) ms->coef[r] = __ldg(a.walsh + (r < W ? (1 << r) : 7));
         if (!(ok = kgroup_sync(ms, &kgc, a.fault))) break;
-        const int j = r;  // coordinate handled by this thread
-        const float dl = c_k_delta[j & 7], mean = c_k_mean[j & 7];
-        float qv[GP], sv[GP];
+        const int j = r;  // coordinate: word j / 32, bit x = j % 32 -> layer x % 8, byte x / 8
+        const int jl = j & 7, jk = 4 * jl + ((j & 31) >> 3), jw = j >> 5;
+        const float dl = c_delta[jl], mean = c_mean[jl];
+        float qv[GP], sv[GP], cf[NPM];
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
           qv[g] = g < a.G ? __ldg(a.qt + (size_t)(head0 + g) * kD + j) : 0.f;
           sv[g] = g < a.G ? __ldg(a.st + (size_t)(head0 + g) * kD + j) : 0.f;
         }
-        float cf[NPM];
 #pragma unroll
         for (int P = 0; P < NPM; ++P) cf[P] = ms->coef[P];
 #pragma unroll
@@ -489,67 +375,106 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         }
         if (!(ok = kgroup_sync(ms, &kgc, a.fault))) break;
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          int e;
-          frexpf(ms->amax[0][g], &e);
-          E_m[g] = ms->amax[0][g] > 0.f ? ldexpf(1.f, e - 8) : 1.f;
-          frexpf(ms->amax[1][g], &e);
-          E_q[g] = ms->amax[1][g] > 0.f ? ldexpf(1.f, e - 8) : 1.f;
-        }
-        // element position of coordinate j in a 128-element key plane row
-        const int eidx = 4 * (8 * (j >> 5) + (j & 7)) + ((j & 31) >> 3);
-#pragma unroll
-        for (int P = 0; P < NP; ++P) {
+        for (int p = 0; p < 2; ++p)
 #pragma unroll
           for (int g = 0; g < GP; ++g) {
-            const bool mse = P < NPM;
-            const float E = mse ? E_m[g] : E_q[g];
-            float x = (mse ? 2.f * cf[P < NPM ? P : 0] * qv[g] : 2.f * sv[g]) / dl / E;
-            float rep = 0.f, sc = 1.f;
+            int e;
+            frexpf(ms->amax[p][g], &e);
+            E[p][g] = ms->amax[p][g] > 0.f ? ldexpf(1.f, e - 8) : 1.f;
+          }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const __nv_fp8_storage_t p8 = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-              const float pv = __half2float(__half(__nv_cvt_fp8_to_halfraw(p8, __NV_E4M3)));
-              smem[kOffBK + P * 4096 + sw128(k * GP + g, eidx)] = p8;
-              rep += pv * sc;
-              x = (x - pv) * 16.f;
-              sc *= 0.0625f;
+        for (int P = 0; P < NP; ++P) {
+          const int part = P < NPM ? 0 : 1;
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            const float w = (part == 0 ? 2.f * cf[P < NPM ? P : 0] * qv[g] : 2.f * sv[g]) / dl;
+            uint8_t pc[3];
+            const float rep = pieces3(w / E[part][g], pc);
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+              const int c = k * GP + g;
+              BK[(((P * 4 + jw) * NT + (c >> 3)) * 8 + (c & 7)) * 32 + jk] = pc[k];
             }
-            float o = rep * E * mean;
+            float o = rep * E[part][g] * mean;
 #pragma unroll
             for (int s = 16; s > 0; s >>= 1) o += __shfl_xor_sync(0xffffffffu, o, s);
-            if (lane == 0) atomicAdd(&ms->O[mse ? 0 : 1][g], o);
+            if (lane == 0) atomicAdd(&ms->O[part][g], o);
           }
         }
-        fence_proxy_async_smem();
         if (!(ok = kgroup_sync(ms, &kgc, a.fault))) break;
 #pragma unroll
-        for (int g = 0; g < GP; ++g) O_m[g] = ms->O[0][g], O_q[g] = ms->O[1][g];
-        if (lane == 0) mbar_arrive(smem_u32(&ms->bk_full));
+        for (int g = 0; g < GP; ++g) O[0][g] = ms->O[0][g], O[1][g] = ms->O[1][g];
+        if constexpr (Sh::kBRegs) {
+#pragma unroll
+          for (int ks = 0; ks < NKS; ++ks)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint32_t* row = reinterpret_cast<const uint32_t*>(BK + ((ks * NT + nt) * 8 + gq) * 32);
+              bf[ks][nt][0] = row[tig];
+              bf[ks][nt][1] = row[4 + tig];
+            }
+        }
 
-        // ---- tiles: expand the next tile's keys, then score / weigh this one
-        if (!(ok = expand(gi))) break;
         for (int k = 0; ok && k < sg.n; ++k) {
           const int64_t g = gi + k;
-          if (k + 1 < sg.n && !(ok = expand(g + 1))) break;
-          const int sb = (int)(g & 1), s = (int)(g % kStages);
-          if (!(ok = wait(&ms->s_full[sb], (uint32_t)((g >> 1) & 1)))) break;
-          tc_fence_after();
-          float dv[2 * NH];
-          {
-            uint32_t v[32];
+          const int s = (int)(g % kStages), buf = (int)(g & 1);
+          if (!(ok = wait(&ms->ld_full[s], (uint32_t)((g / kStages) & 1)))) break;
+          const uint8_t* stg = smem + Sh::kOffRing + s * Sh::kStage;
+          const uint32_t* kiw = reinterpret_cast<const uint32_t*>(stg + Sh::kOffKIdx);
+          const uint32_t* ksw = reinterpret_cast<const uint32_t*>(stg + Sh::kOffKSgn);
+          // ---- scores: 2 groups of 16 tokens, rows gq and gq + 8 of each; pieces -> S[token][part][col]
+#pragma unroll 1
+          for (int gr = 0; gr < 2; ++gr) {
+            const int tA = 32 * warp + 16 * gr + gq, tB = tA + 8;
+            float acc[2][NT][4];
 #pragma unroll
-            for (int c = 0; c < 2 * NH / 32; ++c) {
-              tmem_ld32(tmem + lane_base + Sh::kColS + sb * 2 * NH + 32 * c, v);
-              tmem_ld_wait();
+            for (int p = 0; p < 2; ++p)
 #pragma unroll
-              for (int e = 0; e < 32; ++e) dv[32 * c + e] = __uint_as_float(v[e]);
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[p][nt][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < NKS; ++ks) {
+              const int P = ks >> 2, kw = ks & 3, part = P < NPM ? 0 : 1;
+              uint32_t wA, wB;
+              if (P < W) {
+                wA = kiw[tA * 4 * W + P * 4 + kw];
+                wB = kiw[tB * 4 * W + P * 4 + kw];
+              } else if (P < NPM) {  // w = 3 product plane: b0 ^ b1 ^ b2
+                wA = kiw[tA * 4 * W + kw] ^ kiw[tA * 4 * W + (4 + kw) % (4 * W)] ^ kiw[tA * 4 * W + (8 + kw) % (4 * W)];
+                wB = kiw[tB * 4 * W + kw] ^ kiw[tB * 4 * W + (4 + kw) % (4 * W)] ^ kiw[tB * 4 * W + (8 + kw) % (4 * W)];
+              } else {
+                wA = ksw[tA * 4 + kw];
+                wB = ksw[tB * 4 + kw];
+              }
+              const uint32_t a0 = ly.lo(wA), a1 = ly.lo(wB), a2 = ly.hi(wA), a3 = ly.hi(wB);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                uint32_t b0, b1;
+                if constexpr (Sh::kBRegs) {
+                  b0 = bf[ks][nt][0];
+                  b1 = bf[ks][nt][1];
+                } else {
+                  const uint32_t* row = reinterpret_cast<const uint32_t*>(BK + ((ks * NT + nt) * 8 + gq) * 32);
+                  b0 = row[tig];
+                  b1 = row[4 + tig];
+                }
+                mma_e4m3(acc[part][nt], a0, a1, a2, a3, b0, b1);
+              }
             }
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const int c = p * NT * 8 + 8 * nt + 2 * tig;
+                S[tA * Sh::SP + c] = acc[p][nt][0];
+                S[tA * Sh::SP + c + 1] = acc[p][nt][1];
+                S[tB * Sh::SP + c] = acc[p][nt][2];
+                S[tB * Sh::SP + c + 1] = acc[p][nt][3];
+              }
           }
-          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ms->s_empty[sb]));
-          const uint8_t* stg = smem + kOffRing + s * Sh::kStage;
+          const float* Sr = S + r * Sh::SP;
           const float kn = reinterpret_cast<const float*>(stg + Sh::kOffKNorm)[r];
           const float kr = reinterpret_cast<const float*>(stg + Sh::kOffKRn)[r];
           const float vn = reinterpret_cast<const float*>(stg + Sh::kOffVNorm)[r];
@@ -559,17 +484,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           float s2[GP], av[GP];
 #pragma unroll
           for (int hh = 0; hh < GP; ++hh) {
-            const float dm = ((dv[hh] + dv[GP + hh] * 0.0625f) + dv[2 * GP + hh] * 0.00390625f) +
-                             dv[3 * GP + hh] * 0.000244140625f;
-            const float dq = ((dv[NH + hh] + dv[NH + GP + hh] * 0.0625f) + dv[NH + 2 * GP + hh] * 0.00390625f) +
-                             dv[NH + 3 * GP + hh] * 0.000244140625f;
-            const float mse = fmaf(E_m[hh], dm, -O_m[hh]);
-            const float qjl = fmaf(E_q[hh], dq, -O_q[hh]);
+            const float dm = (Sr[hh] + Sr[GP + hh] * 0.0625f) + Sr[2 * GP + hh] * 0.00390625f;
+            const float dq = (Sr[NT * 8 + hh] + Sr[NT * 8 + GP + hh] * 0.0625f) + Sr[NT * 8 + 2 * GP + hh] * 0.00390625f;
+            const float mse = fmaf(E[0][hh], dm, -O[0][hh]);
+            const float qjl = fmaf(E[1][hh], dq, -O[1][hh]);
             const float sc = a.scale * fmaf(kn, mse, a.alpha * kr * qjl);
             s2[hh] = (valid && hh < a.G) ? sc * kLog2e : -INFINITY;
             av[hh] = s2[hh] + fmaxf(lvn, -32.f);
           }
-          // tile maximum of log2(p·‖v‖) per head, across the four key warps
+          // tile maximum of log2(p·‖v‖) per head across the key warps
           {
             float x[GP];
 #pragma unroll
@@ -579,80 +502,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           }
           if (!(ok = kgroup_sync(ms, &kgc, a.fault))) break;
           float fac[GP];
-          bool rescale = false;
 #pragma unroll
           for (int hh = 0; hh < GP; ++hh) {
-            const float tm = fmaxf(fmaxf(ms->red[g & 1][0][hh], ms->red[g & 1][1][hh]),
-                                   fmaxf(ms->red[g & 1][2][hh], ms->red[g & 1][3][hh]));
+            float tm = ms->red[g & 1][0][hh];
+#pragma unroll
+            for (int q = 1; q < kKW; ++q) tm = fmaxf(tm, ms->red[g & 1][q][hh]);
             float nm = M[hh];
             if (M[hh] == -INFINITY) nm = tm;
             else if (tm > M[hh] + kTau) nm = tm;
             fac[hh] = (M[hh] != -INFINITY && nm != M[hh]) ? exp2f(M[hh] - nm) : 1.f;
-            rescale |= fac[hh] != 1.f;
             M[hh] = nm;
+            lsum[hh] *= fac[hh];
           }
-          if (rescale) {
-            // value accumulators of the tiles so far: wait for their MMAs (tile g-1's
-            // weight buffer release; its phase is at most one behind, since tile g-3's
-            // release was awaited before tile g-1's weights were written), scale in place
-            if (!(ok = wait(&ms->p_empty[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1)))) break;
-            tc_fence_after();
+          // ---- attention weights of this tile -> value operands (three e4m3 pieces)
+          if (g >= 2 && !(ok = wait(&ms->p_empty[buf], (uint32_t)(((g >> 1) - 1) & 1)))) break;
+          uint8_t* bv = smem + Sh::kOffBV + buf * Sh::kBVBytes;
+          float offv[2][NCP];
 #pragma unroll
-            for (int P = 0; P < NP; ++P) {
-              uint32_t v[16];
-              tmem_ld16(tmem + lane_base + Sh::kColVD + 16 * P, v);
-              tmem_ld_wait();
+          for (int p = 0; p < 2; ++p)
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const int hh = c & 7;
-                if (hh < GP) v[c] = __float_as_uint(__uint_as_float(v[c]) * fac[hh]);
-              }
-              uint32_t v8a[8], v8b[8];
-#pragma unroll
-              for (int c = 0; c < 8; ++c) v8a[c] = v[c], v8b[c] = v[8 + c];
-              tmem_st8(tmem + lane_base + Sh::kColVD + 16 * P, v8a);
-              tmem_st8(tmem + lane_base + Sh::kColVD + 16 * P + 8, v8b);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-#pragma unroll
-            for (int hh = 0; hh < GP; ++hh) lsum[hh] *= fac[hh];
-          }
-          // attention weights of this tile -> f16 B operand of the value MMA
-          if (g >= 2 && !(ok = wait(&ms->p_empty[sb], (uint32_t)(((g >> 1) - 1) & 1)))) break;
-          uint8_t* bv = smem + kOffBV + sb * kBVBytes;
-          float off[2 * GP];
+            for (int c = 0; c < NCP; ++c) offv[p][c] = 0.f;
 #pragma unroll
           for (int hh = 0; hh < GP; ++hh) {
-            off[hh] = off[GP + hh] = 0.f;
-            if (hh >= a.G) continue;
-            const bool live = valid && M[hh] != -INFINITY;
+            const bool live = valid && hh < a.G && M[hh] != -INFINITY;
             const float p = live ? exp2f(s2[hh] - M[hh]) : 0.f;
             const float wm = live ? exp2f(s2[hh] + lvn - M[hh]) : 0.f;
-            const float wq = p * vr;
             lsum[hh] += p;
-            const __half hm = __float2half_rn(wm * two_over_delta);
-            const __half hq = __float2half_rn(wq * two_over_delta);
-            *reinterpret_cast<__half*>(bv + bv_off(hh, r)) = hm;
-            *reinterpret_cast<__half*>(bv + bv_off(8 + hh, r)) = hq;
-            off[hh] = __half2float(hm) * vmean;
-            off[GP + hh] = __half2float(hq) * vmean;
-          }
-          // this warp's operand offsets for every weight row, as f16 hi + lo at
-          // elements 2·warp, 2·warp + 1 of the offset row (A there is -1)
-          {
-            const float o = warp_reduce_many<2 * GP, false>(off, lane);
-            const int c = lane_index<2 * GP>(lane);
-            if ((lane & (16 / GP - 1)) == 0 && (c % GP) < a.G) {
-              const __half hi = __float2half_rn(o), lo = __float2half_rn(o - __half2float(hi));
-              const int n = c < GP ? c : 8 + (c - GP);
-              *reinterpret_cast<__half2*>(bv + 2 * 2048 + sw128(n, 4 * warp)) = __halves2half2(hi, lo);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              uint8_t pc[3];
+              pieces3((part == 0 ? wm : p * vr) * vw2, pc);
+#pragma unroll
+              for (int q = 0; q < 3; ++q) {
+                const int c = q * GP + hh;
+                bv[(((part * 4 + warp) * NT + (c >> 3)) * 8 + (c & 7)) * 32 + vk] = pc[q];
+                offv[part][c] = e4m3_value(pc[q]) * vmean;
+              }
             }
           }
-          fence_proxy_async_smem();
+          // this warp's operand offsets per (part, column)
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const float o = warp_reduce_many<NCP, false>(offv[part], lane);
+            const int c = lane_index<NCP>(lane);
+            if ((lane & (32 / NCP - 1)) == 0 && c < NC) ms->off[buf][warp][part][c] = o;
+          }
+          if (lane < GP) ms->fac[buf][lane] = fac[lane];
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_u32(&ms->p_full[sb]));
+            mbar_arrive(smem_u32(&ms->p_full[buf]));
             mbar_arrive(smem_u32(&ms->ld_empty[s]));
           }
         }
@@ -677,16 +575,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       ++segc;
     }
   } else {
-    // ------------------------------------------------------------ values: thread = coordinate
-    const int j = threadIdx.x - 128;
-    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    {
-      const uint32_t one[8] = {0xBC00BC00u, 0xBC00BC00u, 0xBC00BC00u, 0xBC00BC00u, 0u, 0u, 0u, 0u};
-      tmem_st8(tmem + lane_base + Sh::kColOne, one);
-      tmem_st_wait();
-      tc_fence_before();
-    }
-    int64_t gi = 0, vc = 0;
+    // ------------------------------------------------------------ values: 32 coordinates of every plane
+    const int vwarp = warp - kKW;
+    float* scr = reinterpret_cast<float*>(smem + Sh::kOffScr + vwarp * Sh::kScratch);
+    float vacc[NP][2][NT][4];  // [plane][row tile: coordinates 32v + 16mt + (gq, gq + 8)][n-tile][fragment]
+#pragma unroll
+    for (int P = 0; P < NP; ++P)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) vacc[P][mt][nt][e] = 0.f;
+    int64_t gi = 0;
     int segc = 0;
     bool ok = true;
     for (int64_t f = f0; ok && f < f1;) {
@@ -695,120 +596,165 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       f = next;
       for (int k = 0; ok && k < sg.n; ++k) {
         const int64_t g = gi + k;
-        const int s = (int)(g % kStages);
+        const int s = (int)(g % kStages), buf = (int)(g & 1);
         if (!(ok = wait(&ms->ld_full[s], (uint32_t)((g / kStages) & 1)))) break;
-        const uint32_t* vi = reinterpret_cast<const uint32_t*>(smem + kOffRing + s * Sh::kStage + Sh::kOffVIdx);
-        const uint32_t* vsg = reinterpret_cast<const uint32_t*>(smem + kOffRing + s * Sh::kStage + Sh::kOffVSgn);
-        // half-planes are stored in groups of up to VR, one store wait per group
-        int pending = 0;
-        auto release = [&]() {
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0)
-            for (int e = 0; e < pending; ++e) mbar_arrive(smem_u32(&ms->va_full[(vc - pending + e) % VR]));
-          pending = 0;
-        };
-#pragma unroll 1
-        for (int P = 0; ok && P < NP; ++P) {
-          uint32_t bw[4];
+        if (!(ok = wait(&ms->p_full[buf], (uint32_t)((g >> 1) & 1)))) break;
+        const uint8_t* stg = smem + Sh::kOffRing + s * Sh::kStage;
+        const uint32_t* vi = reinterpret_cast<const uint32_t*>(stg + Sh::kOffVIdx);
+        const uint32_t* vsg = reinterpret_cast<const uint32_t*>(stg + Sh::kOffVSgn);
+        const uint8_t* bv = smem + Sh::kOffBV + buf * Sh::kBVBytes;
+        // lazy rescale of the accumulators (the head of column c is c % GP)
+        {
+          float fh[GP];
+          bool any = false;
 #pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            if (P < W) bw[kb] = vi[(kb * W + P) * kD + j];
-            else if (P < NPM)  // w = 3 product plane
-              bw[kb] = vi[(kb * W) * kD + j] ^ vi[(kb * W + 1 % W) * kD + j] ^ vi[(kb * W + 2 % W) * kD + j];
-            else bw[kb] = vsg[kb * kD + j];
+          for (int hh = 0; hh < GP; ++hh) {
+            fh[hh] = ms->fac[buf][hh];
+            any |= fh[hh] != 1.f;
           }
+          if (any) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int slot = (int)(vc % VR);
-            if (pending == VR) release();
-            if (vc >= VR && !(ok = wait(&ms->va_empty[slot], (uint32_t)((vc / VR - 1) & 1)))) break;
-            uint32_t vals[32];
+            for (int P = 0; P < NP; ++P)
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const uint32_t wd = bw[2 * half + kk];
-              const uint32_t x0 = wd, x1 = wd << 6, x2 = wd << 12;
+              for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int p = vpos(i);
-                const uint32_t src = i >= 10 ? x0 : (i >= 4 ? x1 : x2);
-                vals[16 * kk + i] = (src & ((1u << p) | (1u << (p + 16)))) | c_v_base[p - 10];
-              }
-            }
-            tmem_st32(tmem + lane_base + Sh::kColV + slot * 32, vals);
-            ++vc;
-            ++pending;
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                  for (int e = 0; e < 2; ++e) {
+                    const int c = 8 * nt + 2 * tig + e;
+                    const float x = c < NC ? fh[c % GP] : 1.f;
+                    vacc[P][mt][nt][e] *= x;
+                    vacc[P][mt][nt][2 + e] *= x;
+                  }
           }
         }
-        if (!ok) break;
-        if (pending > 0) release();
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+          uint32_t b0[2][NT], b1[2][NT];
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint32_t* row = reinterpret_cast<const uint32_t*>(bv + (((part * 4 + kb) * NT + nt) * 8 + gq) * 32);
+              b0[part][nt] = row[tig];
+              b1[part][nt] = row[4 + tig];
+            }
+#pragma unroll
+          for (int P = 0; P < NP; ++P) {
+            const int part = P < NPM ? 0 : 1;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              const int jA = 32 * vwarp + 16 * mt + gq, jB = jA + 8;
+              uint32_t wA, wB;
+              if (P < W) {
+                wA = vi[(kb * W + P) * kD + jA];
+                wB = vi[(kb * W + P) * kD + jB];
+              } else if (P < NPM) {  // w = 3 product plane
+                wA = vi[(kb * W) * kD + jA] ^ vi[(kb * W + 1 % W) * kD + jA] ^ vi[(kb * W + 2 % W) * kD + jA];
+                wB = vi[(kb * W) * kD + jB] ^ vi[(kb * W + 1 % W) * kD + jB] ^ vi[(kb * W + 2 % W) * kD + jB];
+              } else {
+                wA = vsg[kb * kD + jA];
+                wB = vsg[kb * kD + jB];
+              }
+              const uint32_t a0 = ly.lo(wA), a1 = ly.lo(wB), a2 = ly.hi(wA), a3 = ly.hi(wB);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_e4m3(vacc[P][mt][nt], a0, a1, a2, a3, b0[part][nt], b1[part][nt]);
+            }
+          }
+        }
+        // minus this tile's operand offsets Σ w·(C + C')/2 per column
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 8 * nt + 2 * tig + e;
+            float om = 0.f, oq = 0.f;
+            if (c < NC) {
+#pragma unroll
+              for (int q = 0; q < kKW; ++q) om += ms->off[buf][q][0][c], oq += ms->off[buf][q][1][c];
+            }
+#pragma unroll
+            for (int P = 0; P < NP; ++P)
+#pragma unroll
+              for (int mt = 0; mt < 2; ++mt) {
+                const float o = P < NPM ? om : oq;
+                vacc[P][mt][nt][e] -= o;
+                vacc[P][mt][nt][2 + e] -= o;
+              }
+          }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ms->ld_empty[s]));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&ms->p_empty[buf]));
+          mbar_arrive(smem_u32(&ms->ld_empty[s]));
+        }
       }
       if (!ok) break;
       // ---- partial of this CTA for the unit
       const int sp = segc & 1;
       if (!(ok = wait(&ms->st_full[sp], (uint32_t)((segc >> 1) & 1)))) break;
-      float d[NP][16];
-      if (sg.n > 0) {
-        // all value MMAs of the segment: the last tile's weight-buffer release.
-        // Its phase is at most one behind: expanding the last tile needed ring
-        // slots freed by the value MMAs of two tiles earlier (the ring holds at
-        // most two tiles), and those MMAs released the same buffer one phase ago.
-        const int64_t last = gi + sg.n - 1;
-        if (!(ok = wait(&ms->p_empty[last & 1], (uint32_t)((last >> 1) & 1)))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int P = 0; P < NP; ++P) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_base + Sh::kColVD + 16 * P, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 16; ++c) d[P][c] = __uint_as_float(v[c]);
-        }
-        tc_fence_before();
-      }
       const int b = (int)(sg.u / a.Hkv), h = (int)(sg.u - (int64_t)b * a.Hkv);
       const int head0 = b * a.Hq + h * a.G;
-      float cf[NPM];
+      constexpr int NO = 32 * GP / 32;  // outputs (coordinate, head) per lane
+      float rot[NO], sgn[NO];
 #pragma unroll
-      for (int P = 0; P < NPM; ++P) cf[P] = __ldg(a.walsh + (P < W ? (1 << P) : 7));
-      for (int hh = 0; hh < a.G && hh < GP; ++hh) {
-        float ar = 0.f, as = 0.f;
-        if (sg.n > 0) {
+      for (int o = 0; o < NO; ++o) rot[o] = sgn[o] = 0.f;
+      if (sg.n > 0) {
 #pragma unroll
-          for (int P = 0; P < NPM; ++P) ar = fmaf(cf[P], d[P][hh], ar);
-          as = d[NPM][8 + hh];
-        }
-        float* pp = a.part + ((size_t)(head0 + hh) * a.smax + sg.slot) * (2 + 2 * kD);
-        pp[2 + j] = ar;
-        pp[2 + kD + j] = as;
-        if (j == 0) {
-          pp[0] = ms->stat_m[sp][hh];
-          pp[1] = (ms->stat_l[sp][0][hh] + ms->stat_l[sp][1][hh]) + (ms->stat_l[sp][2][hh] + ms->stat_l[sp][3][hh]);
+        for (int P = 0; P < NP; ++P) {
+          const float cf = P < NPM ? __ldg(a.walsh + (P < W ? (1 << P) : 7)) : 1.f;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const int c = 8 * nt + 2 * tig, rA = 16 * mt + gq;
+              *reinterpret_cast<float2*>(scr + rA * NT * 8 + c) = make_float2(vacc[P][mt][nt][0], vacc[P][mt][nt][1]);
+              *reinterpret_cast<float2*>(scr + (rA + 8) * NT * 8 + c) =
+                  make_float2(vacc[P][mt][nt][2], vacc[P][mt][nt][3]);
+            }
+          __syncwarp();
+#pragma unroll
+          for (int o = 0; o < NO; ++o) {
+            const int cj = lane, hh = o;  // coordinate 32v + lane, head o
+            const float* row = scr + cj * NT * 8;
+            // Σ_t W_t s_t = (Σ_t w_t (F_t - mean_t)) / kVScale, w in three pieces
+            const float v = ((row[hh] + row[GP + hh] * 0.0625f) + row[2 * GP + hh] * 0.00390625f) * (1.f / kVScale);
+            if (P < NPM) rot[o] = fmaf(cf, v, rot[o]);
+            else sgn[o] = v;
+          }
+          __syncwarp();
         }
       }
+#pragma unroll
+      for (int o = 0; o < NO; ++o) {
+        const int hh = o;
+        if (hh < a.G) {
+          float* pp = a.part + ((size_t)(head0 + hh) * a.smax + sg.slot) * (2 + 2 * kD);
+          pp[2 + 32 * vwarp + lane] = rot[o];
+          pp[2 + kD + 32 * vwarp + lane] = sgn[o];
+          if (vwarp == 0 && lane == 0) {
+            float l = 0.f;
+#pragma unroll
+            for (int q = 0; q < kKW; ++q) l += ms->stat_l[sp][q][hh];
+            pp[0] = ms->stat_m[sp][hh];
+            pp[1] = l;
+          }
+        }
+      }
+#pragma unroll
+      for (int P = 0; P < NP; ++P)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vacc[P][mt][nt][e] = 0.f;
       __syncwarp();
-      if (lane == 0) {
-        if (sg.n > 0) mbar_arrive(smem_u32(&ms->vd_free));
-        mbar_arrive(smem_u32(&ms->st_empty[sp]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&ms->st_empty[sp]));
       gi += sg.n;
       ++segc;
     }
   }
-  tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-template <int W>
-constexpr int smem_bytes() {
-  return 1024 + kOffRing + kStages * Shape<W, 4>::kStage + kMiscBytes;
 }
 
 }  // namespace
@@ -854,10 +800,9 @@ tq_status launch_decode_tc(const tq_plan* plan, const tq_records* K, const tq_re
   if (!a.fault) return TQ_ERR_CUDA;
   const int grid = decode_tc_ctas((int64_t)B * Hkv, a.tpu);
   auto go = [&](auto kern, int smem) -> tq_status {
-    const int bytes = std::max(smem, 120 * 1024);  // one CTA per SM: it owns all of TMEM
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    kern<<<grid, kThreads, bytes, stream>>>(a);
+    kern<<<grid, kThreads, smem, stream>>>(a);
     return launch_status();
   };
   const bool g8 = a.G > 4;
