@@ -101,6 +101,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parity, unsigned* fault, unsigned code,
                                                     volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (*abort) return false;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
