@@ -46,7 +46,7 @@ int choose_splits(int B, int Hkv, int64_t ctx_stride) {
 // Partial slots per head of the tensor-core path (0 when it cannot apply).
 int tc_slots(const DecodeShape& s) {
   if (s.d != 128 || s.m != 128 || s.G > kMaxG || s.ctx_stride % 128 != 0) return 0;
-  const int64_t units = int64_t(s.B) * s.Hkv, tpu = s.ctx_stride / 128;
+  const int64_t units = int64_t(s.B) * s.Hkv, tpu = tq::decode_tc_tpu(s.ctx_stride);
   return tq::decode_tc_slots(units, tpu, tq::decode_tc_ctas(units, tpu));
 }
 
@@ -446,7 +446,7 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
     CombineArgs c{};
     c.s = s;
     c.slots = slots;
-    c.tpu = ctx_stride / 128;
+    c.tpu = tq::decode_tc_tpu(ctx_stride);
     c.ctas = tq::decode_tc_ctas(int64_t(B) * Hkv, c.tpu);
     c.part = part;
     c.pi = plan->pi;

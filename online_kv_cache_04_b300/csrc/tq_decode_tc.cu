@@ -32,19 +32,21 @@
 // and 5 to 8 heads take a second tile over the same expanded bits.
 // Why f16 warp MMAs: decode has one query per head, so every product here
 // is at most 8 columns wide.  A tcgen05.mma costs its issuing thread over a
-// hundred cycles whatever its width, and an e4m3 mma.sync executes about a
-// dozen extra integer instructions per call, while the f16 one runs bare.
+// hundred cycles whatever its width, and an e4m3 or int8 mma.sync runs far
+// below the f16 one.
 //
 // Work split.  A persistent grid of one CTA per SM takes contiguous ranges of
-// 128-token tiles over all (batch, kv head) units; a unit cut between CTAs
-// leaves one partial per CTA, merged by the combine kernel of tq_decode.cu.
-// Eight warps do the same work: warp w scores 16 tokens of each tile and
-// accumulates values for 16 coordinates.  The weights of a tile go through
-// shared memory, already laid out as the value operand, and the warps
-// pipeline one tile deep (scores of tile i, then values of tile i − 1), so
-// one named barrier per tile orders everything: it publishes the weights, it
-// frees the ring stage of tile i − 2, into which one thread then starts the
-// bulk copies of a later tile, and it carries the vote of the lazy softmax.
+// 256-token tiles over all (batch, kv head) units (the last tile of a unit
+// may hold 128); a unit cut between CTAs leaves one partial per CTA, merged
+// by the combine kernel of tq_decode.cu.  Eight warps do the same work: warp
+// w scores the 32 tokens of block w of each tile and accumulates values for
+// 16 coordinates.  The weights of a tile go through shared memory, already
+// laid out as the value operand.  Per tile i there are two named barriers:
+// the first publishes the weights of tile i − 1; between the two, the value
+// products of tile i − 1, the score products of tile i and its softmax run
+// as one block the compiler can interleave; the second carries the vote of
+// the lazy softmax and frees the ring stage of tile i − 1, into which one
+// thread then starts the bulk copies of a later tile.
 //
 // Softmax is online with a lazy reference: the running reference M (of
 // log2(p·max(‖v‖, ‖r_v‖)), clamped at 2^-32) moves only when a tile exceeds
@@ -63,9 +65,10 @@ namespace {
 using namespace tq::sm100;
 
 constexpr int kNW = 8;                                 // warps
-constexpr int kTile = 16 * kNW;                        // tokens per tile
+constexpr int kTile = 32 * kNW;                        // tokens per tile: one 32-row block per warp
+constexpr int kHalfTile = 128;                         // the last tile of a unit may hold this many
 constexpr int kD = 128;
-constexpr int kStages = 8;                             // power of two
+constexpr int kStages = 4;                             // power of two
 constexpr int kThreads = 32 * kNW;
 constexpr float kTau = 6.0f;                           // lazy-rescale threshold (log2 units)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -77,8 +80,28 @@ constexpr uint32_t kSignMask = 0x80008000u, kSignBase = 0x3C003C00u;
 constexpr uint32_t kExpMask = 0x08000800u, kExpBase = 0x30003000u;
 constexpr float kExpDelta = 0.375f, kExpMean = 0.3125f;  // C' - C, (C + C')/2
 
-__device__ __forceinline__ uint32_t sign_op(uint32_t t) { return (t & kSignMask) | kSignBase; }
-__device__ __forceinline__ uint32_t exp_op(uint32_t t) { return (t & kExpMask) | kExpBase; }
+// Per quad index q: 2^(3-q) times 1, 2^4, 2^8, 2^12.  Read from constant
+// memory so that the moves stay integer multiplies (FMA pipe) instead of
+// shifts on the busier integer pipe.
+__constant__ uint32_t c_mul[4][4] = {{8u, 128u, 2048u, 32768u},
+                                     {4u, 64u, 1024u, 16384u},
+                                     {2u, 32u, 512u, 8192u},
+                                     {1u, 16u, 256u, 4096u}};
+
+// The masks and bases live in registers loaded from constant memory: with
+// both in registers each operand is a single three-input logic op.
+__constant__ uint32_t c_ops[4] = {kSignMask, kSignBase, kExpMask, kExpBase};
+struct OperandKinds {
+  uint32_t sm, sb, em, eb;
+  __device__ __forceinline__ OperandKinds() : sm(c_ops[0]), sb(c_ops[1]), em(c_ops[2]), eb(c_ops[3]) {}
+  __device__ __forceinline__ static uint32_t andor(uint32_t t, uint32_t m, uint32_t b) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(t), "r"(m), "r"(b));  // (t & m) | b
+    return r;
+  }
+  __device__ __forceinline__ uint32_t sign(uint32_t t) const { return andor(t, sm, sb); }
+  __device__ __forceinline__ uint32_t expo(uint32_t t) const { return andor(t, em, eb); }
+};
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -92,6 +115,10 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 // Named barrier of all warps, and the same barrier with an OR vote.
@@ -118,7 +145,7 @@ struct TcArgs {
   float scale, alpha;
   float* part;       // [B*Hq][smax][2 + 2*128]
   int smax;
-  int64_t tpu;       // tiles per unit = ctx_stride / 128
+  int64_t tpu;       // tiles per unit = ceil(ctx_stride / 256)
   int64_t total;     // units * tpu
   unsigned* fault;
 };
@@ -139,6 +166,7 @@ struct Shape {
   static constexpr int NKS = 8 * NP;           // score K-steps of 16 coordinates
   static constexpr int GH = GP / 4;            // head tiles = heads per thread
   static constexpr bool kBRegs = NKS * GH * 2 <= 80;  // query-weight fragments held in registers
+  // ring stage of one full tile; a short tile fills the first half of each region
   static constexpr int kIdxBytes = kTile * 4 * W * 4;
   static constexpr int kSgnBytes = kTile * 16, kNormBytes = kTile * 4;
   static constexpr int kStage = 2 * kIdxBytes + 2 * kSgnBytes + 4 * kNormBytes;
@@ -147,8 +175,9 @@ struct Shape {
   static constexpr int kOffVIdx = kOffKRn + kNormBytes, kOffVSgn = kOffVIdx + kIdxBytes,
                        kOffVNorm = kOffVSgn + kSgnBytes, kOffVRn = kOffVNorm + kNormBytes;
   // shared memory plan
-  static constexpr int kBKBytes = NKS * GH * 8 * 16 * 2;   // [ks][head tile][n 8][k 16] f16 query weights
-  static constexpr int kBVBuf = 2 * GH * 4 * 2 * 8 * 4 * 8;  // [part][head tile][block][ks2][n 8][quad 4][b0, b1] f16x2
+  static constexpr int kBKBytes = NKS * GH * 8 * 16 * 2;  // [ks][head tile][n 8][k 16] f16 query weights
+  // [part][head tile][block 8][K half 2][n 8][quad 4][b0, b1] f16x2 attention weights
+  static constexpr int kBVBuf = 2 * GH * 8 * 2 * 8 * 4 * 8;
   static constexpr int kOffRing = 0;
   static constexpr int kOffBK = kOffRing + kStages * kStage;
   static constexpr int kOffBV = kOffBK + kBKBytes;
@@ -170,6 +199,7 @@ template <int W>
 constexpr int smem_bytes() {
   return 1024 + Shape<W, 8>::kOffMisc + kMiscBytes;
 }
+static_assert(smem_bytes<3>() <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
 
 // Segment of this CTA's tile range that falls in one unit.
 struct Seg {
@@ -222,10 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
     mbar_wait_abortable(smem_u32(bar), parity, a.fault, kFaultDecode, abort_flag);
   };
   // Bulk copies, issued by thread 0: tile `issued` of this CTA's sequence of
-  // valid tiles goes to stage issued % kStages once the tile kStages earlier
-  // has been consumed (`done` tiles are).
-  // The cursor (cur, cu, ct, cL) walks flat tiles: unit cu, tile ct in it,
-  // context length cL of the unit.
+  // valid tiles goes to stage issued % kStages once `done` tiles have been
+  // consumed and issued < done + kStages.  The cursor (cur, cu, ct, cL) walks
+  // flat tiles: unit cu, tile ct in it, context length cL of the unit.
   int64_t issued = 0, cur = f0, cu = f0 / a.tpu, ct = f0 - cu * a.tpu;
   int cL = (int)min((int64_t)max(__ldg(a.ctx_len + cu / a.Hkv), 0), a.ctx_stride);
   auto issue_upto = [&](int64_t done) {
@@ -239,40 +268,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         continue;
       }
       const int64_t row0 = cu * a.ctx_stride + ct * kTile;
+      const int ntok = (int)min((int64_t)kTile, a.ctx_stride - ct * kTile);  // 256, or 128 at a unit's end
       ++cur;
       ++ct;
       const int s = (int)(issued & (kStages - 1));
       ++issued;
       const uint32_t bar = smem_u32(&ms->ld_full[s]);
       const uint32_t dst = sbase + Sh::kOffRing + s * Sh::kStage;
-      mbar_arrive_expect_tx(bar, Sh::kStage);
-      bulk_load(dst + Sh::kOffKIdx, a.kidx + row0 * (4 * W), Sh::kIdxBytes, bar);
-      bulk_load(dst + Sh::kOffKSgn, a.ksgn + row0 * 4, Sh::kSgnBytes, bar);
-      bulk_load(dst + Sh::kOffKNorm, a.knorm + row0, Sh::kNormBytes, bar);
-      bulk_load(dst + Sh::kOffKRn, a.krnorm + row0, Sh::kNormBytes, bar);
-      bulk_load(dst + Sh::kOffVIdx, a.vidx + (row0 >> 5) * (W * kD), Sh::kIdxBytes, bar);
-      bulk_load(dst + Sh::kOffVSgn, a.vsgn + (row0 >> 5) * kD, Sh::kSgnBytes, bar);
-      bulk_load(dst + Sh::kOffVNorm, a.vnorm + row0, Sh::kNormBytes, bar);
-      bulk_load(dst + Sh::kOffVRn, a.vrnorm + row0, Sh::kNormBytes, bar);
+      const int idxb = ntok * 16 * W, sgnb = ntok * 16, nrmb = ntok * 4;
+      mbar_arrive_expect_tx(bar, 2 * idxb + 2 * sgnb + 4 * nrmb);
+      bulk_load(dst + Sh::kOffKIdx, a.kidx + row0 * (4 * W), idxb, bar);
+      bulk_load(dst + Sh::kOffKSgn, a.ksgn + row0 * 4, sgnb, bar);
+      bulk_load(dst + Sh::kOffKNorm, a.knorm + row0, nrmb, bar);
+      bulk_load(dst + Sh::kOffKRn, a.krnorm + row0, nrmb, bar);
+      bulk_load(dst + Sh::kOffVIdx, a.vidx + (row0 >> 5) * (W * kD), idxb, bar);
+      bulk_load(dst + Sh::kOffVSgn, a.vsgn + (row0 >> 5) * kD, sgnb, bar);
+      bulk_load(dst + Sh::kOffVNorm, a.vnorm + row0, nrmb, bar);
+      bulk_load(dst + Sh::kOffVRn, a.vrnorm + row0, nrmb, bar);
     }
   };
   if (threadIdx.x == 0) issue_upto(0);
 
-  const int w = warp, kbw = w >> 1, hf = w & 1;
-  // Score rows gq, gq + 8 <-> tokens tok, tok + 1 of the tile (block kbw).
-  // Their value bits are bits L and 16 + L of the block words, L = 8·hf + gq,
+  const int w = warp;
+  // Score rows gq, gq + 8 of group g2 <-> tokens tok + 16·g2, + 1 of block w.
+  // Their value bits are bits L and 16 + L of the block words, L = 8·g2 + gq,
   // i.e. one f16x2 operand register: this thread writes whole registers of
   // the value weights.
-  const int tok = 32 * kbw + 16 * hf + 2 * gq;
+  const int tok = 32 * w + 2 * gq;
   const int crd = 16 * w + 2 * gq;  // value rows gq, gq + 8 <-> coordinates crd, crd + 1
   // multipliers moving bits tig, 4+tig, 8+tig, 12+tig of each half to bits
   // 3, 7, 11, 15 (mul), and each of those to bit 15 (mul·2^12 .. mul)
-  const uint32_t mul = 1u << (3 - tig), mul4 = mul << 4, mul8 = mul << 8, mul12 = mul << 12;
+  const uint32_t mul = c_mul[tig][0], mul4 = c_mul[tig][1], mul8 = c_mul[tig][2], mul12 = c_mul[tig][3];
+  const OperandKinds op;
   uint8_t* BK = smem + Sh::kOffBK;
-  // accumulator slots: with one head tile the two K halves of a word (more
-  // independent chains), with two head tiles the tile
   uint32_t bf[Sh::kBRegs ? NKS : 1][GH][2];
-  float vacc[NP][2][4];
+  float vacc[NP][GH][4];
   float M[GH], lsum[GH], pend[GH], A0[GH], B0[GH], A1[GH], B1[GH];
   int64_t gi = 0;
   int segc = 0;
@@ -285,9 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
     for (int P = 0; P < NP; ++P)
 #pragma unroll
-      for (int sl = 0; sl < 2; ++sl)
+      for (int ht = 0; ht < GH; ++ht)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) vacc[P][sl][e] = 0.f;
+        for (int e = 0; e < 4; ++e) vacc[P][ht][e] = 0.f;
 #pragma unroll
     for (int hh = 0; hh < GH; ++hh) M[hh] = -INFINITY, lsum[hh] = 0.f, pend[hh] = 1.f;
     if (sg.n > 0) {
@@ -384,106 +414,188 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           }
       }
 
-      // ---- tiles: scores of tile k, then values of tile k - 1
-      for (int k = 0; k <= sg.n; ++k) {
-        const int64_t g = gi + k;
-        const bool keys = k < sg.n;
-        float s2[GH][2], mx[GH], vnc[2], vrc[2];
-        bool exceed = false;
-        if (keys) {
-          const int s = (int)(g & (kStages - 1));
-          wait(&ms->ld_full[s], (uint32_t)((g / kStages) & 1));
-          const uint8_t* stg = smem + Sh::kOffRing + s * Sh::kStage;
-          const uint4* kq = reinterpret_cast<const uint4*>(stg + Sh::kOffKIdx);  // token t, plane P: kq[t·W + P]
-          const uint4* sq = reinterpret_cast<const uint4*>(stg + Sh::kOffKSgn);  // token t: sq[t]
-          float acc[NP][2][4];
+      // ---- tiles.  Per tile k: weights of tile k-1 | barrier | values of tile
+      // k-1 and scores of tile k (one straight block) | barrier + vote.
+      float s2p[GH][2][2], vnp[2][2], vrp[2][2];  // tile k-1: scores (log2 units), cleaned value norms
+      float s2c[GH][2][2], vnc[2][2], vrc[2][2], mx[GH];
+
+      // attention weights of the previous tile -> value operand registers (hi, lo)
+      auto weights_step = [&](int kp) {
+        uint32_t* bv = reinterpret_cast<uint32_t*>(smem + Sh::kOffBV + (kp & 1) * Sh::kBVBuf);
 #pragma unroll
-          for (int P = 0; P < NP; ++P)
+        for (int hh = 0; hh < GH; ++hh)
 #pragma unroll
-            for (int sl = 0; sl < 2; ++sl)
+          for (int g2 = 0; g2 < 2; ++g2) {
+            float p[2];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) acc[P][sl][e] = 0.f;
+            for (int r = 0; r < 2; ++r) p[r] = s2p[hh][g2][r] == -INFINITY ? 0.f : exp2f(s2p[hh][g2][r] - M[hh]);
+            lsum[hh] += p[0] + p[1];
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              const float x0 = p[0] * (part == 0 ? vnp[g2][0] : vrp[g2][0]) * kWS;
+              const float x1 = p[1] * (part == 0 ? vnp[g2][1] : vrp[g2][1]) * kWS;
+              const uint32_t whi = f16x2_of(x0, x1);
+              const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&whi));
+              const uint32_t wlo = f16x2_of(x0 - back.x, x1 - back.y);
+              const int base = ((((part * GH + hh) * 8 + w) * 2 + g2) * 8 + 2 * tig) * 8 + (gq & 3) * 2 + (gq >> 2);
+              bv[base] = whi;
+              bv[base + 8] = wlo;
+            }
+          }
+      };
+
+      // values of tile kv (CTA tile index gv): 16 coordinates of every plane.
+      // A short tile's upper blocks hold stale words with zero weights.
+      auto values_step = [&](int kv, int64_t gv) {
+        const uint8_t* stg = smem + Sh::kOffRing + (int)(gv & (kStages - 1)) * Sh::kStage;
+        const uint32_t* vi = reinterpret_cast<const uint32_t*>(stg + Sh::kOffVIdx);
+        const uint32_t* vsg = reinterpret_cast<const uint32_t*>(stg + Sh::kOffVSgn);
+        const uint32_t* bv = reinterpret_cast<const uint32_t*>(smem + Sh::kOffBV + (kv & 1) * Sh::kBVBuf);
+        // the reference moved at tile kv: bring the earlier tiles to it (factor 1 otherwise)
+#pragma unroll
+        for (int P = 0; P < NP; ++P)
+#pragma unroll
+          for (int ht = 0; ht < GH; ++ht)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vacc[P][ht][e] *= pend[ht];
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          uint2 bb[2][GH][2];  // [part][head tile][K half]
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ht = 0; ht < GH; ++ht)
+#pragma unroll
+              for (int s2i = 0; s2i < 2; ++s2i)
+                bb[part][ht][s2i] = *reinterpret_cast<const uint2*>(
+                    bv + (((((part * GH + ht) * 8 + kb) * 2 + s2i) * 8 + gq) * 4 + tig) * 2);
 #pragma unroll
           for (int P = 0; P < NP; ++P) {
-            uint4 wd[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              if (P < W) {
-                wd[r] = kq[(tok + r) * W + P];
-              } else if (P < NPM) {  // product plane b0 ^ b1 ^ b2
-                const uint4 x0 = kq[(tok + r) * W], x1 = kq[(tok + r) * W + 1 % W], x2 = kq[(tok + r) * W + 2 % W];
-                wd[r] = make_uint4(x0.x ^ x1.x ^ x2.x, x0.y ^ x1.y ^ x2.y, x0.z ^ x1.z ^ x2.z, x0.w ^ x1.w ^ x2.w);
-              } else {
-                wd[r] = sq[tok + r];
-              }
+            uint2 ww;
+            if (P < W) {
+              ww = *reinterpret_cast<const uint2*>(vi + (kb * W + P) * kD + crd);
+            } else if (P < NPM) {  // product plane
+              const uint2 x0 = *reinterpret_cast<const uint2*>(vi + (kb * W) * kD + crd);
+              const uint2 x1 = *reinterpret_cast<const uint2*>(vi + (kb * W + 1 % W) * kD + crd);
+              const uint2 x2 = *reinterpret_cast<const uint2*>(vi + (kb * W + 2 % W) * kD + crd);
+              ww = make_uint2(x0.x ^ x1.x ^ x2.x, x0.y ^ x1.y ^ x2.y);
+            } else {
+              ww = *reinterpret_cast<const uint2*>(vsg + kb * kD + crd);
             }
+            const int part = P < NPM ? 0 : 1;
+            // every layer as a sign operand: bit 15 of the word times mul·(4096, 256, 16, 1)
+            const uint32_t a00 = op.sign(ww.x * mul12), a01 = op.sign(ww.y * mul12);
+            const uint32_t a02 = op.sign(ww.x * mul8), a03 = op.sign(ww.y * mul8);
+            const uint32_t a10 = op.sign(ww.x * mul4), a11 = op.sign(ww.y * mul4);
+            const uint32_t a12 = op.sign(ww.x * mul), a13 = op.sign(ww.y * mul);
 #pragma unroll
-            for (int kw = 0; kw < 4; ++kw) {
-              const uint32_t x0 = kw == 0 ? wd[0].x : kw == 1 ? wd[0].y : kw == 2 ? wd[0].z : wd[0].w;
-              const uint32_t x1 = kw == 0 ? wd[1].x : kw == 1 ? wd[1].y : kw == 2 ? wd[1].z : wd[1].w;
-              const uint32_t t0 = x0 * mul, t1 = x1 * mul;          // layers 8+q, 12+q at bits 11, 15
-              const uint32_t u0 = x0 * mul8, u1 = x1 * mul8;        // layers q, 4+q at bits 11, 15
-              const int ks = (P * 4 + kw) * 2;
-              const uint32_t e0 = exp_op(u0), e1 = exp_op(u1), g0 = sign_op(u0), g1 = sign_op(u1);
-              const uint32_t f0r = exp_op(t0), f1r = exp_op(t1), h0 = sign_op(t0), h1 = sign_op(t1);
-#pragma unroll
-              for (int ht = 0; ht < GH; ++ht) {
-                mma_f16(acc[P][GH == 1 ? 0 : ht], e0, e1, g0, g1, bfrag(ks, ht, 0), bfrag(ks, ht, 1));
-                mma_f16(acc[P][GH == 1 ? 1 : ht], f0r, f1r, h0, h1, bfrag(ks + 1, ht, 0), bfrag(ks + 1, ht, 1));
-              }
+            for (int ht = 0; ht < GH; ++ht) {
+              mma_f16(vacc[P][ht], a00, a01, a02, a03, bb[part][ht][0].x, bb[part][ht][0].y);
+              mma_f16(vacc[P][ht], a10, a11, a12, a13, bb[part][ht][1].x, bb[part][ht][1].y);
             }
-          }
-          // dm, dq per (row, head tile): fragment e = 2·row + piece (hi, lo)
-          float dm[2][GH], dq[2][GH];
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int hh = 0; hh < GH; ++hh) {
-              float m = 0.f, qj = 0.f;
-#pragma unroll
-              for (int sl = 0; sl < 2; ++sl) {
-                if (GH == 2 && sl != hh) continue;
-#pragma unroll
-                for (int P = 0; P < NPM; ++P) m += acc[P][sl][2 * r] + acc[P][sl][2 * r + 1];
-                qj += acc[NPM][sl][2 * r] + acc[NPM][sl][2 * r + 1];
-              }
-              dm[r][hh] = m;
-              dq[r][hh] = qj;
-            }
-          const float* kn = reinterpret_cast<const float*>(stg + Sh::kOffKNorm);
-          const float* kr = reinterpret_cast<const float*>(stg + Sh::kOffKRn);
-          const float* vn = reinterpret_cast<const float*>(stg + Sh::kOffVNorm);
-          const float* vr = reinterpret_cast<const float*>(stg + Sh::kOffVRn);
-          const float2 kn2 = *reinterpret_cast<const float2*>(kn + tok), kr2 = *reinterpret_cast<const float2*>(kr + tok);
-          const float2 vn2 = *reinterpret_cast<const float2*>(vn + tok), vr2 = *reinterpret_cast<const float2*>(vr + tok);
-          const int tb = (int)(sg.t0 + k) * kTile;
-#pragma unroll
-          for (int hh = 0; hh < GH; ++hh) mx[hh] = -INFINITY;
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const bool valid = tb + tok + r < sg.L;
-            vnc[r] = valid ? (r ? vn2.y : vn2.x) : 0.f;
-            vrc[r] = valid ? (r ? vr2.y : vr2.x) : 0.f;
-            const float knr = r ? kn2.y : kn2.x, krr = r ? kr2.y : kr2.x;
-            const float lv = __log2f(fmaxf(fmaxf(vnc[r], vrc[r]), 0x1p-32f));
-#pragma unroll
-            for (int hh = 0; hh < GH; ++hh) {
-              const float sc = fmaf(knr, fmaf(A0[hh], dm[r][hh], B0[hh]), krr * fmaf(A1[hh], dq[r][hh], B1[hh]));
-              s2[hh][r] = (valid && 4 * hh + tig < a.G) ? sc : -INFINITY;
-              mx[hh] = fmaxf(mx[hh], s2[hh][r] + lv);
-            }
-          }
-#pragma unroll
-          for (int hh = 0; hh < GH; ++hh) {
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], o));
-            exceed |= M[hh] == -INFINITY ? mx[hh] > -INFINITY : mx[hh] > M[hh] + kTau;
           }
         }
-        // one barrier per tile: weights of tile k - 1 are complete, stage of
-        // tile k - 2 is free, and the vote of the lazy reference
+      };
+
+      // scores of tile kc (CTA tile index gc, stage already landed): block w,
+      // two groups of 16 tokens -> s2c, cleaned norms, and the tile maximum
+      auto scores_step = [&](int kc, int64_t gc) {
+        const uint8_t* stg = smem + Sh::kOffRing + (int)(gc & (kStages - 1)) * Sh::kStage;
+        const uint4* kq = reinterpret_cast<const uint4*>(stg + Sh::kOffKIdx);  // token t, plane P: kq[t·W + P]
+        const uint4* sq = reinterpret_cast<const uint4*>(stg + Sh::kOffKSgn);  // token t: sq[t]
+        float acc[2][2][GH][4];  // [group][part][head tile][fragment]
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2)
+#pragma unroll
+          for (int pt = 0; pt < 2; ++pt)
+#pragma unroll
+            for (int ht = 0; ht < GH; ++ht)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[g2][pt][ht][e] = 0.f;
+#pragma unroll
+        for (int P = 0; P < NP; ++P) {
+          const int part = P < NPM ? 0 : 1;
+          uint4 wd[2][2];  // [group][row]
+#pragma unroll
+          for (int g2 = 0; g2 < 2; ++g2)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int t = tok + 16 * g2 + r;
+              if (P < W) {
+                wd[g2][r] = kq[t * W + P];
+              } else if (P < NPM) {  // product plane b0 ^ b1 ^ b2
+                const uint4 x0 = kq[t * W], x1 = kq[t * W + 1 % W], x2 = kq[t * W + 2 % W];
+                wd[g2][r] =
+                    make_uint4(x0.x ^ x1.x ^ x2.x, x0.y ^ x1.y ^ x2.y, x0.z ^ x1.z ^ x2.z, x0.w ^ x1.w ^ x2.w);
+              } else {
+                wd[g2][r] = sq[t];
+              }
+            }
+#pragma unroll
+          for (int kw = 0; kw < 4; ++kw) {
+            const int ks = (P * 4 + kw) * 2;
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2) {
+              const uint32_t x0 = word_of(wd[g2][0], kw), x1 = word_of(wd[g2][1], kw);
+              const uint32_t t0 = x0 * mul, t1 = x1 * mul;    // layers 8+q, 12+q at bits 11, 15
+              const uint32_t u0 = x0 * mul8, u1 = x1 * mul8;  // layers q, 4+q at bits 11, 15
+#pragma unroll
+              for (int ht = 0; ht < GH; ++ht) {
+                mma_f16(acc[g2][part][ht], op.expo(u0), op.expo(u1), op.sign(u0), op.sign(u1), bfrag(ks, ht, 0),
+                        bfrag(ks, ht, 1));
+                mma_f16(acc[g2][part][ht], op.expo(t0), op.expo(t1), op.sign(t0), op.sign(t1),
+                        bfrag(ks + 1, ht, 0), bfrag(ks + 1, ht, 1));
+              }
+            }
+          }
+        }
+        const float* kn = reinterpret_cast<const float*>(stg + Sh::kOffKNorm);
+        const float* kr = reinterpret_cast<const float*>(stg + Sh::kOffKRn);
+        const float* vn = reinterpret_cast<const float*>(stg + Sh::kOffVNorm);
+        const float* vr = reinterpret_cast<const float*>(stg + Sh::kOffVRn);
+        const int64_t tb = (sg.t0 + kc) * kTile;
+#pragma unroll
+        for (int hh = 0; hh < GH; ++hh) mx[hh] = -INFINITY;
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+          const int t = tok + 16 * g2;
+          const float2 kn2 = *reinterpret_cast<const float2*>(kn + t), kr2 = *reinterpret_cast<const float2*>(kr + t);
+          const float2 vn2 = *reinterpret_cast<const float2*>(vn + t), vr2 = *reinterpret_cast<const float2*>(vr + t);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const bool valid = tb + t + r < sg.L;
+            vnc[g2][r] = valid ? (r ? vn2.y : vn2.x) : 0.f;
+            vrc[g2][r] = valid ? (r ? vr2.y : vr2.x) : 0.f;
+            const float knr = r ? kn2.y : kn2.x, krr = r ? kr2.y : kr2.x;
+            const float lv = __log2f(fmaxf(fmaxf(vnc[g2][r], vrc[g2][r]), 0x1p-32f));
+#pragma unroll
+            for (int hh = 0; hh < GH; ++hh) {
+              const float dm = acc[g2][0][hh][2 * r] + acc[g2][0][hh][2 * r + 1];
+              const float dq = acc[g2][1][hh][2 * r] + acc[g2][1][hh][2 * r + 1];
+              const float sc = fmaf(knr, fmaf(A0[hh], dm, B0[hh]), krr * fmaf(A1[hh], dq, B1[hh]));
+              s2c[hh][g2][r] = (valid && 4 * hh + tig < a.G) ? sc : -INFINITY;
+              mx[hh] = fmaxf(mx[hh], s2c[hh][g2][r] + lv);
+            }
+          }
+        }
+#pragma unroll
+        for (int hh = 0; hh < GH; ++hh)
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], o));
+      };
+
+      // Second barrier of a tile: the vote of the lazy reference on the scores
+      // just computed; `done` tiles are consumed, so their stages take the next
+      // bulk copies.  The scores and norms move to the "previous tile" slots.
+      auto vote_step = [&](bool have_scores, int64_t done) {
+        bool exceed = false;
+        if (have_scores) {
+#pragma unroll
+          for (int hh = 0; hh < GH; ++hh)
+            exceed |= M[hh] == -INFINITY ? mx[hh] > -INFINITY : mx[hh] > M[hh] + kTau;
+        }
         const bool bump = cta_any(exceed);
-        if (threadIdx.x == 0) issue_upto(gi + max(k - 1, 0));
+        if (threadIdx.x == 0) issue_upto(done);
         float fac[GH];
 #pragma unroll
         for (int hh = 0; hh < GH; ++hh) fac[hh] = 1.f;
@@ -505,88 +617,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             lsum[hh] *= fac[hh];
           }
         }
-        if (k > 0) {
-          // ---- values of tile k - 1: 16 coordinates of every plane
-          const int64_t gv = g - 1;
-          const uint8_t* stg = smem + Sh::kOffRing + (int)(gv & (kStages - 1)) * Sh::kStage;
-          const uint32_t* vi = reinterpret_cast<const uint32_t*>(stg + Sh::kOffVIdx);
-          const uint32_t* vsg = reinterpret_cast<const uint32_t*>(stg + Sh::kOffVSgn);
-          const uint32_t* bv = reinterpret_cast<const uint32_t*>(smem + Sh::kOffBV + ((k - 1) & 1) * Sh::kBVBuf);
-          // the reference moved at tile k - 1: bring the earlier tiles to it
-          bool any = false;
 #pragma unroll
-          for (int hh = 0; hh < GH; ++hh) any |= pend[hh] != 1.f;
-          if (any) {
+        for (int hh = 0; hh < GH; ++hh) {
+          pend[hh] = fac[hh];
 #pragma unroll
-            for (int P = 0; P < NP; ++P)
-#pragma unroll
-              for (int sl = 0; sl < 2; ++sl)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) vacc[P][sl][e] *= pend[GH == 1 ? 0 : sl];
-          }
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            uint2 bb[2][GH][2];  // [part][head tile][K half]
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-              for (int ht = 0; ht < GH; ++ht)
-#pragma unroll
-                for (int s2i = 0; s2i < 2; ++s2i)
-                  bb[part][ht][s2i] = *reinterpret_cast<const uint2*>(
-                      bv + (((((part * GH + ht) * 4 + kb) * 2 + s2i) * 8 + gq) * 4 + tig) * 2);
-#pragma unroll
-            for (int P = 0; P < NP; ++P) {
-              uint2 ww;
-              if (P < W) {
-                ww = *reinterpret_cast<const uint2*>(vi + (kb * W + P) * kD + crd);
-              } else if (P < NPM) {  // product plane
-                const uint2 x0 = *reinterpret_cast<const uint2*>(vi + (kb * W) * kD + crd);
-                const uint2 x1 = *reinterpret_cast<const uint2*>(vi + (kb * W + 1 % W) * kD + crd);
-                const uint2 x2 = *reinterpret_cast<const uint2*>(vi + (kb * W + 2 % W) * kD + crd);
-                ww = make_uint2(x0.x ^ x1.x ^ x2.x, x0.y ^ x1.y ^ x2.y);
-              } else {
-                ww = *reinterpret_cast<const uint2*>(vsg + kb * kD + crd);
-              }
-              const int part = P < NPM ? 0 : 1;
-              // every layer as a sign operand: bit 15 of t·(4096, 256, 16, 1)
-              const uint32_t a00 = sign_op(ww.x * mul12), a01 = sign_op(ww.y * mul12), a02 = sign_op(ww.x * mul8),
-                             a03 = sign_op(ww.y * mul8);
-              const uint32_t a10 = sign_op(ww.x * mul4), a11 = sign_op(ww.y * mul4), a12 = sign_op(ww.x * mul),
-                             a13 = sign_op(ww.y * mul);
-#pragma unroll
-              for (int ht = 0; ht < GH; ++ht) {
-                mma_f16(vacc[P][GH == 1 ? 0 : ht], a00, a01, a02, a03, bb[part][ht][0].x, bb[part][ht][0].y);
-                mma_f16(vacc[P][GH == 1 ? 1 : ht], a10, a11, a12, a13, bb[part][ht][1].x, bb[part][ht][1].y);
-              }
-            }
-          }
+          for (int g2 = 0; g2 < 2; ++g2) s2p[hh][g2][0] = s2c[hh][g2][0], s2p[hh][g2][1] = s2c[hh][g2][1];
         }
 #pragma unroll
-        for (int hh = 0; hh < GH; ++hh) pend[hh] = fac[hh];
-        if (keys) {
-          // ---- attention weights of tile k -> value operand registers (hi, lo)
-          uint32_t* bv = reinterpret_cast<uint32_t*>(smem + Sh::kOffBV + (k & 1) * Sh::kBVBuf);
+        for (int g2 = 0; g2 < 2; ++g2)
 #pragma unroll
-          for (int hh = 0; hh < GH; ++hh) {
-            float p[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) p[r] = s2[hh][r] == -INFINITY ? 0.f : exp2f(s2[hh][r] - M[hh]);
-            lsum[hh] += p[0] + p[1];
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const float x0 = p[0] * (part == 0 ? vnc[0] : vrc[0]) * kWS;
-              const float x1 = p[1] * (part == 0 ? vnc[1] : vrc[1]) * kWS;
-              const uint32_t whi = f16x2_of(x0, x1);
-              const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&whi));
-              const uint32_t wlo = f16x2_of(x0 - back.x, x1 - back.y);
-              const int base = ((((part * GH + hh) * 4 + kbw) * 2 + hf) * 8 + 2 * tig) * 8 + (gq & 3) * 2 + (gq >> 2);
-              bv[base] = whi;
-              bv[base + 8] = wlo;
-            }
-          }
-        }
+          for (int r = 0; r < 2; ++r) vnp[g2][r] = vnc[g2][r], vrp[g2][r] = vrc[g2][r];
+      };
+
+      // prologue: scores of the first tile
+      wait(&ms->ld_full[gi & (kStages - 1)], (uint32_t)((gi / kStages) & 1));
+      scores_step(0, gi);
+      vote_step(true, gi);
+      // steady state: the wait comes first so that values and scores form one block
+      for (int k = 1; k < sg.n; ++k) {
+        const int64_t g = gi + k;
+        weights_step(k - 1);
+        cta_sync();
+        wait(&ms->ld_full[g & (kStages - 1)], (uint32_t)((g / kStages) & 1));
+        values_step(k - 1, g - 1);
+        scores_step(k, g);
+        vote_step(true, g);
       }
+      // epilogue: weights and values of the last tile
+      weights_step(sg.n - 1);
+      cta_sync();
+      values_step(sg.n - 1, gi + sg.n - 1);
+      vote_step(false, gi + sg.n);
       gi += sg.n;
     }
     // ---- partial of this CTA for the unit
@@ -611,16 +672,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         float rot[2], sgn[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          float x = 0.f, y = 0.f;
+          float x = 0.f;
 #pragma unroll
-          for (int sl = 0; sl < 2; ++sl) {
-            if (GH == 2 && sl != hh) continue;
-#pragma unroll
-            for (int P = 0; P < NPM; ++P) x = fmaf(cf[P], vacc[P][sl][2 * r] + vacc[P][sl][2 * r + 1], x);
-            y += vacc[NPM][sl][2 * r] + vacc[NPM][sl][2 * r + 1];
-          }
+          for (int P = 0; P < NPM; ++P) x = fmaf(cf[P], vacc[P][hh][2 * r] + vacc[P][hh][2 * r + 1], x);
           rot[r] = -x * (1.f / kWS);
-          sgn[r] = -y * (1.f / kWS);
+          sgn[r] = -(vacc[NPM][hh][2 * r] + vacc[NPM][hh][2 * r + 1]) * (1.f / kWS);
         }
         *reinterpret_cast<float2*>(pp + 2 + crd) = make_float2(rot[0], rot[1]);
         *reinterpret_cast<float2*>(pp + 2 + kD + crd) = make_float2(sgn[0], sgn[1]);
@@ -645,6 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 
 namespace tq {
 
+int64_t decode_tc_tpu(int64_t ctx_stride) { return (ctx_stride + kTile - 1) / kTile; }
+
 // Partial slots per unit for a grid of `ctas` CTAs over units * tpu tiles.
 int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas) {
   const int64_t total = units * tpu;
@@ -660,7 +718,7 @@ int decode_tc_ctas(int64_t units, int64_t tpu) { return (int)std::min<int64_t>(u
 
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride) {
   return plan->d == 128 && plan->m == 128 && G >= 1 && G <= 8 && V->layout == TQ_LAYOUT_BLOCK32 &&
-         ctx_stride % kTile == 0;
+         ctx_stride % kHalfTile == 0;
 }
 
 tq_status launch_decode_tc(const tq_plan* plan, const tq_records* K, const tq_records* V, const int32_t* ctx_len,
@@ -678,7 +736,7 @@ tq_status launch_decode_tc(const tq_plan* plan, const tq_records* K, const tq_re
   a.alpha = plan->qjl_alpha;
   a.part = part;
   a.smax = smax;
-  a.tpu = ctx_stride / kTile;
+  a.tpu = decode_tc_tpu(ctx_stride);
   a.total = (int64_t)B * Hkv * a.tpu;
   a.fault = fault_word();
   if (!a.fault) return TQ_ERR_CUDA;

@@ -54,7 +54,9 @@ tq_status quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_
                       int64_t row0, cudaStream_t st);
 
 // Tensor-core decode (tq_decode_tc.cu): d = m = 128, G <= 8, values in
-// TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Partials [B*Hq][slots][2 + 256].
+// TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Partials [B*Hq][slots][2 + 256];
+// each (batch, kv head) unit is cut into decode_tc_tpu(ctx_stride) tiles.
+int64_t decode_tc_tpu(int64_t ctx_stride);
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride);
 int decode_tc_ctas(int64_t units, int64_t tpu);
 int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas);
