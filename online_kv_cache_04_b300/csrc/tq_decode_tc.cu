@@ -38,10 +38,11 @@
 // Work split.  A persistent grid of one CTA per SM takes contiguous ranges of
 // 256-token tiles over all (batch, kv head) units (the last tile of a unit
 // may hold 128); a unit cut between CTAs leaves one partial per CTA, merged
-// by the combine kernel of tq_decode.cu.  Eight warps do the same work: warp
-// w scores the 32 tokens of block w of each tile and accumulates values for
-// 16 coordinates.  The weights of a tile go through shared memory, already
-// laid out as the value operand.  Per tile i there are two named barriers:
+// by the combine kernel of tq_decode.cu.  Sixteen warps do the same work:
+// warp w scores 16 tokens of each tile (half w & 1 of block w / 2) and
+// accumulates values for 16 coordinates (rows w % 8) over half of the blocks
+// (w / 8); the two halves meet at the end of a unit.  The weights of a tile
+// go through shared memory, already laid out as the value operand.  Per tile i there are two named barriers:
 // the first publishes the weights of tile i − 1; between the two, the value
 // products of tile i − 1, the score products of tile i and its softmax run
 // as one block the compiler can interleave; the second carries the vote of
@@ -64,8 +65,9 @@ namespace {
 
 using namespace tq::sm100;
 
-constexpr int kNW = 8;                                 // warps
-constexpr int kTile = 32 * kNW;                        // tokens per tile: one 32-row block per warp
+constexpr int kNW = 16;                                // warps
+constexpr int kBlocks = 8;                             // 32-row blocks per tile
+constexpr int kTile = 32 * kBlocks;                    // tokens per tile
 constexpr int kHalfTile = 128;                         // the last tile of a unit may hold this many
 constexpr int kD = 128;
 constexpr int kStages = 4;                             // power of two
@@ -165,7 +167,6 @@ struct Shape {
   static constexpr int NP = NPM + 1;           // plus the QJL sign plane
   static constexpr int NKS = 8 * NP;           // score K-steps of 16 coordinates
   static constexpr int GH = GP / 4;            // head tiles = heads per thread
-  static constexpr bool kBRegs = NKS * GH * 2 <= 80;  // query-weight fragments held in registers
   // ring stage of one full tile; a short tile fills the first half of each region
   static constexpr int kIdxBytes = kTile * 4 * W * 4;
   static constexpr int kSgnBytes = kTile * 16, kNormBytes = kTile * 4;
@@ -175,9 +176,10 @@ struct Shape {
   static constexpr int kOffVIdx = kOffKRn + kNormBytes, kOffVSgn = kOffVIdx + kIdxBytes,
                        kOffVNorm = kOffVSgn + kSgnBytes, kOffVRn = kOffVNorm + kNormBytes;
   // shared memory plan
-  static constexpr int kBKBytes = NKS * GH * 8 * 16 * 2;  // [ks][head tile][n 8][k 16] f16 query weights
+  // [ks][head tile][n 8][quad 4][b0, b1][half] f16 query weights, one 64-bit fragment per lane
+  static constexpr int kBKBytes = NKS * GH * 8 * 16 * 2;
   // [part][head tile][block 8][K half 2][n 8][quad 4][b0, b1] f16x2 attention weights
-  static constexpr int kBVBuf = 2 * GH * 8 * 2 * 8 * 4 * 8;
+  static constexpr int kBVBuf = 2 * GH * kBlocks * 2 * 8 * 4 * 8;
   static constexpr int kOffRing = 0;
   static constexpr int kOffBK = kOffRing + kStages * kStage;
   static constexpr int kOffBV = kOffBK + kBKBytes;
@@ -200,6 +202,7 @@ constexpr int smem_bytes() {
   return 1024 + Shape<W, 8>::kOffMisc + kMiscBytes;
 }
 static_assert(smem_bytes<3>() <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
+static_assert(2 * Shape<1, 4>::kBVBuf >= 8 * 2 * kD * 4, "weight buffers double as the end-of-unit scratch");
 
 // Segment of this CTA's tile range that falls in one unit.
 struct Seg {
@@ -228,7 +231,7 @@ __device__ __forceinline__ Seg segment_at(const TcArgs& a, int64_t f, int64_t f1
 template <int W, int GP>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) {
   using Sh = Shape<W, GP>;
-  constexpr int NPM = Sh::NPM, NP = Sh::NP, NKS = Sh::NKS, GH = Sh::GH;
+  constexpr int NPM = Sh::NPM, NP = Sh::NP, GH = Sh::GH;
   constexpr float kWS = 256.f;  // attention weights carry 2^8: up to 2^14 in f16
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -289,19 +292,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   };
   if (threadIdx.x == 0) issue_upto(0);
 
-  const int w = warp;
-  // Score rows gq, gq + 8 of group g2 <-> tokens tok + 16·g2, + 1 of block w.
+  const int w = warp, kbk = w >> 1, g2 = w & 1, vrow = w & 7, vhalf = w >> 3;
+  // Score rows gq, gq + 8 <-> tokens tok, tok + 1 of the tile (block kbk).
   // Their value bits are bits L and 16 + L of the block words, L = 8·g2 + gq,
   // i.e. one f16x2 operand register: this thread writes whole registers of
   // the value weights.
-  const int tok = 32 * w + 2 * gq;
-  const int crd = 16 * w + 2 * gq;  // value rows gq, gq + 8 <-> coordinates crd, crd + 1
+  const int tok = 32 * kbk + 16 * g2 + 2 * gq;
+  const int crd = 16 * vrow + 2 * gq;  // value rows gq, gq + 8 <-> coordinates crd, crd + 1
   // multipliers moving bits tig, 4+tig, 8+tig, 12+tig of each half to bits
   // 3, 7, 11, 15 (mul), and each of those to bit 15 (mul·2^12 .. mul)
   const uint32_t mul = c_mul[tig][0], mul4 = c_mul[tig][1], mul8 = c_mul[tig][2], mul12 = c_mul[tig][3];
   const OperandKinds op;
   uint8_t* BK = smem + Sh::kOffBK;
-  uint32_t bf[Sh::kBRegs ? NKS : 1][GH][2];
   float vacc[NP][GH][4];
   float M[GH], lsum[GH], pend[GH], A0[GH], B0[GH], A1[GH], B1[GH];
   int64_t gi = 0;
@@ -377,7 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             const float E = escale(part, g);
             const float x = wsc * (part == 0 ? cf[P < NPM ? P : 0] * qv[g] : sv[g]) / E;
             const __half xh = __float2half_rn(x), xl = __float2half_rn(x - __half2float(xh));
-            const int base = ((ks * GH + (g >> 2)) * 8 + 2 * (g & 3)) * 16 + kk;
+            // (k, n) sits in lane (n, k % 8 / 2), fragment k / 8, half k % 2
+            const int base = ((((ks * GH + (g >> 2)) * 8 + 2 * (g & 3)) * 4 + ((kk & 7) >> 1)) * 2 + (kk >> 3)) * 2 +
+                             (kk & 1);
             bk[base] = xh;
             bk[base + 16] = xl;
             float o = hi ? 0.f : (__half2float(xh) + __half2float(xl)) * E * kExpMean;
@@ -399,53 +403,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           B1[hh] = -c * a.alpha * ms->O[1][g];
         }
       }
-      auto bfrag = [&](int ks, int ht, int i) -> uint32_t {
-        if constexpr (Sh::kBRegs) return bf[ks][ht][i];
-        return reinterpret_cast<const uint32_t*>(BK + ((ks * GH + ht) * 8 + gq) * 32)[4 * i + tig];
+      auto bfrag = [&](int ks, int ht) -> uint2 {
+        return reinterpret_cast<const uint2*>(BK)[((ks * GH + ht) * 8 + gq) * 4 + tig];
       };
-      if constexpr (Sh::kBRegs) {
-#pragma unroll
-        for (int ks = 0; ks < NKS; ++ks)
-#pragma unroll
-          for (int ht = 0; ht < GH; ++ht) {
-            const uint32_t* row = reinterpret_cast<const uint32_t*>(BK + ((ks * GH + ht) * 8 + gq) * 32);
-            bf[ks][ht][0] = row[tig];
-            bf[ks][ht][1] = row[4 + tig];
-          }
-      }
-
       // ---- tiles.  Per tile k: weights of tile k-1 | barrier | values of tile
       // k-1 and scores of tile k (one straight block) | barrier + vote.
-      float s2p[GH][2][2], vnp[2][2], vrp[2][2];  // tile k-1: scores (log2 units), cleaned value norms
-      float s2c[GH][2][2], vnc[2][2], vrc[2][2], mx[GH];
+      float s2p[GH][2], vnp[2], vrp[2];  // tile k-1: scores (log2 units), cleaned value norms
+      float s2c[GH][2], vnc[2], vrc[2], mx[GH];
 
       // attention weights of the previous tile -> value operand registers (hi, lo)
       auto weights_step = [&](int kp) {
         uint32_t* bv = reinterpret_cast<uint32_t*>(smem + Sh::kOffBV + (kp & 1) * Sh::kBVBuf);
 #pragma unroll
-        for (int hh = 0; hh < GH; ++hh)
+        for (int hh = 0; hh < GH; ++hh) {
+          float p[2];
 #pragma unroll
-          for (int g2 = 0; g2 < 2; ++g2) {
-            float p[2];
+          for (int r = 0; r < 2; ++r) p[r] = s2p[hh][r] == -INFINITY ? 0.f : exp2f(s2p[hh][r] - M[hh]);
+          lsum[hh] += p[0] + p[1];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) p[r] = s2p[hh][g2][r] == -INFINITY ? 0.f : exp2f(s2p[hh][g2][r] - M[hh]);
-            lsum[hh] += p[0] + p[1];
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const float x0 = p[0] * (part == 0 ? vnp[g2][0] : vrp[g2][0]) * kWS;
-              const float x1 = p[1] * (part == 0 ? vnp[g2][1] : vrp[g2][1]) * kWS;
-              const uint32_t whi = f16x2_of(x0, x1);
-              const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&whi));
-              const uint32_t wlo = f16x2_of(x0 - back.x, x1 - back.y);
-              const int base = ((((part * GH + hh) * 8 + w) * 2 + g2) * 8 + 2 * tig) * 8 + (gq & 3) * 2 + (gq >> 2);
-              bv[base] = whi;
-              bv[base + 8] = wlo;
-            }
+          for (int part = 0; part < 2; ++part) {
+            const float x0 = p[0] * (part == 0 ? vnp[0] : vrp[0]) * kWS;
+            const float x1 = p[1] * (part == 0 ? vnp[1] : vrp[1]) * kWS;
+            const uint32_t whi = f16x2_of(x0, x1);
+            const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&whi));
+            const uint32_t wlo = f16x2_of(x0 - back.x, x1 - back.y);
+            const int base =
+                ((((part * GH + hh) * kBlocks + kbk) * 2 + g2) * 8 + 2 * tig) * 8 + (gq & 3) * 2 + (gq >> 2);
+            bv[base] = whi;
+            bv[base + 8] = wlo;
           }
+        }
       };
 
-      // values of tile kv (CTA tile index gv): 16 coordinates of every plane.
-      // A short tile's upper blocks hold stale words with zero weights.
+      // values of tile kv (CTA tile index gv): 16 coordinates of every plane over
+      // blocks 4·vhalf .. 4·vhalf + 3.  A short tile's upper blocks hold stale
+      // words with zero weights.
       auto values_step = [&](int kv, int64_t gv) {
         const uint8_t* stg = smem + Sh::kOffRing + (int)(gv & (kStages - 1)) * Sh::kStage;
         const uint32_t* vi = reinterpret_cast<const uint32_t*>(stg + Sh::kOffVIdx);
@@ -459,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
             for (int e = 0; e < 4; ++e) vacc[P][ht][e] *= pend[ht];
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
+        for (int i = 0; i < kBlocks / 2; ++i) {
+          const int kb = (kBlocks / 2) * vhalf + i;
           uint2 bb[2][GH][2];  // [part][head tile][K half]
 #pragma unroll
           for (int part = 0; part < 2; ++part)
@@ -468,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
               for (int s2i = 0; s2i < 2; ++s2i)
                 bb[part][ht][s2i] = *reinterpret_cast<const uint2*>(
-                    bv + (((((part * GH + ht) * 8 + kb) * 2 + s2i) * 8 + gq) * 4 + tig) * 2);
+                    bv + (((((part * GH + ht) * kBlocks + kb) * 2 + s2i) * 8 + gq) * 4 + tig) * 2);
 #pragma unroll
           for (int P = 0; P < NP; ++P) {
             uint2 ww;
@@ -497,55 +490,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         }
       };
 
-      // scores of tile kc (CTA tile index gc, stage already landed): block w,
-      // two groups of 16 tokens -> s2c, cleaned norms, and the tile maximum
+      // scores of tile kc (CTA tile index gc, stage already landed): 16 tokens
+      // -> s2c, cleaned norms, and the tile maximum
       auto scores_step = [&](int kc, int64_t gc) {
         const uint8_t* stg = smem + Sh::kOffRing + (int)(gc & (kStages - 1)) * Sh::kStage;
         const uint4* kq = reinterpret_cast<const uint4*>(stg + Sh::kOffKIdx);  // token t, plane P: kq[t·W + P]
         const uint4* sq = reinterpret_cast<const uint4*>(stg + Sh::kOffKSgn);  // token t: sq[t]
-        float acc[2][2][GH][4];  // [group][part][head tile][fragment]
+        float acc[2][GH][4];  // [part][head tile][fragment]
 #pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2)
+        for (int pt = 0; pt < 2; ++pt)
 #pragma unroll
-          for (int pt = 0; pt < 2; ++pt)
+          for (int ht = 0; ht < GH; ++ht)
 #pragma unroll
-            for (int ht = 0; ht < GH; ++ht)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) acc[g2][pt][ht][e] = 0.f;
+            for (int e = 0; e < 4; ++e) acc[pt][ht][e] = 0.f;
 #pragma unroll
         for (int P = 0; P < NP; ++P) {
           const int part = P < NPM ? 0 : 1;
-          uint4 wd[2][2];  // [group][row]
+          uint4 wd[2];  // [row]
 #pragma unroll
-          for (int g2 = 0; g2 < 2; ++g2)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int t = tok + 16 * g2 + r;
-              if (P < W) {
-                wd[g2][r] = kq[t * W + P];
-              } else if (P < NPM) {  // product plane b0 ^ b1 ^ b2
-                const uint4 x0 = kq[t * W], x1 = kq[t * W + 1 % W], x2 = kq[t * W + 2 % W];
-                wd[g2][r] =
-                    make_uint4(x0.x ^ x1.x ^ x2.x, x0.y ^ x1.y ^ x2.y, x0.z ^ x1.z ^ x2.z, x0.w ^ x1.w ^ x2.w);
-              } else {
-                wd[g2][r] = sq[t];
-              }
+          for (int r = 0; r < 2; ++r) {
+            const int t = tok + r;
+            if (P < W) {
+              wd[r] = kq[t * W + P];
+            } else if (P < NPM) {  // product plane b0 ^ b1 ^ b2
+              const uint4 x0 = kq[t * W], x1 = kq[t * W + 1 % W], x2 = kq[t * W + 2 % W];
+              wd[r] = make_uint4(x0.x ^ x1.x ^ x2.x, x0.y ^ x1.y ^ x2.y, x0.z ^ x1.z ^ x2.z, x0.w ^ x1.w ^ x2.w);
+            } else {
+              wd[r] = sq[t];
             }
+          }
 #pragma unroll
           for (int kw = 0; kw < 4; ++kw) {
             const int ks = (P * 4 + kw) * 2;
+            const uint32_t x0 = word_of(wd[0], kw), x1 = word_of(wd[1], kw);
+            const uint32_t t0 = x0 * mul, t1 = x1 * mul;    // layers 8+q, 12+q at bits 11, 15
+            const uint32_t u0 = x0 * mul8, u1 = x1 * mul8;  // layers q, 4+q at bits 11, 15
 #pragma unroll
-            for (int g2 = 0; g2 < 2; ++g2) {
-              const uint32_t x0 = word_of(wd[g2][0], kw), x1 = word_of(wd[g2][1], kw);
-              const uint32_t t0 = x0 * mul, t1 = x1 * mul;    // layers 8+q, 12+q at bits 11, 15
-              const uint32_t u0 = x0 * mul8, u1 = x1 * mul8;  // layers q, 4+q at bits 11, 15
-#pragma unroll
-              for (int ht = 0; ht < GH; ++ht) {
-                mma_f16(acc[g2][part][ht], op.expo(u0), op.expo(u1), op.sign(u0), op.sign(u1), bfrag(ks, ht, 0),
-                        bfrag(ks, ht, 1));
-                mma_f16(acc[g2][part][ht], op.expo(t0), op.expo(t1), op.sign(t0), op.sign(t1),
-                        bfrag(ks + 1, ht, 0), bfrag(ks + 1, ht, 1));
-              }
+            for (int ht = 0; ht < GH; ++ht) {
+              const uint2 b0 = bfrag(ks, ht), b1 = bfrag(ks + 1, ht);
+              mma_f16(acc[part][ht], op.expo(u0), op.expo(u1), op.sign(u0), op.sign(u1), b0.x, b0.y);
+              mma_f16(acc[part][ht], op.expo(t0), op.expo(t1), op.sign(t0), op.sign(t1), b1.x, b1.y);
             }
           }
         }
@@ -554,28 +538,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         const float* vn = reinterpret_cast<const float*>(stg + Sh::kOffVNorm);
         const float* vr = reinterpret_cast<const float*>(stg + Sh::kOffVRn);
         const int64_t tb = (sg.t0 + kc) * kTile;
+        const float2 kn2 = *reinterpret_cast<const float2*>(kn + tok), kr2 = *reinterpret_cast<const float2*>(kr + tok);
+        const float2 vn2 = *reinterpret_cast<const float2*>(vn + tok), vr2 = *reinterpret_cast<const float2*>(vr + tok);
 #pragma unroll
         for (int hh = 0; hh < GH; ++hh) mx[hh] = -INFINITY;
 #pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2) {
-          const int t = tok + 16 * g2;
-          const float2 kn2 = *reinterpret_cast<const float2*>(kn + t), kr2 = *reinterpret_cast<const float2*>(kr + t);
-          const float2 vn2 = *reinterpret_cast<const float2*>(vn + t), vr2 = *reinterpret_cast<const float2*>(vr + t);
+        for (int r = 0; r < 2; ++r) {
+          const bool valid = tb + tok + r < sg.L;
+          vnc[r] = valid ? (r ? vn2.y : vn2.x) : 0.f;
+          vrc[r] = valid ? (r ? vr2.y : vr2.x) : 0.f;
+          const float knr = r ? kn2.y : kn2.x, krr = r ? kr2.y : kr2.x;
+          const float lv = __log2f(fmaxf(fmaxf(vnc[r], vrc[r]), 0x1p-32f));
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const bool valid = tb + t + r < sg.L;
-            vnc[g2][r] = valid ? (r ? vn2.y : vn2.x) : 0.f;
-            vrc[g2][r] = valid ? (r ? vr2.y : vr2.x) : 0.f;
-            const float knr = r ? kn2.y : kn2.x, krr = r ? kr2.y : kr2.x;
-            const float lv = __log2f(fmaxf(fmaxf(vnc[g2][r], vrc[g2][r]), 0x1p-32f));
-#pragma unroll
-            for (int hh = 0; hh < GH; ++hh) {
-              const float dm = acc[g2][0][hh][2 * r] + acc[g2][0][hh][2 * r + 1];
-              const float dq = acc[g2][1][hh][2 * r] + acc[g2][1][hh][2 * r + 1];
-              const float sc = fmaf(knr, fmaf(A0[hh], dm, B0[hh]), krr * fmaf(A1[hh], dq, B1[hh]));
-              s2c[hh][g2][r] = (valid && 4 * hh + tig < a.G) ? sc : -INFINITY;
-              mx[hh] = fmaxf(mx[hh], s2c[hh][g2][r] + lv);
-            }
+          for (int hh = 0; hh < GH; ++hh) {
+            const float dm = acc[0][hh][2 * r] + acc[0][hh][2 * r + 1];
+            const float dq = acc[1][hh][2 * r] + acc[1][hh][2 * r + 1];
+            const float sc = fmaf(knr, fmaf(A0[hh], dm, B0[hh]), krr * fmaf(A1[hh], dq, B1[hh]));
+            s2c[hh][r] = (valid && 4 * hh + tig < a.G) ? sc : -INFINITY;
+            mx[hh] = fmaxf(mx[hh], s2c[hh][r] + lv);
           }
         }
 #pragma unroll
@@ -618,15 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           }
         }
 #pragma unroll
-        for (int hh = 0; hh < GH; ++hh) {
-          pend[hh] = fac[hh];
+        for (int hh = 0; hh < GH; ++hh) pend[hh] = fac[hh], s2p[hh][0] = s2c[hh][0], s2p[hh][1] = s2c[hh][1];
 #pragma unroll
-          for (int g2 = 0; g2 < 2; ++g2) s2p[hh][g2][0] = s2c[hh][g2][0], s2p[hh][g2][1] = s2c[hh][g2][1];
-        }
-#pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2)
-#pragma unroll
-          for (int r = 0; r < 2; ++r) vnp[g2][r] = vnc[g2][r], vrp[g2][r] = vrc[g2][r];
+        for (int r = 0; r < 2; ++r) vnp[r] = vnc[r], vrp[r] = vrc[r];
       };
 
       // prologue: scores of the first tile
@@ -659,36 +633,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
       if (gq == 0) ms->lred[sp][w][4 * hh + tig] = l;
     }
-    cta_sync();
     float cf[NPM];
 #pragma unroll
     for (int P = 0; P < NPM; ++P) cf[P] = __ldg(a.walsh + (P < W ? (1 << P) : 7));
+    // fragment e = 2·row + piece; the value operand is -s, so sums enter negated
+    float rot[GH][2], sgn[GH][2];
 #pragma unroll
-    for (int hh = 0; hh < GH; ++hh) {
-      const int head = 4 * hh + tig;
-      if (head < a.G) {
-        float* pp = a.part + ((size_t)(head0 + head) * a.smax + sg.slot) * (2 + 2 * kD);
-        // fragment e = 2·row + piece; the value operand is -s, so sums enter negated
-        float rot[2], sgn[2];
+    for (int hh = 0; hh < GH; ++hh)
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float x = 0.f;
+      for (int r = 0; r < 2; ++r) {
+        float x = 0.f;
 #pragma unroll
-          for (int P = 0; P < NPM; ++P) x = fmaf(cf[P], vacc[P][hh][2 * r] + vacc[P][hh][2 * r + 1], x);
-          rot[r] = -x * (1.f / kWS);
-          sgn[r] = -(vacc[NPM][hh][2 * r] + vacc[NPM][hh][2 * r + 1]) * (1.f / kWS);
-        }
-        *reinterpret_cast<float2*>(pp + 2 + crd) = make_float2(rot[0], rot[1]);
-        *reinterpret_cast<float2*>(pp + 2 + kD + crd) = make_float2(sgn[0], sgn[1]);
-        if (w == 0 && gq == 0) {
-          float l = 0.f;
+        for (int P = 0; P < NPM; ++P) x = fmaf(cf[P], vacc[P][hh][2 * r] + vacc[P][hh][2 * r + 1], x);
+        rot[hh][r] = -x * (1.f / kWS);
+        sgn[hh][r] = -(vacc[NPM][hh][2 * r] + vacc[NPM][hh][2 * r + 1]) * (1.f / kWS);
+      }
+    // the upper block half hands its sums over through the (now idle) weight buffers
+    float* xs = reinterpret_cast<float*>(smem + Sh::kOffBV);  // [head 8][rot, sgn][128]
+    if (vhalf == 1) {
 #pragma unroll
-          for (int q = 0; q < kNW; ++q) l += ms->lred[sp][q][head];
-          pp[0] = M[hh];
-          pp[1] = l;
+      for (int hh = 0; hh < GH; ++hh) {
+        const int head = 4 * hh + tig;
+        *reinterpret_cast<float2*>(xs + (head * 2) * kD + crd) = make_float2(rot[hh][0], rot[hh][1]);
+        *reinterpret_cast<float2*>(xs + (head * 2 + 1) * kD + crd) = make_float2(sgn[hh][0], sgn[hh][1]);
+      }
+    }
+    cta_sync();
+    if (vhalf == 0) {
+#pragma unroll
+      for (int hh = 0; hh < GH; ++hh) {
+        const int head = 4 * hh + tig;
+        if (head < a.G) {
+          float* pp = a.part + ((size_t)(head0 + head) * a.smax + sg.slot) * (2 + 2 * kD);
+          const float2 ro = *reinterpret_cast<const float2*>(xs + (head * 2) * kD + crd);
+          const float2 so = *reinterpret_cast<const float2*>(xs + (head * 2 + 1) * kD + crd);
+          *reinterpret_cast<float2*>(pp + 2 + crd) = make_float2(rot[hh][0] + ro.x, rot[hh][1] + ro.y);
+          *reinterpret_cast<float2*>(pp + 2 + kD + crd) = make_float2(sgn[hh][0] + so.x, sgn[hh][1] + so.y);
+          if (w == 0 && gq == 0) {
+            float l = 0.f;
+#pragma unroll
+            for (int q = 0; q < kNW; ++q) l += ms->lred[sp][q][head];
+            pp[0] = M[hh];
+            pp[1] = l;
+          }
         }
       }
     }
+    cta_sync();  // the scratch is free again before the next unit
   }
   // no copy of this CTA may be in flight when it exits
   if (threadIdx.x == 0)
