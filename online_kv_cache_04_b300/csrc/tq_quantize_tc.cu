@@ -266,32 +266,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&bars->x_empty[s]));
       if (!mbar_wait(smem_u32(&bars->u_full[s]), ph, a.fault, kFaultWait)) break;
       tc_fence_after();
-      const float inv = n > 0.f ? 1.0f / n : 0.f;
+      const float inv = n > 0.f ? 1.0f / n : 0.f, nlive = n > 0.f ? -1.f : 0.f;
       uint32_t planes[W][4];
       float rsq = 0.f;
-#pragma unroll
-      for (int p = 0; p < W; ++p)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) planes[p][c] = 0u;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 16 coordinates per step
-        uint32_t v[16];
-        tmem_ld16(acc + 16 * c, v);
+      // 32 coordinates (one word of every index plane) per TMEM load
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(acc + 32 * c, v);
         tmem_ld_wait();
-        uint32_t hi[8], lo[8];
+        uint32_t pw[W], hi[16], lo[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int p = 0; p < W; ++p) pw[p] = 0u;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
           float rho2[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const float u = __uint_as_float(v[2 * j + e]) * inv;
-            const int idx = bucket<W>(u, bnd);
-            const float rho = n > 0.f ? u - centroid<W>(idx, cent) : 0.f;
+            // bucket predicates against the sorted bounds (idx = how many lie below u)
+            bool pk[(1 << W) - 1];
+#pragma unroll
+            for (int k = 0; k < (1 << W) - 1; ++k) pk[k] = bnd[k] < u;
+            float cv = cent[0];
+#pragma unroll
+            for (int k = 0; k < (1 << W) - 1; ++k) cv = pk[k] ? cent[k + 1] : cv;
+            // index bits from the predicate prefix: bit q of idx
+            bool bq[W];
+            if constexpr (W == 1) {
+              bq[0] = pk[0];
+            } else if constexpr (W == 2) {
+              bq[0] = pk[0] ^ pk[1] ^ pk[2];
+              bq[1] = pk[1];
+            } else {
+              bq[0] = pk[0] ^ pk[1] ^ pk[2] ^ pk[3] ^ pk[4] ^ pk[5] ^ pk[6];
+              bq[1] = pk[1] ^ pk[3] ^ pk[5];
+              bq[2] = pk[3];
+            }
+            const uint32_t bit = 1u << (2 * j + e);
+#pragma unroll
+            for (int p = 0; p < W; ++p)
+              if (bq[p]) pw[p] |= bit;
+            const float rho = fmaf(cv, nlive, u);  // u - c[idx], and 0 for a zero vector
             rsq = fmaf(rho, rho, rsq);
             rho2[e] = rho;
-            const int bit = 16 * (c & 1) + 2 * j + e;
-#pragma unroll
-            for (int p = 0; p < W; ++p) planes[p][c >> 1] |= static_cast<uint32_t>((idx >> p) & 1) << bit;
           }
           const __nv_bfloat162 h = __floats2bfloat162_rn(rho2[0], rho2[1]);
           const float2 hf = __bfloat1622float2(h);
@@ -299,8 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi[j] = *reinterpret_cast<const uint32_t*>(&h);
           lo[j] = *reinterpret_cast<const uint32_t*>(&l);
         }
-        tmem_st8(acc + 128 + 8 * c, hi);
-        tmem_st8(acc + 192 + 8 * c, lo);
+        tmem_st16(acc + 128 + 16 * c, hi);
+        tmem_st16(acc + 192 + 16 * c, lo);
+#pragma unroll
+        for (int p = 0; p < W; ++p) {
+          // chunk c is word c of each plane (rolled loop: select by value)
+          planes[p][0] = c == 0 ? pw[p] : planes[p][0];
+          planes[p][1] = c == 1 ? pw[p] : planes[p][1];
+          planes[p][2] = c == 2 ? pw[p] : planes[p][2];
+          planes[p][3] = c == 3 ? pw[p] : planes[p][3];
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -324,15 +350,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!mbar_wait(smem_u32(&bars->p_full[s]), ph, a.fault, kFaultWait)) break;
       tc_fence_after();
-      uint32_t sg[4] = {0u, 0u, 0u, 0u};
+      uint32_t sg[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[16];
-        tmem_ld16(acc + 16 * c, v);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(acc + 32 * c, v);
         tmem_ld_wait();
+        uint32_t wsg = 0u;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          sg[c >> 1] |= static_cast<uint32_t>(__uint_as_float(v[j]) >= 0.f) << (16 * (c & 1) + j);
+        for (int j = 0; j < 32; ++j)
+          if (__uint_as_float(v[j]) >= 0.f) wsg |= 1u << j;
+        sg[c] = wsg;
       }
       tc_fence_before();
       __syncwarp();
