@@ -78,31 +78,59 @@ bool supported(const DecodeShape& s) {
 }
 
 // ---------------------------------------------------------------- prep
+// out[r] = Σ_{c<k} A[r·lda + c]·x[c] for r < n (A row-major, rows contiguous),
+// by all warps of the block: a warp takes 16 rows at once, each lane reads
+// 4 consecutive columns of each row with one 128-bit load (all 16 loads in
+// flight together), and the 16 dot products are reduced across the warp.
+// x and out live in shared memory, 16-byte aligned; k is a multiple of 4 and
+// lda of 4.  Ends with the block synchronised.
+__device__ __forceinline__ void block_rowdot(const float* __restrict__ A, int lda, int n, int k, const float* x,
+                                             float* out) {
+  constexpr int R = 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int r0 = warp * R; r0 < n; r0 += nw * R) {
+    float acc[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q) acc[q] = 0.f;
+    for (int c = 4 * lane; c < k; c += 128) {
+      const float4 xv = *reinterpret_cast<const float4*>(x + c);
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        if (r0 + q < n) {
+          const float4 av = __ldg(reinterpret_cast<const float4*>(A + (size_t)(r0 + q) * lda + c));
+          acc[q] = fmaf(av.x, xv.x, fmaf(av.y, xv.y, fmaf(av.z, xv.z, fmaf(av.w, xv.w, acc[q]))));
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      float v = acc[q];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && r0 + q < n) out[r0 + q] = v;
+    }
+  }
+  __syncthreads();
+}
+
 template <typename T>
-__global__ void __launch_bounds__(256) prep_kernel(const T* __restrict__ q, const float* __restrict__ pi_t,
-                                                   const float* __restrict__ s_rot_t, int d, int m,
+__global__ void __launch_bounds__(256) prep_kernel(const T* __restrict__ q, const float* __restrict__ pi,
+                                                   const float* __restrict__ s_rot, int d, int m,
                                                    float* __restrict__ qt, float* __restrict__ st) {
   extern __shared__ float sm[];
-  float* qs = sm;       // [d]
-  float* qr = sm + d;   // [d]
+  float* qs = sm;           // [d]
+  float* qr = qs + d;       // [d]   Π q
+  float* sr = qr + d;       // [m]   S q = (S Πᵀ) Π q
   const int head = blockIdx.x;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     if constexpr (sizeof(T) == 2) qs[i] = __bfloat162float(q[(size_t)head * d + i]);
     else qs[i] = q[(size_t)head * d + i];
   }
   __syncthreads();
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
-    float a = 0.0f;
-    for (int i = 0; i < d; ++i) a = fmaf(__ldg(pi_t + (size_t)i * d + j), qs[i], a);
-    qr[j] = a;
-    qt[(size_t)head * d + j] = a;
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < m; j += blockDim.x) {
-    float a = 0.0f;
-    for (int i = 0; i < d; ++i) a = fmaf(__ldg(s_rot_t + (size_t)i * m + j), qr[i], a);
-    st[(size_t)head * m + j] = a;
-  }
+  block_rowdot(pi, d, d, d, qs, qr);  // row j of Π
+  for (int j = threadIdx.x; j < d; j += blockDim.x) qt[(size_t)head * d + j] = qr[j];
+  block_rowdot(s_rot, d, m, d, qr, sr);  // row i of S Πᵀ
+  for (int j = threadIdx.x; j < m; j += blockDim.x) st[(size_t)head * m + j] = sr[j];
 }
 
 struct SplitArgs {
@@ -316,8 +344,8 @@ struct CombineArgs {
   int slots;              // partial slots per head (stride); 0: the general path's nsplit
   int64_t tpu, ctas;      // tensor-core path: per-unit slot count from its tile partition
   const float* part;
-  const float* pi;        // [d][d] Π
-  const float* s_rot;     // [m][d] S Πᵀ
+  const float* pi_t;      // [d][d] Πᵀ
+  const float* s_rot_t;   // [d][m] (S Πᵀ)ᵀ
   float alpha;
   float* out;             // [B*Hq][d]
 };
@@ -337,7 +365,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   }
   float* acc = sm;              // [d + m]
   float* y = acc + d + m;       // [d]
-  float* wgt = y + d;           // [ns]
+  float* o = y + d;             // [d]
+  float* wgt = o + d;           // [ns]
   __shared__ float lsum;
   const float* pp = a.part + (size_t)head * pitch * stride;
   if (threadIdx.x == 0) {
@@ -361,19 +390,13 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   }
   __syncthreads();
   // y = acc_rot + α (S Πᵀ)ᵀ acc_sgn
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
-    float v = 0.0f;
-    for (int i = 0; i < m; ++i) v = fmaf(__ldg(a.s_rot + (size_t)i * d + j), acc[d + i], v);
-    y[j] = fmaf(a.alpha, v, acc[j]);
-  }
+  block_rowdot(a.s_rot_t, m, d, m, acc + d, y);  // row j of (S Πᵀ)ᵀ
+  for (int j = threadIdx.x; j < d; j += blockDim.x) y[j] = fmaf(a.alpha, y[j], acc[j]);
   __syncthreads();
   // o = Πᵀ y / l
+  block_rowdot(a.pi_t, d, d, d, y, o);  // row i of Πᵀ
   const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = 0.0f;
-    for (int j = 0; j < d; ++j) v = fmaf(__ldg(a.pi + (size_t)j * d + i), y[j], v);
-    a.out[(size_t)head * d + i] = v * inv;
-  }
+  for (int i = threadIdx.x; i < d; i += blockDim.x) a.out[(size_t)head * d + i] = o[i] * inv;
 }
 
 tq_status check_common(const tq_plan* plan, const void* q, tq_dtype qd, const tq_records* K, const int32_t* ctx_len,
@@ -402,13 +425,13 @@ size_t split_smem(const DecodeShape& s) {
 
 tq_status tq::launch_query_prep(const tq_plan* plan, const void* q, tq_dtype qd, int nheads, float* qt, float* st,
                                 cudaStream_t stream) {
-  const size_t smem = sizeof(float) * 2 * plan->d;
+  const size_t smem = sizeof(float) * (2 * plan->d + plan->m);
   if (qd == TQ_F32)
-    prep_kernel<float><<<nheads, 256, smem, stream>>>(static_cast<const float*>(q), plan->pi_t, plan->s_rot_t,
+    prep_kernel<float><<<nheads, 256, smem, stream>>>(static_cast<const float*>(q), plan->pi, plan->s_rot,
                                                       plan->d, plan->m, qt, st);
   else
-    prep_kernel<__nv_bfloat16><<<nheads, 256, smem, stream>>>(static_cast<const __nv_bfloat16*>(q), plan->pi_t,
-                                                              plan->s_rot_t, plan->d, plan->m, qt, st);
+    prep_kernel<__nv_bfloat16><<<nheads, 256, smem, stream>>>(static_cast<const __nv_bfloat16*>(q), plan->pi,
+                                                              plan->s_rot, plan->d, plan->m, qt, st);
   return tq::launch_status();
 }
 
@@ -449,11 +472,11 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
     c.tpu = tq::decode_tc_tpu(ctx_stride);
     c.ctas = tq::decode_tc_ctas(int64_t(B) * Hkv, c.tpu);
     c.part = part;
-    c.pi = plan->pi;
-    c.s_rot = plan->s_rot;
+    c.pi_t = plan->pi_t;
+    c.s_rot_t = plan->s_rot_t;
     c.alpha = plan->qjl_alpha;
     c.out = out;
-    combine_kernel<<<B * Hq, 256, sizeof(float) * (2 * s.d + s.m + slots), cs>>>(c);
+    combine_kernel<<<B * Hq, 256, sizeof(float) * (3 * s.d + s.m + slots), cs>>>(c);
     return tq::launch_status();
   }
   SplitArgs a{};
@@ -476,11 +499,11 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
   CombineArgs c{};
   c.s = s;
   c.part = part;
-  c.pi = plan->pi;
-  c.s_rot = plan->s_rot;
+  c.pi_t = plan->pi_t;
+  c.s_rot_t = plan->s_rot_t;
   c.alpha = plan->qjl_alpha;
   c.out = out;
-  combine_kernel<<<B * Hq, 256, sizeof(float) * (2 * s.d + s.m + s.nsplit), cs>>>(c);
+  combine_kernel<<<B * Hq, 256, sizeof(float) * (3 * s.d + s.m + s.nsplit), cs>>>(c);
   return tq::launch_status();
 }
 

@@ -4,7 +4,8 @@
 // Per tile of 128 vectors (one CTA per SM, persistent over tiles):
 //   TMA        x tile (bf16, 128-byte swizzle) -> shared memory, 2 stages
 //   GEMM1      U = x Πᵀ as x·Π_hiᵀ + x·Π_loᵀ (Π split into two bf16 terms;
-//              bf16 x is exact), fp32 accumulator in TMEM
+//              bf16 x is exact): one N = 256 product per K-step against the
+//              stacked [Π_hi; Π_lo], the two fp32 halves summed by epilogue 1
 //   epilogue 1 n = ||x|| from the staged tile, u = U / n, bucketize against
 //              the Lloyd-Max bounds -> index bit-planes, ρ = u - c[idx],
 //              ||ρ||², ρ split into bf16 hi + lo written back to TMEM
@@ -34,12 +35,14 @@ using namespace tq::sm100;
 constexpr int kTile = 128;                       // vectors per tile (MMA M)
 constexpr int kBoxBytes = 64 * 128 * 2;          // TMA box: 64 bf16 columns x 128 rows
 constexpr int kMatBytes = 2 * kBoxBytes;         // one 128 x 128 bf16 operand
-constexpr int kOffPiHi = 0, kOffPiLo = kMatBytes, kOffSHi = 2 * kMatBytes, kOffSLo = 3 * kMatBytes;
+// Π_hi and Π_lo stacked per 64-column box ([box][hi, lo] x 128 rows): one N = 256
+// operand, so GEMM1 is one product per K-step
+constexpr int kOffPi = 0, kOffSHi = 2 * kMatBytes, kOffSLo = 3 * kMatBytes;
 constexpr int kOffX = 4 * kMatBytes;             // two x stages
 constexpr int kOffBar = kOffX + 2 * kMatBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024; // barriers + alignment slack
 constexpr int kThreads = 320, kMmaWarp = 8, kTmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;              // slot s: acc [256s, +128), rho_hi [+128, +64), rho_lo [+192, +64)
+constexpr uint32_t kTmemCols = 512;              // slot s: [256s, +256) = U_hi | U_lo, then P | ρ chunks [hi 16 | lo 16]
 
 constexpr unsigned kFaultWait = 1u;              // fault bit: a pipeline wait ran out of its bound
 
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bfull, 4 * kMatBytes);
       for (int mat = 0; mat < 2; ++mat)
         for (int h = 0; h < 2; ++h) {
-          tma_load_2d(base + kOffPiHi + mat * kMatBytes + h * kBoxBytes, &tm_pi, h * 64, mat * 128, bfull);
+          tma_load_2d(base + kOffPi + (2 * h + mat) * kBoxBytes, &tm_pi, h * 64, mat * 128, bfull);
           tma_load_2d(base + kOffSHi + mat * kMatBytes + h * kBoxBytes, &tm_s, h * 64, mat * 128, bfull);
         }
       int it = 0, last_k[2] = {-1, -1};
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128), idesc256 = idesc_bf16_f32(128, 256);
       bool ok = mbar_wait(smem_u32(&bars->b_full), 0, a.fault, kFaultWait);
       tc_fence_after();
       auto gemm2 = [&](int j) {
@@ -192,12 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // terms (ρ_hi, S_hi), (ρ_hi, S_lo), (ρ_lo, S_hi)
 #pragma unroll 1
         for (int t = 0; t < 3; ++t) {
-          const uint32_t rho = acc + (t == 2 ? 192 : 128);
           const uint64_t sd = desc_sw128(base + (t == 1 ? kOffSLo : kOffSHi));
 #pragma unroll 1
           for (int kk = 0; kk < 8; ++kk) {
+            // K-step kk: ρ pieces of coordinates 16kk.. sit in chunk kk/2 = [hi 16 | lo 16] columns
+            const uint32_t rho = acc + 128 + 32 * (kk >> 1) + 8 * (kk & 1) + (t == 2 ? 16 : 0);
             const uint32_t boff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;  // start address advances in 16 B units
-            mma_ts(acc, rho + kk * 8, sd + (boff >> 4), idesc, (t | kk) != 0);
+            mma_ts(acc, rho, sd + (boff >> 4), idesc, (t | kk) != 0);
           }
         }
         mma_commit(smem_u32(&bars->p_full[s]));
@@ -212,14 +216,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc = tmem + 256 * s;
         const uint32_t xa = base + kOffX + s * kMatBytes;
         const uint64_t xd = desc_sw128(xa);
+        // U_hi | U_lo = x·[Π_hi; Π_lo]ᵀ in 256 accumulator columns (summed by the epilogue)
+        const uint64_t pd = desc_sw128(base + kOffPi);
 #pragma unroll 1
-        for (int term = 0; term < 2; ++term) {
-          const uint64_t pd = desc_sw128(base + (term ? kOffPiLo : kOffPiHi));
-#pragma unroll 1
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(acc, xd + off, pd + off, idesc, (term | kk) != 0);
-          }
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t offa = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          const uint32_t offb = ((kk >> 2) * 2 * kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(acc, xd + offa, pd + offb, idesc256, kk != 0);
         }
         mma_commit(smem_u32(&bars->u_full[s]));
         mma_commit(smem_u32(&bars->x_empty[s]));
@@ -272,8 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 32 coordinates (one word of every index plane) per TMEM load
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
+        uint32_t v[32], vl[32];
         tmem_ld32(acc + 32 * c, v);
+        tmem_ld32(acc + 128 + 32 * c, vl);
         tmem_ld_wait();
         uint32_t pw[W], hi[16], lo[16];
 #pragma unroll
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float rho2[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float u = __uint_as_float(v[2 * j + e]) * inv;
+            const float u = (__uint_as_float(v[2 * j + e]) + __uint_as_float(vl[2 * j + e])) * inv;
             // bucket predicates against the sorted bounds (idx = how many lie below u)
             bool pk[(1 << W) - 1];
 #pragma unroll
@@ -317,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi[j] = *reinterpret_cast<const uint32_t*>(&h);
           lo[j] = *reinterpret_cast<const uint32_t*>(&l);
         }
-        tmem_st16(acc + 128 + 16 * c, hi);
-        tmem_st16(acc + 192 + 16 * c, lo);
+        // into the columns of U_lo just read: chunk c = [hi 16 | lo 16]
+        tmem_st16(acc + 128 + 32 * c, hi);
+        tmem_st16(acc + 128 + 32 * c + 16, lo);
 #pragma unroll
         for (int p = 0; p < W; ++p) {
           // chunk c is word c of each plane (rolled loop: select by value)
