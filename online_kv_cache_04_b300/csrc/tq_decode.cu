@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     const int b = head / a.s.Hq, hq = head - b * a.s.Hq;
     const int64_t u = int64_t(b) * a.s.Hkv + hq / a.s.G, T = int64_t(a.s.B) * a.s.Hkv * a.tpu;
     const int64_t first = ((u * a.tpu + 1) * a.ctas - 1) / T, last = (((u + 1) * a.tpu) * a.ctas - 1) / T;
-    ns = (int)(last - first + 1);
+    ns = 2 * (int)(last - first + 1);  // the tensor-core kernel writes one partial per half of each CTA
     pitch = a.slots;
   }
   float* acc = sm;              // [d + m]

@@ -123,14 +123,18 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// Named barrier of all warps, and the same barrier with an OR vote.
-__device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
-__device__ __forceinline__ bool cta_any(bool p) {
+// Named barriers: all warps (id 3), and the warps of one half h (id 1 + h),
+// plain or with an OR vote.
+__device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 3, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ void half_sync(int h) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + h), "n"(kThreads / 2) : "memory");
+}
+__device__ __forceinline__ bool half_any(int h, bool p) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred q, o;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred o, 1, %2, q;\n selp.u32 %0, 1, 0, o;\n}"
+      "{\n .reg .pred q, o;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred o, %2, %3, q;\n selp.u32 %0, 1, 0, o;\n}"
       : "=r"(r)
-      : "r"((uint32_t)p), "n"(kThreads)
+      : "r"((uint32_t)p), "r"(1 + h), "n"(kThreads / 2)
       : "memory");
   return r != 0;
 }
@@ -187,7 +191,7 @@ struct Shape {
 };
 
 struct Misc {
-  uint64_t ld_full[kStages];
+  uint64_t ld_full[kStages], ld_empty[kStages];  // empty: one arrival per half
   int abort;
   float red[kNW][8];          // per-warp tile maxima (reference moves only)
   float amax[2][8];           // per-unit query weight maxima (as non-negative float bits)
@@ -202,7 +206,6 @@ constexpr int smem_bytes() {
   return 1024 + Shape<W, 8>::kOffMisc + kMiscBytes;
 }
 static_assert(smem_bytes<3>() <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
-static_assert(2 * Shape<1, 4>::kBVBuf >= 8 * 2 * kD * 4, "weight buffers double as the end-of-unit scratch");
 
 // Segment of this CTA's tile range that falls in one unit.
 struct Seg {
@@ -242,7 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   const int64_t f0 = (int64_t)blockIdx.x * a.total / C, f1 = ((int64_t)blockIdx.x + 1) * a.total / C;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&ms->ld_full[s]), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&ms->ld_full[s]), 1);
+      mbar_init(smem_u32(&ms->ld_empty[s]), 2);
+    }
     ms->abort = 0;
     fence_mbar_init();
   }
@@ -275,6 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       ++cur;
       ++ct;
       const int s = (int)(issued & (kStages - 1));
+      // the other half may still be reading the stage's previous tile
+      if (issued >= kStages)
+        wait(&ms->ld_empty[s], (uint32_t)(((issued - kStages) / kStages) & 1));
       ++issued;
       const uint32_t bar = smem_u32(&ms->ld_full[s]);
       const uint32_t dst = sbase + Sh::kOffRing + s * Sh::kStage;
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   };
   if (threadIdx.x == 0) issue_upto(0);
 
-  const int w = warp, kbk = w >> 1, g2 = w & 1, vrow = w & 7, vhalf = w >> 3;
+  const int w = warp, kbk = w >> 1, g2 = w & 1, vrow = w & 7, hf = w >> 3;
   // Score rows gq, gq + 8 <-> tokens tok, tok + 1 of the tile (block kbk).
   // Their value bits are bits L and 16 + L of the block words, L = 8·g2 + gq,
   // i.e. one f16x2 operand register: this thread writes whole registers of
@@ -323,7 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
     for (int hh = 0; hh < GH; ++hh) M[hh] = -INFINITY, lsum[hh] = 0.f, pend[hh] = 1.f;
     if (sg.n > 0) {
-      // ---- query weights of this unit (f16 hi + lo, scale E per part and head) and offsets O
+      // ---- query weights of this unit (f16 hi + lo, scale E per part and head) and offsets O;
+      // both halves must be done with the previous unit's table first
+      cta_sync();
       for (int e = threadIdx.x; e < Sh::kBKBytes / 16; e += kThreads)
         reinterpret_cast<uint4*>(BK)[e] = make_uint4(0, 0, 0, 0);
       if (threadIdx.x < 16) {
@@ -436,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       };
 
       // values of tile kv (CTA tile index gv): 16 coordinates of every plane over
-      // blocks 4·vhalf .. 4·vhalf + 3.  A short tile's upper blocks hold stale
+      // blocks 4·hf .. 4·hf + 3.  A short tile's upper blocks hold stale
       // words with zero weights.
       auto values_step = [&](int kv, int64_t gv) {
         const uint8_t* stg = smem + Sh::kOffRing + (int)(gv & (kStages - 1)) * Sh::kStage;
@@ -452,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             for (int e = 0; e < 4; ++e) vacc[P][ht][e] *= pend[ht];
 #pragma unroll
         for (int i = 0; i < kBlocks / 2; ++i) {
-          const int kb = (kBlocks / 2) * vhalf + i;
+          const int kb = (kBlocks / 2) * hf + i;
           uint2 bb[2][GH][2];  // [part][head tile][K half]
 #pragma unroll
           for (int part = 0; part < 2; ++part)
@@ -564,17 +575,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           for (int o = 4; o < 32; o <<= 1) mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], o));
       };
 
-      // Second barrier of a tile: the vote of the lazy reference on the scores
-      // just computed; `done` tiles are consumed, so their stages take the next
-      // bulk copies.  The scores and norms move to the "previous tile" slots.
-      auto vote_step = [&](bool have_scores, int64_t done) {
+      // Second barrier of a tile (this half's warps): the vote of the lazy
+      // reference on the scores just computed.  With have_values, this half is
+      // through tile done - 1, whose stage it hands back; thread 0 refills
+      // stages.  The scores and norms move to the "previous tile" slots.
+      auto vote_step = [&](bool have_scores, bool have_values, int64_t done) {
         bool exceed = false;
         if (have_scores) {
 #pragma unroll
           for (int hh = 0; hh < GH; ++hh)
             exceed |= M[hh] == -INFINITY ? mx[hh] > -INFINITY : mx[hh] > M[hh] + kTau;
         }
-        const bool bump = cta_any(exceed);
+        const bool bump = half_any(hf, exceed);
+        if (have_values && (threadIdx.x & (kThreads / 2 - 1)) == 0)
+          mbar_arrive(smem_u32(&ms->ld_empty[(done - 1) & (kStages - 1)]));
         if (threadIdx.x == 0) issue_upto(done);
         float fac[GH];
 #pragma unroll
@@ -584,12 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
             for (int hh = 0; hh < GH; ++hh) ms->red[w][4 * hh + tig] = mx[hh];
           }
-          cta_sync();
+          half_sync(hf);
 #pragma unroll
           for (int hh = 0; hh < GH; ++hh) {
-            float tm = ms->red[0][4 * hh + tig];
+            float tm = ms->red[8 * hf][4 * hh + tig];
 #pragma unroll
-            for (int q = 1; q < kNW; ++q) tm = fmaxf(tm, ms->red[q][4 * hh + tig]);
+            for (int q = 1; q < kNW / 2; ++q) tm = fmaxf(tm, ms->red[8 * hf + q][4 * hh + tig]);
             float nm = M[hh];
             if (M[hh] == -INFINITY || tm > M[hh] + kTau) nm = tm;
             fac[hh] = nm == M[hh] ? 1.f : exp2f(M[hh] - nm);
@@ -606,25 +620,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       // prologue: scores of the first tile
       wait(&ms->ld_full[gi & (kStages - 1)], (uint32_t)((gi / kStages) & 1));
       scores_step(0, gi);
-      vote_step(true, gi);
+      vote_step(true, false, gi);
       // steady state: the wait comes first so that values and scores form one block
       for (int k = 1; k < sg.n; ++k) {
         const int64_t g = gi + k;
         weights_step(k - 1);
-        cta_sync();
+        half_sync(hf);
         wait(&ms->ld_full[g & (kStages - 1)], (uint32_t)((g / kStages) & 1));
         values_step(k - 1, g - 1);
         scores_step(k, g);
-        vote_step(true, g);
+        vote_step(true, true, g);
       }
       // epilogue: weights and values of the last tile
       weights_step(sg.n - 1);
-      cta_sync();
+      half_sync(hf);
       values_step(sg.n - 1, gi + sg.n - 1);
-      vote_step(false, gi + sg.n);
+      vote_step(false, true, gi + sg.n);
       gi += sg.n;
     }
-    // ---- partial of this CTA for the unit
+    // ---- partials of this CTA for the unit: one per half (slot 2·slot + half),
+    // each over its own tokens with its own reference
     const int sp = segc & 1;
 #pragma unroll
     for (int hh = 0; hh < GH; ++hh) {
@@ -633,53 +648,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
       if (gq == 0) ms->lred[sp][w][4 * hh + tig] = l;
     }
+    half_sync(hf);
     float cf[NPM];
 #pragma unroll
     for (int P = 0; P < NPM; ++P) cf[P] = __ldg(a.walsh + (P < W ? (1 << P) : 7));
-    // fragment e = 2·row + piece; the value operand is -s, so sums enter negated
-    float rot[GH][2], sgn[GH][2];
 #pragma unroll
-    for (int hh = 0; hh < GH; ++hh)
+    for (int hh = 0; hh < GH; ++hh) {
+      const int head = 4 * hh + tig;
+      if (head < a.G) {
+        float* pp = a.part + ((size_t)(head0 + head) * a.smax + 2 * sg.slot + hf) * (2 + 2 * kD);
+        // fragment e = 2·row + piece; the value operand is -s, so sums enter negated
+        float rot[2], sgn[2];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float x = 0.f;
+        for (int r = 0; r < 2; ++r) {
+          float x = 0.f;
 #pragma unroll
-        for (int P = 0; P < NPM; ++P) x = fmaf(cf[P], vacc[P][hh][2 * r] + vacc[P][hh][2 * r + 1], x);
-        rot[hh][r] = -x * (1.f / kWS);
-        sgn[hh][r] = -(vacc[NPM][hh][2 * r] + vacc[NPM][hh][2 * r + 1]) * (1.f / kWS);
-      }
-    // the upper block half hands its sums over through the (now idle) weight buffers
-    float* xs = reinterpret_cast<float*>(smem + Sh::kOffBV);  // [head 8][rot, sgn][128]
-    if (vhalf == 1) {
+          for (int P = 0; P < NPM; ++P) x = fmaf(cf[P], vacc[P][hh][2 * r] + vacc[P][hh][2 * r + 1], x);
+          rot[r] = -x * (1.f / kWS);
+          sgn[r] = -(vacc[NPM][hh][2 * r] + vacc[NPM][hh][2 * r + 1]) * (1.f / kWS);
+        }
+        *reinterpret_cast<float2*>(pp + 2 + crd) = make_float2(rot[0], rot[1]);
+        *reinterpret_cast<float2*>(pp + 2 + kD + crd) = make_float2(sgn[0], sgn[1]);
+        if (vrow == 0 && gq == 0) {
+          float l = 0.f;
 #pragma unroll
-      for (int hh = 0; hh < GH; ++hh) {
-        const int head = 4 * hh + tig;
-        *reinterpret_cast<float2*>(xs + (head * 2) * kD + crd) = make_float2(rot[hh][0], rot[hh][1]);
-        *reinterpret_cast<float2*>(xs + (head * 2 + 1) * kD + crd) = make_float2(sgn[hh][0], sgn[hh][1]);
-      }
-    }
-    cta_sync();
-    if (vhalf == 0) {
-#pragma unroll
-      for (int hh = 0; hh < GH; ++hh) {
-        const int head = 4 * hh + tig;
-        if (head < a.G) {
-          float* pp = a.part + ((size_t)(head0 + head) * a.smax + sg.slot) * (2 + 2 * kD);
-          const float2 ro = *reinterpret_cast<const float2*>(xs + (head * 2) * kD + crd);
-          const float2 so = *reinterpret_cast<const float2*>(xs + (head * 2 + 1) * kD + crd);
-          *reinterpret_cast<float2*>(pp + 2 + crd) = make_float2(rot[hh][0] + ro.x, rot[hh][1] + ro.y);
-          *reinterpret_cast<float2*>(pp + 2 + kD + crd) = make_float2(sgn[hh][0] + so.x, sgn[hh][1] + so.y);
-          if (w == 0 && gq == 0) {
-            float l = 0.f;
-#pragma unroll
-            for (int q = 0; q < kNW; ++q) l += ms->lred[sp][q][head];
-            pp[0] = M[hh];
-            pp[1] = l;
-          }
+          for (int q = 0; q < kNW / 2; ++q) l += ms->lred[sp][8 * hf + q][head];
+          pp[0] = M[hh];
+          pp[1] = l;
         }
       }
     }
-    cta_sync();  // the scratch is free again before the next unit
   }
   // no copy of this CTA may be in flight when it exits
   if (threadIdx.x == 0)
@@ -694,7 +692,8 @@ namespace tq {
 
 int64_t decode_tc_tpu(int64_t ctx_stride) { return (ctx_stride + kTile - 1) / kTile; }
 
-// Partial slots per unit for a grid of `ctas` CTAs over units * tpu tiles.
+// Partial slots per unit for a grid of `ctas` CTAs over units * tpu tiles: two
+// per CTA that touches the unit (one per half of its warps).
 int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas) {
   const int64_t total = units * tpu;
   int64_t smax = 1;
@@ -702,7 +701,7 @@ int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas) {
     const int64_t s = owner((u + 1) * tpu - 1, total, ctas) - owner(u * tpu, total, ctas) + 1;
     smax = std::max(smax, s);
   }
-  return (int)smax;
+  return 2 * (int)smax;  // one partial per half of each CTA
 }
 
 int decode_tc_ctas(int64_t units, int64_t tpu) { return (int)std::min<int64_t>(units * tpu, sm_count()); }
