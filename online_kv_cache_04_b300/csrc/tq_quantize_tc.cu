@@ -16,9 +16,11 @@
 // §四 three-step pipeline; "TurboQuant压缩效果": codes packed into 32-bit words.)
 //
 // Two TMEM slots and two epilogue warpgroups let the tensor core work on one
-// tile while the epilogue of the other runs.  Warp roles (320 threads):
-// warps 0-3 epilogue of even tiles, 4-7 of odd tiles (warp % 4 = TMEM lane
-// quadrant), warp 8 issues MMAs and owns TMEM, warp 9 issues TMA loads.
+// tile while the epilogue of the other runs.  Warp roles (576 threads):
+// warps 0-7 epilogue of even tiles, 8-15 of odd tiles (warp % 4 = TMEM lane
+// quadrant; the two warps of a quadrant split the 128 coordinates of its 32
+// vectors and meet through shared memory for ||r||), warp 16 issues MMAs and
+// owns TMEM, warp 17 issues TMA loads.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -40,17 +42,21 @@ constexpr int kMatBytes = 2 * kBoxBytes;         // one 128 x 128 bf16 operand
 constexpr int kOffPi = 0, kOffSHi = 2 * kMatBytes, kOffSLo = 3 * kMatBytes;
 constexpr int kOffX = 4 * kMatBytes;             // two x stages
 constexpr int kOffBar = kOffX + 2 * kMatBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024; // barriers + alignment slack
-constexpr int kThreads = 320, kMmaWarp = 8, kTmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;              // slot s: [256s, +256) = U_hi | U_lo, then P | ρ chunks [hi 16 | lo 16]
+constexpr int kOffRsq = kOffBar + 256;           // [slot 2][tile parity 2][128] partial ||ρ||² of the upper half
+constexpr int kSmemBytes = kOffRsq + 2 * 2 * 128 * 4 + 1024; // + alignment slack
+constexpr int kThreads = 576, kMmaWarp = 16, kTmaWarp = 17;
+constexpr uint32_t kTmemCols = 512;              // slot s: [256s, +256) = U_hi | U_lo, then P | ρ K-steps [hi 8 | lo 8]
 
 constexpr unsigned kFaultWait = 1u;              // fault bit: a pipeline wait ran out of its bound
 
 struct Bars {
   uint64_t b_full;
   uint64_t x_full[2], x_empty[2], u_full[2], rho_full[2], p_full[2], acc_empty[2];
+  uint64_t rsq_full[2];  // the upper coordinate half's ||ρ||² partials are in
   uint32_t tmem_base;
 };
+
+static_assert(sizeof(Bars) <= 256, "barriers must fit their shared-memory region");
 
 struct TcArgs {
   int64_t n;
@@ -98,13 +104,15 @@ __device__ __forceinline__ uint32_t unshuffle32(uint32_t x) {
 }
 
 // TQ_LAYOUT_BLOCK32 store of one warp's 32 rows (one block): `words[c]` is
-// this lane's row word for coordinates 32c..32c+31; `valid` has bit L set for
-// valid row L.  Lane L writes the block words of coordinates 32c + L,
-// merging with the stored bits of rows that this call does not write.
-__device__ __forceinline__ void store_block32(uint32_t* blk, const uint32_t (&words)[4], uint32_t valid, int lane) {
+// this lane's row word for coordinates 32c..32c+31 (counted from `blk`);
+// `valid` has bit L set for valid row L.  Lane L writes the block words of
+// coordinates 32c + L, merging with the stored bits of rows that this call
+// does not write.
+template <int NW>
+__device__ __forceinline__ void store_block32(uint32_t* blk, const uint32_t (&words)[NW], uint32_t valid, int lane) {
   const uint32_t vm = unshuffle32(valid);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < NW; ++c) {
     const uint32_t col = unshuffle32(warp_transpose32(words[c], lane));
     uint32_t* dst = blk + 32 * c + lane;
     if (vm == 0xFFFFFFFFu) *dst = col;
@@ -135,11 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bars->b_full), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->x_full[s]), 1);
-      mbar_init(smem_u32(&bars->x_empty[s]), 1 + 4);
+      mbar_init(smem_u32(&bars->x_empty[s]), 1 + 8);
       mbar_init(smem_u32(&bars->u_full[s]), 1);
-      mbar_init(smem_u32(&bars->rho_full[s]), 4);
+      mbar_init(smem_u32(&bars->rho_full[s]), 8);
       mbar_init(smem_u32(&bars->p_full[s]), 1);
-      mbar_init(smem_u32(&bars->acc_empty[s]), 4);
+      mbar_init(smem_u32(&bars->acc_empty[s]), 8);
+      mbar_init(smem_u32(&bars->rsq_full[s]), 4);
     }
     fence_mbar_init();
   }
@@ -198,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t sd = desc_sw128(base + (t == 1 ? kOffSLo : kOffSHi));
 #pragma unroll 1
           for (int kk = 0; kk < 8; ++kk) {
-            // K-step kk: ρ pieces of coordinates 16kk.. sit in chunk kk/2 = [hi 16 | lo 16] columns
-            const uint32_t rho = acc + 128 + 32 * (kk >> 1) + 8 * (kk & 1) + (t == 2 ? 16 : 0);
+            // K-step kk: ρ pieces of coordinates 16kk.. sit in [hi 8 | lo 8] at 128 + 16kk
+            const uint32_t rho = acc + 128 + 16 * kk + (t == 2 ? 8 : 0);
             const uint32_t boff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;  // start address advances in 16 B units
             mma_ts(acc, rho, sd + (boff >> 4), idesc, (t | kk) != 0);
           }
@@ -238,20 +247,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       cent[k] = k < (1 << W) ? __ldg(a.centroids + k) : 0.f;
       bnd[k] = k < (1 << W) - 1 ? __ldg(a.bounds + k) : 0.f;
     }
-    const int g = warp >> 2, q = warp & 3, r = q * 32 + lane;
+    // Warps 0-7 take the even tiles (TMEM slot 0), 8-15 the odd ones (slot 1).
+    // Warp % 4 is the TMEM lane quadrant (32 vectors); the two warps of a
+    // quadrant split the coordinates: half h takes 64h .. 64h + 63.
+    const int g = warp >> 3, h = (warp >> 2) & 1, q = warp & 3, r = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int s = g;
     const uint32_t acc = tmem + lane_base + 256 * s;
+    float* rsq_s = reinterpret_cast<float*>(smem + kOffRsq) + (s * 2) * 128;
     int it = g;
     for (int64_t tile = blockIdx.x + (int64_t)g * gridDim.x; tile < ntiles; tile += 2 * (int64_t)gridDim.x, it += 2) {
       const int ph = (it >> 1) & 1;
       if (!mbar_wait(smem_u32(&bars->x_full[s]), ph, a.fault, kFaultWait)) break;
-      // ||x|| from the staged tile (row r, both 64-column boxes, 128-byte swizzle)
+      // ||x|| from the staged tile (row r, both 64-column boxes, 128-byte swizzle); both halves
       float ss[4] = {0.f, 0.f, 0.f, 0.f};
       const uint8_t* xt = smem + kOffX + s * kMatBytes;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint8_t* row = xt + h * kBoxBytes + (r >> 3) * 1024 + (r & 7) * 128;
+      for (int hb = 0; hb < 2; ++hb) {
+        const uint8_t* row = xt + hb * kBoxBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
@@ -270,20 +283,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(smem_u32(&bars->u_full[s]), ph, a.fault, kFaultWait)) break;
       tc_fence_after();
       const float inv = n > 0.f ? 1.0f / n : 0.f, nlive = n > 0.f ? -1.f : 0.f;
-      uint32_t planes[W][4];
+      uint32_t planes[W][2];
       float rsq = 0.f;
-      // 32 coordinates (one word of every index plane) per TMEM load
+      // 16 coordinates per TMEM load: chunks 4h .. 4h + 3 (two per plane word)
+#pragma unroll
+      for (int p = 0; p < W; ++p) planes[p][0] = planes[p][1] = 0u;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32], vl[32];
-        tmem_ld32(acc + 32 * c, v);
-        tmem_ld32(acc + 128 + 32 * c, vl);
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * h + cc;
+        uint32_t v[16], vl[16];
+        tmem_ld16(acc + 16 * c, v);
+        tmem_ld16(acc + 128 + 16 * c, vl);
         tmem_ld_wait();
-        uint32_t pw[W], hi[16], lo[16];
+        uint32_t pw[W], hi[8], lo[8];
 #pragma unroll
         for (int p = 0; p < W; ++p) pw[p] = 0u;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8; ++j) {
           float rho2[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
@@ -315,69 +331,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             rsq = fmaf(rho, rho, rsq);
             rho2[e] = rho;
           }
-          const __nv_bfloat162 h = __floats2bfloat162_rn(rho2[0], rho2[1]);
-          const float2 hf = __bfloat1622float2(h);
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(rho2[0], rho2[1]);
+          const float2 hf = __bfloat1622float2(hv);
           const __nv_bfloat162 l = __floats2bfloat162_rn(rho2[0] - hf.x, rho2[1] - hf.y);
-          hi[j] = *reinterpret_cast<const uint32_t*>(&h);
+          hi[j] = *reinterpret_cast<const uint32_t*>(&hv);
           lo[j] = *reinterpret_cast<const uint32_t*>(&l);
         }
-        // into the columns of U_lo just read: chunk c = [hi 16 | lo 16]
-        tmem_st16(acc + 128 + 32 * c, hi);
-        tmem_st16(acc + 128 + 32 * c + 16, lo);
+        // into the columns of U_lo just read: K-step c = [hi 8 | lo 8]
+        tmem_st8(acc + 128 + 16 * c, hi);
+        tmem_st8(acc + 128 + 16 * c + 8, lo);
+        // chunk c holds bits 16·(c & 1).. of plane word c / 2 (word (c >> 1) - 2h here)
 #pragma unroll
         for (int p = 0; p < W; ++p) {
-          // chunk c is word c of each plane (rolled loop: select by value)
-          planes[p][0] = c == 0 ? pw[p] : planes[p][0];
-          planes[p][1] = c == 1 ? pw[p] : planes[p][1];
-          planes[p][2] = c == 2 ? pw[p] : planes[p][2];
-          planes[p][3] = c == 3 ? pw[p] : planes[p][3];
+          const uint32_t x = (cc & 1) ? pw[p] << 16 : pw[p];
+          if (cc >> 1) planes[p][1] |= x;
+          else planes[p][0] |= x;
         }
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->rho_full[s]));
+      if (h == 1) {  // the lower half writes ||r|| = n·sqrt(lower + upper partial)
+        rsq_s[(it >> 1 & 1) * 128 + r] = rsq;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->rsq_full[s]));
+      }
       const int64_t row = tile * kTile + r;
       const int64_t blk_row = tile * kTile + q * 32;  // this warp's block (layout 1)
       const uint32_t valid = __ballot_sync(0xffffffffu, row < a.n);
       if constexpr (LAYOUT == TQ_LAYOUT_ROWS) {
         if (row < a.n) {
-          uint4* ip = reinterpret_cast<uint4*>(a.idx + row * (4 * W));
 #pragma unroll
-          for (int p = 0; p < W; ++p) ip[p] = make_uint4(planes[p][0], planes[p][1], planes[p][2], planes[p][3]);
+          for (int p = 0; p < W; ++p)
+            *reinterpret_cast<uint2*>(a.idx + row * (4 * W) + p * 4 + 2 * h) = make_uint2(planes[p][0], planes[p][1]);
         }
       } else {
         if (valid != 0u) {
 #pragma unroll
           for (int p = 0; p < W; ++p)
-            store_block32(a.idx + (blk_row >> 5) * (W * 128) + p * 128, planes[p], valid, lane);
+            store_block32<2>(a.idx + (blk_row >> 5) * (W * 128) + p * 128 + 64 * h, planes[p], valid, lane);
         }
       }
       if (!mbar_wait(smem_u32(&bars->p_full[s]), ph, a.fault, kFaultWait)) break;
       tc_fence_after();
-      uint32_t sg[4];
+      uint32_t sg[2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t v[32];
-        tmem_ld32(acc + 32 * c, v);
+        tmem_ld32(acc + 32 * (2 * h + cc), v);
         tmem_ld_wait();
         uint32_t wsg = 0u;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (__uint_as_float(v[j]) >= 0.f) wsg |= 1u << j;
-        sg[c] = wsg;
+        sg[cc] = wsg;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[s]));
       if constexpr (LAYOUT == TQ_LAYOUT_ROWS) {
-        if (row < a.n) *reinterpret_cast<uint4*>(a.sgn + row * 4) = make_uint4(sg[0], sg[1], sg[2], sg[3]);
+        if (row < a.n) *reinterpret_cast<uint2*>(a.sgn + row * 4 + 2 * h) = make_uint2(sg[0], sg[1]);
       } else {
-        if (valid != 0u) store_block32(a.sgn + (blk_row >> 5) * 128, sg, valid, lane);
+        if (valid != 0u) store_block32<2>(a.sgn + (blk_row >> 5) * 128 + 64 * h, sg, valid, lane);
       }
-      if (row < a.n) {
-        a.norm[row] = n;
-        a.rnorm[row] = n * sqrtf(rsq);
+      if (h == 0) {
+        if (!mbar_wait(smem_u32(&bars->rsq_full[s]), ph, a.fault, kFaultWait)) break;
+        if (row < a.n) {
+          a.norm[row] = n;
+          a.rnorm[row] = n * sqrtf(rsq + rsq_s[(it >> 1 & 1) * 128 + r]);
+        }
       }
     }
   }
