@@ -369,24 +369,41 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   float* wgt = o + d;           // [ns]
   __shared__ float lsum;
   const float* pp = a.part + (size_t)head * pitch * stride;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
+    // slot weights 2^(m_k - max) and l = Σ_k w_k l_k, one slot per lane
+    const int lane = threadIdx.x;
     float mx = -INFINITY;
-    for (int k = 0; k < ns; ++k) mx = fmaxf(mx, pp[(size_t)k * stride]);
+    for (int k = lane; k < ns; k += 32) mx = fmaxf(mx, pp[(size_t)k * stride]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float l = 0.0f;
-    for (int k = 0; k < ns; ++k) {
+    for (int k = lane; k < ns; k += 32) {
       const float mk = pp[(size_t)k * stride];
       const float wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - mx);
       wgt[k] = wk;
-      l += wk * pp[(size_t)k * stride + 1];
+      l = fmaf(wk, pp[(size_t)k * stride + 1], l);
     }
-    lsum = l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) lsum = l;
   }
   __syncthreads();
   for (int j = threadIdx.x; j < d + m; j += blockDim.x) {
-    float v = 0.0f;
-    for (int k = 0; k < ns; ++k)
-      if (wgt[k] != 0.0f) v = fmaf(wgt[k], pp[(size_t)k * stride + 2 + j], v);
-    acc[j] = v;
+    float v0 = 0.0f, v1 = 0.0f, v2 = 0.0f, v3 = 0.0f;
+    int k = 0;
+    // a slot of weight 0 (no token) contributes nothing, whatever it holds
+    auto term = [&](int kk, float v) {
+      const float x = pp[(size_t)kk * stride + 2 + j];
+      return wgt[kk] != 0.0f ? fmaf(wgt[kk], x, v) : v;
+    };
+    for (; k + 4 <= ns; k += 4) {
+      v0 = term(k, v0);
+      v1 = term(k + 1, v1);
+      v2 = term(k + 2, v2);
+      v3 = term(k + 3, v3);
+    }
+    for (; k < ns; ++k) v0 = term(k, v0);
+    acc[j] = (v0 + v1) + (v2 + v3);
   }
   __syncthreads();
   // y = acc_rot + α (S Πᵀ)ᵀ acc_sgn
