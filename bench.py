@@ -232,10 +232,14 @@ def workload_config(wl, bits):
 # --------------------------------------------------------------------- GPU arm
 
 def timed(stream, fn, iters, flush=None):
-    """Mean device ms of fn() over iters calls, each preceded (untimed) by an L2 flush."""
+    """Mean device ms of fn() over iters calls, each preceded (untimed) by an L2 flush.
+
+    Everything is enqueued first and synchronised once, so that the host's
+    launch work for a call overlaps the flush before it instead of leaving the
+    device idle inside the timed interval."""
     import torch
 
-    tot = 0.0
+    ev = []
     for _ in range(iters):
         if flush is not None:
             flush.fill_(1)
@@ -243,9 +247,9 @@ def timed(stream, fn, iters, flush=None):
         e0.record(stream)
         fn()
         e1.record(stream)
-        e1.synchronize()
-        tot += e0.elapsed_time(e1)
-    return tot / iters
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in ev) / iters
 
 
 def decode_sweep(_lib, plan_cache, stream, flush, bits_list, iters=20):
