@@ -37,17 +37,20 @@
 //
 // Work split.  A persistent grid of one CTA per SM takes contiguous ranges of
 // 256-token tiles over all (batch, kv head) units (the last tile of a unit
-// may hold 128); a unit cut between CTAs leaves one partial per CTA, merged
-// by the combine kernel of tq_decode.cu.  Sixteen warps do the same work:
-// warp w scores 16 tokens of each tile (half w & 1 of block w / 2) and
+// may hold 128); the partials of a unit (two per CTA that touches it) are
+// merged by the combine kernel of tq_decode.cu.  Sixteen warps do the same
+// work: warp w scores 16 tokens of each tile (half w & 1 of block w / 2) and
 // accumulates values for 16 coordinates (rows w % 8) over half of the blocks
-// (w / 8); the two halves meet at the end of a unit.  The weights of a tile
-// go through shared memory, already laid out as the value operand.  Per tile i there are two named barriers:
-// the first publishes the weights of tile i − 1; between the two, the value
-// products of tile i − 1, the score products of tile i and its softmax run
-// as one block the compiler can interleave; the second carries the vote of
-// the lazy softmax and frees the ring stage of tile i − 1, into which one
-// thread then starts the bulk copies of a later tile.
+// (w / 8).  Warps 0-7 thus only touch tokens 0-127 of a tile and warps 8-15
+// tokens 128-255, and the two halves run as independent pipelines: each has
+// its own softmax reference, running sum, named barriers and partial.  The
+// weights of a tile go through shared memory, already laid out as the value
+// operand.  Per tile and half there are two named barriers: the first
+// publishes the weights of tile i − 1; between the two, the value products of
+// tile i − 1, the score products of tile i and its softmax run as one block
+// the compiler can interleave; the second carries the vote of the lazy
+// softmax.  One thread starts the bulk copies of later tiles into a ring
+// stage once both halves have handed it back (a two-arrival mbarrier).
 //
 // Softmax is online with a lazy reference: the running reference M (of
 // log2(p·max(‖v‖, ‖r_v‖)), clamped at 2^-32) moves only when a tile exceeds

@@ -71,14 +71,6 @@ struct TcArgs {
 
 __device__ unsigned g_fault_word;
 
-template <int W>
-__device__ __forceinline__ int bucket(float u, const float (&bnd)[8]) {
-  int idx = 0;
-#pragma unroll
-  for (int k = 0; k < (1 << W) - 1; ++k) idx += (bnd[k] < u) ? 1 : 0;
-  return idx;
-}
-
 // 32 x 32 bit transpose across a warp: lane r holds row r on entry (bit c =
 // element (r, c)); on exit lane c holds column c (bit r = element (r, c)).
 __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
@@ -118,14 +110,6 @@ __device__ __forceinline__ void store_block32(uint32_t* blk, const uint32_t (&wo
     if (vm == 0xFFFFFFFFu) *dst = col;
     else if (vm != 0u) *dst = (*dst & ~vm) | (col & vm);
   }
-}
-
-template <int W>
-__device__ __forceinline__ float centroid(int idx, const float (&cent)[8]) {
-  float c = cent[0];
-#pragma unroll
-  for (int k = 1; k < (1 << W); ++k) c = (idx == k) ? cent[k] : c;
-  return c;
 }
 
 template <int W, int LAYOUT>
