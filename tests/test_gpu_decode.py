@@ -1,6 +1,6 @@
 """GPU parity of tq_decode_attention / tq_decode_scores against the float64 oracle.
 
-Decode is judged on identical records: the oracle's own packed records fed
+Decode is compared on identical records: the oracle's own packed records fed
 to the GPU (isolating decode from quantize, and checking the GPU unpacks the
 oracle's words), and the GPU's records fed to the oracle.
 """
