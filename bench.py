@@ -462,7 +462,7 @@ def main():
     kernels = {
         "quantize": {"launches_per_step": 2, "ms_per_launch": t_quant * 1e3, "bytes_per_launch": q_bytes,
                      "gbs": q_bytes / t_quant / 1e9, "mvec_per_s": nvec / t_quant / 1e6},
-        "decode_attention": {"launches_per_call": 3, "ms_per_call_in_step": t_dec_step * 1e3,
+        "decode_attention": {"launches_per_call": 1, "ms_per_call_in_step": t_dec_step * 1e3,
                              "ms_per_call_cold_l2": t_dec * 1e3, "bytes_per_call": dec_bytes,
                              "gbs_cold_l2": dec_bytes / t_dec / 1e9, "kv_tokens_per_s_cold_l2": B * T / t_dec,
                              "frac_of_8tbs_cold_l2": dec_bytes / t_dec / 1e9 / NOMINAL_HBM_GBS},
@@ -470,7 +470,7 @@ def main():
     if 2 * t_quant >= t_dec_step:
         kname, ach, traffic_key = "quantize_tc_kernel", q_bytes / t_quant / 1e9, "quantize_tc_kernel"
     else:
-        kname, ach, traffic_key = "decode_tc_kernel (prep + main + combine)", dec_bytes / t_dec / 1e9, "decode_tc_kernel"
+        kname, ach, traffic_key = "decode_tc_kernel", dec_bytes / t_dec / 1e9, "decode_tc_kernel"
     traffic = dram_traffic(traffic_key, wl.name)
     line = {
         "metric": METRIC, "value": B * T * world / t_step, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -484,7 +484,7 @@ def main():
         "decode_frac_of_8tbs": dec_bytes / t_dec / 1e9 / NOMINAL_HBM_GBS,
         "quantize_mvec_per_s": nvec / t_quant / 1e6,
         "e2e": {"value": B * T * world / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "fault_flags": fault,
         "clocks": clocks,
     }

@@ -11,7 +11,8 @@
 // o = Πᵀ (acc_rot + √(π/2)/m (S Πᵀ)ᵀ acc_sgn) / l.  No dequantized K or V is
 // ever written ("TurboQuant压缩效果": decode in registers while reading).
 //
-// Kernels:
+// Kernels of the general path (any d, m; the d = m = 128 value-block case runs
+// as one launch of the tensor-core kernel in tq_decode_tc.cu instead):
 //   prep     q̃ = Π q and s̃ = (S Πᵀ) q̃ per query head -> workspace
 //   split    grid (splits, B*Hkv): streams one context slice of one kv head
 //            for its G query heads, writes (max, sum, acc) partials
@@ -50,12 +51,27 @@ int tc_slots(const DecodeShape& s) {
   return tq::decode_tc_slots(units, tpu, tq::decode_tc_ctas(units, tpu));
 }
 
-// Workspace: q̃ and s̃ per query head, then the split partials of whichever
-// path runs (sized for the larger of the two).
+// Workspace of the tensor-core path: the per-unit arrival counters, the
+// per-unit query tables, then the partials (byte offsets, 256-byte aligned).
+struct TcLayout {
+  size_t tables, part, bytes;
+};
+TcLayout tc_layout(const DecodeShape& s) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t units = size_t(s.B) * s.Hkv, heads = size_t(s.B) * s.Hq;
+  TcLayout l;
+  l.tables = up(units * sizeof(unsigned));
+  l.part = up(l.tables + units * tq::decode_tc_table_bytes(s.w, s.G));
+  l.bytes = l.part + sizeof(float) * heads * tc_slots(s) * (2 + s.d + s.m);
+  return l;
+}
+
+// Workspace: the general path's q̃ and s̃ per query head and split partials,
+// or the tensor-core path's layout, whichever is larger.
 size_t ws_floats(const DecodeShape& s) {
   const size_t heads = size_t(s.B) * s.Hq;
-  const size_t parts = std::max<size_t>(s.nsplit, tc_slots(s));
-  return heads * (s.d + s.m) + heads * parts * (2 + s.d + s.m);
+  const size_t general = heads * (s.d + s.m) + heads * s.nsplit * (2 + s.d + s.m);
+  return tc_slots(s) > 0 ? std::max(general, (tc_layout(s).bytes + 3) / 4) : general;
 }
 
 bool fill_shape(const tq_plan* plan, int B, int Hq, int Hkv, int64_t ctx_stride, DecodeShape* s) {
@@ -341,8 +357,6 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
 
 struct CombineArgs {
   DecodeShape s;
-  int slots;              // partial slots per head (stride); 0: the general path's nsplit
-  int64_t tpu, ctas;      // tensor-core path: per-unit slot count from its tile partition
   const float* part;
   const float* pi_t;      // [d][d] Πᵀ
   const float* s_rot_t;   // [d][m] (S Πᵀ)ᵀ
@@ -354,15 +368,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   extern __shared__ float sm[];
   const int d = a.s.d, m = a.s.m, stride = 2 + d + m;
   const int head = blockIdx.x;
-  int ns = a.s.nsplit, pitch = a.s.nsplit;
-  if (a.slots > 0) {
-    // CTA c owns flat tiles [c·T/C, (c+1)·T/C): the unit's tiles span CTAs first..last
-    const int b = head / a.s.Hq, hq = head - b * a.s.Hq;
-    const int64_t u = int64_t(b) * a.s.Hkv + hq / a.s.G, T = int64_t(a.s.B) * a.s.Hkv * a.tpu;
-    const int64_t first = ((u * a.tpu + 1) * a.ctas - 1) / T, last = (((u + 1) * a.tpu) * a.ctas - 1) / T;
-    ns = 2 * (int)(last - first + 1);  // the tensor-core kernel writes one partial per half of each CTA
-    pitch = a.slots;
-  }
+  const int ns = a.s.nsplit, pitch = a.s.nsplit;
   float* acc = sm;              // [d + m]
   float* y = acc + d + m;       // [d]
   float* o = y + d;             // [d]
@@ -476,26 +482,15 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
   float* qt = static_cast<float*>(workspace);
   float* stv = qt + size_t(B) * Hq * s.d;
   float* part = stv + size_t(B) * Hq * s.m;
-  if ((st = launch_prep(plan, q, q_dtype, s, qt, stv, cs)) != TQ_OK) return st;
   const float sc = scale > 0.0f ? scale : 1.0f / sqrtf((float)s.d);
   if (tq::decode_tc_supported(plan, s.G, V, ctx_stride)) {
-    const int slots = tc_slots(s);
-    if ((st = tq::launch_decode_tc(plan, K, V, ctx_len, B, Hq, Hkv, ctx_stride, sc, qt, stv, part, slots, cs)) !=
-        TQ_OK)
-      return st;
-    CombineArgs c{};
-    c.s = s;
-    c.slots = slots;
-    c.tpu = tq::decode_tc_tpu(ctx_stride);
-    c.ctas = tq::decode_tc_ctas(int64_t(B) * Hkv, c.tpu);
-    c.part = part;
-    c.pi_t = plan->pi_t;
-    c.s_rot_t = plan->s_rot_t;
-    c.alpha = plan->qjl_alpha;
-    c.out = out;
-    combine_kernel<<<B * Hq, 256, sizeof(float) * (3 * s.d + s.m + slots), cs>>>(c);
-    return tq::launch_status();
+    const TcLayout l = tc_layout(s);
+    uint8_t* ws8 = static_cast<uint8_t*>(workspace);
+    return tq::launch_decode_tc(plan, q, q_dtype, K, V, ctx_len, B, Hq, Hkv, ctx_stride, sc,
+                                reinterpret_cast<float*>(ws8 + l.part), tc_slots(s), ws8 + l.tables,
+                                static_cast<unsigned*>(workspace), out, cs);
   }
+  if ((st = launch_prep(plan, q, q_dtype, s, qt, stv, cs)) != TQ_OK) return st;
   SplitArgs a{};
   a.s = s;
   a.kidx = K->idx; a.ksgn = K->sgn; a.knorm = K->norm; a.krnorm = K->rnorm;

@@ -57,6 +57,7 @@
 // it by more than 2^6; the accumulators are then rescaled.  Every mbarrier
 // wait is bounded; on timeout the kernel sets a fault bit (tq_fault_flags),
 // skips the remaining waits and runs to its end.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -148,14 +149,18 @@ struct TcArgs {
   const int32_t* ctx_len;
   int64_t ctx_stride;
   int B, Hq, Hkv, G;
-  const float* qt;   // [B*Hq][128]  Π q
-  const float* st;   // [B*Hq][128]  S q
+  const void* q;     // [B*Hq][128] queries, bf16 (q_bf16) or fp32
+  int q_bf16;
+  const float *pi, *pi_t, *s_rot, *s_rot_t;  // Π, Πᵀ, S̃ = S Πᵀ, S̃ᵀ (128 x 128, row-major)
   const float* walsh;
   float scale, alpha;
   float* part;       // [B*Hq][smax][2 + 2*128]
   int smax;
   int64_t tpu;       // tiles per unit = ceil(ctx_stride / 256)
   int64_t total;     // units * tpu
+  uint8_t* tables;     // [B*Hkv] per-unit query tables (unit_table_kernel)
+  unsigned* arrivals;  // [B*Hkv] CTAs of each unit done with their partials (zeroed by unit_table_kernel)
+  float* out;        // [B*Hq][128]
   unsigned* fault;
 };
 
@@ -194,12 +199,15 @@ struct Shape {
 };
 
 struct Misc {
+  alignas(16) float consts[4][8];  // this unit's A0, B0, A1, B1 per head (bulk copy of its table's tail)
   uint64_t ld_full[kStages], ld_empty[kStages];  // empty: one arrival per half
+  uint64_t tab_full;          // the unit's query table has landed
   int abort;
   float red[kNW][8];          // per-warp tile maxima (reference moves only)
-  float amax[2][8];           // per-unit query weight maxima (as non-negative float bits)
-  float O[2][8];              // per-unit score offsets per (part, head)
   float lred[2][kNW][8];      // per segment parity, per warp: Σ p per head
+  float Mh[2][8];             // per half: softmax reference per head at the end of a segment
+  float cf[4];                // Walsh coefficients of the codebook planes
+  int last;                   // this CTA is the last of its unit to hand in its partial
 };
 constexpr int kMiscBytes = 2048;
 static_assert(sizeof(Misc) <= kMiscBytes, "barriers and per-head state must fit their region");
@@ -234,10 +242,326 @@ __device__ __forceinline__ Seg segment_at(const TcArgs& a, int64_t f, int64_t f1
   return s;
 }
 
+// Scratch of the per-unit query transform, half merge and unit merge: the
+// query-weight table and the value-weight buffers, both dead between units (the
+// ring may already hold copies of the next unit and is not touched).  Global
+// loads on these one-off paths are issued in as few dependent rounds as the
+// registers allow: a round trip to L2 costs over a microsecond here.
+constexpr int kMaxCtas = 160;                          // grid limit: bounds the slots per unit
+template <int GP>
+struct Scratch {
+  static constexpr int kPrep = 7 * GP * kD;                                // q, 4 partial sums, Πq, Sq
+  static constexpr int kHalf = GP * 2 * kD;                                // one half's acc_rot | acc_sgn
+  static constexpr int kMerge = GP * (2 + kMaxCtas + 2 * kD + 4 * kD + kD);  // see unit_merge
+};
+
+// Column c = threadIdx % 128 of rows 32·grp .. 32·grp + 31 (grp = threadIdx / 128)
+// of a 128 x 128 row-major matrix: consecutive threads read whole rows.
+__device__ __forceinline__ void load_cols(const float* __restrict__ A, float (&v)[32]) {
+  const int grp = threadIdx.x >> 7, c = threadIdx.x & (kD - 1);
+#pragma unroll
+  for (int t = 0; t < 32; ++t) v[t] = __ldg(A + (32 * grp + t) * kD + c);
+}
+
+// red[grp][g][c] = Σ_t v[t] · x[g][32·grp + t]: this thread's share of
+// (Aᵀ x_g)_c for GP vectors x_g of stride xs in shared memory.
+template <int GP>
+__device__ __forceinline__ void cols_times(const float (&v)[32], const float* x, int xs, float* red) {
+  const int grp = threadIdx.x >> 7, c = threadIdx.x & (kD - 1);
+  float acc[GP];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) acc[g] = 0.f;
+#pragma unroll
+  for (int t = 0; t < 32; ++t)
+#pragma unroll
+    for (int g = 0; g < GP; ++g) acc[g] = fmaf(v[t], x[g * xs + 32 * grp + t], acc[g]);
+#pragma unroll
+  for (int g = 0; g < GP; ++g) red[(grp * GP + g) * kD + c] = acc[g];
+}
+
+__device__ __forceinline__ float sum4(const float* red, int e, int stride) {
+  return (red[e] + red[stride + e]) + (red[2 * stride + e] + red[3 * stride + e]);
+}
+
+// Query transform of the unit's heads head0 .. head0 + G - 1 ("TurboQuant 与 AI
+// 效率革命" §三: the estimator takes Π q and S q): on return qr[g][j] = (Π q_g)_j
+// and sr[g][i] = (S̃ Π q_g)_i = (S q_g)_i, zero for g >= G.  All threads; one
+// round of global loads (q and both matrices).
+template <int GP>
+__device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* scr, float** qr_out,
+                                             float** sr_out) {
+  float* qs = scr;
+  float* red = qs + GP * kD;
+  float* qr = red + 4 * GP * kD;
+  float* sr = qr + GP * kD;
+  constexpr int QP = GP * kD / kThreads;  // query elements per thread
+  float qv[QP];
+#pragma unroll
+  for (int i = 0; i < QP; ++i) {
+    const int e = threadIdx.x + kThreads * i;
+    const size_t off = (size_t)head0 * kD + e;
+    qv[i] = (e >> 7) >= a.G ? 0.f
+            : a.q_bf16      ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[off])
+                            : reinterpret_cast<const float*>(a.q)[off];
+  }
+  float v1[32], v2[32];
+  load_cols(a.pi_t, v1);     // (Π q)_j = Σ_c Πᵀ[c][j] q_c
+  load_cols(a.s_rot_t, v2);  // (S̃ q̃)_i = Σ_j S̃ᵀ[j][i] q̃_j
+  // bring Π and S̃ (row-major), which the unit's merge reads, into L2 meanwhile
+  for (int e = threadIdx.x; e < 2 * kD * kD / 32; e += kThreads) {
+    const float* line = e < kD * kD / 32 ? a.pi + 32 * e : a.s_rot + 32 * (e - kD * kD / 32);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+  }
+#pragma unroll
+  for (int i = 0; i < QP; ++i) qs[threadIdx.x + kThreads * i] = qv[i];
+  cta_sync();
+  cols_times<GP>(v1, qs, kD, red);
+  cta_sync();
+  for (int e = threadIdx.x; e < GP * kD; e += kThreads) qr[e] = sum4(red, e, GP * kD);
+  cta_sync();
+  cols_times<GP>(v2, qr, kD, red);
+  cta_sync();
+  for (int e = threadIdx.x; e < GP * kD; e += kThreads) sr[e] = sum4(red, e, GP * kD);
+  cta_sync();
+  *qr_out = qr;
+  *sr_out = sr;
+}
+
+// Merge of the ns partials (one per CTA) of each head of the unit, log-sum-exp
+// over their references, and the output o = Πᵀ(acc_rot + α S̃ᵀ acc_sgn) / l, by
+// the last CTA of the unit to hand in its partial.  All threads; partials
+// written by other CTAs are read past L1.  Two rounds of global loads when ns
+// fits one chunk: (references, sums, partial values), then both matrices.
+template <int GP>
+__device__ __noinline__ void unit_merge(const TcArgs& a, int head0, int ns, float* scr) {
+  constexpr int kStride = 2 + 2 * kD;
+  float* ml = scr;                      // [GP][2] reference max, Σ w·l
+  float* wgt = ml + 2 * GP;             // [GP][kMaxCtas] slot weights
+  float* acc = wgt + GP * kMaxCtas;     // [GP][256] merged acc_rot | acc_sgn
+  float* red = acc + GP * 2 * kD;       // [4][GP][128]
+  float* y = red + 4 * GP * kD;         // [GP][128]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // outputs o = threadIdx.x + 512·r (head o / 256, element o % 256), U slots per chunk
+  constexpr int R = GP * 2 * kD / kThreads, U = 48 / R;
+  const float* pp[R];
+  const float* wg[R];
+  float v[R], x[R][U];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int o = threadIdx.x + kThreads * r, g = o >> 8, j = o & (2 * kD - 1);
+    pp[r] = a.part + (size_t)(head0 + min(g, a.G - 1)) * a.smax * kStride + 2 + j;
+    wg[r] = wgt + g * kMaxCtas;
+    v[r] = 0.f;
+#pragma unroll
+    for (int t = 0; t < U; ++t) x[r][t] = t < ns ? __ldcg(pp[r] + (size_t)t * kStride) : 0.f;
+  }
+  constexpr int kPerLane = kMaxCtas / 32;
+  if (warp < GP) {
+    const float* pm = a.part + (size_t)(head0 + warp) * a.smax * kStride;
+    float mk[kPerLane], lk[kPerLane];
+#pragma unroll
+    for (int t = 0; t < kPerLane; ++t) {
+      const int k = lane + 32 * t;
+      const bool in = warp < a.G && k < ns;
+      mk[t] = in ? __ldcg(pm + (size_t)k * kStride) : -INFINITY;
+      lk[t] = in ? __ldcg(pm + (size_t)k * kStride + 1) : 0.f;
+    }
+    float mx = -INFINITY, l = 0.f;
+#pragma unroll
+    for (int t = 0; t < kPerLane; ++t) mx = fmaxf(mx, mk[t]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+    for (int t = 0; t < kPerLane; ++t) {
+      const float wk = mk[t] == -INFINITY ? 0.f : exp2f(mk[t] - mx);
+      wgt[warp * kMaxCtas + lane + 32 * t] = wk;
+      l = fmaf(wk, lk[t], l);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) ml[2 * warp] = mx, ml[2 * warp + 1] = l;
+  }
+  cta_sync();
+  // acc[g][j] = Σ_k w_k part_k[j]; a slot of weight 0 (no token, or past ns) adds
+  // nothing, whatever it holds
+  for (int k0 = 0; k0 < ns; k0 += U) {
+    if (k0 > 0) {
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int t = 0; t < U; ++t) x[r][t] = k0 + t < ns ? __ldcg(pp[r] + (size_t)(k0 + t) * kStride) : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int t = 0; t < U; ++t) {
+        const float wk = k0 + t < ns ? wg[r][k0 + t] : 0.f;
+        v[r] = wk != 0.f ? fmaf(wk, x[r][t], v[r]) : v[r];
+      }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[threadIdx.x + kThreads * r] = v[r];
+  float v1[32], v2[32];
+  load_cols(a.s_rot, v1);  // (S̃ᵀ acc_sgn)_j = Σ_i S̃[i][j] acc_sgn_i
+  load_cols(a.pi, v2);     // (Πᵀ y)_i = Σ_j Π[j][i] y_j
+  cta_sync();
+  cols_times<GP>(v1, acc + kD, 2 * kD, red);
+  cta_sync();
+  for (int e = threadIdx.x; e < GP * kD; e += kThreads)
+    y[e] = fmaf(a.alpha, sum4(red, e, GP * kD), acc[(e >> 7) * 2 * kD + (e & (kD - 1))]);
+  cta_sync();
+  cols_times<GP>(v2, y, kD, red);
+  cta_sync();
+  for (int e = threadIdx.x; e < a.G * kD; e += kThreads) {
+    const float l = ml[2 * (e >> 7) + 1];
+    a.out[(size_t)head0 * kD + e] = sum4(red, e, GP * kD) * (l > 0.f ? 1.f / l : 0.f);
+  }
+  cta_sync();
+}
+
+// Per-unit query table, built once per (batch, kv head) unit by
+// unit_table_kernel and bulk-copied by every decode CTA that works on the unit:
+// the query operand of the score products (the shared-memory image: f16 hi + lo
+// per head and K index, stored divided by a power of two E per part and head)
+// followed by the constants A0, B0, A1, B1 of each head's affine map from the
+// products to scores in log2 units.
+template <int W, int GP>
+struct Table {
+  static constexpr int kConstBytes = 4 * 8 * 4;
+  static constexpr int kBytes = Shape<W, GP>::kBKBytes + kConstBytes;
+};
+struct TableState {
+  float amax[2][8];  // per part and head: largest |weight| (as non-negative float bits)
+  float O[2][8];     // per part and head: score offset of the exponent-kind operands
+  float cf[4];       // Walsh coefficients of the codebook planes
+};
+template <int W, int GP>
+constexpr int table_smem_bytes() {
+  return 1024 + Shape<W, GP>::kBKBytes + Scratch<GP>::kPrep * 4 + (int)sizeof(TableState);
+}
+
+// One CTA per unit: q̃ = Π q and s̃ = S q of its G heads, then the table.  The
+// key operand bits are exact ±1 (sign kind) or 0.125 / 0.5 (exponent kind) per
+// f16 lane, so a head's weight x enters as x·s (sign kind, s = -F) or as
+// x·(F - mean)·2/δ (exponent kind), the mean folded into the offset O.  Also
+// zeroes the unit's arrival counter for the decode kernel that follows.
+template <int W, int GP>
+__global__ void __launch_bounds__(kThreads) unit_table_kernel(const TcArgs a) {
+  using Sh = Shape<W, GP>;
+  constexpr int NPM = Sh::NPM, NP = Sh::NP, GH = Sh::GH;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* BK = smem;
+  float* scr = reinterpret_cast<float*>(smem + Sh::kBKBytes);
+  TableState* ts = reinterpret_cast<TableState*>(smem + Sh::kBKBytes + Scratch<GP>::kPrep * 4);
+  const int u = blockIdx.x, lane = threadIdx.x & 31;
+  const int b = u / a.Hkv, h = u - b * a.Hkv, head0 = b * a.Hq + h * a.G;
+  // the decode kernel may start now: it reads tables and counters only after
+  // waiting for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) a.arrivals[u] = 0u;
+  if (threadIdx.x < NPM) ts->cf[threadIdx.x] = __ldg(a.walsh + (threadIdx.x < W ? (1 << threadIdx.x) : 7));
+  if (threadIdx.x < 16) {
+    ts->amax[threadIdx.x >> 3][threadIdx.x & 7] = 0.f;
+    ts->O[threadIdx.x >> 3][threadIdx.x & 7] = 0.f;
+  }
+  for (int e = threadIdx.x; e < Sh::kBKBytes / 16; e += kThreads)
+    reinterpret_cast<uint4*>(BK)[e] = make_uint4(0, 0, 0, 0);
+  float *qr, *sr;
+  unit_query_prep<GP>(a, head0, scr, &qr, &sr);  // its first barrier publishes the lines above
+  // thread group grp = threadIdx / 128 takes heads grp and grp + 4; thread j its coordinate
+  // j: word kw, bit x = 16e + L; L = 8·ks2 + 4·hi + q -> K index 8·hi + 2q + e
+  constexpr int HG = GP / 4;  // heads per thread group
+  const int grp = threadIdx.x >> 7, j = threadIdx.x & (kD - 1);
+  const int kw = j >> 5, e16 = (j >> 4) & 1, L = j & 15, ks2 = L >> 3, hi = (L >> 2) & 1, q4 = L & 3;
+  const int kk = 8 * hi + 2 * q4 + e16;
+  // exponent-kind operand (hi = 0): s = (F - mean)·2/δ; sign kind: s = -F
+  const float wsc = hi ? -1.f : 2.f / kExpDelta;
+  float qv[HG], sv[HG], cf[NPM];
+#pragma unroll
+  for (int i = 0; i < HG; ++i) qv[i] = qr[(grp + 4 * i) * kD + j], sv[i] = sr[(grp + 4 * i) * kD + j];
+#pragma unroll
+  for (int P = 0; P < NPM; ++P) cf[P] = ts->cf[P];
+#pragma unroll
+  for (int i = 0; i < HG; ++i) {
+    const int g = grp + 4 * i;
+    float am = 0.f;
+#pragma unroll
+    for (int P = 0; P < NPM; ++P) am = fmaxf(am, fabsf(wsc * cf[P] * qv[i]));
+    float aq = fabsf(wsc * sv[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      aq = fmaxf(aq, __shfl_xor_sync(0xffffffffu, aq, o));
+    }
+    if (lane == 0) {
+      atomicMax(reinterpret_cast<int*>(&ts->amax[0][g]), __float_as_int(am));
+      atomicMax(reinterpret_cast<int*>(&ts->amax[1][g]), __float_as_int(aq));
+    }
+  }
+  cta_sync();
+  // E: the power of two taking a part's largest weight below 2^12 (weights are
+  // stored divided by E, exactly)
+  auto escale = [&](int p, int g, bool inverse) {
+    const float am = ts->amax[p][g];
+    int ex;
+    frexpf(am, &ex);
+    return am > 0.f ? ldexpf(1.f, inverse ? 12 - ex : ex - 12) : 1.f;
+  };
+  {
+    __half* bk = reinterpret_cast<__half*>(BK);
+#pragma unroll
+    for (int i = 0; i < HG; ++i) {
+      const int g = grp + 4 * i;
+      const float inv0 = escale(0, g, true), inv1 = escale(1, g, true);
+      float osum0 = 0.f, osum1 = 0.f;
+#pragma unroll
+      for (int P = 0; P < NP; ++P) {
+        const int part = P < NPM ? 0 : 1;
+        const int ks = (P * 4 + kw) * 2 + ks2;
+        const float x = part == 0 ? wsc * cf[P < NPM ? P : 0] * qv[i] * inv0 : wsc * sv[i] * inv1;
+        const __half xh = __float2half_rn(x), xl = __float2half_rn(x - __half2float(xh));
+        // (k, n) sits in lane (n, k % 8 / 2), fragment k / 8, half k % 2
+        const int base =
+            ((((ks * GH + (g >> 2)) * 8 + 2 * (g & 3)) * 4 + ((kk & 7) >> 1)) * 2 + (kk >> 3)) * 2 + (kk & 1);
+        bk[base] = xh;
+        bk[base + 16] = xl;
+        if (!hi) (part == 0 ? osum0 : osum1) += __half2float(xh) + __half2float(xl);
+      }
+      // offsets O[part][g] = mean · E · Σ (stored exponent-kind weights)
+#pragma unroll
+      for (int sh = 16; sh > 0; sh >>= 1) {
+        osum0 += __shfl_xor_sync(0xffffffffu, osum0, sh);
+        osum1 += __shfl_xor_sync(0xffffffffu, osum1, sh);
+      }
+      if (lane == 0) {
+        atomicAdd(&ts->O[0][g], osum0 * escale(0, g, false) * kExpMean);
+        atomicAdd(&ts->O[1][g], osum1 * escale(1, g, false) * kExpMean);
+      }
+    }
+  }
+  cta_sync();
+  uint8_t* dst = a.tables + (size_t)u * Table<W, GP>::kBytes;
+  for (int e = threadIdx.x; e < Sh::kBKBytes / 16; e += kThreads)
+    reinterpret_cast<uint4*>(dst)[e] = reinterpret_cast<const uint4*>(BK)[e];
+  if (threadIdx.x < 8) {
+    const int g = threadIdx.x;
+    const float c = a.scale * kLog2e;
+    float* cs = reinterpret_cast<float*>(dst + Sh::kBKBytes);
+    cs[g] = c * escale(0, g, false);
+    cs[8 + g] = -c * ts->O[0][g];
+    cs[16 + g] = c * a.alpha * escale(1, g, false);
+    cs[24 + g] = -c * a.alpha * ts->O[1][g];
+  }
+}
+
 template <int W, int GP>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) {
   using Sh = Shape<W, GP>;
   constexpr int NPM = Sh::NPM, NP = Sh::NP, GH = Sh::GH;
+  static_assert(Scratch<GP>::kPrep * 4 <= 2 * Sh::kBVBuf && Scratch<GP>::kHalf * 4 <= 2 * Sh::kBVBuf,
+                "query transform or half-merge scratch exceeds the value-weight buffers");
+  static_assert(Scratch<GP>::kMerge * 4 <= Sh::kOffMisc - Sh::kOffBK, "merge scratch exceeds the weight tables");
   constexpr float kWS = 256.f;  // attention weights carry 2^8: up to 2^14 in f16
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -252,12 +576,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       mbar_init(smem_u32(&ms->ld_full[s]), 1);
       mbar_init(smem_u32(&ms->ld_empty[s]), 2);
     }
+    mbar_init(smem_u32(&ms->tab_full), 1);
     ms->abort = 0;
     fence_mbar_init();
   }
-  // weight operands start at zero (columns of absent heads are never written)
-  for (int e = threadIdx.x; e < 2 * Sh::kBVBuf / 16; e += kThreads)
-    reinterpret_cast<uint4*>(smem + Sh::kOffBV)[e] = make_uint4(0u, 0u, 0u, 0u);
+  // (every tile rewrites the whole value-weight buffer it uses, zeros for absent
+  // heads and tokens, so the buffers need no initial value)
+  // The codebook coefficients stay in flight in a register until each segment
+  // publishes them; the two matrices of the unit merge are brought into L2.
+  const float cf_ld = threadIdx.x < NPM ? __ldg(a.walsh + (threadIdx.x < W ? (1 << threadIdx.x) : 7)) : 0.f;
+  for (int e = threadIdx.x; e < 2 * kD * kD / 32; e += kThreads) {
+    const float* line = e < kD * kD / 32 ? a.pi + 32 * e : a.s_rot + 32 * (e - kD * kD / 32);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+  }
   __syncthreads();
   volatile int* abort_flag = &ms->abort;
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -303,6 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
     }
   };
   if (threadIdx.x == 0) issue_upto(0);
+  // the query tables and arrival counters come from unit_table_kernel, which may
+  // still be running (programmatic dependent launch): wait for it to complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int w = warp, kbk = w >> 1, g2 = w & 1, vrow = w & 7, hf = w >> 3;
   // Score rows gq, gq + 8 <-> tokens tok, tok + 1 of the tile (block kbk).
@@ -320,12 +654,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   float M[GH], lsum[GH], pend[GH], A0[GH], B0[GH], A1[GH], B1[GH];
   int64_t gi = 0;
   int segc = 0;
+  uint32_t tab_phase = 0u;
   for (int64_t f = f0; f < f1; ++segc) {
     int64_t next;
     const Seg sg = segment_at(a, f, f1, &next);
     f = next;
     const int b = (int)(sg.u / a.Hkv), h = (int)(sg.u - (int64_t)b * a.Hkv);
     const int head0 = b * a.Hq + h * a.G;
+    if (threadIdx.x < NPM) ms->cf[threadIdx.x] = cf_ld;  // read after the next CTA barrier
 #pragma unroll
     for (int P = 0; P < NP; ++P)
 #pragma unroll
@@ -335,87 +671,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
     for (int hh = 0; hh < GH; ++hh) M[hh] = -INFINITY, lsum[hh] = 0.f, pend[hh] = 1.f;
     if (sg.n > 0) {
-      // ---- query weights of this unit (f16 hi + lo, scale E per part and head) and offsets O;
-      // both halves must be done with the previous unit's table first
+      // ---- this unit's query table (unit_table_kernel): one bulk copy once both
+      // halves are done with the previous unit's table (the unit merge also
+      // writes the region through the generic proxy)
       cta_sync();
-      for (int e = threadIdx.x; e < Sh::kBKBytes / 16; e += kThreads)
-        reinterpret_cast<uint4*>(BK)[e] = make_uint4(0, 0, 0, 0);
-      if (threadIdx.x < 16) {
-        ms->amax[threadIdx.x >> 3][threadIdx.x & 7] = 0.f;
-        ms->O[threadIdx.x >> 3][threadIdx.x & 7] = 0.f;
+      if (threadIdx.x == 0) {
+        fence_proxy_async_smem();
+        const uint32_t bar = smem_u32(&ms->tab_full);
+        const uint8_t* src = a.tables + (size_t)sg.u * Table<W, GP>::kBytes;
+        mbar_arrive_expect_tx(bar, Table<W, GP>::kBytes);
+        bulk_load(smem_u32(BK), src, Sh::kBKBytes, bar);
+        bulk_load(smem_u32(&ms->consts[0][0]), src + Sh::kBKBytes, Table<W, GP>::kConstBytes, bar);
       }
-      cta_sync();
-      // coordinate j: word kw, bit x = 16e + L; L = 8·ks2 + 4·hi + q -> K index 8·hi + 2q + e
-      const int j = threadIdx.x & (kD - 1);
-      const bool setup = threadIdx.x < kD;
-      const int kw = j >> 5, e16 = (j >> 4) & 1, L = j & 15, ks2 = L >> 3, hi = (L >> 2) & 1, q4 = L & 3;
-      const int kk = 8 * hi + 2 * q4 + e16;
-      // exponent-kind operand (hi = 0): s = (F - mean)·2/δ; sign kind: s = -F
-      const float wsc = hi ? -1.f : 2.f / kExpDelta;
-      float qv[GP], sv[GP], cf[NPM];
+      wait(&ms->tab_full, tab_phase);
+      tab_phase ^= 1u;
 #pragma unroll
-      for (int P = 0; P < NPM; ++P) cf[P] = __ldg(a.walsh + (P < W ? (1 << P) : 7));
-      if (setup) {
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          qv[g] = g < a.G ? __ldg(a.qt + (size_t)(head0 + g) * kD + j) : 0.f;
-          sv[g] = g < a.G ? __ldg(a.st + (size_t)(head0 + g) * kD + j) : 0.f;
-          float am = 0.f;
-#pragma unroll
-          for (int P = 0; P < NPM; ++P) am = fmaxf(am, fabsf(wsc * cf[P] * qv[g]));
-          float aq = fabsf(wsc * sv[g]);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-            aq = fmaxf(aq, __shfl_xor_sync(0xffffffffu, aq, o));
-          }
-          if (lane == 0) {
-            atomicMax(reinterpret_cast<int*>(&ms->amax[0][g]), __float_as_int(am));
-            atomicMax(reinterpret_cast<int*>(&ms->amax[1][g]), __float_as_int(aq));
-          }
-        }
-      }
-      cta_sync();
-      auto escale = [&](int p, int g) {  // power of two taking the part's largest weight below 2^12
-        const float am = ms->amax[p][g];
-        int ex;
-        frexpf(am, &ex);
-        return am > 0.f ? ldexpf(1.f, ex - 12) : 1.f;
-      };
-      if (setup) {
-        __half* bk = reinterpret_cast<__half*>(BK);
-#pragma unroll
-        for (int P = 0; P < NP; ++P) {
-          const int part = P < NPM ? 0 : 1;
-          const int ks = (P * 4 + kw) * 2 + ks2;
-#pragma unroll
-          for (int g = 0; g < GP; ++g) {
-            const float E = escale(part, g);
-            const float x = wsc * (part == 0 ? cf[P < NPM ? P : 0] * qv[g] : sv[g]) / E;
-            const __half xh = __float2half_rn(x), xl = __float2half_rn(x - __half2float(xh));
-            // (k, n) sits in lane (n, k % 8 / 2), fragment k / 8, half k % 2
-            const int base = ((((ks * GH + (g >> 2)) * 8 + 2 * (g & 3)) * 4 + ((kk & 7) >> 1)) * 2 + (kk >> 3)) * 2 +
-                             (kk & 1);
-            bk[base] = xh;
-            bk[base + 16] = xl;
-            float o = hi ? 0.f : (__half2float(xh) + __half2float(xl)) * E * kExpMean;
-#pragma unroll
-            for (int sh = 16; sh > 0; sh >>= 1) o += __shfl_xor_sync(0xffffffffu, o, sh);
-            if (lane == 0) atomicAdd(&ms->O[part][g], o);
-          }
-        }
-      }
-      cta_sync();
-      {
-        const float c = a.scale * kLog2e;
-#pragma unroll
-        for (int hh = 0; hh < GH; ++hh) {
-          const int g = 4 * hh + tig;
-          A0[hh] = c * escale(0, g);
-          B0[hh] = -c * ms->O[0][g];
-          A1[hh] = c * a.alpha * escale(1, g);
-          B1[hh] = -c * a.alpha * ms->O[1][g];
-        }
+      for (int hh = 0; hh < GH; ++hh) {
+        const int g = 4 * hh + tig;
+        A0[hh] = ms->consts[0][g];
+        B0[hh] = ms->consts[1][g];
+        A1[hh] = ms->consts[2][g];
+        B1[hh] = ms->consts[3][g];
       }
       auto bfrag = [&](int ks, int ht) -> uint2 {
         return reinterpret_cast<const uint2*>(BK)[((ks * GH + ht) * 8 + gq) * 4 + tig];
@@ -641,8 +917,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       vote_step(false, true, gi + sg.n);
       gi += sg.n;
     }
-    // ---- partials of this CTA for the unit: one per half (slot 2·slot + half),
-    // each over its own tokens with its own reference
+    // ---- the partial of this CTA for the unit: the two halves, each over its
+    // own tokens with its own reference, merged on chip (half 1 hands its share
+    // to half 0 through the value-weight buffers)
     const int sp = segc & 1;
 #pragma unroll
     for (int hh = 0; hh < GH; ++hh) {
@@ -650,36 +927,71 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
       if (gq == 0) ms->lred[sp][w][4 * hh + tig] = l;
+      if (vrow == 0 && gq == 0) ms->Mh[hf][4 * hh + tig] = M[hh];
     }
-    half_sync(hf);
-    float cf[NPM];
+    cta_sync();
+    {
+      float cf[NPM];
 #pragma unroll
-    for (int P = 0; P < NPM; ++P) cf[P] = __ldg(a.walsh + (P < W ? (1 << P) : 7));
+      for (int P = 0; P < NPM; ++P) cf[P] = ms->cf[P];
+      float* hs = reinterpret_cast<float*>(smem + Sh::kOffBV);  // [GP][acc_rot 128 | acc_sgn 128]
+      float rot[GH][2], sgn[GH][2], Mx[GH], f0[GH], f1[GH];
 #pragma unroll
-    for (int hh = 0; hh < GH; ++hh) {
-      const int head = 4 * hh + tig;
-      if (head < a.G) {
-        float* pp = a.part + ((size_t)(head0 + head) * a.smax + 2 * sg.slot + hf) * (2 + 2 * kD);
+      for (int hh = 0; hh < GH; ++hh) {
+        const int head = 4 * hh + tig;
+        const float M0 = ms->Mh[0][head], M1 = ms->Mh[1][head];
+        Mx[hh] = fmaxf(M0, M1);
+        f0[hh] = M0 == -INFINITY ? 0.f : exp2f(M0 - Mx[hh]);
+        f1[hh] = M1 == -INFINITY ? 0.f : exp2f(M1 - Mx[hh]);
         // fragment e = 2·row + piece; the value operand is -s, so sums enter negated
-        float rot[2], sgn[2];
+        const float fs = -(hf ? f1[hh] : f0[hh]) * (1.f / kWS);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           float x = 0.f;
 #pragma unroll
           for (int P = 0; P < NPM; ++P) x = fmaf(cf[P], vacc[P][hh][2 * r] + vacc[P][hh][2 * r + 1], x);
-          rot[r] = -x * (1.f / kWS);
-          sgn[r] = -(vacc[NPM][hh][2 * r] + vacc[NPM][hh][2 * r + 1]) * (1.f / kWS);
+          rot[hh][r] = x * fs;
+          sgn[hh][r] = (vacc[NPM][hh][2 * r] + vacc[NPM][hh][2 * r + 1]) * fs;
         }
-        *reinterpret_cast<float2*>(pp + 2 + crd) = make_float2(rot[0], rot[1]);
-        *reinterpret_cast<float2*>(pp + 2 + kD + crd) = make_float2(sgn[0], sgn[1]);
-        if (vrow == 0 && gq == 0) {
-          float l = 0.f;
-#pragma unroll
-          for (int q = 0; q < kNW / 2; ++q) l += ms->lred[sp][8 * hf + q][head];
-          pp[0] = M[hh];
-          pp[1] = l;
+        if (hf == 1) {
+          *reinterpret_cast<float2*>(hs + head * 2 * kD + crd) = make_float2(rot[hh][0], rot[hh][1]);
+          *reinterpret_cast<float2*>(hs + head * 2 * kD + kD + crd) = make_float2(sgn[hh][0], sgn[hh][1]);
         }
       }
+      cta_sync();
+      if (hf == 0) {
+#pragma unroll
+        for (int hh = 0; hh < GH; ++hh) {
+          const int head = 4 * hh + tig;
+          if (head < a.G) {
+            float* pp = a.part + ((size_t)(head0 + head) * a.smax + sg.slot) * (2 + 2 * kD);
+            const float2 hr = *reinterpret_cast<const float2*>(hs + head * 2 * kD + crd);
+            const float2 hq = *reinterpret_cast<const float2*>(hs + head * 2 * kD + kD + crd);
+            *reinterpret_cast<float2*>(pp + 2 + crd) = make_float2(rot[hh][0] + hr.x, rot[hh][1] + hr.y);
+            *reinterpret_cast<float2*>(pp + 2 + kD + crd) = make_float2(sgn[hh][0] + hq.x, sgn[hh][1] + hq.y);
+            if (vrow == 0 && gq == 0) {
+              float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+              for (int q = 0; q < kNW / 2; ++q) l0 += ms->lred[sp][q][head], l1 += ms->lred[sp][8 + q][head];
+              pp[0] = Mx[hh];
+              pp[1] = fmaf(f0[hh], l0, f1[hh] * l1);
+            }
+          }
+        }
+      }
+    }
+    // ---- the last CTA of the unit to hand in its partial merges them all
+    __threadfence();
+    cta_sync();
+    if (threadIdx.x == 0) {
+      const int64_t nct = owner((sg.u + 1) * a.tpu - 1, a.total, C) - owner(sg.u * a.tpu, a.total, C) + 1;
+      ms->last = atomicAdd(a.arrivals + sg.u, 1u) == (unsigned)(nct - 1);
+      if (ms->last) __threadfence();
+    }
+    cta_sync();
+    if (ms->last) {
+      const int ns = (int)(owner((sg.u + 1) * a.tpu - 1, a.total, C) - owner(sg.u * a.tpu, a.total, C) + 1);
+      unit_merge<GP>(a, head0, ns, reinterpret_cast<float*>(smem + Sh::kOffBK));
     }
   }
   // no copy of this CTA may be in flight when it exits
@@ -695,8 +1007,8 @@ namespace tq {
 
 int64_t decode_tc_tpu(int64_t ctx_stride) { return (ctx_stride + kTile - 1) / kTile; }
 
-// Partial slots per unit for a grid of `ctas` CTAs over units * tpu tiles: two
-// per CTA that touches the unit (one per half of its warps).
+// Partial slots per unit for a grid of `ctas` CTAs over units * tpu tiles: one
+// per CTA that touches the unit.
 int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas) {
   const int64_t total = units * tpu;
   int64_t smax = 1;
@@ -704,26 +1016,43 @@ int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas) {
     const int64_t s = owner((u + 1) * tpu - 1, total, ctas) - owner(u * tpu, total, ctas) + 1;
     smax = std::max(smax, s);
   }
-  return 2 * (int)smax;  // one partial per half of each CTA
+  return (int)smax;  // one partial per CTA
 }
 
-int decode_tc_ctas(int64_t units, int64_t tpu) { return (int)std::min<int64_t>(units * tpu, sm_count()); }
+int decode_tc_ctas(int64_t units, int64_t tpu) {
+  return (int)std::min<int64_t>(units * tpu, std::min(sm_count(), kMaxCtas));
+}
 
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride) {
   return plan->d == 128 && plan->m == 128 && G >= 1 && G <= 8 && V->layout == TQ_LAYOUT_BLOCK32 &&
          ctx_stride % kHalfTile == 0;
 }
 
-tq_status launch_decode_tc(const tq_plan* plan, const tq_records* K, const tq_records* V, const int32_t* ctx_len,
-                           int B, int Hq, int Hkv, int64_t ctx_stride, float scale, const float* qt, const float* st,
-                           float* part, int smax, cudaStream_t stream) {
+size_t decode_tc_table_bytes(int w, int G) {
+  const bool g8 = G > 4;
+  switch (w) {
+    case 1: return g8 ? Table<1, 8>::kBytes : Table<1, 4>::kBytes;
+    case 2: return g8 ? Table<2, 8>::kBytes : Table<2, 4>::kBytes;
+    default: return g8 ? Table<3, 8>::kBytes : Table<3, 4>::kBytes;
+  }
+}
+
+tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype, const tq_records* K,
+                           const tq_records* V, const int32_t* ctx_len, int B, int Hq, int Hkv, int64_t ctx_stride,
+                           float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
+                           cudaStream_t stream) {
   TcArgs a{};
   a.kidx = K->idx; a.ksgn = K->sgn; a.knorm = K->norm; a.krnorm = K->rnorm;
   a.vidx = V->idx; a.vsgn = V->sgn; a.vnorm = V->norm; a.vrnorm = V->rnorm;
   a.ctx_len = ctx_len;
   a.ctx_stride = ctx_stride;
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
-  a.qt = qt; a.st = st;
+  a.q = q;
+  a.q_bf16 = q_dtype == TQ_BF16;
+  a.pi = plan->pi; a.pi_t = plan->pi_t; a.s_rot = plan->s_rot; a.s_rot_t = plan->s_rot_t;
+  a.tables = tables;
+  a.arrivals = arrivals;
+  a.out = out;
   a.walsh = plan->walsh;
   a.scale = scale;
   a.alpha = plan->qjl_alpha;
@@ -733,19 +1062,38 @@ tq_status launch_decode_tc(const tq_plan* plan, const tq_records* K, const tq_re
   a.total = (int64_t)B * Hkv * a.tpu;
   a.fault = fault_word();
   if (!a.fault) return TQ_ERR_CUDA;
-  const int grid = decode_tc_ctas((int64_t)B * Hkv, a.tpu);
-  auto go = [&](auto kern, int smem) -> tq_status {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  const int units = B * Hkv;
+  const int grid = decode_tc_ctas(units, a.tpu);
+  // the per-unit query tables (and zeroed arrival counters), then the decode
+  auto go = [&](auto table_kern, int table_smem, auto kern, int smem) -> tq_status {
+    if (cudaFuncSetAttribute(table_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, table_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    kern<<<grid, kThreads, smem, stream>>>(a);
+    table_kern<<<units, kThreads, table_smem, stream>>>(a);
+    if (launch_status() != TQ_OK) return TQ_ERR_CUDA;
+    // the decode kernel's prologue and first copies overlap the table kernel
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
   };
+#define TQ_DECODE_TC_GO(W_, GP_) \
+  go(unit_table_kernel<W_, GP_>, table_smem_bytes<W_, GP_>(), decode_tc_kernel<W_, GP_>, smem_bytes<W_>())
   const bool g8 = a.G > 4;
   switch (plan->w) {
-    case 1: return g8 ? go(decode_tc_kernel<1, 8>, smem_bytes<1>()) : go(decode_tc_kernel<1, 4>, smem_bytes<1>());
-    case 2: return g8 ? go(decode_tc_kernel<2, 8>, smem_bytes<2>()) : go(decode_tc_kernel<2, 4>, smem_bytes<2>());
-    default: return g8 ? go(decode_tc_kernel<3, 8>, smem_bytes<3>()) : go(decode_tc_kernel<3, 4>, smem_bytes<3>());
+    case 1: return g8 ? TQ_DECODE_TC_GO(1, 8) : TQ_DECODE_TC_GO(1, 4);
+    case 2: return g8 ? TQ_DECODE_TC_GO(2, 8) : TQ_DECODE_TC_GO(2, 4);
+    default: return g8 ? TQ_DECODE_TC_GO(3, 8) : TQ_DECODE_TC_GO(3, 4);
   }
+#undef TQ_DECODE_TC_GO
 }
 
 }  // namespace tq

@@ -54,14 +54,20 @@ tq_status quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_
                       int64_t row0, cudaStream_t st);
 
 // Tensor-core decode (tq_decode_tc.cu): d = m = 128, G <= 8, values in
-// TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Partials [B*Hq][slots][2 + 256];
-// each (batch, kv head) unit is cut into decode_tc_tpu(ctx_stride) tiles.
+// TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Two launches: one CTA per
+// (batch, kv head) unit builds its query table (decode_tc_table_bytes(w, G)
+// bytes, 16-byte aligned) and zeroes its arrival counter; the decode kernel
+// then does the scores, softmax and values, and the last CTA of each unit
+// merges the unit's partials ([B*Hq][smax][2 + 256]) into out.  Each unit is
+// cut into decode_tc_tpu(ctx_stride) tiles.
 int64_t decode_tc_tpu(int64_t ctx_stride);
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride);
 int decode_tc_ctas(int64_t units, int64_t tpu);
 int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas);
-tq_status launch_decode_tc(const tq_plan* plan, const tq_records* K, const tq_records* V, const int32_t* ctx_len,
-                           int B, int Hq, int Hkv, int64_t ctx_stride, float scale, const float* qt, const float* st,
-                           float* part, int smax, cudaStream_t stream);
+size_t decode_tc_table_bytes(int w, int G);
+tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype, const tq_records* K,
+                           const tq_records* V, const int32_t* ctx_len, int B, int Hq, int Hkv, int64_t ctx_stride,
+                           float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
+                           cudaStream_t stream);
 
 }  // namespace tq
