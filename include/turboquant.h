@@ -159,6 +159,18 @@ typedef struct tq_records {
 tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
                       const tq_records* out, int64_t out_offset, tq_stream stream);
 
+/* tq_quantize of two inputs of the same shape -- the key and value rows of
+ * the same tokens -- in one call: x0 -> rows [out_offset, out_offset + n) of
+ * out0 and x1 -> the same rows of out1 (each output in its own layout).
+ * Results are those of the two tq_quantize calls; where the tensor-core
+ * quantizer applies (bf16, d = m = 128, and out_offset % 32 == 0 for a block
+ * layout output) both run in one launch, which starts and drains its
+ * pipeline once.  Same arguments, ownership and errors as tq_quantize, for
+ * each of the two; out0 and out1 must not overlap. */
+tq_status tq_quantize_pair(const tq_plan* plan, const void* x0, const void* x1, tq_dtype dtype, int64_t n,
+                           int64_t ld_x, const tq_records* out0, const tq_records* out1, int64_t out_offset,
+                           tq_stream stream);
+
 /* ------------------------------------------------------------------ decode
  * One decode step of GQA softmax attention over compressed K/V caches.
  * Per query head g (kv head h = g / (Hq/Hkv)) and token t < ctx_len[b]:

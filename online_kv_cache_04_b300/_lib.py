@@ -44,6 +44,8 @@ _SIGNATURES = {
                                     _c_double_p, _c_double_p, _c_double_p, _vp, ctypes.c_size_t, _vp]),
     "tq_quantize": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.POINTER(tq_records), ctypes.c_int64, _vp]),
+    "tq_quantize_pair": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, _vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), ctypes.c_int64, _vp]),
     "tq_decode_workspace_size": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]),
     "tq_decode_attention": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -208,6 +210,16 @@ def tq_quantize(plan, x, out, out_offset=0, stream=None):
     ld = x.stride(0) if x.dim() == 2 and n > 0 else plan.d
     _check("tq_quantize", load().tq_quantize(plan.ref, x.data_ptr(), _dtype_code(x), n, ld, out.ref, out_offset,
                                              _stream(stream)))
+
+
+def tq_quantize_pair(plan, x0, x1, out0, out1, out_offset=0, stream=None):
+    """Quantize x0 into out0 and x1 into out1 (same shape, dtype and row stride), rows out_offset onward."""
+    if x0.shape != x1.shape or x0.dtype != x1.dtype or x0.stride() != x1.stride():
+        raise ValueError("tq_quantize_pair: x0 and x1 must have the same shape, dtype and strides")
+    n = x0.shape[0]
+    ld = x0.stride(0) if x0.dim() == 2 and n > 0 else plan.d
+    _check("tq_quantize_pair", load().tq_quantize_pair(plan.ref, x0.data_ptr(), x1.data_ptr(), _dtype_code(x0), n, ld,
+                                                       out0.ref, out1.ref, out_offset, _stream(stream)))
 
 
 def tq_decode_workspace_size(plan, B, Hq, Hkv, ctx_stride):

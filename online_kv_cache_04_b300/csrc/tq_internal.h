@@ -49,9 +49,11 @@ unsigned* fault_word();
 
 // tcgen05 quantizer (bf16 input, d = m = 128); rows already offset.
 bool quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n);
-// Rows [row0, row0 + n) of `out`; for TQ_LAYOUT_BLOCK32, row0 % 32 == 0.
-tq_status quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, const tq_records* out,
-                      int64_t row0, cudaStream_t st);
+// x0 -> rows [row0, row0 + n) of out0 and, when x1 and out1 are given, x1 ->
+// the same rows of out1, in one launch; for a TQ_LAYOUT_BLOCK32 output,
+// row0 % 32 == 0.
+tq_status quantize_tc(const tq_plan* plan, const void* x0, const void* x1, int64_t n, int64_t ld_x,
+                      const tq_records* out0, const tq_records* out1, int64_t row0, cudaStream_t st);
 
 // Tensor-core decode (tq_decode_tc.cu): d = m = 128, G <= 8, values in
 // TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Two launches: one CTA per

@@ -90,7 +90,6 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
       const int64_t row = v0 + v;
       xs[e] = row < a.n ? load_elem<T>(x + row * a.ld + i) : 0.0f;
     }
-    if (tid < TV) rsq[tid] = 0.0f;
     __syncthreads();
     for (int v = warp; v < TV; v += kThreads / 32) {
       float s = 0.0f;
@@ -137,8 +136,6 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
           for (int p = 0; p < 3; ++p)
             if (p < w && ((idx >> p) & 1)) pbits[p][k] |= bit;
         }
-        const float r2 = warp_sum(rho * rho);
-        if (lane == 0) atomicAdd(&rsq[v], r2);
       }
       if constexpr (LAYOUT == TQ_LAYOUT_BLOCK32) {
         for (int p = 0; p < w; ++p) {
@@ -146,6 +143,14 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
           merge_block_word(w0, w0 + w * d, pbits[p], mask);
         }
       }
+    }
+    __syncthreads();
+    // ||ρ||² per vector in a fixed order (the records do not depend on scheduling)
+    for (int v = warp; v < TV; v += kThreads / 32) {
+      float s2 = 0.0f;
+      for (int i = lane; i < d; i += 32) s2 = fmaf(rs[v * d + i], rs[v * d + i], s2);
+      s2 = warp_sum(s2);
+      if (lane == 0) rsq[v] = s2;
     }
     __syncthreads();
 
@@ -236,7 +241,8 @@ extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dt
   a.row0 = out_offset;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (rows) {
-    if (tq::quantize_tc_supported(plan, dtype, n)) return tq::quantize_tc(plan, x, n, ld_x, out, out_offset, st);
+    if (tq::quantize_tc_supported(plan, dtype, n))
+      return tq::quantize_tc(plan, x, nullptr, n, ld_x, out, nullptr, out_offset, st);
     return launch_simt_any<TQ_LAYOUT_ROWS>(a, dtype, st);
   }
   // 32-row blocks: rows up to the first block boundary go through the SIMT
@@ -252,7 +258,8 @@ extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dt
   const int64_t rest = n - head;
   const size_t esz = dtype == TQ_F32 ? 4 : 2;
   const void* xr = static_cast<const char*>(x) + head * ld_x * esz;
-  if (tq::quantize_tc_supported(plan, dtype, rest)) return tq::quantize_tc(plan, xr, rest, ld_x, out, out_offset + head, st);
+  if (tq::quantize_tc_supported(plan, dtype, rest))
+    return tq::quantize_tc(plan, xr, nullptr, rest, ld_x, out, nullptr, out_offset + head, st);
   QuantArgs r = a;
   r.x = xr;
   r.n = rest;
@@ -260,4 +267,24 @@ extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dt
   r.rnorm += head;
   r.row0 = out_offset + head;
   return launch_simt_any<TQ_LAYOUT_BLOCK32>(r, dtype, st);
+}
+
+extern "C" tq_status tq_quantize_pair(const tq_plan* plan, const void* x0, const void* x1, tq_dtype dtype, int64_t n,
+                                      int64_t ld_x, const tq_records* out0, const tq_records* out1,
+                                      int64_t out_offset, tq_stream stream) {
+  // the same checks as tq_quantize, for both pairs, before anything is launched
+  if (!tq::valid_plan(plan) || !tq::valid_records(out0) || !tq::valid_records(out1) || n < 0 || out_offset < 0)
+    return TQ_ERR_ARG;
+  if (dtype != TQ_F32 && dtype != TQ_BF16) return TQ_ERR_ARG;
+  if (n == 0) return TQ_OK;
+  for (const void* x : {x0, x1})
+    if (x == nullptr || !tq::aligned16(x) || ld_x < plan->d || ld_x % 8 != 0) return TQ_ERR_ARG;
+  for (const tq_records* o : {out0, out1})
+    if (out_offset > o->capacity || n > o->capacity - out_offset) return TQ_ERR_ARG;
+  const bool aligned = out_offset % 32 == 0 ||
+                       (out0->layout == TQ_LAYOUT_ROWS && out1->layout == TQ_LAYOUT_ROWS);
+  if (tq::quantize_tc_supported(plan, dtype, n) && aligned)
+    return tq::quantize_tc(plan, x0, x1, n, ld_x, out0, out1, out_offset, reinterpret_cast<cudaStream_t>(stream));
+  const tq_status s = tq_quantize(plan, x0, dtype, n, ld_x, out0, out_offset, stream);
+  return s != TQ_OK ? s : tq_quantize(plan, x1, dtype, n, ld_x, out1, out_offset, stream);
 }

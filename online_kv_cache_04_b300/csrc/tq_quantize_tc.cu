@@ -58,12 +58,22 @@ struct Bars {
 
 static_assert(sizeof(Bars) <= 256, "barriers must fit their shared-memory region");
 
-struct TcArgs {
-  int64_t n;
+// One output of a launch: the records of `n` input rows.
+struct TcOut {
   uint32_t* idx;           // TQ_LAYOUT_ROWS: row 0 of this call; TQ_LAYOUT_BLOCK32: block of row 0
   uint32_t* sgn;
   float* norm;             // row 0 of this call
   float* rnorm;
+  int64_t n;
+  int layout;              // tq_layout
+};
+
+// A launch quantizes one or two inputs of 128-row tiles: tiles [0, ntiles0) are
+// input 0's, the rest input 1's (the keys and values of the same tokens, say),
+// so that one persistent grid fills and drains its pipeline once for both.
+struct TcArgs {
+  TcOut out0, out1;
+  int64_t ntiles0, ntiles;
   const float* centroids;  // device [2^w]
   const float* bounds;     // device [2^w - 1]
   unsigned* fault;
@@ -112,16 +122,17 @@ __device__ __forceinline__ void store_block32(uint32_t* blk, const uint32_t (&wo
   }
 }
 
-template <int W, int LAYOUT>
+template <int W>
 __global__ void __launch_bounds__(kThreads, 1)
-    quantize_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi,
+    quantize_tc_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
+                       const __grid_constant__ CUtensorMap tm_pi,
                        const __grid_constant__ CUtensorMap tm_s, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t base = smem_u32(smem);
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ntiles = (a.n + kTile - 1) / kTile;
+  const int64_t ntiles = a.ntiles;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->b_full), 1);
@@ -141,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kTmaWarp && lane == 0) {
-    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_x0);
+    if (a.ntiles > a.ntiles0) tma_prefetch_desc(&tm_x1);
     tma_prefetch_desc(&tm_pi);
     tma_prefetch_desc(&tm_s);
   }
@@ -166,8 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t xf = smem_u32(&bars->x_full[s]);
         mbar_arrive_expect_tx(xf, kMatBytes);
         const uint32_t dst = base + kOffX + s * kMatBytes;
-        tma_load_2d(dst, &tm_x, 0, (int32_t)(tile * kTile), xf);
-        tma_load_2d(dst + kBoxBytes, &tm_x, 64, (int32_t)(tile * kTile), xf);
+        const bool second = tile >= a.ntiles0;
+        const CUtensorMap* tm = second ? &tm_x1 : &tm_x0;
+        const int32_t y = (int32_t)((tile - (second ? a.ntiles0 : 0)) * kTile);
+        tma_load_2d(dst, tm, 0, y, xf);
+        tma_load_2d(dst + kBoxBytes, tm, 64, y, xf);
         last_k[s] = k;
       }
       // no copy of this CTA may still be in flight when it exits
@@ -341,20 +356,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->rsq_full[s]));
       }
-      const int64_t row = tile * kTile + r;
-      const int64_t blk_row = tile * kTile + q * 32;  // this warp's block (layout 1)
-      const uint32_t valid = __ballot_sync(0xffffffffu, row < a.n);
-      if constexpr (LAYOUT == TQ_LAYOUT_ROWS) {
-        if (row < a.n) {
+      // this tile's output (fields picked one by one: no dynamic index into the parameters)
+      const bool second = tile >= a.ntiles0;
+      const int64_t lt = tile - (second ? a.ntiles0 : 0), on = second ? a.out1.n : a.out0.n;
+      const bool rows_layout = (second ? a.out1.layout : a.out0.layout) == TQ_LAYOUT_ROWS;
+      uint32_t* const oidx = second ? a.out1.idx : a.out0.idx;
+      const int64_t row = lt * kTile + r;
+      const int64_t blk_row = lt * kTile + q * 32;  // this warp's block (block layout)
+      const uint32_t valid = __ballot_sync(0xffffffffu, row < on);
+      if (rows_layout) {
+        if (row < on) {
 #pragma unroll
           for (int p = 0; p < W; ++p)
-            *reinterpret_cast<uint2*>(a.idx + row * (4 * W) + p * 4 + 2 * h) = make_uint2(planes[p][0], planes[p][1]);
+            *reinterpret_cast<uint2*>(oidx + row * (4 * W) + p * 4 + 2 * h) = make_uint2(planes[p][0], planes[p][1]);
         }
       } else {
         if (valid != 0u) {
 #pragma unroll
           for (int p = 0; p < W; ++p)
-            store_block32<2>(a.idx + (blk_row >> 5) * (W * 128) + p * 128 + 64 * h, planes[p], valid, lane);
+            store_block32<2>(oidx + (blk_row >> 5) * (W * 128) + p * 128 + 64 * h, planes[p], valid, lane);
         }
       }
       if (!mbar_wait(smem_u32(&bars->p_full[s]), ph, a.fault, kFaultWait)) break;
@@ -374,16 +394,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[s]));
-      if constexpr (LAYOUT == TQ_LAYOUT_ROWS) {
-        if (row < a.n) *reinterpret_cast<uint2*>(a.sgn + row * 4 + 2 * h) = make_uint2(sg[0], sg[1]);
+      uint32_t* const osgn = second ? a.out1.sgn : a.out0.sgn;
+      if (rows_layout) {
+        if (row < on) *reinterpret_cast<uint2*>(osgn + row * 4 + 2 * h) = make_uint2(sg[0], sg[1]);
       } else {
-        if (valid != 0u) store_block32<2>(a.sgn + (blk_row >> 5) * 128 + 64 * h, sg, valid, lane);
+        if (valid != 0u) store_block32<2>(osgn + (blk_row >> 5) * 128 + 64 * h, sg, valid, lane);
       }
       if (h == 0) {
         if (!mbar_wait(smem_u32(&bars->rsq_full[s]), ph, a.fault, kFaultWait)) break;
-        if (row < a.n) {
-          a.norm[row] = n;
-          a.rnorm[row] = n * sqrtf(rsq + rsq_s[(it >> 1 & 1) * 128 + r]);
+        if (row < on) {
+          (second ? a.out1.norm : a.out0.norm)[row] = n;
+          (second ? a.out1.rnorm : a.out0.rnorm)[row] = n * sqrtf(rsq + rsq_s[(it >> 1 & 1) * 128 + r]);
         }
       }
     }
@@ -422,15 +443,14 @@ bool map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int W, int LAYOUT>
-tq_status launch_w(const CUtensorMap& mx, const CUtensorMap& mp, const CUtensorMap& ms, const TcArgs& a,
-                   cudaStream_t st) {
-  auto kern = quantize_tc_kernel<W, LAYOUT>;
+template <int W>
+tq_status launch_w(const CUtensorMap& mx0, const CUtensorMap& mx1, const CUtensorMap& mp, const CUtensorMap& ms,
+                   const TcArgs& a, cudaStream_t st) {
+  auto kern = quantize_tc_kernel<W>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return TQ_ERR_CUDA;
-  const int64_t ntiles = (a.n + kTile - 1) / kTile;
-  const int grid = (int)std::min<int64_t>(ntiles, tq::sm_count());
-  kern<<<grid, kThreads, kSmemBytes, st>>>(mx, mp, ms, a);
+  const int grid = (int)std::min<int64_t>(a.ntiles, tq::sm_count());
+  kern<<<grid, kThreads, kSmemBytes, st>>>(mx0, mx1, mp, ms, a);
   return tq::launch_status();
 }
 
@@ -446,36 +466,43 @@ bool tq::quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n) {
   return plan->d == 128 && plan->m == 128 && dtype == TQ_BF16 && n < (int64_t(1) << 31) && encode_fn() != nullptr;
 }
 
-tq_status tq::quantize_tc(const tq_plan* plan, const void* x, int64_t n, int64_t ld_x, const tq_records* out,
-                          int64_t row0, cudaStream_t st) {
+// Output fields of rows [row0, row0 + n) of `out`.
+static TcOut tc_out(const tq_records* out, int64_t n, int64_t row0, int w) {
   const bool rows = out->layout == TQ_LAYOUT_ROWS;
-  if (!rows && row0 % 32 != 0) return TQ_ERR_ARG;
-  CUtensorMap mx, mp, ms;
-  if (!map_bf16(&mx, x, (uint64_t)n, 128, (uint64_t)ld_x) || !map_bf16(&mp, plan->pi_bf16, 256, 128, 128) ||
-      !map_bf16(&ms, plan->s_bf16, 256, 128, 128))
+  TcOut o;
+  o.idx = rows ? out->idx + row0 * (w * 4) : out->idx + (row0 / 32) * (w * 128);
+  o.sgn = rows ? out->sgn + row0 * 4 : out->sgn + (row0 / 32) * 128;
+  o.norm = out->norm + row0;
+  o.rnorm = out->rnorm + row0;
+  o.n = n;
+  o.layout = out->layout;
+  return o;
+}
+
+tq_status tq::quantize_tc(const tq_plan* plan, const void* x0, const void* x1, int64_t n, int64_t ld_x,
+                          const tq_records* out0, const tq_records* out1, int64_t row0, cudaStream_t st) {
+  for (const tq_records* o : {out0, out1})
+    if (o != nullptr && o->layout != TQ_LAYOUT_ROWS && row0 % 32 != 0) return TQ_ERR_ARG;
+  const bool pair = x1 != nullptr && out1 != nullptr;
+  CUtensorMap mx0, mx1, mp, ms;
+  if (!map_bf16(&mx0, x0, (uint64_t)n, 128, (uint64_t)ld_x) ||
+      !map_bf16(&mx1, pair ? x1 : x0, (uint64_t)n, 128, (uint64_t)ld_x) ||
+      !map_bf16(&mp, plan->pi_bf16, 256, 128, 128) || !map_bf16(&ms, plan->s_bf16, 256, 128, 128))
     return TQ_ERR_CUDA;
   const int w = plan->w;
   TcArgs a{};
-  a.n = n;
-  a.idx = rows ? out->idx + row0 * (w * 4) : out->idx + (row0 / 32) * (w * 128);
-  a.sgn = rows ? out->sgn + row0 * 4 : out->sgn + (row0 / 32) * 128;
-  a.norm = out->norm + row0;
-  a.rnorm = out->rnorm + row0;
+  a.out0 = tc_out(out0, n, row0, w);
+  a.out1 = pair ? tc_out(out1, n, row0, w) : a.out0;
+  a.ntiles0 = (n + kTile - 1) / kTile;
+  a.ntiles = pair ? 2 * a.ntiles0 : a.ntiles0;
   a.centroids = plan->centroids;
   a.bounds = plan->bounds;
   a.fault = tq::fault_word();
   if (!a.fault) return TQ_ERR_CUDA;
-  if (rows) {
-    switch (w) {
-      case 1: return launch_w<1, TQ_LAYOUT_ROWS>(mx, mp, ms, a, st);
-      case 2: return launch_w<2, TQ_LAYOUT_ROWS>(mx, mp, ms, a, st);
-      default: return launch_w<3, TQ_LAYOUT_ROWS>(mx, mp, ms, a, st);
-    }
-  }
   switch (w) {
-    case 1: return launch_w<1, TQ_LAYOUT_BLOCK32>(mx, mp, ms, a, st);
-    case 2: return launch_w<2, TQ_LAYOUT_BLOCK32>(mx, mp, ms, a, st);
-    default: return launch_w<3, TQ_LAYOUT_BLOCK32>(mx, mp, ms, a, st);
+    case 1: return launch_w<1>(mx0, mx1, mp, ms, a, st);
+    case 2: return launch_w<2>(mx0, mx1, mp, ms, a, st);
+    default: return launch_w<3>(mx0, mx1, mp, ms, a, st);
   }
 }
 

@@ -195,3 +195,42 @@ def test_block_layout_fp32_simt(gpu_lib, w):
     K = make_kv(wl, which=1)[0, 0][:1000]
     rec = _run_block(K.cuda(), 128, 128, w, 24, 1024 + 32)
     _compare_block(K.numpy(), rec, 24, 128, 128, w)
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+@pytest.mark.parametrize("n,off,dtype", [(1000, 0, torch.bfloat16), (2048 + 77, 64, torch.bfloat16),
+                                         (300, 20, torch.bfloat16), (500, 0, torch.float32)])
+def test_quantize_pair_equals_two_calls(gpu_lib, w, n, off, dtype):
+    """tq_quantize_pair (keys by row, values in 32-row blocks) gives bit-for-bit the records of
+    two tq_quantize calls: one tensor-core launch for bf16 with a block-aligned offset, the two
+    single calls otherwise (unaligned block offset, fp32 input).  The pair is checked against
+    the oracle too."""
+    d = m = 128
+    wl = WORKLOADS["llama8b"]
+    K = make_kv(wl, B=1, T=n, which=0, device="cuda").reshape(-1, d)[:n].to(dtype).contiguous()
+    V = make_kv(wl, B=1, T=n, which=1, device="cuda").reshape(-1, d)[:n].to(dtype).contiguous()
+    p = plan(d, m, w)
+    cap = (n + off + 64 + 31) // 32 * 32  # block layout capacities are whole blocks
+    outs = []
+    for pair in (True, False):
+        rk = _lib.Records(cap, d, m, w)
+        rv = _lib.Records(cap, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+        for r in (rk, rv):
+            r.idx.fill_(-1), r.sgn.fill_(-1), r.norm.fill_(-7.0), r.rnorm.fill_(-7.0)
+        if pair:
+            _lib.tq_quantize_pair(p, K, V, rk, rv, out_offset=off)
+        else:
+            _lib.tq_quantize(p, K, rk, out_offset=off)
+            _lib.tq_quantize(p, V, rv, out_offset=off)
+        torch.cuda.synchronize()
+        assert _lib.tq_fault_flags() == 0
+        outs.append([t.cpu().numpy() for r in (rk, rv) for t in (r.idx, r.sgn, r.norm, r.rnorm)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    rows = slice(off, off + n)
+    rk = _lib.Records(cap, d, m, w)
+    rv = _lib.Records(cap, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    _lib.tq_quantize_pair(p, K, V, rk, rv, out_offset=off)
+    torch.cuda.synchronize()
+    _compare(K.float().cpu().numpy(), rk, rows, d, m, w)
+    _compare(V.float().cpu().numpy(), rv, rows, d, m, w)

@@ -91,6 +91,15 @@ def test_argument_errors_return_codes_without_launching():
     assert lib.tq_quantize(ref(p), 4096, 1, 10, 100, ref(r), 0, None) == _lib.TQ_ERR_ARG
     assert lib.tq_quantize(ref(p), 4096, 7, 10, 128, ref(r), 0, None) == _lib.TQ_ERR_ARG
     assert lib.tq_quantize(ref(p), 4096, 1, 0, 128, ref(r), 0, None) == _lib.TQ_OK  # n = 0: no-op
+    # the pair entry point checks both inputs and both outputs before any launch
+    r2 = _fake_records(50)
+    assert lib.tq_quantize_pair(ref(p), 4096, 8192, 1, 60, 128, ref(r), ref(r2), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize_pair(ref(p), 4096, 8200, 1, 10, 128, ref(r), ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize_pair(ref(p), 4096, None, 1, 10, 128, ref(r), ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize_pair(ref(p), 4096, 8192, 1, -1, 128, ref(r), ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize_pair(ref(p), 4096, 8192, 1, 10, 100, ref(r), ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize_pair(ref(p), 4096, 8192, 7, 10, 128, ref(r), ref(r), 0, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_quantize_pair(ref(p), 4096, 8192, 1, 0, 128, ref(r), ref(r2), 0, None) == _lib.TQ_OK
     # invalid plan shapes
     for d, m, w in ((100, 128, 2), (128, 128, 4), (2048, 128, 2), (128, 16, 2)):
         bad = _fake_plan(d, m, w)
