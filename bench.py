@@ -34,7 +34,7 @@ NOMINAL_HBM_GBS = 8000.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b")
@@ -85,7 +85,7 @@ def dram_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -96,7 +96,7 @@ class ClockSampler:
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -391,6 +391,10 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # decode alone with a cold L2 (inside the step it reads records that quantize just
+    # wrote); taken before the clock sampler starts, apart from the timed steps
+    t_dec = timed(stream, lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws), 50, flush) / 1e3
+
     sampler = ClockSampler(local)
     sampler.wait_first()
     events = []
@@ -412,10 +416,6 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_step = float(tt.item())
     fault = _lib.tq_fault_flags()
-
-    # decode alone with a cold L2 (inside the step it reads records that quantize just wrote)
-    t_dec = timed(stream, lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws),
-                  max(20, args.steps // 5), flush) / 1e3
 
     # ---- end to end: pinned host inputs in, attention output out, every step
     Kh = K.cpu().pin_memory()
