@@ -290,6 +290,66 @@ def decode_sweep(_lib, plan_cache, stream, flush, bits_list, iters=20):
     return res
 
 
+def config_sweep(_lib, stream, flush, peak):
+    """The two quantize-heavy configurations: bulk prefill quantization (8 kv heads x 65536
+    tokens x {K, V}, bf16, b = 3) and generic d = 1024 vectors (1,048,576 unit-norm fp32, b = 4,
+    m = 1024) with a top-10 inner-product search for 1024 queries over the compressed set."""
+    import torch
+
+    from online_kv_cache_04_b300.workloads import (QJL_SEED, ROTATION_SEED, WORKLOADS, make_generic,
+                                                   make_generic_queries, make_kv)
+
+    out = {}
+    # bulk prefill: keys by row, values in 32-row blocks, one paired launch
+    wl = WORKLOADS["prefill"]
+    d, m, w = wl.d, wl.m, 2
+    nvec = wl.B * wl.Hkv * wl.ctx
+    plan = _lib.Plan(d, m, w, ROTATION_SEED, QJL_SEED)
+    K = make_kv(wl, which=0, device="cuda").reshape(nvec, d)
+    V = make_kv(wl, which=1, device="cuda").reshape(nvec, d)
+    Kr = _lib.Records(nvec, d, m, w)
+    Vr = _lib.Records(nvec, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    fn = lambda: _lib.tq_quantize_pair(plan, K, V, Kr, Vr)
+    for _ in range(3):
+        fn()
+    ms = timed(stream, fn, 20, flush)
+    nbytes = 2 * nvec * (d * K.element_size() + rec_bytes(d, m, w))
+    out["prefill_quantize"] = {"workload": "8 kv heads x 65536 tokens x {K, V}, bf16, b=3", "vectors": 2 * nvec,
+                               "ms_per_call": ms, "mvec_per_s": 2 * nvec / ms / 1e3, "gbs": nbytes / ms / 1e6,
+                               "frac_of_measured_hbm": nbytes / ms / 1e6 / peak, "l2": "flushed before every call"}
+    del K, V, Kr, Vr
+    torch.cuda.empty_cache()
+    # generic d = 1024: quantize, then search
+    wl = WORKLOADS["generic"]
+    d, m, w, n, nq, k = wl.d, wl.m, 3, wl.ctx, wl.n_queries, 10
+    plan = _lib.Plan(d, m, w, ROTATION_SEED, QJL_SEED)
+    X = make_generic(wl, device="cuda")
+    rec = _lib.Records(n, d, m, w)
+    fn = lambda: _lib.tq_quantize(plan, X, rec)
+    fn()
+    ms = timed(stream, fn, 3, flush)
+    rb = rec_bytes(d, m, w)
+    nbytes = n * (d * 4 + rb)
+    out["generic_quantize"] = {"workload": "1,048,576 unit-norm fp32 vectors, d=m=1024, b=4", "vectors": n,
+                               "ms_per_call": ms, "mvec_per_s": n / ms / 1e3, "gbs": nbytes / ms / 1e6,
+                               "frac_of_measured_hbm": nbytes / ms / 1e6 / peak, "l2": "flushed before every call"}
+    del X
+    torch.cuda.empty_cache()
+    Q = make_generic_queries(wl, device="cuda")
+    ws = torch.empty(_lib.tq_search_workspace_size(plan, nq, n, k), dtype=torch.uint8, device="cuda")
+    idx = torch.empty(nq, k, dtype=torch.int32, device="cuda")
+    sc = torch.empty(nq, k, dtype=torch.float32, device="cuda")
+    fn = lambda: _lib.tq_search_topk(plan, Q, rec, n, k, idx, sc, ws)
+    fn()
+    ms = timed(stream, fn, 3, flush)
+    out["generic_search"] = {"workload": "top-10 of 1,048,576 compressed d=1024 vectors for 1024 queries",
+                             "ms_per_call": ms, "queries_per_s": nq / ms * 1e3,
+                             "vector_queries_per_s": nq * n / ms * 1e3, "l2": "flushed before every call"}
+    del Q, ws, rec
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_single(args):
     """One kernel family alone on a (possibly smaller) workload: the command profilers capture."""
     import dataclasses
@@ -487,6 +547,7 @@ def main():
     }
     if world == 1 and not args.no_sweep:
         line["decode_longctx"] = decode_sweep(_lib, {}, stream, flush, (2, 3, 4))
+        line["configs"] = config_sweep(_lib, stream, flush, peak)
     if world == 1 and not args.no_cpu_baseline:
         run, tokens, Ts = oracle_sample(wl, w, 3.0)
         run()

@@ -100,11 +100,17 @@ typedef struct tq_plan {
   const uint16_t* s_bf16;   /* [2][m][d] bf16 hi/lo split of S Πᵀ           */
 } tq_plan;
 
-/* Device bytes needed by tq_plan_init for (d, m, w); 0 if unsupported. */
+/* Device bytes needed by tq_plan_init for (d, m, w); 0 if unsupported.
+ * m = 0 selects stage 1 alone ([memory-wall] §2 stage 1: the rotation and
+ * the MSE-optimal codebook with all w bits, no QJL rows): records then hold
+ * only indices and norms (their sgn and rnorm may be NULL), scores are
+ * ||k|| <Π q, c[idx]> and values ||v|| Πᵀ c[idx].  Such plans run on the
+ * general kernels, not the d = m = 128 tensor-core ones. */
 size_t tq_plan_bytes(int d, int m, int w);
 
 /* Fill `plan` and the device buffer `dev` (bytes >= tq_plan_bytes) from the
- * host float64 tables of tq_make_rotation / tq_make_qjl / tq_make_codebook.
+ * host float64 tables of tq_make_rotation / tq_make_qjl / tq_make_codebook
+ * (s_rot may be NULL when m = 0).
  * Copies are issued on `stream`; the host tables may be released once the
  * stream has passed this call.  walsh[mask] holds the coefficients of the
  * expansion c[idx] = Σ_mask walsh[mask] · Π_{p in mask} (2·bit_p(idx) - 1)

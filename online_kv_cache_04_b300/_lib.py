@@ -153,7 +153,8 @@ class Plan:
 
         self.d, self.m, self.w = d, m, w
         self.pi = tq_make_rotation(d, rotation_seed)
-        self.S, self.s_rot = tq_make_qjl(m, d, qjl_seed, self.pi)
+        # m = 0: stage 1 alone, no QJL matrix
+        self.S, self.s_rot = tq_make_qjl(m, d, qjl_seed, self.pi) if m > 0 else (np.zeros((0, d)), None)
         self.centroids, self.bounds, self.mse = tq_make_codebook(d, w)
         nbytes = load().tq_plan_bytes(d, m, w)
         if nbytes == 0:
@@ -182,11 +183,12 @@ class Records:
 
         self.capacity, self.d, self.m, self.w, self.layout = capacity, d, m, w, layout
         self.idx = torch.empty(capacity, w * d // 32, dtype=torch.int32, device=device)
-        self.sgn = torch.empty(capacity, m // 32, dtype=torch.int32, device=device)
         self.norm = torch.empty(capacity, dtype=torch.float32, device=device)
-        self.rnorm = torch.empty(capacity, dtype=torch.float32, device=device)
-        self.c = tq_records(self.idx.data_ptr(), self.sgn.data_ptr(), self.norm.data_ptr(), self.rnorm.data_ptr(),
-                            capacity, layout)
+        # stage-1-only records (m = 0) carry no signs and no residual norm
+        self.sgn = torch.empty(capacity, m // 32, dtype=torch.int32, device=device) if m > 0 else None
+        self.rnorm = torch.empty(capacity, dtype=torch.float32, device=device) if m > 0 else None
+        self.c = tq_records(self.idx.data_ptr(), self.sgn.data_ptr() if m > 0 else None, self.norm.data_ptr(),
+                            self.rnorm.data_ptr() if m > 0 else None, capacity, layout)
 
     @classmethod
     def wrap(cls, idx, sgn, norm, rnorm, d, m, w, layout=TQ_LAYOUT_ROWS):
@@ -194,7 +196,8 @@ class Records:
         self = cls.__new__(cls)
         self.capacity, self.d, self.m, self.w, self.layout = norm.shape[0], d, m, w, layout
         self.idx, self.sgn, self.norm, self.rnorm = idx, sgn, norm, rnorm
-        self.c = tq_records(idx.data_ptr(), sgn.data_ptr(), norm.data_ptr(), rnorm.data_ptr(), self.capacity, layout)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        self.c = tq_records(idx.data_ptr(), ptr(sgn), norm.data_ptr(), ptr(rnorm), self.capacity, layout)
         return self
 
     @property

@@ -192,7 +192,7 @@ __device__ __forceinline__ void score_token(const SplitArgs& a, int64_t row, con
         if (g < G) d2[g] = fmaf(sts[g * m + k * 32 + b], sg, d2[g]);
     }
   }
-  const float nk = __ldg(a.knorm + row), rk = __ldg(a.krnorm + row);
+  const float nk = __ldg(a.knorm + row), rk = m > 0 ? __ldg(a.krnorm + row) : 0.0f;
 #pragma unroll
   for (int g = 0; g < kMaxG; ++g)
     if (g < G) out[g] = a.scale * (nk * d1[g] + a.alpha * rk * d2[g]);
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
       }
       __syncthreads();
       const float nv = valid ? __ldg(a.vnorm + rowbase + t) : 0.0f;
-      const float rv = valid ? __ldg(a.vrnorm + rowbase + t) : 0.0f;
+      const float rv = valid && m > 0 ? __ldg(a.vrnorm + rowbase + t) : 0.0f;
       for (int g = 0; g < G; ++g) {
         const float p = valid ? exp2f(sc[g] - runm[g]) : 0.0f;
         pn[g * kThreads + tid] = p * nv;
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 tq_status check_common(const tq_plan* plan, const void* q, tq_dtype qd, const tq_records* K, const int32_t* ctx_len,
                        const DecodeShape& s) {
   if (!q || !ctx_len || !tq::aligned16(q) || (qd != TQ_F32 && qd != TQ_BF16)) return TQ_ERR_ARG;
-  if (!tq::valid_records(K)) return TQ_ERR_ARG;
+  if (!tq::valid_records(K, plan)) return TQ_ERR_ARG;
   if (K->layout != TQ_LAYOUT_ROWS) return TQ_ERR_UNSUPPORTED;
   if (K->capacity / s.ctx_stride < int64_t(s.B) * s.Hkv) return TQ_ERR_ARG;
   if (!supported(s)) return TQ_ERR_UNSUPPORTED;
@@ -474,7 +474,7 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
   if (!fill_shape(plan, B, Hq, Hkv, ctx_stride, &s)) return TQ_ERR_ARG;
   tq_status st = check_common(plan, q, q_dtype, K, ctx_len, s);
   if (st != TQ_OK) return st;
-  if (!tq::valid_records(V) || V->capacity / s.ctx_stride < int64_t(B) * Hkv) return TQ_ERR_ARG;
+  if (!tq::valid_records(V, plan) || V->capacity / s.ctx_stride < int64_t(B) * Hkv) return TQ_ERR_ARG;
   if (V->layout == TQ_LAYOUT_BLOCK32 && ctx_stride % 32 != 0) return TQ_ERR_ARG;
   if (!out || !tq::aligned16(out) || !workspace || !tq::aligned16(workspace)) return TQ_ERR_ARG;
   if (ws_bytes < sizeof(float) * ws_floats(s)) return TQ_ERR_WORKSPACE;

@@ -11,17 +11,22 @@ namespace tq {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// m = 0: stage 1 alone (no QJL rows, records without signs or residual norms)
 inline bool valid_shape(int d, int m, int w) {
-  return d >= 32 && d <= 1024 && d % 32 == 0 && m >= 32 && m <= 1024 && m % 32 == 0 && w >= 1 && w <= 3;
+  return d >= 32 && d <= 1024 && d % 32 == 0 && (m == 0 || (m >= 32 && m <= 1024 && m % 32 == 0)) && w >= 1 &&
+         w <= 3;
 }
 
 inline bool valid_plan(const tq_plan* p) {
-  return p != nullptr && valid_shape(p->d, p->m, p->w) && p->pi && p->pi_t && p->s_rot && p->s_rot_t &&
-         p->centroids && p->bounds && p->walsh && p->pi_bf16 && p->s_bf16;
+  return p != nullptr && valid_shape(p->d, p->m, p->w) && p->pi && p->pi_t && p->centroids && p->bounds &&
+         p->walsh && p->pi_bf16 && (p->m == 0 || (p->s_rot && p->s_rot_t && p->s_bf16));
 }
 
-inline bool valid_records(const tq_records* r) {
-  if (r == nullptr || !r->idx || !r->sgn || !r->norm || !r->rnorm || r->capacity < 0) return false;
+// Records of a plan; without QJL rows (plan m = 0) sgn and rnorm may be NULL.
+inline bool valid_records(const tq_records* r, const tq_plan* plan) {
+  const bool qjl = plan->m > 0;
+  if (r == nullptr || !r->idx || !r->norm || r->capacity < 0) return false;
+  if (qjl && (!r->sgn || !r->rnorm)) return false;
   if (!aligned16(r->idx) || !aligned16(r->sgn) || !aligned16(r->norm) || !aligned16(r->rnorm)) return false;
   if (r->layout == TQ_LAYOUT_ROWS) return true;
   return r->layout == TQ_LAYOUT_BLOCK32 && r->capacity % 32 == 0;

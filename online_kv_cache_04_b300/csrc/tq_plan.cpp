@@ -56,7 +56,8 @@ extern "C" size_t tq_plan_bytes(int d, int m, int w) {
 extern "C" tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const double* pi, const double* s_rot,
                                   const double* centroids, const double* bounds, void* dev, size_t bytes,
                                   tq_stream stream) {
-  if (!plan || !pi || !s_rot || !centroids || !bounds || !dev || !tq::valid_shape(d, m, w)) return TQ_ERR_ARG;
+  if (!plan || !pi || (m > 0 && !s_rot) || !centroids || !bounds || !dev || !tq::valid_shape(d, m, w))
+    return TQ_ERR_ARG;
   const Layout l = layout(d, m, w);
   if (bytes < l.total || (reinterpret_cast<uintptr_t>(dev) % kAlign) != 0) return TQ_ERR_ARG;
   const int L = 1 << w;
@@ -104,7 +105,7 @@ extern "C" tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const doub
   plan->d = d;
   plan->m = m;
   plan->w = w;
-  plan->qjl_alpha = static_cast<float>(std::sqrt(M_PI / 2.0) / m);
+  plan->qjl_alpha = m > 0 ? static_cast<float>(std::sqrt(M_PI / 2.0) / m) : 0.0f;
   plan->pi = reinterpret_cast<const float*>(base + l.pi);
   plan->pi_t = reinterpret_cast<const float*>(base + l.pi_t);
   plan->s_rot = reinterpret_cast<const float*>(base + l.s_rot);

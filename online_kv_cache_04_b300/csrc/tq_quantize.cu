@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
     }
     if (tid < TV && v0 + tid < a.n) {
       a.norm[v0 + tid] = nrm[tid];
-      a.rnorm[v0 + tid] = nrm[tid] * sqrtf(rsq[tid]);
+      if (m > 0) a.rnorm[v0 + tid] = nrm[tid] * sqrtf(rsq[tid]);
     }
     __syncthreads();
   }
@@ -217,7 +217,7 @@ tq_status launch_simt_any(const QuantArgs& a, tq_dtype dtype, cudaStream_t st) {
 
 extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
                                  const tq_records* out, int64_t out_offset, tq_stream stream) {
-  if (!tq::valid_plan(plan) || !tq::valid_records(out) || n < 0 || out_offset < 0) return TQ_ERR_ARG;
+  if (!tq::valid_plan(plan) || !tq::valid_records(out, plan) || n < 0 || out_offset < 0) return TQ_ERR_ARG;
   if (dtype != TQ_F32 && dtype != TQ_BF16) return TQ_ERR_ARG;
   if (n == 0) return TQ_OK;
   if (x == nullptr || !tq::aligned16(x) || ld_x < plan->d || ld_x % 8 != 0) return TQ_ERR_ARG;
@@ -273,7 +273,8 @@ extern "C" tq_status tq_quantize_pair(const tq_plan* plan, const void* x0, const
                                       int64_t ld_x, const tq_records* out0, const tq_records* out1,
                                       int64_t out_offset, tq_stream stream) {
   // the same checks as tq_quantize, for both pairs, before anything is launched
-  if (!tq::valid_plan(plan) || !tq::valid_records(out0) || !tq::valid_records(out1) || n < 0 || out_offset < 0)
+  if (!tq::valid_plan(plan) || !tq::valid_records(out0, plan) || !tq::valid_records(out1, plan) || n < 0 ||
+      out_offset < 0)
     return TQ_ERR_ARG;
   if (dtype != TQ_F32 && dtype != TQ_BF16) return TQ_ERR_ARG;
   if (n == 0) return TQ_OK;

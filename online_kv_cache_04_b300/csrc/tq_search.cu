@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kVB) score_kernel(ScoreArgs a) {
       for (int q = 0; q < kQB; ++q) d2[q] = fmaf(sts[q * m + j], sg, d2[q]);
     }
   }
-  const float nv = __ldg(a.norm + i), rv = __ldg(a.rnorm + i);
+  const float nv = __ldg(a.norm + i), rv = m > 0 ? __ldg(a.rnorm + i) : 0.0f;
   for (int q = 0; q < nqb; ++q) a.scores[(size_t)(q0 + q) * a.n + i] = nv * d1[q] + a.alpha * rv * d2[q];
 }
 
@@ -182,7 +182,7 @@ extern "C" tq_status tq_search_workspace_size(const tq_plan* plan, int nq, int64
 extern "C" tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype q_dtype, int nq,
                                     const tq_records* recs, int64_t n, int k, int32_t* idx_out, float* score_out,
                                     void* workspace, size_t ws_bytes, tq_stream stream) {
-  if (!tq::valid_plan(plan) || !tq::valid_records(recs) || !q || !tq::aligned16(q) || nq < 1 || n < 1 ||
+  if (!tq::valid_plan(plan) || !tq::valid_records(recs, plan) || !q || !tq::aligned16(q) || nq < 1 || n < 1 ||
       n > recs->capacity || n > INT32_MAX || k < 1 || k > 64 || !idx_out || !score_out || !workspace ||
       !tq::aligned16(workspace) || (q_dtype != TQ_F32 && q_dtype != TQ_BF16))
     return TQ_ERR_ARG;

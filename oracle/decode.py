@@ -31,8 +31,9 @@ def reconstruct_cache(rec, Pi, S, centroids, qjl_stage=True):
     lead = idx.shape[:-1]
     d = idx.shape[-1]
     m = rec["sgn"].shape[-1]
-    x = reconstruct(idx.reshape(-1, d), rec["sgn"].reshape(-1, m), rec["norm"].reshape(-1),
-                    rec["rnorm"].reshape(-1), Pi, S, centroids, qjl_stage=qjl_stage)
+    n = int(np.prod(lead))  # explicit: a stage-1-only record has m = 0 sign columns
+    x = reconstruct(idx.reshape(n, d), rec["sgn"].reshape(n, m), rec["norm"].reshape(n),
+                    rec["rnorm"].reshape(n), Pi, S, centroids, qjl_stage=qjl_stage)
     return x.reshape(lead + (d,))
 
 

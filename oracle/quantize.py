@@ -64,6 +64,18 @@ def quantize(X: np.ndarray, Pi: np.ndarray, S: np.ndarray, centroids: np.ndarray
                      u=u, p=p, rnorm64=rn)
 
 
+def quantize_mse(X: np.ndarray, Pi: np.ndarray, centroids: np.ndarray, bounds: np.ndarray) -> Quantized:
+    """Stage 1 alone as the stored format: the rotation and the MSE-optimal
+    per-coordinate codebook with every bit of the budget ([memory-wall] §2
+    stage 1), stored as (idx, fp32 ‖x‖) -- no QJL rows,
+    no residual norm.  Its reconstruction n · Πᵀ c[idx] is the MSE-optimal one;
+    its inner products carry the stage-1 bias (2/π at one bit)."""
+    n, u, idx, _ = stage1(X, Pi, centroids, bounds)
+    N = idx.shape[0]
+    return Quantized(idx=idx, sgn=np.zeros((N, 0), dtype=bool), norm=n.astype(np.float32),
+                     rnorm=np.zeros(N, dtype=np.float32), u=u, p=np.zeros((N, 0)), rnorm64=np.zeros(N))
+
+
 def reconstruct(idx: np.ndarray, sgn: np.ndarray, norm: np.ndarray, rnorm: np.ndarray,
                 Pi: np.ndarray, S: np.ndarray, centroids: np.ndarray, qjl_stage: bool = True) -> np.ndarray:
     """Unbiased reconstruction from stored record values.

@@ -15,14 +15,14 @@ import numpy as np
 from .quantize import reconstruct
 
 
-def scores(Q, rec, Pi, S, centroids):
-    """[nq, N] estimated inner products."""
-    xh = reconstruct(rec["idx"], rec["sgn"], rec["norm"], rec["rnorm"], Pi, S, centroids)
+def scores(Q, rec, Pi, S, centroids, qjl_stage=True):
+    """[nq, N] estimated inner products (stage 1 alone when qjl_stage is False)."""
+    xh = reconstruct(rec["idx"], rec["sgn"], rec["norm"], rec["rnorm"], Pi, S, centroids, qjl_stage=qjl_stage)
     return np.asarray(Q, dtype=np.float64) @ xh.T
 
 
-def topk(Q, rec, Pi, S, centroids, k):
+def topk(Q, rec, Pi, S, centroids, k, qjl_stage=True):
     """(indices [nq, k] int64, scores [nq, k] float64)."""
-    sc = scores(Q, rec, Pi, S, centroids)
+    sc = scores(Q, rec, Pi, S, centroids, qjl_stage=qjl_stage)
     order = np.argsort(-sc, axis=1, kind="stable")[:, :k]
     return order, np.take_along_axis(sc, order, axis=1)

@@ -51,12 +51,29 @@ def plan(d, m, w):
 
 
 def oracle_quantize(X, d, m, w):
+    """The oracle's records; m = 0 is stage 1 alone (no QJL rows)."""
     Pi, S, c, b = oracle_tables(d, m, w)
+    if m == 0:
+        return oquant.quantize_mse(np.asarray(X, dtype=np.float64), Pi, c, b)
     return oquant.quantize(np.asarray(X, dtype=np.float64), Pi, S, c, b)
 
 
 def gpu_records_to_numpy(rec, rows, d, m, w):
     """Unpack rows of a GPU Records object with the oracle's unpacker (either layout)."""
+    if m == 0:  # stage-1-only records: no sign words, no residual norms
+        if getattr(rec, "layout", _lib.TQ_LAYOUT_ROWS) == _lib.TQ_LAYOUT_ROWS:
+            idx_w = rec.idx[rows].cpu().numpy().view(np.uint32)
+            idx = opack.unpack_indices(idx_w, w, d)
+            norm = rec.norm[rows].cpu().numpy()
+        else:
+            r = np.arange(rec.capacity)[rows] if isinstance(rows, slice) else np.asarray(rows)
+            b0, b1 = int(r.min()) // 32, int(r.max()) // 32 + 1
+            iw = rec.idx.reshape(-1)[b0 * 32 * (w * d // 32):b1 * 32 * (w * d // 32)].cpu().numpy().view(np.uint32)
+            idx = opack.unpack_indices_block32(iw.reshape(b1 - b0, w * d), w, d)[r - 32 * b0]
+            norm = rec.norm[torch.as_tensor(r)].cpu().numpy()
+        n = idx.shape[0]
+        return {"idx": idx, "sgn": np.zeros((n, 0), dtype=bool), "norm": norm, "rnorm": np.zeros(n, np.float32),
+                "idx_words": opack.pack_indices(idx, w), "sgn_words": np.zeros((n, 0), np.uint32)}
     if getattr(rec, "layout", _lib.TQ_LAYOUT_ROWS) == _lib.TQ_LAYOUT_ROWS:
         idx_w = rec.idx[rows].cpu().numpy().view(np.uint32)
         sgn_w = rec.sgn[rows].cpu().numpy().view(np.uint32)
@@ -79,6 +96,11 @@ def oracle_records_to_gpu(q, d, m, w, device="cuda", layout=None):
     """Pack an oracle Quantized result with the oracle's packer and upload it."""
     layout = _lib.TQ_LAYOUT_ROWS if layout is None else layout
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    if m == 0:  # stage-1-only records: indices and norms
+        n = q.idx.shape[0]
+        idx_w = (opack.pack_indices(q.idx, w) if layout == _lib.TQ_LAYOUT_ROWS else
+                 opack.pack_indices_block32(q.idx, w).reshape(n, w * d // 32)).view(np.int32)
+        return _lib.Records.wrap(t(idx_w), None, t(q.norm), None, d, m, w, layout=layout)
     if layout == _lib.TQ_LAYOUT_ROWS:
         idx_w = opack.pack_indices(q.idx, w).view(np.int32)
         sgn_w = opack.pack_signs(q.sgn).view(np.int32)

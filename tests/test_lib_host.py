@@ -100,6 +100,16 @@ def test_argument_errors_return_codes_without_launching():
     assert lib.tq_quantize_pair(ref(p), 4096, 8192, 1, 10, 100, ref(r), ref(r), 0, None) == _lib.TQ_ERR_ARG
     assert lib.tq_quantize_pair(ref(p), 4096, 8192, 7, 10, 128, ref(r), ref(r), 0, None) == _lib.TQ_ERR_ARG
     assert lib.tq_quantize_pair(ref(p), 4096, 8192, 1, 0, 128, ref(r), ref(r2), 0, None) == _lib.TQ_OK
+    # stage 1 alone: plans with m = 0 exist, and their records may omit signs and residual norms
+    assert lib.tq_plan_bytes(128, 0, 2) > 0
+    assert lib.tq_plan_bytes(128, 0, 2) < lib.tq_plan_bytes(128, 128, 2)
+    nosig = _lib.tq_records(4096, None, 12288, None, 100)
+    assert lib.tq_quantize(ref(p), 4096, 1, 10, 128, ref(nosig), 0, None) == _lib.TQ_ERR_ARG  # m = 128 needs them
+    p0 = _fake_plan(128, 0, 2)
+    assert lib.tq_quantize(ref(p0), 4096, 1, 0, 128, ref(nosig), 0, None) == _lib.TQ_OK
+    assert lib.tq_quantize(ref(p0), 4096, 1, -1, 128, ref(nosig), 0, None) == _lib.TQ_ERR_ARG
+    noidx = _lib.tq_records(None, None, 12288, None, 100)
+    assert lib.tq_quantize(ref(p0), 4096, 1, 0, 128, ref(noidx), 0, None) == _lib.TQ_ERR_ARG
     # invalid plan shapes
     for d, m, w in ((100, 128, 2), (128, 128, 4), (2048, 128, 2), (128, 16, 2)):
         bad = _fake_plan(d, m, w)

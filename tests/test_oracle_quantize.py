@@ -216,3 +216,26 @@ def test_pack_block32_round_trip_and_transpose_of_row_layout(w):
                 a = (int(rw[r, p * (d // 32) + j // 32]) >> (j % 32)) & 1
                 b = (int(bw[r // 32, p * d + j]) >> int(pack.block32_bit(r % 32))) & 1
                 assert a == b
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_stage1_only_records(w):
+    """Stage-1-only records hold stage 1's indices and fp32 norms and no sign rows;
+    reconstructing them without the QJL term gives stage 1's n · Πᵀ c[idx].  With centroids
+    at the cell means, the error is orthogonal to the reconstruction on average, so
+    ⟨x, x̃⟩ / ‖x‖² = 1 − D/‖x‖² < 1: inner products through stage 1 alone are shrunk."""
+    d = 64
+    Pi, S, c, b, mse = _setup(d, w)
+    rng = np.random.default_rng(40 + w)
+    X = rng.standard_normal((300, d))
+    z = quantize.quantize_mse(X, Pi, c, b)
+    n, _, idx, xt = quantize.stage1(X, Pi, c, b)
+    assert np.array_equal(z.idx, idx)
+    assert np.array_equal(z.norm, n.astype(np.float32))
+    assert z.sgn.shape == (300, 0)
+    xr = quantize.reconstruct(z.idx, z.sgn, z.norm, z.rnorm, Pi, S[:0], c, qjl_stage=False)
+    # the stored fp32 norm differs from the float64 one by at most half an ulp
+    assert np.abs(xr - xt).max() <= 1e-7 * np.abs(xt).max()
+    ip = np.sum(X * xt, axis=1) / np.sum(X * X, axis=1)
+    assert abs(ip.mean() - (1.0 - d * mse)) < 5 * ip.std() / np.sqrt(len(ip)) + 1e-3
+    assert ip.mean() < 1.0
