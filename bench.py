@@ -347,6 +347,35 @@ def config_sweep(_lib, stream, flush, peak):
                              "vector_queries_per_s": nq * n / ms * 1e3, "l2": "flushed before every call"}
     del Q, ws, rec
     torch.cuda.empty_cache()
+    # stage 1 alone (m = 0) at b = 3 = w on the Llama-3.1-8B-shaped layer: general kernels
+    wl = WORKLOADS["llama8b"]
+    d, w = wl.d, 3
+    B, Hq, Hkv, T = wl.B, wl.Hq, wl.Hkv, wl.ctx
+    nvec = B * Hkv * T
+    plan = _lib.Plan(d, 0, w, ROTATION_SEED, QJL_SEED)
+    K = make_kv(wl, which=0, device="cuda").reshape(nvec, d)
+    V = make_kv(wl, which=1, device="cuda").reshape(nvec, d)
+    Kr = _lib.Records(nvec, d, 0, w)
+    Vr = _lib.Records(nvec, d, 0, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    fq = lambda: _lib.tq_quantize_pair(plan, K, V, Kr, Vr)
+    fq()
+    ms_q = timed(stream, fq, 10, flush)
+    from online_kv_cache_04_b300.workloads import make_queries
+
+    q = make_queries(wl, device="cuda")
+    ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    o = torch.empty(B, Hq, d, device="cuda")
+    ws = torch.empty(_lib.tq_decode_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+    fd = lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, o, ws)
+    fd()
+    ms_d = timed(stream, fd, 20, flush)
+    rb = d * w // 8 + 4
+    out["stage1_only_llama8b"] = {"workload": "Llama-3.1-8B-shaped layer, stage 1 alone (m=0), b=w=3, general kernels",
+                                  "quantize_ms_per_call": ms_q, "quantize_mvec_per_s": 2 * nvec / ms_q / 1e3,
+                                  "decode_ms_per_call": ms_d, "decode_kv_tokens_per_s": B * T / ms_d * 1e3,
+                                  "decode_gbs": 2 * nvec * rb / ms_d / 1e6, "l2": "flushed before every call"}
+    del K, V, Kr, Vr, ws
+    torch.cuda.empty_cache()
     return out
 
 
