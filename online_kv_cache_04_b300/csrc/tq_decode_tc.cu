@@ -307,6 +307,11 @@ __device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* 
   float v1[32], v2[32];
   load_cols(a.pi_t, v1);     // (Π q)_j = Σ_c Πᵀ[c][j] q_c
   load_cols(a.s_rot_t, v2);  // (S̃ q̃)_i = Σ_j S̃ᵀ[j][i] q̃_j
+  // The query and the workspace belong to the stream's earlier launches: wait
+  // for them (programmatic dependent launch).  Only then may the decode kernel
+  // start, since its first copies read the records those launches wrote.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   // bring Π and S̃ (row-major), which the unit's merge reads, into L2 meanwhile
   for (int e = threadIdx.x; e < 2 * kD * kD / 32; e += kThreads) {
     const float* line = e < kD * kD / 32 ? a.pi + 32 * e : a.s_rot + 32 * (e - kD * kD / 32);
@@ -456,10 +461,6 @@ __global__ void __launch_bounds__(kThreads) unit_table_kernel(const TcArgs a) {
   TableState* ts = reinterpret_cast<TableState*>(smem + Sh::kBKBytes + Scratch<GP>::kPrep * 4);
   const int u = blockIdx.x, lane = threadIdx.x & 31;
   const int b = u / a.Hkv, h = u - b * a.Hkv, head0 = b * a.Hq + h * a.G;
-  // the decode kernel may start now: it reads tables and counters only after
-  // waiting for this grid to complete
-  asm volatile("griddepcontrol.launch_dependents;");
-  if (threadIdx.x == 0) a.arrivals[u] = 0u;
   if (threadIdx.x < NPM) ts->cf[threadIdx.x] = __ldg(a.walsh + (threadIdx.x < W ? (1 << threadIdx.x) : 7));
   if (threadIdx.x < 16) {
     ts->amax[threadIdx.x >> 3][threadIdx.x & 7] = 0.f;
@@ -469,6 +470,8 @@ __global__ void __launch_bounds__(kThreads) unit_table_kernel(const TcArgs a) {
     reinterpret_cast<uint4*>(BK)[e] = make_uint4(0, 0, 0, 0);
   float *qr, *sr;
   unit_query_prep<GP>(a, head0, scr, &qr, &sr);  // its first barrier publishes the lines above
+  // (past the grid dependency wait inside unit_query_prep: the workspace is ours)
+  if (threadIdx.x == 0) a.arrivals[u] = 0u;
   // thread group grp = threadIdx / 128 takes heads grp and grp + 4; thread j its coordinate
   // j: word kw, bit x = 16e + L; L = 8·ks2 + 4·hi + q -> K index 8·hi + 2q + e
   constexpr int HG = GP / 4;  // heads per thread group
@@ -1069,19 +1072,23 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
     if (cudaFuncSetAttribute(table_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, table_smem) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    table_kern<<<units, kThreads, table_smem, stream>>>(a);
-    if (launch_status() != TQ_OK) return TQ_ERR_CUDA;
-    // the decode kernel's prologue and first copies overlap the table kernel
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
+    // both as programmatic dependent launches: the table kernel's matrix loads
+    // overlap the previous kernel, the decode kernel's prologue and first copies
+    // overlap the table kernel (each waits for its predecessor before it reads
+    // what that one wrote)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cfg.gridDim = dim3(units);
+    cfg.dynamicSmemBytes = table_smem;
+    if (cudaLaunchKernelEx(&cfg, table_kern, a) != cudaSuccess) return TQ_ERR_CUDA;
+    cfg.gridDim = dim3(grid);
+    cfg.dynamicSmemBytes = smem;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
   };

@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t ntiles = a.ntiles;
 
+  // the next launch in the stream may be scheduled now (it waits for this grid
+  // before it reads anything this grid writes)
+  asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->b_full), 1);
     for (int s = 0; s < 2; ++s) {
@@ -171,6 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(base + kOffPi + (2 * h + mat) * kBoxBytes, &tm_pi, h * 64, mat * 128, bfull);
           tma_load_2d(base + kOffSHi + mat * kMatBytes + h * kBoxBytes, &tm_s, h * 64, mat * 128, bfull);
         }
+      // the inputs may come from the previous launch in the stream: read them
+      // only once it has completed (the plan tables above are not written by it)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int it = 0, last_k[2] = {-1, -1};
       for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
         const int s = it & 1, k = it >> 1;
@@ -239,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && it >= 1) gemm2(it - 1);
     }
   } else {
+    // the previous launch in the stream may still read the records written here
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // epilogue: warpgroup g = warp / 4 handles tiles it ≡ g (mod 2); thread = one vector (TMEM lane)
     float cent[8], bnd[8];
 #pragma unroll
@@ -450,7 +458,19 @@ tq_status launch_w(const CUtensorMap& mx0, const CUtensorMap& mx1, const CUtenso
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return TQ_ERR_CUDA;
   const int grid = (int)std::min<int64_t>(a.ntiles, tq::sm_count());
-  kern<<<grid, kThreads, kSmemBytes, st>>>(mx0, mx1, mp, ms, a);
+  // programmatic dependent launch: the prologue (barriers, TMEM, the plan
+  // operands) overlaps the previous kernel; inputs and outputs wait for it
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, mx0, mx1, mp, ms, a) != cudaSuccess) return TQ_ERR_CUDA;
   return tq::launch_status();
 }
 
