@@ -35,15 +35,24 @@
 // hundred cycles whatever its width, and an e4m3 or int8 mma.sync runs far
 // below the f16 one.
 //
+// Launches.  unit_table_kernel (one CTA per (batch, kv head) unit) computes
+// Π q and S q for the unit's heads and writes the query operand table and the
+// score constants, once per unit; every decode CTA that works on the unit
+// fetches that table with one bulk copy.  Both kernels are programmatic
+// dependent launches (each waits for its predecessor before reading what the
+// predecessor wrote).
+//
 // Work split.  A persistent grid of one CTA per SM takes contiguous ranges of
 // 256-token tiles over all (batch, kv head) units (the last tile of a unit
-// may hold 128); the partials of a unit (two per CTA that touches it) are
-// merged by the combine kernel of tq_decode.cu.  Sixteen warps do the same
+// may hold 128).  At the end of its part of a unit a CTA merges its two
+// halves on chip into one partial, then counts itself in on the unit's
+// arrival counter; the CTA that arrives last merges the unit's partials and
+// applies the unrotation, so there is no combine launch.  Sixteen warps do the same
 // work: warp w scores 16 tokens of each tile (half w & 1 of block w / 2) and
 // accumulates values for 16 coordinates (rows w % 8) over half of the blocks
 // (w / 8).  Warps 0-7 thus only touch tokens 0-127 of a tile and warps 8-15
 // tokens 128-255, and the two halves run as independent pipelines: each has
-// its own softmax reference, running sum, named barriers and partial.  The
+// its own softmax reference, running sum and named barriers.  The
 // weights of a tile go through shared memory, already laid out as the value
 // operand.  Per tile and half there are two named barriers: the first
 // publishes the weights of tile i − 1; between the two, the value products of

@@ -15,6 +15,12 @@
 // ("谷歌TurboQuant如何绕过内存墙？" §2 stages 1 and 2; "TurboQuant 与 AI 效率革命"
 // §四 three-step pipeline; "TurboQuant压缩效果": codes packed into 32-bit words.)
 //
+// One launch covers one input or two (tq_quantize_pair: the keys and values
+// of the same tokens, each with its own output layout) as one sequence of
+// tiles, so the pipeline fills and drains once.  It is a programmatic
+// dependent launch: the prologue overlaps the previous kernel, and the input
+// loads and record stores wait for it.
+//
 // Two TMEM slots and two epilogue warpgroups let the tensor core work on one
 // tile while the epilogue of the other runs.  Warp roles (576 threads):
 // warps 0-7 epilogue of even tiles, 8-15 of odd tiles (warp % 4 = TMEM lane
