@@ -77,4 +77,12 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
                            float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
                            cudaStream_t stream);
 
+// Tensor-core search scores (tq_search_tc.cu): d and m multiples of 128 (m may
+// be 0), records in TQ_LAYOUT_ROWS.  `table`: search_tc_table_bytes(plan, nq)
+// bytes, 16-byte aligned; scores [nq][n] as the SIMT score kernel writes them.
+bool search_tc_supported(const tq_plan* plan, const tq_records* recs);
+size_t search_tc_table_bytes(const tq_plan* plan, int nq);
+tq_status launch_search_tc(const tq_plan* plan, const tq_records* recs, int64_t n, int nq, const float* qt,
+                           const float* st, void* table, float* scores, cudaStream_t stream);
+
 }  // namespace tq

@@ -8,8 +8,10 @@
 // index (the order (score desc, index asc) is total, so selection is exact).
 //
 // Kernels: query prep (shared with decode), a score kernel that writes the
-// nq x n score matrix to the workspace, then two selection passes: per chunk
-// of vectors, and a merge of the per-chunk candidates.
+// nq x n score matrix to the workspace (the tensor-core one of tq_search_tc.cu
+// when d and m are multiples of 128, the SIMT one below otherwise), then two
+// selection passes: per chunk of vectors, and a merge of the per-chunk
+// candidates.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -24,17 +26,22 @@ constexpr int kSel = 256;       // threads per selection CTA
 constexpr int64_t kChunk = 4096;
 
 struct SearchLayout {
-  size_t qt, st, scores, cand_idx, cand_sc, total;
+  size_t qt, st, table, scores, cand_idx, cand_sc, total;
   int64_t nchunks;
 };
 
-SearchLayout layout(int d, int m, int nq, int64_t n, int k) {
+// Workspace: q̃, s̃, the tensor-core query table (sized whenever the plan's
+// shape allows that path), the score matrix and the selection candidates.
+SearchLayout layout(const tq_plan* plan, int nq, int64_t n, int k) {
+  const int d = plan->d, m = plan->m;
   SearchLayout l{};
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   l.nchunks = tq::cdiv(n, kChunk);
   size_t o = 0;
   l.qt = o; o += up(sizeof(float) * size_t(nq) * d);
   l.st = o; o += up(sizeof(float) * size_t(nq) * m);
+  l.table = o;
+  if (d % 128 == 0 && m % 128 == 0) o += up(tq::search_tc_table_bytes(plan, nq));
   l.scores = o; o += up(sizeof(float) * size_t(nq) * size_t(n));
   l.cand_idx = o; o += up(sizeof(int32_t) * size_t(nq) * l.nchunks * k);
   l.cand_sc = o; o += up(sizeof(float) * size_t(nq) * l.nchunks * k);
@@ -175,7 +182,7 @@ __global__ void __launch_bounds__(kSel) merge_kernel(const int32_t* cand_idx, co
 
 extern "C" tq_status tq_search_workspace_size(const tq_plan* plan, int nq, int64_t n, int k, size_t* bytes) {
   if (!tq::valid_plan(plan) || !bytes || nq < 1 || n < 1 || n > INT32_MAX || k < 1 || k > 64) return TQ_ERR_ARG;
-  *bytes = layout(plan->d, plan->m, nq, n, k).total;
+  *bytes = layout(plan, nq, n, k).total;
   return TQ_OK;
 }
 
@@ -187,7 +194,7 @@ extern "C" tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype
       !tq::aligned16(workspace) || (q_dtype != TQ_F32 && q_dtype != TQ_BF16))
     return TQ_ERR_ARG;
   if (recs->layout != TQ_LAYOUT_ROWS) return TQ_ERR_UNSUPPORTED;
-  const SearchLayout l = layout(plan->d, plan->m, nq, n, k);
+  const SearchLayout l = layout(plan, nq, n, k);
   if (ws_bytes < l.total) return TQ_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -198,14 +205,18 @@ extern "C" tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype
   float* cand_sc = reinterpret_cast<float*>(ws + l.cand_sc);
   tq_status s = tq::launch_query_prep(plan, q, q_dtype, nq, qt, st, cs);
   if (s != TQ_OK) return s;
-  ScoreArgs a{recs->idx, recs->sgn, recs->norm, recs->rnorm, n, nq, plan->d, plan->m, plan->w, qt, st,
-              plan->centroids, plan->qjl_alpha, scores};
-  const size_t smem = sizeof(float) * (kQB * (plan->d + plan->m) + 8);
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return TQ_ERR_CUDA;
-  score_kernel<<<dim3((unsigned)tq::cdiv(n, kVB), (unsigned)tq::cdiv(nq, kQB)), kVB, smem, cs>>>(a);
-  if ((s = tq::launch_status()) != TQ_OK) return s;
+  if (tq::search_tc_supported(plan, recs)) {
+    if ((s = tq::launch_search_tc(plan, recs, n, nq, qt, st, ws + l.table, scores, cs)) != TQ_OK) return s;
+  } else {
+    ScoreArgs a{recs->idx, recs->sgn, recs->norm, recs->rnorm, n, nq, plan->d, plan->m, plan->w, qt, st,
+                plan->centroids, plan->qjl_alpha, scores};
+    const size_t smem = sizeof(float) * (kQB * (plan->d + plan->m) + 8);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return TQ_ERR_CUDA;
+    score_kernel<<<dim3((unsigned)tq::cdiv(n, kVB), (unsigned)tq::cdiv(nq, kQB)), kVB, smem, cs>>>(a);
+    if ((s = tq::launch_status()) != TQ_OK) return s;
+  }
   select_chunks_kernel<<<dim3((unsigned)l.nchunks, nq), kSel, 0, cs>>>(scores, n, l.nchunks, k, cand_idx, cand_sc);
   if ((s = tq::launch_status()) != TQ_OK) return s;
   merge_kernel<<<nq, kSel, 0, cs>>>(cand_idx, cand_sc, l.nchunks, k, idx_out, score_out);

@@ -1,0 +1,315 @@
+// Search scores on the tensor cores: for d and m multiples of 128 (m may be
+// 0), w in 1..3, records in TQ_LAYOUT_ROWS.
+//
+// The score of stored vector i for query q ("TurboQuant压缩效果": vector
+// search engines; the estimator of "TurboQuant 与 AI 效率革命" §三 applied to
+// the residual as in "谷歌TurboQuant如何绕过内存墙？" §2 stage 2) is
+//   score = ‖x_i‖ Σ_P coef_P ⟨Π q, s_P,i⟩ + √(π/2)/m ‖r_i‖ ⟨S q, σ_i⟩,
+// where c[idx] = Σ_P coef_P s_P is the Walsh expansion of the symmetric
+// codebook into ±1 bit-planes (w = 3 adds the product plane b0 ^ b1 ^ b2) and
+// σ is one more ±1 plane.  Over many queries this is a dense contraction:
+// rows = stored vectors, K = planes x coordinates, columns = queries.
+//
+// search_table_kernel: per group of four queries, the column operand of
+//   every K-step, laid out as the mma.sync B fragments (f16 hi + lo pairs of
+//   -coef_P (Π q)_j / E0 and -(S q)_j / E1, E a power of two per query and
+//   part), and the per-query constants E0 and α·E1.
+// search_score_kernel: a CTA scores 128 vectors against 32 queries with
+//   mma.sync m16n8k16 f16.  The bits of a record word become exact ±1 f16
+//   operands in registers: one integer multiply moves bits L and 16 + L to the
+//   sign positions of an f16x2 register and one logic op fills in 1.0, so the
+//   operand is -s.  The query operand streams through shared memory in
+//   16 KiB chunks (bulk copies, two buffers); fp32 accumulators per part
+//   stay in registers; the epilogue scales by the record's norms and writes
+//   the score matrix that the selection kernels of tq_search.cu read.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <type_traits>
+
+#include "tq_internal.h"
+#include "tq_sm100.cuh"
+
+namespace {
+
+using namespace tq::sm100;
+
+constexpr int kWarps = 8, kThreads = 32 * kWarps;
+constexpr int kRows = 16 * kWarps;         // vectors per CTA
+constexpr int kTilesPerCta = 8;            // groups of four queries per CTA: 32 queries
+constexpr int kChunkWords = 4;             // one chunk: 4 words (128 coordinates) of one plane = 8 K-steps
+constexpr int kChunkSteps = 2 * kChunkWords;
+constexpr int kFragBytes = 256;            // one (K-step, query group) B operand: 32 lanes x uint2
+constexpr int kChunkBytes = kChunkSteps * kTilesPerCta * kFragBytes;
+constexpr unsigned kFaultSearch = 4u;
+
+// Per lane q: 2^(3-q), 2^(7-q), 2^(11-q), 2^(15-q) (multiplier from constant
+// memory: the move stays an integer multiply on the FMA pipe).
+__constant__ uint32_t c_smul[4][4] = {{8u, 128u, 2048u, 32768u},
+                                      {4u, 64u, 1024u, 16384u},
+                                      {2u, 32u, 512u, 8192u},
+                                      {1u, 16u, 256u, 4096u}};
+
+struct SearchTcArgs {
+  const uint32_t* idx; const uint32_t* sgn; const float* norm; const float* rnorm;
+  int64_t n;
+  int nq, d, m, w, npm;     // npm: codebook planes (w, or 4 with the product plane)
+  int groups;               // query groups of four
+  int64_t ksteps;           // 2 (npm d + m) / 32
+  const float* qt; const float* st;   // [nq][d] Π q, [nq][m] S q
+  const float* walsh;
+  float alpha;
+  __half* table;            // [ksteps][groups][8 n][4 quad][2 reg][2 half]
+  float* consts;            // [nq][2]: E0, α E1
+  float* scores;            // [nq][n]
+  unsigned* fault;
+};
+
+__device__ __forceinline__ uint32_t sign_operand(uint32_t t) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(t), "r"(0x80008000u), "r"(0x3C003C00u));
+  return r;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Query column operand.  Coordinate j of a plane sits in word j / 32 at bit
+// x = 16e + L (e: f16 half of the operand register, L = 0..15); K-step
+// 2·(word) + L / 8 of the plane; inside it K index 8·((L / 4) % 2) + 2·(L % 4) + e.
+__global__ void __launch_bounds__(kThreads) search_table_kernel(SearchTcArgs a) {
+  __shared__ float amax[2][4];
+  const int grp = blockIdx.x, lane = threadIdx.x & 31;
+  if (threadIdx.x < 8) amax[threadIdx.x >> 2][threadIdx.x & 3] = 0.f;
+  __syncthreads();
+  float cmax = 0.f;
+  for (int P = 0; P < a.npm; ++P) cmax = fmaxf(cmax, fabsf(__ldg(a.walsh + (P < a.w ? (1 << P) : 7))));
+  for (int g = 0; g < 4; ++g) {
+    const int q = 4 * grp + g;
+    float m0 = 0.f, m1 = 0.f;
+    if (q < a.nq) {
+      for (int j = threadIdx.x; j < a.d; j += kThreads) m0 = fmaxf(m0, fabsf(a.qt[(size_t)q * a.d + j]) * cmax);
+      for (int j = threadIdx.x; j < a.m; j += kThreads) m1 = fmaxf(m1, fabsf(a.st[(size_t)q * a.m + j]));
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+    if (lane == 0) {
+      atomicMax(reinterpret_cast<int*>(&amax[0][g]), __float_as_int(m0));
+      atomicMax(reinterpret_cast<int*>(&amax[1][g]), __float_as_int(m1));
+    }
+  }
+  __syncthreads();
+  // E: the power of two taking the part's largest weight below 2^12; weights are stored divided by E
+  auto escale = [&](int p, int g) {
+    int ex;
+    frexpf(amax[p][g], &ex);
+    return amax[p][g] > 0.f ? ldexpf(1.f, ex - 12) : 1.f;
+  };
+  if (threadIdx.x < 4 && 4 * grp + (int)threadIdx.x < a.nq) {
+    const int g = threadIdx.x;
+    a.consts[(size_t)(4 * grp + g) * 2] = escale(0, g);
+    a.consts[(size_t)(4 * grp + g) * 2 + 1] = a.alpha * escale(1, g);
+  }
+  const int words_d = a.d / 32;
+  const int64_t total = (int64_t)a.npm * a.d + a.m;  // plane coordinates, codebook planes first
+  for (int64_t e = threadIdx.x; e < total; e += kThreads) {
+    const bool qjl = e >= (int64_t)a.npm * a.d;
+    const int P = qjl ? a.npm : (int)(e / a.d);
+    const int j = qjl ? (int)(e - (int64_t)a.npm * a.d) : (int)(e - (int64_t)P * a.d);
+    const int x = j & 31, eh = x >> 4, L = x & 15;
+    const int64_t ks = 2 * ((int64_t)P * words_d + (j >> 5)) + (L >> 3);
+    const int kk = 8 * ((L >> 2) & 1) + 2 * (L & 3) + eh;
+    const float coef = qjl ? 0.f : __ldg(a.walsh + (P < a.w ? (1 << P) : 7));
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int q = 4 * grp + g;
+      float xv = 0.f;
+      if (q < a.nq) {
+        xv = qjl ? -a.st[(size_t)q * a.m + j] / escale(1, g) : -coef * a.qt[(size_t)q * a.d + j] / escale(0, g);
+      }
+      const __half xh = __float2half_rn(xv), xl = __float2half_rn(xv - __half2float(xh));
+      // [n][quad][reg][half]: column 2g holds hi, 2g + 1 lo
+      const size_t base = ((((size_t)ks * a.groups + grp) * 8 + 2 * g) * 4 + ((kk & 7) >> 1)) * 4 +
+                          (kk >> 3) * 2 + (kk & 1);
+      a.table[base] = xh;
+      a.table[base + 16] = xl;
+    }
+  }
+}
+
+// CTA (vector block bx, query block by): rows v0 .. v0 + 127, query groups
+// 8·by .. 8·by + 7.  Warp wp takes rows v0 + 16 wp + (0..15): fragment row gq
+// is vector v0 + 16 wp + gq, row gq + 8 the vector eight further.
+__global__ void __launch_bounds__(kThreads) search_score_kernel(SearchTcArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* buf = smem;  // [2][kChunkSteps][kTilesPerCta][256 B]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * kChunkBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+  const int64_t v0 = (int64_t)blockIdx.x * kRows;
+  const int g0 = blockIdx.y * kTilesPerCta, ntl = min(kTilesPerCta, a.groups - g0);
+  const int words_d = a.d / 32, words_m = a.m / 32;
+  const int nchunks = (a.npm * words_d + words_m) / kChunkWords;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&full[0]), 1);
+    mbar_init(smem_u32(&full[1]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // chunk c covers K-steps 8c .. 8c + 7; its operand for groups g0 .. g0 + ntl - 1
+  // is ntl contiguous 256-byte fragments per K-step in the table
+  auto issue = [&](int c) {
+    const uint32_t bar = smem_u32(&full[c & 1]);
+    mbar_arrive_expect_tx(bar, (uint32_t)(kChunkSteps * ntl * kFragBytes));
+    const uint32_t dst = smem_u32(buf + (c & 1) * kChunkBytes);
+    for (int s = 0; s < kChunkSteps; ++s) {
+      const int64_t ks = (int64_t)kChunkSteps * c + s;
+      bulk_load(dst + s * kTilesPerCta * kFragBytes, a.table + (ks * a.groups + g0) * (kFragBytes / 2),
+                ntl * kFragBytes, bar);
+    }
+  };
+  if (threadIdx.x == 0) {
+    issue(0);
+    if (nchunks > 1) issue(1);
+  }
+  const int64_t r0 = v0 + 16 * warp + gq, r1 = r0 + 8;
+  const bool ok0 = r0 < a.n, ok1 = r1 < a.n;
+  const int wi = a.w * words_d;  // index words per record
+  float acc[2][kTilesPerCta][4];
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int t = 0; t < kTilesPerCta; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[p][t][e] = 0.f;
+  const uint32_t m15 = c_smul[tig][3], m11 = c_smul[tig][2], m7 = c_smul[tig][1], m3 = c_smul[tig][0];
+  bool alive = true;
+  int nissued = nchunks > 1 ? 2 : 1;  // thread 0: chunks whose copies were started
+  int ndone = 0;                      // chunks whose copies this thread has seen land
+  // one chunk into the accumulators of part PART (0: codebook planes, 1: QJL plane)
+  auto chunk = [&](int c, auto part_tag) {
+    constexpr int PART = decltype(part_tag)::value;
+    const int wpos = c * kChunkWords;  // word position over all planes
+    const int P = PART ? a.npm : wpos / words_d;
+    const int kw0 = PART ? wpos - a.npm * words_d : wpos - P * words_d;
+    uint4 x[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int64_t row = r ? r1 : r0;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r ? ok1 : ok0) {
+        if (PART) {
+          v = __ldg(reinterpret_cast<const uint4*>(a.sgn + row * words_m + kw0));
+        } else if (P < a.w) {
+          v = __ldg(reinterpret_cast<const uint4*>(a.idx + row * wi + P * words_d + kw0));
+        } else {  // product plane b0 ^ b1 ^ b2
+          const uint4 p0 = __ldg(reinterpret_cast<const uint4*>(a.idx + row * wi + kw0));
+          const uint4 p1 = __ldg(reinterpret_cast<const uint4*>(a.idx + row * wi + words_d + kw0));
+          const uint4 p2 = __ldg(reinterpret_cast<const uint4*>(a.idx + row * wi + 2 * words_d + kw0));
+          v = make_uint4(p0.x ^ p1.x ^ p2.x, p0.y ^ p1.y ^ p2.y, p0.z ^ p1.z ^ p2.z, p0.w ^ p1.w ^ p2.w);
+        }
+      }
+      x[r] = v;
+    }
+    if (alive) {
+      alive = mbar_wait(smem_u32(&full[c & 1]), (uint32_t)((c >> 1) & 1), a.fault, kFaultSearch);
+      ndone += alive ? 1 : 0;
+    }
+    const uint2* bfr = reinterpret_cast<const uint2*>(buf + (c & 1) * kChunkBytes);
+#pragma unroll
+    for (int kw = 0; kw < kChunkWords; ++kw) {
+      const uint32_t w0 = kw == 0 ? x[0].x : kw == 1 ? x[0].y : kw == 2 ? x[0].z : x[0].w;
+      const uint32_t w1 = kw == 0 ? x[1].x : kw == 1 ? x[1].y : kw == 2 ? x[1].z : x[1].w;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        // layers q + 8s (K 2q + e) and 4 + q + 8s (K 8 + 2q + e) to the sign bits
+        const uint32_t mlo = s ? m7 : m15, mhi = s ? m3 : m11;
+        const uint32_t a0 = sign_operand(w0 * mlo), a1 = sign_operand(w1 * mlo);
+        const uint32_t a2 = sign_operand(w0 * mhi), a3 = sign_operand(w1 * mhi);
+        const int sl = 2 * kw + s;
+#pragma unroll
+        for (int t = 0; t < kTilesPerCta; ++t) {
+          const uint2 b = bfr[(sl * kTilesPerCta + t) * 32 + lane];
+          mma16816(acc[PART][t], a0, a1, a2, a3, b.x, b.y);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with this buffer
+    if (threadIdx.x == 0 && c + 2 < nchunks && alive) {
+      issue(c + 2);
+      nissued = c + 3;
+    }
+  };
+  const int ncb = a.npm * words_d / kChunkWords;  // codebook chunks; the QJL plane's follow
+#pragma unroll 1
+  for (int c = 0; c < ncb; ++c) chunk(c, std::integral_constant<int, 0>{});
+#pragma unroll 1
+  for (int c = ncb; c < nchunks; ++c) chunk(c, std::integral_constant<int, 1>{});
+  // no copy of this CTA may be in flight when it exits: after a wait ran out,
+  // thread 0 waits (bounded again) for every copy it started
+  if (threadIdx.x == 0 && !alive)
+    for (int c = ndone; c < nissued; ++c)
+      mbar_wait(smem_u32(&full[c & 1]), (uint32_t)((c >> 1) & 1), a.fault, kFaultSearch);
+  // epilogue: column pair (hi, lo) 2·tig of tile t is query 4 (g0 + t) + tig
+  const float nv0 = ok0 ? __ldg(a.norm + r0) : 0.f, nv1 = ok1 ? __ldg(a.norm + r1) : 0.f;
+  const float rv0 = ok0 && a.m > 0 ? __ldg(a.rnorm + r0) : 0.f, rv1 = ok1 && a.m > 0 ? __ldg(a.rnorm + r1) : 0.f;
+#pragma unroll
+  for (int t = 0; t < kTilesPerCta; ++t) {
+    const int q = 4 * (g0 + t) + tig;
+    if (t < ntl && q < a.nq) {
+      const float e0 = a.consts[(size_t)q * 2], e1 = a.consts[(size_t)q * 2 + 1];
+      if (ok0)
+        a.scores[(size_t)q * a.n + r0] =
+            fmaf(nv0 * e0, acc[0][t][0] + acc[0][t][1], rv0 * e1 * (acc[1][t][0] + acc[1][t][1]));
+      if (ok1)
+        a.scores[(size_t)q * a.n + r1] =
+            fmaf(nv1 * e0, acc[0][t][2] + acc[0][t][3], rv1 * e1 * (acc[1][t][2] + acc[1][t][3]));
+    }
+  }
+}
+
+}  // namespace
+
+bool tq::search_tc_supported(const tq_plan* plan, const tq_records* recs) {
+  return plan->d % 128 == 0 && plan->m % 128 == 0 && recs->layout == TQ_LAYOUT_ROWS;
+}
+
+size_t tq::search_tc_table_bytes(const tq_plan* plan, int nq) {
+  const int npm = plan->w == 3 ? 4 : plan->w;
+  const size_t ksteps = 2 * (size_t(npm) * plan->d + plan->m) / 32;
+  return ksteps * size_t((nq + 3) / 4) * kFragBytes + sizeof(float) * 2 * size_t(nq);
+}
+
+tq_status tq::launch_search_tc(const tq_plan* plan, const tq_records* recs, int64_t n, int nq, const float* qt,
+                               const float* st, void* table, float* scores, cudaStream_t stream) {
+  SearchTcArgs a{};
+  a.idx = recs->idx; a.sgn = recs->sgn; a.norm = recs->norm; a.rnorm = recs->rnorm;
+  a.n = n;
+  a.nq = nq;
+  a.d = plan->d; a.m = plan->m; a.w = plan->w;
+  a.npm = plan->w == 3 ? 4 : plan->w;
+  a.groups = (nq + 3) / 4;
+  a.ksteps = 2 * (int64_t(a.npm) * a.d + a.m) / 32;
+  a.qt = qt; a.st = st;
+  a.walsh = plan->walsh;
+  a.alpha = plan->qjl_alpha;
+  a.table = static_cast<__half*>(table);
+  a.consts = reinterpret_cast<float*>(static_cast<uint8_t*>(table) + size_t(a.ksteps) * a.groups * kFragBytes);
+  a.scores = scores;
+  a.fault = tq::fault_word();
+  if (!a.fault) return TQ_ERR_CUDA;
+  search_table_kernel<<<a.groups, kThreads, 0, stream>>>(a);
+  if (launch_status() != TQ_OK) return TQ_ERR_CUDA;
+  const int smem = 2 * kChunkBytes + 64;
+  if (cudaFuncSetAttribute(search_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  const dim3 grid((unsigned)((n + kRows - 1) / kRows), (unsigned)((a.groups + kTilesPerCta - 1) / kTilesPerCta));
+  search_score_kernel<<<grid, kThreads, smem, stream>>>(a);
+  return launch_status();
+}
