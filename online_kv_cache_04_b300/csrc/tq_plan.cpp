@@ -12,7 +12,8 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t pi, pi_t, s_rot, s_rot_t, cent, bnd, walsh, pi_bf, s_bf, total;
+  size_t pi, pi_t, s_rot, s_rot_t, cent, bnd, walsh, pi_bf, s_bf, pi_fr, s_fr, total;
+  bool frag;  // warp-MMA operand copies present (d >= 256)
 };
 
 Layout layout(int d, int m, int w) {
@@ -28,6 +29,9 @@ Layout layout(int d, int m, int w) {
   l.walsh = o;   o += up(sizeof(float) * L);
   l.pi_bf = o;   o += up(sizeof(uint16_t) * 2 * d * d);
   l.s_bf = o;    o += up(sizeof(uint16_t) * 2 * size_t(m) * d);
+  l.frag = d >= 256 && d % 128 == 0;
+  l.pi_fr = o;   o += l.frag ? up(sizeof(uint16_t) * 2 * size_t(d) * d) : 0;
+  l.s_fr = o;    o += l.frag ? up(sizeof(uint16_t) * 2 * size_t(m) * d) : 0;
   l.total = o;
   return l;
 }
@@ -84,6 +88,27 @@ extern "C" tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const doub
       H(l.s_bf)[size_t(i) * d + j] = hi;
       H(l.s_bf)[size_t(m) * d + size_t(i) * d + j] = lo;
     }
+  // warp-MMA operand order of the pieces (see tq_plan.pi_frag)
+  if (l.frag) {
+    auto frag = [&](size_t off, const uint16_t* src, int rows) {
+      const size_t ks_n = d / 16, fr_n = rows / 8;
+      for (int p = 0; p < 2; ++p)
+        for (size_t ks = 0; ks < ks_n; ++ks)
+          for (size_t f = 0; f < fr_n; ++f)
+            for (int lane = 0; lane < 32; ++lane) {
+              const int g = lane >> 2, t = lane & 3;
+              const size_t r = 8 * f + g, c = 16 * ks + 2 * t;
+              uint16_t* dst = H(off) + (((p * ks_n + ks) * fr_n + f) * 32 + lane) * 4;
+              const uint16_t* row = src + size_t(p) * rows * d + r * d;
+              dst[0] = row[c];
+              dst[1] = row[c + 1];
+              dst[2] = row[c + 8];
+              dst[3] = row[c + 9];
+            }
+    };
+    frag(l.pi_fr, H(l.pi_bf), d);
+    frag(l.s_fr, H(l.s_bf), m);
+  }
   for (int k = 0; k < L; ++k) F(l.cent)[k] = static_cast<float>(centroids[k]);
   for (int k = 0; k < L - 1; ++k) F(l.bnd)[k] = static_cast<float>(bounds[k]);
   // Walsh coefficients: walsh[mask] = 2^-w Σ_idx c[idx] Π_{p in mask} (2 bit_p(idx) - 1)
@@ -115,5 +140,7 @@ extern "C" tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const doub
   plan->walsh = reinterpret_cast<const float*>(base + l.walsh);
   plan->pi_bf16 = reinterpret_cast<const uint16_t*>(base + l.pi_bf);
   plan->s_bf16 = reinterpret_cast<const uint16_t*>(base + l.s_bf);
+  plan->pi_frag = l.frag ? reinterpret_cast<const uint16_t*>(base + l.pi_fr) : nullptr;
+  plan->s_frag = l.frag && m > 0 ? reinterpret_cast<const uint16_t*>(base + l.s_fr) : nullptr;
   return TQ_OK;
 }

@@ -13,8 +13,8 @@
 // (the dropped x_lo Π_lo and the rest of x beyond 16 bits are ~2^-16
 // relative), and the same for P = ρ (S Πᵀ)ᵀ.  A CTA takes 16 vectors: their
 // bf16 pieces sit in shared memory (rows padded against bank conflicts), the
-// matrix pieces are read as B fragments straight from the plan's bf16
-// copies, and each of the eight warps owns d/8 output coordinates.  After the
+// matrix pieces are read as B fragments straight from the plan's copies in
+// operand order, and each of the eight warps owns d/8 output coordinates.  After the
 // first product the warps bucketize in registers, pack the index planes with
 // quad shuffles, and write ρ's bf16 pieces over x's for the second product.
 #include <cuda_bf16.h>
@@ -34,8 +34,8 @@ struct MmaArgs {
   const void* x;
   int64_t n, ld;
   int d, m;
-  const uint16_t* pi_bf;   // [2][d][d] Π hi, lo (row-major)
-  const uint16_t* s_bf;    // [2][m][d] S Πᵀ hi, lo
+  const uint2* pi_fr;      // Π hi, lo in warp-MMA operand order (tq_plan.pi_frag)
+  const uint2* s_fr;       // S Πᵀ hi, lo likewise
   const float* centroids;
   const float* bounds;
   uint32_t* idx;           // rows already offset
@@ -66,12 +66,15 @@ template <>
 __device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
 // acc[f] += A[16 x K] · B for the warp's n-fragments f < nf, B[k][col] = M[col][k]
-// of a row-major bf16 matrix pair (hi at mh, lo at ml), columns col0 + 8f + (0..7).
-// A's pieces (hi, lo) are rows of stride `lda` bf16 in shared memory.
+// for a matrix M of `rows` rows whose bf16 pieces (hi at mh, lo at ml) are in
+// warp-MMA operand order: one 8-byte load per lane and fragment, 256 contiguous
+// bytes per warp.  Columns col0 + 8f + (0..7).  A's pieces (hi, lo) are rows of
+// stride `lda` bf16 in shared memory.
 __device__ __forceinline__ void gemm_split(float (&acc)[kMaxNF][4], const uint16_t* ah, const uint16_t* al,
-                                           int lda, const uint16_t* __restrict__ mh,
-                                           const uint16_t* __restrict__ ml, int K, int col0, int nf, int lane) {
+                                           int lda, const uint2* __restrict__ mh, const uint2* __restrict__ ml,
+                                           int K, int rows, int col0, int nf, int lane) {
   const int gq = lane >> 2, tig = lane & 3;
+  const int frs = rows / 8;  // row groups of M
 #pragma unroll 1
   for (int k0 = 0; k0 < K; k0 += 16) {
     const int c0 = k0 + 2 * tig;
@@ -83,17 +86,15 @@ __device__ __forceinline__ void gemm_split(float (&acc)[kMaxNF][4], const uint16
     const uint32_t xl1 = *reinterpret_cast<const uint32_t*>(al + (gq + 8) * lda + c0);
     const uint32_t xl2 = *reinterpret_cast<const uint32_t*>(al + gq * lda + c0 + 8);
     const uint32_t xl3 = *reinterpret_cast<const uint32_t*>(al + (gq + 8) * lda + c0 + 8);
+    const size_t kbase = (size_t)(k0 / 16) * frs + col0 / 8;
 #pragma unroll
     for (int f = 0; f < kMaxNF; ++f) {
       if (f < nf) {
-        const size_t row = (size_t)(col0 + 8 * f + gq) * K + c0;
-        const uint32_t bh0 = __ldg(reinterpret_cast<const uint32_t*>(mh + row));
-        const uint32_t bh1 = __ldg(reinterpret_cast<const uint32_t*>(mh + row + 8));
-        const uint32_t bl0 = __ldg(reinterpret_cast<const uint32_t*>(ml + row));
-        const uint32_t bl1 = __ldg(reinterpret_cast<const uint32_t*>(ml + row + 8));
-        mma_bf16(acc[f], xh0, xh1, xh2, xh3, bh0, bh1);
-        mma_bf16(acc[f], xh0, xh1, xh2, xh3, bl0, bl1);
-        mma_bf16(acc[f], xl0, xl1, xl2, xl3, bh0, bh1);
+        const uint2 bh = __ldg(mh + (kbase + f) * 32 + lane);
+        const uint2 bl = __ldg(ml + (kbase + f) * 32 + lane);
+        mma_bf16(acc[f], xh0, xh1, xh2, xh3, bh.x, bh.y);
+        mma_bf16(acc[f], xh0, xh1, xh2, xh3, bl.x, bl.y);
+        mma_bf16(acc[f], xl0, xl1, xl2, xl3, bh.x, bh.y);
       }
     }
   }
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) quantize_mma_kernel(MmaArgs a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[f][e] = 0.f;
   const int nf1 = d / 64, col1 = warp * (d / 8);
-  gemm_split(acc, ah, al, lda, a.pi_bf, a.pi_bf + (size_t)d * d, d, col1, nf1, lane);
+  gemm_split(acc, ah, al, lda, a.pi_fr, a.pi_fr + (size_t)d * d / 4, d, d, col1, nf1, lane);
 
   // ---- stage 1 in registers: u = U / n, idx, ρ (kept in acc), ||ρ||², index words
   constexpr int L = 1 << W;
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) quantize_mma_kernel(MmaArgs a) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[f][e] = 0.f;
     const int nf2 = m / 64, col2 = warp * (m / 8);
-    gemm_split(acc, ah, al, lda, a.s_bf, a.s_bf + (size_t)m * d, d, col2, nf2, lane);
+    gemm_split(acc, ah, al, lda, a.s_fr, a.s_fr + (size_t)m * d / 4, d, m, col2, nf2, lane);
     uint32_t sb0 = 0u, sb1 = 0u;
 #pragma unroll
     for (int f = 0; f < kMaxNF; ++f) {
@@ -292,7 +293,7 @@ tq_status launch_mma(const MmaArgs& a, cudaStream_t st) {
 
 bool tq::quantize_mma_supported(const tq_plan* plan, const tq_records* out) {
   return plan->d % 128 == 0 && plan->d >= 256 && plan->d <= 1024 && (plan->m == plan->d || plan->m == 0) &&
-         out->layout == TQ_LAYOUT_ROWS;
+         out->layout == TQ_LAYOUT_ROWS && plan->pi_frag != nullptr && (plan->m == 0 || plan->s_frag != nullptr);
 }
 
 tq_status tq::quantize_mma(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
@@ -303,8 +304,8 @@ tq_status tq::quantize_mma(const tq_plan* plan, const void* x, tq_dtype dtype, i
   a.ld = ld_x;
   a.d = plan->d;
   a.m = plan->m;
-  a.pi_bf = plan->pi_bf16;
-  a.s_bf = plan->s_bf16;
+  a.pi_fr = reinterpret_cast<const uint2*>(plan->pi_frag);
+  a.s_fr = reinterpret_cast<const uint2*>(plan->s_frag);
   a.centroids = plan->centroids;
   a.bounds = plan->bounds;
   a.idx = out->idx + row0 * (plan->w * plan->d / 32);
