@@ -43,6 +43,11 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the long-context decode sweep")
     ap.add_argument("--decode-only", action="store_true",
                     help="time tq_decode_attention alone (cold L2) on --workload / --batch; for profilers")
+    ap.add_argument("--generic-only", action="store_true",
+                    help="time tq_quantize and tq_search_topk (top-10) alone on --vectors unit-norm d = 1024 fp32 "
+                         "vectors and --queries queries; for profilers")
+    ap.add_argument("--vectors", type=int, default=262144)
+    ap.add_argument("--queries", type=int, default=256)
     ap.add_argument("--quantize-only", action="store_true",
                     help="time tq_quantize_pair alone (K and V, one launch) on --workload / --batch; for profilers")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (0: keep)")
@@ -379,6 +384,38 @@ def config_sweep(_lib, stream, flush, peak):
     return out
 
 
+def run_generic(args):
+    """Generic d = m = 1024, b = 4 vectors: quantize and top-10 search alone (the command profilers capture)."""
+    import torch
+
+    from online_kv_cache_04_b300 import _lib
+    from online_kv_cache_04_b300.workloads import (QJL_SEED, ROTATION_SEED, WORKLOADS, make_generic,
+                                                   make_generic_queries)
+
+    wl = WORKLOADS["generic"]
+    d, m, w, n, nq, k = wl.d, wl.m, 3, args.vectors, args.queries, 10
+    plan = _lib.Plan(d, m, w, ROTATION_SEED, QJL_SEED)
+    X = make_generic(wl, n=n, device="cuda")
+    rec = _lib.Records(n, d, m, w)
+    Q = make_generic_queries(wl, nq=nq, device="cuda")
+    ws = torch.empty(_lib.tq_search_workspace_size(plan, nq, n, k), dtype=torch.uint8, device="cuda")
+    idx = torch.empty(nq, k, dtype=torch.int32, device="cuda")
+    sc = torch.empty(nq, k, dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    fq = lambda: _lib.tq_quantize(plan, X, rec)
+    fs = lambda: _lib.tq_search_topk(plan, Q, rec, n, k, idx, sc, ws)
+    for _ in range(args.warmup):
+        fq()
+        fs()
+    ms_q = timed(stream, fq, args.steps, flush)
+    ms_s = timed(stream, fs, args.steps, flush)
+    print(json.dumps({"mode": "generic quantize + search", "vectors": n, "queries": nq,
+                      "quantize_ms": ms_q, "quantize_mvec_per_s": n / ms_q / 1e3,
+                      "search_ms": ms_s, "vector_queries_per_s": n * nq / ms_s * 1e3,
+                      "fault_flags": _lib.tq_fault_flags()}), flush=True)
+
+
 def run_single(args):
     """One kernel family alone on a (possibly smaller) workload: the command profilers capture."""
     import dataclasses
@@ -431,6 +468,9 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.generic_only:
+        run_generic(args)
         return
     if args.decode_only or args.quantize_only:
         run_single(args)
