@@ -234,3 +234,16 @@ def test_quantize_pair_equals_two_calls(gpu_lib, w, n, off, dtype):
     torch.cuda.synchronize()
     _compare(K.float().cpu().numpy(), rk, rows, d, m, w)
     _compare(V.float().cpu().numpy(), rv, rows, d, m, w)
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_wide_vectors_bf16_ragged_offset(gpu_lib, w):
+    """d = m = 512 bf16 input, 1000 vectors (not a multiple of the 16-vector tile) written at row 37
+    of a 1100-row cache: indices, signs and norms against the oracle, other rows untouched."""
+    d = 512
+    g = torch.Generator().manual_seed(500 + w)
+    X = (torch.randn(1000, d, generator=g) * (1 + 9 * (torch.rand(d, generator=g) < 0.03))).to(torch.bfloat16)
+    rec = _run(X.cuda(), d, d, w, offset=37, capacity=1100)
+    _compare(X.float().numpy(), rec, slice(37, 1037), d, d, w)
+    assert bool((rec.idx[:37] == -1).all()) and bool((rec.idx[1037:] == -1).all())
+    assert bool((rec.sgn[:37] == -1).all()) and bool((rec.sgn[1037:] == -1).all())

@@ -88,3 +88,12 @@ def test_generic_d1024_slice(gpu_lib):
     Q = make_generic_queries(wl, nq=64, device="cuda")
     gidx, gsc, osc = _run(X, Q, 1024, 1024, 3, 10)
     _check_topk(gidx, gsc, osc, 10)
+
+
+def test_d512_w1_partial_query_tiles(gpu_lib):
+    """d = m = 512, b = 2 (w = 1), 5000 stored vectors, 40 queries (a partial 32-query tile), top-10."""
+    g = torch.Generator().manual_seed(512)
+    X = torch.randn(5000, 512, generator=g)
+    Q = torch.randn(40, 512, generator=g)
+    gidx, gsc, osc = _run(X.cuda(), Q.cuda(), 512, 512, 1, 10)
+    _check_topk(gidx, gsc, osc, 10)
