@@ -98,8 +98,8 @@ typedef struct tq_plan {
   const float* walsh;       /* [2^w] Walsh coefficients of the codebook    */
   const uint16_t* pi_bf16;  /* [2][d][d] bf16 hi/lo split of Π              */
   const uint16_t* s_bf16;   /* [2][m][d] bf16 hi/lo split of S Πᵀ           */
-  /* The same bf16 pieces in warp-MMA operand order, for d >= 256 (NULL
-   * otherwise): piece p, K-step k (16 columns), row group f (8 rows), lane
+  /* The same bf16 pieces in warp-MMA operand order, for d a multiple of 128
+   * (NULL otherwise): piece p, K-step k (16 columns), row group f (8 rows), lane
    * l = 4g + t hold M[8f + g][16k + 2t + {0, 1, 8, 9}] at 4 consecutive
    * halves ((p·(K/16) + k)·(rows/8) + f)·32 + l, for M = Π and M = S Πᵀ. */
   const uint16_t* pi_frag;  /* [2][d/16][d/8][32][4]                        */

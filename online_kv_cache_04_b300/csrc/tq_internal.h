@@ -77,8 +77,8 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
                            float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
                            cudaStream_t stream);
 
-// Warp tensor-core quantizer (tq_quantize_mma.cu): d a multiple of 128 in
-// [256, 1024], m = d or 0, fp32 or bf16 input, TQ_LAYOUT_ROWS output; rows
+// Warp tensor-core quantizer (tq_quantize_mma.cu): d a multiple of 128 up to
+// 1024, m = d or 0, fp32 or bf16 input, TQ_LAYOUT_ROWS output; rows
 // [row0, row0 + n) of `out`.
 bool quantize_mma_supported(const tq_plan* plan, const tq_records* out);
 tq_status quantize_mma(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,

@@ -29,7 +29,7 @@ Layout layout(int d, int m, int w) {
   l.walsh = o;   o += up(sizeof(float) * L);
   l.pi_bf = o;   o += up(sizeof(uint16_t) * 2 * d * d);
   l.s_bf = o;    o += up(sizeof(uint16_t) * 2 * size_t(m) * d);
-  l.frag = d >= 256 && d % 128 == 0;
+  l.frag = d % 128 == 0;
   l.pi_fr = o;   o += l.frag ? up(sizeof(uint16_t) * 2 * size_t(d) * d) : 0;
   l.s_fr = o;    o += l.frag ? up(sizeof(uint16_t) * 2 * size_t(m) * d) : 0;
   l.total = o;

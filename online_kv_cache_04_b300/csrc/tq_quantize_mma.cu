@@ -1,6 +1,6 @@
-// tq_quantize on the warp tensor-core path for wide vectors: d a multiple of
-// 128 in [256, 1024], m = d or m = 0, fp32 or bf16 input, records in
-// TQ_LAYOUT_ROWS.  (d = m = 128 bf16 takes the tcgen05 quantizer.)
+// tq_quantize on the warp tensor-core path: d a multiple of 128 up to 1024,
+// m = d or m = 0, fp32 or bf16 input, records in TQ_LAYOUT_ROWS.  (d = m = 128
+// bf16 takes the tcgen05 quantizer.)
 //
 // What is computed is the two-stage quantizer of tq_quantize.cu
 // ("谷歌TurboQuant如何绕过内存墙？" §2 stages 1 and 2; "TurboQuant 与 AI
@@ -14,9 +14,11 @@
 // relative), and the same for P = ρ (S Πᵀ)ᵀ.  A CTA takes 16 vectors: their
 // bf16 pieces sit in shared memory (rows padded against bank conflicts), the
 // matrix pieces are read as B fragments straight from the plan's copies in
-// operand order, and each of the eight warps owns d/8 output coordinates.  After the
-// first product the warps bucketize in registers, pack the index planes with
-// quad shuffles, and write ρ's bf16 pieces over x's for the second product.
+// operand order, and each warp owns max(d/8, 32) output coordinates (at
+// d = 128 four warps own 32 each, so that every index word fills in one warp,
+// and the other four only stage and wait).  After the first product the warps
+// bucketize in registers, pack the index planes with quad shuffles, and write
+// ρ's bf16 pieces over x's for the second product.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -153,7 +155,8 @@ __global__ void __launch_bounds__(kThreads) quantize_mma_kernel(MmaArgs a) {
   for (int f = 0; f < kMaxNF; ++f)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[f][e] = 0.f;
-  const int nf1 = d / 64, col1 = warp * (d / 8);
+  // a warp's block of output coordinates is a whole number of 32-bit words
+  const int cw1 = max(d / 8, 32), nf1 = warp * cw1 < d ? cw1 / 8 : 0, col1 = warp * cw1;
   gemm_split(acc, ah, al, lda, a.pi_fr, a.pi_fr + (size_t)d * d / 4, d, d, col1, nf1, lane);
 
   // ---- stage 1 in registers: u = U / n, idx, ρ (kept in acc), ||ρ||², index words
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) quantize_mma_kernel(MmaArgs a) {
     for (int f = 0; f < kMaxNF; ++f)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[f][e] = 0.f;
-    const int nf2 = m / 64, col2 = warp * (m / 8);
+    const int cw2 = max(m / 8, 32), nf2 = warp * cw2 < m ? cw2 / 8 : 0, col2 = warp * cw2;
     gemm_split(acc, ah, al, lda, a.s_fr, a.s_fr + (size_t)m * d / 4, d, m, col2, nf2, lane);
     uint32_t sb0 = 0u, sb1 = 0u;
 #pragma unroll
@@ -292,7 +295,7 @@ tq_status launch_mma(const MmaArgs& a, cudaStream_t st) {
 }  // namespace
 
 bool tq::quantize_mma_supported(const tq_plan* plan, const tq_records* out) {
-  return plan->d % 128 == 0 && plan->d >= 256 && plan->d <= 1024 && (plan->m == plan->d || plan->m == 0) &&
+  return plan->d % 128 == 0 && plan->d <= 1024 && (plan->m == plan->d || plan->m == 0) &&
          out->layout == TQ_LAYOUT_ROWS && plan->pi_frag != nullptr && (plan->m == 0 || plan->s_frag != nullptr);
 }
 
