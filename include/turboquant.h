@@ -248,8 +248,9 @@ tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype q_dtype, i
 
 /* Fault bits set on the device by kernels whose pipeline waits are bounded
  * (bit 0: a tensor-core quantize wait ran out of its bound, a few seconds;
- * rows of that launch are undefined).  Kernels never spin forever: they set
- * the bit and finish.  Copies the word to *flags (synchronous) and clears it
+ * bit 1: a tensor-core decode wait; bit 2: a tensor-core search wait; the
+ * outputs of that launch are then undefined).  Kernels never spin forever:
+ * they set the bit and finish.  Copies the word to *flags (synchronous) and clears it
  * when reset != 0.  Errors: TQ_ERR_ARG (NULL), TQ_ERR_CUDA. */
 tq_status tq_fault_flags(uint32_t* flags, int reset);
 
