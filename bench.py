@@ -227,6 +227,28 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(times, world, device):
+    """Each time (seconds) maximised over the ranks of the default process group.
+
+    Every rank must call it with a list of the same length; with one rank the
+    list comes back unchanged.
+    """
+    times = [float(t) for t in times]
+    if world <= 1:
+        return times
+    import torch
+    import torch.distributed as dist
+
+    tt = torch.tensor(times, dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return [float(t) for t in tt.cpu().tolist()]
+
+
+def job_throughput(units_per_rank, world, seconds):
+    """Whole-job rate: the units all replicas processed over the slowest replica's time."""
+    return units_per_rank * world / seconds
+
+
 def workload_config(wl, bits):
     return {"workload": (f"{wl.name}: B={wl.B}, Hq={wl.Hq}, Hkv={wl.Hkv}, d={wl.d}, m={wl.m}, ctx={wl.ctx}, "
                          f"b={bits}, K/V {str(wl.dtype).replace('torch.', '')}"),
@@ -540,10 +562,6 @@ def main():
     t_step = sum(e[0].elapsed_time(e[2]) for e in events) / args.steps / 1e3
     t_quant = sum(e[0].elapsed_time(e[1]) for e in events) / args.steps / 1e3
     t_dec_step = sum(e[1].elapsed_time(e[2]) for e in events) / args.steps / 1e3
-    if world > 1:
-        tt = torch.tensor([t_step], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
     fault = _lib.tq_fault_flags()
 
     # ---- end to end: pinned host inputs in, attention output out, every step
@@ -574,6 +592,9 @@ def main():
     t_e2e = e0.elapsed_time(e1) / n_e2e / 1e3
     h2d = (Kh.numel() + Vh.numel()) * Kh.element_size() + qh.numel() * qh.element_size()
     d2h = outh.numel() * outh.element_size()
+    # the job is as slow as its slowest replica (every rank joins the reduction)
+    t_step, t_quant, t_dec_step, t_dec, t_e2e = max_over_ranks([t_step, t_quant, t_dec_step, t_dec, t_e2e], world,
+                                                               "cuda")
 
     if rank != 0:
         if world > 1:
@@ -599,9 +620,9 @@ def main():
         kname, ach, traffic_key = "decode_tc_kernel", dec_bytes / t_dec / 1e9, "decode_tc_kernel"
     traffic = dram_traffic(traffic_key, wl.name)
     line = {
-        "metric": METRIC, "value": B * T * world / t_step, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "metric": METRIC, "value": job_throughput(B * T, world, t_step), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(wl, args.bits),
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_kind": peak_kind, "traffic": traffic},
@@ -609,7 +630,8 @@ def main():
         "decode_kv_tokens_per_s": B * T / t_dec,
         "decode_frac_of_8tbs": dec_bytes / t_dec / 1e9 / NOMINAL_HBM_GBS,
         "quantize_mvec_per_s": 2 * nvec / t_quant / 1e6,
-        "e2e": {"value": B * T * world / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": job_throughput(B * T, world, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
         "fault_flags": fault,
         "clocks": clocks,
