@@ -46,6 +46,47 @@ def test_exact_codewords_reduce_to_library_attention():
         assert np.abs(out[bi] - ref[0].numpy()).max() < 1e-12
 
 
+def _estimate(rec, at, y, Pi, S, c):
+    """The two-stage estimate of ⟨x, y⟩ for the record at index ``at``, piece by
+    piece: ‖x‖ ⟨Π y, c[idx]⟩ + √(π/2)/m ‖r‖ ⟨S y, σ⟩."""
+    stage1 = float(rec["norm"][at]) * float(c[rec["idx"][at]] @ (Pi @ y))
+    sig = np.where(rec["sgn"][at], 1.0, -1.0)
+    return stage1 + qjl.estimate(S, y, float(rec["rnorm"][at]), sig)
+
+
+def test_decode_scores_are_the_two_stage_estimator():
+    """Every logit is the key's two-stage inner-product estimate times 1/√d."""
+    B, Hq, Hkv, T, d, w = 2, 4, 2, 12, 32, 2
+    _, Krec, Pi, S, c = _cache(B, Hkv, T, d, d, w, 14)
+    _, Vrec, _, _, _ = _cache(B, Hkv, T, d, d, w, 15)
+    q = np.random.default_rng(7).standard_normal((B, Hq, d))
+    ctx = np.array([T, 5])
+    _, sc = decode.decode_attention(q, Krec, Vrec, ctx, Pi, S, c)
+    for bi in range(B):
+        for g in range(Hq):
+            h = g // (Hq // Hkv)
+            for t in range(T):
+                if t >= ctx[bi]:
+                    assert sc[bi, g, t] == -np.inf
+                    continue
+                est = _estimate(Krec, (bi, h, t), q[bi, g], Pi, S, c)
+                assert abs(sc[bi, g, t] - est / np.sqrt(d)) < 1e-12 * (1 + abs(est))
+
+
+def test_context_one_output_is_the_value_estimator():
+    """With one token the output is that value's reconstruction: ⟨o, y⟩ is the
+    two-stage estimate of ⟨v, y⟩ for any y."""
+    B, H, T, d, w = 1, 1, 4, 32, 3
+    _, Krec, Pi, S, c = _cache(B, H, T, d, d, w, 16)
+    _, Vrec, _, _, _ = _cache(B, H, T, d, d, w, 17)
+    rng = np.random.default_rng(8)
+    out, _ = decode.decode_attention(rng.standard_normal((B, 3, d)), Krec, Vrec, np.array([1]), Pi, S, c)
+    for y in rng.standard_normal((4, d)):
+        est = _estimate(Vrec, (0, 0, 0), y, Pi, S, c)
+        for g in range(3):
+            assert abs(out[0, g] @ y - est) < 1e-12 * (1 + abs(est))
+
+
 def test_context_one_returns_reconstructed_value():
     B, H, T, d, w = 1, 1, 8, 32, 3
     _, Krec, Pi, S, c = _cache(B, H, T, d, d, w, 4)
@@ -104,6 +145,18 @@ def test_search_exact_codewords_is_brute_force_mips():
         ref = np.argsort(-(X @ Q[i]))[:10]
         assert np.array_equal(idx[i], ref)
         assert np.allclose(sc[i], (X @ Q[i])[ref], rtol=1e-12, atol=1e-12)
+
+
+def test_search_scores_are_the_two_stage_estimator():
+    N, d, w = 40, 32, 3
+    _, rec, Pi, S, c = _cache(1, 1, N, d, d, w, 18)
+    rec = {k: v.reshape((N,) + v.shape[3:]) for k, v in rec.items()}
+    Q = np.random.default_rng(9).standard_normal((3, d))
+    sc = search.scores(Q, rec, Pi, S, c)
+    for i in range(3):
+        for j in range(N):
+            est = _estimate(rec, j, Q[i], Pi, S, c)
+            assert abs(sc[i, j] - est) < 1e-12 * (1 + abs(est))
 
 
 def test_search_ties_go_to_lower_index():

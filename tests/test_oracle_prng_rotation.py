@@ -39,6 +39,10 @@ def test_box_muller_normals_are_standard_normal():
     assert abs(z.mean()) < 4.0 / 256
     assert abs(z.var() - 1.0) < 0.03
     assert stats.kstest(z, "norm").pvalue > 1e-3
+    # the two members of a pair are independent: uncorrelated, and z₁² + z₂² ~ Exp(mean 2)
+    z1, z2 = z[0::2], z[1::2]
+    assert abs(np.corrcoef(z1, z2)[0, 1]) < 4.0 / np.sqrt(len(z1))
+    assert stats.kstest(z1 * z1 + z2 * z2, "expon", args=(0.0, 2.0)).pvalue > 1e-3
     # odd count is a prefix of the even fill
     assert np.array_equal(prng.normals(12345, 7), z[:7])
 
