@@ -111,6 +111,15 @@ def _signs_stored_inverted(f):
     return quant
 
 
+def _rnorm_of_x(f):
+    """Two-stage quantizer storing ‖x‖ where ‖r‖ belongs (the plain-QJL norm)."""
+    def quant(*args):
+        z = f(*args)
+        z.rnorm = z.norm.copy()
+        return z
+    return quant
+
+
 def _decode_dropping_qjl(keys):
     """Attention over records that leaves out the QJL term of the keys (or of the values)."""
     def dec(q, K_rec, V_rec, ctx_len, Pi, S, centroids, scale=None, qjl_stage=True):
@@ -191,6 +200,8 @@ MUTANTS = [
            t_q.test_two_stage_score_is_unbiased_over_S),
     Mutant("stored_sign_convention_inverted", quantize, "quantize", _signs_stored_inverted,
            t_q.test_two_stage_score_is_unbiased_over_S),
+    Mutant("residual_norm_replaced_by_vector_norm", quantize, "quantize", _rnorm_of_x,
+           lambda: t_q.test_tiny_workload_score_errors_match_the_closed_form_spread(2)),
     Mutant("qjl_scale_without_sqrt_pi_over_2", qjl, "qjl_alpha", lambda f: (lambda m: 1.0 / m),
            t_q.test_qjl_estimator_unbiased_with_closed_form_variance),
     Mutant("qjl_signs_of_transposed_s", qjl, "signs", lambda f: (lambda S, r: f(S.T, r)),

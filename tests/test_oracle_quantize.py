@@ -244,3 +244,29 @@ def test_stage1_only_records(w):
     ip = np.sum(X * xt, axis=1) / np.sum(X * X, axis=1)
     assert abs(ip.mean() - (1.0 - d * mse)) < 5 * ip.std() / np.sqrt(len(ip)) + 1e-3
     assert ip.mean() < 1.0
+
+
+@pytest.mark.parametrize("w", [1, 2, 3])
+def test_tiny_workload_score_errors_match_the_closed_form_spread(w):
+    """The 4096 keys and 8 queries of the tiny workload, one draw of S: the
+    two-stage estimate's error e = est - ⟨q, k⟩, divided by the closed-form
+    deviation √(((π/2)‖q‖²‖r‖² - ⟨q, r⟩²)/m), has mean ≈ 0 and mean square ≈ 1."""
+    from online_kv_cache_04_b300.workloads import QJL_SEED, ROTATION_SEED, WORKLOADS, make_kv, make_queries
+
+    wl = WORKLOADS["tiny"]
+    d = m = wl.d
+    K = make_kv(wl, which=0)[0, 0].double().numpy()
+    q = make_queries(wl)[0].double().numpy()
+    Pi = rotation.make_rotation(d, ROTATION_SEED)
+    S = qjl.make_qjl(m, d, QJL_SEED)
+    c, b, _, _ = codebook.lloyd_max(d, w)
+    z = quantize.quantize(K, Pi, S, c, b)
+    est = q @ quantize.reconstruct(z.idx, z.sgn, z.norm, z.rnorm, Pi, S, c).T
+    _, _, _, xt = quantize.stage1(K, Pi, c, b)
+    R = K - xt
+    qr = q @ R.T
+    var = ((math.pi / 2) * np.sum(q * q, axis=1)[:, None] * np.sum(R * R, axis=1)[None, :] - qr ** 2) / m
+    zs = (est - q @ K.T) / np.sqrt(var)
+    assert abs(zs.mean()) < 0.03                 # 32768 errors; per-head means stay within ±0.03
+    assert np.all(np.abs(zs.mean(axis=1)) < 0.06)
+    assert 0.85 < np.mean(zs * zs) < 1.15
