@@ -5,7 +5,7 @@ import os
 
 import numpy as np
 import pytest
-from scipy import integrate, special
+from scipy import integrate
 
 from oracle import codebook
 

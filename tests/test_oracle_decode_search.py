@@ -1,7 +1,6 @@
 """Pins for the oracle's attention and search over stored records (no GPU)."""
 
 import numpy as np
-import pytest
 import torch
 
 from oracle import codebook, decode, qjl, quantize, rotation, search

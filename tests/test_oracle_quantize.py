@@ -4,7 +4,6 @@ import math
 
 import numpy as np
 import pytest
-from scipy import special
 
 from oracle import codebook, pack, prng, qjl, quantize, rotation
 
