@@ -67,21 +67,33 @@ def measured_peaks():
         return 6400.0, "fallback"
 
 
-def sources_sha():
+# The files that decide what a profiled kernel does per launch: its own
+# translation unit, the file that dispatches and launches it, and the shared
+# internal headers.  A DRAM-traffic record stays valid while these hash the same.
+KERNEL_SOURCES = {
+    "quantize_tc_kernel": ("tq_quantize_tc.cu", "tq_quantize.cu"),
+    "decode_tc_kernel": ("tq_decode_tc.cu", "tq_decode.cu"),
+}
+SHARED_SOURCES = ("tq_internal.h", "tq_sm100.cuh")
+
+
+def kernel_sources_sha(kernel, csrc=None):
+    """First 16 hex digits of the SHA-256 of a kernel's source files (KERNEL_SOURCES)."""
+    csrc = csrc or os.path.join(ROOT, "online_kv_cache_04_b300", "csrc")
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "online_kv_cache_04_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel] + SHARED_SOURCES:
+        h.update(f.encode() + b"\0")
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def dram_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current sources."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
+def dram_traffic(kernel, workload, record=None, csrc=None):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the kernel's current sources."""
+    path = record or os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
-    sha = sources_sha()
+    sha = kernel_sources_sha(kernel, csrc)
     for line in open(path):
         v = line.split()
         if len(v) == 4 and not line.startswith("#") and v[0] == kernel and v[1] == sha and v[3] == workload:
