@@ -239,7 +239,8 @@ tq_status tq_decode_scores(const tq_plan* plan, const void* q, tq_dtype q_dtype,
  * vector search engines): score_i = ||x_i|| <Π q, c[idx_i]> + √(π/2)/m
  * ||r_i|| <S q, σ_i>, k largest in descending order, equal scores -> lower
  * index.  q: device [nq][d] of q_dtype; idx_out: device int32 [nq][k];
- * score_out: device fp32 [nq][k]; 1 <= k <= 64.
+ * score_out: device fp32 [nq][k]; 1 <= k <= 64.  When k > n, ranks n .. k-1
+ * hold index -1 and score -inf.
  * Errors: TQ_ERR_ARG, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
 tq_status tq_search_workspace_size(const tq_plan* plan, int nq, int64_t n, int k, size_t* bytes);
 tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype q_dtype, int nq, const tq_records* recs,

@@ -81,6 +81,19 @@ def test_k_equals_n_and_k_64(gpu_lib):
     _check_topk(gidx, gsc, osc, 64)
 
 
+@pytest.mark.parametrize("d", [128, 96])
+def test_k_beyond_n_pads_with_minus_one(gpu_lib, d):
+    """k > n: the n stored vectors in rank order, then index -1 and score -inf
+    (d = 128 on the tensor-core scores, d = 96 on the SIMT scores)."""
+    g = torch.Generator().manual_seed(11 + d)
+    n, k = 5, 12
+    X = torch.randn(n, d, generator=g)
+    Q = torch.randn(3, d, generator=g)
+    gidx, gsc, osc = _run(X.cuda(), Q.cuda(), d, d, 2, k)
+    _check_topk(gidx[:, :n], gsc[:, :n], osc, n)
+    assert np.all(gidx[:, n:] == -1) and np.all(gsc[:, n:] == -np.inf)
+
+
 def test_generic_d1024_slice(gpu_lib):
     """Unit-norm anisotropic vectors, d = m = 1024, b = 4: 65536 stored, 64 queries, top-10."""
     wl = WORKLOADS["generic"]
