@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--queries", type=int, default=256)
     ap.add_argument("--quantize-only", action="store_true",
                     help="time tq_quantize_pair alone (K and V, one launch) on --workload / --batch; for profilers")
+    ap.add_argument("--append-only", action="store_true",
+                    help="time tq_append_kv (one new key and value per batch row and kv head, into full caches) "
+                         "followed by tq_decode_attention on --workload / --batch")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (0: keep)")
     return ap.parse_args()
 
@@ -484,6 +487,9 @@ def run_single(args):
             _lib.tq_quantize(plan, X, rec)
             del X
         q = make_queries(wl, device="cuda")
+        if args.append_only:
+            run_append_step(args, _lib, plan, wl, Kr, Vr, q, stream, flush)
+            return
         ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
         out = torch.empty(B, Hq, d, device="cuda")
         ws = torch.empty(_lib.tq_decode_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
@@ -498,6 +504,45 @@ def run_single(args):
           flush=True)
 
 
+def run_append_step(args, _lib, plan, wl, Kr, Vr, q, stream, flush):
+    """A decode step with its online append: tq_append_kv writes token ctx-1 of every (batch row,
+    kv head) and advances the lengths to ctx, then tq_decode_attention reads the whole cache."""
+    import torch
+
+    from online_kv_cache_04_b300.workloads import make_kv
+
+    B, Hq, Hkv, T, d = wl.B, wl.Hq, wl.Hkv, wl.ctx, wl.d
+    kn = make_kv(wl, B=B, T=1, which=0, device="cuda")[:, :, 0].contiguous()  # [B, Hkv, d]
+    vn = make_kv(wl, B=B, T=1, which=1, device="cuda")[:, :, 0].contiguous()
+    ctx = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, Hq, d, device="cuda")
+    ws = torch.empty(_lib.tq_decode_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+    evs = []
+    n_iter = max(args.warmup, 3) + args.steps
+    # a bounded spin (about 0.1 s) at the head of the queue lets the host enqueue every
+    # step before the device reaches the first, so no host time lands inside a timed interval
+    torch.cuda._sleep(200_000_000)
+    for i in range(n_iter):
+        ctx.fill_(T - 1)  # outside the timed interval, like the L2 flush
+        flush.fill_(1)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        _lib.tq_append_kv(plan, kn, vn, Kr, Vr, ctx, T)
+        e[1].record(stream)
+        _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws)
+        e[2].record(stream)
+        if i >= max(args.warmup, 3):
+            evs.append(e)
+    torch.cuda.synchronize()
+    t_app = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
+    print(json.dumps({"mode": "append one key and value per (batch row, kv head), then decode",
+                      "workload": f"{wl.name} B={B}", "bits": args.bits, "appended_vectors": 2 * B * Hkv,
+                      "append_ms": t_app, "decode_ms": t_dec, "step_ms": t_app + t_dec,
+                      "ctx_after": int(ctx[0].item()), "fault_flags": _lib.tq_fault_flags(),
+                      "l2": "flushed before every step"}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -506,7 +551,7 @@ def main():
     if args.generic_only:
         run_generic(args)
         return
-    if args.decode_only or args.quantize_only:
+    if args.decode_only or args.quantize_only or args.append_only:
         run_single(args)
         return
     import torch

@@ -183,6 +183,23 @@ tq_status tq_quantize_pair(const tq_plan* plan, const void* x0, const void* x1, 
                            int64_t ld_x, const tq_records* out0, const tq_records* out1, int64_t out_offset,
                            tq_stream stream);
 
+/* The online step of a decode loop ([efficiency] §四: quantize every new
+ * vector as it arrives; [memory-wall] §2): quantize the new key and value of
+ * every (batch row b, kv head h) exactly as tq_quantize does and store them
+ * at token t = ctx_len[b] of their caches (row (b*Hkv + h)*ctx_stride + t,
+ * merged into its 32-row block in TQ_LAYOUT_BLOCK32), then add one to
+ * ctx_len[b] on the device, stream-ordered after every read of it.
+ * k_new, v_new: device [B][Hkv][d] of dtype, rows contiguous.  K, V: distinct
+ * caches of B*Hkv*ctx_stride rows or more (ctx_stride a multiple of 32 when
+ * either is in TQ_LAYOUT_BLOCK32).  ctx_len: device int32 [B], read and
+ * advanced.  A batch row whose cache is full (ctx_len[b] >= ctx_stride) or
+ * whose length is negative is neither written nor advanced, and fault bit 3
+ * is set.  Two launches.
+ * Errors: TQ_ERR_ARG (shapes, capacity, NULL, misaligned), TQ_ERR_CUDA. */
+tq_status tq_append_kv(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B, int Hkv,
+                       const tq_records* K, const tq_records* V, int32_t* ctx_len, int64_t ctx_stride,
+                       tq_stream stream);
+
 /* ------------------------------------------------------------------ decode
  * One decode step of GQA softmax attention over compressed K/V caches.
  * Per query head g (kv head h = g / (Hq/Hkv)) and token t < ctx_len[b]:
@@ -250,8 +267,9 @@ tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype q_dtype, i
 /* Fault bits set on the device by kernels whose pipeline waits are bounded
  * (bit 0: a tensor-core quantize wait ran out of its bound, a few seconds;
  * bit 1: a tensor-core decode wait; bit 2: a tensor-core search wait; the
- * outputs of that launch are then undefined).  Kernels never spin forever:
- * they set the bit and finish.  Copies the word to *flags (synchronous) and clears it
+ * outputs of that launch are then undefined.  Bit 3: tq_append_kv met a
+ * full cache or a negative length and skipped that batch row).  Kernels
+ * never spin forever: they set the bit and finish.  Copies the word to *flags (synchronous) and clears it
  * when reset != 0.  Errors: TQ_ERR_ARG (NULL), TQ_ERR_CUDA. */
 tq_status tq_fault_flags(uint32_t* flags, int reset);
 

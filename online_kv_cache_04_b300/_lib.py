@@ -47,6 +47,9 @@ _SIGNATURES = {
                                    ctypes.POINTER(tq_records), ctypes.c_int64, _vp]),
     "tq_quantize_pair": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, _vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), ctypes.c_int64, _vp]),
+    "tq_append_kv": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), _vp, ctypes.c_int64,
+                                    _vp]),
     "tq_decode_workspace_size": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]),
     "tq_decode_attention": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -226,6 +229,24 @@ def tq_quantize_pair(plan, x0, x1, out0, out1, out_offset=0, stream=None):
                                                        out0.ref, out1.ref, out_offset, _stream(stream)))
 
 
+def tq_append_kv(plan, k_new, v_new, K, V, ctx_len, ctx_stride, stream=None):
+    """Store the new key and value of every (batch row, kv head) at token ctx_len[b] and advance ctx_len.
+
+    k_new, v_new: device [B, Hkv, d] (fp32 or bf16, contiguous); ctx_len: device int32 [B], updated in place.
+    """
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype or k_new.dim() != 3:
+        raise ValueError("tq_append_kv: k_new and v_new must both be [B, Hkv, d] of one dtype")
+    if not (k_new.is_contiguous() and v_new.is_contiguous()):
+        raise ValueError("tq_append_kv: k_new and v_new must be contiguous")
+    import torch
+
+    if ctx_len.dtype != torch.int32 or ctx_len.numel() != k_new.shape[0]:
+        raise ValueError("tq_append_kv: ctx_len must be int32 [B]")
+    B, Hkv, _ = k_new.shape
+    _check("tq_append_kv", load().tq_append_kv(plan.ref, k_new.data_ptr(), v_new.data_ptr(), _dtype_code(k_new), B,
+                                               Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride, _stream(stream)))
+
+
 def tq_decode_workspace_size(plan, B, Hq, Hkv, ctx_stride):
     n = ctypes.c_size_t(0)
     _check("tq_decode_workspace_size", load().tq_decode_workspace_size(plan.ref, B, Hq, Hkv, ctx_stride,
@@ -269,7 +290,7 @@ def tq_search_topk(plan, q, recs, n, k, idx_out, score_out, workspace, stream=No
 
 
 def tq_fault_flags(reset=True):
-    """Device fault bits of the bounded-wait kernels (0 = none)."""
+    """Device fault bits: bounded waits that ran out, appends to a full cache (0 = none)."""
     v = ctypes.c_uint32(0)
     _check("tq_fault_flags", load().tq_fault_flags(ctypes.byref(v), 1 if reset else 0))
     return v.value
