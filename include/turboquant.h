@@ -190,7 +190,7 @@ tq_status tq_quantize_pair(const tq_plan* plan, const void* x0, const void* x1, 
  * merged into its 32-row block in TQ_LAYOUT_BLOCK32), then add one to
  * ctx_len[b] on the device, stream-ordered after every read of it.
  * k_new, v_new: device [B][Hkv][d] of dtype, rows contiguous.  K, V: distinct
- * caches of B*Hkv*ctx_stride rows or more (ctx_stride a multiple of 32 when
+ * caches (sharing a word array is TQ_ERR_ARG) of B*Hkv*ctx_stride rows or more (ctx_stride a multiple of 32 when
  * either is in TQ_LAYOUT_BLOCK32).  ctx_len: device int32 [B], read and
  * advanced.  A batch row whose cache is full (ctx_len[b] >= ctx_stride) or
  * whose length is negative is neither written nor advanced, and fault bit 3

@@ -199,6 +199,8 @@ extern "C" tq_status tq_append_kv(const tq_plan* plan, const void* k_new, const 
       !tq::aligned16(k_new) || !tq::aligned16(v_new) || !ctx_len || B < 1 || Hkv < 1 || ctx_stride < 1 ||
       ctx_stride > INT32_MAX || (dtype != TQ_F32 && dtype != TQ_BF16))
     return TQ_ERR_ARG;
+  // keys and values of one step land on the same rows: one cache for both would race
+  if (K->idx == V->idx || (K->sgn && K->sgn == V->sgn) || K->norm == V->norm) return TQ_ERR_ARG;
   const int64_t units = (int64_t)B * Hkv;
   if (units > INT32_MAX || units * ctx_stride > K->capacity || units * ctx_stride > V->capacity) return TQ_ERR_ARG;
   // a block-layout cache keeps whole 32-row blocks per (batch row, kv head)

@@ -134,14 +134,16 @@ def test_argument_errors_return_codes_without_launching():
                                    n.value, None) == _lib.TQ_ERR_UNSUPPORTED
     # append: capacity, block-layout stride, dtype, shapes
     kv = _fake_records(2 * 64)
-    blk = _lib.tq_records(4096, 8192, 12288, 16384, 2 * 64, _lib.TQ_LAYOUT_BLOCK32)
-    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv), 4096, 65, None) == _lib.TQ_ERR_ARG
-    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 2, 1, ref(kv), ref(blk), 4096, 48, None) == _lib.TQ_ERR_ARG
-    assert lib.tq_append_kv(ref(p), 4096, 4096, 7, 1, 2, ref(kv), ref(kv), 4096, 64, None) == _lib.TQ_ERR_ARG
-    assert lib.tq_append_kv(ref(p), 4096, 4100, 1, 1, 2, ref(kv), ref(kv), 4096, 64, None) == _lib.TQ_ERR_ARG
-    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 0, 2, ref(kv), ref(kv), 4096, 64, None) == _lib.TQ_ERR_ARG
-    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv), None, 64, None) == _lib.TQ_ERR_ARG
-    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv), 4096, 0, None) == _lib.TQ_ERR_ARG
+    kv2 = _lib.tq_records(20480, 24576, 28672, 32768, 2 * 64)
+    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv), 4096, 64, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv2), 4096, 65, None) == _lib.TQ_ERR_ARG
+    blk2 = _lib.tq_records(20480, 24576, 28672, 32768, 2 * 64, _lib.TQ_LAYOUT_BLOCK32)
+    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 2, 1, ref(kv), ref(blk2), 4096, 48, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_append_kv(ref(p), 4096, 4096, 7, 1, 2, ref(kv), ref(kv2), 4096, 64, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_append_kv(ref(p), 4096, 4100, 1, 1, 2, ref(kv), ref(kv2), 4096, 64, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 0, 2, ref(kv), ref(kv2), 4096, 64, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv2), None, 64, None) == _lib.TQ_ERR_ARG
+    assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv2), 4096, 0, None) == _lib.TQ_ERR_ARG
     # search: k range
     assert lib.tq_search_workspace_size(ref(p), 4, 100, 0, ref(n)) == _lib.TQ_ERR_ARG
     assert lib.tq_search_workspace_size(ref(p), 4, 100, 65, ref(n)) == _lib.TQ_ERR_ARG
