@@ -113,6 +113,26 @@ def _stream(stream):
     return getattr(stream, "cuda_stream", stream)
 
 
+def _on_device(name, *tensors):
+    """Device calls take CUDA tensors: a host pointer would reach a kernel and fault there."""
+    for t in tensors:
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name}: every tensor argument must live on a CUDA device")
+
+
+def _records_on_device(name, *recs):
+    for r in recs:
+        _on_device(name, r.idx, r.sgn, r.norm, r.rnorm)
+
+
+def _lengths(name, ctx_len):
+    import torch
+
+    _on_device(name, ctx_len)
+    if ctx_len.dtype != torch.int32:
+        raise ValueError(f"{name}: ctx_len must be int32")
+
+
 def _dtype_code(t):
     import torch
 
@@ -213,6 +233,8 @@ class Records:
 
 def tq_quantize(plan, x, out, out_offset=0, stream=None):
     """Quantize the rows of x [n, ld>=d] (fp32 or bf16, device) into out[out_offset:]."""
+    _on_device("tq_quantize", x)
+    _records_on_device("tq_quantize", out)
     n = x.shape[0]
     ld = x.stride(0) if x.dim() == 2 and n > 0 else plan.d
     _check("tq_quantize", load().tq_quantize(plan.ref, x.data_ptr(), _dtype_code(x), n, ld, out.ref, out_offset,
@@ -221,6 +243,8 @@ def tq_quantize(plan, x, out, out_offset=0, stream=None):
 
 def tq_quantize_pair(plan, x0, x1, out0, out1, out_offset=0, stream=None):
     """Quantize x0 into out0 and x1 into out1 (same shape, dtype and row stride), rows out_offset onward."""
+    _on_device("tq_quantize_pair", x0, x1)
+    _records_on_device("tq_quantize_pair", out0, out1)
     if x0.shape != x1.shape or x0.dtype != x1.dtype or x0.stride() != x1.stride():
         raise ValueError("tq_quantize_pair: x0 and x1 must have the same shape, dtype and strides")
     n = x0.shape[0]
@@ -242,6 +266,8 @@ def tq_append_kv(plan, k_new, v_new, K, V, ctx_len, ctx_stride, stream=None):
 
     if ctx_len.dtype != torch.int32 or ctx_len.numel() != k_new.shape[0]:
         raise ValueError("tq_append_kv: ctx_len must be int32 [B]")
+    _on_device("tq_append_kv", k_new, v_new, ctx_len)
+    _records_on_device("tq_append_kv", K, V)
     B, Hkv, _ = k_new.shape
     _check("tq_append_kv", load().tq_append_kv(plan.ref, k_new.data_ptr(), v_new.data_ptr(), _dtype_code(k_new), B,
                                                Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride, _stream(stream)))
@@ -255,6 +281,9 @@ def tq_decode_workspace_size(plan, B, Hq, Hkv, ctx_stride):
 
 
 def tq_decode_attention(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, workspace, scale=0.0, stream=None):
+    _on_device("tq_decode_attention", q, out, workspace)
+    _lengths("tq_decode_attention", ctx_len)
+    _records_on_device("tq_decode_attention", K, V)
     B, Hq, _ = q.shape
     _check("tq_decode_attention", load().tq_decode_attention(
         plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride,
@@ -264,6 +293,9 @@ def tq_decode_attention(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, workspace,
 
 def tq_decode_attention_noalloc(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, scale=0.0, stream=None):
     """tq_decode_attention with the library's built-in scratch array (no workspace argument)."""
+    _on_device("tq_decode_attention_noalloc", q, out)
+    _lengths("tq_decode_attention_noalloc", ctx_len)
+    _records_on_device("tq_decode_attention_noalloc", K, V)
     B, Hq, _ = q.shape
     _check("tq_decode_attention_noalloc", load().tq_decode_attention_noalloc(
         plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride,
@@ -271,6 +303,9 @@ def tq_decode_attention_noalloc(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, sc
 
 
 def tq_decode_scores(plan, q, K, ctx_len, ctx_stride, Hkv, scores, workspace, scale=0.0, stream=None):
+    _on_device("tq_decode_scores", q, scores, workspace)
+    _lengths("tq_decode_scores", ctx_len)
+    _records_on_device("tq_decode_scores", K)
     B, Hq, _ = q.shape
     _check("tq_decode_scores", load().tq_decode_scores(
         plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, ctx_len.data_ptr(), ctx_stride, float(scale),
@@ -284,6 +319,8 @@ def tq_search_workspace_size(plan, nq, n, k):
 
 
 def tq_search_topk(plan, q, recs, n, k, idx_out, score_out, workspace, stream=None):
+    _on_device("tq_search_topk", q, idx_out, score_out, workspace)
+    _records_on_device("tq_search_topk", recs)
     _check("tq_search_topk", load().tq_search_topk(
         plan.ref, q.data_ptr(), _dtype_code(q), q.shape[0], recs.ref, n, k, idx_out.data_ptr(),
         score_out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -178,3 +178,27 @@ def test_layout_argument_checks():
     assert lib.tq_search_workspace_size(ref(p), 4, 100, 10, ref(n)) == _lib.TQ_OK
     assert lib.tq_search_topk(ref(p), 4096, 1, 4, ref(blk), 100, 10, 4096, 4096, 4096, n.value,
                               None) == _lib.TQ_ERR_UNSUPPORTED
+
+
+def test_binding_refuses_host_tensors_before_any_call():
+    """A host pointer reaching a kernel would fault the GPU: the binding raises first."""
+    import torch
+
+    x = torch.zeros(4, 128)
+    ctx = torch.zeros(1, dtype=torch.int32)
+    rec = _lib.Records(64, 128, 128, 2, device="cpu")
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib.tq_quantize(None, x, rec)
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib.tq_quantize_pair(None, x, x, rec, rec)
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib.tq_append_kv(None, x[None], x[None], rec, rec, torch.zeros(1, dtype=torch.int32), 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib.tq_decode_attention(None, x[None], rec, rec, ctx, 64, 1, x[None], torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib.tq_decode_attention_noalloc(None, x[None], rec, rec, ctx, 64, 1, x[None])
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib.tq_decode_scores(None, x[None], rec, ctx, 64, 1, x, torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib.tq_search_topk(None, x, rec, 64, 10, torch.zeros(4, 10, dtype=torch.int32), torch.zeros(4, 10),
+                            torch.zeros(16, dtype=torch.uint8))
