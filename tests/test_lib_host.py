@@ -39,7 +39,7 @@ def test_rotation_matches_oracle(d):
 
 
 @pytest.mark.parametrize("d", [8, 32, 128, 1024])
-@pytest.mark.parametrize("w", [1, 2, 3])
+@pytest.mark.parametrize("w", [1, 2, 3, 4])
 def test_codebook_matches_oracle(d, w):
     c, b, mse = _lib.tq_make_codebook(d, w)
     oc, ob, omse, _ = ocb.lloyd_max(d, w)
