@@ -226,7 +226,7 @@ tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_dtype q_dty
 /* Decode attention without a caller workspace, for callers that cannot
  * allocate device memory (graph captures that forbid allocation, embedded
  * runtimes with memory fixed at start-up, plugins whose host owns the
- * allocator).  The paper has no counterpart: this is a deployment variant of
+ * allocator).  The sources describe no counterpart: this is a deployment variant of
  * tq_decode_attention, with the same arguments minus the workspace and the
  * same results.
  * Scratch: one array of TQ_NOALLOC_SCRATCH_BYTES (8 MiB) compiled into the
