@@ -18,8 +18,9 @@
  * Conventions shared by every call
  *   - Ownership: the caller owns every buffer.  The library never allocates
  *     or frees memory and may be called concurrently on different streams
- *     with disjoint outputs.  Its only state is one device word of fault
- *     bits (see tq_fault_flags).
+ *     with disjoint outputs.  Its state is one device word of fault bits
+ *     (see tq_fault_flags) and the fixed scratch array of
+ *     tq_decode_attention_noalloc, with that array's per-device address.
  *   - Device calls are asynchronous on the given stream (NULL = legacy
  *     default stream).  Argument errors are detected on the host and
  *     returned before anything is launched; a failed launch returns
@@ -232,7 +233,10 @@ tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_dtype q_dty
  * Scratch: one array of TQ_NOALLOC_SCRATCH_BYTES (8 MiB) compiled into the
  * library, resident on every GPU that loads it until the process exits.  The
  * first call on a device looks up the array's device address (make that first
- * call before any stream capture); no call allocates or frees memory.  All
+ * call before any stream capture) and later calls reuse it for the life of
+ * the process; a cudaDeviceReset of that device invalidates it, so do not
+ * call this entry point on a device after resetting it.  No call allocates
+ * or frees memory.  All
  * calls share the array: calls whose GPU work overlaps race on it, so order
  * them on one stream.  Nothing in the array needs clearing between calls.
  * Errors: as tq_decode_attention; TQ_ERR_WORKSPACE when the shape needs more
