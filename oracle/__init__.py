@@ -33,6 +33,7 @@ quantize   the two-stage quantizer (rotate, bucketize, residual, QJL signs)
 pack       bit-sliced packing of indices and signs into 32-bit words
 decode     scores and softmax attention over stored records
 search     inner-product top-k over stored records
+mixed      outlier-channel split precision (two instances, b + 1 / b bits)
 """
 
-from . import prng, rotation, codebook, qjl, quantize, pack, decode, search  # noqa: F401
+from . import prng, rotation, codebook, qjl, quantize, pack, decode, search, mixed  # noqa: F401
