@@ -34,6 +34,7 @@ pack       bit-sliced packing of indices and signs into 32-bit words
 decode     scores and softmax attention over stored records
 search     inner-product top-k over stored records
 mixed      outlier-channel split precision (two instances, b + 1 / b bits)
+polar      PolarQuant's recursive polar stage, an alternative stage 1
 """
 
-from . import prng, rotation, codebook, qjl, quantize, pack, decode, search, mixed  # noqa: F401
+from . import prng, rotation, codebook, qjl, quantize, pack, decode, search, mixed, polar  # noqa: F401
