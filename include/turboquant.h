@@ -255,6 +255,48 @@ tq_status tq_decode_scores(const tq_plan* plan, const void* q, tq_dtype q_dtype,
                            const tq_records* K, const int32_t* ctx_len, int64_t ctx_stride, float scale,
                            float* scores, void* workspace, size_t ws_bytes, tq_stream stream);
 
+/* ------------------------------------------------------------------ split
+ * Outlier-channel split precision ("TurboQuant压缩效果": the 128 channels of a
+ * head split, the few outlier channels quantized one bit higher than the
+ * rest -- the 2.5- and 3.5-bit settings, the label being the average over
+ * the channels).  perm: device int32 [d], a permutation of the head's d
+ * channels: perm[0 .. d_o) are the outlier channels, perm[d_o .. d) the
+ * regular ones (fixed per head, chosen by the caller, e.g. the channels of
+ * largest mean square).  Each side is its own instance with its own plan:
+ * plan_o with d = d_o channels and w = b bits of MSE indices (b + 1 total
+ * bits), plan_r with d = d - d_o and w = b - 1 (b total bits), both with
+ * QJL rows (m > 0), each side at most 128 channels.  Records of each side are
+ * TQ_LAYOUT_ROWS, one row per vector as for tq_quantize.  Bits per
+ * coordinate (indices and signs): b + d_o/d, e.g. 2.5 for b = 2, d_o = d/2.
+ */
+
+/* Quantize n vectors of d = plan_o->d + plan_r->d channels: the channels
+ * perm[0 .. d_o) of each row through plan_o into out_o, the rest through
+ * plan_r into out_r, rows [out_offset, out_offset + n) of both.  x: device,
+ * row stride ld_x elements (>= d, multiple of 8).  Two launches.
+ * Errors: TQ_ERR_ARG (shapes, capacity, NULL, misaligned, a record set not in
+ * TQ_LAYOUT_ROWS), TQ_ERR_CUDA. */
+tq_status tq_quantize_split(const tq_plan* plan_o, const tq_plan* plan_r, const int32_t* perm, const void* x,
+                            tq_dtype dtype, int64_t n, int64_t ld_x, const tq_records* out_o,
+                            const tq_records* out_r, int64_t out_offset, tq_stream stream);
+
+/* Decode attention over split records: the score of a key is the sum of the
+ * two sides' estimators (the inner product splits over the channel sets),
+ * one softmax over those sums, and the output carries each side's
+ * unrotated value sum at its own channels.  Arguments as tq_decode_attention
+ * (q: device [B][Hq][d], out: device fp32 [B][Hq][d], scale <= 0 means
+ * 1/√d), with both sides' key and value records (row
+ * (b*Hkv + h)*ctx_stride + t in each), at most 8 query heads per kv head.
+ * Three launches (query prep, context splits, combine).
+ * Errors: TQ_ERR_ARG, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_decode_split_workspace_size(const tq_plan* plan_o, const tq_plan* plan_r, int B, int Hq, int Hkv,
+                                         int64_t ctx_stride, size_t* bytes);
+tq_status tq_decode_attention_split(const tq_plan* plan_o, const tq_plan* plan_r, const int32_t* perm, const void* q,
+                                    tq_dtype q_dtype, int B, int Hq, int Hkv, const tq_records* K_o,
+                                    const tq_records* K_r, const tq_records* V_o, const tq_records* V_r,
+                                    const int32_t* ctx_len, int64_t ctx_stride, float scale, float* out,
+                                    void* workspace, size_t ws_bytes, tq_stream stream);
+
 /* ------------------------------------------------------------------ search
  * Inner-product top-k over n compressed vectors ([video] / [memory-wall]:
  * vector search engines): score_i = ||x_i|| <Π q, c[idx_i]> + √(π/2)/m

@@ -67,6 +67,17 @@ _SIGNATURES = {
     "tq_search_topk": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int,
                                       ctypes.POINTER(tq_records), ctypes.c_int64, ctypes.c_int, _vp, _vp, _vp,
                                       ctypes.c_size_t, _vp]),
+    "tq_quantize_split": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.POINTER(tq_plan), _vp, _vp, ctypes.c_int,
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(tq_records),
+                                         ctypes.POINTER(tq_records), ctypes.c_int64, _vp]),
+    "tq_decode_split_workspace_size": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.POINTER(tq_plan), ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                                      ctypes.POINTER(ctypes.c_size_t)]),
+    "tq_decode_attention_split": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.POINTER(tq_plan), _vp, _vp,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.POINTER(tq_records), ctypes.POINTER(tq_records),
+                                                 ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), _vp,
+                                                 ctypes.c_int64, ctypes.c_float, _vp, _vp, ctypes.c_size_t, _vp]),
     "tq_fault_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -324,6 +335,41 @@ def tq_search_topk(plan, q, recs, n, k, idx_out, score_out, workspace, stream=No
     _check("tq_search_topk", load().tq_search_topk(
         plan.ref, q.data_ptr(), _dtype_code(q), q.shape[0], recs.ref, n, k, idx_out.data_ptr(),
         score_out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_quantize_split(plan_o, plan_r, perm, x, out_o, out_r, out_offset=0, stream=None):
+    """Outlier channels perm[:plan_o.d] of each row of x [n, ld>=d] through plan_o into out_o,
+    the rest through plan_r into out_r.  perm: device int32 [d]."""
+    _on_device("tq_quantize_split", x, perm)
+    _records_on_device("tq_quantize_split", out_o, out_r)
+    import torch
+
+    if perm.dtype != torch.int32:
+        raise ValueError("tq_quantize_split: perm must be int32")
+    n = x.shape[0]
+    ld = x.stride(0) if x.dim() == 2 and n > 0 else plan_o.d + plan_r.d
+    _check("tq_quantize_split", load().tq_quantize_split(plan_o.ref, plan_r.ref, perm.data_ptr(), x.data_ptr(),
+                                                         _dtype_code(x), n, ld, out_o.ref, out_r.ref, out_offset,
+                                                         _stream(stream)))
+
+
+def tq_decode_split_workspace_size(plan_o, plan_r, B, Hq, Hkv, ctx_stride):
+    n = ctypes.c_size_t(0)
+    _check("tq_decode_split_workspace_size", load().tq_decode_split_workspace_size(
+        plan_o.ref, plan_r.ref, B, Hq, Hkv, ctx_stride, ctypes.byref(n)))
+    return n.value
+
+
+def tq_decode_attention_split(plan_o, plan_r, perm, q, K_o, K_r, V_o, V_r, ctx_len, ctx_stride, Hkv, out, workspace,
+                              scale=0.0, stream=None):
+    _on_device("tq_decode_attention_split", perm, q, out, workspace)
+    _lengths("tq_decode_attention_split", ctx_len)
+    _records_on_device("tq_decode_attention_split", K_o, K_r, V_o, V_r)
+    B, Hq, _ = q.shape
+    _check("tq_decode_attention_split", load().tq_decode_attention_split(
+        plan_o.ref, plan_r.ref, perm.data_ptr(), q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K_o.ref, K_r.ref, V_o.ref,
+        V_r.ref, ctx_len.data_ptr(), ctx_stride, float(scale), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def tq_fault_flags(reset=True):

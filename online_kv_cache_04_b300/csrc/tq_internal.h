@@ -77,6 +77,12 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
                            float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
                            cudaStream_t stream);
 
+// SIMT quantizer over a column subset (tq_quantize.cu): element j of row r is
+// x[r][cols[j]] for j < plan->d (cols: device int32); rows [out_offset,
+// out_offset + n) of `out`, TQ_LAYOUT_ROWS.  Arguments already checked.
+tq_status quantize_simt_cols(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
+                             const int32_t* cols, const tq_records* out, int64_t out_offset, cudaStream_t st);
+
 // Warp tensor-core quantizer (tq_quantize_mma.cu): d a multiple of 128 up to
 // 1024, m = d or 0, fp32 or bf16 input, TQ_LAYOUT_ROWS output; rows
 // [row0, row0 + n) of `out`.

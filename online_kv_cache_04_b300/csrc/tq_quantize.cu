@@ -32,6 +32,7 @@ struct QuantArgs {
   float* norm;           // rows already offset
   float* rnorm;
   int64_t row0;          // cache row of x's row 0 (layout 1 addressing)
+  const int32_t* cols;   // optional [d] device column list: element j of a row is x[row][cols[j]]
 };
 
 // Layout 1: merge the bits of the tile's rows into the 32-row block words.
@@ -88,7 +89,8 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantArgs a) {
     for (int e = tid; e < TV * d; e += kThreads) {
       const int v = e / d, i = e - v * d;
       const int64_t row = v0 + v;
-      xs[e] = row < a.n ? load_elem<T>(x + row * a.ld + i) : 0.0f;
+      const int64_t col = a.cols ? __ldg(a.cols + i) : i;
+      xs[e] = row < a.n ? load_elem<T>(x + row * a.ld + col) : 0.0f;
     }
     __syncthreads();
     for (int v = warp; v < TV; v += kThreads / 32) {
@@ -215,6 +217,28 @@ tq_status launch_simt_any(const QuantArgs& a, tq_dtype dtype, cudaStream_t st) {
 
 }  // namespace
 
+tq_status tq::quantize_simt_cols(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
+                                 const int32_t* cols, const tq_records* out, int64_t out_offset, cudaStream_t st) {
+  QuantArgs a{};
+  a.x = x;
+  a.n = n;
+  a.ld = ld_x;
+  a.d = plan->d;
+  a.m = plan->m;
+  a.w = plan->w;
+  a.pi_t = plan->pi_t;
+  a.s_rot_t = plan->s_rot_t;
+  a.centroids = plan->centroids;
+  a.bounds = plan->bounds;
+  a.idx = out->idx + out_offset * (plan->w * plan->d / 32);
+  a.sgn = plan->m > 0 ? out->sgn + out_offset * (plan->m / 32) : nullptr;
+  a.norm = out->norm + out_offset;
+  a.rnorm = plan->m > 0 ? out->rnorm + out_offset : nullptr;
+  a.row0 = out_offset;
+  a.cols = cols;
+  return launch_simt_any<TQ_LAYOUT_ROWS>(a, dtype, st);
+}
+
 extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
                                  const tq_records* out, int64_t out_offset, tq_stream stream) {
   if (!tq::valid_plan(plan) || !tq::valid_records(out, plan) || n < 0 || out_offset < 0) return TQ_ERR_ARG;
@@ -223,7 +247,7 @@ extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dt
   if (x == nullptr || !tq::aligned16(x) || ld_x < plan->d || ld_x % 8 != 0) return TQ_ERR_ARG;
   if (out_offset > out->capacity || n > out->capacity - out_offset) return TQ_ERR_ARG;
   const bool rows = out->layout == TQ_LAYOUT_ROWS;
-  QuantArgs a;
+  QuantArgs a{};
   a.x = x;
   a.n = n;
   a.ld = ld_x;

@@ -28,6 +28,10 @@ import torch
 
 ROTATION_SEED = 0x71550001
 QJL_SEED = 0x71550002
+# split precision: the outlier side's and the regular side's own instances
+SPLIT_SEEDS = {"outlier": (0x71550011, 0x71550012), "regular": (0x71550021, 0x71550022)}
+# the polar stage's rotation and QJL matrix
+POLAR_SEEDS = (0x71550031, 0x71550032)
 
 
 @dataclass(frozen=True)
