@@ -111,12 +111,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, interval_ms=50):
         self.index = index
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -160,6 +160,14 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- oracle arm
+
+def sampled(index, fn):
+    """fn() with the GPU's clocks sampled (every 200 ms) over its run: (result, clocks)."""
+    sampler = ClockSampler(index, interval_ms=200)
+    sampler.wait_first()
+    out = fn()
+    return out, sampler.stop()
+
 
 def oracle_step(wl, w, heads, T):
     """The float64 oracle on `heads` kv heads x T tokens of batch row 0: quantize K, V, then decode."""
@@ -281,6 +289,9 @@ def timed(stream, fn, iters, flush=None):
     device idle inside the timed interval."""
     import torch
 
+    # a bounded spin (about 0.1 s) at the head of the queue: the host enqueues
+    # every call before the device reaches the first one
+    torch.cuda._sleep(200_000_000)
     ev = []
     for _ in range(iters):
         if flush is not None:

@@ -281,21 +281,92 @@ tq_status tq_quantize_split(const tq_plan* plan_o, const tq_plan* plan_r, const 
                             const tq_records* out_r, int64_t out_offset, tq_stream stream);
 
 /* Decode attention over split records: the score of a key is the sum of the
- * two sides' estimators (the inner product splits over the channel sets),
- * one softmax over those sums, and the output carries each side's
- * unrotated value sum at its own channels.  Arguments as tq_decode_attention
- * (q: device [B][Hq][d], out: device fp32 [B][Hq][d], scale <= 0 means
- * 1/√d), with both sides' key and value records (row
- * (b*Hkv + h)*ctx_stride + t in each), at most 8 query heads per kv head.
- * Three launches (query prep, context splits, combine).
+ * two sides' estimators (the inner product splits over the channel sets; the
+ * query is split by perm_k, the keys' permutation), one softmax over those
+ * sums, and the output carries each side's unrotated value sum at its own
+ * channels of perm_v (the values' permutation: the outlier channels of keys
+ * and values differ).  Other arguments as tq_decode_attention (q: device
+ * [B][Hq][d], out: device fp32 [B][Hq][d], scale <= 0 means 1/√d), with both
+ * sides' key and value records (row (b*Hkv + h)*ctx_stride + t in each), at
+ * most 8 query heads per kv head.  Three launches (query prep, context
+ * splits, combine).
  * Errors: TQ_ERR_ARG, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
 tq_status tq_decode_split_workspace_size(const tq_plan* plan_o, const tq_plan* plan_r, int B, int Hq, int Hkv,
                                          int64_t ctx_stride, size_t* bytes);
-tq_status tq_decode_attention_split(const tq_plan* plan_o, const tq_plan* plan_r, const int32_t* perm, const void* q,
+tq_status tq_decode_attention_split(const tq_plan* plan_o, const tq_plan* plan_r, const int32_t* perm_k,
+                                    const int32_t* perm_v, const void* q,
                                     tq_dtype q_dtype, int B, int Hq, int Hkv, const tq_records* K_o,
                                     const tq_records* K_r, const tq_records* V_o, const tq_records* V_r,
                                     const int32_t* ctx_len, int64_t ctx_stride, float scale, float* out,
                                     void* workspace, size_t ws_bytes, tq_stream stream);
+
+/* ------------------------------------------------------------------ polar
+ * PolarQuant's recursive polar stage as an alternative first stage, then the
+ * same 1-bit QJL stage on the residual ("TurboQuant 与 AI 效率革命" §二
+ * "突破：极坐标" and §四; "TurboQuant压缩效果": 4 bits at the first level,
+ * 2 at later ones).  A rotated vector u = Π x (d a power of two) becomes one
+ * radius and d - 1 angles: level 1 pairs (u_2i, u_2i+1) into a radius and
+ * atan2(u_2i+1, u_2i) in [0, 2π); level l >= 2 pairs the level l-1 radii
+ * (a, b) into sqrt(a² + b²) and atan2(b, a) in [0, π/2].  Level-1 angles are
+ * uniform and take 2^b1 equal cells with midpoint centroids; a level-l angle
+ * follows the law ∝ sin^(k-1)(2ψ), k = 2^(l-1), with mean π/4 ("TurboQuant 与
+ * AI 效率革命" §二) and takes the Lloyd-Max codebook of that law at b bits.
+ * Shapes: d a power of two in [4, 256], m a multiple of 32 in [32, 256],
+ * b1 and b in {1, 2, 4}.
+ */
+
+/* Angle codebooks, float64, host.  centroids: 2^b1 level-1 values, then
+ * 2^b per level for levels 2 .. log2(d); bounds: 2^b1 - 1, then 2^b - 1 per
+ * level (ascending within each level).  Errors: TQ_ERR_ARG, TQ_ERR_NUMERIC. */
+tq_status tq_make_polar_codebooks(int d, int b1, int b, double* centroids, double* bounds);
+
+/* 32-bit index words of one polar record: the d/2 level-1 codes (b1 bits)
+ * packed 32/b1 to a word, code i at bits b1·(i mod 32/b1) of word
+ * i / (32/b1) ("TurboQuant压缩效果": eight 4-bit numbers in one 32-bit word),
+ * then from the next word the codes of levels 2, 3, ... in that order, b bits
+ * each, packed the same way.  0 for an unsupported shape. */
+int tq_polar_index_words(int d, int b1, int b);
+
+typedef struct tq_polar_plan {
+  int d, m, b1, b;
+  float qjl_alpha;          /* √(π/2)/m                                     */
+  const float* pi;          /* [d][d]  Π                                    */
+  const float* pi_t;        /* [d][d]  Πᵀ                                   */
+  const float* s_rot;       /* [m][d]  S Πᵀ                                 */
+  const float* s_rot_t;     /* [d][m]                                       */
+  const float* tables;      /* [levels][3][16]: cos, sin of the centroids, bounds */
+} tq_polar_plan;
+
+/* Device bytes of a polar plan (0 if unsupported), and its initialisation
+ * from tq_make_rotation, tq_make_qjl (s_rot) and tq_make_polar_codebooks
+ * (one caller-owned device buffer; the copy completes before the call
+ * returns).  Errors: TQ_ERR_ARG, TQ_ERR_CUDA. */
+size_t tq_polar_plan_bytes(int d, int m, int b1, int b);
+tq_status tq_polar_plan_init(tq_polar_plan* plan, int d, int m, int b1, int b, const double* pi,
+                             const double* s_rot, const double* centroids, const double* bounds, void* dev,
+                             size_t bytes, tq_stream stream);
+
+/* Quantize n vectors: rotate, transform, bucketize every angle with its
+ * level's codebook (a tie goes to the lower cell), rebuild ũ from the
+ * centroids and the norm, and take σ = sign(S r), ||r|| for r = x - Πᵀũ.
+ * out: TQ_LAYOUT_ROWS records with tq_polar_index_words(d, b1, b) index words
+ * per row, m/32 sign words, norm = ||x|| and rnorm = ||r||, rows
+ * [out_offset, out_offset + n).  x: device, row stride ld_x (>= d, multiple
+ * of 8).  Errors: TQ_ERR_ARG, TQ_ERR_CUDA. */
+tq_status tq_quantize_polar(const tq_polar_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
+                            const tq_records* out, int64_t out_offset, tq_stream stream);
+
+/* Decode attention over polar records, as tq_decode_attention: score of key
+ * t = scale·(⟨Π q, ũ_t⟩ + √(π/2)/m ||r_t|| ⟨S q, σ_t⟩), softmax, values
+ * accumulated in the rotated domain, one unrotation.  At most 8 query heads
+ * per kv head.  Three launches (query prep, context splits, combine).
+ * Errors: TQ_ERR_ARG, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_decode_polar_workspace_size(const tq_polar_plan* plan, int B, int Hq, int Hkv, int64_t ctx_stride,
+                                         size_t* bytes);
+tq_status tq_decode_attention_polar(const tq_polar_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq,
+                                    int Hkv, const tq_records* K, const tq_records* V, const int32_t* ctx_len,
+                                    int64_t ctx_stride, float scale, float* out, void* workspace, size_t ws_bytes,
+                                    tq_stream stream);
 
 /* ------------------------------------------------------------------ search
  * Inner-product top-k over n compressed vectors ([video] / [memory-wall]:

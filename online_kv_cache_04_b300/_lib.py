@@ -29,6 +29,12 @@ class tq_plan(ctypes.Structure):
                 ("s_frag", _vp)]
 
 
+class tq_polar_plan(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("m", ctypes.c_int), ("b1", ctypes.c_int), ("b", ctypes.c_int),
+                ("qjl_alpha", ctypes.c_float), ("pi", _vp), ("pi_t", _vp), ("s_rot", _vp), ("s_rot_t", _vp),
+                ("tables", _vp)]
+
+
 class tq_records(ctypes.Structure):
     _fields_ = [("idx", _vp), ("sgn", _vp), ("norm", _vp), ("rnorm", _vp), ("capacity", ctypes.c_int64),
                 ("layout", ctypes.c_int32)]
@@ -73,11 +79,25 @@ _SIGNATURES = {
     "tq_decode_split_workspace_size": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.POINTER(tq_plan), ctypes.c_int,
                                                       ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                       ctypes.POINTER(ctypes.c_size_t)]),
-    "tq_decode_attention_split": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.POINTER(tq_plan), _vp, _vp,
+    "tq_decode_attention_split": (ctypes.c_int, [ctypes.POINTER(tq_plan), ctypes.POINTER(tq_plan), _vp, _vp, _vp,
                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  ctypes.POINTER(tq_records), ctypes.POINTER(tq_records),
                                                  ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), _vp,
                                                  ctypes.c_int64, ctypes.c_float, _vp, _vp, ctypes.c_size_t, _vp]),
+    "tq_make_polar_codebooks": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_double_p, _c_double_p]),
+    "tq_polar_index_words": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "tq_polar_plan_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "tq_polar_plan_init": (ctypes.c_int, [ctypes.POINTER(tq_polar_plan), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, _c_double_p, _c_double_p, _c_double_p, _c_double_p, _vp,
+                                          ctypes.c_size_t, _vp]),
+    "tq_quantize_polar": (ctypes.c_int, [ctypes.POINTER(tq_polar_plan), _vp, ctypes.c_int, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.POINTER(tq_records), ctypes.c_int64, _vp]),
+    "tq_decode_polar_workspace_size": (ctypes.c_int, [ctypes.POINTER(tq_polar_plan), ctypes.c_int, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]),
+    "tq_decode_attention_polar": (ctypes.c_int, [ctypes.POINTER(tq_polar_plan), _vp, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.POINTER(tq_records),
+                                                 ctypes.POINTER(tq_records), _vp, ctypes.c_int64, ctypes.c_float,
+                                                 _vp, _vp, ctypes.c_size_t, _vp]),
     "tq_fault_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -360,16 +380,92 @@ def tq_decode_split_workspace_size(plan_o, plan_r, B, Hq, Hkv, ctx_stride):
     return n.value
 
 
-def tq_decode_attention_split(plan_o, plan_r, perm, q, K_o, K_r, V_o, V_r, ctx_len, ctx_stride, Hkv, out, workspace,
-                              scale=0.0, stream=None):
-    _on_device("tq_decode_attention_split", perm, q, out, workspace)
+def tq_decode_attention_split(plan_o, plan_r, perm_k, perm_v, q, K_o, K_r, V_o, V_r, ctx_len, ctx_stride, Hkv, out,
+                              workspace, scale=0.0, stream=None):
+    _on_device("tq_decode_attention_split", perm_k, perm_v, q, out, workspace)
     _lengths("tq_decode_attention_split", ctx_len)
     _records_on_device("tq_decode_attention_split", K_o, K_r, V_o, V_r)
     B, Hq, _ = q.shape
     _check("tq_decode_attention_split", load().tq_decode_attention_split(
-        plan_o.ref, plan_r.ref, perm.data_ptr(), q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K_o.ref, K_r.ref, V_o.ref,
+        plan_o.ref, plan_r.ref, perm_k.data_ptr(), perm_v.data_ptr(), q.data_ptr(), _dtype_code(q), B, Hq, Hkv,
+        K_o.ref, K_r.ref, V_o.ref,
         V_r.ref, ctx_len.data_ptr(), ctx_stride, float(scale), out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_make_polar_codebooks(d, b1=4, b=2):
+    """Per-level (centroids, bounds) lists, float64."""
+    L = int(d).bit_length() - 1
+    c = np.empty((1 << b1) + (L - 1) * (1 << b), dtype=np.float64)
+    bd = np.empty(((1 << b1) - 1) + (L - 1) * ((1 << b) - 1), dtype=np.float64)
+    _check("tq_make_polar_codebooks", load().tq_make_polar_codebooks(d, b1, b, _dptr(c), _dptr(bd)))
+    books = [(c[:1 << b1], bd[:(1 << b1) - 1])]
+    for lev in range(L - 1):
+        o, ob = (1 << b1) + lev * (1 << b), ((1 << b1) - 1) + lev * ((1 << b) - 1)
+        books.append((c[o:o + (1 << b)], bd[ob:ob + (1 << b) - 1]))
+    return books, c, bd
+
+
+class PolarPlan:
+    """Device tables of the polar stage of one (d, m, b1, b) shape."""
+
+    def __init__(self, d, m, b1, b, rotation_seed, qjl_seed, device="cuda", stream=None):
+        import torch
+
+        self.d, self.m, self.b1, self.b = d, m, b1, b
+        self.pi = tq_make_rotation(d, rotation_seed)
+        self.S, self.s_rot = tq_make_qjl(m, d, qjl_seed, self.pi)
+        self.books, c, bd = tq_make_polar_codebooks(d, b1, b)
+        self.nw = load().tq_polar_index_words(d, b1, b)
+        nbytes = load().tq_polar_plan_bytes(d, m, b1, b)
+        if nbytes == 0 or self.nw == 0:
+            raise TQError("tq_polar_plan_bytes", TQ_ERR_ARG)
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.c = tq_polar_plan()
+        _check("tq_polar_plan_init", load().tq_polar_plan_init(
+            ctypes.byref(self.c), d, m, b1, b, _dptr(self.pi), _dptr(self.s_rot), _dptr(c), _dptr(bd),
+            self.buffer.data_ptr(), nbytes, _stream(stream)))
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+    def records(self, capacity, device="cuda"):
+        """Polar records of `capacity` rows (TQ_LAYOUT_ROWS)."""
+        import torch
+
+        idx = torch.empty(capacity, self.nw, dtype=torch.int32, device=device)
+        sgn = torch.empty(capacity, self.m // 32, dtype=torch.int32, device=device)
+        norm = torch.empty(capacity, dtype=torch.float32, device=device)
+        rnorm = torch.empty(capacity, dtype=torch.float32, device=device)
+        return Records.wrap(idx, sgn, norm, rnorm, self.d, self.m, 0)
+
+
+def tq_quantize_polar(plan, x, out, out_offset=0, stream=None):
+    _on_device("tq_quantize_polar", x)
+    _records_on_device("tq_quantize_polar", out)
+    n = x.shape[0]
+    ld = x.stride(0) if x.dim() == 2 and n > 0 else plan.d
+    _check("tq_quantize_polar", load().tq_quantize_polar(plan.ref, x.data_ptr(), _dtype_code(x), n, ld, out.ref,
+                                                         out_offset, _stream(stream)))
+
+
+def tq_decode_polar_workspace_size(plan, B, Hq, Hkv, ctx_stride):
+    n = ctypes.c_size_t(0)
+    _check("tq_decode_polar_workspace_size", load().tq_decode_polar_workspace_size(plan.ref, B, Hq, Hkv, ctx_stride,
+                                                                                   ctypes.byref(n)))
+    return n.value
+
+
+def tq_decode_attention_polar(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, workspace, scale=0.0, stream=None):
+    _on_device("tq_decode_attention_polar", q, out, workspace)
+    _lengths("tq_decode_attention_polar", ctx_len)
+    _records_on_device("tq_decode_attention_polar", K, V)
+    B, Hq, _ = q.shape
+    _check("tq_decode_attention_polar", load().tq_decode_attention_polar(
+        plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride,
+        float(scale), out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
 
 
 def tq_fault_flags(reset=True):

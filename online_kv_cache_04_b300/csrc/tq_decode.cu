@@ -458,6 +458,23 @@ tq_status tq::launch_query_prep(const tq_plan* plan, const void* q, tq_dtype qd,
   return tq::launch_status();
 }
 
+tq_status tq::launch_decode_combine(const float* part, int B, int Hq, int nsplit, int d, int m, const float* pi_t,
+                                   const float* s_rot_t, float alpha, float* out, cudaStream_t stream) {
+  CombineArgs c{};
+  c.s.B = B;
+  c.s.Hq = Hq;
+  c.s.d = d;
+  c.s.m = m;
+  c.s.nsplit = nsplit;
+  c.part = part;
+  c.pi_t = pi_t;
+  c.s_rot_t = s_rot_t;
+  c.alpha = alpha;
+  c.out = out;
+  combine_kernel<<<B * Hq, 256, sizeof(float) * (3 * d + m + nsplit), stream>>>(c);
+  return tq::launch_status();
+}
+
 extern "C" tq_status tq_decode_workspace_size(const tq_plan* plan, int B, int Hq, int Hkv, int64_t ctx_stride,
                                               size_t* bytes) {
   DecodeShape s;

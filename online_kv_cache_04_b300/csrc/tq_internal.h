@@ -49,6 +49,12 @@ inline int sm_count() {
 tq_status launch_query_prep(const tq_plan* plan, const void* q, tq_dtype qd, int nheads, float* qt, float* st,
                             cudaStream_t stream);
 
+// Log-sum-exp merge of nsplit partials [B*Hq][nsplit][2 + d + m] (reference,
+// sum, acc_rot[d], acc_sgn[m]) per query head and the output
+// o = Πᵀ(acc_rot + alpha·S̃ᵀ acc_sgn)/l (tq_decode.cu).
+tq_status launch_decode_combine(const float* part, int B, int Hq, int nsplit, int d, int m, const float* pi_t,
+                                const float* s_rot_t, float alpha, float* out, cudaStream_t stream);
+
 // Device word of fault bits set by bounded waits (tq_quantize_tc.cu).
 unsigned* fault_word();
 

@@ -3,8 +3,9 @@
 // 3.5-bit settings: the 128 channels split, the few outlier channels one bit
 // higher than the rest, the label being the average).
 //
-// A permutation `perm` of the d channels names the outlier channels
-// perm[0 .. d_o) and the regular ones perm[d_o .. d).  Each side is a complete
+// A permutation of the d channels names the outlier channels perm[0 .. d_o)
+// and the regular ones perm[d_o .. d); keys and values have their own (their
+// outlier channels differ), the query is split like the keys.  Each side is a complete
 // instance with its own plan (its rotation of dimension d_o or d - d_o, its
 // codebook, its QJL rows) and its own records, so a key's score is the sum
 // of the two estimators
@@ -415,15 +416,16 @@ extern "C" tq_status tq_decode_split_workspace_size(const tq_plan* plan_o, const
   return TQ_OK;
 }
 
-extern "C" tq_status tq_decode_attention_split(const tq_plan* plan_o, const tq_plan* plan_r, const int32_t* perm,
-                                               const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
+extern "C" tq_status tq_decode_attention_split(const tq_plan* plan_o, const tq_plan* plan_r, const int32_t* perm_k,
+                                               const int32_t* perm_v, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
                                                const tq_records* K_o, const tq_records* K_r, const tq_records* V_o,
                                                const tq_records* V_r, const int32_t* ctx_len, int64_t ctx_stride,
                                                float scale, float* out, void* workspace, size_t ws_bytes,
                                                tq_stream stream) {
   Shape2 s;
   if (!fill_shape2(plan_o, plan_r, B, Hq, Hkv, ctx_stride, &s)) return TQ_ERR_ARG;
-  if (!perm || !q || !ctx_len || !tq::aligned16(q) || (q_dtype != TQ_F32 && q_dtype != TQ_BF16)) return TQ_ERR_ARG;
+  if (!perm_k || !perm_v || !q || !ctx_len || !tq::aligned16(q) || (q_dtype != TQ_F32 && q_dtype != TQ_BF16))
+    return TQ_ERR_ARG;
   const int64_t rows = int64_t(B) * Hkv * ctx_stride;
   if (!rows_records(K_o, plan_o, rows) || !rows_records(V_o, plan_o, rows) || !rows_records(K_r, plan_r, rows) ||
       !rows_records(V_r, plan_r, rows))
@@ -432,7 +434,9 @@ extern "C" tq_status tq_decode_attention_split(const tq_plan* plan_o, const tq_p
   if (ws_bytes < sizeof(float) * ws_floats2(s)) return TQ_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int d = s.dt;
-  const Side so = side_of(plan_o, perm), sr = side_of(plan_r, perm + plan_o->d);
+  // the query is split like the keys, the output is assembled like the values
+  const Side so = side_of(plan_o, perm_k), sr = side_of(plan_r, perm_k + plan_o->d);
+  const Side vo = side_of(plan_o, perm_v), vr = side_of(plan_r, perm_v + plan_o->d);
   float* qt = static_cast<float*>(workspace);
   float* st = qt + size_t(B) * Hq * s.dt;
   float* part = st + size_t(B) * Hq * s.mt;
@@ -466,6 +470,6 @@ extern "C" tq_status tq_decode_attention_split(const tq_plan* plan_o, const tq_p
     return TQ_ERR_CUDA;
   split2_kernel<<<dim3(s.nsplit, B * Hkv), kThreads, smem, cs>>>(a);
   if ((rc = tq::launch_status()) != TQ_OK) return rc;
-  combine2_kernel<<<B * Hq, 256, sizeof(float) * (2 * s.dt + s.mt + s.nsplit), cs>>>(s, so, sr, part, d, out);
+  combine2_kernel<<<B * Hq, 256, sizeof(float) * (2 * s.dt + s.mt + s.nsplit), cs>>>(s, vo, vr, part, d, out);
   return tq::launch_status();
 }

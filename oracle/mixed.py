@@ -132,13 +132,15 @@ def bits_per_coordinate(d: int, n_o: int, bits_regular: int, with_norms: bool = 
     return bits / d
 
 
-def decode_attention_split(q, K_O, K_R, V_O, V_R, ctx_len, t: SplitTables, scale=None):
+def decode_attention_split(q, K_O, K_R, V_O, V_R, ctx_len, t: SplitTables, scale=None, t_v: SplitTables = None):
     """Softmax attention over split records.  q [B, Hq, d]; each record dict as
     in decode.reconstruct_cache ([B, Hkv, T, ...]); the cache reconstructions are
-    assembled channel by channel and then attended exactly as decode.attention."""
+    assembled channel by channel (keys with t, values with t_v, default t) and
+    then attended exactly as decode.attention."""
+    t_v = t if t_v is None else t_v
     from .decode import attention
 
-    def recon(RO, RR):
+    def recon(RO, RR, t):
         lead = RO["idx"].shape[:-1]
         n = int(np.prod(lead))
         flat = lambda R, k, last: R[k].reshape((n,) + ((last,) if last is not None else ()))
@@ -150,4 +152,4 @@ def decode_attention_split(q, K_O, K_R, V_O, V_R, ctx_len, t: SplitTables, scale
                                 rnorm64=None)
         return reconstruct_split(qO, qR, t).reshape(lead + (t.perm.shape[0],))
 
-    return attention(q, recon(K_O, K_R), recon(V_O, V_R), ctx_len, scale)
+    return attention(q, recon(K_O, K_R, t), recon(V_O, V_R, t_v), ctx_len, scale)

@@ -211,6 +211,50 @@ def bits_per_vector(d: int, b1: int = 4, b: int = 2) -> int:
     return (d // 2) * b1 + (d // 2 - 1) * b
 
 
+def index_words(d: int, b1: int = 4, b: int = 2) -> int:
+    """32-bit words of one vector's angle codes (see pack_indices)."""
+    return -(-(d // 2) * b1 // 32) + -(-(d // 2 - 1) * b // 32)
+
+
+def pack_indices(idx, d: int, b1: int = 4, b: int = 2) -> np.ndarray:
+    """Angle codes of N vectors -> [N, index_words] uint32.  The d/2 level-1
+    codes (b1 bits) come first, 32/b1 to a word, code i at bits
+    [b1·(i mod 32/b1), +b1) of word i // (32/b1) ("TurboQuant压缩效果": eight
+    4-bit numbers in one 32-bit integer); then, from the next word on, the
+    codes of levels 2, 3, ... in that order, b bits each, packed the same way."""
+    N = idx[0].shape[0]
+    out = np.zeros((N, index_words(d, b1, b)), dtype=np.uint64)
+    first = np.asarray(idx[0], dtype=np.uint64)
+    per1 = 32 // b1
+    for i in range(d // 2):
+        out[:, i // per1] |= first[:, i] << np.uint64(b1 * (i % per1))
+    rest = np.concatenate([np.asarray(a, dtype=np.uint64) for a in idx[1:]], axis=1) if len(idx) > 1 else \
+        np.zeros((N, 0), dtype=np.uint64)
+    base = -(-(d // 2) * b1 // 32)
+    per = 32 // b
+    for i in range(rest.shape[1]):
+        out[:, base + i // per] |= rest[:, i] << np.uint64(b * (i % per))
+    return out.astype(np.uint32)
+
+
+def unpack_indices(words, d: int, b1: int = 4, b: int = 2):
+    """Inverse of pack_indices: list of per-level [N, d/2^ℓ] int64 codes."""
+    w = np.asarray(words, dtype=np.uint64)
+    per1, per = 32 // b1, 32 // b
+    first = np.stack([(w[:, i // per1] >> np.uint64(b1 * (i % per1))) & np.uint64((1 << b1) - 1)
+                      for i in range(d // 2)], axis=1).astype(np.int64)
+    base = -(-(d // 2) * b1 // 32)
+    rest = np.stack([(w[:, base + i // per] >> np.uint64(b * (i % per))) & np.uint64((1 << b) - 1)
+                     for i in range(d // 2 - 1)], axis=1).astype(np.int64) if d > 2 else np.zeros((w.shape[0], 0),
+                                                                                                 dtype=np.int64)
+    out, off = [first], 0
+    for lev in range(2, levels(d) + 1):
+        n = d >> lev
+        out.append(rest[:, off:off + n])
+        off += n
+    return out
+
+
 def decode_attention_polar(q, K: PolarQuantized, V: PolarQuantized, shape, ctx_len, Pi, S, cb, scale=None):
     """Softmax attention over polar records; shape = (B, Hkv, T), rows in that order."""
     from .decode import attention

@@ -51,21 +51,24 @@ def test_quantize_split_matches_oracle(gpu_lib, bits, dtype):
 
 
 def _split_case(bits, B, Hq, Hkv, T, ctx, q_dtype, seed, own_records):
+    """Keys and values with their own outlier channels (perm_k, perm_v)."""
     wl = WORKLOADS["llama8b"]
     K = make_kv(wl, B=B, T=T, which=0)[:, :Hkv].float()
     V = make_kv(wl, B=B, T=T, which=1)[:, :Hkv].float()
     g = torch.Generator().manual_seed(seed)
     q = torch.randn(B, Hq, D, generator=g).to(q_dtype)
     t, po, pr, perm = _setup(bits, K[0, 0].numpy())
+    t_v, _, _, perm_v = _setup(bits, V[0, 0].numpy())
+    assert not np.array_equal(t.perm, t_v.perm)
     rows = B * Hkv * T
     Kf, Vf = K.reshape(rows, D).numpy(), V.reshape(rows, D).numpy()
     shape = lambda qq, dim: {"idx": qq.idx.reshape(B, Hkv, T, dim), "sgn": qq.sgn.reshape(B, Hkv, T, dim),
                              "norm": qq.norm.reshape(B, Hkv, T), "rnorm": qq.rnorm.reshape(B, Hkv, T)}
     if own_records:
         recs = []
-        for X in (Kf, Vf):
+        for X, pm in ((Kf, perm), (Vf, perm_v)):
             ro, rr = _lib.Records(rows, NO, NO, bits), _lib.Records(rows, D - NO, D - NO, bits - 1)
-            _lib.tq_quantize_split(po, pr, perm, torch.from_numpy(X).cuda(), ro, rr)
+            _lib.tq_quantize_split(po, pr, pm, torch.from_numpy(X).cuda(), ro, rr)
             recs += [ro, rr]
         torch.cuda.synchronize()
         unp = [gpu_records_to_numpy(recs[i], slice(0, rows), dim, dim, w)
@@ -77,16 +80,16 @@ def _split_case(bits, B, Hq, Hkv, T, ctx, q_dtype, seed, own_records):
         Ko_g, Kr_g, Vo_g, Vr_g = recs
     else:
         kO, kR = mixed.quantize_split(Kf, t)
-        vO, vR = mixed.quantize_split(Vf, t)
+        vO, vR = mixed.quantize_split(Vf, t_v)
         o_recs = [shape(kO, NO), shape(kR, D - NO), shape(vO, NO), shape(vR, D - NO)]
         Ko_g, Kr_g = oracle_records_to_gpu(kO, NO, NO, bits), oracle_records_to_gpu(kR, D - NO, D - NO, bits - 1)
         Vo_g, Vr_g = oracle_records_to_gpu(vO, NO, NO, bits), oracle_records_to_gpu(vR, D - NO, D - NO, bits - 1)
-    want, _ = mixed.decode_attention_split(q.float().numpy(), *o_recs, ctx, t)
+    want, _ = mixed.decode_attention_split(q.float().numpy(), *o_recs, ctx, t, t_v=t_v)
     ws = torch.empty(_lib.tq_decode_split_workspace_size(po, pr, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
     ws.fill_(0xFF)
     out = torch.full((B, Hq, D), float("nan"), device="cuda")
     ctx_t = torch.tensor(ctx, dtype=torch.int32, device="cuda")
-    _lib.tq_decode_attention_split(po, pr, perm, q.cuda(), Ko_g, Kr_g, Vo_g, Vr_g, ctx_t, T, Hkv, out, ws)
+    _lib.tq_decode_attention_split(po, pr, perm, perm_v, q.cuda(), Ko_g, Kr_g, Vo_g, Vr_g, ctx_t, T, Hkv, out, ws)
     torch.cuda.synchronize()
     return out.cpu().numpy(), want
 

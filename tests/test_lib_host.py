@@ -17,7 +17,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 
 def _declared():
     src = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:tq_status|size_t|const char\*)\s+(tq_\w+)\s*\(", src, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:tq_status|size_t|int|const char\*)\s+(tq_\w+)\s*\(", src, re.M)))
 
 
 def test_library_exports_every_declared_symbol():
@@ -202,3 +202,18 @@ def test_binding_refuses_host_tensors_before_any_call():
     with pytest.raises(ValueError, match="CUDA"):
         _lib.tq_search_topk(None, x, rec, 64, 10, torch.zeros(4, 10, dtype=torch.int32), torch.zeros(4, 10),
                             torch.zeros(16, dtype=torch.uint8))
+
+
+@pytest.mark.parametrize("d", [4, 16, 128, 256])
+def test_polar_codebooks_match_oracle(d):
+    """The library's angle codebooks (uniform level 1, Lloyd-Max of sin^(k-1)(2ψ) later) against the oracle's."""
+    from oracle import polar
+
+    books, _, _ = _lib.tq_make_polar_codebooks(d)
+    want = polar.make_codebooks(d)
+    assert len(books) == len(want.books) == polar.levels(d)
+    for (c, b), (wc, wb) in zip(books, want.books):
+        assert np.allclose(c, wc, rtol=0, atol=1e-11)
+        assert np.allclose(b, wb, rtol=0, atol=1e-11)
+    assert _lib.load().tq_polar_index_words(d, 4, 2) == polar.index_words(d)
+    assert _lib.load().tq_polar_index_words(96, 4, 2) == 0  # not a power of two

@@ -124,3 +124,19 @@ def test_polar_plus_qjl_score_is_unbiased_over_qjl_draws():
         est[i] = float(polar.reconstruct(q, Pi, S, cb)[0] @ qv)
     se = est.std(ddof=1) / math.sqrt(len(est))
     assert abs(est.mean() - float(x[0] @ qv)) < 3 * se
+
+
+def test_index_packing_hand_pattern_and_round_trip():
+    """d = 8, b1 = 4, b = 2: level-1 codes 1, 2, 3, 4 -> word 0 = 0x4321; level 2
+    codes 3, 0 and level 3 code 2 -> word 1 = 3 | 0 << 2 | 2 << 4."""
+    idx = [np.array([[1, 2, 3, 4]]), np.array([[3, 0]]), np.array([[2]])]
+    w = polar.pack_indices(idx, 8)
+    assert w.shape == (1, polar.index_words(8)) == (1, 2)
+    assert int(w[0, 0]) == 0x4321 and int(w[0, 1]) == 3 | (2 << 4)
+    rng = np.random.default_rng(5)
+    for d in (4, 16, 128, 256):
+        lv = [rng.integers(0, 16, size=(7, d // 2))] + [rng.integers(0, 4, size=(7, d >> l))
+                                                         for l in range(2, polar.levels(d) + 1)]
+        back = polar.unpack_indices(polar.pack_indices(lv, d), d)
+        assert all(np.array_equal(a, b) for a, b in zip(lv, back))
+    assert polar.index_words(128) == 8 + 4
