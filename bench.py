@@ -54,6 +54,7 @@ def parse():
                     help="time tq_append_kv (one new key and value per batch row and kv head, into full caches) "
                          "followed by tq_decode_attention on --workload / --batch")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (0: keep)")
+    ap.add_argument("--oracle-rate", type=float, default=0.0, help=argparse.SUPPRESS)  # child of the CPU baseline
     return ap.parse_args()
 
 
@@ -197,13 +198,43 @@ def oracle_step(wl, w, heads, T):
 
 
 def cpu_cores():
+    """(BLAS threads of this process, host CPUs).  Without threadpoolctl the pool
+    size is the one the environment sets, else OpenBLAS's default: every CPU this
+    process may run on."""
+    avail = len(os.sched_getaffinity(0))
     try:
         from threadpoolctl import threadpool_info
 
         blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
     except Exception:
-        blas = 1
+        env = [os.environ.get(v) for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")]
+        blas = next((int(e) for e in env if e and e.isdigit()), avail)
     return blas, os.cpu_count()
+
+
+def oracle_rate(wl, w, budget):
+    """KV tokens/s of the oracle (oracle_sample runs repeated for about budget s)."""
+    run, tokens, Ts = oracle_sample(wl, w, 3.0)
+    run()
+    n, t0 = 0, time.perf_counter()
+    while n < 3 or time.perf_counter() - t0 < budget:
+        run()
+        n += 1
+    return tokens / ((time.perf_counter() - t0) / n), n, Ts
+
+
+def oracle_rate_in_child(args, threads, budget):
+    """oracle_rate in a fresh process whose BLAS pool has `threads` threads (set
+    through the environment before numpy loads); returns (value, runs, T, threads)."""
+    env = dict(os.environ)
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""  # the oracle runs on the host alone
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-rate", str(budget),
+                          "--workload", args.workload, "--bits", str(args.bits)],
+                         env=env, capture_output=True, text=True, check=True)
+    r = json.loads(out.stdout.strip().splitlines()[-1])
+    return r["value"], r["runs"], r["T"], r["threads"]
 
 
 def oracle_sample(wl, w, budget_s):
@@ -429,7 +460,130 @@ def config_sweep(_lib, stream, flush, peak):
                                   "decode_gbs": 2 * nvec * rb / ms_d / 1e6, "l2": "flushed before every call"}
     del K, V, Kr, Vr, ws
     torch.cuda.empty_cache()
+    out["llama8b_b4"] = llama_step_at(_lib, stream, flush, peak, 4)
+    out["split_2p5bit_llama8b"] = split_config(_lib, stream, flush)
+    out["polar_llama8b"] = polar_config(_lib, stream, flush)
     return out
+
+
+def llama_step_at(_lib, stream, flush, peak, bits):
+    """The Llama-3.1-8B-shaped layer at another bit width: paired quantize and decode, each alone."""
+    import torch
+
+    from online_kv_cache_04_b300.workloads import QJL_SEED, ROTATION_SEED, WORKLOADS, make_kv, make_queries
+
+    wl = WORKLOADS["llama8b"]
+    d, m, w = wl.d, wl.m, bits - 1
+    B, Hq, Hkv, T = wl.B, wl.Hq, wl.Hkv, wl.ctx
+    nvec = B * Hkv * T
+    plan = _lib.Plan(d, m, w, ROTATION_SEED, QJL_SEED)
+    K = make_kv(wl, which=0, device="cuda").reshape(nvec, d)
+    V = make_kv(wl, which=1, device="cuda").reshape(nvec, d)
+    Kr = _lib.Records(nvec, d, m, w)
+    Vr = _lib.Records(nvec, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    fq = lambda: _lib.tq_quantize_pair(plan, K, V, Kr, Vr)
+    fq()
+    ms_q = timed(stream, fq, 50, flush)
+    q = make_queries(wl, device="cuda")
+    ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    o = torch.empty(B, Hq, d, device="cuda")
+    ws = torch.empty(_lib.tq_decode_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+    fd = lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, o, ws)
+    fd()
+    ms_d = timed(stream, fd, 50, flush)
+    rb = rec_bytes(d, m, w)
+    qb = 2 * nvec * (d * K.element_size() + rb)
+    db = 2 * nvec * rb + q.numel() * q.element_size() + o.numel() * 4
+    res = {"workload": f"Llama-3.1-8B-shaped layer (B=1, 32/8 heads, ctx 32768), b={bits}",
+           "quantize_ms_per_call": ms_q, "quantize_gbs": qb / ms_q / 1e6, "quantize_frac_of_measured_hbm":
+           qb / ms_q / 1e6 / peak, "decode_ms_per_call": ms_d, "decode_gbs": db / ms_d / 1e6,
+           "decode_frac_of_8tbs": db / ms_d / 1e6 / NOMINAL_HBM_GBS, "decode_kv_tokens_per_s": B * T / ms_d * 1e3,
+           "l2": "flushed before every call"}
+    del K, V, Kr, Vr, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def split_config(_lib, stream, flush):
+    """Outlier-channel split at 2.5 bits per coordinate on the Llama-3.1-8B-shaped layer: the 64
+    channels of largest mean square over the layer's keys (values) at 3 bits, the rest at 2."""
+    import numpy as np
+    import torch
+
+    from online_kv_cache_04_b300.workloads import SPLIT_SEEDS, WORKLOADS, make_kv, make_queries
+
+    wl = WORKLOADS["llama8b"]
+    d, no, bits = wl.d, 64, 2
+    B, Hq, Hkv, T = wl.B, wl.Hq, wl.Hkv, wl.ctx
+    nvec = B * Hkv * T
+    (ro, qo), (rr, qr) = SPLIT_SEEDS["outlier"], SPLIT_SEEDS["regular"]
+    po, pr = _lib.Plan(no, no, bits, ro, qo), _lib.Plan(d - no, d - no, bits - 1, rr, qr)
+    K = make_kv(wl, which=0, device="cuda").reshape(nvec, d)
+    V = make_kv(wl, which=1, device="cuda").reshape(nvec, d)
+
+    def perm_of(X):  # channels by mean square over a sample, largest first (ties to the lower channel)
+        ms2 = (X[::64].float() ** 2).mean(dim=0).cpu().numpy()
+        order = sorted(range(d), key=lambda j: (-ms2[j], j))
+        p = np.concatenate([np.sort(order[:no]), np.sort(order[no:])]).astype(np.int32)
+        return torch.from_numpy(p).cuda()
+
+    pk, pv = perm_of(K), perm_of(V)
+    Ko, Kr = _lib.Records(nvec, no, no, bits), _lib.Records(nvec, d - no, d - no, bits - 1)
+    Vo, Vr = _lib.Records(nvec, no, no, bits), _lib.Records(nvec, d - no, d - no, bits - 1)
+    fq = lambda: (_lib.tq_quantize_split(po, pr, pk, K, Ko, Kr), _lib.tq_quantize_split(po, pr, pv, V, Vo, Vr))
+    fq()
+    ms_q = timed(stream, fq, 10, flush)
+    q = make_queries(wl, device="cuda")
+    ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    o = torch.empty(B, Hq, d, device="cuda")
+    ws = torch.empty(_lib.tq_decode_split_workspace_size(po, pr, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+    fd = lambda: _lib.tq_decode_attention_split(po, pr, pk, pv, q, Ko, Kr, Vo, Vr, ctx, T, Hkv, o, ws)
+    fd()
+    ms_d = timed(stream, fd, 20, flush)
+    rec = (no * bits + no) // 8 + 8 + ((d - no) * (bits - 1) + (d - no)) // 8 + 8
+    res = {"workload": "Llama-3.1-8B-shaped layer, 64 of 128 channels at 3 bits, the rest at 2 (2.5 bit/coord), "
+                       "keys and values with their own outlier channels, general kernels",
+           "record_bytes_per_vector": rec, "quantize_ms_per_call": ms_q, "quantize_mvec_per_s": 2 * nvec / ms_q / 1e3,
+           "decode_ms_per_call": ms_d, "decode_kv_tokens_per_s": B * T / ms_d * 1e3,
+           "decode_gbs": 2 * nvec * rec / ms_d / 1e6, "l2": "flushed before every call"}
+    del K, V, Ko, Kr, Vo, Vr, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def polar_config(_lib, stream, flush):
+    """PolarQuant stage (+ QJL) on the Llama-3.1-8B-shaped layer: 4-bit first level, 2-bit later levels."""
+    import torch
+
+    from online_kv_cache_04_b300.workloads import POLAR_SEEDS, WORKLOADS, make_kv, make_queries
+
+    wl = WORKLOADS["llama8b"]
+    d = wl.d
+    B, Hq, Hkv, T = wl.B, wl.Hq, wl.Hkv, wl.ctx
+    nvec = B * Hkv * T
+    plan = _lib.PolarPlan(d, d, 4, 2, *POLAR_SEEDS)
+    K = make_kv(wl, which=0, device="cuda").reshape(nvec, d)
+    V = make_kv(wl, which=1, device="cuda").reshape(nvec, d)
+    Kr, Vr = plan.records(nvec), plan.records(nvec)
+    fq = lambda: (_lib.tq_quantize_polar(plan, K, Kr), _lib.tq_quantize_polar(plan, V, Vr))
+    fq()
+    ms_q = timed(stream, fq, 10, flush)
+    q = make_queries(wl, device="cuda")
+    ctx = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    o = torch.empty(B, Hq, d, device="cuda")
+    ws = torch.empty(_lib.tq_decode_polar_workspace_size(plan, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+    fd = lambda: _lib.tq_decode_attention_polar(plan, q, Kr, Vr, ctx, T, Hkv, o, ws)
+    fd()
+    ms_d = timed(stream, fd, 20, flush)
+    rec = 4 * plan.nw + d // 8 + 8
+    res = {"workload": "Llama-3.1-8B-shaped layer, polar stage (4-bit level 1, 2-bit later levels) + QJL, "
+                       "general kernels", "record_bytes_per_vector": rec,
+           "quantize_ms_per_call": ms_q, "quantize_mvec_per_s": 2 * nvec / ms_q / 1e3,
+           "decode_ms_per_call": ms_d, "decode_kv_tokens_per_s": B * T / ms_d * 1e3,
+           "decode_gbs": 2 * nvec * rec / ms_d / 1e6, "l2": "flushed before every call"}
+    del K, V, Kr, Vr, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_generic(args):
@@ -556,6 +710,12 @@ def run_append_step(args, _lib, plan, wl, Kr, Vr, q, stream, flush):
 
 def main():
     args = parse()
+    if args.oracle_rate > 0:
+        from online_kv_cache_04_b300.workloads import WORKLOADS
+
+        value, runs, T = oracle_rate(WORKLOADS[args.workload], args.bits - 1, args.oracle_rate)
+        print(json.dumps({"value": value, "runs": runs, "T": T, "threads": cpu_cores()[0]}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -612,7 +772,9 @@ def main():
     torch.cuda.synchronize()
     # decode alone with a cold L2 (inside the step it reads records that quantize just
     # wrote); taken before the clock sampler starts, apart from the timed steps
-    t_dec = timed(stream, lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws), 50, flush) / 1e3
+    t_dec, clk_cold = sampled(local, lambda: timed(
+        stream, lambda: _lib.tq_decode_attention(plan, q, Kr, Vr, ctx, T, Hkv, out, ws), 50, flush))
+    t_dec /= 1e3
 
     sampler = ClockSampler(local)
     sampler.wait_first()
@@ -660,9 +822,39 @@ def main():
     t_e2e = e0.elapsed_time(e1) / n_e2e / 1e3
     h2d = (Kh.numel() + Vh.numel()) * Kh.element_size() + qh.numel() * qh.element_size()
     d2h = outh.numel() * outh.element_size()
+
+    # ---- end to end, a decode loop: the step's query and new key and value in,
+    # appended to the compressed cache (at token T - 1), attention over it, output out
+    kn_h = make_kv(wl, T=1, which=0)[:, :, 0].contiguous().pin_memory()  # [B, Hkv, d]
+    vn_h = make_kv(wl, T=1, which=1)[:, :, 0].contiguous().pin_memory()
+    kn_d, vn_d = torch.empty_like(kn_h, device="cuda"), torch.empty_like(vn_h, device="cuda")
+
+    def loop_step():
+        qd.copy_(qh, non_blocking=True)
+        kn_d.copy_(kn_h, non_blocking=True)
+        vn_d.copy_(vn_h, non_blocking=True)
+        ctx.fill_(T - 1)  # the same cache position every step: a fixed-size benchmark cache
+        _lib.tq_append_kv(plan, kn_d, vn_d, Kr, Vr, ctx, T)
+        _lib.tq_decode_attention(plan, qd, Kr, Vr, ctx, T, Hkv, out, ws)
+        outh.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        loop_step()
+    torch.cuda.synchronize()
+    n_loop = max(10, min(args.steps, 200))
+    torch.cuda._sleep(200_000_000)
+    e0.record(stream)
+    for _ in range(n_loop):
+        loop_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_loop = e0.elapsed_time(e1) / n_loop / 1e3
+    h2d_loop = (qh.numel() * qh.element_size() + kn_h.numel() * kn_h.element_size()
+                + vn_h.numel() * vn_h.element_size())
+    ctx.fill_(T)
     # the job is as slow as its slowest replica (every rank joins the reduction)
-    t_step, t_quant, t_dec_step, t_dec, t_e2e = max_over_ranks([t_step, t_quant, t_dec_step, t_dec, t_e2e], world,
-                                                               "cuda")
+    t_step, t_quant, t_dec_step, t_dec, t_e2e, t_loop = max_over_ranks(
+        [t_step, t_quant, t_dec_step, t_dec, t_e2e, t_loop], world, "cuda")
 
     if rank != 0:
         if world > 1:
@@ -699,27 +891,34 @@ def main():
         "decode_frac_of_8tbs": dec_bytes / t_dec / 1e9 / NOMINAL_HBM_GBS,
         "quantize_mvec_per_s": 2 * nvec / t_quant / 1e6,
         "e2e": {"value": job_throughput(B * T, world, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "step": "pinned host K and V caches (bf16) and queries in, quantize + decode, output out"},
+        "e2e_decode_loop": {"value": job_throughput(B * T, world, t_loop), "unit": UNIT,
+                            "ms_per_step": t_loop * 1e3, "h2d_bytes_per_step": h2d_loop,
+                            "d2h_bytes_per_step": d2h,
+                            "step": ("pinned host query and the step's new key and value (bf16) in, "
+                                     "tq_append_kv into the compressed cache, decode over its "
+                                     f"{T} tokens, output out")},
         "gpu_launches": 3 * args.steps,
         "fault_flags": fault,
         "clocks": clocks,
+        "clocks_regions": {"cold_decode": clk_cold},
     }
     if world == 1 and not args.no_sweep:
-        line["decode_longctx"] = decode_sweep(_lib, {}, stream, flush, (2, 3, 4))
-        line["configs"] = config_sweep(_lib, stream, flush, peak)
+        line["decode_longctx"], line["clocks_regions"]["decode_longctx"] = sampled(
+            local, lambda: decode_sweep(_lib, {}, stream, flush, (2, 3, 4)))
+        line["configs"], line["clocks_regions"]["configs"] = sampled(
+            local, lambda: config_sweep(_lib, stream, flush, peak))
     if world == 1 and not args.no_cpu_baseline:
-        run, tokens, Ts = oracle_sample(wl, w, 3.0)
-        run()
-        n, t0 = 0, time.perf_counter()
-        while n < 3 or time.perf_counter() - t0 < 10.0:
-            run()
-            n += 1
-        dt = (time.perf_counter() - t0) / n
-        threads, cores = cpu_cores()
-        line["cpu_baseline"] = {"value": tokens / dt, "unit": UNIT, "cores": threads, "host_cpus": cores,
-                                "kind": "oracle",
-                                "sample": (f"1 of {Hkv} kv heads x first {Ts} of {T} tokens (batch row 0), "
-                                           f"{n} runs, scaled to the layer's KV tokens")}
+        cores = os.cpu_count()
+        v_all, n_all, Ts, threads = oracle_rate_in_child(args, len(os.sched_getaffinity(0)), 10.0)
+        v_one, n_one, Ts1, _ = oracle_rate_in_child(args, 1, 10.0)
+        sample = lambda n, t: (f"1 of {Hkv} kv heads x first {t} of {T} tokens (batch row 0), {n} runs, "
+                               f"scaled to the layer's KV tokens")
+        line["cpu_baseline"] = {"value": v_all, "unit": UNIT, "cores": threads, "host_cpus": cores, "kind": "oracle",
+                                "sample": sample(n_all, Ts)}
+        line["cpu_baseline_1core"] = {"value": v_one, "unit": UNIT, "cores": 1, "host_cpus": cores,
+                                      "kind": "oracle", "sample": sample(n_one, Ts1)}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -246,6 +246,28 @@ tq_status tq_decode_attention_noalloc(const tq_plan* plan, const void* q, tq_dty
                                       const tq_records* K, const tq_records* V, const int32_t* ctx_len,
                                       int64_t ctx_stride, float scale, float* out, tq_stream stream);
 
+/* Paged caches (a decode loop whose sequences grow by pages instead of each
+ * owning one contiguous stretch of ctx_stride rows; "谷歌TurboQuant如何绕过
+ * 内存墙？" §2: the quantizer is online, one vector at a time).  Token t of
+ * (batch row b, kv head h) lives at record row pages[(b*Hkv + h)*max_pages +
+ * t/256]*256 + t%256: a page is 256 consecutive rows (eight 32-row blocks of
+ * TQ_LAYOUT_BLOCK32) starting at a multiple of 256, and each sequence holds
+ * up to max_pages of them, in any order.  pages: device int32
+ * [B*Hkv][max_pages], 16-byte aligned; an entry must lie in
+ * [0, capacity/256) of both caches -- an entry outside is read as page 0 and
+ * sets fault bit 4 (the outputs of that call are then undefined).
+ * Decode: as tq_decode_attention with ctx_stride = 256*max_pages (workspace
+ * from tq_decode_workspace_size with that ctx_stride); results equal those of
+ * the contiguous call on the same tokens.  Append: as tq_append_kv, the new
+ * token at position ctx_len[b] of its sequence. */
+tq_status tq_decode_attention_paged(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
+                                    const tq_records* K, const tq_records* V, const int32_t* ctx_len,
+                                    const int32_t* pages, int max_pages, float scale, float* out, void* workspace,
+                                    size_t ws_bytes, tq_stream stream);
+tq_status tq_append_kv_paged(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B,
+                             int Hkv, const tq_records* K, const tq_records* V, int32_t* ctx_len,
+                             const int32_t* pages, int max_pages, tq_stream stream);
+
 /* Attention logits alone (the quantity the H100 timings of [efficiency] §四
  * and [memory-wall] §2 measure): scores[b][g][t] = s_{g,t} as above for
  * t < ctx_len[b]; entries t >= ctx_len[b] are left untouched.
@@ -385,7 +407,8 @@ tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype q_dtype, i
  * (bit 0: a tensor-core quantize wait ran out of its bound, a few seconds;
  * bit 1: a tensor-core decode wait; bit 2: a tensor-core search wait; the
  * outputs of that launch are then undefined.  Bit 3: tq_append_kv met a
- * full cache or a negative length and skipped that batch row).  Kernels
+ * full cache or a negative length and skipped that batch row; bit 4: a
+ * page-table entry outside the record arrays).  Kernels
  * never spin forever: they set the bit and finish.  Copies the word to *flags (synchronous) and clears it
  * when reset != 0.  Errors: TQ_ERR_ARG (NULL), TQ_ERR_CUDA. */
 tq_status tq_fault_flags(uint32_t* flags, int reset);

@@ -98,6 +98,13 @@ _SIGNATURES = {
                                                  ctypes.c_int, ctypes.c_int, ctypes.POINTER(tq_records),
                                                  ctypes.POINTER(tq_records), _vp, ctypes.c_int64, ctypes.c_float,
                                                  _vp, _vp, ctypes.c_size_t, _vp]),
+    "tq_decode_attention_paged": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.POINTER(tq_records),
+                                                 ctypes.POINTER(tq_records), _vp, _vp, ctypes.c_int, ctypes.c_float,
+                                                 _vp, _vp, ctypes.c_size_t, _vp]),
+    "tq_append_kv_paged": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, _vp, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), _vp,
+                                          _vp, ctypes.c_int, _vp]),
     "tq_fault_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -331,6 +338,33 @@ def tq_decode_attention_noalloc(plan, q, K, V, ctx_len, ctx_stride, Hkv, out, sc
     _check("tq_decode_attention_noalloc", load().tq_decode_attention_noalloc(
         plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), ctx_stride,
         float(scale), out.data_ptr(), _stream(stream)))
+
+
+def tq_decode_attention_paged(plan, q, K, V, ctx_len, pages, Hkv, out, workspace, scale=0.0, stream=None):
+    """Decode over paged caches: pages [B*Hkv, max_pages] int32 (device), 256 tokens per page."""
+    _on_device("tq_decode_attention_paged", q, out, workspace, pages)
+    _lengths("tq_decode_attention_paged", ctx_len)
+    _records_on_device("tq_decode_attention_paged", K, V)
+    B, Hq, _ = q.shape
+    _check("tq_decode_attention_paged", load().tq_decode_attention_paged(
+        plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), pages.data_ptr(),
+        pages.shape[-1], float(scale), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_append_kv_paged(plan, k_new, v_new, K, V, ctx_len, pages, stream=None):
+    """tq_append_kv into paged caches (pages [B*Hkv, max_pages] int32, device)."""
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype or k_new.dim() != 3:
+        raise ValueError("tq_append_kv_paged: k_new and v_new must both be [B, Hkv, d] of one dtype")
+    if not (k_new.is_contiguous() and v_new.is_contiguous() and pages.is_contiguous()):
+        raise ValueError("tq_append_kv_paged: k_new, v_new and pages must be contiguous")
+    _on_device("tq_append_kv_paged", k_new, v_new, pages)
+    _lengths("tq_append_kv_paged", ctx_len)
+    _records_on_device("tq_append_kv_paged", K, V)
+    B, Hkv, _ = k_new.shape
+    _check("tq_append_kv_paged", load().tq_append_kv_paged(
+        plan.ref, k_new.data_ptr(), v_new.data_ptr(), _dtype_code(k_new), B, Hkv, K.ref, V.ref, ctx_len.data_ptr(),
+        pages.data_ptr(), pages.shape[-1], _stream(stream)))
 
 
 def tq_decode_scores(plan, q, K, ctx_len, ctx_stride, Hkv, scores, workspace, scale=0.0, stream=None):

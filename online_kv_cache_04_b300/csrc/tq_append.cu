@@ -21,6 +21,8 @@
 // with a negative length are left alone and raise fault bit kFaultAppend.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "tq_internal.h"
 
 namespace {
@@ -42,7 +44,12 @@ struct AppendArgs {
   const float* centroids;
   const float* bounds;
   unsigned* fault;
+  const int32_t* pages;    // paged caches: [B*Hkv][ctx_stride / 256] (NULL: contiguous rows)
+  int64_t npages;          // pages the record arrays hold
 };
+
+constexpr int kPage = 256;             // tokens per page of a paged cache
+constexpr unsigned kFaultPage = 16u;   // a page-table entry outside the record arrays
 
 template <typename T>
 __device__ __forceinline__ float load_elem(const T* p);
@@ -113,7 +120,15 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   float* const rnrm = which ? a.rec[1].norm : a.rec[0].norm;
   float* const rrn = which ? a.rec[1].rnorm : a.rec[0].rnorm;
   const bool rows = (which ? a.rec[1].layout : a.rec[0].layout) == TQ_LAYOUT_ROWS;
-  const int64_t row = (int64_t)unit * a.ctx_stride + t;
+  int64_t row = (int64_t)unit * a.ctx_stride + t;
+  if (a.pages != nullptr) {  // the page holding token t
+    const int64_t pg = a.pages[(int64_t)unit * (a.ctx_stride / kPage) + t / kPage];
+    if (pg < 0 || pg >= a.npages) {
+      if (tid == 0) atomicOr(a.fault, kFaultPage);
+      return;
+    }
+    row = pg * kPage + t % kPage;
+  }
   const T* x = static_cast<const T*>(which ? a.x[1] : a.x[0]) + (size_t)unit * d;
   if (tid < L) cent[tid] = a.centroids[tid];
   if (tid < L - 1) bnd[tid] = a.bounds[tid];
@@ -192,9 +207,11 @@ __global__ void advance_kernel(int32_t* ctx_len, int B, int64_t ctx_stride) {
 
 }  // namespace
 
-extern "C" tq_status tq_append_kv(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B,
-                                  int Hkv, const tq_records* K, const tq_records* V, int32_t* ctx_len,
-                                  int64_t ctx_stride, tq_stream stream) {
+namespace {
+
+tq_status append_impl(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B, int Hkv,
+                      const tq_records* K, const tq_records* V, int32_t* ctx_len, int64_t ctx_stride,
+                      tq_stream stream, const int32_t* pages) {
   if (!tq::valid_plan(plan) || !tq::valid_records(K, plan) || !tq::valid_records(V, plan) || !k_new || !v_new ||
       !tq::aligned16(k_new) || !tq::aligned16(v_new) || !ctx_len || B < 1 || Hkv < 1 || ctx_stride < 1 ||
       ctx_stride > INT32_MAX || (dtype != TQ_F32 && dtype != TQ_BF16))
@@ -202,13 +219,16 @@ extern "C" tq_status tq_append_kv(const tq_plan* plan, const void* k_new, const 
   // keys and values of one step land on the same rows: one cache for both would race
   if (K->idx == V->idx || (K->sgn && K->sgn == V->sgn) || K->norm == V->norm) return TQ_ERR_ARG;
   const int64_t units = (int64_t)B * Hkv;
-  if (units > INT32_MAX || units * ctx_stride > K->capacity || units * ctx_stride > V->capacity) return TQ_ERR_ARG;
+  if (units > INT32_MAX) return TQ_ERR_ARG;
+  if (pages == nullptr && (units * ctx_stride > K->capacity || units * ctx_stride > V->capacity)) return TQ_ERR_ARG;
+  if (pages != nullptr && (K->capacity < kPage || V->capacity < kPage)) return TQ_ERR_ARG;
   // a block-layout cache keeps whole 32-row blocks per (batch row, kv head)
   if ((K->layout == TQ_LAYOUT_BLOCK32 || V->layout == TQ_LAYOUT_BLOCK32) && ctx_stride % 32 != 0) return TQ_ERR_ARG;
   unsigned* fault = tq::fault_word();
   if (!fault) return TQ_ERR_CUDA;
   AppendArgs a{{k_new, v_new}, {*K, *V}, ctx_len, ctx_stride, Hkv, plan->d, plan->m, plan->w, plan->pi_t,
-               plan->s_rot_t, plan->centroids, plan->bounds, fault};
+               plan->s_rot_t, plan->centroids, plan->bounds, fault, pages,
+               std::min(K->capacity, V->capacity) / kPage};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid((unsigned)units, 2);
   if (dtype == TQ_F32)
@@ -219,4 +239,19 @@ extern "C" tq_status tq_append_kv(const tq_plan* plan, const void* k_new, const 
   if (s != TQ_OK) return s;
   advance_kernel<<<1, 256, 0, cs>>>(ctx_len, B, ctx_stride);
   return tq::launch_status();
+}
+
+}  // namespace
+
+extern "C" tq_status tq_append_kv(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B,
+                                  int Hkv, const tq_records* K, const tq_records* V, int32_t* ctx_len,
+                                  int64_t ctx_stride, tq_stream stream) {
+  return append_impl(plan, k_new, v_new, dtype, B, Hkv, K, V, ctx_len, ctx_stride, stream, nullptr);
+}
+
+extern "C" tq_status tq_append_kv_paged(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype,
+                                        int B, int Hkv, const tq_records* K, const tq_records* V, int32_t* ctx_len,
+                                        const int32_t* pages, int max_pages, tq_stream stream) {
+  if (pages == nullptr || !tq::aligned16(pages) || max_pages < 1) return TQ_ERR_ARG;
+  return append_impl(plan, k_new, v_new, dtype, B, Hkv, K, V, ctx_len, int64_t(max_pages) * kPage, stream, pages);
 }

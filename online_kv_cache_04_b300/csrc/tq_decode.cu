@@ -46,7 +46,7 @@ int choose_splits(int B, int Hkv, int64_t ctx_stride) {
 
 // Partial slots per head of the tensor-core path (0 when it cannot apply).
 int tc_slots(const DecodeShape& s) {
-  if (s.d != 128 || s.m != 128 || s.G > kMaxG || s.ctx_stride % 128 != 0) return 0;
+  if (s.d != 128 || (s.m != 128 && s.m != 0) || s.G > kMaxG || s.ctx_stride % 128 != 0) return 0;
   const int64_t units = int64_t(s.B) * s.Hkv, tpu = tq::decode_tc_tpu(s.ctx_stride);
   return tq::decode_tc_slots(units, tpu, tq::decode_tc_ctas(units, tpu));
 }
@@ -61,8 +61,8 @@ TcLayout tc_layout(const DecodeShape& s) {
   const size_t units = size_t(s.B) * s.Hkv, heads = size_t(s.B) * s.Hq;
   TcLayout l;
   l.tables = up(units * sizeof(unsigned));
-  l.part = up(l.tables + units * tq::decode_tc_table_bytes(s.w, s.G));
-  l.bytes = l.part + sizeof(float) * heads * tc_slots(s) * (2 + s.d + s.m);
+  l.part = up(l.tables + units * tq::decode_tc_table_bytes(s.w, s.G, s.m));
+  l.bytes = l.part + sizeof(float) * heads * tc_slots(s) * (2 + 2 * s.d);  // reference, sum, acc_rot, acc_sgn
   return l;
 }
 
@@ -160,7 +160,25 @@ struct SplitArgs {
   float scale, alpha;
   float* part;                         // [B*Hq][nsplit][2 + d + m]
   float* scores;                       // scores-only mode: [B*Hq][ctx_stride]
+  const int32_t* pages;                // paged caches: [B*Hkv][max_pages] (NULL: contiguous rows)
+  int64_t max_pages, npages;           // pages per unit; pages the record arrays hold
+  unsigned* fault;
 };
+
+constexpr int kPage = 256;             // tokens per page of a paged cache
+constexpr unsigned kFaultPage = 16u;   // a page-table entry outside the record arrays
+
+// Record row of token t of unit bh: contiguous units, or through the page table
+// (an entry outside the record arrays reads page 0 and raises kFaultPage).
+__device__ __forceinline__ int64_t row_of(const SplitArgs& a, int64_t bh, int64_t t) {
+  if (a.pages == nullptr) return bh * a.s.ctx_stride + t;
+  int64_t pg = __ldg(a.pages + bh * a.max_pages + t / kPage);
+  if (pg < 0 || pg >= a.npages) {
+    atomicOr(a.fault, kFaultPage);
+    pg = 0;
+  }
+  return pg * kPage + t % kPage;
+}
 
 // score of one token for all G heads (thread-private record in registers)
 __device__ __forceinline__ void score_token(const SplitArgs& a, int64_t row, const float* qts, const float* sts,
@@ -226,7 +244,6 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
   if (tid < kMaxG) runm[tid] = -INFINITY;
   __syncthreads();
 
-  const int64_t rowbase = (int64_t)bh * s.ctx_stride;
   float acc_r[2][kMaxG], acc_s[2][kMaxG], lsum[kMaxG];
 #pragma unroll
   for (int k = 0; k < 2; ++k)
@@ -242,7 +259,8 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
     float sc[kMaxG];
 #pragma unroll
     for (int g = 0; g < kMaxG; ++g) sc[g] = -INFINITY;
-    if (valid) score_token(a, rowbase + t, qts, sts, cent, G, sc);
+    const int64_t row = valid ? row_of(a, bh, t) : 0;
+    if (valid) score_token(a, row, qts, sts, cent, G, sc);
     if constexpr (kScoresOnly) {
       if (valid)
         for (int g = 0; g < G; ++g) a.scores[(size_t)(head0 + g) * s.ctx_stride + t] = sc[g];
@@ -262,14 +280,14 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
       // index words then sign words, one coordinate per word.
       if (a.v_layout == TQ_LAYOUT_ROWS) {
         if (valid) {
-          const uint32_t* ip = a.vidx + (rowbase + t) * wi;
-          const uint32_t* sp = a.vsgn + (rowbase + t) * ws;
+          const uint32_t* ip = a.vidx + row * wi;
+          const uint32_t* sp = a.vsgn + row * ws;
           for (int k = 0; k < wi; ++k) vw[tid * wr + k] = __ldg(ip + k);
           for (int k = 0; k < ws; ++k) vw[tid * wr + wi + k] = __ldg(sp + k);
         }
       } else {
         const int nb = (cnt + 31) >> 5, bw = w * d + m;
-        const int64_t blk = (rowbase + c0) >> 5;
+        const int64_t blk = row_of(a, bh, c0) >> 5;  // a chunk never straddles a page
         for (int e = tid; e < nb * bw; e += kThreads) {
           const int kb = e / bw, o = e - kb * bw;
           vw[e] = o < w * d ? __ldg(a.vidx + (blk + kb) * (int64_t)(w * d) + o)
@@ -284,8 +302,8 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a) {
         runm[tid] = nm;
       }
       __syncthreads();
-      const float nv = valid ? __ldg(a.vnorm + rowbase + t) : 0.0f;
-      const float rv = valid && m > 0 ? __ldg(a.vrnorm + rowbase + t) : 0.0f;
+      const float nv = valid ? __ldg(a.vnorm + row) : 0.0f;
+      const float rv = valid && m > 0 ? __ldg(a.vrnorm + row) : 0.0f;
       for (int g = 0; g < G; ++g) {
         const float p = valid ? exp2f(sc[g] - runm[g]) : 0.0f;
         pn[g * kThreads + tid] = p * nv;
@@ -483,15 +501,25 @@ extern "C" tq_status tq_decode_workspace_size(const tq_plan* plan, int B, int Hq
   return TQ_OK;
 }
 
-extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
-                                         const tq_records* K, const tq_records* V, const int32_t* ctx_len,
-                                         int64_t ctx_stride, float scale, float* out, void* workspace,
-                                         size_t ws_bytes, tq_stream stream) {
+namespace {
+
+tq_status decode_impl(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
+                      const tq_records* K, const tq_records* V, const int32_t* ctx_len, int64_t ctx_stride,
+                      float scale, float* out, void* workspace, size_t ws_bytes, tq_stream stream,
+                      const int32_t* pages) {
   DecodeShape s;
   if (!fill_shape(plan, B, Hq, Hkv, ctx_stride, &s)) return TQ_ERR_ARG;
-  tq_status st = check_common(plan, q, q_dtype, K, ctx_len, s);
-  if (st != TQ_OK) return st;
-  if (!tq::valid_records(V, plan) || V->capacity / s.ctx_stride < int64_t(B) * Hkv) return TQ_ERR_ARG;
+  tq_status st = TQ_OK;
+  if (pages == nullptr) {
+    if ((st = check_common(plan, q, q_dtype, K, ctx_len, s)) != TQ_OK) return st;
+    if (!tq::valid_records(V, plan) || V->capacity / s.ctx_stride < int64_t(B) * Hkv) return TQ_ERR_ARG;
+  } else {  // a paged cache: any number of whole pages; the page table names them
+    if (!q || !ctx_len || !tq::aligned16(q) || (q_dtype != TQ_F32 && q_dtype != TQ_BF16)) return TQ_ERR_ARG;
+    if (!tq::valid_records(K, plan) || !tq::valid_records(V, plan) || K->capacity < kPage || V->capacity < kPage)
+      return TQ_ERR_ARG;
+    if (K->layout != TQ_LAYOUT_ROWS) return TQ_ERR_UNSUPPORTED;
+    if (!supported(s)) return TQ_ERR_UNSUPPORTED;
+  }
   if (V->layout == TQ_LAYOUT_BLOCK32 && ctx_stride % 32 != 0) return TQ_ERR_ARG;
   if (!out || !tq::aligned16(out) || !workspace || !tq::aligned16(workspace)) return TQ_ERR_ARG;
   if (ws_bytes < sizeof(float) * ws_floats(s)) return TQ_ERR_WORKSPACE;
@@ -505,7 +533,7 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
     uint8_t* ws8 = static_cast<uint8_t*>(workspace);
     return tq::launch_decode_tc(plan, q, q_dtype, K, V, ctx_len, B, Hq, Hkv, ctx_stride, sc,
                                 reinterpret_cast<float*>(ws8 + l.part), tc_slots(s), ws8 + l.tables,
-                                static_cast<unsigned*>(workspace), out, cs);
+                                static_cast<unsigned*>(workspace), out, cs, pages);
   }
   if ((st = launch_prep(plan, q, q_dtype, s, qt, stv, cs)) != TQ_OK) return st;
   SplitArgs a{};
@@ -519,6 +547,11 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
   a.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)s.d);
   a.alpha = plan->qjl_alpha;
   a.part = part;
+  a.pages = pages;
+  a.max_pages = ctx_stride / kPage;
+  a.npages = std::min(K->capacity, V->capacity) / kPage;
+  a.fault = tq::fault_word();
+  if (!a.fault) return TQ_ERR_CUDA;
   const size_t smem = split_smem(s);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -534,6 +567,26 @@ extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_
   c.out = out;
   combine_kernel<<<B * Hq, 256, sizeof(float) * (3 * s.d + s.m + s.nsplit), cs>>>(c);
   return tq::launch_status();
+}
+
+}  // namespace
+
+extern "C" tq_status tq_decode_attention(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
+                                         const tq_records* K, const tq_records* V, const int32_t* ctx_len,
+                                         int64_t ctx_stride, float scale, float* out, void* workspace,
+                                         size_t ws_bytes, tq_stream stream) {
+  return decode_impl(plan, q, q_dtype, B, Hq, Hkv, K, V, ctx_len, ctx_stride, scale, out, workspace, ws_bytes, stream,
+                     nullptr);
+}
+
+extern "C" tq_status tq_decode_attention_paged(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq,
+                                               int Hkv, const tq_records* K, const tq_records* V,
+                                               const int32_t* ctx_len, const int32_t* pages, int max_pages,
+                                               float scale, float* out, void* workspace, size_t ws_bytes,
+                                               tq_stream stream) {
+  if (pages == nullptr || !tq::aligned16(pages) || max_pages < 1) return TQ_ERR_ARG;
+  return decode_impl(plan, q, q_dtype, B, Hq, Hkv, K, V, ctx_len, int64_t(max_pages) * kPage, scale, out, workspace,
+                     ws_bytes, stream, pages);
 }
 
 extern "C" tq_status tq_decode_scores(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,

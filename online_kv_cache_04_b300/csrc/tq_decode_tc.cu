@@ -98,6 +98,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWS = 256.f;                           // attention weights carry 2^8 (up to 2^14 in f16)
 constexpr int kBMaxExp = 15;                           // query operand entries stay below 2^15
 constexpr unsigned kFaultDecode = 2u;
+constexpr unsigned kFaultPage = 16u;                   // a page-table entry outside the record arrays
 
 // Key operand kinds after the move to bits 12..15: exponent bits over a zero
 // base (values 2^-11, 2^-7, 2 when set, 0 when clear), and the sign of 1.0.
@@ -146,6 +147,8 @@ struct TcArgs {
   const float *knorm, *krnorm, *vnorm, *vrnorm;
   const int32_t* ctx_len;
   int64_t ctx_stride;
+  const int32_t* pages;  // paged caches: [B*Hkv][max_pages] page of each 256-token tile (NULL: contiguous rows)
+  int64_t max_pages, npages;  // pages per unit; pages the record arrays hold
   int B, Hq, Hkv, G;
   const void* q;     // [B*Hq][128] queries, bf16 (q_bf16) or fp32
   int q_bf16;
@@ -186,10 +189,10 @@ __host__ __device__ inline int64_t owner(int64_t f, int64_t total, int64_t ctas)
 // token 8t + 4·sub + e, k-slot 8 + 2t + e token 8t + 4·sub + 2 + e (word bits
 // L = 4t + 2·sub (+1) and 16 + L).
 
-template <int W, int GP>
+template <int W, int GP, bool Q>
 struct Shape {
   static constexpr int NPM = W == 3 ? 4 : W;   // ±1 planes of the codebook
-  static constexpr int NP = NPM + 1;           // plus the QJL sign plane
+  static constexpr int NP = NPM + (Q ? 1 : 0);  // plus the QJL sign plane (none for stage 1 alone)
   static constexpr int NKS = 8 * NP;           // score K-steps of 16 coordinates
   static constexpr int GH = GP / 4;            // score head tiles = heads per thread
   // ring stage of one full tile; a short tile fills the first half of each region
@@ -224,11 +227,11 @@ struct Misc {
 constexpr int kMiscBytes = 2048;
 static_assert(sizeof(Misc) <= kMiscBytes, "barriers and per-head state must fit their region");
 
-template <int W, int GP>
+template <int W, int GP, bool Q>
 constexpr int smem_bytes() {
-  return 1024 + Shape<W, GP>::kOffMisc + kMiscBytes;
+  return 1024 + Shape<W, GP, Q>::kOffMisc + kMiscBytes;
 }
-static_assert(smem_bytes<3, 8>() <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
+static_assert(smem_bytes<3, 8, true>() <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
 
 // Segment of this CTA's tile range that falls in one unit.
 struct Seg {
@@ -306,7 +309,7 @@ __device__ __forceinline__ float sum_groups(const float* red, int e, int stride)
 // 效率革命" §三: the estimator takes Π q and S q): on return qr[g][j] = (Π q_g)_j
 // and sr[g][i] = (S̃ Π q_g)_i = (S q_g)_i, zero for g >= G.  All NT threads; one
 // round of global loads (q and both matrices).
-template <int GP, int NT>
+template <int GP, int NT, bool Q>
 __device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* scr, float** qr_out,
                                              float** sr_out) {
   constexpr int NG = NT / 128, R = 128 * 128 / NT;
@@ -325,15 +328,15 @@ __device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* 
                             : reinterpret_cast<const float*>(a.q)[off];
   }
   float v1[R], v2[R];
-  load_cols<NT>(a.pi_t, v1);     // (Π q)_j = Σ_c Πᵀ[c][j] q_c
-  load_cols<NT>(a.s_rot_t, v2);  // (S̃ q̃)_i = Σ_j S̃ᵀ[j][i] q̃_j
+  load_cols<NT>(a.pi_t, v1);                  // (Π q)_j = Σ_c Πᵀ[c][j] q_c
+  if constexpr (Q) load_cols<NT>(a.s_rot_t, v2);  // (S̃ q̃)_i = Σ_j S̃ᵀ[j][i] q̃_j
   // The query and the workspace belong to the stream's earlier launches: wait
   // for them (programmatic dependent launch).  Only then may the decode kernel
   // start, since its first copies read the records those launches wrote.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   // bring Π and S̃ (row-major), which the unit's merge reads, into L2 meanwhile
-  for (int e = threadIdx.x; e < 2 * kD * kD / 32; e += NT) {
+  for (int e = threadIdx.x; e < (Q ? 2 : 1) * kD * kD / 32; e += NT) {
     const float* line = e < kD * kD / 32 ? a.pi + 32 * e : a.s_rot + 32 * (e - kD * kD / 32);
     asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
   }
@@ -344,9 +347,13 @@ __device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* 
   cta_sync_n<NT>();
   for (int e = threadIdx.x; e < GP * kD; e += NT) qr[e] = sum_groups<NG>(red, e, GP * kD);
   cta_sync_n<NT>();
-  cols_times<GP, NT>(v2, qr, kD, red);
-  cta_sync_n<NT>();
-  for (int e = threadIdx.x; e < GP * kD; e += NT) sr[e] = sum_groups<NG>(red, e, GP * kD);
+  if constexpr (Q) {
+    cols_times<GP, NT>(v2, qr, kD, red);
+    cta_sync_n<NT>();
+    for (int e = threadIdx.x; e < GP * kD; e += NT) sr[e] = sum_groups<NG>(red, e, GP * kD);
+  } else {
+    for (int e = threadIdx.x; e < GP * kD; e += NT) sr[e] = 0.f;
+  }
   cta_sync_n<NT>();
   *qr_out = qr;
   *sr_out = sr;
@@ -357,7 +364,7 @@ __device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* 
 // the last CTA of the unit to hand in its partial.  All NT threads; partials
 // written by other CTAs are read past L1.  Two rounds of global loads when ns
 // fits one chunk: (references, sums, partial values), then both matrices.
-template <int GP, int NT>
+template <int GP, int NT, bool Q>
 __device__ __noinline__ void unit_merge(const TcArgs& a, int head0, int ns, float* scr) {
   constexpr int NG = NT / 128, RR = 128 * 128 / NT;
   constexpr int kStride = 2 + 2 * kD;
@@ -429,13 +436,16 @@ __device__ __noinline__ void unit_merge(const TcArgs& a, int head0, int ns, floa
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[threadIdx.x + NT * r] = v[r];
   float v1[RR], v2[RR];
-  load_cols<NT>(a.s_rot, v1);  // (S̃ᵀ acc_sgn)_j = Σ_i S̃[i][j] acc_sgn_i
-  load_cols<NT>(a.pi, v2);     // (Πᵀ y)_i = Σ_j Π[j][i] y_j
+  if constexpr (Q) load_cols<NT>(a.s_rot, v1);  // (S̃ᵀ acc_sgn)_j = Σ_i S̃[i][j] acc_sgn_i
+  load_cols<NT>(a.pi, v2);                     // (Πᵀ y)_i = Σ_j Π[j][i] y_j
   cta_sync_n<NT>();
-  cols_times<GP, NT>(v1, acc + kD, 2 * kD, red);
-  cta_sync_n<NT>();
+  if constexpr (Q) {
+    cols_times<GP, NT>(v1, acc + kD, 2 * kD, red);
+    cta_sync_n<NT>();
+  }
   for (int e = threadIdx.x; e < GP * kD; e += NT)
-    y[e] = fmaf(a.alpha, sum_groups<NG>(red, e, GP * kD), acc[(e >> 7) * 2 * kD + (e & (kD - 1))]);
+    y[e] = Q ? fmaf(a.alpha, sum_groups<NG>(red, e, GP * kD), acc[(e >> 7) * 2 * kD + (e & (kD - 1))])
+             : acc[(e >> 7) * 2 * kD + (e & (kD - 1))];
   cta_sync_n<NT>();
   cols_times<GP, NT>(v2, y, kD, red);
   cta_sync_n<NT>();
@@ -452,19 +462,19 @@ __device__ __noinline__ void unit_merge(const TcArgs& a, int head0, int ns, floa
 // per head and K index, stored divided by a power of two E per part and head)
 // followed by the constants A0, B0, A1, B1 of each head's affine map from the
 // products to scores in log2 units.
-template <int W, int GP>
+template <int W, int GP, bool Q>
 struct Table {
   static constexpr int kConstBytes = 4 * 8 * 4;
-  static constexpr int kBytes = Shape<W, GP>::kBKBytes + kConstBytes;
+  static constexpr int kBytes = Shape<W, GP, Q>::kBKBytes + kConstBytes;
 };
 struct TableState {
   float amax[2][8];     // per part and head: largest |entry| (as non-negative float bits)
   float osum[16][2][2]; // per warp, part, head of the warp's thread group: Σ of the {0, x} kinds' offsets
   float cf[4];          // Walsh coefficients of the codebook planes
 };
-template <int W, int GP>
+template <int W, int GP, bool Q>
 constexpr int table_smem_bytes() {
-  return 1024 + Shape<W, GP>::kBKBytes + Scratch<GP, kTableThreads>::kPrep * 4 + (int)sizeof(TableState);
+  return 1024 + Shape<W, GP, Q>::kBKBytes + Scratch<GP, kTableThreads>::kPrep * 4 + (int)sizeof(TableState);
 }
 
 // One CTA per unit: q̃ = Π q and s̃ = S q of its G heads, then the table.  A key
@@ -474,9 +484,9 @@ constexpr int table_smem_bytes() {
 // offset Σ w over those coordinates goes into the score constant) or as −w.
 // Also zeroes the unit's arrival counter for the decode kernel that follows.
 // Every sum has a fixed order, so the table is the same on every call.
-template <int W, int GP>
+template <int W, int GP, bool Q>
 __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs a) {
-  using Sh = Shape<W, GP>;
+  using Sh = Shape<W, GP, Q>;
   constexpr int NT = kTableThreads;
   constexpr int NPM = Sh::NPM, NP = Sh::NP, GH = Sh::GH;
   extern __shared__ uint8_t smem_raw[];
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs 
   if (threadIdx.x < 16) ts->amax[threadIdx.x >> 3][threadIdx.x & 7] = 0.f;
   for (int e = threadIdx.x; e < Sh::kBKBytes / 16; e += NT) reinterpret_cast<uint4*>(BK)[e] = make_uint4(0, 0, 0, 0);
   float *qr, *sr;
-  unit_query_prep<GP, NT>(a, head0, scr, &qr, &sr);  // its first barrier publishes the lines above
+  unit_query_prep<GP, NT, Q>(a, head0, scr, &qr, &sr);  // its first barrier publishes the lines above
   // (past the grid dependency wait inside unit_query_prep: the workspace is ours)
   if (threadIdx.x == 0) a.arrivals[u] = 0u;
   // thread group grp = threadIdx / 128 takes heads grp and grp + 4; thread j its coordinate j:
@@ -515,7 +525,7 @@ __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs 
     float am = 0.f;
 #pragma unroll
     for (int P = 0; P < NPM; ++P) am = fmaxf(am, fabsf(wsc * cf[P] * qv[i]));
-    float aq = fabsf(wsc * sv[i]);
+    float aq = Q ? fabsf(wsc * sv[i]) : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
@@ -565,7 +575,7 @@ __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs 
     }
   }
   cta_sync_n<NT>();
-  uint8_t* dst = a.tables + (size_t)u * Table<W, GP>::kBytes;
+  uint8_t* dst = a.tables + (size_t)u * Table<W, GP, Q>::kBytes;
   for (int e = threadIdx.x; e < Sh::kBKBytes / 16; e += NT)
     reinterpret_cast<uint4*>(dst)[e] = reinterpret_cast<const uint4*>(BK)[e];
   if (threadIdx.x < 8) {
@@ -584,9 +594,9 @@ __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs 
   }
 }
 
-template <int W, int GP>
+template <int W, int GP, bool Q>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) {
-  using Sh = Shape<W, GP>;
+  using Sh = Shape<W, GP, Q>;
   constexpr int NPM = Sh::NPM, NP = Sh::NP, GH = Sh::GH;
   constexpr int NT = kThreads;
   static_assert(Scratch<GP, NT>::kMerge * 4 <= Sh::kOffMisc - Sh::kOffBK, "merge scratch exceeds its region");
@@ -634,7 +644,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         if (cur < f1) cL = (int)min((int64_t)max(__ldg(a.ctx_len + cu / a.Hkv), 0), a.ctx_stride);
         continue;
       }
-      const int64_t row0 = cu * a.ctx_stride + ct * kTile;
+      int64_t row0 = cu * a.ctx_stride + ct * kTile;
+      if (a.pages != nullptr) {  // paged cache: the tile is one page
+        int64_t pg = __ldg(a.pages + cu * a.max_pages + ct);
+        if (pg < 0 || pg >= a.npages) {
+          atomicOr(a.fault, kFaultPage);
+          pg = 0;
+        }
+        row0 = pg * kTile;
+      }
       const int ntok = (int)min((int64_t)kTile, a.ctx_stride - ct * kTile);  // 256, or 128 at a unit's end
       ++cur;
       ++ct;
@@ -646,15 +664,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       const uint32_t bar = smem_u32(&ms->ld_full[s]);
       const uint32_t dst = sbase + Sh::kOffRing + s * Sh::kStage;
       const int idxb = ntok * 16 * W, sgnb = ntok * 16, nrmb = ntok * 4;
-      mbar_arrive_expect_tx(bar, 2 * idxb + 2 * sgnb + 4 * nrmb);
+      mbar_arrive_expect_tx(bar, Q ? 2 * idxb + 2 * sgnb + 4 * nrmb : 2 * idxb + 2 * nrmb);
       bulk_load(dst + Sh::kOffKIdx, a.kidx + row0 * (4 * W), idxb, bar);
-      bulk_load(dst + Sh::kOffKSgn, a.ksgn + row0 * 4, sgnb, bar);
       bulk_load(dst + Sh::kOffKNorm, a.knorm + row0, nrmb, bar);
-      bulk_load(dst + Sh::kOffKRn, a.krnorm + row0, nrmb, bar);
       bulk_load(dst + Sh::kOffVIdx, a.vidx + (row0 >> 5) * (W * kD), idxb, bar);
-      bulk_load(dst + Sh::kOffVSgn, a.vsgn + (row0 >> 5) * kD, sgnb, bar);
       bulk_load(dst + Sh::kOffVNorm, a.vnorm + row0, nrmb, bar);
-      bulk_load(dst + Sh::kOffVRn, a.vrnorm + row0, nrmb, bar);
+      if constexpr (Q) {  // stage 1 alone stores no signs and no residual norms
+        bulk_load(dst + Sh::kOffKSgn, a.ksgn + row0 * 4, sgnb, bar);
+        bulk_load(dst + Sh::kOffKRn, a.krnorm + row0, nrmb, bar);
+        bulk_load(dst + Sh::kOffVSgn, a.vsgn + (row0 >> 5) * kD, sgnb, bar);
+        bulk_load(dst + Sh::kOffVRn, a.vrnorm + row0, nrmb, bar);
+      }
     }
   };
   if (threadIdx.x == 0) issue_upto(0);
@@ -701,10 +721,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       if (threadIdx.x == 0) {
         fence_proxy_async_smem();
         const uint32_t bar = smem_u32(&ms->tab_full);
-        const uint8_t* src = a.tables + (size_t)sg.u * Table<W, GP>::kBytes;
-        mbar_arrive_expect_tx(bar, Table<W, GP>::kBytes);
+        const uint8_t* src = a.tables + (size_t)sg.u * Table<W, GP, Q>::kBytes;
+        mbar_arrive_expect_tx(bar, Table<W, GP, Q>::kBytes);
         bulk_load(smem_u32(BK), src, Sh::kBKBytes, bar);
-        bulk_load(smem_u32(&ms->consts[0][0]), src + Sh::kBKBytes, Table<W, GP>::kConstBytes, bar);
+        bulk_load(smem_u32(&ms->consts[0][0]), src + Sh::kBKBytes, Table<W, GP, Q>::kConstBytes, bar);
       }
       wait(&ms->tab_full, tab_phase);
       tab_phase ^= 1u;
@@ -786,8 +806,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
         for (int st = 0; st < 2; ++st) {
           const int t = 32 * warp + 2 * (pr0 + 2 * st);
-          const float2 kn2 = *reinterpret_cast<const float2*>(kn + t), kr2 = *reinterpret_cast<const float2*>(kr + t);
-          const float2 vn2 = *reinterpret_cast<const float2*>(vn + t), vr2 = *reinterpret_cast<const float2*>(vr + t);
+          const float2 kn2 = *reinterpret_cast<const float2*>(kn + t), vn2 = *reinterpret_cast<const float2*>(vn + t);
+          const float2 kr2 = Q ? *reinterpret_cast<const float2*>(kr + t) : make_float2(0.f, 0.f);
+          const float2 vr2 = Q ? *reinterpret_cast<const float2*>(vr + t) : make_float2(0.f, 0.f);
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const bool valid = tb + t + r < sg.L;
@@ -799,7 +820,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             for (int hh = 0; hh < GH; ++hh) {
               const float dm = acc[st][0][hh][2 * r] + acc[st][0][hh][2 * r + 1];
               const float dq = acc[st][1][hh][2 * r] + acc[st][1][hh][2 * r + 1];
-              const float sc = fmaf(knr, fmaf(A0[hh], dm, B0[hh]), krr * fmaf(A1[hh], dq, B1[hh]));
+              const float sc = Q ? fmaf(knr, fmaf(A0[hh], dm, B0[hh]), krr * fmaf(A1[hh], dq, B1[hh]))
+                                 : knr * fmaf(A0[hh], dm, B0[hh]);
               s2[st][hh][r] = (valid && 4 * hh + tig < a.G) ? sc : -INFINITY;
               mx[hh] = fmaxf(mx[hh], s2[st][hh][r] + lv);
             }
@@ -1007,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
     cta_sync_n<NT>();
     if (ms->last) {
       const int ns = (int)(owner((sg.u + 1) * a.tpu - 1, a.total, C) - owner(sg.u * a.tpu, a.total, C) + 1);
-      unit_merge<GP, NT>(a, head0, ns, reinterpret_cast<float*>(smem + Sh::kOffBK));
+      unit_merge<GP, NT, Q>(a, head0, ns, reinterpret_cast<float*>(smem + Sh::kOffBK));
     }
   }
   // no copy of this CTA may be in flight when it exits
@@ -1040,24 +1062,30 @@ int decode_tc_ctas(int64_t units, int64_t tpu) {
 }
 
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride) {
-  return plan->d == 128 && plan->m == 128 && G >= 1 && G <= 8 && V->layout == TQ_LAYOUT_BLOCK32 &&
+  return plan->d == 128 && (plan->m == 128 || plan->m == 0) && G >= 1 && G <= 8 && V->layout == TQ_LAYOUT_BLOCK32 &&
          ctx_stride % kHalfTile == 0;
 }
 
-size_t decode_tc_table_bytes(int w, int G) {
-  const bool g8 = G > 4;
+size_t decode_tc_table_bytes(int w, int G, int m) {
+  const bool g8 = G > 4, q = m > 0;
   switch (w) {
-    case 1: return g8 ? Table<1, 8>::kBytes : Table<1, 4>::kBytes;
-    case 2: return g8 ? Table<2, 8>::kBytes : Table<2, 4>::kBytes;
-    default: return g8 ? Table<3, 8>::kBytes : Table<3, 4>::kBytes;
+    case 1: return q ? (g8 ? Table<1, 8, true>::kBytes : Table<1, 4, true>::kBytes)
+                     : (g8 ? Table<1, 8, false>::kBytes : Table<1, 4, false>::kBytes);
+    case 2: return q ? (g8 ? Table<2, 8, true>::kBytes : Table<2, 4, true>::kBytes)
+                     : (g8 ? Table<2, 8, false>::kBytes : Table<2, 4, false>::kBytes);
+    default: return q ? (g8 ? Table<3, 8, true>::kBytes : Table<3, 4, true>::kBytes)
+                      : (g8 ? Table<3, 8, false>::kBytes : Table<3, 4, false>::kBytes);
   }
 }
 
 tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype, const tq_records* K,
                            const tq_records* V, const int32_t* ctx_len, int B, int Hq, int Hkv, int64_t ctx_stride,
                            float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const int32_t* pages) {
   TcArgs a{};
+  a.pages = pages;
+  a.max_pages = ctx_stride / kTile;
+  a.npages = std::min(K->capacity, V->capacity) / kTile;
   a.kidx = K->idx; a.ksgn = K->sgn; a.knorm = K->norm; a.krnorm = K->rnorm;
   a.vidx = V->idx; a.vsgn = V->sgn; a.vnorm = V->norm; a.vrnorm = V->rnorm;
   a.ctx_len = ctx_len;
@@ -1106,13 +1134,21 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
   };
-#define TQ_DECODE_TC_GO(W_, GP_) \
-  go(unit_table_kernel<W_, GP_>, table_smem_bytes<W_, GP_>(), decode_tc_kernel<W_, GP_>, smem_bytes<W_, GP_>())
+#define TQ_DECODE_TC_GO(W_, GP_, Q_)                                                                \
+  go(unit_table_kernel<W_, GP_, Q_>, table_smem_bytes<W_, GP_, Q_>(), decode_tc_kernel<W_, GP_, Q_>, \
+     smem_bytes<W_, GP_, Q_>())
   const bool g8 = a.G > 4;
-  switch (plan->w) {
-    case 1: return g8 ? TQ_DECODE_TC_GO(1, 8) : TQ_DECODE_TC_GO(1, 4);
-    case 2: return g8 ? TQ_DECODE_TC_GO(2, 8) : TQ_DECODE_TC_GO(2, 4);
-    default: return g8 ? TQ_DECODE_TC_GO(3, 8) : TQ_DECODE_TC_GO(3, 4);
+  if (plan->m > 0) {
+    switch (plan->w) {
+      case 1: return g8 ? TQ_DECODE_TC_GO(1, 8, true) : TQ_DECODE_TC_GO(1, 4, true);
+      case 2: return g8 ? TQ_DECODE_TC_GO(2, 8, true) : TQ_DECODE_TC_GO(2, 4, true);
+      default: return g8 ? TQ_DECODE_TC_GO(3, 8, true) : TQ_DECODE_TC_GO(3, 4, true);
+    }
+  }
+  switch (plan->w) {  // stage 1 alone
+    case 1: return g8 ? TQ_DECODE_TC_GO(1, 8, false) : TQ_DECODE_TC_GO(1, 4, false);
+    case 2: return g8 ? TQ_DECODE_TC_GO(2, 8, false) : TQ_DECODE_TC_GO(2, 4, false);
+    default: return g8 ? TQ_DECODE_TC_GO(3, 8, false) : TQ_DECODE_TC_GO(3, 4, false);
   }
 #undef TQ_DECODE_TC_GO
 }

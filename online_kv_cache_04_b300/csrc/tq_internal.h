@@ -66,9 +66,9 @@ bool quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n);
 tq_status quantize_tc(const tq_plan* plan, const void* x0, const void* x1, int64_t n, int64_t ld_x,
                       const tq_records* out0, const tq_records* out1, int64_t row0, cudaStream_t st);
 
-// Tensor-core decode (tq_decode_tc.cu): d = m = 128, G <= 8, values in
+// Tensor-core decode (tq_decode_tc.cu): d = 128, m = 128 or 0, G <= 8, values in
 // TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Two launches: one CTA per
-// (batch, kv head) unit builds its query table (decode_tc_table_bytes(w, G)
+// (batch, kv head) unit builds its query table (decode_tc_table_bytes(w, G, m)
 // bytes, 16-byte aligned) and zeroes its arrival counter; the decode kernel
 // then does the scores, softmax and values, and the last CTA of each unit
 // merges the unit's partials ([B*Hq][smax][2 + 256]) into out.  Each unit is
@@ -77,11 +77,13 @@ int64_t decode_tc_tpu(int64_t ctx_stride);
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride);
 int decode_tc_ctas(int64_t units, int64_t tpu);
 int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas);
-size_t decode_tc_table_bytes(int w, int G);
+size_t decode_tc_table_bytes(int w, int G, int m);
+// pages: NULL for contiguous units, else the page table of a paged cache
+// ([B*Hkv][ctx_stride / 256] page of each 256-token tile; ctx_stride % 256 == 0).
 tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype, const tq_records* K,
                            const tq_records* V, const int32_t* ctx_len, int B, int Hq, int Hkv, int64_t ctx_stride,
                            float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const int32_t* pages = nullptr);
 
 // SIMT quantizer over a column subset (tq_quantize.cu): element j of row r is
 // x[r][cols[j]] for j < plan->d (cols: device int32); rows [out_offset,

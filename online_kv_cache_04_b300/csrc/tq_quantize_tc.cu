@@ -128,7 +128,10 @@ __device__ __forceinline__ void store_block32(uint32_t* blk, const uint32_t (&wo
   }
 }
 
-template <int W>
+// Q: the QJL stage is on (m = 128); without it (m = 0, stage 1 alone) there is
+// no GEMM2, no residual in TMEM and no sign epilogue: the TMEM slot is free once
+// epilogue 1 has read U.
+template <int W, bool Q>
 __global__ void __launch_bounds__(kThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
                        const __grid_constant__ CUtensorMap tm_pi,
@@ -246,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(smem_u32(&bars->u_full[s]));
         mma_commit(smem_u32(&bars->x_empty[s]));
-        if (it >= 1 && !gemm2(it - 1)) { ok = false; break; }
+        if (Q && it >= 1 && !gemm2(it - 1)) { ok = false; break; }
       }
-      if (ok && it >= 1) gemm2(it - 1);
+      if (Q && ok && it >= 1) gemm2(it - 1);
     }
   } else {
     // the previous launch in the stream may still read the records written here
@@ -344,15 +347,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             rsq = fmaf(rho, rho, rsq);
             rho2[e] = rho;
           }
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(rho2[0], rho2[1]);
-          const float2 hf = __bfloat1622float2(hv);
-          const __nv_bfloat162 l = __floats2bfloat162_rn(rho2[0] - hf.x, rho2[1] - hf.y);
-          hi[j] = *reinterpret_cast<const uint32_t*>(&hv);
-          lo[j] = *reinterpret_cast<const uint32_t*>(&l);
+          if (Q) {
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(rho2[0], rho2[1]);
+            const float2 hf = __bfloat1622float2(hv);
+            const __nv_bfloat162 l = __floats2bfloat162_rn(rho2[0] - hf.x, rho2[1] - hf.y);
+            hi[j] = *reinterpret_cast<const uint32_t*>(&hv);
+            lo[j] = *reinterpret_cast<const uint32_t*>(&l);
+          }
         }
-        // into the columns of U_lo just read: K-step c = [hi 8 | lo 8]
-        tmem_st8(acc + 128 + 16 * c, hi);
-        tmem_st8(acc + 128 + 16 * c + 8, lo);
+        if (Q) {  // into the columns of U_lo just read: K-step c = [hi 8 | lo 8]
+          tmem_st8(acc + 128 + 16 * c, hi);
+          tmem_st8(acc + 128 + 16 * c + 8, lo);
+        }
         // chunk c holds bits 16·(c & 1).. of plane word c / 2 (word (c >> 1) - 2h here)
 #pragma unroll
         for (int p = 0; p < W; ++p) {
@@ -361,11 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           else planes[p][0] |= x;
         }
       }
-      tmem_st_wait();
+      if (Q) tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->rho_full[s]));
-      if (h == 1) {  // the lower half writes ||r|| = n·sqrt(lower + upper partial)
+      // with QJL, GEMM2 reads the residual next; without, the slot is free
+      if (lane == 0) mbar_arrive(smem_u32(Q ? &bars->rho_full[s] : &bars->acc_empty[s]));
+      if (Q && h == 1) {  // the lower half writes ||r|| = n·sqrt(lower + upper partial)
         rsq_s[(it >> 1 & 1) * 128 + r] = rsq;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->rsq_full[s]));
@@ -390,6 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int p = 0; p < W; ++p)
             store_block32<2>(oidx + (blk_row >> 5) * (W * 128) + p * 128 + 64 * h, planes[p], valid, lane);
         }
+      }
+      if (!Q) {  // stage 1 alone: the norm is the record's last field
+        if (h == 0 && row < on) (second ? a.out1.norm : a.out0.norm)[row] = n;
+        continue;
       }
       if (!mbar_wait(smem_u32(&bars->p_full[s]), ph, a.fault, kFaultWait)) break;
       tc_fence_after();
@@ -457,10 +468,10 @@ bool map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int W>
+template <int W, bool Q>
 tq_status launch_w(const CUtensorMap& mx0, const CUtensorMap& mx1, const CUtensorMap& mp, const CUtensorMap& ms,
                    const TcArgs& a, cudaStream_t st) {
-  auto kern = quantize_tc_kernel<W>;
+  auto kern = quantize_tc_kernel<W, Q>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return TQ_ERR_CUDA;
   const int grid = (int)std::min<int64_t>(a.ntiles, tq::sm_count());
@@ -489,7 +500,8 @@ unsigned* tq::fault_word() {
 }
 
 bool tq::quantize_tc_supported(const tq_plan* plan, tq_dtype dtype, int64_t n) {
-  return plan->d == 128 && plan->m == 128 && dtype == TQ_BF16 && n < (int64_t(1) << 31) && encode_fn() != nullptr;
+  return plan->d == 128 && (plan->m == 128 || plan->m == 0) && dtype == TQ_BF16 && n < (int64_t(1) << 31) &&
+         encode_fn() != nullptr;
 }
 
 // Output fields of rows [row0, row0 + n) of `out`.
@@ -497,9 +509,9 @@ static TcOut tc_out(const tq_records* out, int64_t n, int64_t row0, int w) {
   const bool rows = out->layout == TQ_LAYOUT_ROWS;
   TcOut o;
   o.idx = rows ? out->idx + row0 * (w * 4) : out->idx + (row0 / 32) * (w * 128);
-  o.sgn = rows ? out->sgn + row0 * 4 : out->sgn + (row0 / 32) * 128;
+  o.sgn = out->sgn == nullptr ? nullptr : rows ? out->sgn + row0 * 4 : out->sgn + (row0 / 32) * 128;
   o.norm = out->norm + row0;
-  o.rnorm = out->rnorm + row0;
+  o.rnorm = out->rnorm == nullptr ? nullptr : out->rnorm + row0;
   o.n = n;
   o.layout = out->layout;
   return o;
@@ -513,7 +525,8 @@ tq_status tq::quantize_tc(const tq_plan* plan, const void* x0, const void* x1, i
   CUtensorMap mx0, mx1, mp, ms;
   if (!map_bf16(&mx0, x0, (uint64_t)n, 128, (uint64_t)ld_x) ||
       !map_bf16(&mx1, pair ? x1 : x0, (uint64_t)n, 128, (uint64_t)ld_x) ||
-      !map_bf16(&mp, plan->pi_bf16, 256, 128, 128) || !map_bf16(&ms, plan->s_bf16, 256, 128, 128))
+      !map_bf16(&mp, plan->pi_bf16, 256, 128, 128) ||
+      !map_bf16(&ms, plan->m > 0 ? plan->s_bf16 : plan->pi_bf16, 256, 128, 128))  // (m = 0: the S map goes unused)
     return TQ_ERR_CUDA;
   const int w = plan->w;
   TcArgs a{};
@@ -525,10 +538,11 @@ tq_status tq::quantize_tc(const tq_plan* plan, const void* x0, const void* x1, i
   a.bounds = plan->bounds;
   a.fault = tq::fault_word();
   if (!a.fault) return TQ_ERR_CUDA;
+  const bool q = plan->m > 0;
   switch (w) {
-    case 1: return launch_w<1>(mx0, mx1, mp, ms, a, st);
-    case 2: return launch_w<2>(mx0, mx1, mp, ms, a, st);
-    default: return launch_w<3>(mx0, mx1, mp, ms, a, st);
+    case 1: return q ? launch_w<1, true>(mx0, mx1, mp, ms, a, st) : launch_w<1, false>(mx0, mx1, mp, ms, a, st);
+    case 2: return q ? launch_w<2, true>(mx0, mx1, mp, ms, a, st) : launch_w<2, false>(mx0, mx1, mp, ms, a, st);
+    default: return q ? launch_w<3, true>(mx0, mx1, mp, ms, a, st) : launch_w<3, false>(mx0, mx1, mp, ms, a, st);
   }
 }
 

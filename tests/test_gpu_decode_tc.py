@@ -1,7 +1,7 @@
 """GPU parity of the tensor-core decode path (values in 32-row blocks, d = m = 128).
 
-tq_decode_attention takes the tcgen05 kernel when the value records are in
-TQ_LAYOUT_BLOCK32, ctx_stride is a multiple of 128 and there are at most 8
+tq_decode_attention takes the warp-MMA (mma.sync f16) kernel when the value
+records are in TQ_LAYOUT_BLOCK32, ctx_stride is a multiple of 128 and there are at most 8
 query heads per kv head.  Outputs are compared with the float64 oracle on
 identical records (the oracle's own packed records, or the GPU's records
 unpacked by the oracle), relative L2 <= 1e-3.

@@ -71,13 +71,15 @@ def test_quantize_pair_stage1_only_equals_two_calls(gpu_lib, w):
 
 
 @pytest.mark.parametrize("w", [1, 2, 3])
-@pytest.mark.parametrize("vlayout", [0, 1])
-def test_decode_stage1_only_oracle_records(gpu_lib, w, vlayout):
-    """GQA 8 : 2 over two batch rows of ragged length, on the oracle's own records."""
+@pytest.mark.parametrize("vlayout,Hq,T,ctx", [(0, 8, 640, [640, 333]), (1, 8, 640, [640, 333]),
+                                              (1, 16, 1152, [1152, 1]), (1, 4, 9216, [9216, 5000])])
+def test_decode_stage1_only_oracle_records(gpu_lib, w, vlayout, Hq, T, ctx):
+    """GQA 4 : 2 to 16 : 2 over two batch rows of ragged length, on the oracle's own
+    records; values by row take the general kernels, values in blocks the warp-MMA
+    kernel (9216 tokens span many tiles and CTAs)."""
     d = 128
-    B, Hq, Hkv, T = 2, 8, 2, 640
-    ctx = [640, 333]
-    g = torch.Generator().manual_seed(70 + w)
+    B, Hkv = 2, 2
+    g = torch.Generator().manual_seed(70 + w + T)
     K = torch.randn(B, Hkv, T, d, generator=g)
     V = torch.randn(B, Hkv, T, d, generator=g)
     q = torch.randn(B, Hq, d, generator=g)
