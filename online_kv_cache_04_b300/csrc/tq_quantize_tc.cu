@@ -7,8 +7,9 @@
 //              bf16 x is exact): one N = 256 product per K-step against the
 //              stacked [Π_hi; Π_lo], the two fp32 halves summed by epilogue 1
 //   epilogue 1 n = ||x|| from the staged tile, u = U / n, bucketize against
-//              the Lloyd-Max bounds -> index bit-planes, ρ = u - c[idx],
-//              ||ρ||², ρ split into bf16 hi + lo written back to TMEM
+//              the Lloyd-Max bounds (binary search) -> index bit-planes,
+//              ρ = u - c[idx], ||ρ||², ρ split into bf16 hi + lo written back
+//              to TMEM; coordinate pairs in packed fp32x2 arithmetic
 //   GEMM2      P = ρ (S Πᵀ)ᵀ as ρ_hi·S_hi + ρ_hi·S_lo + ρ_lo·S_hi, with ρ
 //              read from TMEM as the A operand
 //   epilogue 2 σ = [P >= 0] packed into words, ||r|| = n ||ρ||, stores
@@ -49,7 +50,8 @@ constexpr int kOffPi = 0, kOffSHi = 2 * kMatBytes, kOffSLo = 3 * kMatBytes;
 constexpr int kOffX = 4 * kMatBytes;             // two x stages
 constexpr int kOffBar = kOffX + 2 * kMatBytes;
 constexpr int kOffRsq = kOffBar + 256;           // [slot 2][tile parity 2][128] partial ||ρ||² of the upper half
-constexpr int kSmemBytes = kOffRsq + 2 * 2 * 128 * 4 + 1024; // + alignment slack
+constexpr int kOffNsq = kOffRsq + 2 * 2 * 128 * 4;  // [slot 2][tile parity 2][half 2][128] partial ||x||²
+constexpr int kSmemBytes = kOffNsq + 2 * 2 * 2 * 128 * 4 + 1024; // + alignment slack
 constexpr int kThreads = 576, kMmaWarp = 16, kTmaWarp = 17;
 constexpr uint32_t kTmemCols = 512;              // slot s: [256s, +256) = U_hi | U_lo, then P | ρ K-steps [hi 8 | lo 8]
 
@@ -59,6 +61,7 @@ struct Bars {
   uint64_t b_full;
   uint64_t x_full[2], x_empty[2], u_full[2], rho_full[2], p_full[2], acc_empty[2];
   uint64_t rsq_full[2];  // the upper coordinate half's ||ρ||² partials are in
+  uint64_t nsq_full[2];  // both halves' ||x||² partials of the slot's tile are in
   uint32_t tmem_base;
 };
 
@@ -156,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->p_full[s]), 1);
       mbar_init(smem_u32(&bars->acc_empty[s]), 8);
       mbar_init(smem_u32(&bars->rsq_full[s]), 4);
+      mbar_init(smem_u32(&bars->nsq_full[s]), 8);
     }
     fence_mbar_init();
   }
@@ -271,36 +275,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = g;
     const uint32_t acc = tmem + lane_base + 256 * s;
     float* rsq_s = reinterpret_cast<float*>(smem + kOffRsq) + (s * 2) * 128;
+    float* nsq_s = reinterpret_cast<float*>(smem + kOffNsq) + (s * 2) * 2 * 128;
     int it = g;
     for (int64_t tile = blockIdx.x + (int64_t)g * gridDim.x; tile < ntiles; tile += 2 * (int64_t)gridDim.x, it += 2) {
       const int ph = (it >> 1) & 1;
       if (!mbar_wait(smem_u32(&bars->x_full[s]), ph, a.fault, kFaultWait)) break;
-      // ||x|| from the staged tile (row r, both 64-column boxes, 128-byte swizzle); both halves
-      float ss[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint8_t* xt = smem + kOffX + s * kMatBytes;
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const uint8_t* row = xt + hb * kBoxBytes + (r >> 3) * 1024 + (r & 7) * 128;
+      // ||x||²: this half's 64 coordinates from the staged tile (row r, box h,
+      // 128-byte swizzle) in two packed pairs of partial sums; the halves meet
+      // in shared memory and both form n from the same two partials
+      uint64_t ssa = 0ull, ssb = 0ull;
+      {
+        const uint8_t* row = smem + kOffX + s * kMatBytes + h * kBoxBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
           const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xFFFF0000u);
-            ss[e] = fmaf(lo, lo, ss[e]);
-            ss[e] = fmaf(hi, hi, ss[e]);
+            const uint64_t x2 = f2_pack(__uint_as_float(wv[e] << 16), __uint_as_float(wv[e] & 0xFFFF0000u));
+            if (e & 1) ssb = f2_fma(x2, x2, ssb);
+            else ssa = f2_fma(x2, x2, ssa);
           }
         }
       }
-      const float n = sqrtf((ss[0] + ss[1]) + (ss[2] + ss[3]));
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->x_empty[s]));
+      float* nsq = nsq_s + ph * 2 * 128;
+      {
+        const float2 pa = f2_unpack(ssa), pb = f2_unpack(ssb);
+        nsq[h * 128 + r] = (pa.x + pa.y) + (pb.x + pb.y);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->nsq_full[s]));
+      if (!mbar_wait(smem_u32(&bars->nsq_full[s]), ph, a.fault, kFaultWait)) break;
+      const float n = sqrtf(nsq[r] + nsq[128 + r]);
       if (!mbar_wait(smem_u32(&bars->u_full[s]), ph, a.fault, kFaultWait)) break;
       tc_fence_after();
       const float inv = n > 0.f ? 1.0f / n : 0.f, nlive = n > 0.f ? -1.f : 0.f;
+      const uint64_t inv2 = f2_pack(inv, inv), nlive2 = f2_pack(nlive, nlive);
       uint32_t planes[W][2];
-      float rsq = 0.f;
+      uint64_t rsq2 = 0ull;
       // 16 coordinates per TMEM load: chunks 4h .. 4h + 3 (two per plane word)
 #pragma unroll
       for (int p = 0; p < W; ++p) planes[p][0] = planes[p][1] = 0u;
@@ -316,41 +330,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = 0; p < W; ++p) pw[p] = 0u;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float rho2[2];
+          // u = (U_hi + U_lo) / n for coordinates 2j, 2j + 1 of the chunk
+          const uint64_t u2 = f2_mul(f2_add(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                                            f2_pack(__uint_as_float(vl[2 * j]), __uint_as_float(vl[2 * j + 1]))),
+                                     inv2);
+          const float2 uu = f2_unpack(u2);
+          float cv[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float u = (__uint_as_float(v[2 * j + e]) + __uint_as_float(vl[2 * j + e])) * inv;
-            // bucket predicates against the sorted bounds (idx = how many lie below u)
-            bool pk[(1 << W) - 1];
-#pragma unroll
-            for (int k = 0; k < (1 << W) - 1; ++k) pk[k] = bnd[k] < u;
-            float cv = cent[0];
-#pragma unroll
-            for (int k = 0; k < (1 << W) - 1; ++k) cv = pk[k] ? cent[k + 1] : cv;
-            // index bits from the predicate prefix: bit q of idx
-            bool bq[W];
-            if constexpr (W == 1) {
-              bq[0] = pk[0];
-            } else if constexpr (W == 2) {
-              bq[0] = pk[0] ^ pk[1] ^ pk[2];
-              bq[1] = pk[1];
-            } else {
-              bq[0] = pk[0] ^ pk[1] ^ pk[2] ^ pk[3] ^ pk[4] ^ pk[5] ^ pk[6];
-              bq[1] = pk[1] ^ pk[3] ^ pk[5];
-              bq[2] = pk[3];
-            }
+            const float u = e ? uu.y : uu.x;
+            // idx = #{k : bound_k < u} by binary search over the sorted bounds;
+            // the branch taken at level l is bit W-1-l of idx (plane W-1-l)
             const uint32_t bit = 1u << (2 * j + e);
-#pragma unroll
-            for (int p = 0; p < W; ++p)
-              if (bq[p]) pw[p] |= bit;
-            const float rho = fmaf(cv, nlive, u);  // u - c[idx], and 0 for a zero vector
-            rsq = fmaf(rho, rho, rsq);
-            rho2[e] = rho;
+            if constexpr (W == 1) {
+              const bool p0 = u > bnd[0];
+              cv[e] = p0 ? cent[1] : cent[0];
+              if (p0) pw[0] |= bit;
+            } else if constexpr (W == 2) {
+              const bool p1 = u > bnd[1];
+              const bool p0 = u > (p1 ? bnd[2] : bnd[0]);
+              const float chi = p1 ? cent[3] : cent[1], clo = p1 ? cent[2] : cent[0];
+              cv[e] = p0 ? chi : clo;
+              if (p1) pw[1] |= bit;
+              if (p0) pw[0] |= bit;
+            } else {
+              const bool p2 = u > bnd[3];
+              const bool p1 = u > (p2 ? bnd[5] : bnd[1]);
+              const bool p0 = u > (p2 ? (p1 ? bnd[6] : bnd[4]) : (p1 ? bnd[2] : bnd[0]));
+              const float codd = p2 ? (p1 ? cent[7] : cent[5]) : (p1 ? cent[3] : cent[1]);
+              const float cevn = p2 ? (p1 ? cent[6] : cent[4]) : (p1 ? cent[2] : cent[0]);
+              cv[e] = p0 ? codd : cevn;
+              if (p2) pw[2] |= bit;
+              if (p1) pw[1] |= bit;
+              if (p0) pw[0] |= bit;
+            }
           }
+          const uint64_t rho2 = f2_fma(f2_pack(cv[0], cv[1]), nlive2, u2);  // u - c[idx], 0 for a zero vector
+          rsq2 = f2_fma(rho2, rho2, rsq2);
           if (Q) {
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(rho2[0], rho2[1]);
+            const float2 rr = f2_unpack(rho2);
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(rr.x, rr.y);
             const float2 hf = __bfloat1622float2(hv);
-            const __nv_bfloat162 l = __floats2bfloat162_rn(rho2[0] - hf.x, rho2[1] - hf.y);
+            const float2 lf = f2_unpack(f2_add(rho2, f2_pack(-hf.x, -hf.y)));
+            const __nv_bfloat162 l = __floats2bfloat162_rn(lf.x, lf.y);
             hi[j] = *reinterpret_cast<const uint32_t*>(&hv);
             lo[j] = *reinterpret_cast<const uint32_t*>(&l);
           }
@@ -367,6 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           else planes[p][0] |= x;
         }
       }
+      const float2 rs = f2_unpack(rsq2);
+      const float rsq = rs.x + rs.y;
       if (Q) tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -410,11 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tmem_ld32(acc + 32 * (2 * h + cc), v);
         tmem_ld_wait();
-        uint32_t wsg = 0u;
+        // bit j = [P_j >= 0]: the sign bits shifted in from the top coordinate
+        // down, then inverted; a zero vector (P = 0 of either sign) takes all ones
+        uint32_t neg = 0u;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (__uint_as_float(v[j]) >= 0.f) wsg |= 1u << j;
-        sg[cc] = wsg;
+        for (int j = 31; j >= 0; --j) neg = __funnelshift_l(v[j], neg, 1);
+        sg[cc] = n > 0.f ? ~neg : 0xFFFFFFFFu;
       }
       tc_fence_before();
       __syncwarp();
