@@ -51,8 +51,8 @@ int tc_slots(const DecodeShape& s) {
   return tq::decode_tc_slots(units, tpu, tq::decode_tc_ctas(units, tpu));
 }
 
-// Workspace of the tensor-core path: the per-unit arrival counters, the
-// per-unit query tables, then the partials (byte offsets, 256-byte aligned).
+// Workspace of the tensor-core path: the per-unit query tables, then the
+// partials (byte offsets, 256-byte aligned).
 struct TcLayout {
   size_t tables, part, bytes;
 };
@@ -60,7 +60,7 @@ TcLayout tc_layout(const DecodeShape& s) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t units = size_t(s.B) * s.Hkv, heads = size_t(s.B) * s.Hq;
   TcLayout l;
-  l.tables = up(units * sizeof(unsigned));
+  l.tables = 0;
   l.part = up(l.tables + units * tq::decode_tc_table_bytes(s.w, s.G, s.m));
   l.bytes = l.part + sizeof(float) * heads * tc_slots(s) * (2 + 2 * s.d);  // reference, sum, acc_rot, acc_sgn
   return l;
@@ -532,8 +532,8 @@ tq_status decode_impl(const tq_plan* plan, const void* q, tq_dtype q_dtype, int 
     const TcLayout l = tc_layout(s);
     uint8_t* ws8 = static_cast<uint8_t*>(workspace);
     return tq::launch_decode_tc(plan, q, q_dtype, K, V, ctx_len, B, Hq, Hkv, ctx_stride, sc,
-                                reinterpret_cast<float*>(ws8 + l.part), tc_slots(s), ws8 + l.tables,
-                                static_cast<unsigned*>(workspace), out, cs, pages);
+                                reinterpret_cast<float*>(ws8 + l.part), tc_slots(s), ws8 + l.tables, out, cs,
+                                pages);
   }
   if ((st = launch_prep(plan, q, q_dtype, s, qt, stv, cs)) != TQ_OK) return st;
   SplitArgs a{};

@@ -160,7 +160,6 @@ struct TcArgs {
   int64_t tpu;       // tiles per unit = ceil(ctx_stride / 256)
   int64_t total;     // units * tpu
   uint8_t* tables;     // [B*Hkv] per-unit query tables (unit_table_kernel)
-  unsigned* arrivals;  // [B*Hkv] CTAs of each unit done with their partials (zeroed by unit_table_kernel)
   float* out;        // [B*Hq][128]
   unsigned* fault;
 };
@@ -222,7 +221,6 @@ struct Misc {
   float mw[kNW][8];           // per warp: softmax reference per head at the end of a segment
   float lw[kNW][8];           // per warp: Σ p per head
   float cf[4];                // Walsh coefficients of the codebook planes
-  int last;                   // this CTA is the last of its unit to hand in its partial
 };
 constexpr int kMiscBytes = 2048;
 static_assert(sizeof(Misc) <= kMiscBytes, "barriers and per-head state must fit their region");
@@ -265,7 +263,7 @@ template <int GP, int NT>
 struct Scratch {
   static constexpr int NG = NT / 128;                                        // thread groups
   static constexpr int kPrep = (3 + NG) * GP * kD;                           // q, NG partial sums, Πq, Sq
-  static constexpr int kMerge = GP * (2 + kMaxCtas + 2 * kD + NG * kD + kD);  // see unit_merge
+  static constexpr int kMerge = GP * (2 + kMaxCtas + 2 * kD + NG * kD + kD);  // see unit_combine_kernel
 };
 
 // Column c = threadIdx % 128 of rows R·grp .. R·grp + R - 1 (grp = threadIdx / 128,
@@ -359,15 +357,30 @@ __device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* 
   *sr_out = sr;
 }
 
-// Merge of the ns partials (one per CTA) of each head of the unit, log-sum-exp
-// over their references, and the output o = Πᵀ(acc_rot + α S̃ᵀ acc_sgn) / l, by
-// the last CTA of the unit to hand in its partial.  All NT threads; partials
-// written by other CTAs are read past L1.  Two rounds of global loads when ns
-// fits one chunk: (references, sums, partial values), then both matrices.
-template <int GP, int NT, bool Q>
-__device__ __noinline__ void unit_merge(const TcArgs& a, int head0, int ns, float* scr) {
+// Merge of the ns partials (one per decode CTA) of each head of a unit,
+// log-sum-exp over their references, and the output o = Πᵀ(acc_rot + α S̃ᵀ
+// acc_sgn) / l: one CTA per unit, a programmatic dependent launch after the
+// decode kernel.  The matrix columns (the plan's, not written by the decode)
+// are loaded before the wait for the decode grid, so they overlap its tail;
+// after the wait the partials come in one round of global loads when ns fits
+// one chunk.
+template <int GP, bool Q>
+__global__ void __launch_bounds__(kThreads, 1) unit_combine_kernel(const TcArgs a, int ctas) {
+  constexpr int NT = kThreads;
   constexpr int NG = NT / 128, RR = 128 * 128 / NT;
   constexpr int kStride = 2 + 2 * kD;
+  extern __shared__ uint8_t smem_raw[];
+  float* scr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int64_t u = blockIdx.x;
+  const int b = (int)(u / a.Hkv), h = (int)(u - (int64_t)b * a.Hkv), head0 = b * a.Hq + h * a.G;
+  // the decode CTAs that own tiles of the unit: one partial slot each
+  const int ns = (int)(owner((u + 1) * a.tpu - 1, a.total, ctas) - owner(u * a.tpu, a.total, ctas) + 1);
+  float v1[RR], v2[RR];
+  if constexpr (Q) load_cols<NT>(a.s_rot, v1);  // (S̃ᵀ acc_sgn)_j = Σ_i S̃[i][j] acc_sgn_i
+  load_cols<NT>(a.pi, v2);                     // (Πᵀ y)_i = Σ_j Π[j][i] y_j
+  // the partials are the decode kernel's: wait for it to complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   float* ml = scr;                      // [GP][2] reference max, Σ w·l
   float* wgt = ml + 2 * GP;             // [GP][kMaxCtas] slot weights
   float* acc = wgt + GP * kMaxCtas;     // [GP][256] merged acc_rot | acc_sgn
@@ -435,9 +448,6 @@ __device__ __noinline__ void unit_merge(const TcArgs& a, int head0, int ns, floa
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[threadIdx.x + NT * r] = v[r];
-  float v1[RR], v2[RR];
-  if constexpr (Q) load_cols<NT>(a.s_rot, v1);  // (S̃ᵀ acc_sgn)_j = Σ_i S̃[i][j] acc_sgn_i
-  load_cols<NT>(a.pi, v2);                     // (Πᵀ y)_i = Σ_j Π[j][i] y_j
   cta_sync_n<NT>();
   if constexpr (Q) {
     cols_times<GP, NT>(v1, acc + kD, 2 * kD, red);
@@ -453,7 +463,6 @@ __device__ __noinline__ void unit_merge(const TcArgs& a, int head0, int ns, floa
     const float l = ml[2 * (e >> 7) + 1];
     a.out[(size_t)head0 * kD + e] = sum_groups<NG>(red, e, GP * kD) * (l > 0.f ? 1.f / l : 0.f);
   }
-  cta_sync_n<NT>();
 }
 
 // Per-unit query table, built once per (batch, kv head) unit by
@@ -502,7 +511,6 @@ __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs 
   float *qr, *sr;
   unit_query_prep<GP, NT, Q>(a, head0, scr, &qr, &sr);  // its first barrier publishes the lines above
   // (past the grid dependency wait inside unit_query_prep: the workspace is ours)
-  if (threadIdx.x == 0) a.arrivals[u] = 0u;
   // thread group grp = threadIdx / 128 takes heads grp and grp + 4; thread j its coordinate j:
   // word kw, half e16, bit L = 4·tq + jj of the half -> K-step (P·4 + kw)·2 + jj / 2,
   // k-slot 8·(jj % 2) + 2·tq + e16
@@ -599,7 +607,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   using Sh = Shape<W, GP, Q>;
   constexpr int NPM = Sh::NPM, NP = Sh::NP, GH = Sh::GH;
   constexpr int NT = kThreads;
-  static_assert(Scratch<GP, NT>::kMerge * 4 <= Sh::kOffMisc - Sh::kOffBK, "merge scratch exceeds its region");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Misc* ms = reinterpret_cast<Misc*>(smem + Sh::kOffMisc);
@@ -681,6 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   // the query tables and arrival counters come from unit_table_kernel, which may
   // still be running (programmatic dependent launch): wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // unit_combine_kernel may be scheduled now: its CTAs take an SM as decode CTAs
+  // leave, load their matrices and wait for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;");
 
   // key words: one multiply moves bits 4·tig .. 4·tig + 3 (and 16 more) to 12..15
   const uint32_t kmul = 1u << (12 - 4 * tig);
@@ -1018,19 +1028,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       }
       cta_sync_n<NT>();
     }
-    // ---- the last CTA of the unit to hand in its partial merges them all
-    __threadfence();
-    cta_sync_n<NT>();
-    if (threadIdx.x == 0) {
-      const int64_t nct = owner((sg.u + 1) * a.tpu - 1, a.total, C) - owner(sg.u * a.tpu, a.total, C) + 1;
-      ms->last = atomicAdd(a.arrivals + sg.u, 1u) == (unsigned)(nct - 1);
-      if (ms->last) __threadfence();
-    }
-    cta_sync_n<NT>();
-    if (ms->last) {
-      const int ns = (int)(owner((sg.u + 1) * a.tpu - 1, a.total, C) - owner(sg.u * a.tpu, a.total, C) + 1);
-      unit_merge<GP, NT, Q>(a, head0, ns, reinterpret_cast<float*>(smem + Sh::kOffBK));
-    }
   }
   // no copy of this CTA may be in flight when it exits
   if (threadIdx.x == 0)
@@ -1080,8 +1077,8 @@ size_t decode_tc_table_bytes(int w, int G, int m) {
 
 tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype, const tq_records* K,
                            const tq_records* V, const int32_t* ctx_len, int B, int Hq, int Hkv, int64_t ctx_stride,
-                           float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
-                           cudaStream_t stream, const int32_t* pages) {
+                           float scale, float* part, int smax, uint8_t* tables, float* out, cudaStream_t stream,
+                           const int32_t* pages) {
   TcArgs a{};
   a.pages = pages;
   a.max_pages = ctx_stride / kTile;
@@ -1095,7 +1092,6 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
   a.q_bf16 = q_dtype == TQ_BF16;
   a.pi = plan->pi; a.pi_t = plan->pi_t; a.s_rot = plan->s_rot; a.s_rot_t = plan->s_rot_t;
   a.tables = tables;
-  a.arrivals = arrivals;
   a.out = out;
   a.walsh = plan->walsh;
   a.scale = scale;
@@ -1108,15 +1104,17 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
   if (!a.fault) return TQ_ERR_CUDA;
   const int units = B * Hkv;
   const int grid = decode_tc_ctas(units, a.tpu);
-  // the per-unit query tables (and zeroed arrival counters), then the decode
-  auto go = [&](auto table_kern, int table_smem, auto kern, int smem) -> tq_status {
+  // the per-unit query tables, the decode, then the per-unit merge
+  auto go = [&](auto table_kern, int table_smem, auto kern, int smem, auto comb_kern, int comb_smem) -> tq_status {
     if (cudaFuncSetAttribute(table_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, table_smem) != cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(comb_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, comb_smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    // both as programmatic dependent launches: the table kernel's matrix loads
-    // overlap the previous kernel, the decode kernel's prologue and first copies
-    // overlap the table kernel (each waits for its predecessor before it reads
-    // what that one wrote)
+    // all three as programmatic dependent launches: the table kernel's matrix
+    // loads overlap the previous kernel, the decode kernel's prologue and first
+    // copies overlap the table kernel, the merge's matrix loads overlap the
+    // decode's tail (each waits for its predecessor before it reads what that
+    // one wrote)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1132,11 +1130,14 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
     cfg.gridDim = dim3(grid);
     cfg.dynamicSmemBytes = smem;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TQ_ERR_CUDA;
+    cfg.gridDim = dim3(units);
+    cfg.dynamicSmemBytes = comb_smem;
+    if (cudaLaunchKernelEx(&cfg, comb_kern, a, grid) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
   };
 #define TQ_DECODE_TC_GO(W_, GP_, Q_)                                                                \
   go(unit_table_kernel<W_, GP_, Q_>, table_smem_bytes<W_, GP_, Q_>(), decode_tc_kernel<W_, GP_, Q_>, \
-     smem_bytes<W_, GP_, Q_>())
+     smem_bytes<W_, GP_, Q_>(), unit_combine_kernel<GP_, Q_>, 16 + Scratch<GP_, kThreads>::kMerge * 4)
   const bool g8 = a.G > 4;
   if (plan->m > 0) {
     switch (plan->w) {

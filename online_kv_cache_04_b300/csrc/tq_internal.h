@@ -82,8 +82,8 @@ size_t decode_tc_table_bytes(int w, int G, int m);
 // ([B*Hkv][ctx_stride / 256] page of each 256-token tile; ctx_stride % 256 == 0).
 tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype, const tq_records* K,
                            const tq_records* V, const int32_t* ctx_len, int B, int Hq, int Hkv, int64_t ctx_stride,
-                           float scale, float* part, int smax, uint8_t* tables, unsigned* arrivals, float* out,
-                           cudaStream_t stream, const int32_t* pages = nullptr);
+                           float scale, float* part, int smax, uint8_t* tables, float* out, cudaStream_t stream,
+                           const int32_t* pages = nullptr);
 
 // SIMT quantizer over a column subset (tq_quantize.cu): element j of row r is
 // x[r][cols[j]] for j < plan->d (cols: device int32); rows [out_offset,
