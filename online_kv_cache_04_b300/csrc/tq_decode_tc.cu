@@ -108,6 +108,14 @@ constexpr uint32_t kSignMask = 0x80008000u, kSignBase = 0x3C003C00u;
 // The sign kind's mask and base in registers (loaded from constant memory):
 // with both in registers the operand is a single three-input logic op.
 __constant__ uint32_t c_ops[2] = {kSignMask, kSignBase};
+// per quad index t: the key multiplier 2^(12-4t) and the value multipliers
+// 2^(15-4t-j), read from constant memory so that the moves stay integer
+// multiplies (FMA pipe) rather than shifts on the busier integer pipe
+__constant__ uint32_t c_kmul[4] = {4096u, 256u, 16u, 1u};
+__constant__ uint32_t c_vmul[4][4] = {{32768u, 16384u, 8192u, 4096u},
+                                      {2048u, 1024u, 512u, 256u},
+                                      {128u, 64u, 32u, 16u},
+                                      {8u, 4u, 2u, 1u}};
 struct SignKind {
   uint32_t m, b;
   __device__ __forceinline__ SignKind() : m(c_ops[0]), b(c_ops[1]) {}
@@ -120,7 +128,7 @@ struct SignKind {
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -693,9 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   asm volatile("griddepcontrol.launch_dependents;");
 
   // key words: one multiply moves bits 4·tig .. 4·tig + 3 (and 16 more) to 12..15
-  const uint32_t kmul = 1u << (12 - 4 * tig);
+  const uint32_t kmul = c_kmul[tig];
   // value words: bit 4·tig + jv (and 16 more) to bit 15 (and 31)
-  const uint32_t vm0 = 1u << (15 - 4 * tig), vm1 = vm0 >> 1, vm2 = vm0 >> 2, vm3 = vm0 >> 3;
+  const uint32_t vm0 = c_vmul[tig][0], vm1 = c_vmul[tig][1], vm2 = c_vmul[tig][2], vm3 = c_vmul[tig][3];
   const SignKind sk;
   const uint8_t* BK = smem + Sh::kOffBK;
   float cf[NPM];
@@ -758,7 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         const uint8_t* stg = smem + Sh::kOffRing + (int)(gc & (kStages - 1)) * Sh::kStage;
         const uint4* kq = reinterpret_cast<const uint4*>(stg + Sh::kOffKIdx);  // token t, plane P: kq[t·W + P]
         const uint4* sq = reinterpret_cast<const uint4*>(stg + Sh::kOffKSgn);  // token t: sq[t]
-        float acc[2][2][GH][4];  // [score tile][part][head tile][fragment]
+        // [score tile][part][head tile][fragment], one chain per K-substep
+        float acc[2][2][GH][4], acc2[2][2][GH][4];
 #pragma unroll
         for (int st = 0; st < 2; ++st)
 #pragma unroll
@@ -766,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 #pragma unroll
             for (int ht = 0; ht < GH; ++ht)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) acc[st][pt][ht][e] = 0.f;
+              for (int e = 0; e < 4; ++e) acc[st][pt][ht][e] = acc2[st][pt][ht][e] = 0.f;
 #pragma unroll
         for (int P = 0; P < NP; ++P) {
           const int part = P < NPM ? 0 : 1;
@@ -801,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
               for (int st = 0; st < 2; ++st) {
                 const uint32_t u0 = u[st][0], u1 = u[st][1];
                 mma_f16(acc[st][part][ht], u0 & kK12, u1 & kK12, u0 & kK13, u1 & kK13, b0.x, b0.y);
-                mma_f16(acc[st][part][ht], u0 & kK14, u1 & kK14, sk(u0), sk(u1), b1.x, b1.y);
+                mma_f16(acc2[st][part][ht], u0 & kK14, u1 & kK14, sk(u0), sk(u1), b1.x, b1.y);
               }
             }
           }
@@ -828,8 +837,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             const float lv = __log2f(fmaxf(fmaxf(vnc[st][r], vrc[st][r]), 0x1p-32f));
 #pragma unroll
             for (int hh = 0; hh < GH; ++hh) {
-              const float dm = acc[st][0][hh][2 * r] + acc[st][0][hh][2 * r + 1];
-              const float dq = acc[st][1][hh][2 * r] + acc[st][1][hh][2 * r + 1];
+              const float dm = (acc[st][0][hh][2 * r] + acc[st][0][hh][2 * r + 1]) +
+                               (acc2[st][0][hh][2 * r] + acc2[st][0][hh][2 * r + 1]);
+              const float dq = (acc[st][1][hh][2 * r] + acc[st][1][hh][2 * r + 1]) +
+                               (acc2[st][1][hh][2 * r] + acc2[st][1][hh][2 * r + 1]);
               const float sc = Q ? fmaf(knr, fmaf(A0[hh], dm, B0[hh]), krr * fmaf(A1[hh], dq, B1[hh]))
                                  : knr * fmaf(A0[hh], dm, B0[hh]);
               s2[st][hh][r] = (valid && 4 * hh + tig < a.G) ? sc : -INFINITY;
