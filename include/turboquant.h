@@ -111,8 +111,8 @@ typedef struct tq_plan {
  * m = 0 selects stage 1 alone ([memory-wall] §2 stage 1: the rotation and
  * the MSE-optimal codebook with all w bits, no QJL rows): records then hold
  * only indices and norms (their sgn and rnorm may be NULL), scores are
- * ||k|| <Π q, c[idx]> and values ||v|| Πᵀ c[idx].  Such plans run on the
- * general kernels, not the d = m = 128 tensor-core ones. */
+ * ||k|| <Π q, c[idx]> and values ||v|| Πᵀ c[idx].  At d = 128 such plans run
+ * on the tensor-core quantizer and decode like the two-stage ones. */
 size_t tq_plan_bytes(int d, int m, int w);
 
 /* Fill `plan` and the device buffer `dev` (bytes >= tq_plan_bytes) from the
@@ -267,6 +267,29 @@ tq_status tq_decode_attention_paged(const tq_plan* plan, const void* q, tq_dtype
 tq_status tq_append_kv_paged(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B,
                              int Hkv, const tq_records* K, const tq_records* V, int32_t* ctx_len,
                              const int32_t* pages, int max_pages, tq_stream stream);
+
+/* A whole decode step with the online append fused in ([memory-wall] §2:
+ * the quantizer runs per vector as tokens arrive; [efficiency] §四): the new
+ * key and value of every (b, h) are quantized exactly as tq_append_kv does
+ * and stored at token ctx_len[b], attention then runs over ctx_len[b] + 1
+ * tokens as tq_decode_attention does, and ctx_len[b] is advanced on the
+ * device.  On the tensor-core path (as tq_decode_attention's) the append
+ * happens inside the decode's own launches -- the per-(b, h) table kernel
+ * writes the new rows before the decode kernel copies any tile and the merge
+ * kernel advances ctx_len -- so a step is one call and no extra launch;
+ * other caches run tq_append_kv's two launches first.  Arguments as
+ * tq_append_kv (k_new, v_new, kv_dtype, ctx_len, read and advanced) and
+ * tq_decode_attention (q, out, workspace of tq_decode_workspace_size with
+ * this ctx_stride); pages: NULL for contiguous caches, else the page table of
+ * tq_decode_attention_paged ([B*Hkv][ctx_stride / 256], ctx_stride a multiple
+ * of 256).  A row whose cache is full or whose length is negative is neither
+ * written nor advanced (fault bit 3) and attends over its ctx_len[b] tokens.
+ * Errors: those of tq_append_kv and tq_decode_attention. */
+tq_status tq_decode_attention_append(const tq_plan* plan, const void* q, tq_dtype q_dtype, const void* k_new,
+                                     const void* v_new, tq_dtype kv_dtype, int B, int Hq, int Hkv,
+                                     const tq_records* K, const tq_records* V, int32_t* ctx_len, int64_t ctx_stride,
+                                     const int32_t* pages, float scale, float* out, void* workspace,
+                                     size_t ws_bytes, tq_stream stream);
 
 /* Attention logits alone (the quantity the H100 timings of [efficiency] §四
  * and [memory-wall] §2 measure): scores[b][g][t] = s_{g,t} as above for

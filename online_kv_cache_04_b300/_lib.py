@@ -105,6 +105,10 @@ _SIGNATURES = {
     "tq_append_kv_paged": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, _vp, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.POINTER(tq_records), ctypes.POINTER(tq_records), _vp,
                                           _vp, ctypes.c_int, _vp]),
+    "tq_decode_attention_append": (ctypes.c_int, [ctypes.POINTER(tq_plan), _vp, ctypes.c_int, _vp, _vp, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(tq_records),
+                                                  ctypes.POINTER(tq_records), _vp, ctypes.c_int64, _vp, ctypes.c_float,
+                                                  _vp, _vp, ctypes.c_size_t, _vp]),
     "tq_fault_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -350,6 +354,26 @@ def tq_decode_attention_paged(plan, q, K, V, ctx_len, pages, Hkv, out, workspace
         plan.ref, q.data_ptr(), _dtype_code(q), B, Hq, Hkv, K.ref, V.ref, ctx_len.data_ptr(), pages.data_ptr(),
         pages.shape[-1], float(scale), out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_decode_attention_append(plan, q, k_new, v_new, K, V, ctx_len, ctx_stride, Hkv, out, workspace, pages=None,
+                               scale=0.0, stream=None):
+    """One decode step with the append fused in: store k_new, v_new ([B, Hkv, d]) at token ctx_len[b], attend over
+    ctx_len[b] + 1 tokens, advance ctx_len.  pages: None (contiguous caches) or [B*Hkv, ctx_stride / 256] int32."""
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype or k_new.dim() != 3:
+        raise ValueError("tq_decode_attention_append: k_new and v_new must both be [B, Hkv, d] of one dtype")
+    if not (k_new.is_contiguous() and v_new.is_contiguous()):
+        raise ValueError("tq_decode_attention_append: k_new and v_new must be contiguous")
+    _on_device("tq_decode_attention_append", q, k_new, v_new, out, workspace)
+    _lengths("tq_decode_attention_append", ctx_len)
+    _records_on_device("tq_decode_attention_append", K, V)
+    if pages is not None:
+        _on_device("tq_decode_attention_append", pages)
+    B, Hq, _ = q.shape
+    _check("tq_decode_attention_append", load().tq_decode_attention_append(
+        plan.ref, q.data_ptr(), _dtype_code(q), k_new.data_ptr(), v_new.data_ptr(), _dtype_code(k_new), B, Hq, Hkv,
+        K.ref, V.ref, ctx_len.data_ptr(), ctx_stride, None if pages is None else pages.data_ptr(), float(scale),
+        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def tq_append_kv_paged(plan, k_new, v_new, K, V, ctx_len, pages, stream=None):

@@ -243,6 +243,13 @@ tq_status append_impl(const tq_plan* plan, const void* k_new, const void* v_new,
 
 }  // namespace
 
+tq_status tq::append_kv(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B, int Hkv,
+                        const tq_records* K, const tq_records* V, int32_t* ctx_len, int64_t ctx_stride,
+                        cudaStream_t stream, const int32_t* pages) {
+  return append_impl(plan, k_new, v_new, dtype, B, Hkv, K, V, ctx_len, ctx_stride,
+                     reinterpret_cast<tq_stream>(stream), pages);
+}
+
 extern "C" tq_status tq_append_kv(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B,
                                   int Hkv, const tq_records* K, const tq_records* V, int32_t* ctx_len,
                                   int64_t ctx_stride, tq_stream stream) {

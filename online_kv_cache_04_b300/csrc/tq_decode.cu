@@ -503,10 +503,13 @@ extern "C" tq_status tq_decode_workspace_size(const tq_plan* plan, int B, int Hq
 
 namespace {
 
+// app: the fused append of tq_decode_attention_append (NULL: none).  The
+// tensor-core path quantizes the new rows inside its launch sequence; the
+// general path runs tq_append_kv's launches first.
 tq_status decode_impl(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,
                       const tq_records* K, const tq_records* V, const int32_t* ctx_len, int64_t ctx_stride,
                       float scale, float* out, void* workspace, size_t ws_bytes, tq_stream stream,
-                      const int32_t* pages) {
+                      const int32_t* pages, const tq::TcAppend* app = nullptr) {
   DecodeShape s;
   if (!fill_shape(plan, B, Hq, Hkv, ctx_stride, &s)) return TQ_ERR_ARG;
   tq_status st = TQ_OK;
@@ -533,8 +536,12 @@ tq_status decode_impl(const tq_plan* plan, const void* q, tq_dtype q_dtype, int 
     uint8_t* ws8 = static_cast<uint8_t*>(workspace);
     return tq::launch_decode_tc(plan, q, q_dtype, K, V, ctx_len, B, Hq, Hkv, ctx_stride, sc,
                                 reinterpret_cast<float*>(ws8 + l.part), tc_slots(s), ws8 + l.tables, out, cs,
-                                pages);
+                                pages, app);
   }
+  if (app != nullptr &&
+      (st = tq::append_kv(plan, app->k_new, app->v_new, app->bf16 ? TQ_BF16 : TQ_F32, B, Hkv, K, V, app->ctx_len,
+                          ctx_stride, cs, pages)) != TQ_OK)
+    return st;
   if ((st = launch_prep(plan, q, q_dtype, s, qt, stv, cs)) != TQ_OK) return st;
   SplitArgs a{};
   a.s = s;
@@ -587,6 +594,21 @@ extern "C" tq_status tq_decode_attention_paged(const tq_plan* plan, const void* 
   if (pages == nullptr || !tq::aligned16(pages) || max_pages < 1) return TQ_ERR_ARG;
   return decode_impl(plan, q, q_dtype, B, Hq, Hkv, K, V, ctx_len, int64_t(max_pages) * kPage, scale, out, workspace,
                      ws_bytes, stream, pages);
+}
+
+extern "C" tq_status tq_decode_attention_append(const tq_plan* plan, const void* q, tq_dtype q_dtype,
+                                                const void* k_new, const void* v_new, tq_dtype kv_dtype, int B,
+                                                int Hq, int Hkv, const tq_records* K, const tq_records* V,
+                                                int32_t* ctx_len, int64_t ctx_stride, const int32_t* pages,
+                                                float scale, float* out, void* workspace, size_t ws_bytes,
+                                                tq_stream stream) {
+  if (!k_new || !v_new || !tq::aligned16(k_new) || !tq::aligned16(v_new) || (kv_dtype != TQ_F32 && kv_dtype != TQ_BF16))
+    return TQ_ERR_ARG;
+  if (!K || !V || K->idx == V->idx || (K->sgn && K->sgn == V->sgn) || K->norm == V->norm) return TQ_ERR_ARG;
+  if (pages != nullptr && (!tq::aligned16(pages) || ctx_stride % kPage != 0)) return TQ_ERR_ARG;
+  const tq::TcAppend app{k_new, v_new, kv_dtype == TQ_BF16, ctx_len};
+  return decode_impl(plan, q, q_dtype, B, Hq, Hkv, K, V, ctx_len, ctx_stride, scale, out, workspace, ws_bytes, stream,
+                     pages, &app);
 }
 
 extern "C" tq_status tq_decode_scores(const tq_plan* plan, const void* q, tq_dtype q_dtype, int B, int Hq, int Hkv,

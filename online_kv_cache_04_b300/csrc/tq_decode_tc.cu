@@ -99,6 +99,7 @@ constexpr float kWS = 256.f;                           // attention weights carr
 constexpr int kBMaxExp = 15;                           // query operand entries stay below 2^15
 constexpr unsigned kFaultDecode = 2u;
 constexpr unsigned kFaultPage = 16u;                   // a page-table entry outside the record arrays
+constexpr unsigned kFaultAppend = 8u;                  // fused append: a full cache or a negative length
 
 // Key operand kinds after the move to bits 12..15: exponent bits over a zero
 // base (values 2^-11, 2^-7, 2 when set, 0 when clear), and the sign of 1.0.
@@ -151,8 +152,8 @@ __device__ __forceinline__ void cta_sync_n() {
 }
 
 struct TcArgs {
-  const uint32_t *kidx, *ksgn, *vidx, *vsgn;
-  const float *knorm, *krnorm, *vnorm, *vrnorm;
+  uint32_t *kidx, *ksgn, *vidx, *vsgn;  // written only by the fused append
+  float *knorm, *krnorm, *vnorm, *vrnorm;
   const int32_t* ctx_len;
   int64_t ctx_stride;
   const int32_t* pages;  // paged caches: [B*Hkv][max_pages] page of each 256-token tile (NULL: contiguous rows)
@@ -162,6 +163,15 @@ struct TcArgs {
   int q_bf16;
   const float *pi, *pi_t, *s_rot, *s_rot_t;  // Π, Πᵀ, S̃ = S Πᵀ, S̃ᵀ (128 x 128, row-major)
   const float* walsh;
+  // Fused append (append != 0): the step's new key and value of every unit
+  // ([B*Hkv][128], bf16 or fp32) go to token ctx_len[b] of the caches, written
+  // by unit_table_kernel before the decode reads them; the decode attends over
+  // ctx_len[b] + 1 tokens and unit_combine_kernel advances ctx_len[b].  A row
+  // with a full cache or a negative length is left alone (kFaultAppend).
+  int append, new_bf16;
+  const void *k_new, *v_new;
+  int32_t* ctx_len_mut;      // the same array as ctx_len
+  const float *centroids, *bounds;
   float scale, alpha;
   float* part;       // [B*Hq][smax][2 + 2*128]
   int smax;
@@ -175,6 +185,14 @@ struct TcArgs {
 // CTA that owns flat tile f when `total` tiles are cut into `ctas` even ranges.
 __host__ __device__ inline int64_t owner(int64_t f, int64_t total, int64_t ctas) {
   return ((f + 1) * ctas - 1) / total;
+}
+
+// Token count of batch row b that this launch attends over: ctx_len[b] (0 if
+// negative, at most ctx_stride), plus the appended token when there is one.
+__device__ __forceinline__ int ctx_of(const TcArgs& a, int b) {
+  const int L = __ldg(a.ctx_len + b);
+  const bool app = a.append && L >= 0 && L < a.ctx_stride;
+  return (int)min((int64_t)max(L, 0) + (app ? 1 : 0), a.ctx_stride);
 }
 
 // Score columns: head g sits in head tile g / 4, columns 2·(g % 4) (hi) and
@@ -255,7 +273,7 @@ __device__ __forceinline__ Seg segment_at(const TcArgs& a, int64_t f, int64_t f1
   const int64_t fe = min(f1, (s.u + 1) * a.tpu);
   *next = fe;
   const int b = (int)(s.u / a.Hkv);
-  s.L = (int)min((int64_t)max(__ldg(a.ctx_len + b), 0), a.ctx_stride);
+  s.L = ctx_of(a, b);
   const int64_t nvalid = (s.L + kTile - 1) / kTile;
   const int64_t tend = s.t0 + (fe - f);
   s.n = (int)max((int64_t)0, min(tend, nvalid) - s.t0);
@@ -271,6 +289,7 @@ template <int GP, int NT>
 struct Scratch {
   static constexpr int NG = NT / 128;                                        // thread groups
   static constexpr int kPrep = (3 + NG) * GP * kD;                           // q, NG partial sums, Πq, Sq
+  static constexpr int kAppend = 2 * kD + NG * 2 * kD + 16;                  // see append_step
   static constexpr int kMerge = GP * (2 + kMaxCtas + 2 * kD + NG * kD + kD);  // see unit_combine_kernel
 };
 
@@ -311,12 +330,112 @@ __device__ __forceinline__ float sum_groups(const float* red, int e, int stride)
   return s;
 }
 
+// Fused append of unit u: its new key (into K, row layout) and new value (into
+// V, 32-row blocks) quantized at token L = ctx_len[b] by the two stages of
+// "谷歌TurboQuant如何绕过内存墙？" §2 -- n = ||x||, u = Π x / n, the bucket
+// index against the Lloyd-Max bounds, ρ = u - c[idx], σ = sign(S Πᵀ ρ) with
+// sign(0) = +1, ||r|| = n ||ρ||, the zero vector stored as u = 0, r = 0 --
+// with the columns of Πᵀ (v1) and S̃ᵀ (v2) this thread already holds.  All NT
+// threads; thread t < 256 finishes coordinate t % 128 of vector t / 128, so a
+// warp ballot forms one packed row word.  `scr`: Scratch::kAppend floats.
+template <int W, int NT, bool Q>
+__device__ __forceinline__ void append_step(const TcArgs& a, int u, const float (&v1)[128 * 128 / NT],
+                                            const float (&v2)[128 * 128 / NT], float* scr) {
+  constexpr int NG = NT / 128;
+  const int b = u / a.Hkv;
+  const int L = __ldg(a.ctx_len + b);
+  if (L < 0 || L >= a.ctx_stride) {  // uniform over the CTA
+    if (threadIdx.x == 0) atomicOr(a.fault, kFaultAppend);
+    return;
+  }
+  int64_t row = (int64_t)u * a.ctx_stride + L;
+  if (a.pages != nullptr) {  // the page holding token L
+    const int64_t pg = __ldg(a.pages + (int64_t)u * a.max_pages + L / kTile);
+    if (pg < 0 || pg >= a.npages) {
+      if (threadIdx.x == 0) atomicOr(a.fault, kFaultPage);
+      return;
+    }
+    row = pg * kTile + L % kTile;
+  }
+  float* xs = scr;                 // [2][128] the new vectors, then ρ
+  float* red = xs + 2 * kD;        // [NG][2][128] partial sums
+  float* wsum = red + NG * 2 * kD; // [2 vectors][4 warps] partial ||x||², then ||ρ||²
+  const int t = threadIdx.x, vec = t >> 7, j = t & (kD - 1), lane = t & 31, wv = (t >> 5) & 3;
+  const bool mine = t < 2 * kD;
+  float x = 0.f;
+  if (mine) {
+    const size_t off = (size_t)u * kD + j;
+    const void* src = vec ? a.v_new : a.k_new;
+    x = a.new_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(src)[off])
+                   : reinterpret_cast<const float*>(src)[off];
+    xs[t] = x;
+    float s2 = x * x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    if (lane == 0) wsum[vec * 4 + wv] = s2;
+  }
+  cta_sync_n<NT>();
+  cols_times<2, NT>(v1, xs, kD, red);  // (Π x)_j
+  cta_sync_n<NT>();
+  float n = 0.f, rho = 0.f;
+  int idx = 0;
+  if (mine) {
+    n = sqrtf((wsum[vec * 4] + wsum[vec * 4 + 1]) + (wsum[vec * 4 + 2] + wsum[vec * 4 + 3]));
+    const float uj = n > 0.f ? sum_groups<NG>(red, t, 2 * kD) / n : 0.f;
+#pragma unroll
+    for (int k = 0; k < (1 << W) - 1; ++k) idx += __ldg(a.bounds + k) < uj ? 1 : 0;
+    rho = n > 0.f ? uj - __ldg(a.centroids + idx) : 0.f;
+  }
+  cta_sync_n<NT>();  // everyone is through with xs and wsum
+  if (mine) {
+    xs[t] = rho;
+    float r2 = rho * rho;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r2 += __shfl_xor_sync(0xffffffffu, r2, o);
+    if (lane == 0) wsum[vec * 4 + wv] = r2;
+    const uint32_t bbit = 1u << tq::block32_bit((int)(row & 31));
+#pragma unroll
+    for (int p = 0; p < W; ++p) {
+      const bool bit = (idx >> p) & 1;
+      const uint32_t word = __ballot_sync(0xffffffffu, bit);
+      if (vec == 0) {
+        if (lane == 0) a.kidx[row * (4 * W) + p * 4 + (j >> 5)] = word;
+      } else {
+        uint32_t* wp = a.vidx + (row >> 5) * (W * kD) + p * kD + j;
+        *wp = bit ? (*wp | bbit) : (*wp & ~bbit);
+      }
+    }
+    if (j == 0) (vec ? a.vnorm : a.knorm)[row] = n;
+  }
+  if constexpr (Q) {
+    cta_sync_n<NT>();
+    cols_times<2, NT>(v2, xs, kD, red);  // (S̃ ρ)_i
+    cta_sync_n<NT>();
+    if (mine) {
+      const bool pos = sum_groups<NG>(red, t, 2 * kD) >= 0.f;
+      const uint32_t bbit = 1u << tq::block32_bit((int)(row & 31));
+      const uint32_t word = __ballot_sync(0xffffffffu, pos);
+      if (vec == 0) {
+        if (lane == 0) a.ksgn[row * 4 + (j >> 5)] = word;
+      } else {
+        uint32_t* wp = a.vsgn + (row >> 5) * kD + j;
+        *wp = pos ? (*wp | bbit) : (*wp & ~bbit);
+      }
+      if (j == 0) {
+        const float r2 = (wsum[vec * 4] + wsum[vec * 4 + 1]) + (wsum[vec * 4 + 2] + wsum[vec * 4 + 3]);
+        (vec ? a.vrnorm : a.krnorm)[row] = n * sqrtf(r2);
+      }
+    }
+  }
+  cta_sync_n<NT>();
+}
+
 // Query transform of the unit's heads head0 .. head0 + G - 1 ("TurboQuant 与 AI
 // 效率革命" §三: the estimator takes Π q and S q): on return qr[g][j] = (Π q_g)_j
 // and sr[g][i] = (S̃ Π q_g)_i = (S q_g)_i, zero for g >= G.  All NT threads; one
 // round of global loads (q and both matrices).
-template <int GP, int NT, bool Q>
-__device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* scr, float** qr_out,
+template <int W, int GP, int NT, bool Q>
+__device__ __noinline__ void unit_query_prep(const TcArgs& a, int u, int head0, float* scr, float** qr_out,
                                              float** sr_out) {
   constexpr int NG = NT / 128, R = 128 * 128 / NT;
   float* qs = scr;
@@ -361,6 +480,8 @@ __device__ __noinline__ void unit_query_prep(const TcArgs& a, int head0, float* 
     for (int e = threadIdx.x; e < GP * kD; e += NT) sr[e] = 0.f;
   }
   cta_sync_n<NT>();
+  // the fused append reuses the matrix columns this thread holds
+  if (a.append) append_step<W, NT, Q>(a, u, v1, v2, sr + GP * kD);
   *qr_out = qr;
   *sr_out = sr;
 }
@@ -389,6 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1) unit_combine_kernel(const TcArgs 
   // the partials are the decode kernel's: wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
+  // fused append: every read of ctx_len[b] is done; its first unit advances it
+  if (a.append && h == 0 && threadIdx.x == 0) {
+    const int L = a.ctx_len_mut[b];
+    if (L >= 0 && L < a.ctx_stride) a.ctx_len_mut[b] = L + 1;
+  }
   float* ml = scr;                      // [GP][2] reference max, Σ w·l
   float* wgt = ml + 2 * GP;             // [GP][kMaxCtas] slot weights
   float* acc = wgt + GP * kMaxCtas;     // [GP][256] merged acc_rot | acc_sgn
@@ -491,7 +617,8 @@ struct TableState {
 };
 template <int W, int GP, bool Q>
 constexpr int table_smem_bytes() {
-  return 1024 + Shape<W, GP, Q>::kBKBytes + Scratch<GP, kTableThreads>::kPrep * 4 + (int)sizeof(TableState);
+  return 1024 + Shape<W, GP, Q>::kBKBytes + (Scratch<GP, kTableThreads>::kPrep + Scratch<GP, kTableThreads>::kAppend) * 4 +
+         (int)sizeof(TableState);
 }
 
 // One CTA per unit: q̃ = Π q and s̃ = S q of its G heads, then the table.  A key
@@ -510,14 +637,15 @@ __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* BK = smem;
   float* scr = reinterpret_cast<float*>(smem + Sh::kBKBytes);
-  TableState* ts = reinterpret_cast<TableState*>(smem + Sh::kBKBytes + Scratch<GP, NT>::kPrep * 4);
+  TableState* ts = reinterpret_cast<TableState*>(smem + Sh::kBKBytes +
+                                                 (Scratch<GP, NT>::kPrep + Scratch<GP, NT>::kAppend) * 4);
   const int u = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = u / a.Hkv, h = u - b * a.Hkv, head0 = b * a.Hq + h * a.G;
   if (threadIdx.x < NPM) ts->cf[threadIdx.x] = __ldg(a.walsh + (threadIdx.x < W ? (1 << threadIdx.x) : 7));
   if (threadIdx.x < 16) ts->amax[threadIdx.x >> 3][threadIdx.x & 7] = 0.f;
   for (int e = threadIdx.x; e < Sh::kBKBytes / 16; e += NT) reinterpret_cast<uint4*>(BK)[e] = make_uint4(0, 0, 0, 0);
   float *qr, *sr;
-  unit_query_prep<GP, NT, Q>(a, head0, scr, &qr, &sr);  // its first barrier publishes the lines above
+  unit_query_prep<W, GP, NT, Q>(a, u, head0, scr, &qr, &sr);  // its first barrier publishes the lines above
   // (past the grid dependency wait inside unit_query_prep: the workspace is ours)
   // thread group grp = threadIdx / 128 takes heads grp and grp + 4; thread j its coordinate j:
   // word kw, half e16, bit L = 4·tq + jj of the half -> K-step (P·4 + kw)·2 + jj / 2,
@@ -648,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   // consumed by warp 0 and issued < done + kStages.  The cursor (cur, cu, ct,
   // cL) walks flat tiles: unit cu, tile ct in it, context length cL of the unit.
   int64_t issued = 0, cur = f0, cu = f0 / a.tpu, ct = f0 - cu * a.tpu;
-  int cL = (int)min((int64_t)max(__ldg(a.ctx_len + cu / a.Hkv), 0), a.ctx_stride);
+  int cL = ctx_of(a, (int)(cu / a.Hkv));
   auto issue_upto = [&](int64_t done) {
     const uint32_t sbase = smem_u32(smem);
     while (issued < done + kStages && cur < f1 && !*abort_flag) {
@@ -656,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         cur += a.tpu - ct;
         ++cu;
         ct = 0;
-        if (cur < f1) cL = (int)min((int64_t)max(__ldg(a.ctx_len + cu / a.Hkv), 0), a.ctx_stride);
+        if (cur < f1) cL = ctx_of(a, (int)(cu / a.Hkv));
         continue;
       }
       int64_t row0 = cu * a.ctx_stride + ct * kTile;
@@ -692,10 +820,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       }
     }
   };
-  if (threadIdx.x == 0) issue_upto(0);
-  // the query tables and arrival counters come from unit_table_kernel, which may
-  // still be running (programmatic dependent launch): wait for it to complete
+  // the first copies overlap unit_table_kernel, unless it appends to the caches
+  if (threadIdx.x == 0 && !a.append) issue_upto(0);
+  // the query tables come from unit_table_kernel, which may still be running
+  // (programmatic dependent launch): wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0 && a.append) issue_upto(0);
   // unit_combine_kernel may be scheduled now: its CTAs take an SM as decode CTAs
   // leave, load their matrices and wait for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;");
@@ -1089,8 +1219,17 @@ size_t decode_tc_table_bytes(int w, int G, int m) {
 tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype, const tq_records* K,
                            const tq_records* V, const int32_t* ctx_len, int B, int Hq, int Hkv, int64_t ctx_stride,
                            float scale, float* part, int smax, uint8_t* tables, float* out, cudaStream_t stream,
-                           const int32_t* pages) {
+                           const int32_t* pages, const TcAppend* app) {
   TcArgs a{};
+  if (app != nullptr) {
+    a.append = 1;
+    a.k_new = app->k_new;
+    a.v_new = app->v_new;
+    a.new_bf16 = app->bf16;
+    a.ctx_len_mut = app->ctx_len;
+    a.centroids = plan->centroids;
+    a.bounds = plan->bounds;
+  }
   a.pages = pages;
   a.max_pages = ctx_stride / kTile;
   a.npages = std::min(K->capacity, V->capacity) / kTile;

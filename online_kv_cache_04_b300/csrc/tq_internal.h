@@ -80,10 +80,23 @@ int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas);
 size_t decode_tc_table_bytes(int w, int G, int m);
 // pages: NULL for contiguous units, else the page table of a paged cache
 // ([B*Hkv][ctx_stride / 256] page of each 256-token tile; ctx_stride % 256 == 0).
+// Fused append of the step's new keys and values (tq_decode_attention_append):
+// [B*Hkv][d] each, bf16 (bf16 != 0) or fp32; ctx_len is the decode's length
+// array, advanced on the device by the launch.
+struct TcAppend {
+  const void* k_new;
+  const void* v_new;
+  int bf16;
+  int32_t* ctx_len;
+};
 tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype, const tq_records* K,
                            const tq_records* V, const int32_t* ctx_len, int B, int Hq, int Hkv, int64_t ctx_stride,
                            float scale, float* part, int smax, uint8_t* tables, float* out, cudaStream_t stream,
-                           const int32_t* pages = nullptr);
+                           const int32_t* pages = nullptr, const TcAppend* app = nullptr);
+// tq_append_kv's two launches (tq_append.cu), for caches the fused path does not take.
+tq_status append_kv(const tq_plan* plan, const void* k_new, const void* v_new, tq_dtype dtype, int B, int Hkv,
+                    const tq_records* K, const tq_records* V, int32_t* ctx_len, int64_t ctx_stride,
+                    cudaStream_t stream, const int32_t* pages);
 
 // SIMT quantizer over a column subset (tq_quantize.cu): element j of row r is
 // x[r][cols[j]] for j < plan->d (cols: device int32); rows [out_offset,
