@@ -111,12 +111,16 @@ bool quantize_mma_supported(const tq_plan* plan, const tq_records* out);
 tq_status quantize_mma(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
                        const tq_records* out, int64_t row0, cudaStream_t st);
 
-// Tensor-core search scores (tq_search_tc.cu): d and m multiples of 128 (m may
-// be 0), records in TQ_LAYOUT_ROWS.  `table`: search_tc_table_bytes(plan, nq)
-// bytes, 16-byte aligned; scores [nq][n] as the SIMT score kernel writes them.
+// Tensor-core search with the selection fused in (tq_search_tc.cu): d and m
+// multiples of 128 (m may be 0), records in TQ_LAYOUT_ROWS, k <= 64.
+// `table`: search_tc_table_bytes(plan, nq) bytes, 16-byte aligned.  Writes,
+// per query, search_tc_vchunks(n, nq) lists of the k best (score desc, index
+// asc; index -1 for an empty entry) to cand_idx / cand_sc [nq][vchunks][k].
 bool search_tc_supported(const tq_plan* plan, const tq_records* recs);
 size_t search_tc_table_bytes(const tq_plan* plan, int nq);
+int search_tc_vchunks(int64_t n, int nq);
 tq_status launch_search_tc(const tq_plan* plan, const tq_records* recs, int64_t n, int nq, const float* qt,
-                           const float* st, void* table, float* scores, cudaStream_t stream);
+                           const float* st, void* table, int k, int32_t* cand_idx, float* cand_sc,
+                           cudaStream_t stream);
 
 }  // namespace tq

@@ -14,14 +14,19 @@
 //   every K-step, laid out as the mma.sync B fragments (f16 hi + lo pairs of
 //   -coef_P (Π q)_j / E0 and -(S q)_j / E1, E a power of two per query and
 //   part), and the per-query constants E0 and α·E1.
-// search_score_kernel: a CTA scores 128 vectors against 32 queries with
-//   mma.sync m16n8k16 f16.  The bits of a record word become exact ±1 f16
+// search_score_kernel: a CTA scores blocks of 128 vectors against 32 queries
+//   with mma.sync m16n8k16 f16, block after block (vector blocks blockIdx.x,
+//   + gridDim.x, ...).  The bits of a record word become exact ±1 f16
 //   operands in registers: one integer multiply moves bits L and 16 + L to the
 //   sign positions of an f16x2 register and one logic op fills in 1.0, so the
 //   operand is -s.  The query operand streams through shared memory in
 //   16 KiB chunks (bulk copies, two buffers); fp32 accumulators per part
-//   stay in registers; the epilogue scales by the record's norms and writes
-//   the score matrix that the selection kernels of tq_search.cu read.
+//   stay in registers.  The epilogue scales by the record's norms and keeps,
+//   per query, the k best (score desc, index asc) of every vector the CTA has
+//   seen: warp w owns the shared-memory lists of the CTA's queries 4w .. 4w + 3
+//   and merges each block's scores into them.  At the end the lists go to the workspace as candidates, which
+//   the merge kernel of tq_search.cu reduces to the k best: the nq x n score
+//   matrix is never written.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -42,6 +47,8 @@ constexpr int kChunkSteps = 2 * kChunkWords;
 constexpr int kFragBytes = 256;            // one (K-step, query group) B operand: 32 lanes x uint2
 constexpr int kChunkBytes = kChunkSteps * kTilesPerCta * kFragBytes;
 constexpr unsigned kFaultSearch = 4u;
+constexpr int kMaxK = 64;                  // list entries a warp keeps per query (two per lane)
+constexpr int kStagePitch = kRows + 1;     // floats per query row of the score staging area
 
 // Per lane q: 2^(3-q), 2^(7-q), 2^(11-q), 2^(15-q) (multiplier from constant
 // memory: the move stays an integer multiply on the FMA pipe).
@@ -61,7 +68,10 @@ struct SearchTcArgs {
   float alpha;
   __half* table;            // [ksteps][groups][8 n][4 quad][2 reg][2 half]
   float* consts;            // [nq][2]: E0, α E1
-  float* scores;            // [nq][n]
+  int k;                    // list length (1 .. kMaxK)
+  int vchunks;              // gridDim.x: CTAs along the vectors = candidate lists per query
+  int32_t* cand_idx;        // [nq][vchunks][k]
+  float* cand_sc;
   unsigned* fault;
 };
 
@@ -144,30 +154,38 @@ __global__ void __launch_bounds__(kThreads) search_table_kernel(SearchTcArgs a) 
   }
 }
 
-// CTA (vector block bx, query block by): rows v0 .. v0 + 127, query groups
-// 8·by .. 8·by + 7.  Warp wp takes rows v0 + 16 wp + (0..15): fragment row gq
-// is vector v0 + 16 wp + gq, row gq + 8 the vector eight further.
-__global__ void __launch_bounds__(kThreads) search_score_kernel(SearchTcArgs a) {
+// CTA (vector chunk bx, query block by): vector blocks bx, bx + gridDim.x, ...
+// of 128 rows each (rows v0 .. v0 + 127), query groups 8·by .. 8·by + 7.  Warp
+// wp takes rows v0 + 16 wp + (0..15): fragment row gq is vector v0 + 16 wp +
+// gq, row gq + 8 the vector eight further.
+__global__ void __launch_bounds__(kThreads, 2) search_score_kernel(SearchTcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* buf = smem;  // [2][kChunkSteps][kTilesPerCta][256 B]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * kChunkBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
-  const int64_t v0 = (int64_t)blockIdx.x * kRows;
   const int g0 = blockIdx.y * kTilesPerCta, ntl = min(kTilesPerCta, a.groups - g0);
   const int words_d = a.d / 32, words_m = a.m / 32;
   const int nchunks = (a.npm * words_d + words_m) / kChunkWords;
+  float* stage = reinterpret_cast<float*>(smem + 2 * kChunkBytes + 64);  // [32 queries][kStagePitch]
+  float* lsc = stage + 32 * kStagePitch;                                   // [32 queries][kMaxK] list scores
+  int32_t* lid = reinterpret_cast<int32_t*>(lsc + 32 * kMaxK);              // [32 queries][kMaxK] list indices
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&full[0]), 1);
     mbar_init(smem_u32(&full[1]), 1);
     fence_mbar_init();
   }
   __syncthreads();
-  // chunk c covers K-steps 8c .. 8c + 7; its operand for groups g0 .. g0 + ntl - 1
-  // is ntl contiguous 256-byte fragments per K-step in the table
-  auto issue = [&](int c) {
-    const uint32_t bar = smem_u32(&full[c & 1]);
+  const int64_t nblocks = (a.n + kRows - 1) / kRows;
+  const int64_t myblocks = blockIdx.x < nblocks ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int64_t total_chunks = myblocks * nchunks;  // over all of this CTA's vector blocks
+  // global chunk gc = (block iteration)·nchunks + c covers K-steps 8c .. 8c + 7;
+  // its operand for groups g0 .. g0 + ntl - 1 is ntl contiguous 256-byte
+  // fragments per K-step in the table
+  auto issue = [&](int64_t gc) {
+    const int c = (int)(gc % nchunks);
+    const uint32_t bar = smem_u32(&full[gc & 1]);
     mbar_arrive_expect_tx(bar, (uint32_t)(kChunkSteps * ntl * kFragBytes));
-    const uint32_t dst = smem_u32(buf + (c & 1) * kChunkBytes);
+    const uint32_t dst = smem_u32(buf + (gc & 1) * kChunkBytes);
     for (int s = 0; s < kChunkSteps; ++s) {
       const int64_t ks = (int64_t)kChunkSteps * c + s;
       bulk_load(dst + s * kTilesPerCta * kFragBytes, a.table + (ks * a.groups + g0) * (kFragBytes / 2),
@@ -175,23 +193,20 @@ __global__ void __launch_bounds__(kThreads) search_score_kernel(SearchTcArgs a) 
     }
   };
   if (threadIdx.x == 0) {
-    issue(0);
-    if (nchunks > 1) issue(1);
+    if (total_chunks > 0) issue(0);
+    if (total_chunks > 1) issue(1);
   }
-  const int64_t r0 = v0 + 16 * warp + gq, r1 = r0 + 8;
-  const bool ok0 = r0 < a.n, ok1 = r1 < a.n;
   const int wi = a.w * words_d;  // index words per record
-  float acc[2][kTilesPerCta][4];
-#pragma unroll
-  for (int p = 0; p < 2; ++p)
-#pragma unroll
-    for (int t = 0; t < kTilesPerCta; ++t)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[p][t][e] = 0.f;
   const uint32_t m15 = c_smul[tig][3], m11 = c_smul[tig][2], m7 = c_smul[tig][1], m3 = c_smul[tig][0];
   bool alive = true;
-  int nissued = nchunks > 1 ? 2 : 1;  // thread 0: chunks whose copies were started
-  int ndone = 0;                      // chunks whose copies this thread has seen land
+  int64_t nissued = total_chunks > 1 ? 2 : total_chunks;  // thread 0: chunks whose copies were started
+  int64_t ndone = 0;                                      // chunks whose copies this thread has seen land
+  // the k-best lists, in rank order; empty entries rank last
+  for (int e = threadIdx.x; e < 32 * kMaxK; e += kThreads) lsc[e] = -INFINITY, lid[e] = INT32_MAX;
+  float acc[2][kTilesPerCta][4];
+  int64_t r0 = 0, r1 = 0;
+  bool ok0 = false, ok1 = false;
+  int64_t gbase = 0;  // global chunk number of this block's chunk 0
   // one chunk into the accumulators of part PART (0: codebook planes, 1: QJL plane)
   auto chunk = [&](int c, auto part_tag) {
     constexpr int PART = decltype(part_tag)::value;
@@ -217,11 +232,12 @@ __global__ void __launch_bounds__(kThreads) search_score_kernel(SearchTcArgs a) 
       }
       x[r] = v;
     }
+    const int64_t gc = gbase + c;
     if (alive) {
-      alive = mbar_wait(smem_u32(&full[c & 1]), (uint32_t)((c >> 1) & 1), a.fault, kFaultSearch);
+      alive = mbar_wait(smem_u32(&full[gc & 1]), (uint32_t)((gc >> 1) & 1), a.fault, kFaultSearch);
       ndone += alive ? 1 : 0;
     }
-    const uint2* bfr = reinterpret_cast<const uint2*>(buf + (c & 1) * kChunkBytes);
+    const uint2* bfr = reinterpret_cast<const uint2*>(buf + (gc & 1) * kChunkBytes);
 #pragma unroll
     for (int kw = 0; kw < kChunkWords; ++kw) {
       const uint32_t w0 = kw == 0 ? x[0].x : kw == 1 ? x[0].y : kw == 2 ? x[0].z : x[0].w;
@@ -241,35 +257,102 @@ __global__ void __launch_bounds__(kThreads) search_score_kernel(SearchTcArgs a) 
       }
     }
     __syncthreads();  // every warp is done with this buffer
-    if (threadIdx.x == 0 && c + 2 < nchunks && alive) {
-      issue(c + 2);
-      nissued = c + 3;
+    if (threadIdx.x == 0 && gc + 2 < total_chunks && alive) {
+      issue(gc + 2);
+      nissued = gc + 3;
     }
   };
   const int ncb = a.npm * words_d / kChunkWords;  // codebook chunks; the QJL plane's follow
+  const int k = a.k;
 #pragma unroll 1
-  for (int c = 0; c < ncb; ++c) chunk(c, std::integral_constant<int, 0>{});
+  for (int64_t it = 0; it < myblocks; ++it) {
+    const int64_t v0 = ((int64_t)blockIdx.x + it * gridDim.x) * kRows;
+    gbase = it * nchunks;
+    r0 = v0 + 16 * warp + gq;
+    r1 = r0 + 8;
+    ok0 = r0 < a.n;
+    ok1 = r1 < a.n;
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+      for (int t = 0; t < kTilesPerCta; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[p][t][e] = 0.f;
 #pragma unroll 1
-  for (int c = ncb; c < nchunks; ++c) chunk(c, std::integral_constant<int, 1>{});
+    for (int c = 0; c < ncb; ++c) chunk(c, std::integral_constant<int, 0>{});
+#pragma unroll 1
+    for (int c = ncb; c < nchunks; ++c) chunk(c, std::integral_constant<int, 1>{});
+    // scores of the block: column pair (hi, lo) 2·tig of tile t is query
+    // 4 (g0 + t) + tig, staged as [4t + tig][vector - v0] (-inf past n)
+    const float nv0 = ok0 ? __ldg(a.norm + r0) : 0.f, nv1 = ok1 ? __ldg(a.norm + r1) : 0.f;
+    const float rv0 = ok0 && a.m > 0 ? __ldg(a.rnorm + r0) : 0.f, rv1 = ok1 && a.m > 0 ? __ldg(a.rnorm + r1) : 0.f;
+#pragma unroll
+    for (int t = 0; t < kTilesPerCta; ++t) {
+      const int q = 4 * (g0 + t) + tig;
+      const bool live = t < ntl && q < a.nq;
+      const float e0 = live ? a.consts[(size_t)q * 2] : 0.f, e1 = live ? a.consts[(size_t)q * 2 + 1] : 0.f;
+      float* row = stage + (4 * t + tig) * kStagePitch + 16 * warp + gq;
+      row[0] = ok0 ? fmaf(nv0 * e0, acc[0][t][0] + acc[0][t][1], rv0 * e1 * (acc[1][t][0] + acc[1][t][1]))
+                   : -INFINITY;
+      row[8] = ok1 ? fmaf(nv1 * e0, acc[0][t][2] + acc[0][t][3], rv1 * e1 * (acc[1][t][2] + acc[1][t][3]))
+                   : -INFINITY;
+    }
+    __syncthreads();
+    // merge into the lists: candidates in increasing vector order, each inserted
+    // at its rank (entries ranking after it move down one, the last falls off)
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+      const float* row = stage + (4 * warp + j) * kStagePitch;
+      float* qs = lsc + (4 * warp + j) * kMaxK;
+      int32_t* qi = lid + (4 * warp + j) * kMaxK;
+#pragma unroll 1
+      for (int part = 0; part < kRows / 32; ++part) {
+        const float sv = row[32 * part + lane];
+        const int32_t iv = (int32_t)(v0 + 32 * part + lane);
+        const float ks = qs[k - 1];  // the list's last entry
+        const int32_t ki = qi[k - 1];
+        uint32_t want = __ballot_sync(0xffffffffu, sv > -INFINITY && (sv > ks || (sv == ks && iv < ki)));
+        while (want != 0u) {
+          const int src = __ffs(want) - 1;
+          want &= want - 1;
+          const float cs = __shfl_sync(0xffffffffu, sv, src);
+          const int32_t ci = __shfl_sync(0xffffffffu, iv, src);
+          // rank = entries that rank before (cs, ci); lane l looks at entries l and l + 32
+          const float s0 = qs[lane], s1 = qs[lane + 32];
+          const int32_t i0 = qi[lane], i1 = qi[lane + 32];
+          const bool b0 = s0 > cs || (s0 == cs && i0 < ci);
+          const bool b1 = s1 > cs || (s1 == cs && i1 < ci);
+          const int pos = __popc(__ballot_sync(0xffffffffu, b0)) + __popc(__ballot_sync(0xffffffffu, b1));
+          if (pos >= k) continue;  // no longer makes the list (it grew better meanwhile)
+          // entries pos .. k - 2 move down one, the candidate takes pos
+          const float t0 = lane > 0 ? qs[lane - 1] : 0.f, t1 = qs[lane + 31];
+          const int32_t u0 = lane > 0 ? qi[lane - 1] : 0, u1 = qi[lane + 31];
+          __syncwarp();
+          if (lane > pos && lane < k) qs[lane] = t0, qi[lane] = u0;
+          else if (lane == pos) qs[lane] = cs, qi[lane] = ci;
+          if (lane + 32 > pos && lane + 32 < k) qs[lane + 32] = t1, qi[lane + 32] = u1;
+          else if (lane + 32 == pos) qs[lane + 32] = cs, qi[lane + 32] = ci;
+          __syncwarp();
+        }
+      }
+    }
+    __syncthreads();  // the staging area is rewritten by the next block
+  }
   // no copy of this CTA may be in flight when it exits: after a wait ran out,
   // thread 0 waits (bounded again) for every copy it started
   if (threadIdx.x == 0 && !alive)
-    for (int c = ndone; c < nissued; ++c)
+    for (int64_t c = ndone; c < nissued; ++c)
       mbar_wait(smem_u32(&full[c & 1]), (uint32_t)((c >> 1) & 1), a.fault, kFaultSearch);
-  // epilogue: column pair (hi, lo) 2·tig of tile t is query 4 (g0 + t) + tig
-  const float nv0 = ok0 ? __ldg(a.norm + r0) : 0.f, nv1 = ok1 ? __ldg(a.norm + r1) : 0.f;
-  const float rv0 = ok0 && a.m > 0 ? __ldg(a.rnorm + r0) : 0.f, rv1 = ok1 && a.m > 0 ? __ldg(a.rnorm + r1) : 0.f;
-#pragma unroll
-  for (int t = 0; t < kTilesPerCta; ++t) {
-    const int q = 4 * (g0 + t) + tig;
-    if (t < ntl && q < a.nq) {
-      const float e0 = a.consts[(size_t)q * 2], e1 = a.consts[(size_t)q * 2 + 1];
-      if (ok0)
-        a.scores[(size_t)q * a.n + r0] =
-            fmaf(nv0 * e0, acc[0][t][0] + acc[0][t][1], rv0 * e1 * (acc[1][t][0] + acc[1][t][1]));
-      if (ok1)
-        a.scores[(size_t)q * a.n + r1] =
-            fmaf(nv1 * e0, acc[0][t][2] + acc[0][t][3], rv1 * e1 * (acc[1][t][2] + acc[1][t][3]));
+  // the lists as candidates: [q][blockIdx.x][k], empty entries as index -1
+  for (int j = 0; j < 4; ++j) {
+    const int ql = 4 * warp + j, q = 4 * g0 + ql;
+    if (ql < 4 * ntl && q < a.nq) {
+      const size_t o = ((size_t)q * a.vchunks + blockIdx.x) * k;
+      for (int e = lane; e < k; e += 32) {
+        a.cand_sc[o + e] = lsc[ql * kMaxK + e];
+        const int32_t id = lid[ql * kMaxK + e];
+        a.cand_idx[o + e] = id == INT32_MAX ? -1 : id;
+      }
     }
   }
 }
@@ -286,8 +369,18 @@ size_t tq::search_tc_table_bytes(const tq_plan* plan, int nq) {
   return ksteps * size_t((nq + 3) / 4) * kFragBytes + sizeof(float) * 2 * size_t(nq);
 }
 
+int tq::search_tc_vchunks(int64_t n, int nq) {
+  // as many CTAs as one wave of two per SM of a B300 (148 SMs) holds, over the
+  // query blocks: every CTA then gets the same number of vector blocks, give or take one
+  const int64_t qblocks = ((nq + 3) / 4 + kTilesPerCta - 1) / kTilesPerCta;
+  const int64_t nblocks = (n + kRows - 1) / kRows;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(nblocks, 2 * 148 / qblocks));
+}
+
 tq_status tq::launch_search_tc(const tq_plan* plan, const tq_records* recs, int64_t n, int nq, const float* qt,
-                               const float* st, void* table, float* scores, cudaStream_t stream) {
+                               const float* st, void* table, int k, int32_t* cand_idx, float* cand_sc,
+                               cudaStream_t stream) {
+  if (k < 1 || k > kMaxK) return TQ_ERR_ARG;
   SearchTcArgs a{};
   a.idx = recs->idx; a.sgn = recs->sgn; a.norm = recs->norm; a.rnorm = recs->rnorm;
   a.n = n;
@@ -301,15 +394,18 @@ tq_status tq::launch_search_tc(const tq_plan* plan, const tq_records* recs, int6
   a.alpha = plan->qjl_alpha;
   a.table = static_cast<__half*>(table);
   a.consts = reinterpret_cast<float*>(static_cast<uint8_t*>(table) + size_t(a.ksteps) * a.groups * kFragBytes);
-  a.scores = scores;
+  a.k = k;
+  a.vchunks = search_tc_vchunks(n, nq);
+  a.cand_idx = cand_idx;
+  a.cand_sc = cand_sc;
   a.fault = tq::fault_word();
   if (!a.fault) return TQ_ERR_CUDA;
   search_table_kernel<<<a.groups, kThreads, 0, stream>>>(a);
   if (launch_status() != TQ_OK) return TQ_ERR_CUDA;
-  const int smem = 2 * kChunkBytes + 64;
+  const int smem = 2 * kChunkBytes + 64 + 32 * kStagePitch * 4 + 32 * kMaxK * 8;
   if (cudaFuncSetAttribute(search_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return TQ_ERR_CUDA;
-  const dim3 grid((unsigned)((n + kRows - 1) / kRows), (unsigned)((a.groups + kTilesPerCta - 1) / kTilesPerCta));
+  const dim3 grid((unsigned)a.vchunks, (unsigned)((a.groups + kTilesPerCta - 1) / kTilesPerCta));
   search_score_kernel<<<grid, kThreads, smem, stream>>>(a);
   return launch_status();
 }

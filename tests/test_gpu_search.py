@@ -103,6 +103,34 @@ def test_generic_d1024_slice(gpu_lib):
     _check_topk(gidx, gsc, osc, 10)
 
 
+def test_generic_d1024_full_size(gpu_lib):
+    """The generic configuration at its full size: 1,048,576 unit-norm anisotropic vectors,
+    d = m = 1024, b = 4, top-10 for 8 queries.  The oracle scores the GPU's records in
+    chunks of 65,536."""
+    wl = WORKLOADS["generic"]
+    n, nq, k, d, m, w = 1 << 20, 8, 10, 1024, 1024, 3
+    X = make_generic(wl, n=n, device="cuda")
+    Q = make_generic_queries(wl, nq=nq, device="cuda")
+    p = plan(d, m, w)
+    rec = _lib.Records(n, d, m, w)
+    _lib.tq_quantize(p, X, rec)
+    del X
+    ws = torch.empty(_lib.tq_search_workspace_size(p, nq, n, k), dtype=torch.uint8, device="cuda")
+    idx = torch.full((nq, k), -7, dtype=torch.int32, device="cuda")
+    sc = torch.empty(nq, k, device="cuda")
+    _lib.tq_search_topk(p, Q, rec, n, k, idx, sc, ws)
+    torch.cuda.synchronize()
+    assert _lib.tq_fault_flags() == 0
+    Pi, S, cent, _ = oracle_tables(d, m, w)
+    Qn = Q.float().cpu().numpy()
+    osc = np.empty((nq, n))
+    step = 1 << 16
+    for r0 in range(0, n, step):
+        got = gpu_records_to_numpy(rec, slice(r0, r0 + step), d, m, w)
+        osc[:, r0:r0 + step] = osearch.scores(Qn, got, Pi, S, cent)
+    _check_topk(idx.cpu().numpy(), sc.cpu().numpy(), osc, k)
+
+
 def test_d512_w1_partial_query_tiles(gpu_lib):
     """d = m = 512, b = 2 (w = 1), 5000 stored vectors, 40 queries (a partial 32-query tile), top-10."""
     g = torch.Generator().manual_seed(512)
