@@ -47,10 +47,12 @@
 //
 // Launches.  unit_table_kernel (one CTA per (batch, kv head) unit) computes
 // Π q and S q for the unit's heads and writes the query operand table and the
-// score constants, once per unit; every decode CTA that works on the unit
-// fetches that table with one bulk copy.  Both kernels are programmatic
-// dependent launches (each waits for its predecessor before reading what the
-// predecessor wrote).
+// score constants, once per unit (and, for tq_decode_attention_append, also
+// quantizes the unit's new key and value into the caches); every decode CTA
+// that works on the unit fetches that table with one bulk copy.
+// unit_combine_kernel (one CTA per unit) then merges the unit's partials and
+// unrotates.  All three are programmatic dependent launches (each waits for
+// its predecessor before reading what the predecessor wrote).
 //
 // Work split.  A persistent grid of one CTA per SM takes contiguous ranges of
 // 256-token tiles over all (batch, kv head) units (the last tile of a unit
@@ -63,10 +65,8 @@
 // tiles (a stage is refilled once all eight warps have arrived on its
 // stage-empty mbarrier).  Within a warp the values of tile k − 1 and the
 // scores of tile k form one straight block.  At the end of its part of a
-// unit a CTA merges the eight warps on chip into one partial, then counts
-// itself in on the unit's arrival counter; the CTA that arrives last merges
-// the unit's partials and applies the unrotation, so there is no combine
-// launch.
+// unit a CTA merges the eight warps on chip into one partial (reference, Σ p
+// and the two value sums per head) for unit_combine_kernel.
 //
 // Softmax is online with a lazy reference per warp: the running reference M
 // (of log2(p·max(‖v‖, ‖r_v‖)), clamped at 2^-32) moves only when a tile
@@ -626,7 +626,6 @@ constexpr int table_smem_bytes() {
 // 16 more: x = 2^-11, 2^-7, 2) or ±1 (word bits 4t+3, 4t+19: exactly −s).  A
 // head's weight w enters as 2w/x (then the product is w·(1 + s), and the
 // offset Σ w over those coordinates goes into the score constant) or as −w.
-// Also zeroes the unit's arrival counter for the decode kernel that follows.
 // Every sum has a fixed order, so the table is the same on every call.
 template <int W, int GP, bool Q>
 __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs a) {

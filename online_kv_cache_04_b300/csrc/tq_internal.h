@@ -67,12 +67,12 @@ tq_status quantize_tc(const tq_plan* plan, const void* x0, const void* x1, int64
                       const tq_records* out0, const tq_records* out1, int64_t row0, cudaStream_t st);
 
 // Tensor-core decode (tq_decode_tc.cu): d = 128, m = 128 or 0, G <= 8, values in
-// TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Two launches: one CTA per
+// TQ_LAYOUT_BLOCK32, ctx_stride % 128 == 0.  Three launches: one CTA per
 // (batch, kv head) unit builds its query table (decode_tc_table_bytes(w, G, m)
-// bytes, 16-byte aligned) and zeroes its arrival counter; the decode kernel
-// then does the scores, softmax and values, and the last CTA of each unit
-// merges the unit's partials ([B*Hq][smax][2 + 256]) into out.  Each unit is
-// cut into decode_tc_tpu(ctx_stride) tiles.
+// bytes, 16-byte aligned); the decode kernel does the scores, softmax and
+// values and writes one partial per CTA and head ([B*Hq][smax][2 + 256]); one
+// CTA per unit merges the unit's partials into out.  Each unit is cut into
+// decode_tc_tpu(ctx_stride) tiles.
 int64_t decode_tc_tpu(int64_t ctx_stride);
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride);
 int decode_tc_ctas(int64_t units, int64_t tpu);
