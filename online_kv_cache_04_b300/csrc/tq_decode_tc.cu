@@ -488,20 +488,35 @@ __device__ __noinline__ void unit_query_prep(const TcArgs& a, int u, int head0, 
 
 // Merge of the ns partials (one per decode CTA) of each head of a unit,
 // log-sum-exp over their references, and the output o = Πᵀ(acc_rot + α S̃ᵀ
-// acc_sgn) / l: one CTA per unit, a programmatic dependent launch after the
-// decode kernel.  The matrix columns (the plan's, not written by the decode)
+// acc_sgn) / l: one CTA per unit (HEAD = false), or, when the heads are few
+// enough for one wave, one CTA per query head (HEAD = true, GP = 1: a
+// quarter of the partial loads and products per CTA, all slots in one round);
+// a programmatic dependent launch after the decode kernel.  The matrix columns (the plan's, not written by the decode)
 // are loaded before the wait for the decode grid, so they overlap its tail;
 // after the wait the partials come in one round of global loads when ns fits
 // one chunk.
-template <int GP, bool Q>
+template <int GP, bool Q, bool HEAD>
 __global__ void __launch_bounds__(kThreads, 1) unit_combine_kernel(const TcArgs a, int ctas) {
+  static_assert(!HEAD || GP == 1, "one head per CTA");
   constexpr int NT = kThreads;
   constexpr int NG = NT / 128, RR = 128 * 128 / NT;
   constexpr int kStride = 2 + 2 * kD;
   extern __shared__ uint8_t smem_raw[];
   float* scr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
-  const int64_t u = blockIdx.x;
-  const int b = (int)(u / a.Hkv), h = (int)(u - (int64_t)b * a.Hkv), head0 = b * a.Hq + h * a.G;
+  // this CTA's heads head0 .. head0 + G - 1, of unit u = (b, h)
+  int b, h, head0, G;
+  if (HEAD) {
+    head0 = blockIdx.x;
+    b = head0 / a.Hq;
+    h = (head0 - b * a.Hq) / a.G;
+    G = 1;
+  } else {
+    b = (int)(blockIdx.x / a.Hkv);
+    h = (int)(blockIdx.x - b * a.Hkv);
+    head0 = b * a.Hq + h * a.G;
+    G = a.G;
+  }
+  const int64_t u = (int64_t)b * a.Hkv + h;
   // the decode CTAs that own tiles of the unit: one partial slot each
   const int ns = (int)(owner((u + 1) * a.tpu - 1, a.total, ctas) - owner(u * a.tpu, a.total, ctas) + 1);
   float v1[RR], v2[RR];
@@ -510,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1) unit_combine_kernel(const TcArgs 
   // the partials are the decode kernel's: wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  // fused append: every read of ctx_len[b] is done; its first unit advances it
-  if (a.append && h == 0 && threadIdx.x == 0) {
+  // fused append: every read of ctx_len[b] is done; the row's first CTA advances it
+  if (a.append && threadIdx.x == 0 && (HEAD ? head0 == b * a.Hq : h == 0)) {
     const int L = a.ctx_len_mut[b];
     if (L >= 0 && L < a.ctx_stride) a.ctx_len_mut[b] = L + 1;
   }
@@ -529,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) unit_combine_kernel(const TcArgs 
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int o = threadIdx.x + NT * r, g = o >> 8, j = o & (2 * kD - 1);
-    pp[r] = a.part + (size_t)(head0 + min(g, a.G - 1)) * a.smax * kStride + 2 + j;
+    pp[r] = a.part + (size_t)(head0 + min(g, G - 1)) * a.smax * kStride + 2 + j;
     wg[r] = wgt + g * kMaxCtas;
     v[r] = 0.f;
 #pragma unroll
@@ -543,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) unit_combine_kernel(const TcArgs 
 #pragma unroll
     for (int t = 0; t < kPerLane; ++t) {
       const int k = lane + 32 * t;
-      const bool in = warp < a.G && k < ns;
+      const bool in = warp < G && k < ns;
       mk[t] = in ? __ldcg(pm + (size_t)k * kStride) : -INFINITY;
       lk[t] = in ? __ldcg(pm + (size_t)k * kStride + 1) : 0.f;
     }
@@ -593,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) unit_combine_kernel(const TcArgs 
   cta_sync_n<NT>();
   cols_times<GP, NT>(v2, y, kD, red);
   cta_sync_n<NT>();
-  for (int e = threadIdx.x; e < a.G * kD; e += NT) {
+  for (int e = threadIdx.x; e < G * kD; e += NT) {
     const float l = ml[2 * (e >> 7) + 1];
     a.out[(size_t)head0 * kD + e] = sum_groups<NG>(red, e, GP * kD) * (l > 0.f ? 1.f / l : 0.f);
   }
@@ -1254,7 +1269,12 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
   const int units = B * Hkv;
   const int grid = decode_tc_ctas(units, a.tpu);
   // the per-unit query tables, the decode, then the per-unit merge
-  auto go = [&](auto table_kern, int table_smem, auto kern, int smem, auto comb_kern, int comb_smem) -> tq_status {
+  // the merge: one CTA per query head when those fit one wave, else one per unit
+  const bool per_head = (int64_t)B * Hq <= sm_count();
+  auto go = [&](auto table_kern, int table_smem, auto kern, int smem, auto comb_unit, int comb_unit_smem,
+                auto comb_head, int comb_head_smem) -> tq_status {
+    void (*comb_kern)(const TcArgs, int) = per_head ? comb_head : comb_unit;
+    const int comb_smem = per_head ? comb_head_smem : comb_unit_smem;
     if (cudaFuncSetAttribute(table_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, table_smem) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaFuncSetAttribute(comb_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, comb_smem) != cudaSuccess)
@@ -1279,14 +1299,15 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
     cfg.gridDim = dim3(grid);
     cfg.dynamicSmemBytes = smem;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TQ_ERR_CUDA;
-    cfg.gridDim = dim3(units);
+    cfg.gridDim = dim3(per_head ? B * Hq : units);
     cfg.dynamicSmemBytes = comb_smem;
     if (cudaLaunchKernelEx(&cfg, comb_kern, a, grid) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
   };
 #define TQ_DECODE_TC_GO(W_, GP_, Q_)                                                                \
   go(unit_table_kernel<W_, GP_, Q_>, table_smem_bytes<W_, GP_, Q_>(), decode_tc_kernel<W_, GP_, Q_>, \
-     smem_bytes<W_, GP_, Q_>(), unit_combine_kernel<GP_, Q_>, 16 + Scratch<GP_, kThreads>::kMerge * 4)
+     smem_bytes<W_, GP_, Q_>(), unit_combine_kernel<GP_, Q_, false>, 16 + Scratch<GP_, kThreads>::kMerge * 4, \
+     unit_combine_kernel<1, Q_, true>, 16 + Scratch<1, kThreads>::kMerge * 4)
   const bool g8 = a.G > 4;
   if (plan->m > 0) {
     switch (plan->w) {
