@@ -61,6 +61,12 @@ struct SearchTcArgs {
   const uint32_t* idx; const uint32_t* sgn; const float* norm; const float* rnorm;
   int64_t n;
   int nq, d, m, w, npm;     // npm: codebook planes (w, or 4 with the product plane)
+  // deq (w = 3): the codebook part contracts the centroid values themselves,
+  // c[idx] as f16 hi + lo looked up from the index bits, against one block of
+  // Π q (npm_t = 1 table block instead of npm planes)
+  int deq, npm_t;
+  const float* centroids;   // [2^w]
+  uint32_t* ctab;           // deq: [8] bytes of f16 c_hi[0..7] (lo bytes, hi bytes), then of c_lo[0..7]
   int groups;               // query groups of four
   int64_t ksteps;           // 2 (npm d + m) / 32
   const float* qt; const float* st;   // [nq][d] Π q, [nq][m] S q
@@ -81,6 +87,21 @@ __device__ __forceinline__ uint32_t sign_operand(uint32_t t) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(sel));
+  return r;
+}
+
+// Bucket indices of four coordinates, as the four selector nibbles of a byte
+// permute: bits 0, 1, 8, 9 of each plane word t_p (already shifted) are the
+// coordinates' bit p; nibble k of the result = Σ_p bit_p << p of coordinate k
+// (bits 0, 1, 8, 9 -> nibbles 0, 1, 2, 3).  (t & 0x303)·9 copies bits 0, 1, 8, 9
+// to 3, 4, 11, 12 without overlap, so the mask keeps bits 0, 4, 8, 12.
+__device__ __forceinline__ uint32_t index_nibbles(uint32_t t0, uint32_t t1, uint32_t t2) {
+  return (((t0 & 0x303u) * 9u) & 0x1111u) | (((t1 & 0x303u) * 18u) & 0x2222u) | (((t2 & 0x303u) * 36u) & 0x4444u);
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -99,6 +120,7 @@ __global__ void __launch_bounds__(kThreads) search_table_kernel(SearchTcArgs a) 
   __syncthreads();
   float cmax = 0.f;
   for (int P = 0; P < a.npm; ++P) cmax = fmaxf(cmax, fabsf(__ldg(a.walsh + (P < a.w ? (1 << P) : 7))));
+  if (a.deq) cmax = 1.f;  // the weights are Π q itself
   for (int g = 0; g < 4; ++g) {
     const int q = 4 * grp + g;
     float m0 = 0.f, m1 = 0.f;
@@ -122,21 +144,42 @@ __global__ void __launch_bounds__(kThreads) search_table_kernel(SearchTcArgs a) 
     frexpf(amax[p][g], &ex);
     return amax[p][g] > 0.f ? ldexpf(1.f, ex - 12) : 1.f;
   };
+  if (a.deq && grp == 0 && threadIdx.x == 0) {
+    // the centroids as f16 hi + lo pairs, byte-sliced for byte permutes: word
+    // 2s + h (s: 0 lo bytes, 1 hi bytes; h: entries 4h .. 4h + 3) of piece pc
+    uint32_t words[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    for (int i = 0; i < 8; ++i) {
+      const float c = __ldg(a.centroids + i);
+      const __half ch = __float2half_rn(c), cl = __float2half_rn(c - __half2float(ch));
+      const uint32_t bits[2] = {__half_as_ushort(ch), __half_as_ushort(cl)};
+      for (int pc = 0; pc < 2; ++pc) {
+        words[4 * pc + (i >> 2)] |= (bits[pc] & 0xFFu) << (8 * (i & 3));
+        words[4 * pc + 2 + (i >> 2)] |= (bits[pc] >> 8) << (8 * (i & 3));
+      }
+    }
+    for (int i = 0; i < 8; ++i) a.ctab[i] = words[i];
+  }
   if (threadIdx.x < 4 && 4 * grp + (int)threadIdx.x < a.nq) {
     const int g = threadIdx.x;
     a.consts[(size_t)(4 * grp + g) * 2] = escale(0, g);
     a.consts[(size_t)(4 * grp + g) * 2 + 1] = a.alpha * escale(1, g);
   }
   const int words_d = a.d / 32;
-  const int64_t total = (int64_t)a.npm * a.d + a.m;  // plane coordinates, codebook planes first
+  const int np = a.npm_t;
+  const int64_t total = (int64_t)np * a.d + a.m;  // plane coordinates, codebook planes first
   for (int64_t e = threadIdx.x; e < total; e += kThreads) {
-    const bool qjl = e >= (int64_t)a.npm * a.d;
-    const int P = qjl ? a.npm : (int)(e / a.d);
-    const int j = qjl ? (int)(e - (int64_t)a.npm * a.d) : (int)(e - (int64_t)P * a.d);
+    const bool qjl = e >= (int64_t)np * a.d;
+    const int P = qjl ? np : (int)(e / a.d);
+    const int j = qjl ? (int)(e - (int64_t)np * a.d) : (int)(e - (int64_t)P * a.d);
     const int x = j & 31, eh = x >> 4, L = x & 15;
-    const int64_t ks = 2 * ((int64_t)P * words_d + (j >> 5)) + (L >> 3);
-    const int kk = 8 * ((L >> 2) & 1) + 2 * (L & 3) + eh;
-    const float coef = qjl ? 0.f : __ldg(a.walsh + (P < a.w ? (1 << P) : 7));
+    int64_t ks = 2 * ((int64_t)P * words_d + (j >> 5)) + (L >> 3);
+    int kk = 8 * ((L >> 2) & 1) + 2 * (L & 3) + eh;
+    if (a.deq && !qjl) {  // centroid values: coordinate j at K-step j / 16, K index j % 16
+      ks = j >> 4;
+      kk = j & 15;
+    }
+    // the ±1 planes' operand is -s, so their weight is negated; centroids carry their sign
+    const float coef = qjl ? 0.f : a.deq ? -1.f : __ldg(a.walsh + (P < a.w ? (1 << P) : 7));
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const int q = 4 * grp + g;
@@ -158,6 +201,7 @@ __global__ void __launch_bounds__(kThreads) search_table_kernel(SearchTcArgs a) 
 // of 128 rows each (rows v0 .. v0 + 127), query groups 8·by .. 8·by + 7.  Warp
 // wp takes rows v0 + 16 wp + (0..15): fragment row gq is vector v0 + 16 wp +
 // gq, row gq + 8 the vector eight further.
+template <bool DEQ>
 __global__ void __launch_bounds__(kThreads, 2) search_score_kernel(SearchTcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* buf = smem;  // [2][kChunkSteps][kTilesPerCta][256 B]
@@ -165,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 2) search_score_kernel(SearchTcArgs 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
   const int g0 = blockIdx.y * kTilesPerCta, ntl = min(kTilesPerCta, a.groups - g0);
   const int words_d = a.d / 32, words_m = a.m / 32;
-  const int nchunks = (a.npm * words_d + words_m) / kChunkWords;
+  const int nchunks = (a.npm_t * words_d + words_m) / kChunkWords;
   float* stage = reinterpret_cast<float*>(smem + 2 * kChunkBytes + 64);  // [32 queries][kStagePitch]
   float* lsc = stage + 32 * kStagePitch;                                   // [32 queries][kMaxK] list scores
   int32_t* lid = reinterpret_cast<int32_t*>(lsc + 32 * kMaxK);              // [32 queries][kMaxK] list indices
@@ -207,12 +251,71 @@ __global__ void __launch_bounds__(kThreads, 2) search_score_kernel(SearchTcArgs 
   int64_t r0 = 0, r1 = 0;
   bool ok0 = false, ok1 = false;
   int64_t gbase = 0;  // global chunk number of this block's chunk 0
+  // deq: the byte tables of f16 c_hi and c_lo (lo bytes of entries 0..7, then hi bytes)
+  uint32_t ct[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ct[i] = DEQ ? __ldg(a.ctab + i) : 0u;
+  // one chunk of centroid values (deq): 128 coordinates of every index plane;
+  // K-step sl covers coordinates 16·sl .. 16·sl + 15 of the chunk in order
+  auto chunk_deq = [&](int c) {
+    const int kw0 = c * kChunkWords;
+    uint4 x[2][3];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int64_t row = r ? r1 : r0;
+#pragma unroll
+      for (int p = 0; p < 3; ++p)
+        x[r][p] = (r ? ok1 : ok0) ? __ldg(reinterpret_cast<const uint4*>(a.idx + row * wi + p * words_d + kw0))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int64_t gc = gbase + c;
+    if (alive) {
+      alive = mbar_wait(smem_u32(&full[gc & 1]), (uint32_t)((gc >> 1) & 1), a.fault, kFaultSearch);
+      ndone += alive ? 1 : 0;
+    }
+    const uint2* bfr = reinterpret_cast<const uint2*>(buf + (gc & 1) * kChunkBytes);
+#pragma unroll
+    for (int kw = 0; kw < kChunkWords; ++kw) {
+#pragma unroll
+      for (int sh = 0; sh < 2; ++sh) {
+        // this lane's coordinates 2·tig, 2·tig + 1, 8 + 2·tig, 9 + 2·tig of K-step 2·kw + sh
+        const int off = 16 * sh + 2 * tig;
+        uint32_t hi[2][2], lo[2][2];  // [row][k-slot pair 2tig | 8 + 2tig]
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint4* xr = x[r];
+          auto word = [&](int p) {
+            return kw == 0 ? xr[p].x : kw == 1 ? xr[p].y : kw == 2 ? xr[p].z : xr[p].w;
+          };
+          const uint32_t sel = index_nibbles(word(0) >> off, word(1) >> off, word(2) >> off);
+          const uint32_t hl = prmt(ct[0], ct[1], sel), hh = prmt(ct[2], ct[3], sel);
+          const uint32_t ll = prmt(ct[4], ct[5], sel), lh = prmt(ct[6], ct[7], sel);
+          hi[r][0] = prmt(hl, hh, 0x5140u);
+          hi[r][1] = prmt(hl, hh, 0x7362u);
+          lo[r][0] = prmt(ll, lh, 0x5140u);
+          lo[r][1] = prmt(ll, lh, 0x7362u);
+        }
+        const int sl = 2 * kw + sh;
+#pragma unroll
+        for (int t = 0; t < kTilesPerCta; ++t) {
+          const uint2 b = bfr[(sl * kTilesPerCta + t) * 32 + lane];
+          mma16816(acc[0][t], hi[0][0], hi[1][0], hi[0][1], hi[1][1], b.x, b.y);
+          mma16816(acc[0][t], lo[0][0], lo[1][0], lo[0][1], lo[1][1], b.x, b.y);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with this buffer
+    if (threadIdx.x == 0 && gc + 2 < total_chunks && alive) {
+      issue(gc + 2);
+      nissued = gc + 3;
+    }
+  };
   // one chunk into the accumulators of part PART (0: codebook planes, 1: QJL plane)
   auto chunk = [&](int c, auto part_tag) {
     constexpr int PART = decltype(part_tag)::value;
     const int wpos = c * kChunkWords;  // word position over all planes
-    const int P = PART ? a.npm : wpos / words_d;
-    const int kw0 = PART ? wpos - a.npm * words_d : wpos - P * words_d;
+    const int P = PART ? a.npm_t : wpos / words_d;
+    const int kw0 = PART ? wpos - a.npm_t * words_d : wpos - P * words_d;
     uint4 x[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -262,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 2) search_score_kernel(SearchTcArgs 
       nissued = gc + 3;
     }
   };
-  const int ncb = a.npm * words_d / kChunkWords;  // codebook chunks; the QJL plane's follow
+  const int ncb = a.npm_t * words_d / kChunkWords;  // codebook chunks; the QJL plane's follow
   const int k = a.k;
 #pragma unroll 1
   for (int64_t it = 0; it < myblocks; ++it) {
@@ -278,8 +381,13 @@ __global__ void __launch_bounds__(kThreads, 2) search_score_kernel(SearchTcArgs 
       for (int t = 0; t < kTilesPerCta; ++t)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[p][t][e] = 0.f;
+    if constexpr (DEQ) {
 #pragma unroll 1
-    for (int c = 0; c < ncb; ++c) chunk(c, std::integral_constant<int, 0>{});
+      for (int c = 0; c < ncb; ++c) chunk_deq(c);
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < ncb; ++c) chunk(c, std::integral_constant<int, 0>{});
+    }
 #pragma unroll 1
     for (int c = ncb; c < nchunks; ++c) chunk(c, std::integral_constant<int, 1>{});
     // scores of the block: column pair (hi, lo) 2·tig of tile t is query
@@ -363,10 +471,15 @@ bool tq::search_tc_supported(const tq_plan* plan, const tq_records* recs) {
   return plan->d % 128 == 0 && plan->m % 128 == 0 && recs->layout == TQ_LAYOUT_ROWS;
 }
 
+namespace {
+// Codebook planes of the query table: w ±1 planes (4 with the product plane at
+// w = 3), or, at w = 3, one block of centroid values.
+int table_planes(const tq_plan* plan) { return plan->w == 3 ? 1 : plan->w; }
+}  // namespace
+
 size_t tq::search_tc_table_bytes(const tq_plan* plan, int nq) {
-  const int npm = plan->w == 3 ? 4 : plan->w;
-  const size_t ksteps = 2 * (size_t(npm) * plan->d + plan->m) / 32;
-  return ksteps * size_t((nq + 3) / 4) * kFragBytes + sizeof(float) * 2 * size_t(nq);
+  const size_t ksteps = 2 * (size_t(table_planes(plan)) * plan->d + plan->m) / 32;
+  return ksteps * size_t((nq + 3) / 4) * kFragBytes + sizeof(float) * 2 * size_t(nq) + 8 * sizeof(uint32_t);
 }
 
 int tq::search_tc_vchunks(int64_t n, int nq) {
@@ -387,13 +500,17 @@ tq_status tq::launch_search_tc(const tq_plan* plan, const tq_records* recs, int6
   a.nq = nq;
   a.d = plan->d; a.m = plan->m; a.w = plan->w;
   a.npm = plan->w == 3 ? 4 : plan->w;
+  a.deq = plan->w == 3;
+  a.npm_t = table_planes(plan);
   a.groups = (nq + 3) / 4;
-  a.ksteps = 2 * (int64_t(a.npm) * a.d + a.m) / 32;
+  a.ksteps = 2 * (int64_t(a.npm_t) * a.d + a.m) / 32;
+  a.centroids = plan->centroids;
   a.qt = qt; a.st = st;
   a.walsh = plan->walsh;
   a.alpha = plan->qjl_alpha;
   a.table = static_cast<__half*>(table);
   a.consts = reinterpret_cast<float*>(static_cast<uint8_t*>(table) + size_t(a.ksteps) * a.groups * kFragBytes);
+  a.ctab = reinterpret_cast<uint32_t*>(a.consts + 2 * size_t(nq));
   a.k = k;
   a.vchunks = search_tc_vchunks(n, nq);
   a.cand_idx = cand_idx;
@@ -403,9 +520,10 @@ tq_status tq::launch_search_tc(const tq_plan* plan, const tq_records* recs, int6
   search_table_kernel<<<a.groups, kThreads, 0, stream>>>(a);
   if (launch_status() != TQ_OK) return TQ_ERR_CUDA;
   const int smem = 2 * kChunkBytes + 64 + 32 * kStagePitch * 4 + 32 * kMaxK * 8;
-  if (cudaFuncSetAttribute(search_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  auto kern = a.deq ? search_score_kernel<true> : search_score_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return TQ_ERR_CUDA;
   const dim3 grid((unsigned)a.vchunks, (unsigned)((a.groups + kTilesPerCta - 1) / kTilesPerCta));
-  search_score_kernel<<<grid, kThreads, smem, stream>>>(a);
+  kern<<<grid, kThreads, smem, stream>>>(a);
   return launch_status();
 }
