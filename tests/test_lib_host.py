@@ -144,6 +144,16 @@ def test_argument_errors_return_codes_without_launching():
     assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 0, 2, ref(kv), ref(kv2), 4096, 64, None) == _lib.TQ_ERR_ARG
     assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv2), None, 64, None) == _lib.TQ_ERR_ARG
     assert lib.tq_append_kv(ref(p), 4096, 4096, 1, 1, 2, ref(kv), ref(kv2), 4096, 0, None) == _lib.TQ_ERR_ARG
+    # decode with the fused append: the append's own checks, then the decode's, before any launch
+    assert lib.tq_decode_workspace_size(ref(p), 1, 8, 2, 64, ref(n)) == _lib.TQ_OK
+    app = lambda kn, vn, kvd, K, V, stride, pages, ws_bytes: lib.tq_decode_attention_append(
+        ref(p), 4096, 1, kn, vn, kvd, 1, 8, 2, ref(K), ref(V), 4096, stride, pages, 0.0, 4096, 4096, ws_bytes, None)
+    assert app(4096, 4096, 1, kv, kv, 64, None, n.value) == _lib.TQ_ERR_ARG      # K and V share their arrays
+    assert app(4100, 4096, 1, kv, kv2, 64, None, n.value) == _lib.TQ_ERR_ARG     # misaligned new key
+    assert app(4096, None, 1, kv, kv2, 64, None, n.value) == _lib.TQ_ERR_ARG     # no new value
+    assert app(4096, 4096, 7, kv, kv2, 64, None, n.value) == _lib.TQ_ERR_ARG     # dtype
+    assert app(4096, 4096, 1, kv, kv2, 64, 4096, n.value) == _lib.TQ_ERR_ARG     # pages need 256-token stride
+    assert app(4096, 4096, 1, kv, kv2, 64, None, n.value - 4) == _lib.TQ_ERR_WORKSPACE
     # search: k range
     assert lib.tq_search_workspace_size(ref(p), 4, 100, 0, ref(n)) == _lib.TQ_ERR_ARG
     assert lib.tq_search_workspace_size(ref(p), 4, 100, 65, ref(n)) == _lib.TQ_ERR_ARG
