@@ -105,6 +105,10 @@ typedef struct tq_plan {
    * halves ((p·(K/16) + k)·(rows/8) + f)·32 + l, for M = Π and M = S Πᵀ. */
   const uint16_t* pi_frag;  /* [2][d/16][d/8][32][4]                        */
   const uint16_t* s_frag;   /* [2][d/16][m/8][32][4]                        */
+  /* bf16 hi/lo split of S itself (= (S Πᵀ) Π), for d a multiple of 256 with
+   * m = d (NULL otherwise): the wide tensor-core quantizer forms the signs as
+   * S x / n - (S Πᵀ) c[idx] = S r / n without holding the residual. */
+  const uint16_t* s_x_bf16; /* [2][m][d]                                    */
 } tq_plan;
 
 /* Device bytes needed by tq_plan_init for (d, m, w); 0 if unsupported.

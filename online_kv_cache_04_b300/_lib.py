@@ -26,7 +26,7 @@ class tq_plan(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("m", ctypes.c_int), ("w", ctypes.c_int), ("qjl_alpha", ctypes.c_float),
                 ("pi", _vp), ("pi_t", _vp), ("s_rot", _vp), ("s_rot_t", _vp), ("centroids", _vp),
                 ("bounds", _vp), ("walsh", _vp), ("pi_bf16", _vp), ("s_bf16", _vp), ("pi_frag", _vp),
-                ("s_frag", _vp)]
+                ("s_frag", _vp), ("s_x_bf16", _vp)]
 
 
 class tq_polar_plan(ctypes.Structure):

@@ -1,6 +1,7 @@
 // Internal helpers shared by the libturboquant translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -103,6 +104,19 @@ tq_status append_kv(const tq_plan* plan, const void* k_new, const void* v_new, t
 // out_offset + n) of `out`, TQ_LAYOUT_ROWS.  Arguments already checked.
 tq_status quantize_simt_cols(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
                              const int32_t* cols, const tq_records* out, int64_t out_offset, cudaStream_t st);
+
+// tcgen05 quantizer for wide vectors (tq_quantize_wide.cu): d a multiple of
+// 256 up to 1024, m = d (with the plan's pieces of S) or 0, fp32 or bf16 input,
+// TQ_LAYOUT_ROWS output; rows [row0, row0 + n) of `out`.
+bool quantize_wide_supported(const tq_plan* plan, const tq_records* out);
+tq_status quantize_wide(const tq_plan* plan, const void* x, tq_dtype dtype, int64_t n, int64_t ld_x,
+                        const tq_records* out, int64_t row0, cudaStream_t st);
+
+// 2-D tensor map over a rows x cols bf16 matrix of row stride ld elements:
+// boxes of 64 columns x box_rows rows, 128-byte swizzle (tq_quantize_tc.cu).
+// False if the driver's encoder is unavailable or rejects the map.
+bool map_bf16_tiles(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                    uint32_t box_rows);
 
 // Warp tensor-core quantizer (tq_quantize_mma.cu): d a multiple of 128 up to
 // 1024, m = d or 0, fp32 or bf16 input, TQ_LAYOUT_ROWS output; rows

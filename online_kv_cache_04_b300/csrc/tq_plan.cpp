@@ -1,7 +1,9 @@
 // Device plan: fp32 / bf16 copies of the setup tables in one caller-owned
 // buffer.  Host-side conversion, then plain cudaMemcpyAsync uploads.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <thread>
 #include <vector>
 
 #include "tq_internal.h"
@@ -12,8 +14,9 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t pi, pi_t, s_rot, s_rot_t, cent, bnd, walsh, pi_bf, s_bf, pi_fr, s_fr, total;
-  bool frag;  // warp-MMA operand copies present (d >= 256)
+  size_t pi, pi_t, s_rot, s_rot_t, cent, bnd, walsh, pi_bf, s_bf, pi_fr, s_fr, s_x, total;
+  bool frag;  // warp-MMA operand copies present (d a multiple of 128)
+  bool sx;    // bf16 pieces of S itself present (d a multiple of 256, m = d)
 };
 
 Layout layout(int d, int m, int w) {
@@ -32,6 +35,8 @@ Layout layout(int d, int m, int w) {
   l.frag = d % 128 == 0;
   l.pi_fr = o;   o += l.frag ? up(sizeof(uint16_t) * 2 * size_t(d) * d) : 0;
   l.s_fr = o;    o += l.frag ? up(sizeof(uint16_t) * 2 * size_t(m) * d) : 0;
+  l.sx = d % 256 == 0 && m == d;
+  l.s_x = o;     o += l.sx ? up(sizeof(uint16_t) * 2 * size_t(m) * d) : 0;
   l.total = o;
   return l;
 }
@@ -48,6 +53,30 @@ double bf16_value(uint16_t h) {
   float f;
   std::memcpy(&f, &u, 4);
   return f;
+}
+
+// S = (S Πᵀ) Π (m x d, float64), rows split over host threads.
+std::vector<double> unrotate_qjl(const double* s_rot, const double* pi, int m, int d) {
+  std::vector<double> S(size_t(m) * d, 0.0);
+  auto rows = [&](int i0, int i1) {
+    for (int i = i0; i < i1; ++i) {
+      double* out = S.data() + size_t(i) * d;
+      for (int k = 0; k < d; ++k) {
+        const double a = s_rot[size_t(i) * d + k];
+        const double* p = pi + size_t(k) * d;
+        for (int j = 0; j < d; ++j) out[j] += a * p[j];
+      }
+    }
+  };
+  const int nt = std::max(1, std::min<int>(16, static_cast<int>(std::thread::hardware_concurrency())));
+  std::vector<std::thread> pool;
+  const int per = (m + nt - 1) / nt;
+  for (int t = 0; t < nt; ++t) {
+    const int i0 = t * per, i1 = std::min(m, i0 + per);
+    if (i0 < i1) pool.emplace_back(rows, i0, i1);
+  }
+  for (auto& th : pool) th.join();
+  return S;
 }
 
 }  // namespace
@@ -88,6 +117,15 @@ extern "C" tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const doub
       H(l.s_bf)[size_t(i) * d + j] = hi;
       H(l.s_bf)[size_t(m) * d + size_t(i) * d + j] = lo;
     }
+  // bf16 pieces of S = (S Πᵀ) Π for the wide tensor-core quantizer's sign stage
+  if (l.sx) {
+    const std::vector<double> S = unrotate_qjl(s_rot, pi, m, d);
+    for (size_t e = 0; e < size_t(m) * d; ++e) {
+      const uint16_t hi = bf16_rne(static_cast<float>(S[e]));
+      H(l.s_x)[e] = hi;
+      H(l.s_x)[size_t(m) * d + e] = bf16_rne(static_cast<float>(S[e] - bf16_value(hi)));
+    }
+  }
   // warp-MMA operand order of the pieces (see tq_plan.pi_frag)
   if (l.frag) {
     auto frag = [&](size_t off, const uint16_t* src, int rows) {
@@ -142,5 +180,6 @@ extern "C" tq_status tq_plan_init(tq_plan* plan, int d, int m, int w, const doub
   plan->s_bf16 = reinterpret_cast<const uint16_t*>(base + l.s_bf);
   plan->pi_frag = l.frag ? reinterpret_cast<const uint16_t*>(base + l.pi_fr) : nullptr;
   plan->s_frag = l.frag && m > 0 ? reinterpret_cast<const uint16_t*>(base + l.s_fr) : nullptr;
+  plan->s_x_bf16 = l.sx ? reinterpret_cast<const uint16_t*>(base + l.s_x) : nullptr;
   return TQ_OK;
 }

@@ -267,6 +267,7 @@ extern "C" tq_status tq_quantize(const tq_plan* plan, const void* x, tq_dtype dt
   if (rows) {
     if (tq::quantize_tc_supported(plan, dtype, n))
       return tq::quantize_tc(plan, x, nullptr, n, ld_x, out, nullptr, out_offset, st);
+    if (tq::quantize_wide_supported(plan, out)) return tq::quantize_wide(plan, x, dtype, n, ld_x, out, out_offset, st);
     if (tq::quantize_mma_supported(plan, out)) return tq::quantize_mma(plan, x, dtype, n, ld_x, out, out_offset, st);
     return launch_simt_any<TQ_LAYOUT_ROWS>(a, dtype, st);
   }

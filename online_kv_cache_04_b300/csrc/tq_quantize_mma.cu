@@ -14,9 +14,10 @@
 // relative), and the same for P = ρ (S Πᵀ)ᵀ.  A CTA takes 16 vectors: their
 // bf16 pieces sit in shared memory (rows padded against bank conflicts), the
 // matrix pieces are read as B fragments straight from the plan's copies in
-// operand order, and each warp owns max(d/8, 32) output coordinates (at
-// d = 128 four warps own 32 each, so that every index word fills in one warp,
-// and the other four only stage and wait).  After the first product the warps
+// operand order, and each warp owns max(d/8, 32) output coordinates rounded
+// up to whole 32-bit words, so that every index word fills in one warp (at
+// d = 128 four warps own 32 each and the other four only stage and wait; at
+// d = 384 six own 64 each).  After the first product the warps
 // bucketize in registers, pack the index planes with quad shuffles, and write
 // ρ's bf16 pieces over x's for the second product.
 #include <cuda_bf16.h>
@@ -109,6 +110,9 @@ __device__ __forceinline__ uint32_t quad_or(uint32_t v) {
   return v;
 }
 
+// Output coordinates per warp: d/8, at least 32, rounded up to whole 32-bit words.
+__device__ __forceinline__ int words_per_warp(int d) { return (max(d / 8, 32) + 31) / 32 * 32; }
+
 __device__ __forceinline__ float warp_total(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -156,7 +160,8 @@ __global__ void __launch_bounds__(kThreads) quantize_mma_kernel(MmaArgs a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[f][e] = 0.f;
   // a warp's block of output coordinates is a whole number of 32-bit words
-  const int cw1 = max(d / 8, 32), nf1 = warp * cw1 < d ? cw1 / 8 : 0, col1 = warp * cw1;
+  // (d/8 rounded up to one; at d = 384, say, six warps own 64 each)
+  const int cw1 = words_per_warp(d), col1 = warp * cw1, nf1 = col1 < d ? min(cw1, d - col1) / 8 : 0;
   gemm_split(acc, ah, al, lda, a.pi_fr, a.pi_fr + (size_t)d * d / 4, d, d, col1, nf1, lane);
 
   // ---- stage 1 in registers: u = U / n, idx, ρ (kept in acc), ||ρ||², index words
@@ -243,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) quantize_mma_kernel(MmaArgs a) {
     for (int f = 0; f < kMaxNF; ++f)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[f][e] = 0.f;
-    const int cw2 = max(m / 8, 32), nf2 = warp * cw2 < m ? cw2 / 8 : 0, col2 = warp * cw2;
+    const int cw2 = words_per_warp(m), col2 = warp * cw2, nf2 = col2 < m ? min(cw2, m - col2) / 8 : 0;
     gemm_split(acc, ah, al, lda, a.s_fr, a.s_fr + (size_t)m * d / 4, d, m, col2, nf2, lane);
     uint32_t sb0 = 0u, sb1 = 0u;
 #pragma unroll
