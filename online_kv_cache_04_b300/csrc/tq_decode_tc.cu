@@ -879,9 +879,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
       // ---- this unit's query table (unit_table_kernel): one bulk copy once every
       // warp is done with the previous unit's table (the merges also write the
       // region through the generic proxy)
+      fence_proxy_async_smem();
       cta_sync_n<NT>();
       if (threadIdx.x == 0) {
-        fence_proxy_async_smem();
         const uint32_t bar = smem_u32(&ms->tab_full);
         const uint8_t* src = a.tables + (size_t)sg.u * Table<W, GP, Q>::kBytes;
         mbar_arrive_expect_tx(bar, Table<W, GP, Q>::kBytes);
@@ -1106,6 +1106,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
 
       // this warp is through CTA tile g: hand its stage back; thread 0 refills
       auto release = [&](int64_t g, int64_t done) {
+        fence_proxy_async_smem();  // these generic reads before the refilling bulk copy
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ms->ld_empty[g & (kStages - 1)]));
         if (threadIdx.x == 0) issue_upto(done);

@@ -117,6 +117,11 @@ tq_status quantize_wide(const tq_plan* plan, const void* x, tq_dtype dtype, int6
 // False if the driver's encoder is unavailable or rejects the map.
 bool map_bf16_tiles(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
                     uint32_t box_rows);
+// The driver's tensor-map encoder (NULL if unavailable).
+typedef CUresult (*TensorMapEncoder)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+TensorMapEncoder tensor_map_encoder();
 
 // Warp tensor-core quantizer (tq_quantize_mma.cu): d a multiple of 128 up to
 // 1024, m = d or 0, fp32 or bf16 input, TQ_LAYOUT_ROWS output; rows

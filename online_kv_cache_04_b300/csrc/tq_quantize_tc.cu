@@ -298,6 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // the next TMA write into this stage (async proxy) follows these generic reads
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->x_empty[s]));
       float* nsq = nsq_s + ph * 2 * 128;
@@ -522,6 +524,8 @@ bool tq::map_bf16_tiles(CUtensorMap* map, const void* ptr, uint64_t rows, uint64
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+tq::TensorMapEncoder tq::tensor_map_encoder() { return encode_fn(); }
 
 unsigned* tq::fault_word() {
   void* p = nullptr;

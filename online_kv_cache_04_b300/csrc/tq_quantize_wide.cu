@@ -58,14 +58,15 @@ constexpr int kCols = 256;                        // output columns per pass (MM
 constexpr int kKc = 64;                           // K columns per stage (one 128-byte swizzle atom)
 constexpr int kPieceA = kTile * kKc * 2;          // 16 KB: one bf16 piece of an A stage
 constexpr int kSlotA = 2 * kPieceA;               // hi | lo
+constexpr int kSlotR = kTile * kKc * 4;           // 32 KB: the raw input of a stage (fp32 at most)
 constexpr int kSlotB = kCols * kKc * 2;           // 32 KB: one bf16 piece of a B stage
-constexpr int kNA = 3, kNB = 4;                   // ring depths
-constexpr int kOffA = 0, kOffB = kNA * kSlotA, kOffAux = kOffB + kNB * kSlotB;
+constexpr int kNA = 2, kNR = 2, kNB = 3;          // ring depths
+constexpr int kOffA = 0, kOffR = kNA * kSlotA, kOffB = kOffR + kNR * kSlotR, kOffAux = kOffB + kNB * kSlotB;
 constexpr int kOffBar = kOffAux;                  // Bars (256 B)
 constexpr int kOffNrm = kOffBar + 256;            // [tile parity 2][128] ||x||
 constexpr int kOffCtab = kOffNrm + 2 * kTile * 4; // [64] uint2: -c of a coordinate pair, bf16 hi and lo
 constexpr int kSmemBytes = kOffCtab + 64 * 8 + 1024;  // + alignment slack
-constexpr int kThreads = 576, kProdWarp0 = 8, kTmaWarp = 16, kMmaWarp = 17;
+constexpr int kThreads = 608, kProdWarp0 = 8, kTmaWarp = 16, kMmaWarp = 17, kRawWarp = 18;
 constexpr uint32_t kTmemCols = 512;               // two 256-column accumulator slots
 constexpr unsigned kFaultWait = 1u;               // fault bit: a pipeline wait ran out of its bound
 
@@ -76,7 +77,8 @@ static_assert(kSmemBytes <= 232448, "shared memory beyond the per-CTA limit");
 // ahead); "empty" takes the arrivals of whichever group read the slot, in
 // pass order.
 struct Bars {
-  uint64_t a_full[kNA], a_empty[kNA], b_full[kNB], b_empty[kNB], u_full[2], p_full[2], acc_empty[2];
+  uint64_t a_full[kNA], a_empty[kNA], r_full[kNR], r_empty[kNR], b_full[kNB], b_empty[kNB];
+  uint64_t u_full[2], p_full[2], acc_empty[2];
   uint64_t norm_ready;  // the tile's norms are in shared memory
   uint64_t idx_ready;   // the tile's index planes are in global memory
   uint64_t drain;       // every MMA of this CTA has completed
@@ -124,39 +126,15 @@ __device__ __forceinline__ void split8(const float (&f)[8], uint4& hi, uint4& lo
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Eight consecutive input elements of a row as floats (zeros past the end).
-template <typename T>
-__device__ __forceinline__ void load8(const T* p, bool valid, float (&f)[8]);
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, bool valid, float (&f)[8]) {
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-  if (valid) {
-    a = __ldcg(reinterpret_cast<const float4*>(p));
-    b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
-  }
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, bool valid, float (&f)[8]) {
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (valid) v = __ldcg(reinterpret_cast<const uint4*>(p));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    f[2 * j] = __uint_as_float(w[j] << 16);
-    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-  }
-}
-
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
 // K-major tile of 128-byte rows (8-row groups of 1024 bytes).
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
 template <typename T, int W, bool Q>
 __global__ void __launch_bounds__(kThreads, 1)
-    quantize_wide_kernel(const __grid_constant__ CUtensorMap tm_pi, const __grid_constant__ CUtensorMap tm_s,
-                         const __grid_constant__ CUtensorMap tm_sr, const WideArgs a) {
+    quantize_wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi,
+                         const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_sr,
+                         const WideArgs a) {
   constexpr bool kBf16 = sizeof(T) == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,6 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNA; ++i) {
       mbar_init(smem_u32(&bars->a_full[i]), 8);  // one arrival per producer warp
       mbar_init(smem_u32(&bars->a_empty[i]), 1);
+    }
+    for (int i = 0; i < kNR; ++i) {
+      mbar_init(smem_u32(&bars->r_full[i]), 1);
+      mbar_init(smem_u32(&bars->r_empty[i]), 8);  // one arrival per producer warp
     }
     for (int i = 0; i < kNB; ++i) {
       mbar_init(smem_u32(&bars->b_full[i]), 1);
@@ -198,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_sr);
     }
   }
+  if (warp == kRawWarp && lane == 0) tma_prefetch_desc(&tm_x);
   // -c over a pair of coordinates: entry bits (plane 0 of s, of s + 1, plane 1
   // of s, of s + 1, plane 2 of s, of s + 1), value (bf16 hi pair, bf16 lo pair)
   if (Q && threadIdx.x >= 32 * kProdWarp0 && threadIdx.x < 32 * kProdWarp0 + 64) {
@@ -242,6 +225,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       // no copy of this CTA may still be in flight when it exits
       for (int64_t j = bs > kNB ? bs - kNB : 0; j < bs; ++j)
         mbar_wait(smem_u32(&bars->b_full[j % kNB]), (uint32_t)(j / kNB) & 1u, a.fault, kFaultWait);
+    }
+  } else if (warp == kRawWarp) {
+    if (lane == 0) {
+      // The input's columns of every stage that reads them, by TMA (rows past
+      // n read as zeros), and the next tile's rows into L2 ahead of its first
+      // pass: once its input columns are all issued, in the last pass.
+      const T* x = static_cast<const T*>(a.x);
+      auto prefetch_tile = [&](int64_t tile) {
+        for (int r = 0; r < kTile; ++r) {
+          const int64_t v = tile * kTile + r;
+          if (v < a.n) bulk_prefetch_l2(x + v * a.ld, (uint32_t)(d * sizeof(T)));
+        }
+      };
+      if (blockIdx.x < a.ntiles) prefetch_tile(blockIdx.x);
+      int64_t rs = 0;  // raw stages issued
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; ok && tile < a.ntiles; tile += gridDim.x) {
+        for (int p = 0; ok && p < sc.passes(); ++p) {
+          for (int k = 0; ok && k < sc.KC; ++k) {
+            const int s = (int)(rs % kNR);
+            if (!mbar_wait(smem_u32(&bars->r_empty[s]), ((uint32_t)(rs / kNR) & 1u) ^ 1u, a.fault, kFaultWait)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = smem_u32(&bars->r_full[s]);
+            mbar_arrive_expect_tx(full, kTile * kKc * (uint32_t)sizeof(T));
+            tma_load_2d(base + kOffR + s * kSlotR, &tm_x, k * kKc, (int32_t)(tile * kTile), full);
+            ++rs;
+            const bool last = p == sc.passes() - 1;
+            if (last && k == (Q ? sc.KC - 1 : sc.KC / 2) && tile + gridDim.x < a.ntiles)
+              prefetch_tile(tile + gridDim.x);
+          }
+        }
+      }
+      for (int64_t j = rs > kNR ? rs - kNR : 0; j < rs; ++j)
+        mbar_wait(smem_u32(&bars->r_full[j % kNR]), (uint32_t)(j / kNR) & 1u, a.fault, kFaultWait);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -305,93 +324,143 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kProdWarp0) {
     // A operands.  Warp pw fills rows 16pw .. 16pw + 15, four per step: lane
     // -> row 16pw + 4i + lane/8 and 16-byte chunk c = lane % 8 (8 columns).
+    // The input's columns arrive in the raw ring by TMA; the index-plane
+    // words of a centroid stage are loaded one stage ahead.
     const int pw = warp - kProdWarp0, c = lane & 7;
     const int wi = W * d / 32;
-    const T* x = static_cast<const T*>(a.x);
-    int64_t as = 0;  // A stages filled
+    const int ust = sc.P1 * sc.KC, nst = ust + sc.P2 * 2 * sc.KC;  // A stages per tile
+    int64_t as = 0, rs = 0;  // A stages filled, raw stages consumed
+    float ss[4], inv[4];
+    uint32_t wn[4][W];       // plane words of the next centroid stage
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ss[i] = inv[i] = 0.f;
+#pragma unroll
+      for (int pl = 0; pl < W; ++pl) wn[i][pl] = 0u;
+    }
+    auto stage_pk = [&](int st, int& p, int& k) {
+      if (st < ust) {
+        p = st / sc.KC;
+        k = st - p * sc.KC;
+      } else {
+        const int s2 = st - ust;
+        p = sc.P1 + s2 / (2 * sc.KC);
+        k = s2 - (p - sc.P1) * 2 * sc.KC;
+      }
+    };
     bool ok = true;
     int it = 0;
     for (int64_t tile = blockIdx.x; ok && tile < a.ntiles; tile += gridDim.x, ++it) {
-      int r[4];
-      int64_t v[4];
-      bool val[4];
-      float ss[4], inv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        r[i] = 16 * pw + 4 * i + (lane >> 3);
-        v[i] = tile * kTile + r[i];
-        val[i] = v[i] < a.n;
-        ss[i] = 0.f;
-        inv[i] = 0.f;
-      }
-      for (int p = 0; ok && p < sc.passes(); ++p) {
+      const int64_t v0 = tile * kTile;  // row r of the tile is vector v0 + r
+      const int r0 = 16 * pw + (lane >> 3);  // rows r0 + 4i
+      for (int st = 0; st < nst; ++st) {
+        int p, k;
+        stage_pk(st, p, k);
         const bool u = p < sc.P1;
-        for (int k = 0; ok && k < sc.stages(p); ++k) {
-          if (Q && p == sc.P1 && k == sc.KC) {  // the centroid columns read the tile's index planes
-            if (!mbar_wait(smem_u32(&bars->idx_ready), (uint32_t)it & 1u, a.fault, kFaultWait)) {
-              ok = false;
-              break;
-            }
-          }
-          const int sa = (int)(as % kNA);
-          if (!mbar_wait(smem_u32(&bars->a_empty[sa]), ((uint32_t)(as / kNA) & 1u) ^ 1u, a.fault, kFaultWait)) {
+        float f[4][8];
+        if (k < sc.KC) {  // input columns k·64 .. from the raw ring
+          const int rsl = (int)(rs % kNR);
+          if (!mbar_wait(smem_u32(&bars->r_full[rsl]), (uint32_t)(rs / kNR) & 1u, a.fault, kFaultWait)) {
             ok = false;
             break;
           }
-          uint8_t* hi = smem + kOffA + sa * kSlotA;
-          uint8_t* lo = hi + kPieceA;
-          if (k < sc.KC) {  // input columns k·64 ..: x for U, x / n for P
-            float f[4][8];
+          const uint8_t* raw = smem + kOffR + rsl * kSlotR;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) load8<T>(x + (val[i] ? v[i] : 0) * a.ld + k * kKc + 8 * c, val[i], f[i]);
+          for (int i = 0; i < 4; ++i) {
+            if constexpr (kBf16) {
+              const uint4 q = *reinterpret_cast<const uint4*>(raw + (r0 + 4 * i) * (kKc * 2) + 16 * c);
+              const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (p == 0) {  // the first U pass sees every column once: ||x||² on the way
-                float s8 = 0.f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) s8 = fmaf(f[i][j], f[i][j], s8);
-                ss[i] += s8;
+              for (int j = 0; j < 4; ++j) {
+                f[i][2 * j] = __uint_as_float(w4[j] << 16);
+                f[i][2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
               }
-              if (!u) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) f[i][j] *= inv[i];
-              }
-              uint4 h4, l4;
-              split8(f[i], h4, l4);
-              *reinterpret_cast<uint4*>(hi + sw128(r[i], c)) = h4;
-              if (!(kBf16 && u)) *reinterpret_cast<uint4*>(lo + sw128(r[i], c)) = l4;
-            }
-          } else {  // centroid columns (k - KC)·64 ..: -c[idx] from the index planes
-            const int kc = k - sc.KC;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t vb = 0u;  // byte pl: plane pl's bits of the chunk's 8 coordinates
-              if (val[i]) {
-#pragma unroll
-                for (int pl = 0; pl < W; ++pl) {
-                  const uint32_t wd = __ldcg(a.idx + v[i] * wi + pl * (d / 32) + 2 * kc + (c >> 2));
-                  vb |= ((wd >> (8 * (c & 3))) & 0xFFu) << (8 * pl);
-                }
-              }
-              uint32_t h[4], l[4];
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {  // coordinates 2t, 2t + 1
-                const uint32_t g = (vb >> (2 * t)) & 0x030303u;
-                const uint2 e = ctab[(g | (g >> 6) | (g >> 12)) & 0x3Fu];
-                h[t] = e.x;
-                l[t] = e.y;
-              }
-              *reinterpret_cast<uint4*>(hi + sw128(r[i], c)) = make_uint4(h[0], h[1], h[2], h[3]);
-              *reinterpret_cast<uint4*>(lo + sw128(r[i], c)) = make_uint4(l[0], l[1], l[2], l[3]);
+            } else {
+              const float4 q0 = *reinterpret_cast<const float4*>(raw + (r0 + 4 * i) * (kKc * 4) + 32 * c);
+              const float4 q1 = *reinterpret_cast<const float4*>(raw + (r0 + 4 * i) * (kKc * 4) + 32 * c + 16);
+              f[i][0] = q0.x; f[i][1] = q0.y; f[i][2] = q0.z; f[i][3] = q0.w;
+              f[i][4] = q1.x; f[i][5] = q1.y; f[i][6] = q1.z; f[i][7] = q1.w;
             }
           }
-          // generic-proxy stores -> visible to the tensor core's reads
+          // the next TMA write into this slot (async proxy) must follow these
+          // generic-proxy reads: the mbarrier alone does not order the two proxies
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[sa]));
-          ++as;
+          if (lane == 0) mbar_arrive(smem_u32(&bars->r_empty[rsl]));
+          ++rs;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (p == 0) {  // the first U pass sees every column once: ||x||² on the way
+              if (k == 0) ss[i] = 0.f;
+              float s8 = 0.f;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) s8 = fmaf(f[i][j], f[i][j], s8);
+              ss[i] += s8;
+            }
+            if (!u) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) f[i][j] *= inv[i];
+            }
+          }
         }
-        if (ok && p == 0) {
+        const int sa = (int)(as % kNA);
+        if (!mbar_wait(smem_u32(&bars->a_empty[sa]), ((uint32_t)(as / kNA) & 1u) ^ 1u, a.fault, kFaultWait)) {
+          ok = false;
+          break;
+        }
+        uint8_t* hi = smem + kOffA + sa * kSlotA;
+        uint8_t* lo = hi + kPieceA;
+        if (k < sc.KC) {  // x for U, x / n for P, split into bf16 hi and lo
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 h4, l4;
+            split8(f[i], h4, l4);
+            *reinterpret_cast<uint4*>(hi + sw128(r0 + 4 * i, c)) = h4;
+            if (!(kBf16 && u)) *reinterpret_cast<uint4*>(lo + sw128(r0 + 4 * i, c)) = l4;
+          }
+        } else {  // centroid columns (k - KC)·64 ..: -c[idx] from the index planes
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t vb = 0u;  // byte pl: plane pl's bits of the chunk's 8 coordinates
+#pragma unroll
+            for (int pl = 0; pl < W; ++pl) vb |= ((wn[i][pl] >> (8 * (c & 3))) & 0xFFu) << (8 * pl);
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {  // coordinates 2t, 2t + 1
+              const uint32_t g = (vb >> (2 * t)) & 0x030303u;
+              const uint2 e = ctab[(g | (g >> 6) | (g >> 12)) & 0x3Fu];
+              h[t] = e.x;
+              l[t] = e.y;
+            }
+            *reinterpret_cast<uint4*>(hi + sw128(r0 + 4 * i, c)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(lo + sw128(r0 + 4 * i, c)) = make_uint4(l[0], l[1], l[2], l[3]);
+          }
+        }
+        // generic-proxy stores -> visible to the tensor core's reads
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[sa]));
+        ++as;
+        if (Q && st + 1 < nst) {  // the next stage's index words, when it is a centroid stage
+          int p1, k1;
+          stage_pk(st + 1, p1, k1);
+          if (k1 >= sc.KC) {
+            if (p1 == sc.P1 && k1 == sc.KC &&  // the tile's planes must be written first
+                !mbar_wait(smem_u32(&bars->idx_ready), (uint32_t)it & 1u, a.fault, kFaultWait)) {
+              ok = false;
+              break;
+            }
+            const int kc = k1 - sc.KC;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int64_t v = v0 + r0 + 4 * i;
+#pragma unroll
+              for (int pl = 0; pl < W; ++pl)
+                wn[i][pl] = v < a.n ? __ldcg(a.idx + v * wi + pl * (d / 32) + 2 * kc + (c >> 2)) : 0u;
+            }
+          }
+        }
+        if (p == 0 && k == sc.KC - 1) {
           // the eight lanes of a row hold its eight column chunks: the norms
           float* nrm = nrm_s + (it & 1) * kTile;
 #pragma unroll
@@ -403,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float nn = sqrtf(t);
             inv[i] = nn > 0.f ? 1.0f / nn : 0.f;
             if (c == 0) {
-              nrm[r[i]] = nn;
-              if (val[i]) a.norm[v[i]] = nn;
+              nrm[r0 + 4 * i] = nn;
+              if (v0 + r0 + 4 * i < a.n) a.norm[v0 + r0 + 4 * i] = nn;
             }
           }
           __syncwarp();
@@ -552,31 +621,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+struct WideMaps {
+  CUtensorMap x, pi, s, sr;
+};
+
 template <typename T, int W, bool Q>
-tq_status launch_wide(const CUtensorMap& mp, const CUtensorMap& ms, const CUtensorMap& msr, const WideArgs& a,
-                      cudaStream_t st) {
+tq_status launch_wide(const WideMaps& mp, const WideArgs& a, cudaStream_t st) {
   auto kern = quantize_wide_kernel<T, W, Q>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return TQ_ERR_CUDA;
   const int grid = (int)std::min<int64_t>(a.ntiles, tq::sm_count());
-  kern<<<grid, kThreads, kSmemBytes, st>>>(mp, ms, msr, a);
+  kern<<<grid, kThreads, kSmemBytes, st>>>(mp.x, mp.pi, mp.s, mp.sr, a);
   return tq::launch_status();
 }
 
 template <typename T>
-tq_status launch_wide_t(int w, bool q, const CUtensorMap& mp, const CUtensorMap& ms, const CUtensorMap& msr,
-                        const WideArgs& a, cudaStream_t st) {
+tq_status launch_wide_t(int w, bool q, const WideMaps& mp, const WideArgs& a, cudaStream_t st) {
   switch (w) {
-    case 1: return q ? launch_wide<T, 1, true>(mp, ms, msr, a, st) : launch_wide<T, 1, false>(mp, ms, msr, a, st);
-    case 2: return q ? launch_wide<T, 2, true>(mp, ms, msr, a, st) : launch_wide<T, 2, false>(mp, ms, msr, a, st);
-    default: return q ? launch_wide<T, 3, true>(mp, ms, msr, a, st) : launch_wide<T, 3, false>(mp, ms, msr, a, st);
+    case 1: return q ? launch_wide<T, 1, true>(mp, a, st) : launch_wide<T, 1, false>(mp, a, st);
+    case 2: return q ? launch_wide<T, 2, true>(mp, a, st) : launch_wide<T, 2, false>(mp, a, st);
+    default: return q ? launch_wide<T, 3, true>(mp, a, st) : launch_wide<T, 3, false>(mp, a, st);
   }
+}
+
+// Input rows by TMA: n x d elements of row stride ld, 64-column x 128-row
+// boxes without swizzle (rows past n read as zeros).
+bool map_input(CUtensorMap* map, const void* x, tq_dtype dtype, int64_t n, int d, int64_t ld) {
+  auto fn = tq::tensor_map_encoder();
+  if (!fn) return false;
+  const size_t esz = dtype == TQ_F32 ? 4 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)n};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
+  cuuint32_t box[2] = {(cuuint32_t)kKc, (cuuint32_t)kTile};
+  cuuint32_t es[2] = {1, 1};
+  return fn(map, dtype == TQ_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
 bool tq::quantize_wide_supported(const tq_plan* plan, const tq_records* out) {
-  return plan->d % 256 == 0 && plan->d >= 256 && plan->d <= 1024 &&
+  return plan->d % 256 == 0 && plan->d >= 256 && plan->d <= 1024 && tq::tensor_map_encoder() != nullptr &&
          (plan->m == 0 || (plan->m == plan->d && plan->s_x_bf16 != nullptr)) && out->layout == TQ_LAYOUT_ROWS;
 }
 
@@ -584,11 +670,13 @@ tq_status tq::quantize_wide(const tq_plan* plan, const void* x, tq_dtype dtype, 
                             const tq_records* out, int64_t row0, cudaStream_t st) {
   const int d = plan->d, m = plan->m, w = plan->w;
   const bool q = m > 0;
-  CUtensorMap mp, ms, msr;
+  if (n >= (int64_t(1) << 31)) return TQ_ERR_ARG;  // TMA row coordinates are 32-bit
+  WideMaps mp;
   // (m = 0: the two S maps go unused)
-  if (!tq::map_bf16_tiles(&mp, plan->pi_bf16, 2 * (uint64_t)d, d, d, kCols) ||
-      !tq::map_bf16_tiles(&ms, q ? plan->s_x_bf16 : plan->pi_bf16, 2 * (uint64_t)(q ? m : d), d, d, kCols) ||
-      !tq::map_bf16_tiles(&msr, q ? plan->s_bf16 : plan->pi_bf16, 2 * (uint64_t)(q ? m : d), d, d, kCols))
+  if (!map_input(&mp.x, x, dtype, n, d, ld_x) ||
+      !tq::map_bf16_tiles(&mp.pi, plan->pi_bf16, 2 * (uint64_t)d, d, d, kCols) ||
+      !tq::map_bf16_tiles(&mp.s, q ? plan->s_x_bf16 : plan->pi_bf16, 2 * (uint64_t)(q ? m : d), d, d, kCols) ||
+      !tq::map_bf16_tiles(&mp.sr, q ? plan->s_bf16 : plan->pi_bf16, 2 * (uint64_t)(q ? m : d), d, d, kCols))
     return TQ_ERR_CUDA;
   WideArgs a{};
   a.x = x;
@@ -605,6 +693,5 @@ tq_status tq::quantize_wide(const tq_plan* plan, const void* x, tq_dtype dtype, 
   a.rnorm = q ? out->rnorm + row0 : nullptr;
   a.fault = tq::fault_word();
   if (!a.fault) return TQ_ERR_CUDA;
-  return dtype == TQ_F32 ? launch_wide_t<float>(w, q, mp, ms, msr, a, st)
-                         : launch_wide_t<__nv_bfloat16>(w, q, mp, ms, msr, a, st);
+  return dtype == TQ_F32 ? launch_wide_t<float>(w, q, mp, a, st) : launch_wide_t<__nv_bfloat16>(w, q, mp, a, st);
 }

@@ -304,7 +304,10 @@ __global__ void __launch_bounds__(kThreads, 2) search_score_kernel(SearchTcArgs 
         }
       }
     }
-    __syncthreads();  // every warp is done with this buffer
+    // every warp is done with this buffer; its generic-proxy reads are ordered
+    // before the bulk copy (async proxy) that refills it
+    fence_proxy_async_smem();
+    __syncthreads();
     if (threadIdx.x == 0 && gc + 2 < total_chunks && alive) {
       issue(gc + 2);
       nissued = gc + 3;
@@ -359,7 +362,10 @@ __global__ void __launch_bounds__(kThreads, 2) search_score_kernel(SearchTcArgs 
         }
       }
     }
-    __syncthreads();  // every warp is done with this buffer
+    // every warp is done with this buffer; its generic-proxy reads are ordered
+    // before the bulk copy (async proxy) that refills it
+    fence_proxy_async_smem();
+    __syncthreads();
     if (threadIdx.x == 0 && gc + 2 < total_chunks && alive) {
       issue(gc + 2);
       nissued = gc + 3;
