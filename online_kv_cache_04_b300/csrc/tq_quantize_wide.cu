@@ -126,6 +126,21 @@ __device__ __forceinline__ void split8(const float (&f)[8], uint4& hi, uint4& lo
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
 // K-major tile of 128-byte rows (8-row groups of 1024 bytes).
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
@@ -251,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t full = smem_u32(&bars->r_full[s]);
             mbar_arrive_expect_tx(full, kTile * kKc * (uint32_t)sizeof(T));
-            tma_load_2d(base + kOffR + s * kSlotR, &tm_x, k * kKc, (int32_t)(tile * kTile), full);
+            // 128-byte rows: fp32 in two 32-column halves, bf16 in one box
+            for (int h = 0; h < (int)sizeof(T) / 2; ++h)
+              tma_load_2d(base + kOffR + s * kSlotR + h * (kSlotR / 2), &tm_x, k * kKc + h * 32,
+                          (int32_t)(tile * kTile), full);
             ++rs;
             const bool last = p == sc.passes() - 1;
             if (last && k == (Q ? sc.KC - 1 : sc.KC / 2) && tile + gridDim.x < a.ntiles)
@@ -322,22 +340,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&bars->drain), 0u, a.fault, kFaultWait);
     }
   } else if (warp >= kProdWarp0) {
-    // A operands.  Warp pw fills rows 16pw .. 16pw + 15, four per step: lane
-    // -> row 16pw + 4i + lane/8 and 16-byte chunk c = lane % 8 (8 columns).
-    // The input's columns arrive in the raw ring by TMA; the index-plane
-    // words of a centroid stage are loaded one stage ahead.
-    const int pw = warp - kProdWarp0, c = lane & 7;
+    // A operands.  Warp pw fills rows ra = 16pw + lane % 8 and rb = ra + 8,
+    // 16-byte chunks (8 columns) cc = lane / 8 and cc + 4 of each: in every
+    // 8-lane phase the rows differ, so the 128-byte-swizzled reads and writes
+    // meet no bank conflicts.  The input's columns arrive in the raw ring by
+    // TMA (128-byte swizzled rows: fp32 as two 32-column halves, bf16 as one
+    // box); the index-plane words of a centroid stage are loaded one stage
+    // ahead.
+    const int pw = warp - kProdWarp0, cc = lane >> 3;
+    const int ra = 16 * pw + (lane & 7), rb = ra + 8;
     const int wi = W * d / 32;
     const int ust = sc.P1 * sc.KC, nst = ust + sc.P2 * 2 * sc.KC;  // A stages per tile
     int64_t as = 0, rs = 0;  // A stages filled, raw stages consumed
-    float ss[4], inv[4];
-    uint32_t wn[4][W];       // plane words of the next centroid stage
+    float ssa = 0.f, ssb = 0.f, inva = 0.f, invb = 0.f;
+    uint2 wn[2][W];          // plane words (2kc, 2kc + 1) of rows ra, rb for the next centroid stage
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      ss[i] = inv[i] = 0.f;
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int pl = 0; pl < W; ++pl) wn[i][pl] = 0u;
-    }
+      for (int pl = 0; pl < W; ++pl) wn[h][pl] = make_uint2(0u, 0u);
+    const uint32_t ctab_s = smem_u32(ctab);
     auto stage_pk = [&](int st, int& p, int& k) {
       if (st < ust) {
         p = st / sc.KC;
@@ -350,13 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     int it = 0;
+    int pending_r = -1;  // raw slot read by the stage just published
     for (int64_t tile = blockIdx.x; ok && tile < a.ntiles; tile += gridDim.x, ++it) {
       const int64_t v0 = tile * kTile;  // row r of the tile is vector v0 + r
-      const int r0 = 16 * pw + (lane >> 3);  // rows r0 + 4i
       for (int st = 0; st < nst; ++st) {
         int p, k;
         stage_pk(st, p, k);
         const bool u = p < sc.P1;
+        // items q = (row ra, chunk cc), (ra, cc + 4), (rb, cc), (rb, cc + 4)
         float f[4][8];
         if (k < sc.KC) {  // input columns k·64 .. from the raw ring
           const int rsl = (int)(rs % kNR);
@@ -364,43 +386,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const uint8_t* raw = smem + kOffR + rsl * kSlotR;
+          const uint32_t raw = base + kOffR + rsl * kSlotR;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int q = 0; q < 4; ++q) {
+            const int r = q < 2 ? ra : rb, c = cc + 4 * (q & 1);
             if constexpr (kBf16) {
-              const uint4 q = *reinterpret_cast<const uint4*>(raw + (r0 + 4 * i) * (kKc * 2) + 16 * c);
-              const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+              const uint4 w4 = lds128(raw + sw128(r, c));
+              const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                f[i][2 * j] = __uint_as_float(w4[j] << 16);
-                f[i][2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+                f[q][2 * j] = __uint_as_float(wv[j] << 16);
+                f[q][2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
               }
-            } else {
-              const float4 q0 = *reinterpret_cast<const float4*>(raw + (r0 + 4 * i) * (kKc * 4) + 32 * c);
-              const float4 q1 = *reinterpret_cast<const float4*>(raw + (r0 + 4 * i) * (kKc * 4) + 32 * c + 16);
-              f[i][0] = q0.x; f[i][1] = q0.y; f[i][2] = q0.z; f[i][3] = q0.w;
-              f[i][4] = q1.x; f[i][5] = q1.y; f[i][6] = q1.z; f[i][7] = q1.w;
+            } else {  // columns 8c .. 8c + 7: half c / 4, chunks 2(c % 4) and 2(c % 4) + 1 of its row
+              const uint32_t hb = raw + (c >> 2) * (kSlotR / 2);
+              const uint4 w0 = lds128(hb + sw128(r, 2 * (c & 3))), w1 = lds128(hb + sw128(r, 2 * (c & 3) + 1));
+              f[q][0] = __uint_as_float(w0.x); f[q][1] = __uint_as_float(w0.y);
+              f[q][2] = __uint_as_float(w0.z); f[q][3] = __uint_as_float(w0.w);
+              f[q][4] = __uint_as_float(w1.x); f[q][5] = __uint_as_float(w1.y);
+              f[q][6] = __uint_as_float(w1.z); f[q][7] = __uint_as_float(w1.w);
             }
           }
-          // the next TMA write into this slot (async proxy) must follow these
-          // generic-proxy reads: the mbarrier alone does not order the two proxies
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bars->r_empty[rsl]));
+          pending_r = rsl;
           ++rs;
+          if (p == 0) {  // the first U pass sees every column once: ||x||² on the way
+            if (k == 0) ssa = ssb = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (p == 0) {  // the first U pass sees every column once: ||x||² on the way
-              if (k == 0) ss[i] = 0.f;
+            for (int q = 0; q < 4; ++q) {
               float s8 = 0.f;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) s8 = fmaf(f[i][j], f[i][j], s8);
-              ss[i] += s8;
+              for (int j = 0; j < 8; ++j) s8 = fmaf(f[q][j], f[q][j], s8);
+              if (q < 2) ssa += s8;
+              else ssb += s8;
             }
-            if (!u) {
+          }
+          if (!u) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) f[i][j] *= inv[i];
-            }
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) f[q][j] *= q < 2 ? inva : invb;
           }
         }
         const int sa = (int)(as % kNA);
@@ -408,38 +432,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* hi = smem + kOffA + sa * kSlotA;
-        uint8_t* lo = hi + kPieceA;
+        const uint32_t hi = base + kOffA + sa * kSlotA, lo = hi + kPieceA;
         if (k < sc.KC) {  // x for U, x / n for P, split into bf16 hi and lo
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int q = 0; q < 4; ++q) {
+            const int r = q < 2 ? ra : rb, c = cc + 4 * (q & 1);
             uint4 h4, l4;
-            split8(f[i], h4, l4);
-            *reinterpret_cast<uint4*>(hi + sw128(r0 + 4 * i, c)) = h4;
-            if (!(kBf16 && u)) *reinterpret_cast<uint4*>(lo + sw128(r0 + 4 * i, c)) = l4;
+            split8(f[q], h4, l4);
+            sts128(hi + sw128(r, c), h4);
+            if (!(kBf16 && u)) sts128(lo + sw128(r, c), l4);
           }
         } else {  // centroid columns (k - KC)·64 ..: -c[idx] from the index planes
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int q = 0; q < 4; ++q) {
+            const int r = q < 2 ? ra : rb, c = cc + 4 * (q & 1);
             uint32_t vb = 0u;  // byte pl: plane pl's bits of the chunk's 8 coordinates
 #pragma unroll
-            for (int pl = 0; pl < W; ++pl) vb |= ((wn[i][pl] >> (8 * (c & 3))) & 0xFFu) << (8 * pl);
+            for (int pl = 0; pl < W; ++pl) {
+              const uint2 w2 = wn[q >> 1][pl];
+              vb |= (((q & 1) ? w2.y : w2.x) >> (8 * cc) & 0xFFu) << (8 * pl);
+            }
             uint32_t h[4], l[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {  // coordinates 2t, 2t + 1
               const uint32_t g = (vb >> (2 * t)) & 0x030303u;
-              const uint2 e = ctab[(g | (g >> 6) | (g >> 12)) & 0x3Fu];
+              const uint2 e = lds64(ctab_s + 8 * ((g | (g >> 6) | (g >> 12)) & 0x3Fu));
               h[t] = e.x;
               l[t] = e.y;
             }
-            *reinterpret_cast<uint4*>(hi + sw128(r0 + 4 * i, c)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(lo + sw128(r0 + 4 * i, c)) = make_uint4(l[0], l[1], l[2], l[3]);
+            sts128(hi + sw128(r, c), make_uint4(h[0], h[1], h[2], h[3]));
+            sts128(lo + sw128(r, c), make_uint4(l[0], l[1], l[2], l[3]));
           }
         }
-        // generic-proxy stores -> visible to the tensor core's reads
+        // One proxy fence orders this stage's generic-proxy accesses before the
+        // async proxy's: the A stores before the tensor core reads them, and
+        // the raw reads before the next TMA write into that raw slot.
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[sa]));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&bars->a_full[sa]));
+          if (pending_r >= 0) mbar_arrive(smem_u32(&bars->r_empty[pending_r]));
+        }
+        pending_r = -1;
         ++as;
         if (Q && st + 1 < nst) {  // the next stage's index words, when it is a centroid stage
           int p1, k1;
@@ -452,28 +486,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int kc = k1 - sc.KC;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int64_t v = v0 + r0 + 4 * i;
+            for (int h = 0; h < 2; ++h) {
+              const int64_t v = v0 + (h ? rb : ra);
 #pragma unroll
               for (int pl = 0; pl < W; ++pl)
-                wn[i][pl] = v < a.n ? __ldcg(a.idx + v * wi + pl * (d / 32) + 2 * kc + (c >> 2)) : 0u;
+                wn[h][pl] = v < a.n ? __ldcg(reinterpret_cast<const uint2*>(a.idx + v * wi + pl * (d / 32) + 2 * kc))
+                                    : make_uint2(0u, 0u);
             }
           }
         }
         if (p == 0 && k == sc.KC - 1) {
-          // the eight lanes of a row hold its eight column chunks: the norms
+          // the four lanes of a row (cc = 0..3) hold its eight column chunks: the norms
           float* nrm = nrm_s + (it & 1) * kTile;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float t = ss[i];
-            t += __shfl_xor_sync(0xffffffffu, t, 1);
-            t += __shfl_xor_sync(0xffffffffu, t, 2);
-            t += __shfl_xor_sync(0xffffffffu, t, 4);
+          for (int h = 0; h < 2; ++h) {
+            float t = h ? ssb : ssa;
+            t += __shfl_xor_sync(0xffffffffu, t, 8);
+            t += __shfl_xor_sync(0xffffffffu, t, 16);
             const float nn = sqrtf(t);
-            inv[i] = nn > 0.f ? 1.0f / nn : 0.f;
-            if (c == 0) {
-              nrm[r0 + 4 * i] = nn;
-              if (v0 + r0 + 4 * i < a.n) a.norm[v0 + r0 + 4 * i] = nn;
+            const float iv = nn > 0.f ? 1.0f / nn : 0.f;
+            if (h) invb = iv;
+            else inva = iv;
+            const int r = h ? rb : ra;
+            if (cc == 0) {
+              nrm[r] = nn;
+              if (v0 + r < a.n) a.norm[v0 + r] = nn;
             }
           }
           __syncwarp();
@@ -644,18 +681,19 @@ tq_status launch_wide_t(int w, bool q, const WideMaps& mp, const WideArgs& a, cu
   }
 }
 
-// Input rows by TMA: n x d elements of row stride ld, 64-column x 128-row
-// boxes without swizzle (rows past n read as zeros).
+// Input rows by TMA: n x d elements of row stride ld, boxes of 128-byte rows
+// (32 fp32 or 64 bf16 columns) x 128 rows, 128-byte swizzle (rows past n read
+// as zeros).
 bool map_input(CUtensorMap* map, const void* x, tq_dtype dtype, int64_t n, int d, int64_t ld) {
   auto fn = tq::tensor_map_encoder();
   if (!fn) return false;
   const size_t esz = dtype == TQ_F32 ? 4 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)n};
   cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
-  cuuint32_t box[2] = {(cuuint32_t)kKc, (cuuint32_t)kTile};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)kTile};
   cuuint32_t es[2] = {1, 1};
   return fn(map, dtype == TQ_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-            const_cast<void*>(x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            const_cast<void*>(x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
