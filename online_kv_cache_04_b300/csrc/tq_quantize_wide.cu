@@ -27,19 +27,21 @@
 // P = (x/n)·Sᵀ + (-c[idx])·(S Πᵀ)ᵀ (K = 2d: the input's columns, then the
 // centroid values'), each pass into one of two 256-column TMEM slots so that
 // the epilogue of one pass overlaps the products of the next.  Warp roles
-// (576 threads):
+// (864 threads):
 //   warps 0-3   epilogue of the U passes (warp = TMEM lane quadrant = 32
 //               vectors): u = U / n, binary-search bucketize into index
 //               planes, ||ρ||², ||r||
 //   warps 4-7   epilogue of the P passes: sign words (idle when m = 0)
-//   warps 8-15  A operands, 128 rows x 64 columns per stage, 128-byte
+//   warps 8-23  A operands, 128 rows x 64 columns per stage, 128-byte
 //               swizzled K-major: x (or x / n) split into bf16 hi and lo, or
 //               the centroid values -c[idx] (hi, lo) looked up per pair of
 //               coordinates in a 64-entry table; the first U pass reads
 //               every column of the tile once, so it also yields ||x||
-//   warp 16     B operands by TMA: 256 rows x 64 columns of Π, S or S Πᵀ,
+//   warp 24     B operands by TMA: 256 rows x 64 columns of Π, S or S Πᵀ,
 //               hi or lo, per stage
-//   warp 17     MMA issue (one thread), TMEM owner
+//   warp 25     MMA issue (one thread), TMEM owner
+//   warp 26     the input's columns by TMA into a raw ring, and the next
+//               tile's rows into L2 during the last pass
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -66,7 +68,8 @@ constexpr int kOffBar = kOffAux;                  // Bars (256 B)
 constexpr int kOffNrm = kOffBar + 256;            // [tile parity 2][128] ||x||
 constexpr int kOffCtab = kOffNrm + 2 * kTile * 4; // [64] uint2: -c of a coordinate pair, bf16 hi and lo
 constexpr int kSmemBytes = kOffCtab + 64 * 8 + 1024;  // + alignment slack
-constexpr int kThreads = 608, kProdWarp0 = 8, kTmaWarp = 16, kMmaWarp = 17, kRawWarp = 18;
+constexpr int kProdWarp0 = 8, kProdWarps = 16;  // A-operand producers: warps 8 .. 23
+constexpr int kTmaWarp = 24, kMmaWarp = 25, kRawWarp = 26, kThreads = 32 * 27;
 constexpr uint32_t kTmemCols = 512;               // two 256-column accumulator slots
 constexpr unsigned kFaultWait = 1u;               // fault bit: a pipeline wait ran out of its bound
 
@@ -163,12 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNA; ++i) {
-      mbar_init(smem_u32(&bars->a_full[i]), 8);  // one arrival per producer warp
+      mbar_init(smem_u32(&bars->a_full[i]), kProdWarps);  // one arrival per producer warp
       mbar_init(smem_u32(&bars->a_empty[i]), 1);
     }
     for (int i = 0; i < kNR; ++i) {
       mbar_init(smem_u32(&bars->r_full[i]), 1);
-      mbar_init(smem_u32(&bars->r_empty[i]), 8);  // one arrival per producer warp
+      mbar_init(smem_u32(&bars->r_empty[i]), kProdWarps);  // one arrival per producer warp
     }
     for (int i = 0; i < kNB; ++i) {
       mbar_init(smem_u32(&bars->b_full[i]), 1);
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->p_full[s]), 1);
       mbar_init(smem_u32(&bars->acc_empty[s]), 4);  // the four warps of the pass's epilogue group
     }
-    mbar_init(smem_u32(&bars->norm_ready), 8);
+    mbar_init(smem_u32(&bars->norm_ready), kProdWarps);
     mbar_init(smem_u32(&bars->idx_ready), 4);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_mbar_init();
@@ -339,25 +342,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(smem_u32(&bars->drain));
       mbar_wait(smem_u32(&bars->drain), 0u, a.fault, kFaultWait);
     }
-  } else if (warp >= kProdWarp0) {
-    // A operands.  Warp pw fills rows ra = 16pw + lane % 8 and rb = ra + 8,
-    // 16-byte chunks (8 columns) cc = lane / 8 and cc + 4 of each: in every
-    // 8-lane phase the rows differ, so the 128-byte-swizzled reads and writes
-    // meet no bank conflicts.  The input's columns arrive in the raw ring by
+  } else if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
+    // A operands.  Warp pw fills row r = 8pw + lane % 8, 16-byte chunks (8
+    // columns) cc = lane / 8 and cc + 4: in every 8-lane phase the rows
+    // differ, so the 128-byte-swizzled reads and writes meet no bank conflicts.  The input's columns arrive in the raw ring by
     // TMA (128-byte swizzled rows: fp32 as two 32-column halves, bf16 as one
     // box); the index-plane words of a centroid stage are loaded one stage
     // ahead.
     const int pw = warp - kProdWarp0, cc = lane >> 3;
-    const int ra = 16 * pw + (lane & 7), rb = ra + 8;
+    const int r = 8 * pw + (lane & 7);
     const int wi = W * d / 32;
     const int ust = sc.P1 * sc.KC, nst = ust + sc.P2 * 2 * sc.KC;  // A stages per tile
     int64_t as = 0, rs = 0;  // A stages filled, raw stages consumed
-    float ssa = 0.f, ssb = 0.f, inva = 0.f, invb = 0.f;
-    uint2 wn[2][W];          // plane words (2kc, 2kc + 1) of rows ra, rb for the next centroid stage
+    float ss = 0.f, inv = 0.f;
+    uint2 wn[W];             // plane words (2kc, 2kc + 1) of row r for the next centroid stage
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int pl = 0; pl < W; ++pl) wn[h][pl] = make_uint2(0u, 0u);
+    for (int pl = 0; pl < W; ++pl) wn[pl] = make_uint2(0u, 0u);
     const uint32_t ctab_s = smem_u32(ctab);
     auto stage_pk = [&](int st, int& p, int& k) {
       if (st < ust) {
@@ -378,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int p, k;
         stage_pk(st, p, k);
         const bool u = p < sc.P1;
-        // items q = (row ra, chunk cc), (ra, cc + 4), (rb, cc), (rb, cc + 4)
-        float f[4][8];
+        // items q: chunk cc + 4q of row r
+        float f[2][8];
         if (k < sc.KC) {  // input columns k·64 .. from the raw ring
           const int rsl = (int)(rs % kNR);
           if (!mbar_wait(smem_u32(&bars->r_full[rsl]), (uint32_t)(rs / kNR) & 1u, a.fault, kFaultWait)) {
@@ -388,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t raw = base + kOffR + rsl * kSlotR;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = q < 2 ? ra : rb, c = cc + 4 * (q & 1);
+          for (int q = 0; q < 2; ++q) {
+            const int c = cc + 4 * q;
             if constexpr (kBf16) {
               const uint4 w4 = lds128(raw + sw128(r, c));
               const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -410,21 +410,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           pending_r = rsl;
           ++rs;
           if (p == 0) {  // the first U pass sees every column once: ||x||² on the way
-            if (k == 0) ssa = ssb = 0.f;
+            if (k == 0) ss = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
               float s8 = 0.f;
 #pragma unroll
               for (int j = 0; j < 8; ++j) s8 = fmaf(f[q][j], f[q][j], s8);
-              if (q < 2) ssa += s8;
-              else ssb += s8;
+              ss += s8;
             }
           }
           if (!u) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 2; ++q)
 #pragma unroll
-              for (int j = 0; j < 8; ++j) f[q][j] *= q < 2 ? inva : invb;
+              for (int j = 0; j < 8; ++j) f[q][j] *= inv;
           }
         }
         const int sa = (int)(as % kNA);
@@ -435,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t hi = base + kOffA + sa * kSlotA, lo = hi + kPieceA;
         if (k < sc.KC) {  // x for U, x / n for P, split into bf16 hi and lo
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = q < 2 ? ra : rb, c = cc + 4 * (q & 1);
+          for (int q = 0; q < 2; ++q) {
+            const int c = cc + 4 * q;
             uint4 h4, l4;
             split8(f[q], h4, l4);
             sts128(hi + sw128(r, c), h4);
@@ -444,14 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {  // centroid columns (k - KC)·64 ..: -c[idx] from the index planes
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = q < 2 ? ra : rb, c = cc + 4 * (q & 1);
+          for (int q = 0; q < 2; ++q) {
+            const int c = cc + 4 * q;
             uint32_t vb = 0u;  // byte pl: plane pl's bits of the chunk's 8 coordinates
 #pragma unroll
-            for (int pl = 0; pl < W; ++pl) {
-              const uint2 w2 = wn[q >> 1][pl];
-              vb |= (((q & 1) ? w2.y : w2.x) >> (8 * cc) & 0xFFu) << (8 * pl);
-            }
+            for (int pl = 0; pl < W; ++pl) vb |= ((q ? wn[pl].y : wn[pl].x) >> (8 * cc) & 0xFFu) << (8 * pl);
             uint32_t h[4], l[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {  // coordinates 2t, 2t + 1
@@ -485,33 +481,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const int kc = k1 - sc.KC;
+            const int64_t v = v0 + r;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int64_t v = v0 + (h ? rb : ra);
-#pragma unroll
-              for (int pl = 0; pl < W; ++pl)
-                wn[h][pl] = v < a.n ? __ldcg(reinterpret_cast<const uint2*>(a.idx + v * wi + pl * (d / 32) + 2 * kc))
-                                    : make_uint2(0u, 0u);
-            }
+            for (int pl = 0; pl < W; ++pl)
+              wn[pl] = v < a.n ? __ldcg(reinterpret_cast<const uint2*>(a.idx + v * wi + pl * (d / 32) + 2 * kc))
+                               : make_uint2(0u, 0u);
           }
         }
         if (p == 0 && k == sc.KC - 1) {
           // the four lanes of a row (cc = 0..3) hold its eight column chunks: the norms
           float* nrm = nrm_s + (it & 1) * kTile;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float t = h ? ssb : ssa;
-            t += __shfl_xor_sync(0xffffffffu, t, 8);
-            t += __shfl_xor_sync(0xffffffffu, t, 16);
-            const float nn = sqrtf(t);
-            const float iv = nn > 0.f ? 1.0f / nn : 0.f;
-            if (h) invb = iv;
-            else inva = iv;
-            const int r = h ? rb : ra;
-            if (cc == 0) {
-              nrm[r] = nn;
-              if (v0 + r < a.n) a.norm[v0 + r] = nn;
-            }
+          float t = ss;
+          t += __shfl_xor_sync(0xffffffffu, t, 8);
+          t += __shfl_xor_sync(0xffffffffu, t, 16);
+          const float nn = sqrtf(t);
+          inv = nn > 0.f ? 1.0f / nn : 0.f;
+          if (cc == 0) {
+            nrm[r] = nn;
+            if (v0 + r < a.n) a.norm[v0 + r] = nn;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->norm_ready));
@@ -555,15 +542,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t* oidx = a.idx + v * wi + p * 8;  // word j of plane pl at pl·(d/32) + j
 #pragma unroll 1
             for (int j = 0; j < 8; ++j) {
-              uint32_t uv[32];
-              tmem_ld32(tmem + lane_base + kCols * slot + 32 * j, uv);
-              tmem_ld_wait();
               uint32_t pw[W];
 #pragma unroll
               for (int pl = 0; pl < W; ++pl) pw[pl] = 0u;
 #pragma unroll
-              for (int jj = 0; jj < 16; ++jj) {
-                const uint64_t u2 = f2_mul(f2_pack(__uint_as_float(uv[2 * jj]), __uint_as_float(uv[2 * jj + 1])), inv2);
+              for (int half = 0; half < 2; ++half) {  // 16 columns per TMEM load
+              uint32_t uv[16];
+              tmem_ld16(tmem + lane_base + kCols * slot + 32 * j + 16 * half, uv);
+              tmem_ld_wait();
+#pragma unroll
+              for (int jj = 8 * half; jj < 8 * half + 8; ++jj) {
+                const uint64_t u2 = f2_mul(f2_pack(__uint_as_float(uv[2 * jj - 16 * half]),
+                                                   __uint_as_float(uv[2 * jj + 1 - 16 * half])), inv2);
                 const float2 uu = f2_unpack(u2);
                 float cv[2];
 #pragma unroll
@@ -599,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint64_t rho2 = f2_fma(f2_pack(cv[0], cv[1]), nlive2, u2);  // u - c[idx]; 0 for a zero vector
                   rsq2 = f2_fma(rho2, rho2, rsq2);
                 }
+              }
               }
               if (valid) {
 #pragma unroll
