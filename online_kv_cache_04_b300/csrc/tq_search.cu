@@ -7,12 +7,13 @@
 // The k best are returned in descending order; equal scores go to the lower
 // index (the order (score desc, index asc) is total, so selection is exact).
 //
-// Kernels: query prep (shared with decode); when d and m are multiples of
-// 128, the tensor-core score kernel of tq_search_tc.cu, which keeps each
-// query's k best per CTA as it goes, then a merge of those candidate lists;
-// otherwise the SIMT score kernel below writes the nq x n score matrix to the
-// workspace and two selection passes follow (per chunk of vectors, then a
-// merge of the per-chunk candidates).
+// Kernels: query prep (shared with decode); for d a multiple of 256 (m = d or
+// 0) and k <= 16, the tcgen05 kernel of tq_search_wide.cu; otherwise, when d
+// and m are multiples of 128, the warp-MMA kernel of tq_search_tc.cu.  Both
+// keep each query's k best per CTA as they go, and a merge of those candidate
+// lists follows.  Otherwise the SIMT score kernel below writes the nq x n
+// score matrix to the workspace and two selection passes follow (per chunk of
+// vectors, then a merge of the per-chunk candidates).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -35,15 +36,16 @@ struct SearchLayout {
 // lists, or the general path's score matrix and per-chunk candidates.
 SearchLayout layout(const tq_plan* plan, int nq, int64_t n, int k) {
   const int d = plan->d, m = plan->m;
-  const bool tc = d % 128 == 0 && m % 128 == 0;
+  const bool wide = tq::search_wide_supported(plan, k);
+  const bool tc = wide || (d % 128 == 0 && m % 128 == 0);
   SearchLayout l{};
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  l.nchunks = tc ? tq::search_tc_vchunks(n, nq) : tq::cdiv(n, kChunk);
+  l.nchunks = wide ? tq::search_wide_groups(nq) : tc ? tq::search_tc_vchunks(n, nq) : tq::cdiv(n, kChunk);
   size_t o = 0;
   l.qt = o; o += up(sizeof(float) * size_t(nq) * d);
   l.st = o; o += up(sizeof(float) * size_t(nq) * m);
   l.table = o;
-  if (tc) o += up(tq::search_tc_table_bytes(plan, nq));
+  if (tc) o += up(wide ? tq::search_wide_table_bytes(plan, nq) : tq::search_tc_table_bytes(plan, nq));
   l.scores = o;
   if (!tc) o += up(sizeof(float) * size_t(nq) * size_t(n));
   l.cand_idx = o; o += up(sizeof(int32_t) * size_t(nq) * l.nchunks * k);
@@ -208,9 +210,11 @@ extern "C" tq_status tq_search_topk(const tq_plan* plan, const void* q, tq_dtype
   float* cand_sc = reinterpret_cast<float*>(ws + l.cand_sc);
   tq_status s = tq::launch_query_prep(plan, q, q_dtype, nq, qt, st, cs);
   if (s != TQ_OK) return s;
-  if (tq::search_tc_supported(plan, recs)) {
-    if ((s = tq::launch_search_tc(plan, recs, n, nq, qt, st, ws + l.table, k, cand_idx, cand_sc, cs)) != TQ_OK)
-      return s;
+  const bool wide = tq::search_wide_supported(plan, k);
+  if (wide || tq::search_tc_supported(plan, recs)) {
+    s = wide ? tq::launch_search_wide(plan, recs, n, nq, qt, st, ws + l.table, k, cand_idx, cand_sc, cs)
+             : tq::launch_search_tc(plan, recs, n, nq, qt, st, ws + l.table, k, cand_idx, cand_sc, cs);
+    if (s != TQ_OK) return s;
     merge_kernel<<<nq, kSel, 0, cs>>>(cand_idx, cand_sc, l.nchunks, k, idx_out, score_out);
     return tq::launch_status();
   } else {
