@@ -134,10 +134,10 @@ tq_status quantize_mma(const tq_plan* plan, const void* x, tq_dtype dtype, int64
 // 1024, m = d or 0, k <= 16, records in TQ_LAYOUT_ROWS (the entry point's
 // requirement for every path).  `table`:
 // search_wide_table_bytes(plan, nq) bytes, 256-byte aligned.  Writes, per query,
-// search_wide_groups(nq) lists of the k best (score desc, index asc; index -1
-// for an empty entry) to cand_idx / cand_sc [nq][groups][k].
+// search_wide_lists(nq) lists of the k best (score desc, index asc; index -1
+// for an empty entry) to cand_idx / cand_sc [nq][lists][k].
 bool search_wide_supported(const tq_plan* plan, int k);
-int search_wide_groups(int nq);
+int search_wide_lists(int nq);
 size_t search_wide_table_bytes(const tq_plan* plan, int nq);
 tq_status launch_search_wide(const tq_plan* plan, const tq_records* recs, int64_t n, int nq, const float* qt,
                              const float* st, void* table, int k, int32_t* cand_idx, float* cand_sc,

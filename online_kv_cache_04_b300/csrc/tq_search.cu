@@ -40,7 +40,7 @@ SearchLayout layout(const tq_plan* plan, int nq, int64_t n, int k) {
   const bool tc = wide || (d % 128 == 0 && m % 128 == 0);
   SearchLayout l{};
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  l.nchunks = wide ? tq::search_wide_groups(nq) : tc ? tq::search_tc_vchunks(n, nq) : tq::cdiv(n, kChunk);
+  l.nchunks = wide ? tq::search_wide_lists(nq) : tc ? tq::search_tc_vchunks(n, nq) : tq::cdiv(n, kChunk);
   size_t o = 0;
   l.qt = o; o += up(sizeof(float) * size_t(nq) * d);
   l.st = o; o += up(sizeof(float) * size_t(nq) * m);

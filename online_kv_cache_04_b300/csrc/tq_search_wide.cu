@@ -18,13 +18,14 @@
 //   S  = A_hi·σ + A_lo·σ over the m sign coordinates, fp32 in TMEM
 //   score = 2^E_q (‖x_i‖ C + α ‖r_i‖ S).
 // A CTA keeps one block of 128 queries and walks every G-th unit of stored
-// vectors; each epilogue thread owns one query and keeps its 16 best
-// (score desc, index asc) in registers.  At the end the lists go to the
+// vectors; each epilogue thread owns one query and one half of the unit's
+// columns and keeps its 16 best (score desc, index asc) in registers.  At the end the lists go to the
 // workspace as candidates, which the merge kernel of tq_search.cu reduces to
 // the k best: the nq x n score matrix is never formed.
 //
-// Warp roles (704 threads): warps 0-3 epilogue (TMEM lane quadrants), 4-19
-// B producers, warp 20 TMA for A, warp 21 MMA issue and TMEM owner.
+// Warp roles (832 threads): warps 0-7 epilogue (warp % 4 = TMEM lane quadrant,
+// warp / 4 = column half), 8-23 B producers, warp 24 TMA for A, warp 25 MMA
+// issue and TMEM owner.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -50,8 +51,9 @@ constexpr int kOffA = 0, kOffB = kNA * kSlotA, kOffAux = kOffB + kNB * kSlotB;
 constexpr int kOffBar = kOffAux;               // Bars (256 B)
 constexpr int kOffPair = kOffBar + 256;        // [64] uint2: c of a coordinate pair, f16 hi pair and lo pair
 constexpr int kSmemBytes = kOffPair + 64 * 8 + 1024;  // + alignment slack
-constexpr int kProdWarp0 = 4, kProdWarps = 16;  // B producers: warps 4 .. 19
-constexpr int kTmaWarp = 20, kMmaWarp = 21, kThreads = 32 * 22;
+constexpr int kEpiWarps = 8;                   // epilogue: two per TMEM lane quadrant
+constexpr int kProdWarp0 = 8, kProdWarps = 16;  // B producers: warps 8 .. 23
+constexpr int kTmaWarp = 24, kMmaWarp = 25, kThreads = 32 * 26;
 constexpr int kList = 16;                      // list entries per query (k <= kList)
 constexpr uint32_t kTmemCols = 512;            // C: columns 0..255, S: 256..511
 constexpr unsigned kFaultSearch = 4u;          // fault bit: a pipeline wait ran out of its bound
@@ -73,10 +75,10 @@ struct SearchWideArgs {
   float alpha;
   const float* centroids;  // [2^w]
   const float* qscale;     // [nq padded]: 2^E_q
-  int qtiles, groups;      // query blocks; CTAs per query block (= candidate lists per query)
+  int qtiles, groups;      // query blocks; CTAs per query block (two candidate lists per query each)
   int64_t units;           // blocks of kN stored vectors
   int k;
-  int32_t* cand_idx;       // [nq][groups][k]
+  int32_t* cand_idx;       // [nq][2 groups][k]
   float* cand_sc;
   unsigned* fault;
 };
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->b_empty[i]), 1);
     }
     mbar_init(smem_u32(&bars->acc_full), 1);
-    mbar_init(smem_u32(&bars->acc_empty), 4);  // the four epilogue warps
+    mbar_init(smem_u32(&bars->acc_empty), kEpiWarps);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_mbar_init();
   }
@@ -343,11 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&bars->b_full[sb]));
       ++bs;
     }
-  } else if (warp < 4) {
-    // Epilogue: thread = query 32·warp + lane of the block (its TMEM lane).
-    const int qi = 32 * warp + lane;
+  } else if (warp < kEpiWarps) {
+    // Epilogue: thread = query 32·(warp % 4) + lane of the block (its TMEM
+    // lane), columns 128·(warp / 4) .. + 127 of each unit.
+    const int qd = warp & 3, hh = warp >> 2;
+    const int qi = 32 * qd + lane;
     const int64_t qg = (int64_t)qt * kQ + qi;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
     float ls[kList];
     int32_t li[kList];
 #pragma unroll
@@ -357,27 +361,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint32_t uses = 0;
     for (int64_t u = g; u < a.units; u += a.groups, ++uses) {
+      // the norms of 32 columns at a time, lane l holding column 32J + l
+      // (broadcast below by shuffles), loaded one block ahead
+      const int64_t v0 = u * kN + 128 * hh;
+      auto norms = [&](int J, float& nn, float& an) {
+        const int64_t v = v0 + lane + 32 * J;
+        nn = v < a.n ? __ldg(a.norm + v) : 0.f;
+        an = Q && v < a.n ? a.alpha * __ldg(a.rnorm + v) : 0.f;
+      };
+      float nNext, aNext;
+      norms(0, nNext, aNext);
+      const int nv = a.n - v0 < 128 ? (int)(a.n - v0) : 128;  // stored vectors of this half (may be <= 0)
       if (!mbar_wait(smem_u32(&bars->acc_full), uses & 1u, a.fault, kFaultSearch)) break;
       tc_fence_after();
-      const int64_t v0 = u * kN;
-      const int nv = a.n - v0 < kN ? (int)(a.n - v0) : kN;  // stored vectors of this unit
 #pragma unroll 1
-      for (int jb = 0; jb < kN / 8; ++jb) {
-        uint32_t cv[8], sv[8];
-        tmem_ld8(tmem + lane_base + 8 * jb, cv);
-        if (Q) tmem_ld8(tmem + lane_base + kN + 8 * jb, sv);
-        tmem_ld_wait();
+      for (int J = 0; J < 4; ++J) {
+        const float nJ = nNext, aJ = aNext;
+        if (J < 3) norms(J + 1, nNext, aNext);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int col = 8 * jb + j;
-          if (col < nv) {
-            const int64_t v = v0 + col;
-            float sc = __ldg(a.norm + v) * __uint_as_float(cv[j]);
-            if (Q) sc = fmaf(a.alpha * __ldg(a.rnorm + v), __uint_as_float(sv[j]), sc);
-            if (sc > ls[kList - 1]) {
+        for (int jb = 0; jb < 8; ++jb) {
+          const int c0 = 32 * J + 4 * jb;  // first column of these four, within the half
+          uint32_t cv[4], sv[4];
+          tmem_ld4(tmem + lane_base + 128 * hh + c0, cv);
+          if (Q) tmem_ld4(tmem + lane_base + kN + 128 * hh + c0, sv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float nrm = __shfl_sync(0xffffffffu, nJ, 4 * jb + j);
+            float sc = nrm * __uint_as_float(cv[j]);
+            if (Q) sc = fmaf(__shfl_sync(0xffffffffu, aJ, 4 * jb + j), __uint_as_float(sv[j]), sc);
+            if (c0 + j < nv && sc > ls[kList - 1]) {
               // insertion: an equal score stays behind the earlier (lower) index
               float cs = sc;
-              int32_t ci = (int32_t)v;
+              int32_t ci = (int32_t)(v0 + c0 + j);
 #pragma unroll
               for (int e = 0; e < kList; ++e) {
                 const bool sw = cs > ls[e];
@@ -398,13 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (qg < a.nq) {
       const float qs = a.qscale[qg];
-      int32_t* oi = a.cand_idx + ((size_t)qg * a.groups + g) * a.k;
-      float* os = a.cand_sc + ((size_t)qg * a.groups + g) * a.k;
+      const size_t o = ((size_t)qg * 2 * a.groups + 2 * g + hh) * a.k;
 #pragma unroll
       for (int j = 0; j < kList; ++j) {
         if (j < a.k) {
-          oi[j] = li[j];
-          os[j] = li[j] >= 0 ? ls[j] * qs : -INFINITY;
+          a.cand_idx[o + j] = li[j];
+          a.cand_sc[o + j] = li[j] >= 0 ? ls[j] * qs : -INFINITY;
         }
       }
     }
@@ -427,6 +442,7 @@ tq_status launch_wide(const CUtensorMap& mq, const SearchWideArgs& a, cudaStream
 }
 
 int qtiles_of(int nq) { return (nq + kQ - 1) / kQ; }
+int groups_of(int nq) { return std::max(1, tq::sm_count() / qtiles_of(nq)); }
 
 }  // namespace
 
@@ -435,7 +451,7 @@ bool tq::search_wide_supported(const tq_plan* plan, int k) {
          plan->w <= 3 && k <= kList && tq::tensor_map_encoder() != nullptr;
 }
 
-int tq::search_wide_groups(int nq) { return std::max(1, tq::sm_count() / qtiles_of(nq)); }
+int tq::search_wide_lists(int nq) { return 2 * groups_of(nq); }
 
 size_t tq::search_wide_table_bytes(const tq_plan* plan, int nq) {
   const size_t rows = (size_t)qtiles_of(nq) * kQ;
@@ -468,7 +484,7 @@ tq_status tq::launch_search_wide(const tq_plan* plan, const tq_records* recs, in
   a.centroids = plan->centroids;
   a.qscale = qscale;
   a.qtiles = qtiles;
-  a.groups = tq::search_wide_groups(nq);
+  a.groups = groups_of(nq);
   a.units = (n + kN - 1) / kN;
   a.k = k;
   a.cand_idx = cand_idx;
