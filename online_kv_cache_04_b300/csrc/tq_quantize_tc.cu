@@ -4,12 +4,15 @@
 // Per tile of 128 vectors (one CTA per SM, persistent over tiles):
 //   TMA        x tile (bf16, 128-byte swizzle) -> shared memory, 2 stages
 //   GEMM1      U = x Πᵀ as x·Π_hiᵀ + x·Π_loᵀ (Π split into two bf16 terms;
-//              bf16 x is exact): one N = 256 product per K-step against the
-//              stacked [Π_hi; Π_lo], the two fp32 halves summed by epilogue 1
-//   epilogue 1 n = ||x|| from the staged tile, u = U / n, bucketize against
+//              bf16 x is exact): two N = 128 products per K-step into one
+//              fp32 accumulator of 128 columns
+//   norms      n = ||x|| of the tile's vectors from the staged tile, by one
+//              warp of its own (the epilogue warps never read x)
+//   epilogue 1 u = U / n, bucketize against
 //              the Lloyd-Max bounds (binary search) -> index bit-planes,
 //              ρ = u - c[idx], ||ρ||², ρ split into bf16 hi + lo written back
-//              to TMEM; coordinate pairs in packed fp32x2 arithmetic
+//              to TMEM over the columns of U just read; coordinate pairs in
+//              packed fp32x2 arithmetic
 //   GEMM2      P = ρ (S Πᵀ)ᵀ as ρ_hi·S_hi + ρ_hi·S_lo + ρ_lo·S_hi, with ρ
 //              read from TMEM as the A operand
 //   epilogue 2 σ = [P >= 0] packed into words, ||r|| = n ||ρ||, stores
@@ -22,12 +25,20 @@
 // dependent launch: the prologue overlaps the previous kernel, and the input
 // loads and record stores wait for it.
 //
-// Two TMEM slots and two epilogue warpgroups let the tensor core work on one
-// tile while the epilogue of the other runs.  Warp roles (576 threads):
+// TMEM holds four regions of 128 columns.  Tile i keeps U (then ρ) in region
+// i mod 4 and writes P into region (i - 1) mod 4, the one that held tile
+// i - 1's residual: GEMM1 of tile i waits only for the sign epilogue of tile
+// i - 3, so the tensor core has the products of three tiles to choose from
+// while the epilogues of the others run (with two slots of U | P, GEMM1 of
+// tile i waited for the sign epilogue of tile i - 2).  Two epilogue
+// warpgroups take alternate tiles.  Warp roles (640 threads):
 // warps 0-7 epilogue of even tiles, 8-15 of odd tiles (warp % 4 = TMEM lane
 // quadrant; the two warps of a quadrant split the 128 coordinates of its 32
-// vectors and meet through shared memory for ||r||), warp 16 issues MMAs and
-// owns TMEM, warp 17 issues TMA loads.
+// vectors and meet through shared memory for ||r||), warp 16 issues GEMM1
+// and owns TMEM, warp 17 issues TMA loads, warp 18 issues GEMM2, warp 19
+// forms the norms.  A
+// tcgen05.mma costs its issuing thread far more cycles than the tensor core
+// needs for an N = 128 product, so the two GEMMs have an issuer each.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -44,24 +55,28 @@ using namespace tq::sm100;
 constexpr int kTile = 128;                       // vectors per tile (MMA M)
 constexpr int kBoxBytes = 64 * 128 * 2;          // TMA box: 64 bf16 columns x 128 rows
 constexpr int kMatBytes = 2 * kBoxBytes;         // one 128 x 128 bf16 operand
-// Π_hi and Π_lo stacked per 64-column box ([box][hi, lo] x 128 rows): one N = 256
-// operand, so GEMM1 is one product per K-step
+// Π_hi and Π_lo per 64-column box ([box][hi, lo] x 128 rows)
 constexpr int kOffPi = 0, kOffSHi = 2 * kMatBytes, kOffSLo = 3 * kMatBytes;
 constexpr int kOffX = 4 * kMatBytes;             // two x stages
 constexpr int kOffBar = kOffX + 2 * kMatBytes;
 constexpr int kOffRsq = kOffBar + 256;           // [slot 2][tile parity 2][128] partial ||ρ||² of the upper half
-constexpr int kOffNsq = kOffRsq + 2 * 2 * 128 * 4;  // [slot 2][tile parity 2][half 2][128] partial ||x||²
-constexpr int kSmemBytes = kOffNsq + 2 * 2 * 2 * 128 * 4 + 1024; // + alignment slack
-constexpr int kThreads = 576, kMmaWarp = 16, kTmaWarp = 17;
-constexpr uint32_t kTmemCols = 512;              // slot s: [256s, +256) = U_hi | U_lo, then P | ρ K-steps [hi 8 | lo 8]
+constexpr int kOffNrm = kOffRsq + 2 * 2 * 128 * 4;  // [tile parity 2][128] ||x|| of the tile's vectors
+constexpr int kSmemBytes = kOffNrm + 2 * 128 * 4 + 1024;  // + alignment slack
+constexpr int kThreads = 640, kMmaWarp = 16, kTmaWarp = 17, kMma2Warp = 18, kNormWarp = 19;
+constexpr uint32_t kTmemCols = 512;              // four regions of 128 columns: U, then ρ K-steps [hi 8 | lo 8]; or P
 
 constexpr unsigned kFaultWait = 1u;              // fault bit: a pipeline wait ran out of its bound
 
 struct Bars {
   uint64_t b_full;
-  uint64_t x_full[2], x_empty[2], u_full[2], rho_full[2], p_full[2], acc_empty[2];
-  uint64_t rsq_full[2];  // the upper coordinate half's ||ρ||² partials are in
-  uint64_t nsq_full[2];  // both halves' ||x||² partials of the slot's tile are in
+  uint64_t x_full[2], x_empty[2], rho_full[2], p_full[2];
+  // indexed by tile mod 4: a barrier completes at most once per four tiles,
+  // so no waiter can see it complete twice (the epilogue warpgroups and the
+  // issuers run up to three tiles apart)
+  uint64_t u_full[4], acc_empty[4];
+  uint64_t norm_full[2], norm_empty[2];  // the norms of the tile's vectors are in / have been read
+  uint64_t rsq_full[2];   // the upper coordinate half's ||ρ||² partials are in
+  uint64_t rsq_empty[2];  // the lower half has read them (the halves run apart otherwise)
   uint32_t tmem_base;
 };
 
@@ -153,13 +168,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bars->b_full), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->x_full[s]), 1);
-      mbar_init(smem_u32(&bars->x_empty[s]), 1 + 8);
-      mbar_init(smem_u32(&bars->u_full[s]), 1);
+      mbar_init(smem_u32(&bars->x_empty[s]), 2);  // GEMM1 done, norms read
+      mbar_init(smem_u32(&bars->norm_full[s]), 1);
+      mbar_init(smem_u32(&bars->norm_empty[s]), 8);
       mbar_init(smem_u32(&bars->rho_full[s]), 8);
       mbar_init(smem_u32(&bars->p_full[s]), 1);
-      mbar_init(smem_u32(&bars->acc_empty[s]), 8);
       mbar_init(smem_u32(&bars->rsq_full[s]), 4);
-      mbar_init(smem_u32(&bars->nsq_full[s]), 8);
+      mbar_init(smem_u32(&bars->rsq_empty[s]), 4);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(smem_u32(&bars->u_full[i]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[i]), 8);
     }
     fence_mbar_init();
   }
@@ -210,52 +229,113 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last_k[s] >= 0) mbar_wait(smem_u32(&bars->x_full[s]), last_k[s] & 1, a.fault, kFaultWait);
     }
   } else if (warp == kMmaWarp) {
+    // GEMM1 of every tile (U into region it mod 4; it mod 2 without QJL)
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 128), idesc256 = idesc_bf16_f32(128, 256);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
       bool ok = mbar_wait(smem_u32(&bars->b_full), 0, a.fault, kFaultWait);
       tc_fence_after();
-      auto gemm2 = [&](int j) {
-        const int s = j & 1, k = j >> 1;
-        if (!mbar_wait(smem_u32(&bars->rho_full[s]), k & 1, a.fault, kFaultWait)) return false;
-        tc_fence_after();
-        const uint32_t acc = tmem + 256 * s;
-        // terms (ρ_hi, S_hi), (ρ_hi, S_lo), (ρ_lo, S_hi)
-#pragma unroll 1
-        for (int t = 0; t < 3; ++t) {
-          const uint64_t sd = desc_sw128(base + (t == 1 ? kOffSLo : kOffSHi));
-#pragma unroll 1
-          for (int kk = 0; kk < 8; ++kk) {
-            // K-step kk: ρ pieces of coordinates 16kk.. sit in [hi 8 | lo 8] at 128 + 16kk
-            const uint32_t rho = acc + 128 + 16 * kk + (t == 2 ? 8 : 0);
-            const uint32_t boff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;  // start address advances in 16 B units
-            mma_ts(acc, rho, sd + (boff >> 4), idesc, (t | kk) != 0);
-          }
-        }
-        mma_commit(smem_u32(&bars->p_full[s]));
-        return true;
-      };
+      const uint64_t pd = desc_sw128(base + kOffPi);
       int it = 0;
       for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
         const int s = it & 1, k = it >> 1;
-        if (!mbar_wait(smem_u32(&bars->x_full[s]), k & 1, a.fault, kFaultWait)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&bars->acc_empty[s]), (k & 1) ^ 1, a.fault, kFaultWait)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars->x_full[s]), k & 1, a.fault, kFaultWait)) break;
+        // the region this tile's U goes into: with QJL, tile it - 3 held its P
+        // there (released by that tile's sign epilogue, after GEMM2 of tiles up
+        // to it - 3 completed); without, tile it - 2 held its U in region it mod 2
+        // (released once epilogue 1 read it)
+        if (Q ? (it >= 3 && !mbar_wait(smem_u32(&bars->acc_empty[(it - 3) & 3]), ((it - 3) >> 2) & 1, a.fault,
+                                       kFaultWait))
+              : (it >= 2 && !mbar_wait(smem_u32(&bars->acc_empty[(it - 2) & 3]), ((it - 2) >> 2) & 1, a.fault,
+                                       kFaultWait)))
+          break;
         tc_fence_after();
-        const uint32_t acc = tmem + 256 * s;
-        const uint32_t xa = base + kOffX + s * kMatBytes;
-        const uint64_t xd = desc_sw128(xa);
-        // U_hi | U_lo = x·[Π_hi; Π_lo]ᵀ in 256 accumulator columns (summed by the epilogue)
-        const uint64_t pd = desc_sw128(base + kOffPi);
+        const uint32_t acc = tmem + 128 * (Q ? (it & 3) : s);
+        const uint64_t xd = desc_sw128(base + kOffX + s * kMatBytes);
+        // U = x·Π_hiᵀ + x·Π_loᵀ: both products of a K-step into the same 128 columns
 #pragma unroll 1
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t offa = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
           const uint32_t offb = ((kk >> 2) * 2 * kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(acc, xd + offa, pd + offb, idesc256, kk != 0);
+          mma_ss(acc, xd + offa, pd + offb, idesc, kk != 0);
+          mma_ss(acc, xd + offa, pd + offb + (kBoxBytes >> 4), idesc, 1u);
         }
-        mma_commit(smem_u32(&bars->u_full[s]));
+        mma_commit(smem_u32(&bars->u_full[it & 3]));
         mma_commit(smem_u32(&bars->x_empty[s]));
-        if (Q && it >= 1 && !gemm2(it - 1)) { ok = false; break; }
       }
-      if (Q && ok && it >= 1) gemm2(it - 1);
+    }
+  } else if (warp == kMma2Warp) {
+    // GEMM2 of every tile j, issued by a thread of its own so that its products
+    // queue beside GEMM1's: A = ρ from region j mod 4, P into region (j - 1) mod 4
+    if (Q && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      bool ok = mbar_wait(smem_u32(&bars->b_full), 0, a.fault, kFaultWait);
+      const uint64_t shd = desc_sw128(base + kOffSHi), sld = desc_sw128(base + kOffSLo);
+      int j = 0;
+      for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++j) {
+        const int s = j & 1, k = j >> 1;
+        if (!mbar_wait(smem_u32(&bars->rho_full[s]), k & 1, a.fault, kFaultWait)) break;
+        // region (j - 1) mod 4 held tile j - 1's residual: its GEMM2 must have read it
+        if (j >= 1 && !mbar_wait(smem_u32(&bars->p_full[s ^ 1]), ((j - 1) >> 1) & 1, a.fault, kFaultWait)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + 128 * ((j + 3) & 3), rreg = tmem + 128 * (j & 3);
+        // terms (ρ_hi, S_hi), (ρ_hi, S_lo), (ρ_lo, S_hi); K-step kk: ρ pieces of
+        // coordinates 16kk.. sit in [hi 8 | lo 8] at 16kk, and the B start
+        // address advances in 16-byte units
+#pragma unroll 1
+        for (int t = 0; t < 3; ++t) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t boff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ts(acc, rreg + 16 * kk + (t == 2 ? 8 : 0), (t == 1 ? sld : shd) + boff, idesc, (t | kk) != 0);
+          }
+        }
+        mma_commit(smem_u32(&bars->p_full[s]));
+      }
+    }
+  } else if (warp == kNormWarp) {
+    // ||x|| of every vector of the tile from the staged tile (row r, 128-byte
+    // swizzle): each 64-coordinate box in two packed pairs of partial sums,
+    // lower box + upper box; lane l takes rows l, l + 32, l + 64, l + 96
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      const int s = it & 1, k = it >> 1;
+      if (!mbar_wait(smem_u32(&bars->x_full[s]), k & 1, a.fault, kFaultWait)) break;
+      // the slot's previous norms (tile it - 2) have been read by its epilogue
+      if (!mbar_wait(smem_u32(&bars->norm_empty[s]), (k & 1) ^ 1, a.fault, kFaultWait)) break;
+      float* nrm = reinterpret_cast<float*>(smem + kOffNrm) + s * 128;
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        float part0 = 0.f, part1 = 0.f;
+#pragma unroll 1
+        for (int hb = 0; hb < 2; ++hb) {
+          uint64_t ssa = 0ull, ssb = 0ull;
+          const uint8_t* row = smem + kOffX + s * kMatBytes + hb * kBoxBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint64_t x2 = f2_pack(__uint_as_float(wv[e] << 16), __uint_as_float(wv[e] & 0xFFFF0000u));
+              if (e & 1) ssb = f2_fma(x2, x2, ssb);
+              else ssa = f2_fma(x2, x2, ssa);
+            }
+          }
+          const float2 pa = f2_unpack(ssa), pb = f2_unpack(ssb);
+          const float ps = (pa.x + pa.y) + (pb.x + pb.y);
+          if (hb == 0) part0 = ps;
+          else part1 = ps;
+        }
+        nrm[r] = sqrtf(part0 + part1);
+      }
+      // the next TMA write into this stage (async proxy) follows these generic reads
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&bars->x_empty[s]));
+        mbar_arrive(smem_u32(&bars->norm_full[s]));
+      }
     }
   } else {
     // the previous launch in the stream may still read the records written here
@@ -273,45 +353,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = warp >> 3, h = (warp >> 2) & 1, q = warp & 3, r = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int s = g;
-    const uint32_t acc = tmem + lane_base + 256 * s;
     float* rsq_s = reinterpret_cast<float*>(smem + kOffRsq) + (s * 2) * 128;
-    float* nsq_s = reinterpret_cast<float*>(smem + kOffNsq) + (s * 2) * 2 * 128;
     int it = g;
     for (int64_t tile = blockIdx.x + (int64_t)g * gridDim.x; tile < ntiles; tile += 2 * (int64_t)gridDim.x, it += 2) {
       const int ph = (it >> 1) & 1;
-      if (!mbar_wait(smem_u32(&bars->x_full[s]), ph, a.fault, kFaultWait)) break;
-      // ||x||²: this half's 64 coordinates from the staged tile (row r, box h,
-      // 128-byte swizzle) in two packed pairs of partial sums; the halves meet
-      // in shared memory and both form n from the same two partials
-      uint64_t ssa = 0ull, ssb = 0ull;
-      {
-        const uint8_t* row = smem + kOffX + s * kMatBytes + h * kBoxBytes + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint64_t x2 = f2_pack(__uint_as_float(wv[e] << 16), __uint_as_float(wv[e] & 0xFFFF0000u));
-            if (e & 1) ssb = f2_fma(x2, x2, ssb);
-            else ssa = f2_fma(x2, x2, ssa);
-          }
-        }
-      }
-      // the next TMA write into this stage (async proxy) follows these generic reads
-      fence_proxy_async_smem();
+      // n = ||x|| from the norm warp
+      if (!mbar_wait(smem_u32(&bars->norm_full[s]), ph, a.fault, kFaultWait)) break;
+      const float n = reinterpret_cast<const float*>(smem + kOffNrm)[s * 128 + r];
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->x_empty[s]));
-      float* nsq = nsq_s + ph * 2 * 128;
-      {
-        const float2 pa = f2_unpack(ssa), pb = f2_unpack(ssb);
-        nsq[h * 128 + r] = (pa.x + pa.y) + (pb.x + pb.y);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->nsq_full[s]));
-      if (!mbar_wait(smem_u32(&bars->nsq_full[s]), ph, a.fault, kFaultWait)) break;
-      const float n = sqrtf(nsq[r] + nsq[128 + r]);
-      if (!mbar_wait(smem_u32(&bars->u_full[s]), ph, a.fault, kFaultWait)) break;
+      if (lane == 0) mbar_arrive(smem_u32(&bars->norm_empty[s]));
+      // U (then ρ) in region it mod 4 (it mod 2 without QJL), P in region (it - 1) mod 4
+      const uint32_t uacc = tmem + lane_base + 128 * (Q ? (it & 3) : s);
+      const uint32_t pacc = tmem + lane_base + 128 * ((it + 3) & 3);
+      if (!mbar_wait(smem_u32(&bars->u_full[it & 3]), (it >> 2) & 1, a.fault, kFaultWait)) break;
       tc_fence_after();
       const float inv = n > 0.f ? 1.0f / n : 0.f, nlive = n > 0.f ? -1.f : 0.f;
       const uint64_t inv2 = f2_pack(inv, inv), nlive2 = f2_pack(nlive, nlive);
@@ -323,19 +377,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         const int c = 4 * h + cc;
-        uint32_t v[16], vl[16];
-        tmem_ld16(acc + 16 * c, v);
-        tmem_ld16(acc + 128 + 16 * c, vl);
+        uint32_t v[16];
+        tmem_ld16(uacc + 16 * c, v);
         tmem_ld_wait();
         uint32_t pw[W], hi[8], lo[8];
 #pragma unroll
         for (int p = 0; p < W; ++p) pw[p] = 0u;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          // u = (U_hi + U_lo) / n for coordinates 2j, 2j + 1 of the chunk
-          const uint64_t u2 = f2_mul(f2_add(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
-                                            f2_pack(__uint_as_float(vl[2 * j]), __uint_as_float(vl[2 * j + 1]))),
-                                     inv2);
+          // u = U / n for coordinates 2j, 2j + 1 of the chunk
+          const uint64_t u2 = f2_mul(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), inv2);
           const float2 uu = f2_unpack(u2);
           float cv[2];
 #pragma unroll
@@ -379,9 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[j] = *reinterpret_cast<const uint32_t*>(&l);
           }
         }
-        if (Q) {  // into the columns of U_lo just read: K-step c = [hi 8 | lo 8]
-          tmem_st8(acc + 128 + 16 * c, hi);
-          tmem_st8(acc + 128 + 16 * c + 8, lo);
+        if (Q) {  // over the columns of U just read: K-step c = [hi 8 | lo 8]
+          tmem_st8(uacc + 16 * c, hi);
+          tmem_st8(uacc + 16 * c + 8, lo);
         }
         // chunk c holds bits 16·(c & 1).. of plane word c / 2 (word (c >> 1) - 2h here)
 #pragma unroll
@@ -397,8 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       // with QJL, GEMM2 reads the residual next; without, the slot is free
-      if (lane == 0) mbar_arrive(smem_u32(Q ? &bars->rho_full[s] : &bars->acc_empty[s]));
+      if (lane == 0) mbar_arrive(smem_u32(Q ? &bars->rho_full[s] : &bars->acc_empty[it & 3]));
       if (Q && h == 1) {  // the lower half writes ||r|| = n·sqrt(lower + upper partial)
+        // once it has read this slot's partials of the group's previous tile
+        if (!mbar_wait(smem_u32(&bars->rsq_empty[s]), ph ^ 1, a.fault, kFaultWait)) break;
         rsq_s[(it >> 1 & 1) * 128 + r] = rsq;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->rsq_full[s]));
@@ -433,19 +486,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sg[2];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(acc + 32 * (2 * h + cc), v);
-        tmem_ld_wait();
         // bit j = [P_j >= 0]: the sign bits shifted in from the top coordinate
-        // down, then inverted; a zero vector (P = 0 of either sign) takes all ones
+        // down (upper 16 columns first), then inverted; a zero vector (P = 0 of
+        // either sign) takes all ones
         uint32_t neg = 0u;
 #pragma unroll
-        for (int j = 31; j >= 0; --j) neg = __funnelshift_l(v[j], neg, 1);
+        for (int hc = 1; hc >= 0; --hc) {
+          uint32_t v[16];
+          tmem_ld16(pacc + 32 * (2 * h + cc) + 16 * hc, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 15; j >= 0; --j) neg = __funnelshift_l(v[j], neg, 1);
+        }
         sg[cc] = n > 0.f ? ~neg : 0xFFFFFFFFu;
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[s]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[it & 3]));
       uint32_t* const osgn = second ? a.out1.sgn : a.out0.sgn;
       if (rows_layout) {
         if (row < on) *reinterpret_cast<uint2*>(osgn + row * 4 + 2 * h) = make_uint2(sg[0], sg[1]);
@@ -458,6 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           (second ? a.out1.norm : a.out0.norm)[row] = n;
           (second ? a.out1.rnorm : a.out0.rnorm)[row] = n * sqrtf(rsq + rsq_s[(it >> 1 & 1) * 128 + r]);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->rsq_empty[s]));
       }
     }
   }
@@ -493,6 +552,8 @@ tq_status launch_w(const CUtensorMap& mx0, const CUtensorMap& mx1, const CUtenso
   auto kern = quantize_tc_kernel<W, Q>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return TQ_ERR_CUDA;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.maxThreadsPerBlock < kThreads) return TQ_ERR_CUDA;
   const int grid = (int)std::min<int64_t>(a.ntiles, tq::sm_count());
   // programmatic dependent launch: the prologue (barriers, TMEM, the plan
   // operands) overlaps the previous kernel; inputs and outputs wait for it
