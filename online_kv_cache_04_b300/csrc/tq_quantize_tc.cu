@@ -105,16 +105,21 @@ struct TcArgs {
 
 __device__ unsigned g_fault_word;
 
-// 32 x 32 bit transpose across a warp: lane r holds row r on entry (bit c =
-// element (r, c)); on exit lane c holds column c (bit r = element (r, c)).
-__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+// 32 x 32 bit transpose across a warp into the block layout's bit order.  On
+// entry lane r holds row r (bit c = element (r, c)).  The butterfly runs with
+// every lane index rotated left by one bit (lane L plays position
+// t/2 + 16·(t%2) of row t = L), so on exit lane L holds column
+// L/2 + 16·(L%2) with row t at bit t/2 + 16·(t%2): the block layout's word,
+// with no separate bit permutation.
+__device__ __forceinline__ uint32_t warp_transpose32_block(uint32_t x, int lane) {
   const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
 #pragma unroll
   for (int k = 0; k < 5; ++k) {
-    const int sh = 16 >> k;
+    const int sh = 16 >> k;                             // bit distance within the word
+    const int ls = ((sh << 1) & 31) | (sh >> 4);        // lane distance: sh rotated left by one
     const uint32_t m = masks[k];
-    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, sh);
-    x = (lane & sh) ? ((x & ~m) | ((y >> sh) & m)) : ((x & m) | ((y & m) << sh));
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, ls);
+    x = (lane & ls) ? ((x & ~m) | ((y >> sh) & m)) : ((x & m) | ((y & m) << sh));
   }
   return x;
 }
@@ -131,16 +136,18 @@ __device__ __forceinline__ uint32_t unshuffle32(uint32_t x) {
 
 // TQ_LAYOUT_BLOCK32 store of one warp's 32 rows (one block): `words[c]` is
 // this lane's row word for coordinates 32c..32c+31 (counted from `blk`);
-// `valid` has bit L set for valid row L.  Lane L writes the block words of
-// coordinates 32c + L, merging with the stored bits of rows that this call
-// does not write.
+// `valid` has bit L set for valid row L.  Lane L writes the block word of
+// coordinate 32c + L/2 + 16·(L%2) (the warp's 32 stores still cover 128
+// contiguous bytes), merging with the stored bits of rows that this call does
+// not write.
 template <int NW>
 __device__ __forceinline__ void store_block32(uint32_t* blk, const uint32_t (&words)[NW], uint32_t valid, int lane) {
   const uint32_t vm = unshuffle32(valid);
+  const int colw = (lane >> 1) | ((lane & 1) << 4);
 #pragma unroll
   for (int c = 0; c < NW; ++c) {
-    const uint32_t col = unshuffle32(warp_transpose32(words[c], lane));
-    uint32_t* dst = blk + 32 * c + lane;
+    const uint32_t col = warp_transpose32_block(words[c], lane);
+    uint32_t* dst = blk + 32 * c + colw;
     if (vm == 0xFFFFFFFFu) *dst = col;
     else if (vm != 0u) *dst = (*dst & ~vm) | (col & vm);
   }
