@@ -295,10 +295,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
+    // The next unit's record words are brought into L2 while this one is
+    // expanded, so the loads above meet L2 rather than DRAM latency (one lane
+    // of warp 0 issues the bulk prefetches, 16 KiB at a time, when the arrays
+    // are 16-byte aligned as bulk copies require).
+    const bool pf = pw == 0 && lane == 0 && (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0 &&
+                    (!Q || (reinterpret_cast<uintptr_t>(a.sgn) & 15) == 0);
+    auto prefetch_unit = [&](int64_t uu) {
+      if (!pf || uu >= a.units) return;
+      const int64_t v0 = uu * kN, nv = a.n - v0 < kN ? a.n - v0 : kN;
+      const char* pi = reinterpret_cast<const char*>(a.idx + v0 * wi);
+      const int64_t bi = nv * wi * 4;  // rows of W·d/8 bytes: a multiple of 16
+      for (int64_t o = 0; o < bi; o += 16384) bulk_prefetch_l2(pi + o, (uint32_t)(bi - o < 16384 ? bi - o : 16384));
+      if (Q) {
+        const char* ps = reinterpret_cast<const char*>(a.sgn + v0 * (m / 32));
+        const int64_t bs = nv * (m / 8);
+        for (int64_t o = 0; o < bs; o += 16384) bulk_prefetch_l2(ps + o, (uint32_t)(bs - o < 16384 ? bs - o : 16384));
+      }
+    };
     bool ok = true;
     int64_t u = g;
     int st = 0;
     if (u < a.units) load(u, st);
+    prefetch_unit(u + a.groups);
     while (ok && u < a.units) {
       uint2 cw[2][W];
 #pragma unroll
@@ -309,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++st == nst) {
         st = 0;
         u += a.groups;
+        prefetch_unit(u + a.groups);
       }
       if (u < a.units) load(u, st);
       const int sb = (int)(bs % kNB);
