@@ -48,7 +48,7 @@ int choose_splits(int B, int Hkv, int64_t ctx_stride) {
 int tc_slots(const DecodeShape& s) {
   if (s.d != 128 || (s.m != 128 && s.m != 0) || s.G > kMaxG || s.ctx_stride % 128 != 0) return 0;
   const int64_t units = int64_t(s.B) * s.Hkv, tpu = tq::decode_tc_tpu(s.ctx_stride);
-  return tq::decode_tc_slots(units, tpu, tq::decode_tc_ctas(units, tpu));
+  return tq::decode_tc_slots(units, tpu, tq::decode_tc_ctas(units, tpu, s.G));
 }
 
 // Workspace of the tensor-core path: the per-unit query tables, then the

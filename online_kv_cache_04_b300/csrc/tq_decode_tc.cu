@@ -85,13 +85,17 @@ namespace {
 
 using namespace tq::sm100;
 
-constexpr int kNW = 8;                                 // decode warps (one 32-token block each)
-constexpr int kBlocks = 8;                             // 32-row blocks per tile
+constexpr int kNW = 4;                                 // decode warps (one 32-token block each)
+constexpr int kBlocks = 4;                             // 32-row blocks per tile
 constexpr int kTile = 32 * kBlocks;                    // tokens per tile
-constexpr int kHalfTile = 128;                         // the last tile of a unit may hold this many
+constexpr int kPage = 256;                             // tokens per page of a paged cache: two tiles
 constexpr int kD = 128;
-constexpr int kStages = 4;                             // power of two
+constexpr int kStages = 2;                             // power of two
 constexpr int kThreads = 32 * kNW;                     // decode kernel
+// decode CTAs resident per SM: 12 warps at up to 4 heads per kv head; with 8
+// the value accumulators of both parts stay apart and need the registers of 8 warps
+constexpr int ctas_per_sm(int GP) { return GP == 4 ? 3 : 2; }
+constexpr int kCombThreads = 256;                      // unit merge kernel
 constexpr int kTableThreads = 512;                     // query-table kernel
 constexpr float kTau = 6.0f;                           // lazy-rescale threshold (log2 units)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -255,7 +259,10 @@ template <int W, int GP, bool Q>
 constexpr int smem_bytes() {
   return 1024 + Shape<W, GP, Q>::kOffMisc + kMiscBytes;
 }
-static_assert(smem_bytes<3, 8, true>() <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
+// ctas_per_sm(GP) CTAs, each with the 1 KiB the system reserves per CTA, in an SM's 228 KiB
+static_assert(ctas_per_sm(4) * (smem_bytes<3, 4, true>() + 1024) <= 228 * 1024 &&
+                  ctas_per_sm(8) * (smem_bytes<3, 8, true>() + 1024) <= 228 * 1024,
+              "shared memory plan exceeds a CTA's share of an SM");
 
 // Segment of this CTA's tile range that falls in one unit.
 struct Seg {
@@ -284,7 +291,7 @@ __device__ __forceinline__ Seg segment_at(const TcArgs& a, int64_t f, int64_t f1
 // Scratch of the per-unit query transform and of the unit merge.  Global loads
 // on these one-off paths are issued in as few dependent rounds as the
 // registers allow: a round trip to L2 costs over a microsecond here.
-constexpr int kMaxCtas = 160;                          // grid limit: bounds the slots per unit
+constexpr int kMaxCtas = 448;                          // grid limit: bounds the slots per unit
 template <int GP, int NT>
 struct Scratch {
   static constexpr int NG = NT / 128;                                        // thread groups
@@ -350,12 +357,12 @@ __device__ __forceinline__ void append_step(const TcArgs& a, int u, const float 
   }
   int64_t row = (int64_t)u * a.ctx_stride + L;
   if (a.pages != nullptr) {  // the page holding token L
-    const int64_t pg = __ldg(a.pages + (int64_t)u * a.max_pages + L / kTile);
+    const int64_t pg = __ldg(a.pages + (int64_t)u * a.max_pages + L / kPage);
     if (pg < 0 || pg >= a.npages) {
       if (threadIdx.x == 0) atomicOr(a.fault, kFaultPage);
       return;
     }
-    row = pg * kTile + L % kTile;
+    row = pg * kPage + L % kPage;
   }
   float* xs = scr;                 // [2][128] the new vectors, then ρ
   float* red = xs + 2 * kD;        // [NG][2][128] partial sums
@@ -496,9 +503,9 @@ __device__ __noinline__ void unit_query_prep(const TcArgs& a, int u, int head0, 
 // after the wait the partials come in one round of global loads when ns fits
 // one chunk.
 template <int GP, bool Q, bool HEAD>
-__global__ void __launch_bounds__(kThreads, 1) unit_combine_kernel(const TcArgs a, int ctas) {
+__global__ void __launch_bounds__(kCombThreads, 1) unit_combine_kernel(const TcArgs a, int ctas) {
   static_assert(!HEAD || GP == 1, "one head per CTA");
-  constexpr int NT = kThreads;
+  constexpr int NT = kCombThreads;
   constexpr int NG = NT / 128, RR = 128 * 128 / NT;
   constexpr int kStride = 2 + 2 * kD;
   extern __shared__ uint8_t smem_raw[];
@@ -753,7 +760,7 @@ __global__ void __launch_bounds__(kTableThreads) unit_table_kernel(const TcArgs 
 }
 
 template <int W, int GP, bool Q>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(GP)) decode_tc_kernel(const TcArgs a) {
   using Sh = Shape<W, GP, Q>;
   constexpr int NPM = Sh::NPM, NP = Sh::NP, GH = Sh::GH;
   constexpr int NT = kThreads;
@@ -802,15 +809,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         continue;
       }
       int64_t row0 = cu * a.ctx_stride + ct * kTile;
-      if (a.pages != nullptr) {  // paged cache: the tile is one page
-        int64_t pg = __ldg(a.pages + cu * a.max_pages + ct);
+      if (a.pages != nullptr) {  // paged cache: the tile is one half of a page
+        int64_t pg = __ldg(a.pages + cu * a.max_pages + ct / (kPage / kTile));
         if (pg < 0 || pg >= a.npages) {
           atomicOr(a.fault, kFaultPage);
           pg = 0;
         }
-        row0 = pg * kTile;
+        row0 = pg * kPage + (ct % (kPage / kTile)) * kTile;
       }
-      const int ntok = (int)min((int64_t)kTile, a.ctx_stride - ct * kTile);  // 256, or 128 at a unit's end
+      const int ntok = kTile;
       ++cur;
       ++ct;
       const int s = (int)(issued & (kStages - 1));
@@ -855,7 +862,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
   for (int P = 0; P < NPM; ++P) cf[P] = ms->cf[P];
   // this thread's score rows in the warp's block: pair Qs of score tile s = tokens 2Qs, 2Qs + 1
   const int pr0 = 4 * (gq >> 1) + (gq & 1);  // Q of tile 0; tile 1 adds 2
-  float vacc[2][8][4];   // [part][row tile][fragment]: c[idx] sums (part 0), σ sums (part 1)
+  // [part][row tile][fragment]: c[idx] sums (part 0), σ sums (part 1).  With at
+  // most 4 heads (GP = 4) both parts share one accumulator: value column 2·tig
+  // holds head tig's c[idx] sums and column 2·tig + 1 its σ sums (the B
+  // fragment of a plane is zero in the other part's columns); with GP = 8 the
+  // columns are heads tig and tig + 4, one accumulator per part.
+  constexpr int NPART = GP == 4 ? 1 : 2;
+  float vacc[NPART][8][4];
   float M[GH], lsum[GH], A0[GH], B0[GH], A1[GH], B1[GH];
   uint32_t bv[NP][2][2];  // value B fragments of the previous tile: [plane][K-step][b0, b1]
   int64_t gi = 0;
@@ -868,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
     const int b = (int)(sg.u / a.Hkv), h = (int)(sg.u - (int64_t)b * a.Hkv);
     const int head0 = b * a.Hq + h * a.G;
 #pragma unroll
-    for (int p = 0; p < 2; ++p)
+    for (int p = 0; p < NPART; ++p)
 #pragma unroll
       for (int rt = 0; rt < 8; ++rt)
 #pragma unroll
@@ -1018,7 +1031,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
           // value column 2·tig + c holds head tig (GP = 4, both columns) or head
           // tig + 4c (GP = 8)
 #pragma unroll
-          for (int p = 0; p < 2; ++p)
+          for (int p = 0; p < NPART; ++p)
 #pragma unroll
             for (int rt = 0; rt < 8; ++rt)
 #pragma unroll
@@ -1027,8 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         // this thread's weights, one f16x2 register per (score tile, head tile, plane,
         // piece): the pair of tokens 2Q, 2Q + 1, times -coef_P (index planes) or -1
         // (sign plane) since the value operand is -s
-        constexpr int NPC = GP == 4 ? 2 : 1;  // pieces per weight: hi, lo (GP = 4) or hi
-        uint32_t hv[2][GH][NP][NPC];
+        uint32_t hv[2][GH][NP];  // f16 alone: a value weight's rounding averages out over tokens
 #pragma unroll
         for (int st = 0; st < 2; ++st)
 #pragma unroll
@@ -1042,17 +1054,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
               const float c = P < NPM ? -cf[P] * kWS : -kWS;
               const float x0 = p[0] * (P < NPM ? vnc[st][0] : vrc[st][0]) * c;
               const float x1 = p[1] * (P < NPM ? vnc[st][1] : vrc[st][1]) * c;
-              const uint32_t whi = f16x2_of(x0, x1);
-              hv[st][hh][P][0] = whi;
-              if (NPC == 2) {
-                const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&whi));
-                hv[st][hh][P][NPC - 1] = f16x2_of(x0 - back.x, x1 - back.y);
-              }
+              hv[st][hh][P] = f16x2_of(x0, x1);
             }
           }
         // B fragment of K-step st for lane (gq, tig): b0 = pair 4·tig + 2·st, b1 =
         // pair 4·tig + 2·st + 1, column gq: from the score thread (2·tig + b, gq / 2)
-        // of score tile st, piece (GP = 4) or head tile (GP = 8) gq % 2
+        // of score tile st; with GP = 4 column gq takes plane P's weights when its
+        // part (gq % 2: c[idx] or σ) is P's and zero otherwise, with GP = 8 head
+        // tile gq % 2
 #pragma unroll
         for (int st = 0; st < 2; ++st)
 #pragma unroll
@@ -1060,15 +1069,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             const int src = 4 * (2 * tig + bb) + (gq >> 1);
 #pragma unroll
             for (int P = 0; P < NP; ++P) {
-              uint32_t x0, x1;
               if (GP == 4) {
-                x0 = __shfl_sync(0xffffffffu, hv[st][0][P][0], src);
-                x1 = __shfl_sync(0xffffffffu, hv[st][0][P][NPC - 1], src);
+                const uint32_t x0 = __shfl_sync(0xffffffffu, hv[st][0][P], src);
+                bv[P][st][bb] = (gq & 1) == (P < NPM ? 0 : 1) ? x0 : 0u;
               } else {
-                x0 = __shfl_sync(0xffffffffu, hv[st][0][P][0], src);
-                x1 = __shfl_sync(0xffffffffu, hv[st][GH - 1][P][0], src);
+                const uint32_t x0 = __shfl_sync(0xffffffffu, hv[st][0][P], src);
+                const uint32_t x1 = __shfl_sync(0xffffffffu, hv[st][GH - 1][P], src);
+                bv[P][st][bb] = (gq & 1) ? x1 : x0;
               }
-              bv[P][st][bb] = (gq & 1) ? x1 : x0;
             }
           }
       };
@@ -1095,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
             } else {
               ww = *reinterpret_cast<const uint2*>(vsg + crd);
             }
-            const int part = P < NPM ? 0 : 1;
+            const int part = GP == 4 || P < NPM ? 0 : 1;
             mma_f16(vacc[part][rt], sk(ww.x * vm0), sk(ww.y * vm0), sk(ww.x * vm1), sk(ww.y * vm1), bv[P][0][0],
                     bv[P][0][1]);
             mma_f16(vacc[part][rt], sk(ww.x * vm2), sk(ww.y * vm2), sk(ww.x * vm3), sk(ww.y * vm3), bv[P][1][0],
@@ -1166,16 +1174,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const TcArgs a) 
         for (int rt = 0; rt < 8; ++rt)
 #pragma unroll
           for (int rp = 0; rp < 2; ++rp) {
-            const float x = GP == 4 ? vacc[p][rt][2 * rp] + vacc[p][rt][2 * rp + 1] : vacc[p][rt][2 * rp + hp];
+            const float x = GP == 4 ? vacc[0][rt][2 * rp + p] : vacc[p][rt][2 * rp + hp];
             red[(warp * 32 + p * 16 + rt * 2 + rp) * 32 + lane] = x * fs;
           }
       cta_sync_n<NT>();
       {
-        // thread (value group vg = warp, lane): values 4·vg .. 4·vg + 3 of lane, summed over warps
+        // thread (value group vg = warp, lane): values VPW·vg .. VPW·vg + VPW - 1 of
+        // lane, summed over warps
+        constexpr int VPW = 32 / kNW;
         const int ln = lane, lg = ln >> 2, lt = ln & 3, gh = lt + 4 * hp;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int v = 4 * warp + i, p = v >> 4, rt = (v >> 1) & 7, rp = v & 1;
+        for (int i = 0; i < VPW; ++i) {
+          const int v = VPW * warp + i, p = v >> 4, rt = (v >> 1) & 7, rp = v & 1;
           float s = 0.f;
 #pragma unroll
           for (int w = 0; w < kNW; ++w) s += red[(w * 32 + v) * 32 + ln];
@@ -1210,13 +1220,13 @@ int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas) {
   return (int)smax;  // one partial per CTA
 }
 
-int decode_tc_ctas(int64_t units, int64_t tpu) {
-  return (int)std::min<int64_t>(units * tpu, std::min(sm_count(), kMaxCtas));
+int decode_tc_ctas(int64_t units, int64_t tpu, int G) {
+  return (int)std::min<int64_t>(units * tpu, std::min(ctas_per_sm(G > 4 ? 8 : 4) * sm_count(), kMaxCtas));
 }
 
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride) {
   return plan->d == 128 && (plan->m == 128 || plan->m == 0) && G >= 1 && G <= 8 && V->layout == TQ_LAYOUT_BLOCK32 &&
-         ctx_stride % kHalfTile == 0;
+         ctx_stride % kTile == 0;
 }
 
 size_t decode_tc_table_bytes(int w, int G, int m) {
@@ -1246,8 +1256,8 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
     a.bounds = plan->bounds;
   }
   a.pages = pages;
-  a.max_pages = ctx_stride / kTile;
-  a.npages = std::min(K->capacity, V->capacity) / kTile;
+  a.max_pages = ctx_stride / kPage;
+  a.npages = std::min(K->capacity, V->capacity) / kPage;
   a.kidx = K->idx; a.ksgn = K->sgn; a.knorm = K->norm; a.krnorm = K->rnorm;
   a.vidx = V->idx; a.vsgn = V->sgn; a.vnorm = V->norm; a.vrnorm = V->rnorm;
   a.ctx_len = ctx_len;
@@ -1268,7 +1278,7 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
   a.fault = fault_word();
   if (!a.fault) return TQ_ERR_CUDA;
   const int units = B * Hkv;
-  const int grid = decode_tc_ctas(units, a.tpu);
+  const int grid = decode_tc_ctas(units, a.tpu, a.G);
   // the per-unit query tables, the decode, then the per-unit merge
   // the merge: one CTA per query head when those fit one wave, else one per unit
   const bool per_head = (int64_t)B * Hq <= sm_count();
@@ -1300,6 +1310,7 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
     cfg.gridDim = dim3(grid);
     cfg.dynamicSmemBytes = smem;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TQ_ERR_CUDA;
+    cfg.blockDim = dim3(kCombThreads);
     cfg.gridDim = dim3(per_head ? B * Hq : units);
     cfg.dynamicSmemBytes = comb_smem;
     if (cudaLaunchKernelEx(&cfg, comb_kern, a, grid) != cudaSuccess) return TQ_ERR_CUDA;
@@ -1307,8 +1318,8 @@ tq_status launch_decode_tc(const tq_plan* plan, const void* q, tq_dtype q_dtype,
   };
 #define TQ_DECODE_TC_GO(W_, GP_, Q_)                                                                \
   go(unit_table_kernel<W_, GP_, Q_>, table_smem_bytes<W_, GP_, Q_>(), decode_tc_kernel<W_, GP_, Q_>, \
-     smem_bytes<W_, GP_, Q_>(), unit_combine_kernel<GP_, Q_, false>, 16 + Scratch<GP_, kThreads>::kMerge * 4, \
-     unit_combine_kernel<1, Q_, true>, 16 + Scratch<1, kThreads>::kMerge * 4)
+     smem_bytes<W_, GP_, Q_>(), unit_combine_kernel<GP_, Q_, false>, 16 + Scratch<GP_, kCombThreads>::kMerge * 4, \
+     unit_combine_kernel<1, Q_, true>, 16 + Scratch<1, kCombThreads>::kMerge * 4)
   const bool g8 = a.G > 4;
   if (plan->m > 0) {
     switch (plan->w) {

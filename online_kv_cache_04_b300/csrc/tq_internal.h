@@ -76,7 +76,7 @@ tq_status quantize_tc(const tq_plan* plan, const void* x0, const void* x1, int64
 // decode_tc_tpu(ctx_stride) tiles.
 int64_t decode_tc_tpu(int64_t ctx_stride);
 bool decode_tc_supported(const tq_plan* plan, int G, const tq_records* V, int64_t ctx_stride);
-int decode_tc_ctas(int64_t units, int64_t tpu);
+int decode_tc_ctas(int64_t units, int64_t tpu, int G);
 int decode_tc_slots(int64_t units, int64_t tpu, int64_t ctas);
 size_t decode_tc_table_bytes(int w, int G, int m);
 // pages: NULL for contiguous units, else the page table of a paged cache
