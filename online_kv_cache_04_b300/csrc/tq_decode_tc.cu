@@ -923,7 +923,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(GP)) decode_tc_kernel(co
         const uint8_t* stg = smem + Sh::kOffRing + (int)(gc & (kStages - 1)) * Sh::kStage;
         const uint4* kq = reinterpret_cast<const uint4*>(stg + Sh::kOffKIdx);  // token t, plane P: kq[t·W + P]
         const uint4* sq = reinterpret_cast<const uint4*>(stg + Sh::kOffKSgn);  // token t: sq[t]
-        // [score tile][part][head tile][fragment], one chain per K-substep
+        // [score tile][part][head tile][fragment]: one chain per K-substep at
+        // GP = 8 and at w = 3; otherwise (12 warps a SM hide the chain's latency,
+        // and the registers are short) one chain, acc2 staying zero
+        constexpr bool kTwoChains = GP == 8 || W == 3;
         float acc[2][2][GH][4], acc2[2][2][GH][4];
 #pragma unroll
         for (int st = 0; st < 2; ++st)
@@ -967,7 +970,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(GP)) decode_tc_kernel(co
               for (int st = 0; st < 2; ++st) {
                 const uint32_t u0 = u[st][0], u1 = u[st][1];
                 mma_f16(acc[st][part][ht], u0 & kK12, u1 & kK12, u0 & kK13, u1 & kK13, b0.x, b0.y);
-                mma_f16(acc2[st][part][ht], u0 & kK14, u1 & kK14, sk(u0), sk(u1), b1.x, b1.y);
+                if constexpr (kTwoChains)
+                  mma_f16(acc2[st][part][ht], u0 & kK14, u1 & kK14, sk(u0), sk(u1), b1.x, b1.y);
+                else
+                  mma_f16(acc[st][part][ht], u0 & kK14, u1 & kK14, sk(u0), sk(u1), b1.x, b1.y);
               }
             }
           }
