@@ -54,19 +54,21 @@
 // unrotates.  All three are programmatic dependent launches (each waits for
 // its predecessor before reading what the predecessor wrote).
 //
-// Work split.  A persistent grid of one CTA per SM takes contiguous ranges of
-// 256-token tiles over all (batch, kv head) units (the last tile of a unit
-// may hold 128).  Each of the eight warps owns one 32-token block of every
-// tile and does everything for it: the scores of its 32 tokens (two 16-row
-// tiles), its own online softmax, and the values of those tokens for all 128
+// Work split.  A persistent grid of 4-warp CTAs, three per SM (two when a kv
+// head serves more than four query heads), takes contiguous ranges of
+// 128-token tiles over all (batch, kv head) units.  The kernel is bound by
+// instruction issue, so the 12 warps a SM are what hides the latency of each
+// warp's dependent chains.  Each warp owns one 32-token block of every tile
+// and does everything for it: the scores of its 32 tokens (two 16-row tiles),
+// its own online softmax, and the values of those tokens for all 128
 // coordinates.  The attention weights go from the score fragments to the
 // value operands by shuffles inside the warp, so warps never wait for one
 // another within a unit; the only shared state is the ring of bulk-copied
-// tiles (a stage is refilled once all eight warps have arrived on its
+// tiles (a stage is refilled once all four warps have arrived on its
 // stage-empty mbarrier).  Within a warp the values of tile k − 1 and the
 // scores of tile k form one straight block.  At the end of its part of a
-// unit a CTA merges the eight warps on chip into one partial (reference, Σ p
-// and the two value sums per head) for unit_combine_kernel.
+// unit a CTA merges its warps on chip into one partial (reference, Σ p and
+// the two value sums per head) for unit_combine_kernel.
 //
 // Softmax is online with a lazy reference per warp: the running reference M
 // (of log2(p·max(‖v‖, ‖r_v‖)), clamped at 2^-32) moves only when a tile
@@ -93,7 +95,7 @@ constexpr int kD = 128;
 constexpr int kStages = 2;                             // power of two
 constexpr int kThreads = 32 * kNW;                     // decode kernel
 // decode CTAs resident per SM: 12 warps at up to 4 heads per kv head; with 8
-// the value accumulators of both parts stay apart and need the registers of 8 warps
+// the value accumulators of both parts stay apart and take more registers
 constexpr int ctas_per_sm(int GP) { return GP == 4 ? 3 : 2; }
 constexpr int kCombThreads = 256;                      // unit merge kernel
 constexpr int kTableThreads = 512;                     // query-table kernel
@@ -160,7 +162,7 @@ struct TcArgs {
   float *knorm, *krnorm, *vnorm, *vrnorm;
   const int32_t* ctx_len;
   int64_t ctx_stride;
-  const int32_t* pages;  // paged caches: [B*Hkv][max_pages] page of each 256-token tile (NULL: contiguous rows)
+  const int32_t* pages;  // paged caches: [B*Hkv][max_pages] page of each 256 tokens (NULL: contiguous rows)
   int64_t max_pages, npages;  // pages per unit; pages the record arrays hold
   int B, Hq, Hkv, G;
   const void* q;     // [B*Hq][128] queries, bf16 (q_bf16) or fp32
@@ -179,7 +181,7 @@ struct TcArgs {
   float scale, alpha;
   float* part;       // [B*Hq][smax][2 + 2*128]
   int smax;
-  int64_t tpu;       // tiles per unit = ceil(ctx_stride / 256)
+  int64_t tpu;       // tiles per unit = ceil(ctx_stride / kTile)
   int64_t total;     // units * tpu
   uint8_t* tables;     // [B*Hkv] per-unit query tables (unit_table_kernel)
   float* out;        // [B*Hq][128]
@@ -1143,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(GP)) decode_tc_kernel(co
       release(gi + sg.n - 1, gi + sg.n);
       gi += sg.n;
     }
-    // ---- the partial of this CTA for the unit: the eight warps, each over its
+    // ---- the partial of this CTA for the unit: its warps, each over its
     // own tokens with its own reference, merged on chip
 #pragma unroll
     for (int hh = 0; hh < GH; ++hh) {
