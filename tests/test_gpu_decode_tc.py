@@ -164,18 +164,19 @@ def test_tiny_workload_g8(gpu_lib):
     assert rel_l2(out, want) <= 1e-3
 
 
-def test_one_unit_g8_over_all_ctas_repeated_calls(gpu_lib):
-    """One kv head with 8 query heads, 160 tiles (every CTA holds a part of the one unit: the
-    most partials a unit can have), decoded three times through one workspace: the per-unit
-    arrival counts restart on every call and each call gives the same result (up to the order of
-    the in-block float atomics of the query offsets)."""
+@pytest.mark.parametrize("G", [4, 8])
+def test_one_unit_over_all_ctas_repeated_calls(gpu_lib, G):
+    """One kv head with G query heads and 512 tiles of 128 tokens: every CTA of the grid (three
+    per SM at 4 heads, two at 8) holds a part of the one unit, the most partials a unit can have.
+    Decoded three times through one workspace: each call gives the same result (up to the order
+    of the in-block float atomics of the query offsets)."""
     d = m = 128
     w = 2
-    T = 40960
+    T = 65536
     g = torch.Generator().manual_seed(29)
     K = torch.randn(1, 1, T, d, generator=g)
     V = torch.randn(1, 1, T, d, generator=g)
-    q = torch.randn(1, 8, d, generator=g)
+    q = torch.randn(1, G, d, generator=g)
     kq, krec = _oracle_recs(K.numpy(), d, m, w)
     vq, vrec = _oracle_recs(V.numpy(), d, m, w)
     Pi, S, c, _ = oracle_tables(d, m, w)
@@ -183,13 +184,13 @@ def test_one_unit_g8_over_all_ctas_repeated_calls(gpu_lib):
     p = plan(d, m, w)
     Kg = oracle_records_to_gpu(kq, d, m, w)
     Vg = oracle_records_to_gpu(vq, d, m, w, layout=BLK)
-    ws = torch.empty(_lib.tq_decode_workspace_size(p, 1, 8, 1, T), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(_lib.tq_decode_workspace_size(p, 1, G, 1, T), dtype=torch.uint8, device="cuda")
     ws.fill_(0xFF)
     ctx_t = torch.tensor([T - 5], dtype=torch.int32, device="cuda")
     qd = q.cuda()
     outs = []
     for _ in range(3):
-        out = torch.full((1, 8, d), float("nan"), device="cuda")
+        out = torch.full((1, G, d), float("nan"), device="cuda")
         _lib.tq_decode_attention(p, qd, Kg, Vg, ctx_t, T, 1, out, ws)
         torch.cuda.synchronize()
         assert _lib.tq_fault_flags() == 0
