@@ -1128,21 +1128,35 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(GP)) decode_tc_kernel(co
         if (threadIdx.x == 0) issue_upto(done);
       };
 
-      // prologue: scores and weights of the first tile
-      wait(&ms->ld_full[gi & (kStages - 1)], (uint32_t)((gi / kStages) & 1));
-      scores_step(0, gi);
-      weights_step();
-      // steady state: values of tile k - 1 and scores of tile k as one block
-      for (int k = 1; k < sg.n; ++k) {
-        const int64_t g = gi + k;
-        wait(&ms->ld_full[g & (kStages - 1)], (uint32_t)((g / kStages) & 1));
-        values_step(g - 1);
-        scores_step(k, g);
-        release(g - 1, g);
+      if constexpr (W < 3 && GP == 4) {
+        // each tile whole: scores, weights, values, then its stage goes back, so
+        // the refill of a two-stage ring has a whole tile's work to land
+        for (int k = 0; k < sg.n; ++k) {
+          const int64_t g = gi + k;
+          wait(&ms->ld_full[g & (kStages - 1)], (uint32_t)((g / kStages) & 1));
+          scores_step(k, g);
+          weights_step();
+          values_step(g);
+          release(g, g + 1);
+        }
+      } else {
+        // w = 3 or 8 heads (more registers): the values of tile k - 1 and the
+        // scores of tile k form one block, which spills less; tile k - 1's stage
+        // goes back as soon as its values are done
+        wait(&ms->ld_full[gi & (kStages - 1)], (uint32_t)((gi / kStages) & 1));
+        scores_step(0, gi);
         weights_step();
+        for (int k = 1; k < sg.n; ++k) {
+          const int64_t g = gi + k;
+          wait(&ms->ld_full[g & (kStages - 1)], (uint32_t)((g / kStages) & 1));
+          values_step(g - 1);
+          release(g - 1, g);
+          scores_step(k, g);
+          weights_step();
+        }
+        values_step(gi + sg.n - 1);
+        release(gi + sg.n - 1, gi + sg.n);
       }
-      values_step(gi + sg.n - 1);
-      release(gi + sg.n - 1, gi + sg.n);
       gi += sg.n;
     }
     // ---- the partial of this CTA for the unit: its warps, each over its
