@@ -247,3 +247,34 @@ def test_wide_vectors_bf16_ragged_offset(gpu_lib, w):
     _compare(X.float().numpy(), rec, slice(37, 1037), d, d, w)
     assert bool((rec.idx[:37] == -1).all()) and bool((rec.idx[1037:] == -1).all())
     assert bool((rec.sgn[:37] == -1).all()) and bool((rec.sgn[1037:] == -1).all())
+
+
+@pytest.mark.parametrize("w,m", [(2, 128), (3, 128), (2, 0)])
+def test_pair_repeated_launches_full_layer(gpu_lib, w, m):
+    """The paired tensor-core launch over a whole Llama-3.1-8B-shaped layer (2 x 262,144
+    vectors: 28 tiles for most CTAs, so the warp roles run several tiles apart) repeated 40
+    times: no bounded wait runs out and every launch writes the same records, bit for bit.
+    Rows sampled across the layer match the oracle."""
+    d = 128
+    wl = WORKLOADS["llama8b"]
+    n = wl.B * wl.Hkv * wl.ctx
+    K = make_kv(wl, which=0, device="cuda").reshape(n, d)
+    V = make_kv(wl, which=1, device="cuda").reshape(n, d)
+    p = plan(d, m, w)
+    rk = _lib.Records(n, d, m, w)
+    rv = _lib.Records(n, d, m, w, layout=_lib.TQ_LAYOUT_BLOCK32)
+    _lib.tq_fault_flags(reset=True)
+    _lib.tq_quantize_pair(p, K, V, rk, rv)
+    torch.cuda.synchronize()
+    fields = lambda: [t.clone() for r in (rk, rv) for t in (r.idx, r.sgn, r.norm, r.rnorm) if t is not None]
+    first = fields()
+    for _ in range(40):
+        _lib.tq_quantize_pair(p, K, V, rk, rv)
+    torch.cuda.synchronize()
+    assert _lib.tq_fault_flags() == 0
+    for a, b in zip(first, fields()):
+        assert torch.equal(a, b)
+    for r0 in (0, n // 2 + 32, n - 64):  # block-aligned ranges at the start, middle and end
+        rows = slice(r0, r0 + 64)
+        _compare(K[rows].float().cpu().numpy(), rk, rows, d, m, w)
+        _compare(V[rows].float().cpu().numpy(), rv, rows, d, m, w)
