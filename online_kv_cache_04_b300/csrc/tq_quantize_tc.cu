@@ -61,7 +61,11 @@ constexpr int kOffX = 4 * kMatBytes;             // two x stages
 constexpr int kOffBar = kOffX + 2 * kMatBytes;
 constexpr int kOffRsq = kOffBar + 256;           // [slot 2][tile parity 2][128] partial ||ρ||² of the upper half
 constexpr int kOffNrm = kOffRsq + 2 * 2 * 128 * 4;  // [tile parity 2][128] ||x|| of the tile's vectors
-constexpr int kSmemBytes = kOffNrm + 2 * 128 * 4 + 1024;  // + alignment slack
+// [slot 2][tile parity 2][word 8][128]: the upper half's index and sign words of
+// a row-layout tile (words 2p, 2p + 1: plane p; 6, 7: signs), which the lower
+// half stores together with its own as whole 16-byte pieces of each record
+constexpr int kOffXch = kOffNrm + 2 * 128 * 4;
+constexpr int kSmemBytes = kOffXch + 2 * 2 * 8 * 128 * 4 + 1024;  // + alignment slack
 constexpr int kThreads = 640, kMmaWarp = 16, kTmaWarp = 17, kMma2Warp = 18, kNormWarp = 19;
 constexpr uint32_t kTmemCols = 512;              // four regions of 128 columns: U, then ρ K-steps [hi 8 | lo 8]; or P
 
@@ -456,13 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       // with QJL, GEMM2 reads the residual next; without, the slot is free
       if (lane == 0) mbar_arrive(smem_u32(Q ? &bars->rho_full[s] : &bars->acc_empty[it & 3]));
-      if (Q && h == 1) {  // the lower half writes ||r|| = n·sqrt(lower + upper partial)
-        // once it has read this slot's partials of the group's previous tile
-        if (!mbar_wait(smem_u32(&bars->rsq_empty[s]), ph ^ 1, a.fault, kFaultWait)) break;
-        rsq_s[(it >> 1 & 1) * 128 + r] = rsq;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->rsq_full[s]));
-      }
       // this tile's output (fields picked one by one: no dynamic index into the parameters)
       const bool second = tile >= a.ntiles0;
       const int64_t lt = tile - (second ? a.ntiles0 : 0), on = second ? a.out1.n : a.out0.n;
@@ -471,8 +468,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t row = lt * kTile + r;
       const int64_t blk_row = lt * kTile + q * 32;  // this warp's block (block layout)
       const uint32_t valid = __ballot_sync(0xffffffffu, row < on);
+      // At w = 3 with QJL the lower half stores whole rows of a row-layout tile
+      // after the sign epilogue (the upper half's words through shared memory):
+      // the index planes then need no registers across the sign epilogue, which
+      // is what the w = 3 epilogue was short of.  At w <= 2 each half stores its
+      // own words as soon as they are known.
+      constexpr bool kStageRows = Q && W == 3;
       if (rows_layout) {
-        if (row < on) {
+        if (!kStageRows && row < on) {
 #pragma unroll
           for (int p = 0; p < W; ++p)
             *reinterpret_cast<uint2*>(oidx + row * (4 * W) + p * 4 + 2 * h) = make_uint2(planes[p][0], planes[p][1]);
@@ -512,15 +515,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[it & 3]));
       uint32_t* const osgn = second ? a.out1.sgn : a.out0.sgn;
       if (rows_layout) {
-        if (row < on) *reinterpret_cast<uint2*>(osgn + row * 4 + 2 * h) = make_uint2(sg[0], sg[1]);
+        if (!kStageRows && row < on) *reinterpret_cast<uint2*>(osgn + row * 4 + 2 * h) = make_uint2(sg[0], sg[1]);
       } else {
         if (valid != 0u) store_block32<2>(osgn + (blk_row >> 5) * 128 + 64 * h, sg, valid, lane);
       }
-      if (h == 0) {
+      // The halves meet once per tile: the upper half hands its ||ρ||² partial
+      // (and, when staged, its index and sign words) to the lower half, which
+      // writes ||x||, ||r|| (and the whole records).
+      float* const rs_slot = rsq_s + (it >> 1 & 1) * 128;
+      uint32_t* const xw = reinterpret_cast<uint32_t*>(smem + kOffXch) + (s * 2 + (it >> 1 & 1)) * 8 * 128 + r;
+      if (h == 1) {
+        // once the lower half has read this slot's words of the group's previous tile
+        if (!mbar_wait(smem_u32(&bars->rsq_empty[s]), ph ^ 1, a.fault, kFaultWait)) break;
+        rs_slot[r] = rsq;
+        if (kStageRows && rows_layout) {
+#pragma unroll
+          for (int p = 0; p < W; ++p) xw[(2 * p) * 128] = planes[p][0], xw[(2 * p + 1) * 128] = planes[p][1];
+          xw[6 * 128] = sg[0];
+          xw[7 * 128] = sg[1];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->rsq_full[s]));
+      } else {
         if (!mbar_wait(smem_u32(&bars->rsq_full[s]), ph, a.fault, kFaultWait)) break;
         if (row < on) {
           (second ? a.out1.norm : a.out0.norm)[row] = n;
-          (second ? a.out1.rnorm : a.out0.rnorm)[row] = n * sqrtf(rsq + rsq_s[(it >> 1 & 1) * 128 + r]);
+          (second ? a.out1.rnorm : a.out0.rnorm)[row] = n * sqrtf(rsq + rs_slot[r]);
+          if (kStageRows && rows_layout) {
+#pragma unroll
+            for (int p = 0; p < W; ++p)
+              *reinterpret_cast<uint4*>(oidx + row * (4 * W) + p * 4) =
+                  make_uint4(planes[p][0], planes[p][1], xw[(2 * p) * 128], xw[(2 * p + 1) * 128]);
+            *reinterpret_cast<uint4*>(osgn + row * 4) = make_uint4(sg[0], sg[1], xw[6 * 128], xw[7 * 128]);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->rsq_empty[s]));
